@@ -1,0 +1,166 @@
+"""fp64 CPU oracle for the SimSD verification step -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never calls it, and
+it imports nothing from the CUDA library: the two sides meet only through
+the seeded generators in ``synth.py``.
+
+The arithmetic lives in plain C (``layout.c``, ``attention.c``,
+``accept.c``; see ``simsd_oracle.h`` for the passages each follows).  This
+module only marshals numpy arrays through ctypes.  ``exact.py`` holds the
+closed-form distribution of the acceptance walk used to pin ``accept``.
+
+Parity unpinned: the RoPE pairing convention and the softmax scale (the
+pages fix neither).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+
+ORACLE_OK, ORACLE_ERR_ARG, ORACLE_ERR_TAU = 0, 1, 2
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        I, D, P = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+        lib.oracle_tau_is_permutation.argtypes = [I, P]
+        lib.oracle_mask_entry.argtypes = [I, I, P, I, I]
+        lib.oracle_layout.argtypes = [I, I, P, P, P]
+        lib.oracle_rope.argtypes = [P, I, I, I, P, D, P]
+        lib.oracle_rope.restype = None
+        lib.oracle_verify_attn_seq.argtypes = [I, I, I, I, I, D, D, I, P, P, P,
+                                               P, P, P, I, P, P, P]
+        lib.oracle_verify_attn.argtypes = [I, P, P, I, I, I, D, D, P, P, P, P,
+                                           P, P, P, I]
+        lib.oracle_accept.argtypes = [I, I, P, P, P, P, P, P, I, P, P, P, P,
+                                      P, I]
+        _LIB = lib
+    return _LIB
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc, what):
+    if rc != ORACLE_OK:
+        raise OracleError("%s failed with code %d" % (what, rc))
+
+
+def tau_is_permutation(tau):
+    tau = _c(tau, np.int32)
+    return bool(_lib().oracle_tau_is_permutation(len(tau), _p(tau)))
+
+
+def layout(P, tau, with_mask=True):
+    """positions int32[P+2B], mask uint8[2B, P+2B] (or None)."""
+    tau = _c(tau, np.int32)
+    B = len(tau)
+    positions = np.zeros(P + 2 * B, np.int32)
+    mask = np.zeros((2 * B, P + 2 * B), np.uint8) if with_mask else None
+    _check(_lib().oracle_layout(P, B, _p(tau), _p(positions), _p(mask)),
+           "oracle_layout")
+    return positions, mask
+
+
+def rope(x, pos, base):
+    """x [n_tok, n_heads, hd] fp64 rotated at pos[n_tok]."""
+    x = _c(x, np.float64)
+    pos = _c(pos, np.int32)
+    n_tok, n_heads, hd = x.shape
+    out = np.empty_like(x)
+    _lib().oracle_rope(_p(x), n_tok, n_heads, hd, _p(pos), float(base), _p(out))
+    return out
+
+
+def verify_attn_seq(q, k_prompt, v_prompt, k_new, v_new, tau, rope_base,
+                    sm_scale, pos_offset=0, rows=None):
+    """One sequence.  q [2B,Hq,hd] raw; k_prompt/v_prompt [P,Hkv,hd] (keys
+    already rotated); k_new/v_new [2B,Hkv,hd] raw; tau [B].
+    rows: None for every row (returns [2B,Hq,hd]) or a list of
+    (token, head) pairs (returns [n,hd])."""
+    q = _c(q, np.float64)
+    k_new, v_new = _c(k_new, np.float64), _c(v_new, np.float64)
+    tau = _c(tau, np.int32)
+    twoB, Hq, hd = q.shape
+    Hkv = k_new.shape[1]
+    P = 0 if k_prompt is None else k_prompt.shape[0]
+    kp = None if P == 0 else _c(k_prompt, np.float64)
+    vp = None if P == 0 else _c(v_prompt, np.float64)
+    if rows is None:
+        out = np.empty((twoB, Hq, hd), np.float64)
+        n, rt, rh = -1, None, None
+    else:
+        rows = np.asarray(rows, np.int32).reshape(-1, 2)
+        n = len(rows)
+        rt, rh = _c(rows[:, 0], np.int32), _c(rows[:, 1], np.int32)
+        out = np.empty((n, hd), np.float64)
+    _check(_lib().oracle_verify_attn_seq(
+        P, len(tau), Hq, Hkv, hd, float(rope_base), float(sm_scale),
+        int(pos_offset), _p(tau), _p(q), _p(kp), _p(vp), _p(k_new), _p(v_new),
+        n, _p(rt), _p(rh), _p(out)), "oracle_verify_attn_seq")
+    return out
+
+
+def verify_attn(lens, cu_B, q, k_prompt, v_prompt, k_new, v_new, tau,
+                rope_base, sm_scale, n_threads=0):
+    """Whole batch, sequences back to back (see simsd_oracle.h)."""
+    lens, cu_B, tau = _c(lens, np.int32), _c(cu_B, np.int32), _c(tau, np.int32)
+    q = _c(q, np.float64)
+    k_new, v_new = _c(k_new, np.float64), _c(v_new, np.float64)
+    k_prompt, v_prompt = _c(k_prompt, np.float64), _c(v_prompt, np.float64)
+    T, Hq, hd = q.shape
+    Hkv = k_new.shape[1]
+    out = np.empty_like(q)
+    _check(_lib().oracle_verify_attn(
+        len(lens), _p(lens), _p(cu_B), Hq, Hkv, hd, float(rope_base),
+        float(sm_scale), _p(tau), _p(q), _p(k_prompt), _p(v_prompt),
+        _p(k_new), _p(v_new), _p(out), int(n_threads)), "oracle_verify_attn")
+    return out
+
+
+def accept(cu_B, target, draft, draft_tokens, tau, uniforms, n_threads=0):
+    """Returns dict(n_accept, token, pos, accept_margin, resample_margin).
+    target/draft [sum B, V] (any float dtype, taken exactly to fp64);
+    uniforms [batch, u_stride] float32."""
+    cu_B = _c(cu_B, np.int32)
+    target, draft = _c(target, np.float64), _c(draft, np.float64)
+    draft_tokens, tau = _c(draft_tokens, np.int32), _c(tau, np.int32)
+    uniforms = _c(uniforms, np.float32)
+    batch = len(cu_B) - 1
+    V = target.shape[1]
+    n_accept = np.zeros(batch, np.int32)
+    token = np.zeros(batch, np.int32)
+    pos = np.zeros(batch, np.int32)
+    am = np.zeros(int(cu_B[-1]), np.float64)
+    rm = np.zeros(batch, np.float64)
+    _check(_lib().oracle_accept(
+        batch, V, _p(cu_B), _p(target), _p(draft), _p(draft_tokens), _p(tau),
+        _p(uniforms), uniforms.shape[1], _p(n_accept), _p(token), _p(pos),
+        _p(am), _p(rm), int(n_threads)), "oracle_accept")
+    return dict(n_accept=n_accept, token=token, pos=pos, accept_margin=am,
+                resample_margin=rm)
+
+
+def library_path():
+    return _build.LIB
+
+
+def default_threads():
+    return len(os.sched_getaffinity(0))

@@ -1,0 +1,136 @@
+/*
+ * accept.c -- rejection-sampling acceptance along the temporal order.
+ * TEST INFRASTRUCTURE ONLY (see simsd_oracle.h).
+ *
+ * SimSD (gist.science, paper 2606.02544), "Speculative Decoding Pipeline",
+ * acceptance: standard rejection sampling is applied along the temporal
+ * order the draft induced, and the longest accepted prefix is committed.
+ * "Standard" is read as the textbook speculative-sampling rule:
+ *   p = softmax(target logits), q = softmax(draft logits) of the same slot;
+ *   step t (t = 1..B) tests the slot k whose label tau(k) = t;
+ *   the draft token x is accepted with probability min(1, p(x)/q(x)),
+ *   i.e. iff u * q(x) < p(x) for a uniform u in [0,1);
+ *   at the first rejection a token is drawn from norm(max(0, p - q)) by
+ *   inverse CDF, and the walk stops.
+ * Readings: no bonus token when every step is accepted (the layout has no
+ * slot after D~_B); u[t-1] tests step t and u[B] draws the residual; the
+ * accept comparison is made in fp32 (the kernel's precision) on p(x), q(x)
+ * computed in fp64 and rounded to fp32, with u the given fp32 value.
+ */
+#include <math.h>
+#include <omp.h>
+#include <stdlib.h>
+#include "simsd_oracle.h"
+
+/* log(sum_v exp(x_v)), fp64, max-shifted. */
+static double log_sum_exp(const double *x, int V) {
+  double m = -INFINITY;
+  for (int v = 0; v < V; ++v)
+    if (x[v] > m) m = x[v];
+  double s = 0.0;
+  for (int v = 0; v < V; ++v) s += exp(x[v] - m);
+  return m + log(s);
+}
+
+static int accept_one(int B, int V, const double *target, const double *draft,
+                      const int *draft_tokens, const int *tau, const float *u,
+                      int *n_accept, int *token, int *pos,
+                      double *accept_margin, double *resample_margin) {
+  int *slot_of_step = (int *)malloc(sizeof(int) * (size_t)B);
+  double *r = (double *)malloc(sizeof(double) * (size_t)V);
+  if (!slot_of_step || !r) { free(slot_of_step); free(r); return ORACLE_ERR_ARG; }
+  for (int k = 0; k < B; ++k) slot_of_step[tau[k] - 1] = k;
+  for (int k = 0; k < B; ++k)
+    if (accept_margin) accept_margin[k] = -1.0;
+  if (resample_margin) *resample_margin = -1.0;
+
+  *n_accept = B;
+  *token = -1;
+  *pos = -1;
+  for (int t = 1; t <= B; ++t) {
+    const int k = slot_of_step[t - 1];
+    const double *tl = target + (size_t)k * V;
+    const double *dl = draft + (size_t)k * V;
+    const int x = draft_tokens[k];
+    const double lse_p = log_sum_exp(tl, V);
+    const double lse_q = log_sum_exp(dl, V);
+    const double px = exp(tl[x] - lse_p);
+    const double qx = exp(dl[x] - lse_q);
+    const float uf = u[t - 1];
+    const int accepted = (uf * (float)qx) < (float)px;
+    if (accept_margin)
+      accept_margin[k] = px > 0.0 ? fabs((double)uf * qx - px) / px
+                                  : ((double)uf * qx > 0.0 ? INFINITY : 0.0);
+    if (accepted) continue;
+
+    /* first rejection: draw from norm(max(0, p - q)) with u[B] */
+    *n_accept = t - 1;
+    *pos = k;
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) {
+      double pv = exp(tl[v] - lse_p), qv = exp(dl[v] - lse_q);
+      r[v] = pv > qv ? pv - qv : 0.0;
+      S += r[v];
+    }
+    if (S == 0.0) { /* p == q: the residual is empty, draw from p itself */
+      for (int v = 0; v < V; ++v) { r[v] = exp(tl[v] - lse_p); S += r[v]; }
+    }
+    const double U = (double)u[B] * S;
+    int chosen = -1;
+    double below = 0.0, c = 0.0;
+    for (int v = 0; v < V; ++v) {
+      below = c;
+      c += r[v];
+      if (c > U) { chosen = v; break; }
+    }
+    if (chosen < 0) { /* rounding left U past the total: last positive bin */
+      for (int v = V - 1; v >= 0; --v)
+        if (r[v] > 0.0) { chosen = v; break; }
+      below = U;
+      c = U;
+    }
+    *token = chosen;
+    if (resample_margin) {
+      double d1 = U - below, d2 = c - U;
+      *resample_margin = (d1 < d2 ? d1 : d2) / S;
+    }
+    break;
+  }
+  free(slot_of_step);
+  free(r);
+  return ORACLE_OK;
+}
+
+int oracle_accept(int batch, int V, const int *cu_B, const double *target,
+                  const double *draft, const int *draft_tokens,
+                  const int *tau, const float *uniforms, int u_stride,
+                  int *n_accept, int *token, int *pos,
+                  double *accept_margin, double *resample_margin,
+                  int n_threads) {
+  if (batch < 0 || V < 1 || !cu_B || !target || !draft || !draft_tokens ||
+      !tau || !uniforms || !n_accept || !token || !pos)
+    return ORACLE_ERR_ARG;
+  for (int b = 0; b < batch; ++b) {
+    int B = cu_B[b + 1] - cu_B[b];
+    if (B < 1 || u_stride < B + 1) return ORACLE_ERR_ARG;
+    if (!oracle_tau_is_permutation(B, tau + cu_B[b])) return ORACLE_ERR_TAU;
+    for (int k = 0; k < B; ++k) {
+      int x = draft_tokens[cu_B[b] + k];
+      if (x < 0 || x >= V) return ORACLE_ERR_ARG;
+    }
+  }
+  int rc = ORACLE_OK;
+  const int nt = n_threads > 0 ? n_threads : omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 16) num_threads(nt) reduction(max : rc)
+  for (int b = 0; b < batch; ++b) {
+    const int s0 = cu_B[b];
+    const int B = cu_B[b + 1] - s0;
+    int r = accept_one(B, V, target + (size_t)s0 * V, draft + (size_t)s0 * V,
+                       draft_tokens + s0, tau + s0,
+                       uniforms + (size_t)b * u_stride, &n_accept[b], &token[b],
+                       &pos[b], accept_margin ? accept_margin + s0 : NULL,
+                       resample_margin ? resample_margin + b : NULL);
+    if (r > rc) rc = r;
+  }
+  return rc;
+}

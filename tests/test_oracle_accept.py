@@ -1,0 +1,173 @@
+"""Pins for the oracle's acceptance walk (rejection sampling in tau order).
+
+Pinned against: the mathematics of standard speculative sampling -- the
+emitted token at each reached step follows the target distribution p
+(losslessness), a step accepts with probability sum_v min(p, q), the walk
+reaches step t with probability prod_{s<=t} alpha_s -- checked on the
+oracle's own decisions by brute force over deterministic grids of uniforms
+and by a fixed-seed Monte Carlo against exact enumeration; plus the special
+cases p = q, u = 0 and a one-hot draft.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import exact
+
+
+def softmax(x):
+    e = np.exp(x - x.max(-1, keepdims=True))
+    return e / e.sum(-1, keepdims=True)
+
+
+def test_exact_module_closed_forms():
+    """exact.py enumerates paths; its totals must meet the closed forms."""
+    rng = np.random.default_rng(1)
+    B, V = 3, 6
+    p = softmax(rng.standard_normal((B, V)) * 2)
+    q = softmax(rng.standard_normal((B, V)) * 2)
+    tau = [2, 3, 1]
+    d = exact.outcome_distribution(p, q, tau)
+    assert abs(sum(d.values()) - 1.0) < 1e-12
+    alpha = np.minimum(p, q).sum(1)
+    order = [tau.index(t) for t in (1, 2, 3)]
+    reach = 1.0
+    for t, k in enumerate(order):
+        r = np.maximum(p[k] - q[k], 0)
+        for v in range(V):
+            np.testing.assert_allclose(d.get((t, v), 0.0), reach * r[v], atol=1e-14)
+        reach *= alpha[k]
+    np.testing.assert_allclose(d[(B, -1)], reach, rtol=1e-12)
+    for k in range(B):
+        np.testing.assert_allclose(exact.step_emission(p[k], q[k]), p[k], atol=1e-14)
+
+
+def run_single_slot(logit_t, logit_d, xs, u0s, u1s):
+    """Many B = 1 sequences sharing one slot's logits."""
+    n = len(xs)
+    V = len(logit_t)
+    target = np.broadcast_to(logit_t, (n, V))
+    draft = np.broadcast_to(logit_d, (n, V))
+    cu = np.arange(n + 1, dtype=np.int32)
+    uni = np.stack([u0s, u1s], 1).astype(np.float32)
+    return oracle.accept(cu, target, draft, xs, np.ones(n, np.int32), uni, n_threads=4)
+
+
+def test_lossless_single_step_by_grid():
+    """Emitted token distribution, integrated over midpoint grids of both
+    uniforms using the oracle's decisions, equals p within grid error."""
+    rng = np.random.default_rng(5)
+    V, N = 8, 2000
+    lt, ld = rng.standard_normal(V) * 1.5, rng.standard_normal(V) * 1.5
+    p, q = softmax(lt), softmax(ld)
+    grid = ((np.arange(N) + 0.5) / N).astype(np.float32)
+    emit = np.zeros(V)
+    for x in range(V):
+        # (a) acceptance probability of draft token x over the u0 grid
+        res = run_single_slot(lt, ld, np.full(N, x), grid, np.full(N, 0.5, np.float32))
+        acc = (res["n_accept"] == 1).mean()
+        assert abs(acc - min(1.0, p[x] / q[x])) <= 1.0 / N + 1e-7
+        emit[x] += q[x] * acc
+        if acc < 1.0:
+            # (b) the residual draw over the u1 grid, forced rejection
+            res = run_single_slot(lt, ld, np.full(N, x), np.full(N, 0.99999, np.float32), grid)
+            assert (res["n_accept"] == 0).all() and (res["pos"] == 0).all()
+            hist = np.bincount(res["token"], minlength=V) / N
+            r = np.maximum(p - q, 0); r /= r.sum()
+            assert np.abs(np.cumsum(hist) - np.cumsum(r)).max() <= 1.0 / N + 1e-9
+            emit += q[x] * (1 - acc) * hist
+    assert np.abs(emit - p).max() < 3.0 / N
+
+
+def test_walk_distribution_monte_carlo():
+    """V = 8, B = 3: fixed-seed Monte Carlo of the whole walk through the
+    oracle against the exact outcome distribution (chi-square)."""
+    rng = np.random.default_rng(12)
+    V, B, n = 8, 3, 200_000
+    lt = rng.standard_normal((B, V)) * np.array([[0.5], [2.0], [1.0]])
+    ld = lt + rng.standard_normal((B, V)) * np.array([[0.3], [2.5], [1.0]])
+    p, q = softmax(lt), softmax(ld)
+    tau = np.array([3, 1, 2])
+    xs = np.stack([rng.choice(V, size=n, p=q[k]) for k in range(B)], 1)
+    uni = rng.random((n, B + 1), dtype=np.float32)
+    cu = np.arange(0, B * n + 1, B, dtype=np.int32)
+    res = oracle.accept(cu, np.tile(lt, (n, 1)), np.tile(ld, (n, 1)), xs.reshape(-1),
+                        np.tile(tau, n), uni, n_threads=4)
+    d = exact.outcome_distribution(p, q, tau)
+    keys = sorted(d)
+    idx = {k: i for i, k in enumerate(keys)}
+    obs = np.zeros(len(keys))
+    order = [list(tau).index(t) for t in (1, 2, 3)]
+    for na, tok, pos in zip(res["n_accept"], res["token"], res["pos"]):
+        obs[idx[(int(na), int(tok))]] += 1
+        assert pos == (order[na] if na < B else -1)
+    exp_counts = np.array([d[k] for k in keys]) * n
+    keep = exp_counts > 5
+    chi2 = (((obs - exp_counts) ** 2 / exp_counts)[keep]).sum()
+    dof = keep.sum() - 1
+    # chi-square upper quantile ~ dof + 4 sqrt(2 dof) is far beyond alpha=1e-3
+    assert chi2 < dof + 4.0 * np.sqrt(2.0 * dof) + 10, (chi2, dof)
+    assert obs[~keep].sum() < 50
+
+
+def test_special_cases():
+    rng = np.random.default_rng(9)
+    V, B, n = 32, 5, 300
+    lt = rng.standard_normal((n * B, V))
+    tau = np.concatenate([rng.permutation(B) + 1 for _ in range(n)])
+    xs = rng.integers(0, V, n * B)
+    cu = np.arange(0, B * n + 1, B, dtype=np.int32)
+    uni = (rng.random((n, B + 1), dtype=np.float32) * np.float32(0.999)).astype(np.float32)
+    # p == q: every step accepted
+    res = oracle.accept(cu, lt, lt, xs, tau, uni)
+    assert (res["n_accept"] == B).all() and (res["token"] == -1).all() and (res["pos"] == -1).all()
+    # u == 0: accepted whenever p(x) > 0, even when q(x) >> p(x)
+    ld = lt + rng.standard_normal((n * B, V)) * 4
+    res = oracle.accept(cu, lt, ld, xs, tau, np.zeros((n, B + 1), np.float32))
+    assert (res["n_accept"] == B).all()
+    # p(x) = 0 (logit -inf): that step always rejects
+    lt2 = lt.copy()
+    k = 2
+    lt2[k::B][np.arange(n), xs[k::B]] = -np.inf
+    res = oracle.accept(cu, lt2, ld, xs, tau, np.zeros((n, B + 1), np.float32))
+    assert (res["pos"] == k).all()
+    assert (res["n_accept"] == tau[k::B] - 1).all()
+    assert (res["token"] != xs[k::B]).all()
+
+
+def test_one_hot_draft():
+    """q one-hot on a, draft token a: accept with probability p(a); on
+    rejection the token follows p restricted to v != a, renormalised."""
+    rng = np.random.default_rng(4)
+    V, N, a = 10, 4000, 3
+    lt = rng.standard_normal(V)
+    ld = np.full(V, -np.inf); ld[a] = 0.0
+    p = softmax(lt)
+    grid = ((np.arange(N) + 0.5) / N).astype(np.float32)
+    res = run_single_slot(lt, ld, np.full(N, a), grid, np.full(N, 0.5, np.float32))
+    assert abs((res["n_accept"] == 1).mean() - p[a]) <= 1.0 / N + 1e-7
+    res = run_single_slot(lt, ld, np.full(N, a), np.full(N, 0.99999, np.float32), grid)
+    hist = np.bincount(res["token"], minlength=V) / N
+    want = p.copy(); want[a] = 0; want /= want.sum()
+    assert hist[a] == 0
+    assert np.abs(np.cumsum(hist) - np.cumsum(want)).max() <= 1.0 / N + 1e-9
+
+
+def test_margins_and_errors():
+    V = 4
+    lt = np.log(np.array([[0.4, 0.3, 0.2, 0.1]]))
+    ld = np.log(np.array([[0.1, 0.2, 0.3, 0.4]]))
+    # p(x=3) = 0.1, q = 0.4: accept iff u < 0.25; u = 0.25 exactly sits on the boundary
+    res = oracle.accept([0, 1], lt, ld, [3], [1], np.array([[0.25, 0.5]], np.float32))
+    assert res["accept_margin"][0] < 1e-6
+    res = oracle.accept([0, 1], lt, ld, [3], [1], np.array([[0.75, 0.5]], np.float32))
+    assert res["n_accept"][0] == 0 and res["pos"][0] == 0
+    # residual r = (0.3, 0.1, 0, 0)/0.4: u = 0.5 -> U = 0.2 -> token 0, margin 0.25
+    assert res["token"][0] == 0
+    assert abs(res["resample_margin"][0] - 0.25) < 1e-12
+    with pytest.raises(oracle.OracleError):
+        oracle.accept([0, 2], np.zeros((2, 4)), np.zeros((2, 4)), [0, 1], [1, 1],
+                      np.zeros((1, 3), np.float32))
+    with pytest.raises(oracle.OracleError):
+        oracle.accept([0, 1], np.zeros((1, 4)), np.zeros((1, 4)), [4], [1],
+                      np.zeros((1, 2), np.float32))
