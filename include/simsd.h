@@ -1,0 +1,233 @@
+/*
+ * simsd.h -- C ABI of libsimsd.so: the SimSD speculative-verification step
+ * for diffusion language models on one NVIDIA GB300 (sm_103a).
+ *
+ * Method: "SimSD: Simple Speculative Decoding in Diffusion Language Models"
+ * (gist.science technical summaries of paper 2606.02544):
+ *   section 1 "Input Layout"            -- prompt | D (B reference tokens) |
+ *                                          D~ (B [MASK] prediction slots);
+ *   section 2 "Temporal Attention Mask" -- step map tau, mask A_ij;
+ *   section 3 "Position Encoding Alignment" -- D~_k reuses D_k's RoPE index;
+ *   section 4 "Speculative Decoding Pipeline" -- one verification forward,
+ *                                          rejection sampling along tau.
+ *
+ * Conventions shared by every call
+ *   - Plain C types only.  "device" pointers are CUDA device memory of the
+ *     current device; "host" pointers are ordinary host memory.
+ *   - All memory is owned by the caller.  The device calls never allocate:
+ *     scratch lives in a caller-provided workspace whose size the matching
+ *     *_workspace_size function returns (256-byte aligned pointer required).
+ *   - Device calls are asynchronous and stream-ordered on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream).  They never
+ *     synchronise the host.
+ *   - Argument errors are detected on the host and returned before anything
+ *     is launched.  A launch failure returns SIMSD_ERR_CUDA.  Kernels never
+ *     trap: a bounded wait that runs out sets a bit in the workspace status
+ *     word, read with simsd_read_status() (which synchronises the stream).
+ *   - Token order inside a sequence with section length B is
+ *     D_1..D_B, D~_1..D~_B (2B tokens); sequences are back to back, so
+ *     sequence b's tokens start at row 2*cu_B[b].
+ *   - Limits: head_dim in {64, 128}; num_q_heads % num_kv_heads == 0;
+ *     1 <= B_b <= 32; page_size == 16; batch >= 1.
+ *   - The library is stateless and re-entrant.  Calls on different streams
+ *     must not share a workspace or write the same cache pages.
+ */
+#ifndef SIMSD_H
+#define SIMSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SIMSD_OK = 0,
+  SIMSD_ERR_NULL = 1,      /* a required pointer is NULL                    */
+  SIMSD_ERR_SHAPE = 2,     /* a size is out of range or inconsistent        */
+  SIMSD_ERR_TAU = 3,       /* tau is not a permutation of 1..B              */
+  SIMSD_ERR_DTYPE = 4,     /* unsupported dtype                             */
+  SIMSD_ERR_WORKSPACE = 5, /* workspace missing, misaligned or too small    */
+  SIMSD_ERR_CUDA = 6,      /* a CUDA runtime call or launch failed          */
+  SIMSD_ERR_TIMEOUT = 7    /* a device-side bounded wait ran out            */
+} simsd_status;
+
+typedef enum { SIMSD_F32 = 0, SIMSD_BF16 = 1 } simsd_dtype;
+
+/* Static text for a status code; never NULL. */
+const char *simsd_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int simsd_version(void);
+
+/* ------------------------------------------------------------------------
+ * simsd_layout -- host only.  Sections 1-3: paired layout, positions, mask.
+ *   prompt_len  P >= 0
+ *   B           1..32 (section length; also the draft length gamma)
+ *   tau         host int32[B], tau[k] = step label of response position k+1
+ *   positions   host int32[P+2B] out: prompt j -> j; D_k -> P+k-1;
+ *               D~_k -> P+k-1 (copied RoPE index)
+ *   mask        host uint8[2B][P+2B] out, may be NULL.  Row r < B is D_{r+1},
+ *               row B+i is D~_{i+1}; column c < P is prompt token c, then D,
+ *               then D~.  1 = may attend.  Slot rows: whole prompt, D_j with
+ *               tau(j) < tau(i), D~_j with tau(j) >= tau(i).  Data rows (a
+ *               convention: their outputs feed later layers, their logits
+ *               are not consumed): prompt and D_j with tau(j) <= tau(i).
+ * Errors: SIMSD_ERR_NULL, SIMSD_ERR_SHAPE, SIMSD_ERR_TAU.
+ * ---------------------------------------------------------------------- */
+simsd_status simsd_layout(int32_t prompt_len, int32_t B, const int32_t *tau,
+                          int32_t *positions, uint8_t *mask);
+
+/* ------------------------------------------------------------------------
+ * simsd_verify_attn -- sections 2-4: one attention layer of the verification
+ * forward over [prompt KV cache | D | D~] for a batch of sequences.
+ *
+ * Kernel sequence on `stream`:
+ *   K1  rotate q (all query heads) and k_new at the layout positions (D~_k
+ *       uses D_k's), write rotated k and raw v of the 2B new tokens into
+ *       cache slots [lens[b], lens[b]+2B_b) of sequence b;
+ *   K2  split-KV attention of all 2B_b x Hq query rows of a sequence and KV
+ *       head against the cache, the temporal mask evaluated on the fly;
+ *   K3  merge of the per-split partial softmax states.
+ * lens[] is NOT advanced: rolling back a rejected draft costs nothing, and
+ * committing accepted tokens is the caller's business.
+ *
+ * Layouts (row-major, innermost last):
+ *   q            device [T][Hq][hd]   raw queries, T = 2 * total_B
+ *   k_new, v_new device [T][Hkv][hd]  raw keys / values of the new tokens
+ *   k_cache, v_cache device [num_pages][Hkv][page_size][hd]; prompt slots
+ *                hold keys already rotated at their own positions
+ *   block_table  device int32[batch][max_pages_per_seq]; entries
+ *                0 .. ceil((lens[b]+2B_b)/16)-1 of row b must be valid page
+ *                ids < num_pages (the rest are never read)
+ *   tau          device int32[total_B]; sequence b's labels at cu_B[b]..
+ *   lens         device int32[batch]   prompt KV length P_b >= 0
+ *   cu_B         device int32[batch+1] prefix sums of B_b (cu_B[0] = 0)
+ *   out          device [T][Hq][hd]    attention output of every new row
+ * dtype applies to q, k/v (new and cache) and out.
+ * Host-side fields (total_B, B_max, max_pages_per_seq) must agree with the
+ * device arrays; the device trusts them and tau (a wrong tau gives a wrong
+ * mask, never an out-of-bounds access; lens[b]+2B_b must fit the table).
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t batch;
+  int32_t num_q_heads;        /* Hq                                         */
+  int32_t num_kv_heads;       /* Hkv                                        */
+  int32_t head_dim;           /* hd: 64 or 128                              */
+  int32_t page_size;          /* 16                                         */
+  int32_t num_pages;          /* pages in each cache array                  */
+  int32_t max_pages_per_seq;  /* row stride of block_table                  */
+  int32_t total_B;            /* sum_b B_b (host copy)                      */
+  int32_t B_max;              /* max_b B_b (host copy), 1..32               */
+  simsd_dtype dtype;
+  float rope_base;            /* RoPE base (e.g. 1e6)                       */
+  float sm_scale;             /* score = sm_scale * q.k                     */
+  const void *q;
+  void *k_cache;
+  void *v_cache;
+  const int32_t *block_table;
+  const void *k_new;
+  const void *v_new;
+  const int32_t *tau;
+  const int32_t *lens;
+  const int32_t *cu_B;
+  void *out;
+  void *workspace;            /* device, 256-byte aligned                   */
+  size_t workspace_bytes;
+} simsd_verify_desc;
+
+/* Bytes of workspace simsd_verify_attn needs for these sizes (reads only
+ * the host-side fields).  Returns 0 if the sizes are invalid. */
+size_t simsd_verify_workspace_size(const simsd_verify_desc *d);
+simsd_status simsd_verify_attn(const simsd_verify_desc *d, void *stream);
+
+/* ------------------------------------------------------------------------
+ * simsd_prompt_append -- K1 on plain positions: rotate n_b raw keys of
+ * sequence b at positions start[b] .. start[b]+n_b-1 and write them (and
+ * the raw values) into the same cache slots.  Fills a prompt's cache, or
+ * commits tokens after acceptance.
+ *   k, v     device [sum n_b][Hkv][hd]   raw keys / values
+ *   start    device int32[batch]         first slot (= position) per seq
+ *   cu_n     device int32[batch+1]       prefix sums of n_b
+ *   total_n  host: sum n_b
+ *   block_table as above; every slot written must be covered.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t batch;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t max_pages_per_seq;
+  int32_t total_n;
+  simsd_dtype dtype;
+  float rope_base;
+  const void *k;
+  const void *v;
+  const int32_t *start;
+  const int32_t *cu_n;
+  void *k_cache;
+  void *v_cache;
+  const int32_t *block_table;
+} simsd_append_desc;
+
+simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
+
+/* ------------------------------------------------------------------------
+ * simsd_accept -- section 4, acceptance: standard rejection sampling along
+ * the temporal order tau.  For sequence b and steps t = 1..B_b, slot
+ * k = tau^-1(t) with draft token x = draft_tokens[k]:
+ *   p = softmax(target row k), q = softmax(draft row k) (fp32 math);
+ *   accept iff u[t-1] * q(x) < p(x);
+ *   at the first rejection draw a token from max(0, p - q) normalised (p
+ *   itself if that is empty) by inverse CDF with u[B_b], and stop.
+ * Kernels: K4a (per slot and vocabulary chunk: max and sum of exponentials
+ * of both rows), K4b (one CTA per sequence: the walk and the residual draw).
+ *   target_logits, draft_logits device [total_B][vocab] (dtype); row k of
+ *                sequence b (at cu_B[b]+k) holds the logits read at D~_k
+ *   draft_tokens device int32[total_B] in [0, vocab)
+ *   tau, cu_B    device, as for simsd_verify_attn
+ *   uniforms     device float32[batch][B_max+1], values in [0, 1)
+ *   n_accept     device int32[batch] out: accepted prefix length (0..B_b)
+ *   token        device int32[batch] out: token drawn at the rejection,
+ *                -1 when every step was accepted (no bonus token: the
+ *                layout has no slot after D~_B)
+ *   pos          device int32[batch] out: response position (0-based k) of
+ *                the rejected slot, -1 when none
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t batch;
+  int32_t vocab;
+  int32_t total_B;            /* host copy                                  */
+  int32_t B_max;              /* host copy, 1..32                           */
+  simsd_dtype dtype;          /* of the logits                              */
+  const void *target_logits;
+  const void *draft_logits;
+  const int32_t *draft_tokens;
+  const int32_t *tau;
+  const int32_t *cu_B;
+  const float *uniforms;
+  int32_t *n_accept;
+  int32_t *token;
+  int32_t *pos;
+  void *workspace;            /* device, 256-byte aligned                   */
+  size_t workspace_bytes;
+} simsd_accept_desc;
+
+size_t simsd_accept_workspace_size(const simsd_accept_desc *d);
+simsd_status simsd_accept(const simsd_accept_desc *d, void *stream);
+
+/* ------------------------------------------------------------------------
+ * simsd_read_status -- synchronise `stream`, copy the device status word of
+ * a workspace used by simsd_verify_attn / simsd_accept to *word_out (bit 0:
+ * a bounded wait ran out) and clear it.  Returns SIMSD_ERR_TIMEOUT when a
+ * bit was set, SIMSD_OK otherwise, SIMSD_ERR_CUDA on a CUDA error.
+ * ---------------------------------------------------------------------- */
+simsd_status simsd_read_status(void *workspace, void *stream,
+                               uint32_t *word_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SIMSD_H */

@@ -1,0 +1,237 @@
+// api.cu -- host side of the C ABI: argument checks, planning, launches.
+//
+// simsd_layout follows SimSD sections 1-3 (paired layout, temporal mask,
+// RoPE copy); simsd_verify_attn and simsd_prompt_append plan and launch the
+// kernels K1-K3; the acceptance entry points live in accept.cu.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace simsd {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+void make_rope_table(float base, int hd, RopeTable *t) {
+  memset(t, 0, sizeof(*t));
+  for (int d = 0; d < hd / 2 && d < 64; ++d)
+    t->inv_freq[d] = pow((double)base, -2.0 * (double)d / (double)hd);
+}
+
+static bool valid_dtype(simsd_dtype t) { return t == SIMSD_F32 || t == SIMSD_BF16; }
+
+simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
+  if (d == nullptr || p == nullptr) return SIMSD_ERR_NULL;
+  if (!valid_dtype(d->dtype)) return SIMSD_ERR_DTYPE;
+  if (d->batch < 1 || d->num_q_heads < 1 || d->num_kv_heads < 1 ||
+      d->num_q_heads % d->num_kv_heads != 0 ||
+      (d->head_dim != 64 && d->head_dim != 128) || d->page_size != kPageTokens ||
+      d->num_pages < 1 || d->max_pages_per_seq < 1 || d->B_max < 1 ||
+      d->B_max > kMaxB || d->total_B < d->batch ||
+      (int64_t)d->total_B > (int64_t)d->batch * d->B_max)
+    return SIMSD_ERR_SHAPE;
+  if (!(d->sm_scale == d->sm_scale) || !(d->rope_base > 1.0f)) return SIMSD_ERR_SHAPE;
+  memset(p, 0, sizeof(*p));
+  p->T = 2 * d->total_B;
+  p->G = d->num_q_heads / d->num_kv_heads;
+  p->M_max = 2 * d->B_max * p->G;
+  p->esize = d->dtype == SIMSD_BF16 ? 2 : 4;
+  if (d->dtype == SIMSD_BF16) {
+    // 8 consumer warps; each owns 16 query rows, warps beyond the rows
+    // split every stage's keys among themselves.
+    int groups = (p->M_max + 15) / 16;
+    int rg = 1;
+    while (rg < groups && rg < 8) rg *= 2;
+    p->rows_per_tile = rg * 16;
+    p->key_splits = 8 / rg;
+  } else {
+    p->rows_per_tile = p->M_max;
+    p->key_splits = 1;
+  }
+  p->row_tiles = (p->M_max + p->rows_per_tile - 1) / p->rows_per_tile;
+  // Split the key range so the grid covers the GPU a few times over, but
+  // no split is longer than 4096 keys (balance for ragged batches).
+  const int64_t max_keys = (int64_t)d->max_pages_per_seq * kPageTokens;
+  const int64_t max_blocks = (max_keys + kBlockKeys - 1) / kBlockKeys;
+  const int64_t pairs = (int64_t)d->batch * d->num_kv_heads * p->row_tiles;
+  int64_t splits = (4 * (int64_t)device_sm_count() + pairs - 1) / pairs;
+  int64_t by_len = (max_keys + 4095) / 4096;
+  if (splits < by_len) splits = by_len;
+  if (splits > max_blocks) splits = max_blocks;
+  if (splits < 1) splits = 1;
+  int64_t blocks_per_split = (max_blocks + splits - 1) / splits;
+  p->chunk = (int)(blocks_per_split * kBlockKeys);
+  p->n_splits = (int)((max_keys + p->chunk - 1) / p->chunk);
+  // workspace
+  size_t off = 0;
+  p->off_status = off;  off = align_up(off + sizeof(uint32_t), kAlign);
+  p->off_qrot = off;    off = align_up(off + (size_t)p->T * d->num_q_heads * d->head_dim * p->esize, kAlign);
+  p->off_tokseq = off;  off = align_up(off + (size_t)p->T * sizeof(int32_t), kAlign);
+  p->off_opart = off;
+  if (p->n_splits > 1) {
+    off = align_up(off + (size_t)p->n_splits * p->T * d->num_q_heads * d->head_dim * sizeof(float), kAlign);
+    p->off_ml = off;
+    off = align_up(off + (size_t)p->n_splits * p->T * d->num_q_heads * sizeof(float2), kAlign);
+  } else {
+    p->off_ml = off;
+  }
+  p->total = off;
+  return SIMSD_OK;
+}
+
+}  // namespace simsd
+
+using namespace simsd;
+
+extern "C" {
+
+const char *simsd_status_string(int status) {
+  switch (status) {
+    case SIMSD_OK: return "ok";
+    case SIMSD_ERR_NULL: return "a required pointer is NULL";
+    case SIMSD_ERR_SHAPE: return "a size is out of range or inconsistent";
+    case SIMSD_ERR_TAU: return "tau is not a permutation of 1..B";
+    case SIMSD_ERR_DTYPE: return "unsupported dtype";
+    case SIMSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SIMSD_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case SIMSD_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+    default: return "unknown status";
+  }
+}
+
+int simsd_version(void) { return 100; }
+
+simsd_status simsd_layout(int32_t P, int32_t B, const int32_t *tau,
+                          int32_t *positions, uint8_t *mask) {
+  if (tau == nullptr || positions == nullptr) return SIMSD_ERR_NULL;
+  if (P < 0 || B < 1 || B > kMaxB) return SIMSD_ERR_SHAPE;
+  // tau must label the B response positions with the steps 1..B, each once
+  uint32_t seen = 0;
+  for (int k = 0; k < B; ++k) {
+    const int t = tau[k];
+    if (t < 1 || t > B || (seen >> (t - 1)) & 1u) return SIMSD_ERR_TAU;
+    seen |= 1u << (t - 1);
+  }
+  for (int j = 0; j < P; ++j) positions[j] = j;
+  for (int k = 0; k < B; ++k) {
+    positions[P + k] = P + k;      // data token D_{k+1}
+    positions[P + B + k] = P + k;  // slot D~_{k+1}: RoPE index copied
+  }
+  if (mask != nullptr) {
+    const int64_t L = (int64_t)P + 2 * B;
+    for (int r = 0; r < 2 * B; ++r) {
+      uint8_t *row = mask + (int64_t)r * L;
+      memset(row, 1, (size_t)P);
+      const bool slot_row = r >= B;
+      const int ti = tau[slot_row ? r - B : r];
+      for (int j = 0; j < B; ++j) {
+        const int tj = tau[j];
+        // data columns: slots see strictly earlier steps, data rows see
+        // their own step and earlier ones
+        row[P + j] = slot_row ? (tj < ti) : (tj <= ti);
+        // slot columns: slots see their own and later steps, data rows none
+        row[P + B + j] = slot_row ? (tj >= ti) : 0;
+      }
+    }
+  }
+  return SIMSD_OK;
+}
+
+size_t simsd_verify_workspace_size(const simsd_verify_desc *d) {
+  VerifyPlan p;
+  if (verify_plan(d, &p) != SIMSD_OK) return 0;
+  return p.total;
+}
+
+simsd_status simsd_verify_attn(const simsd_verify_desc *d, void *stream_ptr) {
+  VerifyPlan p;
+  simsd_status st = verify_plan(d, &p);
+  if (st != SIMSD_OK) return st;
+  if (!d->q || !d->k_cache || !d->v_cache || !d->block_table || !d->k_new ||
+      !d->v_new || !d->tau || !d->lens || !d->cu_B || !d->out)
+    return SIMSD_ERR_NULL;
+  if (d->workspace == nullptr || ((uintptr_t)d->workspace % kAlign) != 0 ||
+      d->workspace_bytes < p.total)
+    return SIMSD_ERR_WORKSPACE;
+  cudaStream_t stream = (cudaStream_t)stream_ptr;
+  char *ws = (char *)d->workspace;
+  uint32_t *status = (uint32_t *)(ws + p.off_status);
+  void *q_rot = ws + p.off_qrot;
+  int32_t *tok_seq = (int32_t *)(ws + p.off_tokseq);
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess)
+    return SIMSD_ERR_CUDA;
+  if (launch_rope_verify(d, p, q_rot, tok_seq, status, stream) != cudaSuccess)
+    return SIMSD_ERR_CUDA;
+  AttnParams a;
+  memset(&a, 0, sizeof(a));
+  a.q_rot = q_rot;
+  a.out = d->out;
+  a.o_part = (float *)(ws + p.off_opart);
+  a.ml_part = (float2 *)(ws + p.off_ml);
+  a.tau = d->tau;
+  a.lens = d->lens;
+  a.cu_B = d->cu_B;
+  a.block_table = d->block_table;
+  a.k_cache = d->k_cache;
+  a.v_cache = d->v_cache;
+  a.status = status;
+  a.max_pages_per_seq = d->max_pages_per_seq;
+  a.num_pages = d->num_pages;
+  a.Hq = d->num_q_heads;
+  a.Hkv = d->num_kv_heads;
+  a.G = p.G;
+  a.T = p.T;
+  a.chunk = p.chunk;
+  a.rows_per_tile = p.rows_per_tile;
+  a.sm_scale = d->sm_scale;
+  cudaError_t e = d->dtype == SIMSD_BF16 ? launch_attn_bf16(d, p, a, stream)
+                                         : launch_attn_f32(d, p, a, stream);
+  if (e != cudaSuccess) return SIMSD_ERR_CUDA;
+  if (p.n_splits > 1 && launch_combine(d, p, a, tok_seq, stream) != cudaSuccess)
+    return SIMSD_ERR_CUDA;
+  return SIMSD_OK;
+}
+
+simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream_ptr) {
+  if (d == nullptr) return SIMSD_ERR_NULL;
+  if (!valid_dtype(d->dtype)) return SIMSD_ERR_DTYPE;
+  if (d->batch < 1 || d->num_kv_heads < 1 ||
+      (d->head_dim != 64 && d->head_dim != 128) || d->page_size != kPageTokens ||
+      d->num_pages < 1 || d->max_pages_per_seq < 1 || d->total_n < 0 ||
+      !(d->rope_base > 1.0f))
+    return SIMSD_ERR_SHAPE;
+  if (!d->k || !d->v || !d->start || !d->cu_n || !d->k_cache || !d->v_cache ||
+      !d->block_table)
+    return SIMSD_ERR_NULL;
+  if (d->total_n == 0) return SIMSD_OK;
+  return launch_rope_append(d, (cudaStream_t)stream_ptr) == cudaSuccess ? SIMSD_OK
+                                                                        : SIMSD_ERR_CUDA;
+}
+
+simsd_status simsd_read_status(void *workspace, void *stream_ptr, uint32_t *word_out) {
+  if (workspace == nullptr) return SIMSD_ERR_NULL;
+  cudaStream_t stream = (cudaStream_t)stream_ptr;
+  uint32_t w = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SIMSD_ERR_CUDA;
+  if (cudaMemcpy(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SIMSD_ERR_CUDA;
+  if (cudaMemset(workspace, 0, sizeof(w)) != cudaSuccess) return SIMSD_ERR_CUDA;
+  if (word_out) *word_out = w;
+  return w ? SIMSD_ERR_TIMEOUT : SIMSD_OK;
+}
+
+}  // extern "C"

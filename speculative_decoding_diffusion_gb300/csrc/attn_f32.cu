@@ -1,0 +1,187 @@
+// attn_f32.cu -- K2 (fp32 I/O) and K3: split-KV masked attention on CUDA
+// cores for fp32 caches, and the merge of split partials for both dtypes.
+//
+// SimSD section 2 "Temporal Attention Mask": every new row sees the whole
+// prompt; slot D~_i sees D_j with tau(j) < tau(i) and D~_j with
+// tau(j) >= tau(i); data row D_i (convention) sees D_j with tau(j) <= tau(i).
+//
+// The fp32 path keeps full fp32 arithmetic (no tensor-core rounding of the
+// operands), for small fp32 workloads that need 1e-4 agreement.  One CTA per
+// (split, KV head, sequence); each warp takes one query row at a time, lanes
+// stride over keys for the scores and over head dimensions for P.V.  The
+// softmax runs online in the log2 domain, like the bf16 kernel, so both
+// produce partials K3 can merge.
+#include "common.cuh"
+#include "internal.h"
+
+namespace simsd {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Visibility of key index `key` (0..P+2B-1) for a new row with token index
+// `tok` (0..2B-1), tau of the new tokens in tau_s[0..2B).
+__device__ __forceinline__ bool visible(int P, int B, const int *tau_s, int tok, int key) {
+  if (key < P) return true;
+  const int j = key - P;
+  const int ti = tau_s[tok], tj = tau_s[j];
+  const bool row_slot = tok >= B, key_slot = j >= B;
+  if (row_slot) return key_slot ? tj >= ti : tj < ti;
+  return !key_slot && tj <= ti;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kWarps * 32)
+attn_f32_kernel(const __grid_constant__ AttnParams a) {
+  constexpr int PER = HD / 32;
+  __shared__ int tau_s[2 * kMaxB];
+  __shared__ float q_s[kWarps][HD];
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int c0 = __ldg(a.cu_B + b);
+  const int B = __ldg(a.cu_B + b + 1) - c0;
+  const int P = __ldg(a.lens + b);
+  const int Lk = P + 2 * B;
+  const int M = 2 * B * a.G;
+  const int k_begin = split * a.chunk;
+  if (B < 1 || B > kMaxSection || P < 0 || (long)Lk > (long)a.max_pages_per_seq * kPage) {
+    if (threadIdx.x == 0 && split == 0 && kvh == 0) raise_status(a.status, kStatusBadInput);
+    return;
+  }
+  if (k_begin >= Lk) return;
+  const int k_end = min(Lk, k_begin + a.chunk);
+  const int n_splits_b = (Lk + a.chunk - 1) / a.chunk;
+  for (int j = threadIdx.x; j < 2 * B; j += blockDim.x)
+    tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float *qr = (const float *)a.q_rot;
+  const float *kc = (const float *)a.k_cache;
+  const float *vc = (const float *)a.v_cache;
+  const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
+  const float scale = a.sm_scale * kLog2e;
+  for (int r = warp; r < M; r += kWarps) {
+    const int tok = r / a.G;
+    const int head = kvh * a.G + r % a.G;
+    const long row = (2L * c0 + tok) * a.Hq + head;
+    for (int d = lane; d < HD; d += 32) q_s[warp][d] = qr[row * HD + d];
+    __syncwarp();
+    float m = -INFINITY, l = 0.f, o[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o[i] = 0.f;
+    for (int base = k_begin; base < k_end; base += 32) {
+      const int key = base + lane;
+      float s = -INFINITY;
+      const int kpage = key < k_end ? __ldg(bt + key / kPage) : -1;
+      if (kpage >= 0 && kpage < a.num_pages && visible(P, B, tau_s, tok, key)) {
+        const int page = kpage;
+        const float *kr = kc + (((long)page * a.Hkv + kvh) * kPage + key % kPage) * HD;
+        float acc = 0.f;
+#pragma unroll 8
+        for (int d = 0; d < HD; ++d) acc = fmaf(q_s[warp][d], kr[d], acc);
+        s = acc * scale;
+      }
+      float cm = s;
+#pragma unroll
+      for (int w = 16; w > 0; w >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, w));
+      const float m_new = fmaxf(m, cm);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = exp2f(m - m_use);
+      const float p = exp2f(s - m_use);
+      float ps = p;
+#pragma unroll
+      for (int w = 16; w > 0; w >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, w);
+      l = l * alpha + ps;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) o[i] *= alpha;
+      for (int j = 0; j < 32; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, p, j);
+        if (pj == 0.f) continue;            // masked or past the end
+        const int kj = base + j;
+        const int page = __ldg(bt + kj / kPage);
+        const float *vr = vc + (((long)page * a.Hkv + kvh) * kPage + kj % kPage) * HD;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) o[i] = fmaf(pj, vr[lane + 32 * i], o[i]);
+      }
+      m = m_new;
+    }
+    if (n_splits_b == 1) {
+      float *out = (float *)a.out + row * HD;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) out[lane + 32 * i] = o[i] / l;
+    } else {
+      const long prow = (long)split * a.T * a.Hq + row;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) a.o_part[prow * HD + lane + 32 * i] = o[i];
+      if (lane == 0) a.ml_part[prow] = make_float2(m, l);
+    }
+    __syncwarp();
+  }
+}
+
+// K3: O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s, one warp per
+// (token, query head) row; rows of single-split sequences were finished by K2.
+template <typename T, int HD>
+__global__ void __launch_bounds__(256)
+combine_kernel(const __grid_constant__ AttnParams a, const int32_t *tok_seq) {
+  constexpr int PER = HD / 32;
+  const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= (long)a.T * a.Hq) return;
+  const int tok = (int)(row / a.Hq);
+  const int b = __ldg(tok_seq + tok);
+  const int c0 = __ldg(a.cu_B + b);
+  const int Lk = __ldg(a.lens + b) + 2 * (__ldg(a.cu_B + b + 1) - c0);
+  const int ns = (Lk + a.chunk - 1) / a.chunk;
+  if (ns <= 1 || (long)Lk > (long)a.max_pages_per_seq * kPage) return;
+  const long stride = (long)a.T * a.Hq;
+  float mstar = -INFINITY;
+  for (int s = 0; s < ns; ++s) mstar = fmaxf(mstar, a.ml_part[s * stride + row].x);
+  const float mu = mstar == -INFINITY ? 0.f : mstar;
+  float den = 0.f, o[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) o[i] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float2 ml = a.ml_part[s * stride + row];
+    const float w = exp2f(ml.x - mu);
+    den += w * ml.y;
+    const float *op = a.o_part + (s * stride + row) * HD;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) o[i] = fmaf(w, op[lane + 32 * i], o[i]);
+  }
+  const float inv = 1.f / den;
+  T *out = (T *)a.out + row * HD;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) Elem<T>::store(out + lane + 32 * i, o[i] * inv);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
+                            const AttnParams &a, cudaStream_t stream) {
+  dim3 grid(p.n_splits, d->num_kv_heads, d->batch);
+  if (d->head_dim == 128)
+    attn_f32_kernel<128><<<grid, kWarps * 32, 0, stream>>>(a);
+  else
+    attn_f32_kernel<64><<<grid, kWarps * 32, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
+                           const AttnParams &a, const int32_t *tok_seq,
+                           cudaStream_t stream) {
+  const long rows = (long)p.T * d->num_q_heads;
+  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  if (d->dtype == SIMSD_BF16) {
+    if (d->head_dim == 128) combine_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, stream>>>(a, tok_seq);
+    else combine_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, stream>>>(a, tok_seq);
+  } else {
+    if (d->head_dim == 128) combine_kernel<float, 128><<<blocks, 256, 0, stream>>>(a, tok_seq);
+    else combine_kernel<float, 64><<<blocks, 256, 0, stream>>>(a, tok_seq);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace simsd

@@ -1,0 +1,83 @@
+// internal.h -- host-side plan and kernel launchers of libsimsd (not ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/simsd.h"
+
+namespace simsd {
+
+constexpr int kBlockKeys = 128;   // keys per pipeline stage of the attention
+constexpr int kPageTokens = 16;  // tokens per KV-cache page (ABI page_size)
+constexpr int kMaxB = 32;
+constexpr size_t kAlign = 256;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Everything simsd_verify_attn derives on the host from the descriptor.
+struct VerifyPlan {
+  int T;             // new tokens, 2 * total_B
+  int G;             // query heads per KV head
+  int M_max;         // max query rows per (sequence, KV head): 2 * B_max * G
+  int rows_per_tile; // query rows one CTA owns
+  int row_tiles;     // CTAs per (sequence, KV head, split) along the rows
+  int key_splits;    // warps sharing one stage's keys (mma path)
+  int chunk;         // keys per split (multiple of kBlockKeys)
+  int n_splits;      // splits of the longest possible sequence
+  size_t esize;      // bytes per q/k/v/out element
+  // workspace carve-up (byte offsets)
+  size_t off_status, off_qrot, off_tokseq, off_opart, off_ml, total;
+};
+
+// Fills *plan; returns SIMSD_OK or the first argument error.
+simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *plan);
+
+// Parameters every attention kernel reads.
+struct AttnParams {
+  const void *q_rot;          // [T][Hq][hd], rotated
+  void *out;                  // [T][Hq][hd]
+  float *o_part;              // [n_splits][T][Hq][hd]
+  float2 *ml_part;            // [n_splits][T][Hq]  (running max, sum)
+  const int32_t *tau;
+  const int32_t *lens;
+  const int32_t *cu_B;
+  const int32_t *block_table;
+  const void *k_cache;        // fp32 path reads the cache directly
+  const void *v_cache;
+  uint32_t *status;
+  int max_pages_per_seq;
+  int num_pages;
+  int Hq, Hkv, G, T;
+  int chunk, rows_per_tile;
+  float sm_scale;
+};
+
+// K1: rotate q and k_new at the layout positions, append k/v to the cache.
+cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
+                               void *q_rot, int32_t *tok_seq, uint32_t *status,
+                               cudaStream_t stream);
+cudaError_t launch_rope_append(const simsd_append_desc *d, cudaStream_t stream);
+
+// K2: split-KV masked attention.
+cudaError_t launch_attn_bf16(const simsd_verify_desc *d, const VerifyPlan &p,
+                             const AttnParams &a, cudaStream_t stream);
+cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
+                            const AttnParams &a, cudaStream_t stream);
+
+// K3: merge split partials.
+cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
+                           const AttnParams &a, const int32_t *tok_seq,
+                           cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// RoPE inverse frequencies base^(-2d/hd), d < hd/2, computed in double.
+struct RopeTable {
+  double inv_freq[64];
+};
+void make_rope_table(float base, int hd, RopeTable *t);
+
+}  // namespace simsd

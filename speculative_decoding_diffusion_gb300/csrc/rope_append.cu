@@ -1,0 +1,245 @@
+// rope_append.cu -- K1: RoPE-copy rotation and paged KV append.
+//
+// SimSD section 3 "Position Encoding Alignment": each mask slot D~_k reuses
+// the RoPE index of its data token D_k, so both new tokens of response
+// position k (1-based) of a sequence with prompt length P rotate at P+k-1.
+// Section 1 "Input Layout": the 2B new tokens occupy layout indices
+// P .. P+2B-1 (D_1..D_B then D~_1..D~_B); those are the cache slots written.
+//
+// One CTA per new token.  The angle pos * base^(-2d/hd) is formed in fp64
+// and reduced modulo 2*pi in fp64 (positions reach ~3.3e4, where an fp32
+// product would be off by ~2e-3 rad); sine and cosine of the reduced angle
+// and the rotation itself are fp32.  Rotate-half pairing: element d pairs
+// with d + hd/2.  Loads and stores are 16-byte vectors.
+#include "common.cuh"
+#include "internal.h"
+
+namespace simsd {
+namespace {
+
+constexpr int kThreads = 128;
+
+// Angles for one position into smem: cs[2d] = cos, cs[2d+1] = sin.
+__device__ __forceinline__ void angles(const RopeTable &tab, int hd, int pos,
+                                       float2 *cs) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int d = threadIdx.x; d < hd / 2; d += blockDim.x) {
+    double th = (double)pos * tab.inv_freq[d];
+    double n = rint(th * (1.0 / two_pi));
+    float r = (float)fma(-n, two_pi, th);  // th - 2*pi*n, |r| <= pi
+    float s, c;
+    sincosf(r, &s, &c);
+    cs[d] = make_float2(c, s);
+  }
+}
+
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int N = 4;
+  using V = float4;
+  static __device__ __forceinline__ void unpack(const V &v, float *f) {
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
+  static __device__ __forceinline__ V pack(const float *f) {
+    return make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  using V = uint4;
+  static __device__ __forceinline__ void unpack(const V &v, float *f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  static __device__ __forceinline__ V pack(const float *f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+  }
+};
+
+// Rotate `heads` rows of hd elements from src into dst (row h at h*hd; dst
+// rows at dst_stride apart) with the angles in cs.
+template <typename T>
+__device__ __forceinline__ void rotate_rows(const T *src, T *dst, int heads,
+                                            int hd, long dst_stride,
+                                            const float2 *cs) {
+  using VT = Vec<T>;
+  constexpr int N = VT::N;
+  const int half = hd / 2;
+  const int per_head = half / N;  // vector pairs per head
+  for (int i = threadIdx.x; i < heads * per_head; i += blockDim.x) {
+    const int h = i / per_head;
+    const int d0 = (i % per_head) * N;
+    const T *x = src + (long)h * hd;
+    typename VT::V a = *reinterpret_cast<const typename VT::V *>(x + d0);
+    typename VT::V b = *reinterpret_cast<const typename VT::V *>(x + d0 + half);
+    float x1[N], x2[N], y1[N], y2[N];
+    VT::unpack(a, x1);
+    VT::unpack(b, x2);
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const float c = cs[d0 + j].x, s = cs[d0 + j].y;
+      y1[j] = x1[j] * c - x2[j] * s;
+      y2[j] = x2[j] * c + x1[j] * s;
+    }
+    T *y = dst + (long)h * dst_stride;
+    *reinterpret_cast<typename VT::V *>(y + d0) = VT::pack(y1);
+    *reinterpret_cast<typename VT::V *>(y + d0 + half) = VT::pack(y2);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ void copy_rows(const T *src, T *dst, int heads,
+                                          int hd, long dst_stride) {
+  using VT = Vec<T>;
+  constexpr int N = VT::N;
+  const int per_head = hd / N;
+  for (int i = threadIdx.x; i < heads * per_head; i += blockDim.x) {
+    const int h = i / per_head;
+    const int d0 = (i % per_head) * N;
+    *reinterpret_cast<typename VT::V *>(dst + (long)h * dst_stride + d0) =
+        *reinterpret_cast<const typename VT::V *>(src + (long)h * hd + d0);
+  }
+}
+
+struct RopeVerifyArgs {
+  RopeTable tab;
+  const void *q;
+  const void *k_new;
+  const void *v_new;
+  void *q_rot;
+  void *k_cache;
+  void *v_cache;
+  const int32_t *block_table;
+  const int32_t *lens;
+  const int32_t *cu_B;
+  int32_t *tok_seq;
+  uint32_t *status;
+  int batch, Hq, Hkv, hd, max_pages, num_pages;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
+  __shared__ float2 cs[64];
+  const int r = blockIdx.x;                  // new-token row
+  const int b = find_seq(a.cu_B, a.batch, r >> 1);
+  const int c0 = __ldg(a.cu_B + b);
+  const int B = __ldg(a.cu_B + b + 1) - c0;
+  const int P = __ldg(a.lens + b);
+  if (threadIdx.x == 0) a.tok_seq[r] = b;    // the merge kernel reads it
+  if (B < 1 || B > kMaxSection || P < 0 || (long)P + 2 * B > (long)a.max_pages * kPage) {
+    if (threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
+    return;                                  // malformed sequence: write nothing
+  }
+  const int j = r - 2 * c0;                  // 0..2B-1 within the sequence
+  const int k = j < B ? j : j - B;           // response index (0-based)
+  const int pos = P + k;                     // D~_k copies D_k's position
+  const int slot = P + j;                    // layout index = cache slot
+  const int page = j < 2 * B ? __ldg(a.block_table + (long)b * a.max_pages + slot / kPage) : -1;
+  if (page < 0 || page >= a.num_pages) {     // cu_B or block table out of range
+    if (threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
+    return;
+  }
+  angles(a.tab, a.hd, pos, cs);
+  __syncthreads();
+  const T *q = (const T *)a.q + (long)r * a.Hq * a.hd;
+  rotate_rows<T>(q, (T *)a.q_rot + (long)r * a.Hq * a.hd, a.Hq, a.hd, a.hd, cs);
+  const long base = ((long)page * a.Hkv * kPage + slot % kPage) * a.hd;
+  const long stride = (long)kPage * a.hd;    // next KV head, same slot
+  rotate_rows<T>((const T *)a.k_new + (long)r * a.Hkv * a.hd,
+                 (T *)a.k_cache + base, a.Hkv, a.hd, stride, cs);
+  copy_rows<T>((const T *)a.v_new + (long)r * a.Hkv * a.hd,
+               (T *)a.v_cache + base, a.Hkv, a.hd, stride);
+}
+
+struct RopeAppendArgs {
+  RopeTable tab;
+  const void *k;
+  const void *v;
+  void *k_cache;
+  void *v_cache;
+  const int32_t *block_table;
+  const int32_t *start;
+  const int32_t *cu_n;
+  int batch, Hkv, hd, max_pages, num_pages;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+rope_append_kernel(const __grid_constant__ RopeAppendArgs a) {
+  __shared__ float2 cs[64];
+  const int r = blockIdx.x;
+  const int b = find_seq(a.cu_n, a.batch, r);
+  const int pos = __ldg(a.start + b) + (r - __ldg(a.cu_n + b));
+  if (pos < 0 || pos >= a.max_pages * kPage) return;   // outside the table row
+  const int page = __ldg(a.block_table + (long)b * a.max_pages + pos / kPage);
+  if (page < 0 || page >= a.num_pages) return;
+  angles(a.tab, a.hd, pos, cs);
+  __syncthreads();
+  const long base = ((long)page * a.Hkv * kPage + pos % kPage) * a.hd;
+  const long stride = (long)kPage * a.hd;
+  rotate_rows<T>((const T *)a.k + (long)r * a.Hkv * a.hd, (T *)a.k_cache + base,
+                 a.Hkv, a.hd, stride, cs);
+  copy_rows<T>((const T *)a.v + (long)r * a.Hkv * a.hd, (T *)a.v_cache + base,
+               a.Hkv, a.hd, stride);
+}
+
+}  // namespace
+
+cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
+                               void *q_rot, int32_t *tok_seq, uint32_t *status,
+                               cudaStream_t stream) {
+  RopeVerifyArgs a;
+  make_rope_table(d->rope_base, d->head_dim, &a.tab);
+  a.q = d->q;
+  a.k_new = d->k_new;
+  a.v_new = d->v_new;
+  a.q_rot = q_rot;
+  a.k_cache = d->k_cache;
+  a.v_cache = d->v_cache;
+  a.block_table = d->block_table;
+  a.lens = d->lens;
+  a.cu_B = d->cu_B;
+  a.tok_seq = tok_seq;
+  a.status = status;
+  a.num_pages = d->num_pages;
+  a.batch = d->batch;
+  a.Hq = d->num_q_heads;
+  a.Hkv = d->num_kv_heads;
+  a.hd = d->head_dim;
+  a.max_pages = d->max_pages_per_seq;
+  if (d->dtype == SIMSD_BF16)
+    rope_verify_kernel<__nv_bfloat16><<<p.T, kThreads, 0, stream>>>(a);
+  else
+    rope_verify_kernel<float><<<p.T, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rope_append(const simsd_append_desc *d, cudaStream_t stream) {
+  RopeAppendArgs a;
+  make_rope_table(d->rope_base, d->head_dim, &a.tab);
+  a.k = d->k;
+  a.v = d->v;
+  a.k_cache = d->k_cache;
+  a.v_cache = d->v_cache;
+  a.block_table = d->block_table;
+  a.start = d->start;
+  a.cu_n = d->cu_n;
+  a.batch = d->batch;
+  a.Hkv = d->num_kv_heads;
+  a.hd = d->head_dim;
+  a.max_pages = d->max_pages_per_seq;
+  a.num_pages = d->num_pages;
+  if (d->dtype == SIMSD_BF16)
+    rope_append_kernel<__nv_bfloat16><<<d->total_n, kThreads, 0, stream>>>(a);
+  else
+    rope_append_kernel<float><<<d->total_n, kThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace simsd

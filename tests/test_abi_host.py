@@ -1,0 +1,149 @@
+"""Host-side checks of libsimsd.so (no GPU needed, no kernel launched).
+
+- the library loads and exports every function include/simsd.h declares;
+- simsd_layout matches the oracle bit for bit (positions and mask) over all
+  orders for B <= 6 and random orders up to B = 32;
+- argument errors come back as status codes before anything is launched.
+"""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_diffusion_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_diffusion_gb300 import build
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(simsd_[a-z_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.simsd_version() >= 100
+    for code in range(8):
+        assert binding.status_string(code) != "unknown status"
+
+
+def test_layout_matches_oracle_all_orders(lib):
+    for B in range(1, 7):
+        for P in (0, 3):
+            for perm in itertools.permutations(range(1, B + 1)):
+                pos, m = binding.layout(P, perm)
+                opos, om = oracle.layout(P, np.array(perm))
+                assert np.array_equal(pos.numpy(), opos)
+                assert np.array_equal(m.numpy(), om)
+
+
+def test_layout_matches_oracle_random(lib):
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        B = int(rng.integers(1, 33))
+        P = int(rng.integers(0, 300))
+        tau = rng.permutation(B) + 1
+        pos, m = binding.layout(P, tau.tolist())
+        opos, om = oracle.layout(P, tau)
+        assert np.array_equal(pos.numpy(), opos)
+        assert np.array_equal(m.numpy(), om)
+        pos2, none = binding.layout(P, tau.tolist(), with_mask=False)
+        assert none is None and np.array_equal(pos2.numpy(), opos)
+
+
+@pytest.mark.parametrize("tau,codes", [([1, 1, 2], (3,)), ([0, 1, 2], (3,)), ([1, 2, 4], (3,)),
+                                       ([], (1, 2)), (list(range(1, 34)), (2,))])
+def test_layout_errors(lib, tau, codes):
+    with pytest.raises(binding.SimsdError) as e:
+        binding.layout(4, tau)
+    assert e.value.code in codes
+
+
+def _desc(**kw):
+    d = binding.VerifyDesc()
+    base = dict(batch=2, num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16,
+                num_pages=300, max_pages_per_seq=150, total_B=8, B_max=4,
+                dtype=binding.SIMSD_BF16, rope_base=1e6, sm_scale=1.0)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_verify_workspace_size_and_shape_errors(lib):
+    n = lib.simsd_verify_workspace_size(ctypes.byref(_desc()))
+    # at least the rotated queries: T * Hq * hd * 2 bytes
+    assert n >= 16 * 32 * 128 * 2 and n % 256 == 0
+    for bad in (dict(head_dim=96), dict(num_q_heads=30), dict(page_size=32),
+                dict(B_max=33), dict(total_B=1), dict(total_B=9), dict(batch=0),
+                dict(dtype=7), dict(num_pages=0)):
+        d = _desc(**bad)
+        assert lib.simsd_verify_workspace_size(ctypes.byref(d)) == 0, bad
+        code = lib.simsd_verify_attn(ctypes.byref(d), None)
+        assert code in (2, 4), (bad, code)
+    # valid sizes but NULL pointers
+    assert lib.simsd_verify_attn(ctypes.byref(_desc()), None) == 1
+    assert lib.simsd_verify_attn(None, None) == 1
+
+
+def test_verify_workspace_errors(lib):
+    d = _desc()
+    fake = 1 << 40     # never dereferenced: the call returns before launching
+    for f in ("q", "k_cache", "v_cache", "block_table", "k_new", "v_new", "tau",
+              "lens", "cu_B", "out"):
+        setattr(d, f, fake)
+    d.workspace = None
+    assert lib.simsd_verify_attn(ctypes.byref(d), None) == 5
+    d.workspace = fake + 8                      # misaligned
+    d.workspace_bytes = 1 << 40
+    assert lib.simsd_verify_attn(ctypes.byref(d), None) == 5
+    d.workspace = fake
+    d.workspace_bytes = lib.simsd_verify_workspace_size(ctypes.byref(d)) - 1
+    assert lib.simsd_verify_attn(ctypes.byref(d), None) == 5
+
+
+def test_accept_errors(lib):
+    d = binding.AcceptDesc()
+    for k, v in dict(batch=4, vocab=1000, total_B=16, B_max=4, dtype=1).items():
+        setattr(d, k, v)
+    n = lib.simsd_accept_workspace_size(ctypes.byref(d))
+    assert n > 0 and n % 256 == 0
+    assert lib.simsd_accept(ctypes.byref(d), None) == 1
+    fake = 1 << 40
+    for f in ("target_logits", "draft_logits", "draft_tokens", "tau", "cu_B",
+              "uniforms", "n_accept", "token", "pos"):
+        setattr(d, f, fake)
+    assert lib.simsd_accept(ctypes.byref(d), None) == 5
+    for bad in (dict(B_max=0), dict(B_max=33), dict(total_B=17), dict(vocab=0),
+                dict(dtype=3), dict(batch=0)):
+        for k, v in bad.items():
+            setattr(d, k, v)
+        assert lib.simsd_accept_workspace_size(ctypes.byref(d)) == 0
+        assert lib.simsd_accept(ctypes.byref(d), None) in (2, 4)
+        for k, v in dict(batch=4, vocab=1000, total_B=16, B_max=4, dtype=1).items():
+            setattr(d, k, v)
+
+
+def test_append_errors(lib):
+    d = binding.AppendDesc()
+    assert lib.simsd_prompt_append(ctypes.byref(d), None) == 2
+    assert lib.simsd_prompt_append(None, None) == 1

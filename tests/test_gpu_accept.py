@@ -1,0 +1,140 @@
+"""GPU parity of simsd_accept (K4a-K4d) against the fp64 oracle.
+
+Decisions (accepted length, rejected position, drawn token) must match the
+oracle exactly on the same logits and uniforms, except for tie-zone
+decisions (see parity.py), which are only checked for validity.  Plus the
+special cases with a known answer, a Monte Carlo of 10^6 walks on V = 8,
+B = 3 against the exact outcome distribution, and vocabularies whose rows
+are not 16-byte multiples.
+"""
+import numpy as np
+import pytest
+import torch
+
+import parity
+import synth
+from oracle import exact
+from speculative_decoding_diffusion_gb300 import binding
+from speculative_decoding_diffusion_gb300.staging import DeviceWorkload
+
+pytestmark = pytest.mark.gpu
+
+
+def run_accept(w):
+    dw = DeviceWorkload(w, with_verify=False)
+    dw.accept()
+    torch.cuda.synchronize()
+    assert binding.read_status(dw.accept_ws) == 0
+    return (dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy())
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_configs_match_oracle(cfg):
+    w = synth.config(cfg)
+    n, tok, pos = run_accept(w)
+    ref = parity.oracle_accept(w)
+    ties = parity.check_accept(w, ref, n, tok, pos)
+    assert ties <= max(1, len(w.lens) // 50)
+
+
+def tiny_accept_spec(**kw):
+    base = dict(name="acc", batch=64, prompt=0, B=(1, 2, 5, 8, 32), Hq=1, Hkv=1, hd=64,
+                dtype="bf16", vocab=1003, logit_sd=2.0, noise_sd=(0.1, 3.0))
+    base.update(kw)
+    return synth.Spec(**base)
+
+
+@pytest.mark.parametrize("dtype,vocab", [("bf16", 1003), ("bf16", 4096 + 8), ("f32", 777),
+                                         ("f32", 2048), ("bf16", 9)])
+def test_odd_vocab_and_mixed_B(dtype, vocab):
+    w = synth.make(tiny_accept_spec(dtype=dtype, vocab=vocab), seed=vocab)
+    n, tok, pos = run_accept(w)
+    parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
+
+
+def test_p_equals_q_accepts_everything():
+    w = synth.make(tiny_accept_spec(), seed=1)
+    w.draft = w.target.copy()
+    w.uniforms = np.minimum(w.uniforms, np.float32(0.999))
+    n, tok, pos = run_accept(w)
+    assert np.array_equal(n, w.Bs) and (tok == -1).all() and (pos == -1).all()
+
+
+def test_zero_uniforms_accept_everything():
+    w = synth.make(tiny_accept_spec(), seed=2)
+    w.uniforms[:] = 0
+    n, tok, pos = run_accept(w)
+    assert np.array_equal(n, w.Bs)
+
+
+def test_certain_rejection_position():
+    # target logit of the draft token at slot k = -inf: the walk stops at
+    # step tau(k) (or earlier), and never draws the draft token there
+    w = synth.make(tiny_accept_spec(dtype="f32"), seed=3)
+    k_of = []
+    for b in range(len(w.lens)):
+        s0, B = int(w.cu_B[b]), int(w.Bs[b])
+        k = B // 2
+        w.target[s0 + k, w.draft_tokens[s0 + k]] = -np.inf
+        k_of.append(k)
+    n, tok, pos = run_accept(w)
+    ref = parity.oracle_accept(w)
+    parity.check_accept(w, ref, n, tok, pos)
+    for b, k in enumerate(k_of):
+        s0 = int(w.cu_B[b])
+        assert n[b] <= w.tau[s0 + k] - 1
+        if pos[b] == k:
+            assert tok[b] != w.draft_tokens[s0 + k]
+
+
+def test_walk_distribution_monte_carlo():
+    """10^6 walks on V = 8, B = 3 through the GPU kernels; chi-square of the
+    (n_accept, token) histogram against the exact enumeration."""
+    rng = np.random.default_rng(2024)
+    V, B, n = 8, 3, 1_000_000
+    lt = (rng.standard_normal((B, V)) * np.array([[0.5], [2.0], [1.0]])).astype(np.float32)
+    ld = (lt + rng.standard_normal((B, V)) * np.array([[0.3], [2.5], [1.0]])).astype(np.float32)
+    p = np.exp(lt - lt.max(1, keepdims=True)); p /= p.sum(1, keepdims=True)
+    q = np.exp(ld - ld.max(1, keepdims=True)); q /= q.sum(1, keepdims=True)
+    tau = np.array([2, 3, 1], np.int32)
+    xs = np.stack([rng.choice(V, size=n, p=q[k]) for k in range(B)], 1).astype(np.int32)
+    dev = "cuda"
+    target = torch.from_numpy(np.tile(lt, (n, 1))).to(dev)
+    draft = torch.from_numpy(np.tile(ld, (n, 1))).to(dev)
+    toks = torch.from_numpy(xs.reshape(-1)).to(dev)
+    taus = torch.from_numpy(np.tile(tau, n)).to(dev)
+    cu = torch.arange(0, B * n + 1, B, dtype=torch.int32, device=dev)
+    uni = torch.from_numpy(rng.random((n, B + 1), dtype=np.float32)).to(dev)
+    n_acc = torch.empty(n, dtype=torch.int32, device=dev)
+    tok = torch.empty_like(n_acc)
+    pos = torch.empty_like(n_acc)
+    # rows of this test: B * n = 3e6 > 65535 slots per launch, so split it
+    chunk = 20000
+    res_n, res_t, res_p = [], [], []
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        c = cu[s:e + 1] - cu[s]
+        args = (target[B * s:B * e], draft[B * s:B * e], toks[B * s:B * e], taus[B * s:B * e],
+                c, uni[s:e], n_acc[s:e], tok[s:e], pos[s:e], B * (e - s), B)
+        ws = torch.empty(binding.accept_workspace_size(*args), dtype=torch.uint8, device=dev)
+        binding.accept(*args[:9], ws, *args[9:])
+    torch.cuda.synchronize()
+    na, tk, ps = n_acc.cpu().numpy(), tok.cpu().numpy(), pos.cpu().numpy()
+    d = exact.outcome_distribution(p.astype(np.float64), q.astype(np.float64), tau)
+    keys = sorted(d)
+    idx = {k: i for i, k in enumerate(keys)}
+    obs = np.zeros(len(keys))
+    codes = na.astype(np.int64) * (V + 1) + (tk + 1)
+    uniq, cnt = np.unique(codes, return_counts=True)
+    order = [list(tau).index(t) for t in (1, 2, 3)]
+    for c_, k_ in zip(uniq, cnt):
+        key = (int(c_ // (V + 1)), int(c_ % (V + 1)) - 1)
+        assert key in idx, key
+        obs[idx[key]] += k_
+    assert np.array_equal(ps[na < B], np.array(order)[na[na < B]])
+    assert (ps[na == B] == -1).all()
+    expc = np.array([d[k] for k in keys]) * n
+    keep = expc > 5
+    chi2 = (((obs - expc) ** 2 / expc)[keep]).sum()
+    dof = keep.sum() - 1
+    assert chi2 < dof + 4.0 * np.sqrt(2.0 * dof) + 10, (chi2, dof)
