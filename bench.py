@@ -1,0 +1,401 @@
+"""Benchmark of the SimSD verification step on GB300.
+
+One step = the whole hot path over one batch: simsd_verify_attn (K1 RoPE-copy
++ paged append, K2 split-KV masked attention, K3 split merge) and
+simsd_accept (K4a-K4d rejection sampling along tau).  Default workload: the
+SDAR-8B-shaped verify step (16 sequences, prompt KV 1024, B = 4, 32/8 heads,
+head dim 128, vocabulary 151,936, bf16), seeded synthetic data.
+
+Prints ONE JSON line.  `value`: verified candidate tokens/s (sum of B over
+the batch / step time) with inputs resident in HBM, timed with CUDA events
+per step, L2 flushed (a 512 MB write) before every timed step.  `e2e`: the
+same metric through the C ABI with host buffers (pinned host -> device
+copies of the step's inputs and device -> host copies of its results inside
+the timed region).  `roofline`: the attention kernel K2 (the dominant one),
+algorithmic bytes per launch over its mean event-timed duration.
+`cpu_baseline`: the fp64 oracle on a bounded sample of the same workload,
+timed on this host's cores.
+
+--impl reference runs the oracle as the reference arm.  Multi-GPU (torchrun):
+each rank runs its own replica batch (sequences are independent; no
+collective on the data path), rank 0 prints the aggregate.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verified candidate tokens/s (attn+accept)"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", type=int, default=1,
+                    help="synthetic configuration index (1 = SDAR-8B verify step)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- algorithmic bytes
+def attn_bytes(w):
+    """K+V of every prompt key, the 2B new keys/values read once and written
+    once, q read once and the output written once."""
+    s = w.spec
+    es = 2 if s.dtype == "bf16" else 4
+    T = 2 * int(w.cu_B[-1])
+    kv_prompt = int(w.lens.sum()) * 2 * s.Hkv * s.hd * es
+    kv_new = T * 2 * s.Hkv * s.hd * es * 2
+    q_out = T * s.Hq * s.hd * es * 2
+    return kv_prompt + kv_new + q_out
+
+
+def k2_bytes(w):
+    """What K2 alone must move: every key/value of the cache range (prompt and
+    new) once, the rotated q once, the output once."""
+    s = w.spec
+    es = 2 if s.dtype == "bf16" else 4
+    T = 2 * int(w.cu_B[-1])
+    keys = int(w.lens.sum()) + T
+    return keys * 2 * s.Hkv * s.hd * es + T * s.Hq * s.hd * es * 2
+
+
+def accept_bytes(w):
+    es = 2 if w.spec.dtype == "bf16" else 4
+    return int(w.cu_B[-1]) * 2 * w.spec.vocab * es
+
+
+# ---------------------------------------------------------------- peaks / clocks
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+                if k in d and d[k]:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(mx)) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- ncu traffic record
+def recorded_traffic():
+    """DRAM bytes per K2 launch from the committed ncu summary, valid only
+    while the kernel source is unchanged (hash recorded with the counters)."""
+    src = os.path.join(ROOT, "speculative_decoding_diffusion_gb300", "csrc", "attn_bf16.cu")
+    rec = os.path.join(ROOT, "profiles", "k2_traffic.json")
+    if not os.path.exists(rec):
+        return None
+    try:
+        d = json.load(open(rec))
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if d.get("source_sha256") == h and d.get("workload") == "sdar8b-verify":
+            return float(d["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_step_sample(w, seconds, threads):
+    """Time the oracle (attention + acceptance) over whole batches of the
+    workload until `seconds` have passed; returns (tokens/s, sample text)."""
+    import oracle
+    import synth
+    q = synth.to_f64(w.q)
+    kp, vp = synth.to_f64(w.k_prompt), synth.to_f64(w.v_prompt)
+    if w.spec.raw_prompt_keys:   # the oracle takes rotated prompt keys
+        off = w.prompt_offsets
+        kp = np.concatenate([oracle.rope(kp[off[b]:off[b + 1]], np.arange(int(w.lens[b])),
+                                         w.spec.rope_base) for b in range(len(w.lens))])
+    kn, vn = synth.to_f64(w.k_new), synth.to_f64(w.v_new)
+    tl, dl = synth.to_f64(w.target), synth.to_f64(w.draft)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify_attn(w.lens, w.cu_B, q, kp, vp, kn, vn, w.tau, w.spec.rope_base,
+                           w.spec.sm_scale, n_threads=threads)
+        oracle.accept(w.cu_B, tl, dl, w.draft_tokens, w.tau, w.uniforms, n_threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    toks = reps * int(w.cu_B[-1])
+    return toks / el, el, reps
+
+
+def cpu_threads():
+    return len(os.sched_getaffinity(0))
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    from oracle import build as obuild
+    obuild.build()
+    w = synth.config(args.workload)
+    threads = cpu_threads()
+    per_step = []
+    per = max(1.0, min(8.0, 60.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        v, el, reps = oracle_step_sample(w, per, threads)
+        if i >= args.warmup:
+            per_step.append(el / reps)
+    ms = float(np.mean(per_step)) * 1e3
+    value = int(w.cu_B[-1]) / (ms / 1e3)
+    sample = ("whole batches of %s, repeated for >= %.1f s per step" % (w.spec.name, per))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, args):
+    s = w.spec
+    return {"workload": s.name, "global_batch": len(w.lens) * max(1, args.gpus),
+            "seq_len": int(w.lens.max()), "B": int(w.Bs.max()), "q_heads": s.Hq,
+            "kv_heads": s.Hkv, "head_dim": s.hd, "vocab": s.vocab,
+            "parallelism": "replicas x%d" % max(1, args.gpus),
+            "l2": "flushed (512 MB write) before every timed step"}
+
+
+# ---------------------------------------------------------------- GPU arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import synth
+    from speculative_decoding_diffusion_gb300 import build as libbuild
+    from speculative_decoding_diffusion_gb300 import binding
+    from speculative_decoding_diffusion_gb300.staging import DeviceWorkload
+    libbuild.build()
+    w = synth.config(args.workload)
+    dw = DeviceWorkload(w, device="cuda:%d" % local)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    vev = [ev() for _ in range(4)]
+    aev = [ev() for _ in range(5)]
+    for e in vev + aev:
+        e.record()       # create the underlying CUDA events
+    torch.cuda.synchronize()
+
+    def step(timed):
+        dw.verify(events=vev if timed else None)
+        dw.accept(events=aev if timed else None)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(False)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    step_ms, k_ms = [], {n: [] for n in ("K1", "K2", "K3", "K4a", "K4b", "K4c", "K4d")}
+    for _ in range(args.steps):
+        flush.zero_()
+        step(True)
+        torch.cuda.synchronize()
+        v = [vev[i].elapsed_time(vev[i + 1]) for i in range(3)]
+        a = [aev[i].elapsed_time(aev[i + 1]) for i in range(4)]
+        step_ms.append(vev[0].elapsed_time(aev[4]))
+        for n, t in zip(("K1", "K2", "K3"), v):
+            k_ms[n].append(t)
+        for n, t in zip(("K4a", "K4b", "K4c", "K4d"), a):
+            k_ms[n].append(t)
+    torch.cuda.synchronize()
+    dev_total_ms = float(np.sum(step_ms))
+    if dist:
+        t = torch.tensor([dev_total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_total_ms = float(t.item())
+
+    # ---- end to end through the C ABI with host buffers
+    def pin(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16
+                             else np.ascontiguousarray(a))
+        return (t.view(torch.bfloat16) if a.dtype == np.uint16 else t).pin_memory()
+
+    host_in = {
+        "q": pin(w.q), "k_new": pin(w.k_new), "v_new": pin(w.v_new),
+        "target": pin(w.target), "draft": pin(w.draft),
+        "draft_tokens": pin(w.draft_tokens.astype(np.int32)), "tau": pin(w.tau),
+        "uniforms": pin(w.uniforms), "lens": pin(w.lens), "cu_B": pin(w.cu_B),
+        "block_table": pin(w.block_table)}
+    dev_of = {"q": dw.q, "k_new": dw.k_new, "v_new": dw.v_new, "target": dw.target,
+              "draft": dw.draft, "draft_tokens": dw.draft_tokens, "tau": dw.tau,
+              "uniforms": dw.uniforms, "lens": dw.lens, "cu_B": dw.cu_B,
+              "block_table": dw.block_table}
+    host_out = {"out": torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory(),
+                "n_accept": torch.empty(len(w.lens), dtype=torch.int32).pin_memory(),
+                "token": torch.empty(len(w.lens), dtype=torch.int32).pin_memory(),
+                "pos": torch.empty(len(w.lens), dtype=torch.int32).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for k, h in host_in.items():
+            dev_of[k].copy_(h, non_blocking=True)
+        dw.verify()
+        dw.accept()
+        host_out["out"].copy_(dw.out, non_blocking=True)
+        host_out["n_accept"].copy_(dw.n_accept, non_blocking=True)
+        host_out["token"].copy_(dw.token, non_blocking=True)
+        host_out["pos"].copy_(dw.pos, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        flush.zero_()
+        e2e_step()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e_total = float(np.sum(e2e_ms))
+    if dist:
+        t = torch.tensor([e2e_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    clk = clocks.stop()
+    status = binding.read_status(dw.verify_ws) | binding.read_status(dw.accept_ws)
+
+    tokens_per_step = int(w.cu_B[-1]) * world
+    ms_per_step = dev_total_ms / args.steps
+    value = tokens_per_step / (ms_per_step / 1e3)
+    e2e_value = tokens_per_step / (e2e_total / args.steps / 1e3)
+    peak, peak_kind = hbm_peak()
+    k2_mean = float(np.mean(k_ms["K2"]))
+    achieved = k2_bytes(w) / (k2_mean / 1e3) / 1e9
+    traffic = recorded_traffic()
+    n_launch = 7 if any(t > 0 for t in k_ms["K3"]) else 6
+    kernels = {n: {"ms": float(np.mean(t))} for n, t in k_ms.items()}
+    attn_ms = sum(kernels[n]["ms"] for n in ("K1", "K2", "K3"))
+    acc_ms = sum(kernels[n]["ms"] for n in ("K4a", "K4b", "K4c", "K4d"))
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.spec.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": config_of(w, args),
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d * world,
+                    "d2h_bytes_per_step": d2h * world},
+            "gpu_launches": n_launch * args.steps,
+            "roofline": {"kernel": "K2 split-KV masked attention", "bound": "hbm",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "traffic": traffic,
+                         "algorithmic_bytes_per_launch": k2_bytes(w)},
+            "verify_attn_GBps": attn_bytes(w) / (attn_ms / 1e3) / 1e9,
+            "accept_GBps": accept_bytes(w) / (acc_ms / 1e3) / 1e9,
+            "kernels_ms": {n: round(k["ms"], 5) for n, k in kernels.items()},
+            "clocks": clk, "status_word": status}
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import build as obuild
+        obuild.build()
+        threads = cpu_threads()
+        v, el, reps = oracle_step_sample(w, args.cpu_seconds, threads)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": "%d whole batch(es) of %s (attention + acceptance), %.1f s"
+                                          % (reps, w.spec.name, el)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -142,6 +142,14 @@ typedef struct {
 size_t simsd_verify_workspace_size(const simsd_verify_desc *d);
 simsd_status simsd_verify_attn(const simsd_verify_desc *d, void *stream);
 
+/* Same as simsd_verify_attn, and records caller-created CUDA events (each a
+ * cudaEvent_t, or NULL to skip) on `stream` at the kernel boundaries:
+ * events[0] before K1, [1] after K1, [2] after K2, [3] after K3 (recorded
+ * even when K3 is not needed).  For per-kernel timing; the events are not
+ * waited on or destroyed. */
+simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream,
+                                     void *const events[4]);
+
 /* ------------------------------------------------------------------------
  * simsd_prompt_append -- K1 on plain positions: rotate n_b raw keys of
  * sequence b at positions start[b] .. start[b]+n_b-1 and write them (and
@@ -217,6 +225,12 @@ typedef struct {
 
 size_t simsd_accept_workspace_size(const simsd_accept_desc *d);
 simsd_status simsd_accept(const simsd_accept_desc *d, void *stream);
+
+/* Same as simsd_accept, recording events (cudaEvent_t or NULL) on `stream`:
+ * events[0] before K4a, [1] after K4a, [2] after K4b, [3] after K4c,
+ * [4] after K4d. */
+simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
+                                void *const events[5]);
 
 /* ------------------------------------------------------------------------
  * simsd_read_status -- synchronise `stream`, copy the device status word of

@@ -46,6 +46,8 @@ def _lib():
                                            P, P, P, I]
         lib.oracle_accept.argtypes = [I, I, P, P, P, P, P, P, I, P, P, P, P,
                                       P, I]
+        lib.oracle_residual.argtypes = [I, P, P, P]
+        lib.oracle_residual.restype = D
         _LIB = lib
     return _LIB
 
@@ -156,6 +158,15 @@ def accept(cu_B, target, draft, draft_tokens, tau, uniforms, n_threads=0):
         _p(am), _p(rm), int(n_threads)), "oracle_accept")
     return dict(n_accept=n_accept, token=token, pos=pos, accept_margin=am,
                 resample_margin=rm)
+
+
+def residual(target_row, draft_row):
+    """(r, S): r = max(0, p - q) of one slot in fp64 (p when empty)."""
+    t = _c(target_row, np.float64)
+    d = _c(draft_row, np.float64)
+    r = np.empty_like(t)
+    S = _lib().oracle_residual(len(t), _p(t), _p(d), _p(r))
+    return r, S
 
 
 def library_path():

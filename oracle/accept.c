@@ -32,6 +32,21 @@ static double log_sum_exp(const double *x, int V) {
   return m + log(s);
 }
 
+double oracle_residual(int V, const double *tl, const double *dl, double *r) {
+  const double lse_p = log_sum_exp(tl, V);
+  const double lse_q = log_sum_exp(dl, V);
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double pv = exp(tl[v] - lse_p), qv = exp(dl[v] - lse_q);
+    r[v] = pv > qv ? pv - qv : 0.0;
+    S += r[v];
+  }
+  if (S == 0.0) { /* p == q: the residual is empty, draw from p itself */
+    for (int v = 0; v < V; ++v) { r[v] = exp(tl[v] - lse_p); S += r[v]; }
+  }
+  return S;
+}
+
 static int accept_one(int B, int V, const double *target, const double *draft,
                       const int *draft_tokens, const int *tau, const float *u,
                       int *n_accept, int *token, int *pos,
@@ -66,15 +81,7 @@ static int accept_one(int B, int V, const double *target, const double *draft,
     /* first rejection: draw from norm(max(0, p - q)) with u[B] */
     *n_accept = t - 1;
     *pos = k;
-    double S = 0.0;
-    for (int v = 0; v < V; ++v) {
-      double pv = exp(tl[v] - lse_p), qv = exp(dl[v] - lse_q);
-      r[v] = pv > qv ? pv - qv : 0.0;
-      S += r[v];
-    }
-    if (S == 0.0) { /* p == q: the residual is empty, draw from p itself */
-      for (int v = 0; v < V; ++v) { r[v] = exp(tl[v] - lse_p); S += r[v]; }
-    }
+    const double S = oracle_residual(V, tl, dl, r);
     const double U = (double)u[B] * S;
     int chosen = -1;
     double below = 0.0, c = 0.0;

@@ -92,6 +92,11 @@ int oracle_verify_attn(int batch, const int *lens, const int *cu_B, int Hq,
                        const double *k_new, const double *v_new,
                        double *out, int n_threads);
 
+/* Residual of one slot: r[v] = max(0, p(v) - q(v)) with p, q the softmax of
+ * the target and draft logit rows (p itself when that is empty); returns
+ * S = sum r.  The acceptance walk draws its token from r / S. */
+double oracle_residual(int V, const double *target, const double *draft, double *r);
+
 /* Rejection-sampling acceptance along the temporal order, fp64.
  *   target, draft: [sum B_b][V] logits; row k of sequence b is response
  *                  position k (the logits read at D~_k).

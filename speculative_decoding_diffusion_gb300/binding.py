@@ -80,6 +80,10 @@ def lib():
         L.simsd_accept_workspace_size.argtypes = [ctypes.POINTER(AcceptDesc)]
         L.simsd_accept.restype = ctypes.c_int
         L.simsd_accept.argtypes = [ctypes.POINTER(AcceptDesc), _vp]
+        L.simsd_verify_attn_timed.restype = ctypes.c_int
+        L.simsd_verify_attn_timed.argtypes = [ctypes.POINTER(VerifyDesc), _vp, ctypes.POINTER(_vp)]
+        L.simsd_accept_timed.restype = ctypes.c_int
+        L.simsd_accept_timed.argtypes = [ctypes.POINTER(AcceptDesc), _vp, ctypes.POINTER(_vp)]
         L.simsd_read_status.restype = ctypes.c_int
         L.simsd_read_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
         _LIB = L
@@ -158,12 +162,25 @@ def verify_workspace_size(q, k_cache, v_cache, block_table, k_new, v_new, tau,
     return int(n)
 
 
+def _events(evs, n):
+    arr = (_vp * n)()
+    for i, e in enumerate(evs):
+        arr[i] = None if e is None else e.cuda_event
+    return arr
+
+
 def verify_attn(q, k_cache, v_cache, block_table, k_new, v_new, tau, lens, cu_B,
-                out, workspace, total_B, B_max, rope_base, sm_scale, stream=None):
-    """simsd_verify_attn on the current (or given) torch stream."""
+                out, workspace, total_B, B_max, rope_base, sm_scale, stream=None,
+                events=None):
+    """simsd_verify_attn on the current (or given) torch stream.  events:
+    optional 4 recorded torch.cuda.Event objects (see simsd_verify_attn_timed)."""
     d = _verify_desc(q, k_cache, v_cache, block_table, k_new, v_new, tau, lens,
                      cu_B, out, total_B, B_max, rope_base, sm_scale, workspace)
-    _check(lib().simsd_verify_attn(ctypes.byref(d), _stream(stream)), "simsd_verify_attn")
+    if events is None:
+        _check(lib().simsd_verify_attn(ctypes.byref(d), _stream(stream)), "simsd_verify_attn")
+    else:
+        _check(lib().simsd_verify_attn_timed(ctypes.byref(d), _stream(stream), _events(events, 4)),
+               "simsd_verify_attn_timed")
 
 
 def prompt_append(k, v, start, cu_n, k_cache, v_cache, block_table, rope_base,
@@ -212,10 +229,15 @@ def accept_workspace_size(target, draft, draft_tokens, tau, cu_B, uniforms, n_ac
 
 
 def accept(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token, pos,
-           workspace, total_B, B_max, stream=None):
+           workspace, total_B, B_max, stream=None, events=None):
+    """simsd_accept; events: optional 5 recorded torch.cuda.Event objects."""
     d = _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
                      pos, total_B, B_max, workspace)
-    _check(lib().simsd_accept(ctypes.byref(d), _stream(stream)), "simsd_accept")
+    if events is None:
+        _check(lib().simsd_accept(ctypes.byref(d), _stream(stream)), "simsd_accept")
+    else:
+        _check(lib().simsd_accept_timed(ctypes.byref(d), _stream(stream), _events(events, 5)),
+               "simsd_accept_timed")
 
 
 def read_status(workspace, stream=None):

@@ -4,22 +4,28 @@
 // rejection sampling along the draft-induced temporal order; the longest
 // accepted prefix is committed.  For sequence b, step t = 1..B tests the
 // slot k = tau^-1(t) with draft token x: p = softmax(target row k),
-// q = softmax(draft row k); accept iff u[t-1] * q(x) < p(x).  At the first
-// rejection a token is drawn from max(0, p - q) normalised (p itself when
-// that is empty) by inverse CDF with u[B].  All softmax math is fp32 in the
-// log2 domain.
+// q = softmax(draft row k); accept iff u[t-1] * q(x) < p(x) (fp32).  At the
+// first rejection a token is drawn from max(0, p - q) normalised (p itself
+// when that is empty) by inverse CDF with u[B].
+//
+// Numerics: every exponential is taken relative to a row maximum M in logit
+// units, 2^((x - M) log2 e): x - M is exact for bf16 logits, so only the
+// product and exp2f round (~2e-7 relative on the entries that carry mass).
+// Cross-thread sums, the normaliser and every running CDF are fp64 (a few
+// hundred additions per CTA); per-thread partial sums of <= 16 entries stay
+// fp32.  The residual CDF is then within ~1e-6 (absolute, probability mass)
+// of the exact one.
 //
 // Four launches, all sized to the data rather than to the batch:
-//   K4a  grid (vocab chunk, slot): running max and sum of 2^(x log2 e) of
-//        the target and draft rows of every slot (the dominant HBM stream);
-//   K4b  one CTA per sequence: merge chunk partials into log-sum-exps, form
-//        p(x), q(x), walk the steps in tau order;
-//   K4c  grid (residual chunk, sequence): per-chunk sums of the residual
-//        max(0, p - q) (and of p) of the rejected slot only;
+//   K4a  grid (vocab chunk, slot): max and sum of exponentials of the target
+//        and draft rows of every slot (the dominant HBM stream);
+//   K4b  one CTA per sequence: merge chunk partials, p(x), q(x), the walk;
+//   K4c  grid (residual chunk, sequence): per-chunk sums of max(0, p - q)
+//        (and of p) of the rejected slot only;
 //   K4d  one CTA per sequence with a rejection: prefix over chunk sums,
 //        inverse CDF inside the selected chunk.  Within a chunk the running
-//        sum is built so that it never decreases (thread totals prefixed
-//        sequentially), hence the chosen token always has positive mass.
+//        sum never decreases (thread totals prefixed sequentially), so the
+//        chosen token always has positive mass.
 #include "common.cuh"
 #include "internal.h"
 
@@ -28,9 +34,17 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kLseChunk = 4096;   // K4a vocabulary chunk
-constexpr int kResPer = 8;        // residual elements per thread
+constexpr int kResPer = 8;        // residual entries per thread
 constexpr int kResChunk = kThreads * kResPer;
 constexpr float kLog2e = 1.4426950408889634f;
+
+// Per sequence, after the walk: rejected slot (-1: none) and the row maxima
+// and normalisers of that slot.
+struct WalkState {
+  int rej;
+  float Mt, Md;
+  double St, Sd;
+};
 
 struct AcceptWs {
   size_t off_status, off_lse, off_state, off_res, total;
@@ -44,8 +58,8 @@ AcceptWs accept_ws(const simsd_accept_desc *d) {
   size_t off = 0;
   w.off_status = off; off = align_up(off + sizeof(uint32_t), kAlign);
   w.off_lse = off;    off = align_up(off + (size_t)d->total_B * w.lse_chunks * sizeof(float4), kAlign);
-  w.off_state = off;  off = align_up(off + (size_t)d->batch * sizeof(float4), kAlign);
-  w.off_res = off;    off = align_up(off + (size_t)d->batch * w.res_chunks * sizeof(float2), kAlign);
+  w.off_state = off;  off = align_up(off + (size_t)d->batch * sizeof(WalkState), kAlign);
+  w.off_res = off;    off = align_up(off + (size_t)d->batch * w.res_chunks * sizeof(double2), kAlign);
   w.total = off;
   return w;
 }
@@ -60,19 +74,27 @@ struct AcceptArgs {
   int32_t *n_accept;
   int32_t *token;
   int32_t *pos;
-  float4 *lse_part;   // [total_B][lse_chunks]: (m_t, s_t, m_d, s_d), log2 domain
-  float4 *state;      // [batch]: (rejected slot, lse2_t, lse2_d, -)
-  float2 *res_part;   // [batch][res_chunks]: (sum r, sum p)
+  float4 *lse_part;     // [total_B][lse_chunks]: (M_t, s_t, M_d, s_d)
+  WalkState *state;     // [batch]
+  double2 *res_part;    // [batch][res_chunks]: (sum r, sum p)
   uint32_t *status;
   int batch, vocab, B_max, lse_chunks, res_chunks, vec_ok;
 };
 
-// (m, s) with s = sum 2^(x - m): merge two partial states.
+// (M, s) with s = sum 2^((x - M) log2 e): merge two partial states.
 __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
   const float mm = fmaxf(m, m2);
   if (mm == -INFINITY) { m = mm; s = 0.f; return; }
-  s = s * exp2f(m - mm) + s2 * exp2f(m2 - mm);
+  s = s * exp2f((m - mm) * kLog2e) + s2 * exp2f((m2 - mm) * kLog2e);
   m = mm;
+}
+
+__device__ __forceinline__ void accum(float &m, float &s, const float *x, int n) {
+  float mx = -INFINITY;
+  for (int i = 0; i < n; ++i) mx = fmaxf(mx, x[i]);
+  if (mx > m) { s *= exp2f((m - mx) * kLog2e); m = mx; }
+  if (m == -INFINITY) return;
+  for (int i = 0; i < n; ++i) s += exp2f((x[i] - m) * kLog2e);
 }
 
 template <typename T> struct Ld;
@@ -100,7 +122,8 @@ template <> struct Ld<__nv_bfloat16> {
   }
 };
 
-// Block-wide merge of (m, s) pairs; result valid in thread 0.
+// Block-wide (M, s) merge: warps in fp32, across warps in fp64 relative to
+// the block maximum.  Result in thread 0.
 __device__ __forceinline__ void block_lse(float &m, float &s, float2 *scratch) {
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) {
@@ -112,7 +135,14 @@ __device__ __forceinline__ void block_lse(float &m, float &s, float2 *scratch) {
   if (lane == 0) scratch[warp] = make_float2(m, s);
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int i = 1; i < kThreads / 32; ++i) lse_merge(m, s, scratch[i].x, scratch[i].y);
+    float M = -INFINITY;
+    for (int i = 0; i < kThreads / 32; ++i) M = fmaxf(M, scratch[i].x);
+    double S = 0.0;
+    if (M != -INFINITY)
+      for (int i = 0; i < kThreads / 32; ++i)
+        S += (double)scratch[i].y * (double)exp2f((scratch[i].x - M) * kLog2e);
+    m = M;
+    s = (float)S;
   }
   __syncthreads();
 }
@@ -130,13 +160,7 @@ lse_kernel(const __grid_constant__ AcceptArgs a) {
   const T *dr = (const T *)a.draft + row;
   float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
   constexpr int N = Ld<T>::N;
-  auto accum = [](float &m, float &s, const float *x, int n) {
-    float mx = -INFINITY;
-    for (int i = 0; i < n; ++i) mx = fmaxf(mx, x[i] * kLog2e);
-    if (mx > m) { s *= exp2f(m - mx); m = mx; }
-    if (m == -INFINITY) return;
-    for (int i = 0; i < n; ++i) s += exp2f(x[i] * kLog2e - m);
-  };
+  int tail0 = v0;
   if (a.vec_ok) {
     for (int v = v0 + threadIdx.x * N; v + N <= v1; v += kThreads * N) {
       float xt[N], xd[N];
@@ -145,66 +169,73 @@ lse_kernel(const __grid_constant__ AcceptArgs a) {
       accum(mt, st, xt, N);
       accum(md, sd, xd, N);
     }
-    // ragged end of the vocabulary (only the last chunk can have one)
-    const int tail0 = v0 + ((v1 - v0) / N) * N;
-    for (int v = tail0 + threadIdx.x; v < v1; v += kThreads) {
-      float xt = Ld<T>::one(tr + v), xd = Ld<T>::one(dr + v);
-      accum(mt, st, &xt, 1);
-      accum(md, sd, &xd, 1);
-    }
-  } else {
-    for (int v = v0 + threadIdx.x; v < v1; v += kThreads) {
-      float xt = Ld<T>::one(tr + v), xd = Ld<T>::one(dr + v);
-      accum(mt, st, &xt, 1);
-      accum(md, sd, &xd, 1);
-    }
+    tail0 = v0 + ((v1 - v0) / N) * N;   // ragged end (last chunk only)
+  }
+  for (int v = tail0 + threadIdx.x; v < v1; v += kThreads) {
+    float xt = Ld<T>::one(tr + v), xd = Ld<T>::one(dr + v);
+    accum(mt, st, &xt, 1);
+    accum(md, sd, &xd, 1);
   }
   block_lse(mt, st, scratch[0]);
   block_lse(md, sd, scratch[1]);
   if (threadIdx.x == 0) a.lse_part[(long)slot * a.lse_chunks + chunk] = make_float4(mt, st, md, sd);
 }
 
+// Row maximum and normaliser of one slot from its chunk partials (one warp).
+__device__ __forceinline__ void row_norm(const float4 *pp, int chunks, int lane,
+                                         float &Mt, double &St, float &Md, double &Sd) {
+  float mt = -INFINITY, md = -INFINITY;
+  for (int c = lane; c < chunks; c += 32) { mt = fmaxf(mt, pp[c].x); md = fmaxf(md, pp[c].z); }
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1) {
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, w));
+    md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, w));
+  }
+  double st = 0.0, sd = 0.0;
+  for (int c = lane; c < chunks; c += 32) {
+    const float4 v = pp[c];
+    if (v.y > 0.f) st += (double)v.y * (double)exp2f((v.x - mt) * kLog2e);
+    if (v.w > 0.f) sd += (double)v.w * (double)exp2f((v.z - md) * kLog2e);
+  }
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1) {
+    st += __shfl_xor_sync(0xffffffffu, st, w);
+    sd += __shfl_xor_sync(0xffffffffu, sd, w);
+  }
+  Mt = mt; St = st; Md = md; Sd = sd;
+}
+
 // ---------------------------------------------------------------- K4b
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 walk_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ float px_s[kMaxB], qx_s[kMaxB], lt_s[kMaxB], ld_s[kMaxB];
+  __shared__ float px_s[kMaxB], qx_s[kMaxB], mt_s[kMaxB], md_s[kMaxB];
+  __shared__ double st_s[kMaxB], sd_s[kMaxB];
   const int b = blockIdx.x;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
   if (B < 1 || B > kMaxB) {                  // malformed sequence: no walk
     if (threadIdx.x == 0) {
       a.n_accept[b] = 0; a.token[b] = -1; a.pos[b] = -1;
-      a.state[b] = make_float4(__int_as_float(-1), 0.f, 0.f, 0.f);
+      a.state[b] = WalkState{-1, 0.f, 0.f, 0.0, 0.0};
       raise_status(a.status, kStatusBadInput);
     }
     return;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int k = warp; k < B; k += kThreads / 32) {
-    float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
-    const float4 *pp = a.lse_part + (long)(c0 + k) * a.lse_chunks;
-    for (int c = lane; c < a.lse_chunks; c += 32) {
-      const float4 v = pp[c];
-      lse_merge(mt, st, v.x, v.y);
-      lse_merge(md, sd, v.z, v.w);
-    }
-#pragma unroll
-    for (int w = 16; w > 0; w >>= 1) {
-      lse_merge(mt, st, __shfl_xor_sync(0xffffffffu, mt, w), __shfl_xor_sync(0xffffffffu, st, w));
-      lse_merge(md, sd, __shfl_xor_sync(0xffffffffu, md, w), __shfl_xor_sync(0xffffffffu, sd, w));
-    }
+    float Mt, Md;
+    double St, Sd;
+    row_norm(a.lse_part + (long)(c0 + k) * a.lse_chunks, a.lse_chunks, lane, Mt, St, Md, Sd);
     if (lane == 0) {
-      const float lse_t = mt + log2f(st), lse_d = md + log2f(sd);
       const long row = (long)(c0 + k) * a.vocab;
       int x = __ldg(a.draft_tokens + c0 + k);
       if (x < 0 || x >= a.vocab) { raise_status(a.status, kStatusBadInput); x = 0; }
       const float tx = Ld<T>::one((const T *)a.target + row + x);
       const float dx = Ld<T>::one((const T *)a.draft + row + x);
-      px_s[k] = exp2f(tx * kLog2e - lse_t);
-      qx_s[k] = exp2f(dx * kLog2e - lse_d);
-      lt_s[k] = lse_t;
-      ld_s[k] = lse_d;
+      px_s[k] = (float)((double)exp2f((tx - Mt) * kLog2e) / St);
+      qx_s[k] = (float)((double)exp2f((dx - Md) * kLog2e) / Sd);
+      mt_s[k] = Mt; md_s[k] = Md; st_s[k] = St; sd_s[k] = Sd;
     }
   }
   __syncthreads();
@@ -223,17 +254,20 @@ walk_kernel(const __grid_constant__ AcceptArgs a) {
     }
     a.n_accept[b] = n;
     a.pos[b] = rej;
-    if (rej < 0) a.token[b] = -1;
-    a.state[b] = make_float4(__int_as_float(rej), rej >= 0 ? lt_s[rej] : 0.f,
-                             rej >= 0 ? ld_s[rej] : 0.f, 0.f);
+    if (rej < 0) {
+      a.token[b] = -1;
+      a.state[b] = WalkState{-1, 0.f, 0.f, 0.0, 0.0};
+    } else {
+      a.state[b] = WalkState{rej, mt_s[rej], md_s[rej], st_s[rej], sd_s[rej]};
+    }
   }
 }
 
-// Residual mass and target mass of one vocabulary entry.
-__device__ __forceinline__ void res_pair(float t, float d, float lse_t, float lse_d,
-                                         float &r, float &p) {
-  p = exp2f(t * kLog2e - lse_t);
-  const float q = exp2f(d * kLog2e - lse_d);
+// Residual mass r = max(0, p - q) and target mass p of one entry.
+__device__ __forceinline__ void res_pair(float t, float d, const WalkState &st,
+                                         float inv_st, float inv_sd, float &r, float &p) {
+  p = exp2f((t - st.Mt) * kLog2e) * inv_st;
+  const float q = exp2f((d - st.Md) * kLog2e) * inv_sd;
   r = fmaxf(p - q, 0.f);
 }
 
@@ -241,12 +275,12 @@ __device__ __forceinline__ void res_pair(float t, float d, float lse_t, float ls
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 residual_sum_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ float2 scratch[kThreads / 32];
+  __shared__ double2 scratch[kThreads / 32];
   const int chunk = blockIdx.x, b = blockIdx.y;
-  const float4 st = a.state[b];
-  const int rej = __float_as_int(st.x);
-  if (rej < 0) return;
-  const long row = (long)(__ldg(a.cu_B + b) + rej) * a.vocab;
+  const WalkState st = a.state[b];
+  if (st.rej < 0) return;
+  const float inv_st = (float)(1.0 / st.St), inv_sd = (float)(1.0 / st.Sd);
+  const long row = (long)(__ldg(a.cu_B + b) + st.rej) * a.vocab;
   const T *tr = (const T *)a.target + row;
   const T *dr = (const T *)a.draft + row;
   const int v0 = chunk * kResChunk + threadIdx.x * kResPer;
@@ -255,19 +289,20 @@ residual_sum_kernel(const __grid_constant__ AcceptArgs a) {
     const int v = v0 + i;
     if (v >= a.vocab) break;
     float r, p;
-    res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st.y, st.z, r, p);
+    res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st, inv_st, inv_sd, r, p);
     sr += r;
     sp += p;
   }
+  double dr_ = sr, dp = sp;
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) {
-    sr += __shfl_xor_sync(0xffffffffu, sr, w);
-    sp += __shfl_xor_sync(0xffffffffu, sp, w);
+    dr_ += __shfl_xor_sync(0xffffffffu, dr_, w);
+    dp += __shfl_xor_sync(0xffffffffu, dp, w);
   }
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = make_float2(sr, sp);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = make_double2(dr_, dp);
   __syncthreads();
   if (threadIdx.x == 0) {
-    float2 tot = scratch[0];
+    double2 tot = scratch[0];
     for (int i = 1; i < kThreads / 32; ++i) { tot.x += scratch[i].x; tot.y += scratch[i].y; }
     a.res_part[(long)b * a.res_chunks + chunk] = tot;
   }
@@ -277,37 +312,32 @@ residual_sum_kernel(const __grid_constant__ AcceptArgs a) {
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 residual_draw_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ float wsum[kThreads];
-  __shared__ int sel_chunk;
-  __shared__ float base_s, U_s;
-  __shared__ int best_s, last_pos_s;
+  __shared__ double wsum[kThreads];
+  __shared__ int sel_chunk, use_p_s, best_s, last_pos_s;
+  __shared__ double base_s, U_s;
   const int b = blockIdx.x;
-  const float4 st = a.state[b];
-  const int rej = __float_as_int(st.x);
-  if (rej < 0) return;
+  const WalkState st = a.state[b];
+  if (st.rej < 0) return;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
-  const float2 *rp = a.res_part + (long)b * a.res_chunks;
-  // empty residual (p == q): draw from p itself
-  __shared__ int use_p_s;
+  const double2 *rp = a.res_part + (long)b * a.res_chunks;
   if (threadIdx.x == 0) {
-    float S = 0.f;
+    double S = 0.0;
     for (int c = 0; c < a.res_chunks; ++c) S += rp[c].x;
-    const int use_p = !(S > 0.f);
-    float tot = 0.f;
+    const int use_p = !(S > 0.0);            // empty residual: draw from p
+    double tot = 0.0;
     if (use_p) for (int c = 0; c < a.res_chunks; ++c) tot += rp[c].y;
     else tot = S;
-    const float U = __ldg(a.uniforms + (long)b * (a.B_max + 1) + B) * tot;
-    // chunk c with T[c] <= U < T[c+1], T the sequential prefix of chunk sums;
-    // if rounding leaves U at or past the total, the last non-empty chunk
-    float T0 = 0.f;
+    const double U = (double)__ldg(a.uniforms + (long)b * (a.B_max + 1) + B) * tot;
+    // chunk c with T[c] <= U < T[c+1] (T: running sum of chunk masses); if
+    // rounding leaves U at or past the total, the last non-empty chunk
+    double T0 = 0.0, sel_base = 0.0, last_base = 0.0;
     int sel = -1, last_nz = 0;
-    float sel_base = 0.f, last_base = 0.f;
     for (int c = 0; c < a.res_chunks; ++c) {
-      const float m = use_p ? rp[c].y : rp[c].x;
-      const float T1 = T0 + m;
-      if (m > 0.f) { last_nz = c; last_base = T0; }
-      if (sel < 0 && U < T1 && m > 0.f) { sel = c; sel_base = T0; }
+      const double m = use_p ? rp[c].y : rp[c].x;
+      const double T1 = T0 + m;
+      if (m > 0.0) { last_nz = c; last_base = T0; }
+      if (sel < 0 && U < T1 && m > 0.0) { sel = c; sel_base = T0; }
       T0 = T1;
     }
     if (sel < 0) { sel = last_nz; sel_base = last_base; }
@@ -320,7 +350,8 @@ residual_draw_kernel(const __grid_constant__ AcceptArgs a) {
   }
   __syncthreads();
   const int use_p = use_p_s;
-  const long row = (long)(c0 + rej) * a.vocab;
+  const float inv_st = (float)(1.0 / st.St), inv_sd = (float)(1.0 / st.Sd);
+  const long row = (long)(c0 + st.rej) * a.vocab;
   const T *tr = (const T *)a.target + row;
   const T *dr = (const T *)a.draft + row;
   const int v0 = sel_chunk * kResChunk + threadIdx.x * kResPer;
@@ -330,19 +361,18 @@ residual_draw_kernel(const __grid_constant__ AcceptArgs a) {
   for (int i = 0; i < kResPer; ++i) {
     const int v = v0 + i;
     float r = 0.f, p = 0.f;
-    if (v < a.vocab) res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st.y, st.z, r, p);
+    if (v < a.vocab) res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st, inv_st, inv_sd, r, p);
     m[i] = use_p ? p : r;
     local += m[i];
   }
-  wsum[threadIdx.x] = local;
+  wsum[threadIdx.x] = (double)local;
   __syncthreads();
   if (threadIdx.x == 0) {   // exclusive prefix of thread totals, in order
-    float run = 0.f;
-    for (int i = 0; i < kThreads; ++i) { const float x = wsum[i]; wsum[i] = run; run += x; }
+    double run = 0.0;
+    for (int i = 0; i < kThreads; ++i) { const double x = wsum[i]; wsum[i] = run; run += x; }
   }
   __syncthreads();
-  const float U = U_s, base = base_s;
-  const float excl = wsum[threadIdx.x];
+  const double U = U_s, base = base_s + wsum[threadIdx.x];
   float lp = 0.f;
   int first = 0x7fffffff, last_pos = -1;
 #pragma unroll
@@ -350,7 +380,7 @@ residual_draw_kernel(const __grid_constant__ AcceptArgs a) {
     lp += m[i];
     if (m[i] > 0.f) {
       last_pos = v0 + i;
-      if (first == 0x7fffffff && base + (excl + lp) > U) first = v0 + i;
+      if (first == 0x7fffffff && base + (double)lp > U) first = v0 + i;
     }
   }
   if (first != 0x7fffffff) atomicMin(&best_s, first);
@@ -359,12 +389,22 @@ residual_draw_kernel(const __grid_constant__ AcceptArgs a) {
   if (threadIdx.x == 0) a.token[b] = best_s != 0x7fffffff ? best_s : last_pos_s;
 }
 
+void mark(void *const *events, int i, cudaStream_t stream) {
+  if (events != nullptr && events[i] != nullptr) cudaEventRecord((cudaEvent_t)events[i], stream);
+}
+
 template <typename T>
-cudaError_t launch_all(const AcceptArgs &a, int total_B, cudaStream_t stream) {
+cudaError_t launch_all(const AcceptArgs &a, int total_B, cudaStream_t stream,
+                       void *const *events) {
+  mark(events, 0, stream);
   lse_kernel<T><<<dim3(a.lse_chunks, total_B), kThreads, 0, stream>>>(a);
+  mark(events, 1, stream);
   walk_kernel<T><<<a.batch, kThreads, 0, stream>>>(a);
+  mark(events, 2, stream);
   residual_sum_kernel<T><<<dim3(a.res_chunks, a.batch), kThreads, 0, stream>>>(a);
+  mark(events, 3, stream);
   residual_draw_kernel<T><<<a.batch, kThreads, 0, stream>>>(a);
+  mark(events, 4, stream);
   return cudaGetLastError();
 }
 
@@ -392,6 +432,11 @@ size_t simsd_accept_workspace_size(const simsd_accept_desc *d) {
 }
 
 simsd_status simsd_accept(const simsd_accept_desc *d, void *stream_ptr) {
+  return simsd_accept_timed(d, stream_ptr, nullptr);
+}
+
+simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream_ptr,
+                                void *const events[5]) {
   simsd_status st = accept_check(d);
   if (st != SIMSD_OK) return st;
   if (!d->target_logits || !d->draft_logits || !d->draft_tokens || !d->tau ||
@@ -416,8 +461,8 @@ simsd_status simsd_accept(const simsd_accept_desc *d, void *stream_ptr) {
   a.token = d->token;
   a.pos = d->pos;
   a.lse_part = (float4 *)(ws + w.off_lse);
-  a.state = (float4 *)(ws + w.off_state);
-  a.res_part = (float2 *)(ws + w.off_res);
+  a.state = (WalkState *)(ws + w.off_state);
+  a.res_part = (double2 *)(ws + w.off_res);
   a.status = (uint32_t *)(ws + w.off_status);
   a.batch = d->batch;
   a.vocab = d->vocab;
@@ -428,8 +473,9 @@ simsd_status simsd_accept(const simsd_accept_desc *d, void *stream_ptr) {
   a.vec_ok = ((size_t)d->vocab * es) % 16 == 0 &&
              ((uintptr_t)d->target_logits % 16) == 0 &&
              ((uintptr_t)d->draft_logits % 16) == 0;
-  cudaError_t e = d->dtype == SIMSD_BF16 ? launch_all<__nv_bfloat16>(a, d->total_B, stream)
-                                         : launch_all<float>(a, d->total_B, stream);
+  cudaError_t e = d->dtype == SIMSD_BF16
+                      ? launch_all<__nv_bfloat16>(a, d->total_B, stream, events)
+                      : launch_all<float>(a, d->total_B, stream, events);
   return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
 }
 

@@ -158,6 +158,16 @@ size_t simsd_verify_workspace_size(const simsd_verify_desc *d) {
 }
 
 simsd_status simsd_verify_attn(const simsd_verify_desc *d, void *stream_ptr) {
+  return simsd_verify_attn_timed(d, stream_ptr, nullptr);
+}
+
+static bool mark(void *const *events, int i, cudaStream_t stream) {
+  if (events == nullptr || events[i] == nullptr) return true;
+  return cudaEventRecord((cudaEvent_t)events[i], stream) == cudaSuccess;
+}
+
+simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_ptr,
+                                     void *const events[4]) {
   VerifyPlan p;
   simsd_status st = verify_plan(d, &p);
   if (st != SIMSD_OK) return st;
@@ -174,7 +184,9 @@ simsd_status simsd_verify_attn(const simsd_verify_desc *d, void *stream_ptr) {
   int32_t *tok_seq = (int32_t *)(ws + p.off_tokseq);
   if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess)
     return SIMSD_ERR_CUDA;
-  if (launch_rope_verify(d, p, q_rot, tok_seq, status, stream) != cudaSuccess)
+  if (!mark(events, 0, stream) ||
+      launch_rope_verify(d, p, q_rot, tok_seq, status, stream) != cudaSuccess ||
+      !mark(events, 1, stream))
     return SIMSD_ERR_CUDA;
   AttnParams a;
   memset(&a, 0, sizeof(a));
@@ -200,10 +212,10 @@ simsd_status simsd_verify_attn(const simsd_verify_desc *d, void *stream_ptr) {
   a.sm_scale = d->sm_scale;
   cudaError_t e = d->dtype == SIMSD_BF16 ? launch_attn_bf16(d, p, a, stream)
                                          : launch_attn_f32(d, p, a, stream);
-  if (e != cudaSuccess) return SIMSD_ERR_CUDA;
+  if (e != cudaSuccess || !mark(events, 2, stream)) return SIMSD_ERR_CUDA;
   if (p.n_splits > 1 && launch_combine(d, p, a, tok_seq, stream) != cudaSuccess)
     return SIMSD_ERR_CUDA;
-  return SIMSD_OK;
+  return mark(events, 3, stream) ? SIMSD_OK : SIMSD_ERR_CUDA;
 }
 
 simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream_ptr) {

@@ -96,17 +96,17 @@ class DeviceWorkload:
                 self.v_new, self.tau, self.lens, self.cu_B, self.out, self.total_B,
                 self.B_max, self.rope_base, self.sm_scale)
 
-    def verify(self, stream=None):
+    def verify(self, stream=None, events=None):
         (q, kc, vc, bt, kn, vn, tau, lens, cu, out, tb, bm, rb, sc) = self._verify_args()
         binding.verify_attn(q, kc, vc, bt, kn, vn, tau, lens, cu, out, self.verify_ws,
-                            tb, bm, rb, sc, stream=stream)
+                            tb, bm, rb, sc, stream=stream, events=events)
 
     def _accept_args(self):
         return (self.target, self.draft, self.draft_tokens, self.tau, self.cu_B,
                 self.uniforms, self.n_accept, self.token, self.pos, self.total_B,
                 self.B_max)
 
-    def accept(self, stream=None):
+    def accept(self, stream=None, events=None):
         (t, d, x, tau, cu, u, n, tok, pos, tb, bm) = self._accept_args()
         binding.accept(t, d, x, tau, cu, u, n, tok, pos, self.accept_ws, tb, bm,
-                       stream=stream)
+                       stream=stream, events=events)

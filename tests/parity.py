@@ -4,11 +4,19 @@ workload and the comparison rules.
 Tolerances (from the stated targets): attention rows agree within a max
 relative error of 2e-2 with bf16 inputs/outputs and 1e-4 with fp32, where a
 row's error is max|o_gpu - o_ref| / max|o_ref| over its head dimension.
-Acceptance decisions are compared exactly except in the tie zone: a step
-whose oracle margin |u q(x) - p(x)| / p(x) is below 1e-5, or a residual draw
-whose inverse-CDF threshold lies within 1e-5 (relative to the residual
-mass) of a bin edge, may flip under fp32 rounding; there the GPU result is
-only checked for validity.
+Acceptance decisions are compared exactly except in the tie zone, where
+fp32 rounding on the GPU may legitimately flip them:
+  - a step whose oracle margin |u q(x) - p(x)| / p(x) is below TIE_ACCEPT
+    (the GPU's p(x), q(x) carry up to ~1.5e-6 relative error: exponent
+    argument rounding up to half an ulp of |x - max| log2 e <= ~40, exp2f's
+    2 ulp, the normaliser);
+  - a residual draw whose threshold u*S lies within TIE_RESIDUAL (absolute
+    probability mass) of a bin edge of the oracle's fp64 CDF (each residual
+    entry carries ~3e-7 relative error weighted by mass, so the GPU's CDF is
+    within ~6e-7 of the exact one; fp64 sums add nothing comparable).
+Inside the tie zone the GPU's result must still be valid: an accepted length
+consistent with the steps decided outside the zone, and a drawn token with
+positive residual mass whose CDF bin lies within TIE_RESIDUAL of u*S.
 """
 import numpy as np
 
@@ -16,7 +24,8 @@ import oracle
 import synth
 
 TOL = {"bf16": 2e-2, "f32": 1e-4}
-TIE = 1e-5
+TIE_ACCEPT = 5e-6
+TIE_RESIDUAL = 2e-6
 
 
 def prompt_keys_f64(w, b):
@@ -73,26 +82,38 @@ def oracle_accept(w):
 
 def check_accept(w, ref, n_accept, token, pos):
     """Exact agreement outside the tie zone; validity inside it.
-    Returns the number of sequences decided in the tie zone."""
-    ties = 0
-    am, rm = ref["accept_margin"], ref["resample_margin"]
+    Returns (accept-step ties, residual-draw ties, residual draws)."""
+    am = ref["accept_margin"]
+    V = w.spec.vocab
+    step_ties = draw_ties = draws = 0
     for b in range(len(w.lens)):
         s0, s1 = int(w.cu_B[b]), int(w.cu_B[b + 1])
         B = s1 - s0
         tested = am[s0:s1]
-        tie_step = (tested >= 0) & (tested < TIE)
-        if tie_step.any():
-            ties += 1
+        if ((tested >= 0) & (tested < TIE_ACCEPT)).any():
+            step_ties += 1
             assert 0 <= n_accept[b] <= B
+            if pos[b] >= 0:
+                assert n_accept[b] < B and 0 <= token[b] < V
             continue
         assert n_accept[b] == ref["n_accept"][b], (b, n_accept[b], ref["n_accept"][b])
         assert pos[b] == ref["pos"][b], (b, pos[b], ref["pos"][b])
         if ref["pos"][b] < 0:
             assert token[b] == -1
             continue
-        if 0 <= rm[b] < TIE:
-            ties += 1
-            assert 0 <= token[b] < w.spec.vocab
+        draws += 1
+        k = s0 + int(ref["pos"][b])
+        r, S = oracle.residual(synth.to_f64(w.target[k]), synth.to_f64(w.draft[k]))
+        C = np.cumsum(r)
+        U = float(w.uniforms[b, B]) * S
+        v = int(ref["token"][b])
+        lo = C[v - 1] if v > 0 else 0.0
+        if min(U - lo, C[v] - U) >= TIE_RESIDUAL:
+            assert token[b] == v, (b, token[b], v)
             continue
-        assert token[b] == ref["token"][b], (b, token[b], ref["token"][b])
-    return ties
+        draw_ties += 1
+        g = int(token[b])
+        assert 0 <= g < V and r[g] > 0, (b, g)
+        glo = C[g - 1] if g > 0 else 0.0
+        assert glo - TIE_RESIDUAL <= U < C[g] + TIE_RESIDUAL, (b, g, v, U, glo, C[g])
+    return step_ties, draw_ties, draws
