@@ -233,6 +233,33 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
                                 void *const events[5]);
 
 /* ------------------------------------------------------------------------
+ * simsd_accept_noalloc -- simsd_accept for callers that cannot allocate
+ * device memory.  (No counterpart in the SimSD paper: it is a deployment
+ * convenience.)  Some callers never get to call cudaMalloc: a serving loop
+ * that runs the acceptance step under a fixed memory budget and must not
+ * allocate per request (an allocation can fail under memory pressure, or
+ * stall the device mid-request), or a plugin whose host framework owns all
+ * device memory and hands it only the input and output tensors.  This entry
+ * point takes the same descriptor, ignores its workspace fields, and keeps
+ * its scratch in a static device array of SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES
+ * bytes that every GPU loading the library holds until the process exits.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - Sizes whose scratch (what simsd_accept_workspace_size reports) exceeds
+ *     the array are rejected with SIMSD_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address
+ *     (once per device, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array per device and it keeps the previous
+ *     call's contents (the call clears what must start at zero).  Calls that
+ *     overlap on the GPU -- on different streams, or from several host
+ *     threads -- race on it: serialise them.
+ *   - The kernels' status word lives in that array, so simsd_read_status
+ *     cannot read it; device-detected input errors are not reported here.
+ * ---------------------------------------------------------------------- */
+#define SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream);
+
+/* ------------------------------------------------------------------------
  * simsd_read_status -- synchronise `stream`, copy the device status word of
  * a workspace used by simsd_verify_attn / simsd_accept to *word_out (bit 0:
  * a bounded wait ran out) and clear it.  Returns SIMSD_ERR_TIMEOUT when a

@@ -84,6 +84,8 @@ def lib():
         L.simsd_verify_attn_timed.argtypes = [ctypes.POINTER(VerifyDesc), _vp, ctypes.POINTER(_vp)]
         L.simsd_accept_timed.restype = ctypes.c_int
         L.simsd_accept_timed.argtypes = [ctypes.POINTER(AcceptDesc), _vp, ctypes.POINTER(_vp)]
+        L.simsd_accept_noalloc.restype = ctypes.c_int
+        L.simsd_accept_noalloc.argtypes = [ctypes.POINTER(AcceptDesc), _vp]
         L.simsd_read_status.restype = ctypes.c_int
         L.simsd_read_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
         _LIB = L
@@ -238,6 +240,16 @@ def accept(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token, po
     else:
         _check(lib().simsd_accept_timed(ctypes.byref(d), _stream(stream), _events(events, 5)),
                "simsd_accept_timed")
+
+
+def accept_noalloc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
+                   pos, total_B, B_max, stream=None):
+    """simsd_accept_noalloc: acceptance with the library's static scratch, for
+    callers that may not allocate device memory (no workspace argument)."""
+    d = _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
+                     pos, total_B, B_max)
+    _check(lib().simsd_accept_noalloc(ctypes.byref(d), _stream(stream)),
+           "simsd_accept_noalloc")
 
 
 def read_status(workspace, stream=None):

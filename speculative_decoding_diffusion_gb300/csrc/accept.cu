@@ -26,6 +26,8 @@
 //        inverse CDF inside the selected chunk.  Within a chunk the running
 //        sum never decreases (thread totals prefixed sequentially), so the
 //        chosen token always has positive mass.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -419,6 +421,32 @@ simsd_status accept_check(const simsd_accept_desc *d) {
   return SIMSD_OK;
 }
 
+// Scratch of simsd_accept_noalloc: one static array per device, alive until
+// the process exits.  Host code may not take its address directly (the
+// name is a host-side stand-in there); static_scratch() looks the device
+// address up once per device.
+constexpr int kMaxDevices = 64;
+static_assert(SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES % kAlign == 0, "scratch size");
+static __device__ __align__(256) unsigned char g_accept_scratch[SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES];
+
+cudaError_t static_scratch(char **out) {
+  static std::mutex mu;
+  static void *addr[kMaxDevices] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_accept_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = (char *)addr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 }  // namespace simsd
 
@@ -476,6 +504,50 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream_ptr,
   cudaError_t e = d->dtype == SIMSD_BF16
                       ? launch_all<__nv_bfloat16>(a, d->total_B, stream, events)
                       : launch_all<float>(a, d->total_B, stream, events);
+  return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
+}
+
+// Same kernels and arguments as simsd_accept; scratch from the static
+// array instead of a caller workspace (see simsd.h for who needs this).
+simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream_ptr) {
+  simsd_status st = accept_check(d);
+  if (st != SIMSD_OK) return st;
+  if (!d->target_logits || !d->draft_logits || !d->draft_tokens || !d->tau ||
+      !d->cu_B || !d->uniforms || !d->n_accept || !d->token || !d->pos)
+    return SIMSD_ERR_NULL;
+  const AcceptWs w = accept_ws(d);
+  if (w.total > SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES) return SIMSD_ERR_WORKSPACE;
+  char *ws = nullptr;
+  if (static_scratch(&ws) != cudaSuccess) return SIMSD_ERR_CUDA;
+  cudaStream_t stream = (cudaStream_t)stream_ptr;
+  if (cudaMemsetAsync(ws + w.off_status, 0, sizeof(uint32_t), stream) != cudaSuccess)
+    return SIMSD_ERR_CUDA;
+  AcceptArgs a;
+  a.target = d->target_logits;
+  a.draft = d->draft_logits;
+  a.draft_tokens = d->draft_tokens;
+  a.tau = d->tau;
+  a.cu_B = d->cu_B;
+  a.uniforms = d->uniforms;
+  a.n_accept = d->n_accept;
+  a.token = d->token;
+  a.pos = d->pos;
+  a.lse_part = (float4 *)(ws + w.off_lse);
+  a.state = (WalkState *)(ws + w.off_state);
+  a.res_part = (double2 *)(ws + w.off_res);
+  a.status = (uint32_t *)(ws + w.off_status);
+  a.batch = d->batch;
+  a.vocab = d->vocab;
+  a.B_max = d->B_max;
+  a.lse_chunks = w.lse_chunks;
+  a.res_chunks = w.res_chunks;
+  const size_t es = d->dtype == SIMSD_BF16 ? 2 : 4;
+  a.vec_ok = ((size_t)d->vocab * es) % 16 == 0 &&
+             ((uintptr_t)d->target_logits % 16) == 0 &&
+             ((uintptr_t)d->draft_logits % 16) == 0;
+  cudaError_t e = d->dtype == SIMSD_BF16
+                      ? launch_all<__nv_bfloat16>(a, d->total_B, stream, nullptr)
+                      : launch_all<float>(a, d->total_B, stream, nullptr);
   return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
 }
 

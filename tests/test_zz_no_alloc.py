@@ -1,0 +1,65 @@
+"""simsd_accept_noalloc: acceptance for callers that cannot allocate.
+
+Serving loops with a fixed device-memory budget, or plugins whose host
+framework owns all device memory, cannot hand the library a workspace from
+cudaMalloc.  The no-allocation entry point keeps its scratch in a static
+device array instead.  Its decisions must equal those of simsd_accept (the
+same kernels on the same inputs, so integers compare exactly), on two calls
+in a row -- the second call sees the first call's leftovers in the shared
+array -- and sizes beyond the array are refused before anything runs.
+
+This file is named to be collected last: it must pass both on its own in a
+fresh process and after every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from speculative_decoding_diffusion_gb300 import binding
+from speculative_decoding_diffusion_gb300.staging import DeviceWorkload
+
+pytestmark = pytest.mark.gpu
+
+
+def _outputs(dw):
+    return (dw.n_accept.cpu().numpy().copy(), dw.token.cpu().numpy().copy(),
+            dw.pos.cpu().numpy().copy())
+
+
+def test_noalloc_matches_workspace_entry_point_twice():
+    w = synth.config(1)                       # 16 x vocab 151936, bf16
+    dw = DeviceWorkload(w, with_verify=False)
+    args = (dw.target, dw.draft, dw.draft_tokens, dw.tau, dw.cu_B, dw.uniforms,
+            dw.n_accept, dw.token, dw.pos, dw.total_B, dw.B_max)
+    rng = np.random.default_rng(77)
+    for call in range(2):
+        if call == 1:   # second call: other uniforms, same shared scratch
+            dw.uniforms.copy_(torch.from_numpy(
+                rng.random(tuple(dw.uniforms.shape), dtype=np.float32)))
+        dw.accept()
+        torch.cuda.synchronize()
+        ref = _outputs(dw)
+        for t in (dw.n_accept, dw.token, dw.pos):
+            t.fill_(-7)
+        binding.accept_noalloc(*args)
+        torch.cuda.synchronize()
+        got = _outputs(dw)
+        for g, r in zip(got, ref):
+            np.testing.assert_array_equal(g, r)
+        assert (got[0] >= 0).all()
+
+
+def test_noalloc_rejects_sizes_beyond_its_array():
+    # 4096 slots x vocab 1e6 needs far more scratch than the static array
+    d = binding.AcceptDesc()
+    for k, v in dict(batch=4096, vocab=1_000_000, total_B=4096, B_max=1,
+                     dtype=binding.SIMSD_BF16).items():
+        setattr(d, k, v)
+    fake = 1 << 40   # never dereferenced: the call returns before launching
+    for f in ("target_logits", "draft_logits", "draft_tokens", "tau", "cu_B",
+              "uniforms", "n_accept", "token", "pos"):
+        setattr(d, f, fake)
+    lib = binding.lib()
+    assert lib.simsd_accept_workspace_size(d) > 8 << 20
+    assert lib.simsd_accept_noalloc(d, None) == 5   # SIMSD_ERR_WORKSPACE
