@@ -191,7 +191,8 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  *   at the first rejection draw a token from max(0, p - q) normalised (p
  *   itself if that is empty) by inverse CDF with u[B_b], and stop.
  * Kernels: K4a (per slot and vocabulary chunk: max and sum of exponentials
- * of both rows), K4b (one CTA per sequence: the walk and the residual draw).
+ * of both rows; the last CTA of a sequence walks its steps), K4b (per
+ * residual chunk of the rejected slot; the last CTA of a sequence draws).
  *   target_logits, draft_logits device [total_B][vocab] (dtype); row k of
  *                sequence b (at cu_B[b]+k) holds the logits read at D~_k
  *   draft_tokens device int32[total_B] in [0, vocab)
@@ -227,10 +228,9 @@ size_t simsd_accept_workspace_size(const simsd_accept_desc *d);
 simsd_status simsd_accept(const simsd_accept_desc *d, void *stream);
 
 /* Same as simsd_accept, recording events (cudaEvent_t or NULL) on `stream`:
- * events[0] before K4a, [1] after K4a, [2] after K4b, [3] after K4c,
- * [4] after K4d. */
+ * events[0] before K4a, [1] after K4a, [2] after K4b. */
 simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
-                                void *const events[5]);
+                                void *const events[3]);
 
 /* ------------------------------------------------------------------------
  * simsd_accept_noalloc -- simsd_accept for callers that cannot allocate

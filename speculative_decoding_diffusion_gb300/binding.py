@@ -232,13 +232,13 @@ def accept_workspace_size(target, draft, draft_tokens, tau, cu_B, uniforms, n_ac
 
 def accept(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token, pos,
            workspace, total_B, B_max, stream=None, events=None):
-    """simsd_accept; events: optional 5 recorded torch.cuda.Event objects."""
+    """simsd_accept; events: optional 3 recorded torch.cuda.Event objects."""
     d = _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
                      pos, total_B, B_max, workspace)
     if events is None:
         _check(lib().simsd_accept(ctypes.byref(d), _stream(stream)), "simsd_accept")
     else:
-        _check(lib().simsd_accept_timed(ctypes.byref(d), _stream(stream), _events(events, 5)),
+        _check(lib().simsd_accept_timed(ctypes.byref(d), _stream(stream), _events(events, 3)),
                "simsd_accept_timed")
 
 

@@ -8,24 +8,19 @@
 // first rejection a token is drawn from max(0, p - q) normalised (p itself
 // when that is empty) by inverse CDF with u[B].
 //
-// Numerics: every exponential is taken relative to a row maximum M in logit
-// units, 2^((x - M) log2 e): x - M is exact for bf16 logits, so only the
-// product and exp2f round (~2e-7 relative on the entries that carry mass).
-// Cross-thread sums, the normaliser and every running CDF are fp64 (a few
-// hundred additions per CTA); per-thread partial sums of <= 16 entries stay
-// fp32.  The residual CDF is then within ~1e-6 (absolute, probability mass)
-// of the exact one.
-//
-// Four launches, all sized to the data rather than to the batch:
+// Two launches:
 //   K4a  grid (vocab chunk, slot): max and sum of exponentials of the target
-//        and draft rows of every slot (the dominant HBM stream);
-//   K4b  one CTA per sequence: merge chunk partials, p(x), q(x), the walk;
-//   K4c  grid (residual chunk, sequence): per-chunk sums of max(0, p - q)
-//        (and of p) of the rejected slot only;
-//   K4d  one CTA per sequence with a rejection: prefix over chunk sums,
-//        inverse CDF inside the selected chunk.  Within a chunk the running
-//        sum never decreases (thread totals prefixed sequentially), so the
-//        chosen token always has positive mass.
+//        and draft rows (the dominant HBM stream).  The last CTA to finish a
+//        sequence (a wait-free counter, no spinning) merges that sequence's
+//        partials and walks its steps in tau order.
+//   K4b  grid (residual chunk, sequence): per-chunk residual mass of the
+//        rejected slot only; the last CTA of a sequence takes the prefix over
+//        chunks and draws the token inside the selected chunk.
+// Numerics: exponentials are taken relative to a row maximum in logit units
+// (x - max is exact for bf16); normalisers, chunk sums and running CDFs are
+// compensated fp32 pairs (two-sum), never fp64 (GB300's fp64 rate is a small
+// fraction of its fp32 rate).  The residual CDF is then within ~1e-6
+// (absolute probability mass) of the exact one.
 #include <mutex>
 
 #include "common.cuh"
@@ -35,33 +30,64 @@ namespace simsd {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kLseChunk = 4096;   // K4a vocabulary chunk
-constexpr int kResPer = 8;        // residual entries per thread
-constexpr int kResChunk = kThreads * kResPer;
+constexpr int kLseVec = 4;                        // 16-byte loads per row per thread per pass
+constexpr int kLseChunk = 8192;                   // K4a vocabulary chunk
+constexpr int kResPer = 8;                        // residual entries per thread
+constexpr int kResChunk = kThreads * kResPer;     // 2048
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Per sequence, after the walk: rejected slot (-1: none) and the row maxima
-// and normalisers of that slot.
+// ------------------------------------------------------------ two-sum pairs
+// value = hi + lo with |lo| <= ulp(hi)/2 (Knuth's two-sum; Dekker's
+// fast-two-sum for the renormalisation).
+struct Ff {
+  float hi, lo;
+};
+__device__ __forceinline__ Ff ff_add(Ff a, Ff b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float err = (a.hi - (s - bb)) + (b.hi - bb);
+  const float lo = err + a.lo + b.lo;
+  const float hi = s + lo;
+  return Ff{hi, lo - (hi - s)};
+}
+__device__ __forceinline__ Ff ff_of(float x) { return Ff{x, 0.f}; }
+__device__ __forceinline__ Ff ff_shfl_xor(Ff a, int m) {
+  return Ff{__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
+}
+__device__ __forceinline__ Ff ff_shfl_up(Ff a, int d) {
+  return Ff{__shfl_up_sync(0xffffffffu, a.hi, d), __shfl_up_sync(0xffffffffu, a.lo, d)};
+}
+// a > u where u is a pair: compare the exact sums' signs
+__device__ __forceinline__ bool ff_gt(Ff a, Ff u) {
+  const Ff d = ff_add(a, Ff{-u.hi, -u.lo});
+  return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
+}
+
+// Per sequence, after the walk: rejected slot (-1: none), that slot's row
+// maxima and normalisers.
 struct WalkState {
   int rej;
-  float Mt, Md;
-  double St, Sd;
+  float Mt, Md, St, Sd;
 };
 
 struct AcceptWs {
-  size_t off_status, off_lse, off_state, off_res, total;
+  size_t off_status, status_bytes, off_lse, off_state, off_res, total;
   int lse_chunks, res_chunks;
 };
 
+// status word, then two per-sequence arrival counters; the whole head is
+// cleared at the start of every call.
 AcceptWs accept_ws(const simsd_accept_desc *d) {
   AcceptWs w;
   w.lse_chunks = (d->vocab + kLseChunk - 1) / kLseChunk;
   w.res_chunks = (d->vocab + kResChunk - 1) / kResChunk;
   size_t off = 0;
-  w.off_status = off; off = align_up(off + sizeof(uint32_t), kAlign);
+  w.off_status = off;
+  w.status_bytes = sizeof(uint32_t) * (1 + 2 * (size_t)d->batch);
+  off = align_up(off + w.status_bytes, kAlign);
   w.off_lse = off;    off = align_up(off + (size_t)d->total_B * w.lse_chunks * sizeof(float4), kAlign);
   w.off_state = off;  off = align_up(off + (size_t)d->batch * sizeof(WalkState), kAlign);
-  w.off_res = off;    off = align_up(off + (size_t)d->batch * w.res_chunks * sizeof(double2), kAlign);
+  w.off_res = off;    off = align_up(off + (size_t)d->batch * w.res_chunks * sizeof(float4), kAlign);
   w.total = off;
   return w;
 }
@@ -78,8 +104,8 @@ struct AcceptArgs {
   int32_t *pos;
   float4 *lse_part;     // [total_B][lse_chunks]: (M_t, s_t, M_d, s_d)
   WalkState *state;     // [batch]
-  double2 *res_part;    // [batch][res_chunks]: (sum r, sum p)
-  uint32_t *status;
+  float4 *res_part;     // [batch][res_chunks]: residual pair, target-mass pair
+  uint32_t *status;     // [0]: status word; [1..batch]: K4a counters; then K4b's
   int batch, vocab, B_max, lse_chunks, res_chunks, vec_ok;
 };
 
@@ -102,16 +128,21 @@ __device__ __forceinline__ void accum(float &m, float &s, const float *x, int n)
 template <typename T> struct Ld;
 template <> struct Ld<float> {
   static constexpr int N = 4;
-  static __device__ __forceinline__ void vec(const float *p, float *f) {
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(p));
-    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  static __device__ __forceinline__ uint4 raw(const float *p) {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+  }
+  static __device__ __forceinline__ void unpack(uint4 v, float *f) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
   }
   static __device__ __forceinline__ float one(const float *p) { return __ldg(p); }
 };
 template <> struct Ld<__nv_bfloat16> {
   static constexpr int N = 8;
-  static __device__ __forceinline__ void vec(const __nv_bfloat16 *p, float *f) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+  static __device__ __forceinline__ uint4 raw(const __nv_bfloat16 *p) {
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+  }
+  static __device__ __forceinline__ void unpack(uint4 v, float *f) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -124,8 +155,8 @@ template <> struct Ld<__nv_bfloat16> {
   }
 };
 
-// Block-wide (M, s) merge: warps in fp32, across warps in fp64 relative to
-// the block maximum.  Result in thread 0.
+// Block-wide (M, s) merge, result in thread 0 (sums as two-sum pairs across
+// warps, relative to the block maximum).
 __device__ __forceinline__ void block_lse(float &m, float &s, float2 *scratch) {
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) {
@@ -139,95 +170,53 @@ __device__ __forceinline__ void block_lse(float &m, float &s, float2 *scratch) {
   if (threadIdx.x == 0) {
     float M = -INFINITY;
     for (int i = 0; i < kThreads / 32; ++i) M = fmaxf(M, scratch[i].x);
-    double S = 0.0;
+    Ff S = ff_of(0.f);
     if (M != -INFINITY)
       for (int i = 0; i < kThreads / 32; ++i)
-        S += (double)scratch[i].y * (double)exp2f((scratch[i].x - M) * kLog2e);
+        S = ff_add(S, ff_of(scratch[i].y * exp2f((scratch[i].x - M) * kLog2e)));
     m = M;
-    s = (float)S;
+    s = S.hi + S.lo;
   }
   __syncthreads();
 }
 
-// ---------------------------------------------------------------- K4a
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-lse_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ float2 scratch[2][kThreads / 32];
-  const int chunk = blockIdx.x, slot = blockIdx.y;
-  const long row = (long)slot * a.vocab;
-  const int v0 = chunk * kLseChunk;
-  const int v1 = min(a.vocab, v0 + kLseChunk);
-  const T *tr = (const T *)a.target + row;
-  const T *dr = (const T *)a.draft + row;
-  float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
-  constexpr int N = Ld<T>::N;
-  int tail0 = v0;
-  if (a.vec_ok) {
-    for (int v = v0 + threadIdx.x * N; v + N <= v1; v += kThreads * N) {
-      float xt[N], xd[N];
-      Ld<T>::vec(tr + v, xt);
-      Ld<T>::vec(dr + v, xd);
-      accum(mt, st, xt, N);
-      accum(md, sd, xd, N);
-    }
-    tail0 = v0 + ((v1 - v0) / N) * N;   // ragged end (last chunk only)
-  }
-  for (int v = tail0 + threadIdx.x; v < v1; v += kThreads) {
-    float xt = Ld<T>::one(tr + v), xd = Ld<T>::one(dr + v);
-    accum(mt, st, &xt, 1);
-    accum(md, sd, &xd, 1);
-  }
-  block_lse(mt, st, scratch[0]);
-  block_lse(md, sd, scratch[1]);
-  if (threadIdx.x == 0) a.lse_part[(long)slot * a.lse_chunks + chunk] = make_float4(mt, st, md, sd);
-}
-
 // Row maximum and normaliser of one slot from its chunk partials (one warp).
 __device__ __forceinline__ void row_norm(const float4 *pp, int chunks, int lane,
-                                         float &Mt, double &St, float &Md, double &Sd) {
+                                         float &Mt, float &St, float &Md, float &Sd) {
   float mt = -INFINITY, md = -INFINITY;
-  for (int c = lane; c < chunks; c += 32) { mt = fmaxf(mt, pp[c].x); md = fmaxf(md, pp[c].z); }
+  for (int c = lane; c < chunks; c += 32) {
+    const float4 v = __ldcg(pp + c);
+    mt = fmaxf(mt, v.x);
+    md = fmaxf(md, v.z);
+  }
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) {
     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, w));
     md = fmaxf(md, __shfl_xor_sync(0xffffffffu, md, w));
   }
-  double st = 0.0, sd = 0.0;
+  Ff st = ff_of(0.f), sd = ff_of(0.f);
   for (int c = lane; c < chunks; c += 32) {
-    const float4 v = pp[c];
-    if (v.y > 0.f) st += (double)v.y * (double)exp2f((v.x - mt) * kLog2e);
-    if (v.w > 0.f) sd += (double)v.w * (double)exp2f((v.z - md) * kLog2e);
+    const float4 v = __ldcg(pp + c);
+    if (v.y > 0.f) st = ff_add(st, ff_of(v.y * exp2f((v.x - mt) * kLog2e)));
+    if (v.w > 0.f) sd = ff_add(sd, ff_of(v.w * exp2f((v.z - md) * kLog2e)));
   }
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) {
-    st += __shfl_xor_sync(0xffffffffu, st, w);
-    sd += __shfl_xor_sync(0xffffffffu, sd, w);
+    st = ff_add(st, ff_shfl_xor(st, w));
+    sd = ff_add(sd, ff_shfl_xor(sd, w));
   }
-  Mt = mt; St = st; Md = md; Sd = sd;
+  Mt = mt; St = st.hi + st.lo; Md = md; Sd = sd.hi + sd.lo;
 }
 
-// ---------------------------------------------------------------- K4b
+// The walk of sequence b (whole CTA): p(x), q(x) per slot, then steps in tau
+// order; writes the outputs and the walk state.
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
-walk_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ float px_s[kMaxB], qx_s[kMaxB], mt_s[kMaxB], md_s[kMaxB];
-  __shared__ double st_s[kMaxB], sd_s[kMaxB];
-  const int b = blockIdx.x;
-  const int c0 = __ldg(a.cu_B + b);
-  const int B = __ldg(a.cu_B + b + 1) - c0;
-  if (B < 1 || B > kMaxB) {                  // malformed sequence: no walk
-    if (threadIdx.x == 0) {
-      a.n_accept[b] = 0; a.token[b] = -1; a.pos[b] = -1;
-      a.state[b] = WalkState{-1, 0.f, 0.f, 0.0, 0.0};
-      raise_status(a.status, kStatusBadInput);
-    }
-    return;
-  }
+__device__ void walk(const AcceptArgs &a, int b, int c0, int B) {
+  __shared__ float px_s[kMaxB], qx_s[kMaxB];
+  __shared__ WalkState ws_s[kMaxB];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int k = warp; k < B; k += kThreads / 32) {
-    float Mt, Md;
-    double St, Sd;
+    float Mt, Md, St, Sd;
     row_norm(a.lse_part + (long)(c0 + k) * a.lse_chunks, a.lse_chunks, lane, Mt, St, Md, Sd);
     if (lane == 0) {
       const long row = (long)(c0 + k) * a.vocab;
@@ -235,9 +224,9 @@ walk_kernel(const __grid_constant__ AcceptArgs a) {
       if (x < 0 || x >= a.vocab) { raise_status(a.status, kStatusBadInput); x = 0; }
       const float tx = Ld<T>::one((const T *)a.target + row + x);
       const float dx = Ld<T>::one((const T *)a.draft + row + x);
-      px_s[k] = (float)((double)exp2f((tx - Mt) * kLog2e) / St);
-      qx_s[k] = (float)((double)exp2f((dx - Md) * kLog2e) / Sd);
-      mt_s[k] = Mt; md_s[k] = Md; st_s[k] = St; sd_s[k] = Sd;
+      px_s[k] = exp2f((tx - Mt) * kLog2e) / St;
+      qx_s[k] = exp2f((dx - Md) * kLog2e) / Sd;
+      ws_s[k] = WalkState{k, Mt, Md, St, Sd};
     }
   }
   __syncthreads();
@@ -258,11 +247,83 @@ walk_kernel(const __grid_constant__ AcceptArgs a) {
     a.pos[b] = rej;
     if (rej < 0) {
       a.token[b] = -1;
-      a.state[b] = WalkState{-1, 0.f, 0.f, 0.0, 0.0};
+      a.state[b] = WalkState{-1, 0.f, 0.f, 1.f, 1.f};
     } else {
-      a.state[b] = WalkState{rej, mt_s[rej], md_s[rej], st_s[rej], sd_s[rej]};
+      a.state[b] = ws_s[rej];
     }
   }
+}
+
+// ---------------------------------------------------------------- K4a
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+lse_walk_kernel(const __grid_constant__ AcceptArgs a) {
+  __shared__ float2 scratch[2][kThreads / 32];
+  __shared__ int last_s;
+  const int chunk = blockIdx.x, slot = blockIdx.y;
+  const long row = (long)slot * a.vocab;
+  const int v0 = chunk * kLseChunk;
+  const int v1 = min(a.vocab, v0 + kLseChunk);
+  const T *tr = (const T *)a.target + row;
+  const T *dr = (const T *)a.draft + row;
+  float mt = -INFINITY, st = 0.f, md = -INFINITY, sd = 0.f;
+  constexpr int N = Ld<T>::N;
+  int tail0 = v0;
+  if (a.vec_ok) {
+    // kLseVec independent 16-byte loads per row in flight per thread
+    constexpr int STEP = kThreads * N;
+    int v = v0 + threadIdx.x * N;
+    for (; v + (kLseVec - 1) * STEP + N <= v1; v += kLseVec * STEP) {
+      uint4 rt[kLseVec], rd[kLseVec];
+#pragma unroll
+      for (int i = 0; i < kLseVec; ++i) { rt[i] = Ld<T>::raw(tr + v + i * STEP); rd[i] = Ld<T>::raw(dr + v + i * STEP); }
+#pragma unroll
+      for (int i = 0; i < kLseVec; ++i) {
+        float xt[N], xd[N];
+        Ld<T>::unpack(rt[i], xt);
+        Ld<T>::unpack(rd[i], xd);
+        accum(mt, st, xt, N);
+        accum(md, sd, xd, N);
+      }
+    }
+    for (; v + N <= v1; v += STEP) {
+      float xt[N], xd[N];
+      Ld<T>::unpack(Ld<T>::raw(tr + v), xt);
+      Ld<T>::unpack(Ld<T>::raw(dr + v), xd);
+      accum(mt, st, xt, N);
+      accum(md, sd, xd, N);
+    }
+    tail0 = v0 + ((v1 - v0) / N) * N;   // ragged end (last chunk only)
+  }
+  for (int v = tail0 + threadIdx.x; v < v1; v += kThreads) {
+    float xt = Ld<T>::one(tr + v), xd = Ld<T>::one(dr + v);
+    accum(mt, st, &xt, 1);
+    accum(md, sd, &xd, 1);
+  }
+  block_lse(mt, st, scratch[0]);
+  block_lse(md, sd, scratch[1]);
+  // the sequence this slot belongs to, and whether this CTA finishes it
+  const int b = find_seq(a.cu_B, a.batch, slot);
+  const int c0 = __ldg(a.cu_B + b);
+  const int B = __ldg(a.cu_B + b + 1) - c0;
+  if (threadIdx.x == 0) {
+    a.lse_part[(long)slot * a.lse_chunks + chunk] = make_float4(mt, st, md, sd);
+    __threadfence();
+    const unsigned total = (unsigned)B * a.lse_chunks;
+    last_s = atomicAdd(a.status + 1 + b, 1u) + 1 == total;
+  }
+  __syncthreads();
+  if (!last_s) return;
+  __threadfence();
+  if (B < 1 || B > kMaxB) {                  // malformed sequence: no walk
+    if (threadIdx.x == 0) {
+      a.n_accept[b] = 0; a.token[b] = -1; a.pos[b] = -1;
+      a.state[b] = WalkState{-1, 0.f, 0.f, 1.f, 1.f};
+      raise_status(a.status, kStatusBadInput);
+    }
+    return;
+  }
+  walk<T>(a, b, c0, B);
 }
 
 // Residual mass r = max(0, p - q) and target mass p of one entry.
@@ -273,90 +334,112 @@ __device__ __forceinline__ void res_pair(float t, float d, const WalkState &st,
   r = fmaxf(p - q, 0.f);
 }
 
-// ---------------------------------------------------------------- K4c
+// Inclusive block scan of two-sum pairs in thread order; returns the
+// exclusive prefix of this thread and the block total (in all threads).
+__device__ __forceinline__ Ff block_excl_scan(Ff x, Ff *warp_tot, Ff &total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ff inc = x;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const Ff y = ff_shfl_up(inc, d);
+    if (lane >= d) inc = ff_add(y, inc);
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  Ff base = ff_of(0.f), tot = ff_of(0.f);
+  for (int w = 0; w < kThreads / 32; ++w) {
+    if (w == warp) base = tot;
+    tot = ff_add(tot, warp_tot[w]);
+  }
+  total = tot;
+  const Ff excl_in_warp = ff_add(inc, Ff{-x.hi, -x.lo});
+  return ff_add(base, excl_in_warp);
+}
+
+// ---------------------------------------------------------------- K4b
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
-residual_sum_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ double2 scratch[kThreads / 32];
+residual_kernel(const __grid_constant__ AcceptArgs a) {
+  __shared__ Ff warp_tot[kThreads / 32];
+  __shared__ int last_s, sel_s, use_p_s, best_s, lastpos_s;
+  __shared__ Ff base_s, U_s;
   const int chunk = blockIdx.x, b = blockIdx.y;
   const WalkState st = a.state[b];
   if (st.rej < 0) return;
-  const float inv_st = (float)(1.0 / st.St), inv_sd = (float)(1.0 / st.Sd);
-  const long row = (long)(__ldg(a.cu_B + b) + st.rej) * a.vocab;
-  const T *tr = (const T *)a.target + row;
-  const T *dr = (const T *)a.draft + row;
-  const int v0 = chunk * kResChunk + threadIdx.x * kResPer;
-  float sr = 0.f, sp = 0.f;
-  for (int i = 0; i < kResPer; ++i) {
-    const int v = v0 + i;
-    if (v >= a.vocab) break;
-    float r, p;
-    res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st, inv_st, inv_sd, r, p);
-    sr += r;
-    sp += p;
-  }
-  double dr_ = sr, dp = sp;
-#pragma unroll
-  for (int w = 16; w > 0; w >>= 1) {
-    dr_ += __shfl_xor_sync(0xffffffffu, dr_, w);
-    dp += __shfl_xor_sync(0xffffffffu, dp, w);
-  }
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = make_double2(dr_, dp);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double2 tot = scratch[0];
-    for (int i = 1; i < kThreads / 32; ++i) { tot.x += scratch[i].x; tot.y += scratch[i].y; }
-    a.res_part[(long)b * a.res_chunks + chunk] = tot;
-  }
-}
-
-// ---------------------------------------------------------------- K4d
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-residual_draw_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ double wsum[kThreads];
-  __shared__ int sel_chunk, use_p_s, best_s, last_pos_s;
-  __shared__ double base_s, U_s;
-  const int b = blockIdx.x;
-  const WalkState st = a.state[b];
-  if (st.rej < 0) return;
+  const float inv_st = 1.f / st.St, inv_sd = 1.f / st.Sd;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
-  const double2 *rp = a.res_part + (long)b * a.res_chunks;
+  const long row = (long)(c0 + st.rej) * a.vocab;
+  const T *tr = (const T *)a.target + row;
+  const T *dr = (const T *)a.draft + row;
+  {
+    const int v0 = chunk * kResChunk + threadIdx.x * kResPer;
+    float sr = 0.f, sp = 0.f;
+    for (int i = 0; i < kResPer; ++i) {
+      const int v = v0 + i;
+      if (v >= a.vocab) break;
+      float r, p;
+      res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st, inv_st, inv_sd, r, p);
+      sr += r;
+      sp += p;
+    }
+    Ff fr = ff_of(sr), fp = ff_of(sp);
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) {
+      fr = ff_add(fr, ff_shfl_xor(fr, w));
+      fp = ff_add(fp, ff_shfl_xor(fp, w));
+    }
+    __shared__ Ff rs[kThreads / 32], ps[kThreads / 32];
+    if ((threadIdx.x & 31) == 0) { rs[threadIdx.x >> 5] = fr; ps[threadIdx.x >> 5] = fp; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      Ff tr_ = rs[0], tp = ps[0];
+      for (int i = 1; i < kThreads / 32; ++i) { tr_ = ff_add(tr_, rs[i]); tp = ff_add(tp, ps[i]); }
+      a.res_part[(long)b * a.res_chunks + chunk] = make_float4(tr_.hi, tr_.lo, tp.hi, tp.lo);
+      __threadfence();
+      last_s = atomicAdd(a.status + 1 + a.batch + b, 1u) + 1 == (unsigned)a.res_chunks;
+    }
+    __syncthreads();
+  }
+  if (!last_s) return;
+  __threadfence();
+  // -- the last CTA of sequence b draws the token
+  const float4 *rp = a.res_part + (long)b * a.res_chunks;
   if (threadIdx.x == 0) {
-    double S = 0.0;
-    for (int c = 0; c < a.res_chunks; ++c) S += rp[c].x;
-    const int use_p = !(S > 0.0);            // empty residual: draw from p
-    double tot = 0.0;
-    if (use_p) for (int c = 0; c < a.res_chunks; ++c) tot += rp[c].y;
-    else tot = S;
-    const double U = (double)__ldg(a.uniforms + (long)b * (a.B_max + 1) + B) * tot;
-    // chunk c with T[c] <= U < T[c+1] (T: running sum of chunk masses); if
-    // rounding leaves U at or past the total, the last non-empty chunk
-    double T0 = 0.0, sel_base = 0.0, last_base = 0.0;
+    Ff S = ff_of(0.f), Sp = ff_of(0.f);
+    for (int c = 0; c < a.res_chunks; ++c) {
+      const float4 v = __ldcg(rp + c);
+      S = ff_add(S, Ff{v.x, v.y});
+      Sp = ff_add(Sp, Ff{v.z, v.w});
+    }
+    const int use_p = !(S.hi > 0.f);         // empty residual: draw from p
+    const Ff tot = use_p ? Sp : S;
+    // U = u * tot as a pair (u exact in fp32; the product's error by fma)
+    const float u = __ldg(a.uniforms + (long)b * (a.B_max + 1) + B);
+    const float uh = u * tot.hi;
+    const Ff U = ff_add(Ff{uh, fmaf(u, tot.hi, -uh)}, ff_of(u * tot.lo));
+    // chunk c with T[c] <= U < T[c+1]; if rounding leaves U at or past the
+    // total, the last non-empty chunk
+    Ff T0 = ff_of(0.f), sel_base = ff_of(0.f), last_base = ff_of(0.f);
     int sel = -1, last_nz = 0;
     for (int c = 0; c < a.res_chunks; ++c) {
-      const double m = use_p ? rp[c].y : rp[c].x;
-      const double T1 = T0 + m;
-      if (m > 0.0) { last_nz = c; last_base = T0; }
-      if (sel < 0 && U < T1 && m > 0.0) { sel = c; sel_base = T0; }
+      const float4 v = __ldcg(rp + c);
+      const Ff m = use_p ? Ff{v.z, v.w} : Ff{v.x, v.y};
+      const Ff T1 = ff_add(T0, m);
+      if (m.hi > 0.f) { last_nz = c; last_base = T0; }
+      if (sel < 0 && m.hi > 0.f && ff_gt(T1, U)) { sel = c; sel_base = T0; }
       T0 = T1;
     }
     if (sel < 0) { sel = last_nz; sel_base = last_base; }
-    sel_chunk = sel;
+    sel_s = sel;
     base_s = sel_base;
     U_s = U;
     use_p_s = use_p;
     best_s = 0x7fffffff;
-    last_pos_s = -1;
+    lastpos_s = -1;
   }
   __syncthreads();
-  const int use_p = use_p_s;
-  const float inv_st = (float)(1.0 / st.St), inv_sd = (float)(1.0 / st.Sd);
-  const long row = (long)(c0 + st.rej) * a.vocab;
-  const T *tr = (const T *)a.target + row;
-  const T *dr = (const T *)a.draft + row;
-  const int v0 = sel_chunk * kResChunk + threadIdx.x * kResPer;
+  const int v0 = sel_s * kResChunk + threadIdx.x * kResPer;
   float m[kResPer];
   float local = 0.f;
 #pragma unroll
@@ -364,17 +447,13 @@ residual_draw_kernel(const __grid_constant__ AcceptArgs a) {
     const int v = v0 + i;
     float r = 0.f, p = 0.f;
     if (v < a.vocab) res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st, inv_st, inv_sd, r, p);
-    m[i] = use_p ? p : r;
+    m[i] = use_p_s ? p : r;
     local += m[i];
   }
-  wsum[threadIdx.x] = (double)local;
-  __syncthreads();
-  if (threadIdx.x == 0) {   // exclusive prefix of thread totals, in order
-    double run = 0.0;
-    for (int i = 0; i < kThreads; ++i) { const double x = wsum[i]; wsum[i] = run; run += x; }
-  }
-  __syncthreads();
-  const double U = U_s, base = base_s + wsum[threadIdx.x];
+  Ff total;
+  const Ff excl = block_excl_scan(ff_of(local), warp_tot, total);
+  const Ff base = ff_add(base_s, excl);
+  const Ff U = U_s;
   float lp = 0.f;
   int first = 0x7fffffff, last_pos = -1;
 #pragma unroll
@@ -382,13 +461,13 @@ residual_draw_kernel(const __grid_constant__ AcceptArgs a) {
     lp += m[i];
     if (m[i] > 0.f) {
       last_pos = v0 + i;
-      if (first == 0x7fffffff && base + (double)lp > U) first = v0 + i;
+      if (first == 0x7fffffff && ff_gt(ff_add(base, ff_of(lp)), U)) first = v0 + i;
     }
   }
   if (first != 0x7fffffff) atomicMin(&best_s, first);
-  if (last_pos >= 0) atomicMax(&last_pos_s, last_pos);
+  if (last_pos >= 0) atomicMax(&lastpos_s, last_pos);
   __syncthreads();
-  if (threadIdx.x == 0) a.token[b] = best_s != 0x7fffffff ? best_s : last_pos_s;
+  if (threadIdx.x == 0) a.token[b] = best_s != 0x7fffffff ? best_s : lastpos_s;
 }
 
 void mark(void *const *events, int i, cudaStream_t stream) {
@@ -399,14 +478,10 @@ template <typename T>
 cudaError_t launch_all(const AcceptArgs &a, int total_B, cudaStream_t stream,
                        void *const *events) {
   mark(events, 0, stream);
-  lse_kernel<T><<<dim3(a.lse_chunks, total_B), kThreads, 0, stream>>>(a);
+  lse_walk_kernel<T><<<dim3(a.lse_chunks, total_B), kThreads, 0, stream>>>(a);
   mark(events, 1, stream);
-  walk_kernel<T><<<a.batch, kThreads, 0, stream>>>(a);
+  residual_kernel<T><<<dim3(a.res_chunks, a.batch), kThreads, 0, stream>>>(a);
   mark(events, 2, stream);
-  residual_sum_kernel<T><<<dim3(a.res_chunks, a.batch), kThreads, 0, stream>>>(a);
-  mark(events, 3, stream);
-  residual_draw_kernel<T><<<a.batch, kThreads, 0, stream>>>(a);
-  mark(events, 4, stream);
   return cudaGetLastError();
 }
 
@@ -476,7 +551,7 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream_ptr,
     return SIMSD_ERR_WORKSPACE;
   cudaStream_t stream = (cudaStream_t)stream_ptr;
   char *ws = (char *)d->workspace;
-  if (cudaMemsetAsync(ws + w.off_status, 0, sizeof(uint32_t), stream) != cudaSuccess)
+  if (cudaMemsetAsync(ws + w.off_status, 0, w.status_bytes, stream) != cudaSuccess)
     return SIMSD_ERR_CUDA;
   AcceptArgs a;
   a.target = d->target_logits;
@@ -490,7 +565,7 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream_ptr,
   a.pos = d->pos;
   a.lse_part = (float4 *)(ws + w.off_lse);
   a.state = (WalkState *)(ws + w.off_state);
-  a.res_part = (double2 *)(ws + w.off_res);
+  a.res_part = (float4 *)(ws + w.off_res);
   a.status = (uint32_t *)(ws + w.off_status);
   a.batch = d->batch;
   a.vocab = d->vocab;
@@ -520,7 +595,7 @@ simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream_ptr) 
   char *ws = nullptr;
   if (static_scratch(&ws) != cudaSuccess) return SIMSD_ERR_CUDA;
   cudaStream_t stream = (cudaStream_t)stream_ptr;
-  if (cudaMemsetAsync(ws + w.off_status, 0, sizeof(uint32_t), stream) != cudaSuccess)
+  if (cudaMemsetAsync(ws + w.off_status, 0, w.status_bytes, stream) != cudaSuccess)
     return SIMSD_ERR_CUDA;
   AcceptArgs a;
   a.target = d->target_logits;
@@ -534,7 +609,7 @@ simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream_ptr) 
   a.pos = d->pos;
   a.lse_part = (float4 *)(ws + w.off_lse);
   a.state = (WalkState *)(ws + w.off_state);
-  a.res_part = (double2 *)(ws + w.off_res);
+  a.res_part = (float4 *)(ws + w.off_res);
   a.status = (uint32_t *)(ws + w.off_status);
   a.batch = d->batch;
   a.vocab = d->vocab;

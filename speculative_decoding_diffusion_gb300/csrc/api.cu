@@ -26,6 +26,44 @@ int device_sm_count() {
   return n;
 }
 
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                  void *, const cuuint64_t *, const cuuint64_t *,
+                                  const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)kPageTokens, (cuuint64_t)Hkv,
+                        (cuuint64_t)num_pages};
+  cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)kPageTokens * hd * 2,
+                           (cuuint64_t)Hkv * kPageTokens * hd * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)kPageTokens, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+
 void make_rope_table(float base, int hd, RopeTable *t) {
   memset(t, 0, sizeof(*t));
   for (int d = 0; d < hd / 2 && d < 64; ++d)
@@ -51,28 +89,32 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
   p->M_max = 2 * d->B_max * p->G;
   p->esize = d->dtype == SIMSD_BF16 ? 2 : 4;
   if (d->dtype == SIMSD_BF16) {
-    // 8 consumer warps; each owns 16 query rows, warps beyond the rows
-    // split every stage's keys among themselves.
-    int groups = (p->M_max + 15) / 16;
-    int rg = 1;
-    while (rg < groups && rg < 8) rg *= 2;
-    p->rows_per_tile = rg * 16;
-    p->key_splits = 8 / rg;
+    p->rows_per_tile = 128;   // the tensor-core tile's M; smaller tiles are padded
+    p->key_splits = 1;
   } else {
     p->rows_per_tile = p->M_max;
     p->key_splits = 1;
   }
   p->row_tiles = (p->M_max + p->rows_per_tile - 1) / p->rows_per_tile;
-  // Split the key range so the grid covers the GPU a few times over, but
-  // no split is longer than 4096 keys (balance for ragged batches).
+  // Split each sequence's keys into `splits` ranges of whole 128-key blocks.
+  // Cost model in block-times for one CTA per SM: waves x (blocks per CTA +
+  // fixed per-CTA cost ~1.5 blocks + 1 block of partial-output traffic when
+  // split) + the merge's read of the partials.  The longest possible
+  // sequence (the block-table width) stands for every sequence.
   const int64_t max_keys = (int64_t)d->max_pages_per_seq * kPageTokens;
   const int64_t max_blocks = (max_keys + kBlockKeys - 1) / kBlockKeys;
   const int64_t pairs = (int64_t)d->batch * d->num_kv_heads * p->row_tiles;
-  int64_t splits = (4 * (int64_t)device_sm_count() + pairs - 1) / pairs;
-  int64_t by_len = (max_keys + 4095) / 4096;
-  if (splits < by_len) splits = by_len;
-  if (splits > max_blocks) splits = max_blocks;
-  if (splits < 1) splits = 1;
+  const int64_t sms = device_sm_count();
+  int64_t splits = 1;
+  double best = 1e300;
+  for (int64_t s = 1; s <= max_blocks && s <= 64; ++s) {
+    const int64_t per = (max_blocks + s - 1) / s;
+    if (s > 1 && (max_blocks + per - 1) / per < s) continue;   // same split as a smaller s
+    const double waves = (double)((pairs * s + sms - 1) / sms);
+    const double cost = waves * ((double)per + 1.5 + (s > 1 ? 1.0 : 0.0)) +
+                        (s > 1 ? (double)(pairs * s) / (double)sms : 0.0);
+    if (cost < best - 1e-9) { best = cost; splits = s; }
+  }
   int64_t blocks_per_split = (max_blocks + splits - 1) / splits;
   p->chunk = (int)(blocks_per_split * kBlockKeys);
   p->n_splits = (int)((max_keys + p->chunk - 1) / p->chunk);
@@ -210,7 +252,7 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   a.chunk = p.chunk;
   a.rows_per_tile = p.rows_per_tile;
   a.sm_scale = d->sm_scale;
-  cudaError_t e = d->dtype == SIMSD_BF16 ? launch_attn_bf16(d, p, a, stream)
+  cudaError_t e = d->dtype == SIMSD_BF16 ? launch_attn_tc(d, p, a, stream)
                                          : launch_attn_f32(d, p, a, stream);
   if (e != cudaSuccess || !mark(events, 2, stream)) return SIMSD_ERR_CUDA;
   if (p.n_splits > 1 && launch_combine(d, p, a, tok_seq, stream) != cudaSuccess)

@@ -403,42 +403,6 @@ attn_bf16_kernel(const __grid_constant__ CUtensorMap tmK,
   named_sync(2, kThreads);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
-                                  void *, const cuuint64_t *, const cuuint64_t *,
-                                  const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)p;
-  }
-  return fn;
-}
-
-// Cache [num_pages][Hkv][16][hd] bf16 as a 4-D tensor (hd, slot, head, page);
-// one box is a page of one head, 64 columns wide (128 bytes, swizzled).
-bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)kPage, (cuuint64_t)Hkv,
-                        (cuuint64_t)num_pages};
-  cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)kPage * hd * 2,
-                           (cuuint64_t)Hkv * kPage * hd * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)kPage, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int HD, int KS>
 cudaError_t launch_variant(const CUtensorMap &mk, const CUtensorMap &mv,
                            const AttnParams &a, dim3 grid, cudaStream_t stream) {

@@ -1,6 +1,7 @@
 // internal.h -- host-side plan and kernel launchers of libsimsd (not ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -60,7 +61,9 @@ cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
                                cudaStream_t stream);
 cudaError_t launch_rope_append(const simsd_append_desc *d, cudaStream_t stream);
 
-// K2: split-KV masked attention.
+// K2: split-KV masked attention (tcgen05 for bf16, CUDA cores for fp32).
+cudaError_t launch_attn_tc(const simsd_verify_desc *d, const VerifyPlan &p,
+                           const AttnParams &a, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const simsd_verify_desc *d, const VerifyPlan &p,
                              const AttnParams &a, cudaStream_t stream);
 cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
@@ -73,6 +76,11 @@ cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
+
+// TMA descriptor of a paged bf16 cache [num_pages][Hkv][16][hd] as the 4-D
+// tensor (hd, slot, head, page); one box = one page of one head, 64 columns
+// (128 bytes) wide, 128-byte swizzle.  False if the driver call fails.
+bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd);
 
 // RoPE inverse frequencies base^(-2d/hd), d < hd/2, computed in double.
 struct RopeTable {
