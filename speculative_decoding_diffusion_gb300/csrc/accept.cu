@@ -16,10 +16,14 @@
 //   K4b  grid (residual chunk, sequence): per-chunk residual mass of the
 //        rejected slot only; the last CTA of a sequence takes the prefix over
 //        chunks and draws the token inside the selected chunk.
-// Numerics: exponentials are taken relative to a row maximum in logit units
-// (x - max is exact for bf16); normalisers, chunk sums and running CDFs are
-// compensated fp32 pairs (two-sum), never fp64 (GB300's fp64 rate is a small
-// fraction of its fp32 rate).  The residual CDF is then within ~1e-6
+// Numerics: a partial state is (R, s) with R a reference in log2 units (the
+// maximum of x log2 e seen so far, rounded once) and s = sum 2^(x log2 e - R),
+// each exponent argument formed by one fma (a single rounding, small for
+// the entries near the maximum that carry the mass) and exponentiated by
+// the MUFU ex2 instruction; references of different partials differ by
+// exactly representable amounts.  Normalisers, chunk sums and running CDFs
+// are compensated fp32 pairs (two-sum), never fp64 (GB300's fp64 rate is a
+// small fraction of its fp32 rate).  The residual CDF is then within ~1e-6
 // (absolute probability mass) of the exact one.
 #include <mutex>
 
@@ -63,8 +67,8 @@ __device__ __forceinline__ bool ff_gt(Ff a, Ff u) {
   return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
 }
 
-// Per sequence, after the walk: rejected slot (-1: none), that slot's row
-// maxima and normalisers.
+// Per sequence, after the walk: rejected slot (-1: none), that slot's
+// references (log2 units) and normalisers.
 struct WalkState {
   int rej;
   float Mt, Md, St, Sd;
@@ -102,27 +106,39 @@ struct AcceptArgs {
   int32_t *n_accept;
   int32_t *token;
   int32_t *pos;
-  float4 *lse_part;     // [total_B][lse_chunks]: (M_t, s_t, M_d, s_d)
+  float4 *lse_part;     // [total_B][lse_chunks]: (R_t, s_t, R_d, s_d)
   WalkState *state;     // [batch]
   float4 *res_part;     // [batch][res_chunks]: residual pair, target-mass pair
   uint32_t *status;     // [0]: status word; [1..batch]: K4a counters; then K4b's
   int batch, vocab, B_max, lse_chunks, res_chunks, vec_ok;
 };
 
-// (M, s) with s = sum 2^((x - M) log2 e): merge two partial states.
+// 2^x on the MUFU (approximate, ~2 ulp; subnormal results flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2^(x log2 e - R): the argument rounded once.
+__device__ __forceinline__ float rel_exp(float x, float R) { return ex2(fmaf(x, kLog2e, -R)); }
+
+// (R, s) with s = sum 2^(x log2 e - R): merge two partial states.
 __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
   const float mm = fmaxf(m, m2);
   if (mm == -INFINITY) { m = mm; s = 0.f; return; }
-  s = s * exp2f((m - mm) * kLog2e) + s2 * exp2f((m2 - mm) * kLog2e);
+  s = s * ex2(m - mm) + s2 * ex2(m2 - mm);
   m = mm;
 }
 
+// Fold n logits into (R, s); R moves to the new maximum (in log2 units).
 __device__ __forceinline__ void accum(float &m, float &s, const float *x, int n) {
   float mx = -INFINITY;
   for (int i = 0; i < n; ++i) mx = fmaxf(mx, x[i]);
-  if (mx > m) { s *= exp2f((m - mx) * kLog2e); m = mx; }
+  const float R = mx * kLog2e;
+  if (R > m) { s *= ex2(m - R); m = R; }
   if (m == -INFINITY) return;
-  for (int i = 0; i < n; ++i) s += exp2f((x[i] - m) * kLog2e);
+  for (int i = 0; i < n; ++i) s += rel_exp(x[i], m);
 }
 
 template <typename T> struct Ld;
@@ -173,7 +189,7 @@ __device__ __forceinline__ void block_lse(float &m, float &s, float2 *scratch) {
     Ff S = ff_of(0.f);
     if (M != -INFINITY)
       for (int i = 0; i < kThreads / 32; ++i)
-        S = ff_add(S, ff_of(scratch[i].y * exp2f((scratch[i].x - M) * kLog2e)));
+        S = ff_add(S, ff_of(scratch[i].y * ex2(scratch[i].x - M)));
     m = M;
     s = S.hi + S.lo;
   }
@@ -197,8 +213,8 @@ __device__ __forceinline__ void row_norm(const float4 *pp, int chunks, int lane,
   Ff st = ff_of(0.f), sd = ff_of(0.f);
   for (int c = lane; c < chunks; c += 32) {
     const float4 v = __ldcg(pp + c);
-    if (v.y > 0.f) st = ff_add(st, ff_of(v.y * exp2f((v.x - mt) * kLog2e)));
-    if (v.w > 0.f) sd = ff_add(sd, ff_of(v.w * exp2f((v.z - md) * kLog2e)));
+    if (v.y > 0.f) st = ff_add(st, ff_of(v.y * ex2(v.x - mt)));
+    if (v.w > 0.f) sd = ff_add(sd, ff_of(v.w * ex2(v.z - md)));
   }
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) {
@@ -224,8 +240,8 @@ __device__ void walk(const AcceptArgs &a, int b, int c0, int B) {
       if (x < 0 || x >= a.vocab) { raise_status(a.status, kStatusBadInput); x = 0; }
       const float tx = Ld<T>::one((const T *)a.target + row + x);
       const float dx = Ld<T>::one((const T *)a.draft + row + x);
-      px_s[k] = exp2f((tx - Mt) * kLog2e) / St;
-      qx_s[k] = exp2f((dx - Md) * kLog2e) / Sd;
+      px_s[k] = rel_exp(tx, Mt) / St;
+      qx_s[k] = rel_exp(dx, Md) / Sd;
       ws_s[k] = WalkState{k, Mt, Md, St, Sd};
     }
   }
@@ -329,8 +345,8 @@ lse_walk_kernel(const __grid_constant__ AcceptArgs a) {
 // Residual mass r = max(0, p - q) and target mass p of one entry.
 __device__ __forceinline__ void res_pair(float t, float d, const WalkState &st,
                                          float inv_st, float inv_sd, float &r, float &p) {
-  p = exp2f((t - st.Mt) * kLog2e) * inv_st;
-  const float q = exp2f((d - st.Md) * kLog2e) * inv_sd;
+  p = rel_exp(t, st.Mt) * inv_st;
+  const float q = rel_exp(d, st.Md) * inv_sd;
   r = fmaxf(p - q, 0.f);
 }
 

@@ -9,18 +9,22 @@
 // One CTA per (key split, KV head x 128-row tile, sequence).  The query tile
 // stacks the 2B tokens x G query heads of one KV head (row = token*G + head
 // in group; rows past 2B*G are zero padding), so each key/value byte read
-// from HBM serves every row.  Warp roles:
-//   warp 0     TMA producer: 128-key blocks (8 pages) of K and V, one 2 KB
-//              box per page and 64-column half (128-byte swizzle), into a
-//              2-stage ring;
-//   warp 1     TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into a
-//              double-buffered TMEM tile (128 x 128 fp32), O += P_j V_j into
-//              a TMEM accumulator (128 x hd fp32); completion by commit;
-//   warps 2-5  softmax, one thread per query row: S_j from TMEM, scale,
-//              mask, running max with an 8 (log2) headroom -- O is rescaled
-//              in TMEM only when a row's maximum outgrows it, which keeps
-//              the result exact (O and l share the stale reference) -- P_j as
-//              bf16 into a 128B-swizzled shared tile, and the epilogue.
+// from HBM serves every row.  The CTA's keys come in 64-key blocks dealt
+// alternately to two independent streams, each with its own score tile S,
+// probability tile P and output accumulator O (and running max / sum); the
+// two are merged in the epilogue.  Warp roles:
+//   warp 0     TMA producer: K and V of each block (4 pages, one 2 KB box
+//              per page and 64-column half, 128-byte swizzle) into a
+//              4-stage ring;
+//   warp 1     TMEM owner and MMA issuer (one thread): S = Q K^T into the
+//              stream's TMEM tile (128 x 64 fp32), O += P V into the stream's
+//              TMEM accumulator (128 x hd fp32); completion by commit;
+//   warps 2-5  softmax of stream 0, warps 6-9 of stream 1, one thread per
+//              query row: S from TMEM, scale, mask, running max with an 8
+//              (log2) headroom -- O is rescaled in TMEM only when a row's
+//              maximum outgrows it, which keeps the result exact (O and l
+//              share the stale reference) -- and P as bf16 into a 128-byte
+//              swizzled shared tile.
 // Q is staged once into shared memory in the same swizzled K-major layout.
 // Every mbarrier wait is bounded; a wait that runs out sets the status word
 // and the CTA drains and returns.
@@ -33,43 +37,62 @@
 namespace simsd {
 namespace {
 
-constexpr int kRows = 128;         // query rows per CTA: the MMA's M
-constexpr int kKeys = kBlockKeys;  // keys per block: S width, P.V depth
-constexpr int kStages = 2;
-constexpr int kWarps = 6;
+constexpr int kRows = 128;           // query rows per CTA: the MMA's M
+constexpr int kKeys = 64;            // keys per block: S width, P.V depth
+constexpr int kPagesPerBlock = kKeys / kPage;
+constexpr int kStages = 4;
+constexpr int kStreams = 2;
+constexpr int kWarps = 2 + 4 * kStreams;
 constexpr int kThreads = kWarps * 32;
-constexpr uint32_t kTmemCols = 512;  // S0 [0,128) S1 [128,256) O [256,256+hd)
-constexpr uint32_t kColO = 256;
+constexpr uint32_t kColO = kStreams * kKeys;   // O accumulators after the S tiles
 constexpr int kBoxBytes = kPage * 128;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kHeadroom = 8.f;   // log2 units a row max may grow before O is rescaled
+constexpr float kHeadroom = 8.f;     // log2 units a row max may grow before O is rescaled
 
-enum { kBarKvFull = 0, kBarKvEmpty = 2, kBarSFull = 4, kBarSEmpty = 6, kBarPFull = 8,
-       kBarPvDone = 9, kNumBars = 10 };
+enum { kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarSFull = kBarKvEmpty + kStages,
+       kBarSEmpty = kBarSFull + kStreams, kBarPFull = kBarSEmpty + kStreams,
+       kBarPvDone = kBarPFull + kStreams, kNumBars = kBarPvDone + kStreams };
 
 template <int HD>
 struct TcSmem {
   static constexpr int kHalves = HD / 64;
-  static constexpr int kHalfRows = kRows * 128;        // one 64-column half of Q or P
+  static constexpr int kHalfRows = kRows * 128;        // one 64-column half of a 128-row tile
   static constexpr int kQ = kHalves * kHalfRows;
-  static constexpr int kP = 2 * kHalfRows;              // 128 keys = two halves
-  static constexpr int kKvHalf = kKeys * 128;
+  static constexpr int kP = kHalfRows;                  // 64 keys: one half
+  static constexpr int kKvHalf = kKeys * 128;           // 64 keys x 64 columns
   static constexpr int kKv = kHalves * kKvHalf;         // K or V tile of a block
   static constexpr int kStage = 2 * kKv;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + kQ;
-  static constexpr int kOffKv = kOffP + kP;
+  static constexpr int kOffP = kOffQ + kQ;              // kStreams tiles
+  static constexpr int kOffKv = kOffP + kStreams * kP;
   static constexpr int kOffBar = kOffKv + kStages * kStage;
   static constexpr int kOffTau = kOffBar + kNumBars * 8;
-  static constexpr int kOffMisc = kOffTau + 2 * kMaxB * 4;  // tmem address, error flag
+  static constexpr int kOffMl = kOffTau + 2 * kMaxB * 4;    // stream 1's (m, l) per row
+  static constexpr int kOffMisc = kOffMl + kRows * 8;       // tmem address, error flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;              // 1024-byte alignment slack
+  static constexpr uint32_t kTmemCols = (kColO + kStreams * HD) <= 256 ? 256 : 512;
 };
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   // byte offset of 16-byte chunk `chunk` (0..7) of `row` in a 128-byte
-  // swizzled half tile whose base is 1024-byte aligned
+  // swizzled tile whose base is 1024-byte aligned
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Visibility of key `key` (0..Lk-1) for a new row (token index tok of the
+// 2B, slot row or data row, step label ti); tau of the new tokens in tau_s.
+__device__ __forceinline__ bool visible(int key, int P, int B, const int *tau_s, bool row_slot,
+                                        int ti) {
+  if (key < P) return true;
+  const int jj = key - P;
+  const int tj = tau_s[jj];
+  const bool key_slot = jj >= B;
+  return row_slot ? (key_slot ? tj >= ti : tj < ti) : (!key_slot && tj <= ti);
 }
 
 template <int HD>
@@ -84,6 +107,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const uint32_t sQ = base + L::kOffQ, sP = base + L::kOffP, sKv = base + L::kOffKv;
   auto bar = [&](int i) { return base + L::kOffBar + 8u * i; };
   int *tau_s = reinterpret_cast<int *>(sb + L::kOffTau);
+  float2 *ml_s = reinterpret_cast<float2 *>(sb + L::kOffMl);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + L::kOffMisc);
   int *flag_s = reinterpret_cast<int *>(sb + L::kOffMisc + 4);
 
@@ -112,21 +136,24 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kBarKvFull + i), 1);
       mbar_init(bar(kBarKvEmpty + i), 1);
+    }
+    for (int i = 0; i < kStreams; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSEmpty + i), 4);
+      mbar_init(bar(kBarPFull + i), 4);
+      mbar_init(bar(kBarPvDone + i), 1);
     }
-    mbar_init(bar(kBarPFull), 4);
-    mbar_init(bar(kBarPvDone), 1);
     *flag_s = 0;
     fence_barrier_init();
   }
   for (int j = threadIdx.x; j < 2 * B; j += kThreads)
     tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
   if (warp == 1) {
-    tc::alloc(smem_u32(tmem_slot), kTmemCols);
+    tc::alloc(smem_u32(tmem_slot), L::kTmemCols);
     tc::relinquish();
   }
-  // Q tile -> shared memory, K-major with the 128-byte swizzle
+  // Q tile -> shared memory (K-major, 128-byte swizzle); P tiles zeroed
+  // once, so padding rows (never written again) hold zeros
   {
     const __nv_bfloat16 *q = (const __nv_bfloat16 *)a.q_rot;
     constexpr int CH = HD / 8;
@@ -140,6 +167,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       }
       *reinterpret_cast<uint4 *>(sb + L::kOffQ + (c >> 3) * L::kHalfRows + swz(r, c & 7)) = v;
     }
+    for (int e = threadIdx.x; e < kStreams * L::kP / 16; e += kThreads)
+      reinterpret_cast<uint4 *>(sb + L::kOffP)[e] = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async_smem();
   tc::fence_before_sync();
@@ -153,14 +182,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
     int issued = 0;
     for (int j = 0; j < n_blocks; ++j) {
-      const int s = j & 1;
-      if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j >> 1) - 1) & 1)) {
+      const int s = j % kStages;
+      const int kb = k_begin + j * kKeys;
+      const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
+      const int page = lane < n_pages ? __ldg(bt + kb / kPage + lane) : 0;   // before the wait
+      if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1)) {
         if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
         break;
       }
-      const int kb = k_begin + j * kKeys;
-      const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
-      const int page = lane < n_pages ? __ldg(bt + kb / kPage + lane) : 0;
       if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + s), n_pages * L::kHalves * 2 * kBoxBytes);
       __syncwarp();
       if (lane < n_pages) {
@@ -177,7 +206,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (*(volatile int *)flag_s) {
       // let copies already in flight land before the CTA can exit
       for (int j = max(0, issued - kStages); j < issued; ++j)
-        (void)mbar_wait_warp(bar(kBarKvFull + (j & 1)), (j >> 1) & 1);
+        (void)mbar_wait_warp(bar(kBarKvFull + j % kStages), (j / kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -188,10 +217,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
       ok = false;
     };
+    // S of block j into its stream's score tile
     auto issue_s = [&](int j) {
-      const int s = j & 1;
-      if (!mbar_wait_warp(bar(kBarKvFull + s), (j >> 1) & 1)) { fail(); return; }
-      if (j >= kStages && !mbar_wait_warp(bar(kBarSEmpty + s), ((j >> 1) - 1) & 1)) { fail(); return; }
+      const int s = j % kStages, st = j & 1;
+      if (!mbar_wait_warp(bar(kBarKvFull + s), (j / kStages) & 1)) { fail(); return; }
+      if (j >= kStreams && !mbar_wait_warp(bar(kBarSEmpty + st), ((j >> 1) - 1) & 1)) { fail(); return; }
       tc::fence_after_sync();
       if (lane == 0) {
         const uint32_t kt = sKv + s * L::kStage;
@@ -199,22 +229,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t qa = sQ + (kk >> 2) * L::kHalfRows + (kk & 3) * 32;
           const uint32_t ka = kt + (kk >> 2) * L::kKvHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + s * kKeys, tc::smem_desc_sw128(qa, 16, 1024),
+          tc::mma_bf16(tmem + st * kKeys, tc::smem_desc_sw128(qa, 16, 1024),
                        tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
         }
-        tc::commit(bar(kBarSFull + s));
+        tc::commit(bar(kBarSFull + st));
       }
       __syncwarp();
     };
-    issue_s(0);
+    for (int j = 0; j < kStreams && j < n_blocks && ok; ++j) issue_s(j);
     for (int j = 0; j < n_blocks && ok; ++j) {
-      if (j + 1 < n_blocks) {
-        issue_s(j + 1);
+      if (j + kStreams < n_blocks) {
+        issue_s(j + kStreams);
         if (!ok) break;
       }
-      if (!mbar_wait_warp(bar(kBarPFull), j & 1)) { fail(); break; }
+      const int st = j & 1, s = j % kStages;
+      if (!mbar_wait_warp(bar(kBarPFull + st), (j >> 1) & 1)) { fail(); break; }
       tc::fence_after_sync();
-      const int s = j & 1;
       const int kb = k_begin + j * kKeys;
       const int valid = min(kKeys, k_end - kb);
       const int loaded = (valid + kPage - 1) & ~(kPage - 1);
@@ -232,152 +262,159 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       }
       __syncwarp();
       if (lane == 0) {
-        for (int kk = 0; kk < loaded / 16; ++kk) {
-          const uint32_t pa = sP + (kk >> 2) * L::kHalfRows + (kk & 3) * 32;
-          const uint32_t va = vt + kk * 2048;
-          tc::mma_bf16(tmem + kColO, tc::smem_desc_sw128(pa, 16, 1024),
-                       tc::smem_desc_sw128(va, L::kKvHalf, 1024), idO, (j > 0 || kk > 0));
-        }
-        tc::commit(bar(kBarPvDone));
+        const uint32_t pt = sP + st * L::kP;
+        for (int kk = 0; kk < loaded / 16; ++kk)
+          tc::mma_bf16(tmem + kColO + st * HD, tc::smem_desc_sw128(pt + kk * 32, 16, 1024),
+                       tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
+                       (j >= kStreams || kk > 0));
+        tc::commit(bar(kBarPvDone + st));
         tc::commit(bar(kBarKvEmpty + s));
       }
       __syncwarp();
     }
   } else {
     // ---------------------------------------------------------- softmax
+    const int st = (warp - 2) >> 2;          // stream of this warpgroup
     const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
     const int r = 32 * q4 + lane;            // query row within the tile
     const int grow = row0 + r;
     const bool row_valid = grow < M;
+    const bool warp_valid = row0 + 32 * q4 < M;
     const int tok = row_valid ? grow / a.G : 0;
     const bool row_slot = tok >= B;
     const int row_tau = tau_s[tok];
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t tS = trow + st * kKeys, tO = trow + kColO + st * HD;
     const float scale = a.sm_scale * kLog2e;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_blocks; ++j) {
-      const int s = j & 1;
-      if (!mbar_wait_warp(bar(kBarSFull + s), (j >> 1) & 1)) {
-        if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
-        ok = false;
-        break;
-      }
+    int i = 0;                               // blocks of this stream so far
+    for (int j = st; j < n_blocks; j += kStreams, ++i) {
+      if (!mbar_wait_warp(bar(kBarSFull + st), i & 1)) { ok = false; break; }
       tc::fence_after_sync();
       uint32_t sr[kKeys];
-#pragma unroll
-      for (int c = 0; c < kKeys / 32; ++c) tc::ld32(trow + s * kKeys + 32 * c, sr + 32 * c);
-      tc::wait_ld();
+      if (warp_valid) {
+        tc::ld32(tS, sr);
+        tc::ld32(tS + 32, sr + 32);
+        tc::wait_ld();
+      }
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSEmpty + s));
+      if (lane == 0) mbar_arrive(bar(kBarSEmpty + st));
       const int kb = k_begin + j * kKeys;
-      const bool no_mask = kb + kKeys <= min(P, k_end);
       float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        float v = __uint_as_float(sr[c]) * scale;
-        if (!no_mask) {
-          const int key = kb + c;
-          bool vis = key < k_end;
-          if (vis && key >= P) {
-            const int jj = key - P;            // 0..2B-1 among the new tokens
-            const int tj = tau_s[jj];
-            const bool key_slot = jj >= B;
-            vis = row_slot ? (key_slot ? tj >= row_tau : tj < row_tau)
-                           : (!key_slot && tj <= row_tau);
+      if (warp_valid) {
+        // visibility of the block's keys as a bit mask (all ones unless the
+        // block reaches past the prompt or the split's end)
+        uint64_t vis = ~0ull;
+        if (kb + kKeys > min(P, k_end)) {
+          vis = 0;
+          for (int c = 0; c < kKeys; ++c) {
+            const int key = kb + c;
+            if (key < k_end && visible(key, P, B, tau_s, row_slot, row_tau)) vis |= 1ull << c;
           }
-          if (!vis) v = -INFINITY;
         }
-        sr[c] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) {
+          float v = __uint_as_float(sr[c]) * scale;
+          if (!((vis >> c) & 1ull)) v = -INFINITY;
+          sr[c] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
       }
       // reference maximum: moves only when this block's max outgrows it
       const bool move = row_valid && mx > m_ref + kHeadroom;
       const float m_new = move ? mx : m_ref;
       const float alpha = move ? exp2f(m_ref - m_new) : 1.f;   // m_ref = -inf -> 0
-      if (j > 0) {
-        // P_{j-1}.V must be done: P's buffer is reused and O may be rescaled
-        if (!mbar_wait_warp(bar(kBarPvDone), (j - 1) & 1)) {
-          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
-          ok = false;
-          break;
-        }
+      if (i > 0) {
+        // this stream's previous P.V must be done: its P tile is reused and
+        // O may be rescaled
+        if (!mbar_wait_warp(bar(kBarPvDone + st), (i - 1) & 1)) { ok = false; break; }
         tc::fence_after_sync();
         if (__any_sync(0xffffffffu, move)) {
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t o[32];
-            tc::ld32(trow + kColO + 32 * c, o);
+            tc::ld32(tO + 32 * c, o);
             tc::wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tc::st32(trow + kColO + 32 * c, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::st32(tO + 32 * c, o);
           }
           tc::wait_st();
         }
       }
       l *= alpha;
       m_ref = m_new;
-      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      // P row (bf16) into the swizzled shared tile, keys as the K dimension
-      uint8_t *prow = sb + L::kOffP;
-      float rs = 0.f;
+      if (row_valid) {
+        // P row (bf16) into the swizzled tile: keys are the K dimension
+        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+        uint8_t *prow = sb + L::kOffP + st * L::kP;
+        float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < kKeys / 8; ++c) {
-        uint32_t w[4];
+        for (int c = 0; c < kKeys / 8; ++c) {
+          uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float p0 = 0.f, p1 = 0.f;
-          if (row_valid) {
-            p0 = exp2f(__uint_as_float(sr[8 * c + 2 * i]) - mu);
-            p1 = exp2f(__uint_as_float(sr[8 * c + 2 * i + 1]) - mu);
+          for (int e = 0; e < 4; ++e) {
+            const float p0 = exp2f(__uint_as_float(sr[8 * c + 2 * e]) - mu);
+            const float p1 = exp2f(__uint_as_float(sr[8 * c + 2 * e + 1]) - mu);
+            rs += p0 + p1;
+            w[e] = pack_bf16x2(p0, p1);
           }
-          rs += p0 + p1;
-          w[i] = pack_bf16x2(p0, p1);
+          *reinterpret_cast<uint4 *>(prow + swz(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4 *>(prow + (c >> 3) * L::kHalfRows + swz(r, c & 7)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        l += rs;
       }
-      l += rs;
       fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull));
+      if (lane == 0) mbar_arrive(bar(kBarPFull + st));
     }
-    // -------------------------------------------------------- epilogue
-    if (ok && !mbar_wait_warp(bar(kBarPvDone), (n_blocks - 1) & 1)) {
-      if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
-      ok = false;
-    }
+    if (ok && i > 0 && !mbar_wait_warp(bar(kBarPvDone + st), (i - 1) & 1)) ok = false;
+    if (!ok && lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
     tc::fence_after_sync();
-    if (ok) {
-      const bool failed = *(volatile int *)flag_s != 0;
+    // -------------------------------------------------------- epilogue
+    // stream 1 hands its (m, l) to stream 0, which merges the two O tiles
+    if (st == 1) ml_s[r] = make_float2(m_ref, l);
+    tc::fence_before_sync();                 // stream 1's O reads/waits before the sync
+    named_sync(1, 4 * kStreams * 32);
+    tc::fence_after_sync();
+    const bool failed = *(volatile int *)flag_s != 0;
+    if (st == 0 && warp_valid) {
+      const bool has1 = n_blocks > 1;        // stream 1 saw at least one block
+      const float2 ml1 = has1 ? ml_s[r] : make_float2(-INFINITY, 0.f);
+      const float mm = fmaxf(m_ref, ml1.x);
+      const float mu = mm == -INFINITY ? 0.f : mm;
+      const float f0 = exp2f(m_ref - mu), f1 = has1 ? exp2f(ml1.x - mu) : 0.f;
+      const float lt = l * f0 + ml1.y * f1;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const long orow = (2L * c0 + tok) * a.Hq + kvh * a.G + (row_valid ? grow % a.G : 0);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
-        uint32_t o[32];
-        tc::ld32(trow + kColO + 32 * c, o);
+        uint32_t o0[32], o1[32];
+        tc::ld32(trow + kColO + 32 * c, o0);
+        if (has1) tc::ld32(trow + kColO + HD + 32 * c, o1);
         tc::wait_ld();
         if (!row_valid || failed) continue;
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          v[e] = __uint_as_float(o0[e]) * f0 + (has1 ? __uint_as_float(o1[e]) * f1 : 0.f);
         if (n_splits_b == 1) {
           uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)a.out + orow * HD + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(
-                pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv, __uint_as_float(o[8 * i + 1]) * inv),
-                pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv),
-                pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv),
-                pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pack_bf16x2(v[8 * e] * inv, v[8 * e + 1] * inv),
+                                pack_bf16x2(v[8 * e + 2] * inv, v[8 * e + 3] * inv),
+                                pack_bf16x2(v[8 * e + 4] * inv, v[8 * e + 5] * inv),
+                                pack_bf16x2(v[8 * e + 6] * inv, v[8 * e + 7] * inv));
         } else {
           const long prow = (long)split * a.T * a.Hq + orow;
           float4 *dst = reinterpret_cast<float4 *>(a.o_part + prow * HD + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                                 __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
-          if (c == 0) a.ml_part[prow] = make_float2(m_ref, l);
+          for (int e = 0; e < 8; ++e)
+            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+          if (c == 0) a.ml_part[prow] = make_float2(mm, lt);
         }
       }
     }
@@ -387,7 +424,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::dealloc(tmem, kTmemCols);
+    tc::dealloc(tmem, L::kTmemCols);
   }
 }
 
