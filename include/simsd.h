@@ -122,7 +122,7 @@ typedef struct {
   int32_t B_max;              /* max_b B_b (host copy), 1..32               */
   simsd_dtype dtype;
   float rope_base;            /* RoPE base (e.g. 1e6)                       */
-  float sm_scale;             /* score = sm_scale * q.k                     */
+  float sm_scale;             /* score = sm_scale * q.k; finite, > 0        */
   const void *q;
   void *k_cache;
   void *v_cache;

@@ -373,15 +373,41 @@ __device__ __forceinline__ Ff block_excl_scan(Ff x, Ff *warp_tot, Ff &total) {
 }
 
 // ---------------------------------------------------------------- K4b
+// The 8 residual / target masses of entries v0..v0+7 of the rejected row.
+template <typename T>
+__device__ __forceinline__ void res_block(const T *tr, const T *dr, int v0, int vocab, bool vec,
+                                          const WalkState &st, float inv_st, float inv_sd,
+                                          float *r, float *p) {
+  constexpr int N = Ld<T>::N;
+  if (vec && v0 + kResPer <= vocab) {
+    float xt[kResPer], xd[kResPer];
+#pragma unroll
+    for (int h = 0; h < kResPer / N; ++h) {
+      Ld<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(tr + v0 + h * N)), xt + h * N);
+      Ld<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(dr + v0 + h * N)), xd + h * N);
+    }
+#pragma unroll
+    for (int i = 0; i < kResPer; ++i) res_pair(xt[i], xd[i], st, inv_st, inv_sd, r[i], p[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kResPer; ++i) {
+      r[i] = p[i] = 0.f;
+      if (v0 + i < vocab)
+        res_pair(Ld<T>::one(tr + v0 + i), Ld<T>::one(dr + v0 + i), st, inv_st, inv_sd, r[i], p[i]);
+    }
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 residual_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ Ff warp_tot[kThreads / 32];
+  __shared__ Ff warp_tot[kThreads / 32], rs[kThreads / 32], ps[kThreads / 32];
   __shared__ int last_s, sel_s, use_p_s, best_s, lastpos_s;
   __shared__ Ff base_s, U_s;
   const int chunk = blockIdx.x, b = blockIdx.y;
   const WalkState st = a.state[b];
   if (st.rej < 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float inv_st = 1.f / st.St, inv_sd = 1.f / st.Sd;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
@@ -389,24 +415,19 @@ residual_kernel(const __grid_constant__ AcceptArgs a) {
   const T *tr = (const T *)a.target + row;
   const T *dr = (const T *)a.draft + row;
   {
-    const int v0 = chunk * kResChunk + threadIdx.x * kResPer;
+    float r[kResPer], p[kResPer];
+    res_block<T>(tr, dr, chunk * kResChunk + threadIdx.x * kResPer, a.vocab, a.vec_ok, st,
+                 inv_st, inv_sd, r, p);
     float sr = 0.f, sp = 0.f;
-    for (int i = 0; i < kResPer; ++i) {
-      const int v = v0 + i;
-      if (v >= a.vocab) break;
-      float r, p;
-      res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st, inv_st, inv_sd, r, p);
-      sr += r;
-      sp += p;
-    }
+#pragma unroll
+    for (int i = 0; i < kResPer; ++i) { sr += r[i]; sp += p[i]; }
     Ff fr = ff_of(sr), fp = ff_of(sp);
 #pragma unroll
     for (int w = 16; w > 0; w >>= 1) {
       fr = ff_add(fr, ff_shfl_xor(fr, w));
       fp = ff_add(fp, ff_shfl_xor(fp, w));
     }
-    __shared__ Ff rs[kThreads / 32], ps[kThreads / 32];
-    if ((threadIdx.x & 31) == 0) { rs[threadIdx.x >> 5] = fr; ps[threadIdx.x >> 5] = fp; }
+    if (lane == 0) { rs[warp] = fr; ps[warp] = fp; }
     __syncthreads();
     if (threadIdx.x == 0) {
       Ff tr_ = rs[0], tp = ps[0];
@@ -419,14 +440,20 @@ residual_kernel(const __grid_constant__ AcceptArgs a) {
   }
   if (!last_s) return;
   __threadfence();
-  // -- the last CTA of sequence b draws the token
+  // -- the last CTA of sequence b draws the token.  Warp 0 scans the chunk
+  // masses 32 at a time for the chunk whose running sum first exceeds U.
   const float4 *rp = a.res_part + (long)b * a.res_chunks;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {
     Ff S = ff_of(0.f), Sp = ff_of(0.f);
-    for (int c = 0; c < a.res_chunks; ++c) {
+    for (int c = lane; c < a.res_chunks; c += 32) {
       const float4 v = __ldcg(rp + c);
       S = ff_add(S, Ff{v.x, v.y});
       Sp = ff_add(Sp, Ff{v.z, v.w});
+    }
+#pragma unroll
+    for (int w = 16; w > 0; w >>= 1) {
+      S = ff_add(S, ff_shfl_xor(S, w));
+      Sp = ff_add(Sp, ff_shfl_xor(Sp, w));
     }
     const int use_p = !(S.hi > 0.f);         // empty residual: draw from p
     const Ff tot = use_p ? Sp : S;
@@ -434,38 +461,59 @@ residual_kernel(const __grid_constant__ AcceptArgs a) {
     const float u = __ldg(a.uniforms + (long)b * (a.B_max + 1) + B);
     const float uh = u * tot.hi;
     const Ff U = ff_add(Ff{uh, fmaf(u, tot.hi, -uh)}, ff_of(u * tot.lo));
-    // chunk c with T[c] <= U < T[c+1]; if rounding leaves U at or past the
-    // total, the last non-empty chunk
-    Ff T0 = ff_of(0.f), sel_base = ff_of(0.f), last_base = ff_of(0.f);
+    Ff carry = ff_of(0.f), last_base = ff_of(0.f), sel_base = ff_of(0.f);
     int sel = -1, last_nz = 0;
-    for (int c = 0; c < a.res_chunks; ++c) {
-      const float4 v = __ldcg(rp + c);
-      const Ff m = use_p ? Ff{v.z, v.w} : Ff{v.x, v.y};
-      const Ff T1 = ff_add(T0, m);
-      if (m.hi > 0.f) { last_nz = c; last_base = T0; }
-      if (sel < 0 && m.hi > 0.f && ff_gt(T1, U)) { sel = c; sel_base = T0; }
-      T0 = T1;
+    for (int c0_ = 0; c0_ < a.res_chunks && sel < 0; c0_ += 32) {
+      const int c = c0_ + lane;
+      Ff m = ff_of(0.f);
+      if (c < a.res_chunks) {
+        const float4 v = __ldcg(rp + c);
+        m = use_p ? Ff{v.z, v.w} : Ff{v.x, v.y};
+      }
+      Ff inc = m;                             // inclusive scan over the lanes
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const Ff y = ff_shfl_up(inc, d);
+        if (lane >= d) inc = ff_add(y, inc);
+      }
+      const Ff T1 = ff_add(carry, inc);
+      const Ff T0 = ff_add(T1, Ff{-m.hi, -m.lo});
+      const unsigned cross = __ballot_sync(0xffffffffu, m.hi > 0.f && ff_gt(T1, U));
+      const unsigned nz = __ballot_sync(0xffffffffu, m.hi > 0.f);
+      if (nz) {
+        const int hl = 31 - __clz(nz);
+        last_nz = c0_ + hl;
+        last_base = Ff{__shfl_sync(0xffffffffu, T0.hi, hl), __shfl_sync(0xffffffffu, T0.lo, hl)};
+      }
+      if (cross) {
+        const int fl = __ffs(cross) - 1;
+        sel = c0_ + fl;
+        sel_base = Ff{__shfl_sync(0xffffffffu, T0.hi, fl), __shfl_sync(0xffffffffu, T0.lo, fl)};
+      }
+      carry = Ff{__shfl_sync(0xffffffffu, T1.hi, 31), __shfl_sync(0xffffffffu, T1.lo, 31)};
     }
-    if (sel < 0) { sel = last_nz; sel_base = last_base; }
-    sel_s = sel;
-    base_s = sel_base;
-    U_s = U;
-    use_p_s = use_p;
-    best_s = 0x7fffffff;
-    lastpos_s = -1;
+    if (lane == 0) {
+      if (sel < 0) { sel = last_nz; sel_base = last_base; }
+      sel_s = sel;
+      base_s = sel_base;
+      U_s = U;
+      use_p_s = use_p;
+      best_s = 0x7fffffff;
+      lastpos_s = -1;
+    }
   }
   __syncthreads();
   const int v0 = sel_s * kResChunk + threadIdx.x * kResPer;
   float m[kResPer];
+  {
+    float r[kResPer], p[kResPer];
+    res_block<T>(tr, dr, v0, a.vocab, a.vec_ok, st, inv_st, inv_sd, r, p);
+#pragma unroll
+    for (int i = 0; i < kResPer; ++i) m[i] = use_p_s ? p[i] : r[i];
+  }
   float local = 0.f;
 #pragma unroll
-  for (int i = 0; i < kResPer; ++i) {
-    const int v = v0 + i;
-    float r = 0.f, p = 0.f;
-    if (v < a.vocab) res_pair(Ld<T>::one(tr + v), Ld<T>::one(dr + v), st, inv_st, inv_sd, r, p);
-    m[i] = use_p_s ? p : r;
-    local += m[i];
-  }
+  for (int i = 0; i < kResPer; ++i) local += m[i];
   Ff total;
   const Ff excl = block_excl_scan(ff_of(local), warp_tot, total);
   const Ff base = ff_add(base_s, excl);

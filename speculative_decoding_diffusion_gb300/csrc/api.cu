@@ -66,8 +66,11 @@ bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd) {
 
 void make_rope_table(float base, int hd, RopeTable *t) {
   memset(t, 0, sizeof(*t));
-  for (int d = 0; d < hd / 2 && d < 64; ++d)
+  for (int d = 0; d < hd / 2 && d < 64; ++d) {
     t->inv_freq[d] = pow((double)base, -2.0 * (double)d / (double)hd);
+    t->hi[d] = (float)t->inv_freq[d];
+    t->lo[d] = (float)(t->inv_freq[d] - (double)t->hi[d]);
+  }
 }
 
 static bool valid_dtype(simsd_dtype t) { return t == SIMSD_F32 || t == SIMSD_BF16; }
@@ -82,7 +85,8 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
       d->B_max > kMaxB || d->total_B < d->batch ||
       (int64_t)d->total_B > (int64_t)d->batch * d->B_max)
     return SIMSD_ERR_SHAPE;
-  if (!(d->sm_scale == d->sm_scale) || !(d->rope_base > 1.0f)) return SIMSD_ERR_SHAPE;
+  if (!(d->sm_scale > 0.0f) || !(d->sm_scale < INFINITY) || !(d->rope_base > 1.0f))
+    return SIMSD_ERR_SHAPE;
   memset(p, 0, sizeof(*p));
   p->T = 2 * d->total_B;
   p->G = d->num_q_heads / d->num_kv_heads;

@@ -80,6 +80,13 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// 2^x on the MUFU (approximate; subnormal results flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -302,30 +309,28 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSEmpty + st));
       const int kb = k_begin + j * kKeys;
-      float mx = -INFINITY;
+      float mx = -INFINITY;                  // block max of the raw scores
       if (warp_valid) {
-        // visibility of the block's keys as a bit mask (all ones unless the
-        // block reaches past the prompt or the split's end)
-        uint64_t vis = ~0ull;
         if (kb + kKeys > min(P, k_end)) {
-          vis = 0;
+          // the block reaches past the prompt or the split's end: mask it
+          uint64_t vis = 0;
           for (int c = 0; c < kKeys; ++c) {
             const int key = kb + c;
             if (key < k_end && visible(key, P, B, tau_s, row_slot, row_tau)) vis |= 1ull << c;
           }
-        }
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          float v = __uint_as_float(sr[c]) * scale;
-          if (!((vis >> c) & 1ull)) v = -INFINITY;
-          sr[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int c = 0; c < kKeys; ++c)
+            if (!((vis >> c) & 1ull)) sr[c] = __float_as_uint(-INFINITY);
         }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;   // scale > 0
       }
       // reference maximum: moves only when this block's max outgrows it
       const bool move = row_valid && mx > m_ref + kHeadroom;
       const float m_new = move ? mx : m_ref;
-      const float alpha = move ? exp2f(m_ref - m_new) : 1.f;   // m_ref = -inf -> 0
+      const float alpha = move ? ex2(m_ref - m_new) : 1.f;     // m_ref = -inf -> 0
       if (i > 0) {
         // this stream's previous P.V must be done: its P tile is reused and
         // O may be rescaled
@@ -348,22 +353,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       m_ref = m_new;
       if (row_valid) {
         // P row (bf16) into the swizzled tile: keys are the K dimension
+        // p = 2^(s * scale - m_ref): one fma and the MUFU per score
         const float mu = m_ref == -INFINITY ? 0.f : m_ref;
         uint8_t *prow = sb + L::kOffP + st * L::kP;
-        float rs = 0.f;
+        float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < kKeys / 8; ++c) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float p0 = exp2f(__uint_as_float(sr[8 * c + 2 * e]) - mu);
-            const float p1 = exp2f(__uint_as_float(sr[8 * c + 2 * e + 1]) - mu);
-            rs += p0 + p1;
+            const float p0 = ex2(fmaf(__uint_as_float(sr[8 * c + 2 * e]), scale, -mu));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[8 * c + 2 * e + 1]), scale, -mu));
+            rs4[e] += p0 + p1;
             w[e] = pack_bf16x2(p0, p1);
           }
           *reinterpret_cast<uint4 *>(prow + swz(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        l += rs;
+        l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       }
       fence_proxy_async_smem();
       tc::fence_before_sync();

@@ -82,9 +82,11 @@ int device_sm_count();
 // (128 bytes) wide, 128-byte swizzle.  False if the driver call fails.
 bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd);
 
-// RoPE inverse frequencies base^(-2d/hd), d < hd/2, computed in double.
+// RoPE inverse frequencies base^(-2d/hd), d < hd/2, computed in double on
+// the host and passed both as double and as a pair of floats hi + lo.
 struct RopeTable {
   double inv_freq[64];
+  float hi[64], lo[64];
 };
 void make_rope_table(float base, int hd, RopeTable *t);
 

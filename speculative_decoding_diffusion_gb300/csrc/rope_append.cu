@@ -6,11 +6,15 @@
 // Section 1 "Input Layout": the 2B new tokens occupy layout indices
 // P .. P+2B-1 (D_1..D_B then D~_1..D~_B); those are the cache slots written.
 //
-// One CTA per new token.  The angle pos * base^(-2d/hd) is formed in fp64
-// and reduced modulo 2*pi in fp64 (positions reach ~3.3e4, where an fp32
-// product would be off by ~2e-3 rad); sine and cosine of the reduced angle
-// and the rotation itself are fp32.  Rotate-half pairing: element d pairs
-// with d + hd/2.  Loads and stores are 16-byte vectors.
+// One CTA per new token.  Positions reach ~3.3e4, where a plain fp32
+// product pos * base^(-2d/hd) is off by ~2e-3 rad, so the angle is formed
+// as an unevaluated sum: the frequency as two floats hi + lo (from fp64 on
+// the host), pos * hi with its exact rounding error recovered by an fma,
+// then reduced modulo 2*pi with Cody and Waite's split constant (2*pi =
+// C1 + C2, each product folded in by one fma) -- ~3e-7 rad, fp32 only (the
+// GB300's fp64 rate is a small fraction of fp32's).  Positions >= 2^24 use
+// fp64.  Sine and cosine of the reduced angle and the rotation are fp32.
+// Rotate-half pairing: element d pairs with d + hd/2.  16-byte vector I/O.
 #include "common.cuh"
 #include "internal.h"
 
@@ -22,11 +26,22 @@ constexpr int kThreads = 128;
 // Angles for one position into smem: cs[2d] = cos, cs[2d+1] = sin.
 __device__ __forceinline__ void angles(const RopeTable &tab, int hd, int pos,
                                        float2 *cs) {
-  const double two_pi = 6.283185307179586476925286766559;
+  // 2*pi = C1 + C2 (C1 the float nearest 2*pi, C2 the float nearest the rest)
+  const float C1 = 6.28318548202514648f, C2 = -1.7484555314695172e-07f;
+  const float inv_two_pi = 0.159154943091895336f;
   for (int d = threadIdx.x; d < hd / 2; d += blockDim.x) {
-    double th = (double)pos * tab.inv_freq[d];
-    double n = rint(th * (1.0 / two_pi));
-    float r = (float)fma(-n, two_pi, th);  // th - 2*pi*n, |r| <= pi
+    float r;
+    if (pos < (1 << 24)) {
+      const float p = (float)pos;                       // exact
+      const float t = p * tab.hi[d];
+      const float t_lo = fmaf(p, tab.lo[d], fmaf(p, tab.hi[d], -t));  // rest of p*(hi+lo)
+      const float n = rintf(t * inv_two_pi);
+      r = fmaf(-n, C2, fmaf(-n, C1, t)) + t_lo;         // t + t_lo - 2*pi*n
+    } else {
+      const double two_pi = 6.283185307179586476925286766559;
+      const double th = (double)pos * tab.inv_freq[d];
+      r = (float)fma(-rint(th * (1.0 / two_pi)), two_pi, th);
+    }
     float s, c;
     sincosf(r, &s, &c);
     cs[d] = make_float2(c, s);
