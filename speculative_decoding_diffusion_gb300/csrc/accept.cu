@@ -75,7 +75,7 @@ struct WalkState {
 };
 
 struct AcceptWs {
-  size_t off_status, status_bytes, off_lse, off_state, off_res, total;
+  size_t off_status, status_bytes, off_lse, off_x, off_state, off_res, total;
   int lse_chunks, res_chunks;
 };
 
@@ -90,6 +90,7 @@ AcceptWs accept_ws(const simsd_accept_desc *d) {
   w.status_bytes = sizeof(uint32_t) * (1 + 2 * (size_t)d->batch);
   off = align_up(off + w.status_bytes, kAlign);
   w.off_lse = off;    off = align_up(off + (size_t)d->total_B * w.lse_chunks * sizeof(float4), kAlign);
+  w.off_x = off;      off = align_up(off + (size_t)d->total_B * sizeof(float2), kAlign);
   w.off_state = off;  off = align_up(off + (size_t)d->batch * sizeof(WalkState), kAlign);
   w.off_res = off;    off = align_up(off + (size_t)d->batch * w.res_chunks * sizeof(float4), kAlign);
   w.total = off;
@@ -107,6 +108,7 @@ struct AcceptArgs {
   int32_t *token;
   int32_t *pos;
   float4 *lse_part;     // [total_B][lse_chunks]: (R_t, s_t, R_d, s_d)
+  float2 *xval;         // [total_B]: target and draft logit at the draft token
   WalkState *state;     // [batch]
   float4 *res_part;     // [batch][res_chunks]: residual pair, target-mass pair
   uint32_t *status;     // [0]: status word; [1..batch]: K4a counters; then K4b's
@@ -236,10 +238,17 @@ __device__ void walk(const AcceptArgs &a, int b, int c0, int B) {
     row_norm(a.lse_part + (long)(c0 + k) * a.lse_chunks, a.lse_chunks, lane, Mt, St, Md, Sd);
     if (lane == 0) {
       const long row = (long)(c0 + k) * a.vocab;
-      int x = __ldg(a.draft_tokens + c0 + k);
-      if (x < 0 || x >= a.vocab) { raise_status(a.status, kStatusBadInput); x = 0; }
-      const float tx = Ld<T>::one((const T *)a.target + row + x);
-      const float dx = Ld<T>::one((const T *)a.draft + row + x);
+      const int x = __ldg(a.draft_tokens + c0 + k);
+      float tx, dx;
+      if (x < 0 || x >= a.vocab) {
+        raise_status(a.status, kStatusBadInput);
+        tx = Ld<T>::one((const T *)a.target + row);
+        dx = Ld<T>::one((const T *)a.draft + row);
+      } else {
+        const float2 xv = __ldcg(a.xval + c0 + k);   // captured by K4a
+        tx = xv.x;
+        dx = xv.y;
+      }
       px_s[k] = rel_exp(tx, Mt) / St;
       qx_s[k] = rel_exp(dx, Md) / Sd;
       ws_s[k] = WalkState{k, Mt, Md, St, Sd};
@@ -271,12 +280,21 @@ __device__ void walk(const AcceptArgs &a, int b, int c0, int B) {
 }
 
 // ---------------------------------------------------------------- K4a
+constexpr int kStageSeqs = 2048;   // sequences whose cu_B fits the smem stage
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 lse_walk_kernel(const __grid_constant__ AcceptArgs a) {
   __shared__ float2 scratch[2][kThreads / 32];
   __shared__ int last_s;
+  __shared__ int32_t cu_s[kStageSeqs + 1];
   const int chunk = blockIdx.x, slot = blockIdx.y;
+  // independent of the stream below: the draft token and cu_B (for the
+  // sequence lookup at the end) are requested first
+  int x = -1;
+  if (threadIdx.x == 0) x = __ldg(a.draft_tokens + slot);
+  if (a.batch <= kStageSeqs)
+    for (int i = threadIdx.x; i <= a.batch; i += kThreads) cu_s[i] = __ldg(a.cu_B + i);
   const long row = (long)slot * a.vocab;
   const int v0 = chunk * kLseChunk;
   const int v1 = min(a.vocab, v0 + kLseChunk);
@@ -317,12 +335,21 @@ lse_walk_kernel(const __grid_constant__ AcceptArgs a) {
     accum(md, sd, &xd, 1);
   }
   block_lse(mt, st, scratch[0]);
-  block_lse(md, sd, scratch[1]);
+  block_lse(md, sd, scratch[1]);             // (its barriers also publish cu_s)
   // the sequence this slot belongs to, and whether this CTA finishes it
-  const int b = find_seq(a.cu_B, a.batch, slot);
-  const int c0 = __ldg(a.cu_B + b);
-  const int B = __ldg(a.cu_B + b + 1) - c0;
+  int b, c0, B;
+  if (a.batch <= kStageSeqs) {
+    b = find_seq_smem(cu_s, a.batch, slot);
+    c0 = cu_s[b];
+    B = cu_s[b + 1] - c0;
+  } else {
+    b = find_seq(a.cu_B, a.batch, slot);
+    c0 = __ldg(a.cu_B + b);
+    B = __ldg(a.cu_B + b + 1) - c0;
+  }
   if (threadIdx.x == 0) {
+    if (x >= v0 && x < v1)                   // this chunk holds the draft token
+      a.xval[slot] = make_float2(Ld<T>::one(tr + x), Ld<T>::one(dr + x));
     a.lse_part[(long)slot * a.lse_chunks + chunk] = make_float4(mt, st, md, sd);
     __threadfence();
     const unsigned total = (unsigned)B * a.lse_chunks;
@@ -535,7 +562,7 @@ residual_kernel(const __grid_constant__ AcceptArgs a) {
 }
 
 void mark(void *const *events, int i, cudaStream_t stream) {
-  if (events != nullptr && events[i] != nullptr) cudaEventRecord((cudaEvent_t)events[i], stream);
+  if (events != nullptr) record_event(events[i], stream);
 }
 
 template <typename T>
@@ -628,6 +655,7 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream_ptr,
   a.token = d->token;
   a.pos = d->pos;
   a.lse_part = (float4 *)(ws + w.off_lse);
+  a.xval = (float2 *)(ws + w.off_x);
   a.state = (WalkState *)(ws + w.off_state);
   a.res_part = (float4 *)(ws + w.off_res);
   a.status = (uint32_t *)(ws + w.off_status);
@@ -672,6 +700,7 @@ simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream_ptr) 
   a.token = d->token;
   a.pos = d->pos;
   a.lse_part = (float4 *)(ws + w.off_lse);
+  a.xval = (float2 *)(ws + w.off_x);
   a.state = (WalkState *)(ws + w.off_state);
   a.res_part = (float4 *)(ws + w.off_res);
   a.status = (uint32_t *)(ws + w.off_status);

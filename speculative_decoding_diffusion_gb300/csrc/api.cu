@@ -48,7 +48,7 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd) {
+static bool encode_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)kPageTokens, (cuuint64_t)Hkv,
@@ -64,13 +64,64 @@ bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd) {
 }
 
 
-void make_rope_table(float base, int hd, RopeTable *t) {
+int current_device() {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
+bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd) {
+  struct Entry {
+    int dev, num_pages, Hkv, hd;
+    void *ptr;
+    CUtensorMap map;
+  };
+  static std::mutex mu;
+  static Entry cache[16];
+  static int used = 0, next = 0;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i) {
+    const Entry &e = cache[i];
+    if (e.dev == dev && e.ptr == ptr && e.num_pages == num_pages && e.Hkv == Hkv && e.hd == hd) {
+      *m = e.map;
+      return true;
+    }
+  }
+  if (!encode_cache_map(m, ptr, num_pages, Hkv, hd)) return false;
+  Entry &e = cache[next];
+  e.dev = dev; e.ptr = ptr; e.num_pages = num_pages; e.Hkv = Hkv; e.hd = hd; e.map = *m;
+  next = (next + 1) % 16;
+  if (used < 16) ++used;
+  return true;
+}
+
+bool record_event(void *event, cudaStream_t stream) {
+  if (event == nullptr) return true;
+  return cudaEventRecordWithFlags((cudaEvent_t)event, stream, cudaEventRecordExternal) ==
+         cudaSuccess;
+}
+
+static void fill_rope_table(float base, int hd, RopeTable *t) {
   memset(t, 0, sizeof(*t));
   for (int d = 0; d < hd / 2 && d < 64; ++d) {
     t->inv_freq[d] = pow((double)base, -2.0 * (double)d / (double)hd);
     t->hi[d] = (float)t->inv_freq[d];
     t->lo[d] = (float)(t->inv_freq[d] - (double)t->hi[d]);
   }
+}
+
+void make_rope_table(float base, int hd, RopeTable *t) {
+  static std::mutex mu;
+  static float last_base = 0.f;
+  static int last_hd = 0;
+  static RopeTable last;
+  std::lock_guard<std::mutex> lock(mu);
+  if (last_hd != hd || last_base != base) {
+    fill_rope_table(base, hd, &last);
+    last_base = base;
+    last_hd = hd;
+  }
+  *t = last;
 }
 
 static bool valid_dtype(simsd_dtype t) { return t == SIMSD_F32 || t == SIMSD_BF16; }
@@ -208,8 +259,7 @@ simsd_status simsd_verify_attn(const simsd_verify_desc *d, void *stream_ptr) {
 }
 
 static bool mark(void *const *events, int i, cudaStream_t stream) {
-  if (events == nullptr || events[i] == nullptr) return true;
-  return cudaEventRecord((cudaEvent_t)events[i], stream) == cudaSuccess;
+  return events == nullptr || record_event(events[i], stream);
 }
 
 simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_ptr,

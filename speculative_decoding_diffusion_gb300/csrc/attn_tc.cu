@@ -11,8 +11,9 @@
 // in group; rows past 2B*G are zero padding), so each key/value byte read
 // from HBM serves every row.  The CTA's keys come in 64-key blocks dealt
 // alternately to two independent streams, each with its own score tile S,
-// probability tile P and output accumulator O (and running max / sum); the
-// two are merged in the epilogue.  Warp roles:
+// two probability tiles P (so a stream's next softmax never waits for its
+// previous P.V) and output accumulator O (and running max / sum); the two
+// are merged in the epilogue.  Warp roles:
 //   warp 0     TMA producer: K and V of each block (4 pages, one 2 KB box
 //              per page and 64-column half, 128-byte swizzle) into a
 //              4-stage ring;
@@ -29,6 +30,8 @@
 // Every mbarrier wait is bounded; a wait that runs out sets the status word
 // and the CTA drains and returns.
 #include <cuda.h>
+
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -49,9 +52,12 @@ constexpr int kBoxBytes = kPage * 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kHeadroom = 8.f;     // log2 units a row max may grow before O is rescaled
 
+constexpr int kPBufs = 2;            // P tiles per stream (double buffered)
+
 enum { kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarSFull = kBarKvEmpty + kStages,
        kBarSEmpty = kBarSFull + kStreams, kBarPFull = kBarSEmpty + kStreams,
-       kBarPvDone = kBarPFull + kStreams, kNumBars = kBarPvDone + kStreams };
+       kBarPvDone = kBarPFull + kStreams * kPBufs, kBarQReady = kBarPvDone + kStreams * kPBufs,
+       kNumBars = kBarQReady + 1 };
 
 template <int HD>
 struct TcSmem {
@@ -64,7 +70,7 @@ struct TcSmem {
   static constexpr int kStage = 2 * kKv;
   static constexpr int kOffQ = 0;
   static constexpr int kOffP = kOffQ + kQ;              // kStreams tiles
-  static constexpr int kOffKv = kOffP + kStreams * kP;
+  static constexpr int kOffKv = kOffP + kStreams * kPBufs * kP;
   static constexpr int kOffBar = kOffKv + kStages * kStage;
   static constexpr int kOffTau = kOffBar + kNumBars * 8;
   static constexpr int kOffMl = kOffTau + 2 * kMaxB * 4;    // stream 1's (m, l) per row
@@ -147,24 +153,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     for (int i = 0; i < kStreams; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarSEmpty + i), 4);
+    }
+    for (int i = 0; i < kStreams * kPBufs; ++i) {
       mbar_init(bar(kBarPFull + i), 4);
       mbar_init(bar(kBarPvDone + i), 1);
     }
+    mbar_init(bar(kBarQReady), 4 * kStreams + 1);
     *flag_s = 0;
     fence_barrier_init();
   }
-  for (int j = threadIdx.x; j < 2 * B; j += kThreads)
-    tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
   if (warp == 1) {
     tc::alloc(smem_u32(tmem_slot), L::kTmemCols);
     tc::relinquish();
   }
-  // Q tile -> shared memory (K-major, 128-byte swizzle); P tiles zeroed
-  // once, so padding rows (never written again) hold zeros
-  {
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  if (warp != 0) {
+    // Q tile -> shared memory (K-major, 128-byte swizzle) and the P tiles
+    // zeroed once (padding rows are never written again), while the
+    // producer already streams K and V; then arrive on the Q barrier
+    const int t = threadIdx.x - 32, nt = kThreads - 32;
+    for (int j = t; j < 2 * B; j += nt) tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
     const __nv_bfloat16 *q = (const __nv_bfloat16 *)a.q_rot;
     constexpr int CH = HD / 8;
-    for (int e = threadIdx.x; e < kRows * CH; e += kThreads) {
+    for (int e = t; e < kRows * CH; e += nt) {
       const int r = e / CH, c = e % CH;
       const int grow = row0 + r;
       uint4 v = make_uint4(0, 0, 0, 0);
@@ -174,14 +188,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       }
       *reinterpret_cast<uint4 *>(sb + L::kOffQ + (c >> 3) * L::kHalfRows + swz(r, c & 7)) = v;
     }
-    for (int e = threadIdx.x; e < kStreams * L::kP / 16; e += kThreads)
+    for (int e = t; e < kStreams * kPBufs * L::kP / 16; e += nt)
       reinterpret_cast<uint4 *>(sb + L::kOffP)[e] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarQReady));
+    // every consumer needs the whole Q tile, tau and zeroed P tiles
+    if (!mbar_wait_warp(bar(kBarQReady), 0)) {
+      if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
+    }
   }
-  fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -250,7 +266,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         if (!ok) break;
       }
       const int st = j & 1, s = j % kStages;
-      if (!mbar_wait_warp(bar(kBarPFull + st), (j >> 1) & 1)) { fail(); break; }
+      const int ib = j >> 1;                 // block index within the stream
+      const int pb = st * kPBufs + (ib & 1); // its P tile
+      if (!mbar_wait_warp(bar(kBarPFull + pb), (ib >> 1) & 1)) { fail(); break; }
       tc::fence_after_sync();
       const int kb = k_begin + j * kKeys;
       const int valid = min(kKeys, k_end - kb);
@@ -269,12 +287,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       }
       __syncwarp();
       if (lane == 0) {
-        const uint32_t pt = sP + st * L::kP;
+        const uint32_t pt = sP + pb * L::kP;
         for (int kk = 0; kk < loaded / 16; ++kk)
           tc::mma_bf16(tmem + kColO + st * HD, tc::smem_desc_sw128(pt + kk * 32, 16, 1024),
                        tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
                        (j >= kStreams || kk > 0));
-        tc::commit(bar(kBarPvDone + st));
+        tc::commit(bar(kBarPvDone + pb));
         tc::commit(bar(kBarKvEmpty + s));
       }
       __syncwarp();
@@ -331,12 +349,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       const bool move = row_valid && mx > m_ref + kHeadroom;
       const float m_new = move ? mx : m_ref;
       const float alpha = move ? ex2(m_ref - m_new) : 1.f;     // m_ref = -inf -> 0
-      if (i > 0) {
-        // this stream's previous P.V must be done: its P tile is reused and
-        // O may be rescaled
-        if (!mbar_wait_warp(bar(kBarPvDone + st), (i - 1) & 1)) { ok = false; break; }
+      const int pb = st * kPBufs + (i & 1);
+      if (i >= kPBufs) {
+        // the P.V that read this P tile two blocks ago must be done
+        if (!mbar_wait_warp(bar(kBarPvDone + pb), ((i >> 1) - 1) & 1)) { ok = false; break; }
         tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, move)) {
+      }
+      if (i > 0 && __any_sync(0xffffffffu, move)) {
+        // rescaling O needs the stream's previous P.V (the latest) done
+        const int pp = st * kPBufs + ((i - 1) & 1);
+        if (!mbar_wait_warp(bar(kBarPvDone + pp), ((i - 1) >> 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        {
 #pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t o[32];
@@ -355,7 +379,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         // P row (bf16) into the swizzled tile: keys are the K dimension
         // p = 2^(s * scale - m_ref): one fma and the MUFU per score
         const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        uint8_t *prow = sb + L::kOffP + st * L::kP;
+        uint8_t *prow = sb + L::kOffP + pb * L::kP;
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < kKeys / 8; ++c) {
@@ -374,9 +398,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       fence_proxy_async_smem();
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + st));
+      if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
     }
-    if (ok && i > 0 && !mbar_wait_warp(bar(kBarPvDone + st), (i - 1) & 1)) ok = false;
+    if (ok && i > 0 &&
+        !mbar_wait_warp(bar(kBarPvDone + st * kPBufs + ((i - 1) & 1)), ((i - 1) >> 1) & 1))
+      ok = false;
     if (!ok && lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
     tc::fence_after_sync();
     // -------------------------------------------------------- epilogue
@@ -434,13 +460,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   }
 }
 
+static_assert(TcSmem<128>::kAlloc <= 227 * 1024, "shared memory budget");
+
 template <int HD>
 cudaError_t launch_hd(const CUtensorMap &mk, const CUtensorMap &mv, const AttnParams &a,
                       dim3 grid, cudaStream_t stream) {
   auto kern = attn_tc_kernel<HD>;
   const int smem = TcSmem<HD>::kAlloc;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+  static std::atomic<uint64_t> configured{0};   // one bit per device
+  const int dev = current_device();
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+  if (!bit || !(configured.load() & bit)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit);
+  }
   kern<<<grid, kThreads, smem, stream>>>(mk, mv, a);
   return cudaGetLastError();
 }

@@ -151,6 +151,20 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0,
 }
 
 // ---------------------------------------------------------------- misc
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Largest b in [0, n) with cu[b] <= row, cu in shared memory.
+__device__ __forceinline__ int find_seq_smem(const int32_t *cu, int n, int row) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= row) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // Sequence that owns row `row` of a prefix-sum array cu[0..n] (cu[0] = 0):
 // the largest b with cu[b] <= row.
 __device__ __forceinline__ int find_seq(const int32_t *cu, int n, int row) {

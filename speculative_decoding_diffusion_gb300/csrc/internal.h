@@ -64,8 +64,6 @@ cudaError_t launch_rope_append(const simsd_append_desc *d, cudaStream_t stream);
 // K2: split-KV masked attention (tcgen05 for bf16, CUDA cores for fp32).
 cudaError_t launch_attn_tc(const simsd_verify_desc *d, const VerifyPlan &p,
                            const AttnParams &a, cudaStream_t stream);
-cudaError_t launch_attn_bf16(const simsd_verify_desc *d, const VerifyPlan &p,
-                             const AttnParams &a, cudaStream_t stream);
 cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
                             const AttnParams &a, cudaStream_t stream);
 
@@ -80,7 +78,17 @@ int device_sm_count();
 // TMA descriptor of a paged bf16 cache [num_pages][Hkv][16][hd] as the 4-D
 // tensor (hd, slot, head, page); one box = one page of one head, 64 columns
 // (128 bytes) wide, 128-byte swizzle.  False if the driver call fails.
+// Descriptors are cached per (device, pointer, sizes): repeated calls on the
+// same cache cost no driver call.
 bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd);
+
+// Records `event` (a cudaEvent_t, may be NULL) on `stream`; under stream
+// capture it becomes an event-record node of the graph, so a replayed graph
+// still yields per-kernel times.
+bool record_event(void *event, cudaStream_t stream);
+
+// Current device, or -1.
+int current_device();
 
 // RoPE inverse frequencies base^(-2d/hd), d < hd/2, computed in double on
 // the host and passed both as double and as a pair of floats hi + lo.
@@ -88,6 +96,6 @@ struct RopeTable {
   double inv_freq[64];
   float hi[64], lo[64];
 };
-void make_rope_table(float base, int hd, RopeTable *t);
+void make_rope_table(float base, int hd, RopeTable *t);   // cached per (base, hd)
 
 }  // namespace simsd

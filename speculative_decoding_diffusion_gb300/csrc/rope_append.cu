@@ -137,15 +137,42 @@ struct RopeVerifyArgs {
   int batch, Hq, Hkv, hd, max_pages, num_pages;
 };
 
+constexpr int kStageSeqs = 2048;   // sequences whose cu_B / lens fit the smem stage
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
   __shared__ float2 cs[64];
+  __shared__ int32_t cu_s[kStageSeqs + 1], lens_s[kStageSeqs];
   const int r = blockIdx.x;                  // new-token row
-  const int b = find_seq(a.cu_B, a.batch, r >> 1);
-  const int c0 = __ldg(a.cu_B + b);
-  const int B = __ldg(a.cu_B + b + 1) - c0;
-  const int P = __ldg(a.lens + b);
+  // this token's rows are needed whatever its sequence: start them towards L2
+  {
+    const char *qrow = (const char *)a.q + (long)r * a.Hq * a.hd * sizeof(T);
+    const char *krow = (const char *)a.k_new + (long)r * a.Hkv * a.hd * sizeof(T);
+    const char *vrow = (const char *)a.v_new + (long)r * a.Hkv * a.hd * sizeof(T);
+    const int qlines = a.Hq * a.hd * (int)sizeof(T) / 128, kvlines = a.Hkv * a.hd * (int)sizeof(T) / 128;
+    for (int i = threadIdx.x; i < qlines; i += blockDim.x) prefetch_l2(qrow + 128 * i);
+    for (int i = threadIdx.x; i < kvlines; i += blockDim.x) {
+      prefetch_l2(krow + 128 * i);
+      prefetch_l2(vrow + 128 * i);
+    }
+  }
+  // sequence of the token: cu_B (and lens) staged once, searched in smem
+  int b, c0, B, P;
+  if (a.batch <= kStageSeqs) {
+    for (int i = threadIdx.x; i <= a.batch; i += blockDim.x) cu_s[i] = __ldg(a.cu_B + i);
+    for (int i = threadIdx.x; i < a.batch; i += blockDim.x) lens_s[i] = __ldg(a.lens + i);
+    __syncthreads();
+    b = find_seq_smem(cu_s, a.batch, r >> 1);
+    c0 = cu_s[b];
+    B = cu_s[b + 1] - c0;
+    P = lens_s[b];
+  } else {
+    b = find_seq(a.cu_B, a.batch, r >> 1);
+    c0 = __ldg(a.cu_B + b);
+    B = __ldg(a.cu_B + b + 1) - c0;
+    P = __ldg(a.lens + b);
+  }
   if (threadIdx.x == 0) a.tok_seq[r] = b;    // the merge kernel reads it
   if (B < 1 || B > kMaxSection || P < 0 || (long)P + 2 * B > (long)a.max_pages * kPage) {
     if (threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
