@@ -173,29 +173,37 @@ template <> struct Ld<__nv_bfloat16> {
   }
 };
 
-// Block-wide (M, s) merge, result in thread 0 (sums as two-sum pairs across
-// warps, relative to the block maximum).
-__device__ __forceinline__ void block_lse(float &m, float &s, float2 *scratch) {
+// Block-wide merge of the (R, s) pairs of both rows; result in thread 0.
+// Warps reduce by shuffles, then warp 0 merges the warps' partials (sums as
+// two-sum pairs relative to the block reference): one barrier per CTA.
+__device__ __forceinline__ void block_lse2(float &mt, float &st, float &md, float &sd,
+                                           float4 *scratch) {
 #pragma unroll
   for (int w = 16; w > 0; w >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, w);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, w);
-    lse_merge(m, s, m2, s2);
+    lse_merge(mt, st, __shfl_xor_sync(0xffffffffu, mt, w), __shfl_xor_sync(0xffffffffu, st, w));
+    lse_merge(md, sd, __shfl_xor_sync(0xffffffffu, md, w), __shfl_xor_sync(0xffffffffu, sd, w));
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) scratch[warp] = make_float2(m, s);
+  if (lane == 0) scratch[warp] = make_float4(mt, st, md, sd);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int i = 0; i < kThreads / 32; ++i) M = fmaxf(M, scratch[i].x);
-    Ff S = ff_of(0.f);
-    if (M != -INFINITY)
-      for (int i = 0; i < kThreads / 32; ++i)
-        S = ff_add(S, ff_of(scratch[i].y * ex2(scratch[i].x - M)));
-    m = M;
-    s = S.hi + S.lo;
+  if (warp == 0) {
+    constexpr int W = kThreads / 32;
+    const float4 v = lane < W ? scratch[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+    float Mt = v.x, Md = v.z;
+#pragma unroll
+    for (int w = W / 2; w > 0; w >>= 1) {
+      Mt = fmaxf(Mt, __shfl_xor_sync(0xffffffffu, Mt, w));
+      Md = fmaxf(Md, __shfl_xor_sync(0xffffffffu, Md, w));
+    }
+    Ff St = ff_of(v.y > 0.f ? v.y * ex2(v.x - Mt) : 0.f);
+    Ff Sd = ff_of(v.w > 0.f ? v.w * ex2(v.z - Md) : 0.f);
+#pragma unroll
+    for (int w = W / 2; w > 0; w >>= 1) {
+      St = ff_add(St, ff_shfl_xor(St, w));
+      Sd = ff_add(Sd, ff_shfl_xor(Sd, w));
+    }
+    mt = Mt; st = St.hi + St.lo; md = Md; sd = Sd.hi + Sd.lo;
   }
-  __syncthreads();
 }
 
 // Row maximum and normaliser of one slot from its chunk partials (one warp).
@@ -285,7 +293,7 @@ constexpr int kStageSeqs = 2048;   // sequences whose cu_B fits the smem stage
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 lse_walk_kernel(const __grid_constant__ AcceptArgs a) {
-  __shared__ float2 scratch[2][kThreads / 32];
+  __shared__ float4 scratch[kThreads / 32];
   __shared__ int last_s;
   __shared__ int32_t cu_s[kStageSeqs + 1];
   const int chunk = blockIdx.x, slot = blockIdx.y;
@@ -334,8 +342,7 @@ lse_walk_kernel(const __grid_constant__ AcceptArgs a) {
     accum(mt, st, &xt, 1);
     accum(md, sd, &xd, 1);
   }
-  block_lse(mt, st, scratch[0]);
-  block_lse(md, sd, scratch[1]);             // (its barriers also publish cu_s)
+  block_lse2(mt, st, md, sd, scratch);       // (its barrier also publishes cu_s)
   // the sequence this slot belongs to, and whether this CTA finishes it
   int b, c0, B;
   if (a.batch <= kStageSeqs) {

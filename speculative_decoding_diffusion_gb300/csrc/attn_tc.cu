@@ -233,69 +233,75 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0);
-    constexpr uint32_t idO = tc::idesc_bf16(kRows, HD, 1);
-    bool ok = true;
-    auto fail = [&]() {
-      if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
-      ok = false;
-    };
-    // S of block j into its stream's score tile
-    auto issue_s = [&](int j) {
-      const int s = j % kStages, st = j & 1;
-      if (!mbar_wait_warp(bar(kBarKvFull + s), (j / kStages) & 1)) { fail(); return; }
-      if (j >= kStreams && !mbar_wait_warp(bar(kBarSEmpty + st), ((j >> 1) - 1) & 1)) { fail(); return; }
-      tc::fence_after_sync();
-      if (lane == 0) {
-        const uint32_t kt = sKv + s * L::kStage;
+    // One thread schedules both MMA kinds as their inputs become ready, so
+    // a P.V never waits behind a later block's K load: S of block ns needs
+    // its K/V stage and its stream's score tile free; P.V of block np needs
+    // its P tile.  P.V goes in block order.
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0);
+      constexpr uint32_t idO = tc::idesc_bf16(kRows, HD, 1);
+      int ns = 0, np = 0;
+      uint32_t idle = 0;
+      while (np < n_blocks) {
+        bool progressed = false;
+        if (ns < n_blocks) {
+          const int s = ns % kStages, st = ns & 1;
+          if (mbar_test(bar(kBarKvFull + s), (ns / kStages) & 1) &&
+              (ns < kStreams || mbar_test(bar(kBarSEmpty + st), ((ns >> 1) - 1) & 1))) {
+            tc::fence_after_sync();
+            const uint32_t kt = sKv + s * L::kStage;
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t qa = sQ + (kk >> 2) * L::kHalfRows + (kk & 3) * 32;
-          const uint32_t ka = kt + (kk >> 2) * L::kKvHalf + (kk & 3) * 32;
-          tc::mma_bf16(tmem + st * kKeys, tc::smem_desc_sw128(qa, 16, 1024),
-                       tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              const uint32_t qa = sQ + (kk >> 2) * L::kHalfRows + (kk & 3) * 32;
+              const uint32_t ka = kt + (kk >> 2) * L::kKvHalf + (kk & 3) * 32;
+              tc::mma_bf16(tmem + st * kKeys, tc::smem_desc_sw128(qa, 16, 1024),
+                           tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
+            }
+            tc::commit(bar(kBarSFull + st));
+            ++ns;
+            progressed = true;
+          }
         }
-        tc::commit(bar(kBarSFull + st));
-      }
-      __syncwarp();
-    };
-    for (int j = 0; j < kStreams && j < n_blocks && ok; ++j) issue_s(j);
-    for (int j = 0; j < n_blocks && ok; ++j) {
-      if (j + kStreams < n_blocks) {
-        issue_s(j + kStreams);
-        if (!ok) break;
-      }
-      const int st = j & 1, s = j % kStages;
-      const int ib = j >> 1;                 // block index within the stream
-      const int pb = st * kPBufs + (ib & 1); // its P tile
-      if (!mbar_wait_warp(bar(kBarPFull + pb), (ib >> 1) & 1)) { fail(); break; }
-      tc::fence_after_sync();
-      const int kb = k_begin + j * kKeys;
-      const int valid = min(kKeys, k_end - kb);
-      const int loaded = (valid + kPage - 1) & ~(kPage - 1);
-      const uint32_t vt = sKv + s * L::kStage + L::kKv;
-      if (kb + valid == Lk && loaded > valid) {
-        // slots past the sequence end in its last page hold arbitrary data;
-        // P is 0 there, but 0 * NaN would poison O, so zero the V rows
-        constexpr int CH = HD / 8;
-        for (int e = lane; e < (loaded - valid) * CH; e += 32) {
-          const int r = valid + e / CH, c = e % CH;
-          *reinterpret_cast<uint4 *>(sb + (vt - base) + (c >> 3) * L::kKvHalf + swz(r, c & 7)) =
-              make_uint4(0, 0, 0, 0);
+        if (np < ns) {
+          const int st = np & 1, s = np % kStages;
+          const int ib = np >> 1;                 // block index within the stream
+          const int pb = st * kPBufs + (ib & 1);  // its P tile
+          if (mbar_test(bar(kBarPFull + pb), (ib >> 1) & 1)) {
+            tc::fence_after_sync();
+            const int kb = k_begin + np * kKeys;
+            const int valid = min(kKeys, k_end - kb);
+            const int loaded = (valid + kPage - 1) & ~(kPage - 1);
+            const uint32_t vt = sKv + s * L::kStage + L::kKv;
+            if (kb + valid == Lk && loaded > valid) {
+              // slots past the sequence end in its last page hold arbitrary
+              // data; P is 0 there, but 0 * NaN would poison O: zero V rows
+              constexpr int CH = HD / 8;
+              for (int e = 0; e < (loaded - valid) * CH; ++e) {
+                const int r = valid + e / CH, c = e % CH;
+                *reinterpret_cast<uint4 *>(sb + (vt - base) + (c >> 3) * L::kKvHalf + swz(r, c & 7)) =
+                    make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+            }
+            const uint32_t pt = sP + pb * L::kP;
+            for (int kk = 0; kk < loaded / 16; ++kk)
+              tc::mma_bf16(tmem + kColO + st * HD, tc::smem_desc_sw128(pt + kk * 32, 16, 1024),
+                           tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
+                           (np >= kStreams || kk > 0));
+            tc::commit(bar(kBarPvDone + pb));
+            tc::commit(bar(kBarKvEmpty + s));
+            ++np;
+            progressed = true;
+          }
         }
-        fence_proxy_async_smem();
+        if (progressed) {
+          idle = 0;
+        } else if (++idle > (kWaitPolls << 4)) {  // bounded: give up, flag, drain
+          raise_status(a.status, kStatusTimeout);
+          atomicOr(flag_s, 1);
+          break;
+        }
       }
-      __syncwarp();
-      if (lane == 0) {
-        const uint32_t pt = sP + pb * L::kP;
-        for (int kk = 0; kk < loaded / 16; ++kk)
-          tc::mma_bf16(tmem + kColO + st * HD, tc::smem_desc_sw128(pt + kk * 32, 16, 1024),
-                       tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
-                       (j >= kStreams || kk > 0));
-        tc::commit(bar(kBarPvDone + pb));
-        tc::commit(bar(kBarKvEmpty + s));
-      }
-      __syncwarp();
     }
   } else {
     // ---------------------------------------------------------- softmax

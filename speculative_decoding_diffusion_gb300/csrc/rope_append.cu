@@ -77,47 +77,73 @@ template <> struct Vec<__nv_bfloat16> {
 };
 
 // Rotate `heads` rows of hd elements from src into dst (row h at h*hd; dst
-// rows at dst_stride apart) with the angles in cs.
+// rows at dst_stride apart) with the angles in cs.  Each thread loads a
+// batch of its vectors before storing any, so the loads are in flight
+// together rather than serialised behind possibly aliasing stores.
 template <typename T>
-__device__ __forceinline__ void rotate_rows(const T *src, T *dst, int heads,
-                                            int hd, long dst_stride,
+__device__ __forceinline__ void rotate_rows(const T *__restrict__ src, T *__restrict__ dst,
+                                            int heads, int hd, long dst_stride,
                                             const float2 *cs) {
   using VT = Vec<T>;
-  constexpr int N = VT::N;
+  constexpr int N = VT::N, BATCH = 4;
   const int half = hd / 2;
   const int per_head = half / N;  // vector pairs per head
-  for (int i = threadIdx.x; i < heads * per_head; i += blockDim.x) {
-    const int h = i / per_head;
-    const int d0 = (i % per_head) * N;
-    const T *x = src + (long)h * hd;
-    typename VT::V a = *reinterpret_cast<const typename VT::V *>(x + d0);
-    typename VT::V b = *reinterpret_cast<const typename VT::V *>(x + d0 + half);
-    float x1[N], x2[N], y1[N], y2[N];
-    VT::unpack(a, x1);
-    VT::unpack(b, x2);
+  const int items = heads * per_head;
+  for (int i0 = threadIdx.x; i0 < items; i0 += BATCH * blockDim.x) {
+    typename VT::V va[BATCH], vb[BATCH];
 #pragma unroll
-    for (int j = 0; j < N; ++j) {
-      const float c = cs[d0 + j].x, s = cs[d0 + j].y;
-      y1[j] = x1[j] * c - x2[j] * s;
-      y2[j] = x2[j] * c + x1[j] * s;
+    for (int u = 0; u < BATCH; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < items) {
+        const T *x = src + (long)(i / per_head) * hd + (i % per_head) * N;
+        va[u] = __ldg(reinterpret_cast<const typename VT::V *>(x));
+        vb[u] = __ldg(reinterpret_cast<const typename VT::V *>(x + half));
+      }
     }
-    T *y = dst + (long)h * dst_stride;
-    *reinterpret_cast<typename VT::V *>(y + d0) = VT::pack(y1);
-    *reinterpret_cast<typename VT::V *>(y + d0 + half) = VT::pack(y2);
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i >= items) break;
+      const int h = i / per_head, d0 = (i % per_head) * N;
+      float x1[N], x2[N], y1[N], y2[N];
+      VT::unpack(va[u], x1);
+      VT::unpack(vb[u], x2);
+#pragma unroll
+      for (int j = 0; j < N; ++j) {
+        const float c = cs[d0 + j].x, sn = cs[d0 + j].y;
+        y1[j] = x1[j] * c - x2[j] * sn;
+        y2[j] = x2[j] * c + x1[j] * sn;
+      }
+      T *y = dst + (long)h * dst_stride;
+      *reinterpret_cast<typename VT::V *>(y + d0) = VT::pack(y1);
+      *reinterpret_cast<typename VT::V *>(y + d0 + half) = VT::pack(y2);
+    }
   }
 }
 
 template <typename T>
-__device__ __forceinline__ void copy_rows(const T *src, T *dst, int heads,
-                                          int hd, long dst_stride) {
+__device__ __forceinline__ void copy_rows(const T *__restrict__ src, T *__restrict__ dst,
+                                          int heads, int hd, long dst_stride) {
   using VT = Vec<T>;
-  constexpr int N = VT::N;
+  constexpr int N = VT::N, BATCH = 4;
   const int per_head = hd / N;
-  for (int i = threadIdx.x; i < heads * per_head; i += blockDim.x) {
-    const int h = i / per_head;
-    const int d0 = (i % per_head) * N;
-    *reinterpret_cast<typename VT::V *>(dst + (long)h * dst_stride + d0) =
-        *reinterpret_cast<const typename VT::V *>(src + (long)h * hd + d0);
+  const int items = heads * per_head;
+  for (int i0 = threadIdx.x; i0 < items; i0 += BATCH * blockDim.x) {
+    typename VT::V v[BATCH];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < items)
+        v[u] = __ldg(reinterpret_cast<const typename VT::V *>(src + (long)(i / per_head) * hd +
+                                                               (i % per_head) * N));
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i >= items) break;
+      *reinterpret_cast<typename VT::V *>(dst + (long)(i / per_head) * dst_stride +
+                                          (i % per_head) * N) = v[u];
+    }
   }
 }
 
