@@ -34,7 +34,7 @@ namespace simsd {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kLseVec = 4;                        // 16-byte loads per row per thread per pass
+constexpr int kLseVec = 2;                        // 16-byte loads per row per thread per pass
 constexpr int kLseChunk = 8192;                   // K4a vocabulary chunk
 constexpr int kResPer = 8;                        // residual entries per thread
 constexpr int kResChunk = kThreads * kResPer;     // 2048
@@ -291,12 +291,13 @@ __device__ void walk(const AcceptArgs &a, int b, int c0, int B) {
 constexpr int kStageSeqs = 2048;   // sequences whose cu_B fits the smem stage
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 8)
 lse_walk_kernel(const __grid_constant__ AcceptArgs a) {
   __shared__ float4 scratch[kThreads / 32];
   __shared__ int last_s;
   __shared__ int32_t cu_s[kStageSeqs + 1];
   const int chunk = blockIdx.x, slot = blockIdx.y;
+  grid_dep_launch();                         // the residual kernel may be scheduled
   // independent of the stream below: the draft token and cu_B (for the
   // sequence lookup at the end) are requested first
   int x = -1;
@@ -439,6 +440,7 @@ residual_kernel(const __grid_constant__ AcceptArgs a) {
   __shared__ int last_s, sel_s, use_p_s, best_s, lastpos_s;
   __shared__ Ff base_s, U_s;
   const int chunk = blockIdx.x, b = blockIdx.y;
+  grid_dep_wait();                           // the walk state comes from K4a
   const WalkState st = a.state[b];
   if (st.rej < 0) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -578,9 +580,10 @@ cudaError_t launch_all(const AcceptArgs &a, int total_B, cudaStream_t stream,
   mark(events, 0, stream);
   lse_walk_kernel<T><<<dim3(a.lse_chunks, total_B), kThreads, 0, stream>>>(a);
   mark(events, 1, stream);
-  residual_kernel<T><<<dim3(a.res_chunks, a.batch), kThreads, 0, stream>>>(a);
+  cudaError_t e = launch_pdl(residual_kernel<T>, dim3(a.res_chunks, a.batch), dim3(kThreads), 0,
+                             stream, a);
   mark(events, 2, stream);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 simsd_status accept_check(const simsd_accept_desc *d) {

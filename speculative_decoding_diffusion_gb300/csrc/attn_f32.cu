@@ -127,6 +127,7 @@ template <typename T, int HD>
 __global__ void __launch_bounds__(256)
 combine_kernel(const __grid_constant__ AttnParams a, const int32_t *tok_seq) {
   constexpr int PER = HD / 32;
+  grid_dep_wait();                           // partials come from the attention kernel
   const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= (long)a.T * a.Hq) return;
@@ -174,14 +175,14 @@ cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
                            cudaStream_t stream) {
   const long rows = (long)p.T * d->num_q_heads;
   const unsigned blocks = (unsigned)((rows + 7) / 8);
-  if (d->dtype == SIMSD_BF16) {
-    if (d->head_dim == 128) combine_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, stream>>>(a, tok_seq);
-    else combine_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, stream>>>(a, tok_seq);
-  } else {
-    if (d->head_dim == 128) combine_kernel<float, 128><<<blocks, 256, 0, stream>>>(a, tok_seq);
-    else combine_kernel<float, 64><<<blocks, 256, 0, stream>>>(a, tok_seq);
-  }
-  return cudaGetLastError();
+  const int32_t *ts = tok_seq;
+  if (d->dtype == SIMSD_BF16)
+    return d->head_dim == 128
+               ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(256), 0, stream, a, ts)
+               : launch_pdl(combine_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(256), 0, stream, a, ts);
+  return d->head_dim == 128
+             ? launch_pdl(combine_kernel<float, 128>, dim3(blocks), dim3(256), 0, stream, a, ts)
+             : launch_pdl(combine_kernel<float, 64>, dim3(blocks), dim3(256), 0, stream, a, ts);
 }
 
 }  // namespace simsd

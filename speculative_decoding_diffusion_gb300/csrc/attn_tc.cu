@@ -144,6 +144,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int n_blocks = (k_end - k_begin + kKeys - 1) / kKeys;
   const int n_splits_b = (Lk + a.chunk - 1) / a.chunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  grid_dep_launch();                         // the split merge may be scheduled
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -176,6 +177,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // producer already streams K and V; then arrive on the Q barrier
     const int t = threadIdx.x - 32, nt = kThreads - 32;
     for (int j = t; j < 2 * B; j += nt) tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
+    grid_dep_wait();                         // rotated q comes from the rotation kernel
     const __nv_bfloat16 *q = (const __nv_bfloat16 *)a.q_rot;
     constexpr int CH = HD / 8;
     for (int e = t; e < kRows * CH; e += nt) {
@@ -204,9 +206,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
     const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
     int issued = 0;
+    bool dep_done = false;
     for (int j = 0; j < n_blocks; ++j) {
       const int s = j % kStages;
       const int kb = k_begin + j * kKeys;
+      if (!dep_done && kb + kKeys > P) {     // the block holds new keys K1 writes
+        grid_dep_wait();
+        dep_done = true;
+      }
       const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
       const int page = lane < n_pages ? __ldg(bt + kb / kPage + lane) : 0;   // before the wait
       if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1)) {
@@ -481,8 +488,7 @@ cudaError_t launch_hd(const CUtensorMap &mk, const CUtensorMap &mv, const AttnPa
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit);
   }
-  kern<<<grid, kThreads, smem, stream>>>(mk, mv, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(kThreads), smem, stream, mk, mv, a);
 }
 
 }  // namespace

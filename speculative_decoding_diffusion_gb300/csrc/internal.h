@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/simsd.h"
 
 namespace simsd {
@@ -89,6 +91,25 @@ bool record_event(void *event, cudaStream_t stream);
 
 // Current device, or -1.
 int current_device();
+
+// Launch `kern` with programmatic stream serialisation: it may begin while
+// the previous kernel on `stream` still runs, and waits for it on the device
+// (grid_dep_wait) before reading its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // RoPE inverse frequencies base^(-2d/hd), d < hd/2, computed in double on
 // the host and passed both as double and as a pair of floats hi + lo.

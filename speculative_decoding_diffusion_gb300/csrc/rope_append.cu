@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads)
 rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
   __shared__ float2 cs[64];
   __shared__ int32_t cu_s[kStageSeqs + 1], lens_s[kStageSeqs];
+  grid_dep_launch();                         // the attention kernel may start its prologue
   const int r = blockIdx.x;                  // new-token row
   // this token's rows are needed whatever its sequence: start them towards L2
   {
