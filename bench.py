@@ -11,8 +11,10 @@ the batch / step time) with inputs resident in HBM: the step's library calls
 are captured once into a CUDA graph (the library allocates nothing and never
 synchronises, so the calls capture as they are) and replayed; each replay is
 timed with CUDA events on the launching stream, with L2 flushed (a 512 MB
-write) before it.  Per-kernel times come from the library's own event marks,
-which the graph keeps as event-record nodes.  `e2e`: the same metric through
+write) before it.  Per-kernel times come from a second graph of the same
+calls with the library's event marks as event-record nodes (those nodes sit
+between kernels, so that graph forgoes the overlap of consecutive kernels
+that the timed graph keeps).  `e2e`: the same metric through
 the C ABI called directly from Python each step with host buffers (pinned
 host -> device copies of the step's inputs and device -> host copies of its
 results inside the timed region; host launch cost included); `e2e_graph`
@@ -284,12 +286,17 @@ def main():
         flush.zero_()
         step(False)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
+    graph = torch.cuda.CUDAGraph()           # the timed step
     with torch.cuda.graph(graph):
+        step(False)
+    kgraph = torch.cuda.CUDAGraph()          # the same step with per-kernel marks
+    with torch.cuda.graph(kgraph):
         step(True)
     for _ in range(3):
         flush.zero_()
         graph.replay()
+        flush.zero_()
+        kgraph.replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
@@ -304,9 +311,13 @@ def main():
         graph.replay()
         t_end.record()
         torch.cuda.synchronize()
+        step_ms.append(t_start.elapsed_time(t_end))
+    for _ in range(max(10, args.steps // 4)):
+        flush.zero_()
+        kgraph.replay()
+        torch.cuda.synchronize()
         v = [vev[i].elapsed_time(vev[i + 1]) for i in range(3)]
         a = [aev[i].elapsed_time(aev[i + 1]) for i in range(2)]
-        step_ms.append(t_start.elapsed_time(t_end))
         for n, t in zip(("K1", "K2", "K3"), v):
             k_ms[n].append(t)
         for n, t in zip(("K4a", "K4b"), a):
