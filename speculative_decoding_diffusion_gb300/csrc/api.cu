@@ -51,15 +51,13 @@ EncodeTiledFn encode_fn() {
 static bool encode_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  // (64 columns, 16 slots, hd/64 column halves, heads, pages): one box is
-  // a whole page of one head, landing as [half][slot][64 columns]
-  cuuint64_t dims[5] = {64, (cuuint64_t)kPageTokens, (cuuint64_t)(hd / 64), (cuuint64_t)Hkv,
+  cuuint64_t dims[4] = {(cuuint64_t)hd, (cuuint64_t)kPageTokens, (cuuint64_t)Hkv,
                         (cuuint64_t)num_pages};
-  cuuint64_t strides[4] = {(cuuint64_t)hd * 2, 128, (cuuint64_t)kPageTokens * hd * 2,
+  cuuint64_t strides[3] = {(cuuint64_t)hd * 2, (cuuint64_t)kPageTokens * hd * 2,
                            (cuuint64_t)Hkv * kPageTokens * hd * 2};
-  cuuint32_t box[5] = {64, (cuuint32_t)kPageTokens, (cuuint32_t)(hd / 64), 1, 1};
-  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, ptr, dims, strides, box, estr,
+  cuuint32_t box[4] = {64, (cuuint32_t)kPageTokens, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

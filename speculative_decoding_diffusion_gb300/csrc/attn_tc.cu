@@ -14,13 +14,12 @@
 // two probability tiles P (so a stream's next softmax never waits for its
 // previous P.V) and output accumulator O (and running max / sum); the two
 // are merged in the epilogue.  Warp roles:
-//   warp 0     TMA producer: K and V of each block (4 pages, one box per
-//              page holding all of its columns for this head, 128-byte
-//              swizzle) into a 4-stage ring;
+//   warp 0     TMA producer: K and V of each block (4 pages, one 2 KB box
+//              per page and 64-column half, 128-byte swizzle) into a
+//              4-stage ring;
 //   warp 1     TMEM owner and MMA issuer (one thread): S = Q K^T into the
-//              stream's TMEM tile (128 x 64 fp32, one N=16 MMA chain per
-//              page), O += P V into the stream's TMEM accumulator (128 x hd
-//              fp32, one 16-key step per page); completion by commit;
+//              stream's TMEM tile (128 x 64 fp32), O += P V into the stream's
+//              TMEM accumulator (128 x hd fp32); completion by commit;
 //   warps 2-5  softmax of stream 0, warps 6-9 of stream 1, one thread per
 //              query row: S from TMEM, scale, mask, running max with an 8
 //              (log2) headroom -- O is rescaled in TMEM only when a row's
@@ -49,7 +48,7 @@ constexpr int kStreams = 2;
 constexpr int kWarps = 2 + 4 * kStreams;
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kColO = kStreams * kKeys;   // O accumulators after the S tiles
-
+constexpr int kBoxBytes = kPage * 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kHeadroom = 8.f;     // log2 units a row max may grow before O is rescaled
 
@@ -66,9 +65,8 @@ struct TcSmem {
   static constexpr int kHalfRows = kRows * 128;        // one 64-column half of a 128-row tile
   static constexpr int kQ = kHalves * kHalfRows;
   static constexpr int kP = kHalfRows;                  // 64 keys: one half
-  static constexpr int kPageHalf = kPage * 128;         // 16 slots x 64 columns
-  static constexpr int kPageBytes = kHalves * kPageHalf;  // one page of one head
-  static constexpr int kKv = kPagesPerBlock * kPageBytes;  // K or V tile of a block
+  static constexpr int kKvHalf = kKeys * 128;           // 64 keys x 64 columns
+  static constexpr int kKv = kHalves * kKvHalf;         // K or V tile of a block
   static constexpr int kStage = 2 * kKv;
   static constexpr int kOffQ = 0;
   static constexpr int kOffP = kOffQ + kQ;              // kStreams tiles
@@ -222,12 +220,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + s), n_pages * 2 * L::kPageBytes);
+      if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + s), n_pages * L::kHalves * 2 * kBoxBytes);
       __syncwarp();
       if (lane < n_pages) {
         const uint32_t kt = sKv + s * L::kStage, vt = kt + L::kKv;
-        tma_load_5d(kt + lane * L::kPageBytes, &tmK, bar(kBarKvFull + s), 0, 0, 0, kvh, page);
-        tma_load_5d(vt + lane * L::kPageBytes, &tmV, bar(kBarKvFull + s), 0, 0, 0, kvh, page);
+#pragma unroll
+        for (int hh = 0; hh < L::kHalves; ++hh) {
+          const uint32_t off = hh * L::kKvHalf + lane * kBoxBytes;
+          tma_load_4d(kt + off, &tmK, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
+          tma_load_4d(vt + off, &tmV, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
+        }
       }
       issued = j + 1;
     }
@@ -243,7 +245,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // its K/V stage and its stream's score tile free; P.V of block np needs
     // its P tile.  P.V goes in block order.
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16(kRows, kPage, 0);   // one page of keys
+      constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0);
       constexpr uint32_t idO = tc::idesc_bf16(kRows, HD, 1);
       int ns = 0, np = 0;
       uint32_t idle = 0;
@@ -255,16 +257,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
               (ns < kStreams || mbar_test(bar(kBarSEmpty + st), ((ns >> 1) - 1) & 1))) {
             tc::fence_after_sync();
             const uint32_t kt = sKv + s * L::kStage;
-            const int kb = k_begin + ns * kKeys;
-            const int pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;  // loaded pages
-            for (int pg = 0; pg < pages; ++pg) {
 #pragma unroll
-              for (int kk = 0; kk < HD / 16; ++kk) {
-                const uint32_t qa = sQ + (kk >> 2) * L::kHalfRows + (kk & 3) * 32;
-                const uint32_t ka = kt + pg * L::kPageBytes + (kk >> 2) * L::kPageHalf + (kk & 3) * 32;
-                tc::mma_bf16(tmem + st * kKeys + pg * kPage, tc::smem_desc_sw128(qa, 16, 1024),
-                             tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
-              }
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              const uint32_t qa = sQ + (kk >> 2) * L::kHalfRows + (kk & 3) * 32;
+              const uint32_t ka = kt + (kk >> 2) * L::kKvHalf + (kk & 3) * 32;
+              tc::mma_bf16(tmem + st * kKeys, tc::smem_desc_sw128(qa, 16, 1024),
+                           tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
             }
             tc::commit(bar(kBarSFull + st));
             ++ns;
@@ -287,16 +285,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
               constexpr int CH = HD / 8;
               for (int e = 0; e < (loaded - valid) * CH; ++e) {
                 const int r = valid + e / CH, c = e % CH;
-                *reinterpret_cast<uint4 *>(sb + (vt - base) + (r / kPage) * L::kPageBytes +
-                                           (c >> 3) * L::kPageHalf + swz(r % kPage, c & 7)) =
+                *reinterpret_cast<uint4 *>(sb + (vt - base) + (c >> 3) * L::kKvHalf + swz(r, c & 7)) =
                     make_uint4(0, 0, 0, 0);
               }
               fence_proxy_async_smem();
             }
             const uint32_t pt = sP + pb * L::kP;
-            for (int kk = 0; kk < loaded / kPage; ++kk)   // one 16-key step per page
+            for (int kk = 0; kk < loaded / 16; ++kk)
               tc::mma_bf16(tmem + kColO + st * HD, tc::smem_desc_sw128(pt + kk * 32, 16, 1024),
-                           tc::smem_desc_sw128(vt + kk * L::kPageBytes, L::kPageHalf, 1024), idO,
+                           tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
                            (np >= kStreams || kk > 0));
             tc::commit(bar(kBarPvDone + pb));
             tc::commit(bar(kBarKvEmpty + s));

@@ -131,16 +131,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap,
       : "memory");
 }
 
-// 5-D tiled bulk tensor load global -> shared, completion on an mbarrier.
-__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, uint32_t bar,
-                                            int c0, int c1, int c2, int c3, int c4) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-      : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -77,10 +77,9 @@ cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
-// TMA descriptor of a paged bf16 cache [num_pages][Hkv][16][hd] as the 5-D
-// tensor (64 columns, slot, column half, head, page); one box = one page of
-// one head (hd/64 halves of 16 rows x 128 bytes), 128-byte swizzle.  False
-// if the driver call fails.
+// TMA descriptor of a paged bf16 cache [num_pages][Hkv][16][hd] as the 4-D
+// tensor (hd, slot, head, page); one box = one page of one head, 64 columns
+// (128 bytes) wide, 128-byte swizzle.  False if the driver call fails.
 // Descriptors are cached per (device, pointer, sizes): repeated calls on the
 // same cache cost no driver call.
 bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd);
