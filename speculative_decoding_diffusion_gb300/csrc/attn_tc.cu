@@ -77,7 +77,8 @@ struct TcSmem {
   static constexpr int kOffBar = kOffV + kStages * kKv;
   static constexpr int kOffTau = kOffBar + kNumBars * 8;
   static constexpr int kOffMl = kOffTau + 2 * kMaxB * 4;    // stream 1's (m, l) per row
-  static constexpr int kOffMisc = kOffMl + kRows * 8;       // tmem address, error flag
+  static constexpr int kOffPid = kOffMl + kRows * 8;        // page ids of in-flight blocks
+  static constexpr int kOffMisc = kOffPid + 2 * kStages * kPagesPerBlock * 4;  // tmem addr, flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;              // 1024-byte alignment slack
   static constexpr uint32_t kTmemCols = (kColO + kStreams * HD) <= 256 ? 256 : 512;
@@ -209,63 +210,74 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    // One thread keeps both rings full: the next K block when its K stage
-    // is free, the next V block when its V stage is free, whichever first.
-    if (lane == 0) {
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
-      const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
-      int nk = 0, nv = 0;
-      bool dep_done = false;
-      uint32_t idle = 0;
-      while (nv < n_blocks) {
-        bool progressed = false;
-        if (nk < n_blocks && (nk < kStages || mbar_test(bar(kBarKEmpty + nk % kStages),
-                                                          ((nk / kStages) - 1) & 1))) {
-          const int s = nk % kStages, kb = k_begin + nk * kKeys;
-          if (!dep_done && kb + kKeys > P) { grid_dep_wait(); dep_done = true; }  // new keys from K1
-          const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
-          mbar_arrive_expect_tx(bar(kBarKFull + s), n_pages * L::kHalves * kBoxBytes);
-          for (int pg = 0; pg < n_pages; ++pg) {
-            const int page = __ldg(bt + kb / kPage + pg);
-#pragma unroll
-            for (int hh = 0; hh < L::kHalves; ++hh)
-              tma_load_4d(sK + s * L::kKv + hh * L::kKvHalf + pg * kBoxBytes, &tmK,
-                          bar(kBarKFull + s), hh * 64, 0, kvh, page);
-          }
-          ++nk;
-          progressed = true;
-        }
-        if (nv < nk && (nv < kStages || mbar_test(bar(kBarVEmpty + nv % kStages),
-                                                    ((nv / kStages) - 1) & 1))) {
-          const int s = nv % kStages, kb = k_begin + nv * kKeys;
-          const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
-          mbar_arrive_expect_tx(bar(kBarVFull + s), n_pages * L::kHalves * kBoxBytes);
-          for (int pg = 0; pg < n_pages; ++pg) {
-            const int page = __ldg(bt + kb / kPage + pg);
-#pragma unroll
-            for (int hh = 0; hh < L::kHalves; ++hh)
-              tma_load_4d(sV + s * L::kKv + hh * L::kKvHalf + pg * kBoxBytes, &tmV,
-                          bar(kBarVFull + s), hh * 64, 0, kvh, page);
-          }
-          ++nv;
-          progressed = true;
-        }
-        if (progressed) {
-          idle = 0;
-        } else if (++idle > (kWaitPolls << 4)) {  // bounded: give up, flag, drain
-          raise_status(a.status, kStatusTimeout);
-          atomicOr(flag_s, 1);
-          break;
-        }
+    // The warp keeps both rings full: the next K block when its K stage is
+    // free, the next V block when its V stage is free, whichever first.
+    // Lane 0 polls and decides; lanes 0..3 fetch a block's page ids in
+    // parallel (V reuses the ids its K fetched) and issue one box each.
+    int *pid_s = reinterpret_cast<int *>(sb + L::kOffPid);   // [2*kStages][pages]
+    if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
+    const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
+    int nk = 0, nv = 0;
+    bool dep_done = false;
+    uint32_t idle = 0;
+    while (nv < n_blocks) {
+      int canK = 0, canV = 0;
+      if (lane == 0) {
+        canK = nk < n_blocks && nk < nv + 2 * kStages &&
+               (nk < kStages || mbar_test(bar(kBarKEmpty + nk % kStages), ((nk / kStages) - 1) & 1));
+        canV = nv < nk &&
+               (nv < kStages || mbar_test(bar(kBarVEmpty + nv % kStages), ((nv / kStages) - 1) & 1));
       }
-      if (*(volatile int *)flag_s) {
-        // let copies already in flight land before the CTA can exit
-        for (int j = max(0, nk - kStages); j < nk; ++j)
-          (void)mbar_wait(bar(kBarKFull + j % kStages), (j / kStages) & 1);
-        for (int j = max(0, nv - kStages); j < nv; ++j)
-          (void)mbar_wait(bar(kBarVFull + j % kStages), (j / kStages) & 1);
+      canK = __shfl_sync(0xffffffffu, canK, 0);
+      canV = __shfl_sync(0xffffffffu, canV, 0);
+      if (canK) {
+        const int s = nk % kStages, kb = k_begin + nk * kKeys;
+        if (!dep_done && kb + kKeys > P) {   // the block holds new keys K1 writes
+          grid_dep_wait();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          dep_done = true;
+        }
+        const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
+        const int page = lane < n_pages ? __ldg(bt + kb / kPage + lane) : 0;
+        if (lane < n_pages) pid_s[(nk % (2 * kStages)) * kPagesPerBlock + lane] = page;
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + s), n_pages * L::kHalves * kBoxBytes);
+        __syncwarp();
+        if (lane < n_pages) {
+#pragma unroll
+          for (int hh = 0; hh < L::kHalves; ++hh)
+            tma_load_4d(sK + s * L::kKv + hh * L::kKvHalf + lane * kBoxBytes, &tmK,
+                        bar(kBarKFull + s), hh * 64, 0, kvh, page);
+        }
+        ++nk;
       }
+      if (canV) {
+        const int s = nv % kStages, kb = k_begin + nv * kKeys;
+        const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
+        const int page = lane < n_pages ? pid_s[(nv % (2 * kStages)) * kPagesPerBlock + lane] : 0;
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + s), n_pages * L::kHalves * kBoxBytes);
+        __syncwarp();
+        if (lane < n_pages) {
+#pragma unroll
+          for (int hh = 0; hh < L::kHalves; ++hh)
+            tma_load_4d(sV + s * L::kKv + hh * L::kKvHalf + lane * kBoxBytes, &tmV,
+                        bar(kBarVFull + s), hh * 64, 0, kvh, page);
+        }
+        ++nv;
+      }
+      if (canK || canV) {
+        idle = 0;
+      } else if (++idle > (kWaitPolls << 4)) {  // bounded: give up, flag, drain
+        if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
+        break;
+      }
+      __syncwarp();
+    }
+    if (*(volatile int *)flag_s) {
+      // let copies already in flight land before the CTA can exit
+      for (int j = max(0, nk - kStages); j < nk; ++j)
+        (void)mbar_wait_warp(bar(kBarKFull + j % kStages), (j / kStages) & 1);
+      for (int j = max(0, nv - kStages); j < nv; ++j)
+        (void)mbar_wait_warp(bar(kBarVFull + j % kStages), (j / kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
