@@ -15,10 +15,8 @@
 // previous P.V) and output accumulator O (and running max / sum); the two
 // are merged in the epilogue.  Warp roles:
 //   warp 0     TMA producer: K and V of each block (4 pages, one 2 KB box
-//              per page and 64-column half, 128-byte swizzle) into two
-//              4-stage rings -- a K stage frees as soon as its scores are
-//              computed, a V stage after its P.V, so K loads run further
-//              ahead of their use than V loads;
+//              per page and 64-column half, 128-byte swizzle) into a
+//              4-stage ring;
 //   warp 1     TMEM owner and MMA issuer (one thread): S = Q K^T into the
 //              stream's TMEM tile (128 x 64 fp32), O += P V into the stream's
 //              TMEM accumulator (128 x hd fp32); completion by commit;
@@ -56,8 +54,7 @@ constexpr float kHeadroom = 8.f;     // log2 units a row max may grow before O i
 
 constexpr int kPBufs = 2;            // P tiles per stream (double buffered)
 
-enum { kBarKFull = 0, kBarKEmpty = kBarKFull + kStages, kBarVFull = kBarKEmpty + kStages,
-       kBarVEmpty = kBarVFull + kStages, kBarSFull = kBarVEmpty + kStages,
+enum { kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarSFull = kBarKvEmpty + kStages,
        kBarSEmpty = kBarSFull + kStreams, kBarPFull = kBarSEmpty + kStreams,
        kBarPvDone = kBarPFull + kStreams * kPBufs, kBarQReady = kBarPvDone + kStreams * kPBufs,
        kNumBars = kBarQReady + 1 };
@@ -70,15 +67,14 @@ struct TcSmem {
   static constexpr int kP = kHalfRows;                  // 64 keys: one half
   static constexpr int kKvHalf = kKeys * 128;           // 64 keys x 64 columns
   static constexpr int kKv = kHalves * kKvHalf;         // K or V tile of a block
+  static constexpr int kStage = 2 * kKv;
   static constexpr int kOffQ = 0;
   static constexpr int kOffP = kOffQ + kQ;              // kStreams tiles
-  static constexpr int kOffK = kOffP + kStreams * kPBufs * kP;
-  static constexpr int kOffV = kOffK + kStages * kKv;
-  static constexpr int kOffBar = kOffV + kStages * kKv;
+  static constexpr int kOffKv = kOffP + kStreams * kPBufs * kP;
+  static constexpr int kOffBar = kOffKv + kStages * kStage;
   static constexpr int kOffTau = kOffBar + kNumBars * 8;
   static constexpr int kOffMl = kOffTau + 2 * kMaxB * 4;    // stream 1's (m, l) per row
-  static constexpr int kOffPid = kOffMl + kRows * 8;        // page ids of in-flight blocks
-  static constexpr int kOffMisc = kOffPid + 2 * kStages * kPagesPerBlock * 4;  // tmem addr, flag
+  static constexpr int kOffMisc = kOffMl + kRows * 8;       // tmem address, error flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;              // 1024-byte alignment slack
   static constexpr uint32_t kTmemCols = (kColO + kStreams * HD) <= 256 ? 256 : 512;
@@ -121,8 +117,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *sb = smem_raw + (base - raw);
-  const uint32_t sQ = base + L::kOffQ, sP = base + L::kOffP;
-  const uint32_t sK = base + L::kOffK, sV = base + L::kOffV;
+  const uint32_t sQ = base + L::kOffQ, sP = base + L::kOffP, sKv = base + L::kOffKv;
   auto bar = [&](int i) { return base + L::kOffBar + 8u * i; };
   int *tau_s = reinterpret_cast<int *>(sb + L::kOffTau);
   float2 *ml_s = reinterpret_cast<float2 *>(sb + L::kOffMl);
@@ -153,10 +148,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kBarKFull + i), 1);
-      mbar_init(bar(kBarKEmpty + i), 1);
-      mbar_init(bar(kBarVFull + i), 1);
-      mbar_init(bar(kBarVEmpty + i), 1);
+      mbar_init(bar(kBarKvFull + i), 1);
+      mbar_init(bar(kBarKvEmpty + i), 1);
     }
     for (int i = 0; i < kStreams; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
@@ -210,74 +203,40 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    // The warp keeps both rings full: the next K block when its K stage is
-    // free, the next V block when its V stage is free, whichever first.
-    // Lane 0 polls and decides; lanes 0..3 fetch a block's page ids in
-    // parallel (V reuses the ids its K fetched) and issue one box each.
-    int *pid_s = reinterpret_cast<int *>(sb + L::kOffPid);   // [2*kStages][pages]
     if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
     const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
-    int nk = 0, nv = 0;
+    int issued = 0;
     bool dep_done = false;
-    uint32_t idle = 0;
-    while (nv < n_blocks) {
-      int canK = 0, canV = 0;
-      if (lane == 0) {
-        canK = nk < n_blocks && nk < nv + 2 * kStages &&
-               (nk < kStages || mbar_test(bar(kBarKEmpty + nk % kStages), ((nk / kStages) - 1) & 1));
-        canV = nv < nk &&
-               (nv < kStages || mbar_test(bar(kBarVEmpty + nv % kStages), ((nv / kStages) - 1) & 1));
+    for (int j = 0; j < n_blocks; ++j) {
+      const int s = j % kStages;
+      const int kb = k_begin + j * kKeys;
+      if (!dep_done && kb + kKeys > P) {     // the block holds new keys K1 writes
+        grid_dep_wait();
+        dep_done = true;
       }
-      canK = __shfl_sync(0xffffffffu, canK, 0);
-      canV = __shfl_sync(0xffffffffu, canV, 0);
-      if (canK) {
-        const int s = nk % kStages, kb = k_begin + nk * kKeys;
-        if (!dep_done && kb + kKeys > P) {   // the block holds new keys K1 writes
-          grid_dep_wait();
-          asm volatile("fence.proxy.async.global;" ::: "memory");
-          dep_done = true;
-        }
-        const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
-        const int page = lane < n_pages ? __ldg(bt + kb / kPage + lane) : 0;
-        if (lane < n_pages) pid_s[(nk % (2 * kStages)) * kPagesPerBlock + lane] = page;
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKFull + s), n_pages * L::kHalves * kBoxBytes);
-        __syncwarp();
-        if (lane < n_pages) {
-#pragma unroll
-          for (int hh = 0; hh < L::kHalves; ++hh)
-            tma_load_4d(sK + s * L::kKv + hh * L::kKvHalf + lane * kBoxBytes, &tmK,
-                        bar(kBarKFull + s), hh * 64, 0, kvh, page);
-        }
-        ++nk;
-      }
-      if (canV) {
-        const int s = nv % kStages, kb = k_begin + nv * kKeys;
-        const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
-        const int page = lane < n_pages ? pid_s[(nv % (2 * kStages)) * kPagesPerBlock + lane] : 0;
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarVFull + s), n_pages * L::kHalves * kBoxBytes);
-        __syncwarp();
-        if (lane < n_pages) {
-#pragma unroll
-          for (int hh = 0; hh < L::kHalves; ++hh)
-            tma_load_4d(sV + s * L::kKv + hh * L::kKvHalf + lane * kBoxBytes, &tmV,
-                        bar(kBarVFull + s), hh * 64, 0, kvh, page);
-        }
-        ++nv;
-      }
-      if (canK || canV) {
-        idle = 0;
-      } else if (++idle > (kWaitPolls << 4)) {  // bounded: give up, flag, drain
+      const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
+      const int page = lane < n_pages ? __ldg(bt + kb / kPage + lane) : 0;   // before the wait
+      if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1)) {
         if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
         break;
       }
+      if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + s), n_pages * L::kHalves * 2 * kBoxBytes);
       __syncwarp();
+      if (lane < n_pages) {
+        const uint32_t kt = sKv + s * L::kStage, vt = kt + L::kKv;
+#pragma unroll
+        for (int hh = 0; hh < L::kHalves; ++hh) {
+          const uint32_t off = hh * L::kKvHalf + lane * kBoxBytes;
+          tma_load_4d(kt + off, &tmK, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
+          tma_load_4d(vt + off, &tmV, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
+        }
+      }
+      issued = j + 1;
     }
     if (*(volatile int *)flag_s) {
       // let copies already in flight land before the CTA can exit
-      for (int j = max(0, nk - kStages); j < nk; ++j)
-        (void)mbar_wait_warp(bar(kBarKFull + j % kStages), (j / kStages) & 1);
-      for (int j = max(0, nv - kStages); j < nv; ++j)
-        (void)mbar_wait_warp(bar(kBarVFull + j % kStages), (j / kStages) & 1);
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        (void)mbar_wait_warp(bar(kBarKvFull + j % kStages), (j / kStages) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -294,10 +253,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         bool progressed = false;
         if (ns < n_blocks) {
           const int s = ns % kStages, st = ns & 1;
-          if (mbar_test(bar(kBarKFull + s), (ns / kStages) & 1) &&
+          if (mbar_test(bar(kBarKvFull + s), (ns / kStages) & 1) &&
               (ns < kStreams || mbar_test(bar(kBarSEmpty + st), ((ns >> 1) - 1) & 1))) {
             tc::fence_after_sync();
-            const uint32_t kt = sK + s * L::kKv;
+            const uint32_t kt = sKv + s * L::kStage;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
               const uint32_t qa = sQ + (kk >> 2) * L::kHalfRows + (kk & 3) * 32;
@@ -306,7 +265,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                            tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
             }
             tc::commit(bar(kBarSFull + st));
-            tc::commit(bar(kBarKEmpty + s));    // K stage free once S is done
             ++ns;
             progressed = true;
           }
@@ -315,13 +273,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           const int st = np & 1, s = np % kStages;
           const int ib = np >> 1;                 // block index within the stream
           const int pb = st * kPBufs + (ib & 1);  // its P tile
-          if (mbar_test(bar(kBarPFull + pb), (ib >> 1) & 1) &&
-              mbar_test(bar(kBarVFull + s), (np / kStages) & 1)) {
+          if (mbar_test(bar(kBarPFull + pb), (ib >> 1) & 1)) {
             tc::fence_after_sync();
             const int kb = k_begin + np * kKeys;
             const int valid = min(kKeys, k_end - kb);
             const int loaded = (valid + kPage - 1) & ~(kPage - 1);
-            const uint32_t vt = sV + s * L::kKv;
+            const uint32_t vt = sKv + s * L::kStage + L::kKv;
             if (kb + valid == Lk && loaded > valid) {
               // slots past the sequence end in its last page hold arbitrary
               // data; P is 0 there, but 0 * NaN would poison O: zero V rows
@@ -339,7 +296,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                            tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
                            (np >= kStreams || kk > 0));
             tc::commit(bar(kBarPvDone + pb));
-            tc::commit(bar(kBarVEmpty + s));
+            tc::commit(bar(kBarKvEmpty + s));
             ++np;
             progressed = true;
           }
