@@ -26,7 +26,9 @@
 //              maximum outgrows it, which keeps the result exact (O and l
 //              share the stale reference) -- and P as bf16 into a 128-byte
 //              swizzled shared tile.
-// Q is staged once into shared memory in the same swizzled K-major layout.
+// Q lives in TMEM as the score MMA's A operand (loaded once by the stream-0
+// softmax warps, a row per thread), which leaves shared memory to the P
+// tiles and a 5-stage K/V ring.
 // Every mbarrier wait is bounded; a wait that runs out sets the status word
 // and the CTA drains and returns.
 #include <cuda.h>
@@ -43,7 +45,7 @@ namespace {
 constexpr int kRows = 128;           // query rows per CTA: the MMA's M
 constexpr int kKeys = 64;            // keys per block: S width, P.V depth
 constexpr int kPagesPerBlock = kKeys / kPage;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kStreams = 2;
 constexpr int kWarps = 2 + 4 * kStreams;
 constexpr int kThreads = kWarps * 32;
@@ -63,13 +65,11 @@ template <int HD>
 struct TcSmem {
   static constexpr int kHalves = HD / 64;
   static constexpr int kHalfRows = kRows * 128;        // one 64-column half of a 128-row tile
-  static constexpr int kQ = kHalves * kHalfRows;
   static constexpr int kP = kHalfRows;                  // 64 keys: one half
   static constexpr int kKvHalf = kKeys * 128;           // 64 keys x 64 columns
   static constexpr int kKv = kHalves * kKvHalf;         // K or V tile of a block
   static constexpr int kStage = 2 * kKv;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffP = kOffQ + kQ;              // kStreams tiles
+  static constexpr int kOffP = 0;                       // kStreams x kPBufs tiles
   static constexpr int kOffKv = kOffP + kStreams * kPBufs * kP;
   static constexpr int kOffBar = kOffKv + kStages * kStage;
   static constexpr int kOffTau = kOffBar + kNumBars * 8;
@@ -77,7 +77,8 @@ struct TcSmem {
   static constexpr int kOffMisc = kOffMl + kRows * 8;       // tmem address, error flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;              // 1024-byte alignment slack
-  static constexpr uint32_t kTmemCols = (kColO + kStreams * HD) <= 256 ? 256 : 512;
+  static constexpr uint32_t kColQ = kColO + kStreams * HD;  // Q: hd bf16 = hd/2 columns
+  static constexpr uint32_t kTmemCols = (kColQ + HD / 2) <= 256 ? 256 : 512;
 };
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -117,7 +118,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *sb = smem_raw + (base - raw);
-  const uint32_t sQ = base + L::kOffQ, sP = base + L::kOffP, sKv = base + L::kOffKv;
+  const uint32_t sP = base + L::kOffP, sKv = base + L::kOffKv;
   auto bar = [&](int i) { return base + L::kOffBar + 8u * i; };
   int *tau_s = reinterpret_cast<int *>(sb + L::kOffTau);
   float2 *ml_s = reinterpret_cast<float2 *>(sb + L::kOffMl);
@@ -172,27 +173,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   if (warp != 0) {
-    // Q tile -> shared memory (K-major, 128-byte swizzle) and the P tiles
-    // zeroed once (padding rows are never written again), while the
-    // producer already streams K and V; then arrive on the Q barrier
+    // tau, the P tiles zeroed once (padding rows are never written again),
+    // and Q into TMEM -- one row per thread of the stream-0 softmax warps,
+    // two bf16 per column -- while the producer already streams K and V;
+    // then arrive on the Q barrier
     const int t = threadIdx.x - 32, nt = kThreads - 32;
     for (int j = t; j < 2 * B; j += nt) tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
-    grid_dep_wait();                         // rotated q comes from the rotation kernel
-    const __nv_bfloat16 *q = (const __nv_bfloat16 *)a.q_rot;
-    constexpr int CH = HD / 8;
-    for (int e = t; e < kRows * CH; e += nt) {
-      const int r = e / CH, c = e % CH;
-      const int grow = row0 + r;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (grow < M) {
-        const long qrow = (2L * c0 + grow / a.G) * a.Hq + kvh * a.G + grow % a.G;
-        v = *reinterpret_cast<const uint4 *>(q + qrow * HD + c * 8);
-      }
-      *reinterpret_cast<uint4 *>(sb + L::kOffQ + (c >> 3) * L::kHalfRows + swz(r, c & 7)) = v;
-    }
     for (int e = t; e < kStreams * kPBufs * L::kP / 16; e += nt)
       reinterpret_cast<uint4 *>(sb + L::kOffP)[e] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
+    if (warp >= 2 && warp < 6) {
+      grid_dep_wait();                       // rotated q comes from the rotation kernel
+      const int q4 = warp & 3, r = 32 * q4 + lane, grow = row0 + r;
+      const uint4 *qrow = nullptr;
+      if (grow < M)
+        qrow = reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q_rot +
+                                               ((2L * c0 + grow / a.G) * a.Hq + kvh * a.G + grow % a.G) * HD);
+#pragma unroll
+      for (int c = 0; c < HD / 64; ++c) {     // 64 bf16 = 32 columns per store
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 v = qrow ? __ldg(qrow + 8 * c + e) : make_uint4(0, 0, 0, 0);
+          w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
+        }
+        tc::st32(tmem + ((uint32_t)(32 * q4) << 16) + L::kColQ + 32 * c, w);
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(kBarQReady));
     // every consumer needs the whole Q tile, tau and zeroed P tiles
@@ -259,10 +268,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             const uint32_t kt = sKv + s * L::kStage;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
-              const uint32_t qa = sQ + (kk >> 2) * L::kHalfRows + (kk & 3) * 32;
               const uint32_t ka = kt + (kk >> 2) * L::kKvHalf + (kk & 3) * 32;
-              tc::mma_bf16(tmem + st * kKeys, tc::smem_desc_sw128(qa, 16, 1024),
-                           tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
+              tc::mma_bf16_ts(tmem + st * kKeys, tmem + L::kColQ + kk * 8,
+                              tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
             }
             tc::commit(bar(kBarSFull + st));
             ++ns;
