@@ -2,7 +2,8 @@
 
 One step = the whole hot path over one batch: simsd_verify_attn (K1 RoPE-copy
 + paged append, K2 split-KV masked attention, K3 split merge) and
-simsd_accept (K4a-K4d rejection sampling along tau).  Default workload: the
+simsd_accept (K4a vocabulary max/sum-exp and the walk along tau, K4b the
+residual draw at a rejection).  Default workload: the
 SDAR-8B-shaped verify step (16 sequences, prompt KV 1024, B = 4, 32/8 heads,
 head dim 128, vocabulary 151,936, bf16), seeded synthetic data.
 

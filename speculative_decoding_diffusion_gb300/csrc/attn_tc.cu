@@ -16,7 +16,7 @@
 // are merged in the epilogue.  Warp roles:
 //   warp 0     TMA producer: K and V of each block (4 pages, one 2 KB box
 //              per page and 64-column half, 128-byte swizzle) into a
-//              4-stage ring;
+//              5-stage ring;
 //   warp 1     TMEM owner and MMA issuer (one thread): S = Q K^T into the
 //              stream's TMEM tile (128 x 64 fp32), O += P V into the stream's
 //              TMEM accumulator (128 x hd fp32); completion by commit;

@@ -1,4 +1,4 @@
-"""GPU parity of simsd_accept (K4a-K4d) against the fp64 oracle.
+"""GPU parity of simsd_accept (K4a, K4b) against the fp64 oracle.
 
 Decisions (accepted length, rejected position, drawn token) must match the
 oracle exactly on the same logits and uniforms, except for tie-zone
