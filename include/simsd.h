@@ -28,7 +28,12 @@
  *     D_1..D_B, D~_1..D~_B (2B tokens); sequences are back to back, so
  *     sequence b's tokens start at row 2*cu_B[b].
  *   - Limits: head_dim in {64, 128}; num_q_heads % num_kv_heads == 0;
- *     1 <= B_b <= 32; page_size == 16; batch >= 1.
+ *     1 <= B_b <= 32; page_size == 16; batch >= 1; one new token's raw
+ *     q, k and v rows together at most 196,608 bytes
+ *     ((num_q_heads + 2 num_kv_heads) * head_dim * element size).
+ *   - Every device array of q, k, v, cache or output values starts on a
+ *     16-byte boundary (SIMSD_ERR_ALIGN otherwise); logits may be unaligned
+ *     (slower element-wise loads).
  *   - The library is stateless and re-entrant.  Calls on different streams
  *     must not share a workspace or write the same cache pages.
  */
@@ -50,7 +55,8 @@ typedef enum {
   SIMSD_ERR_DTYPE = 4,     /* unsupported dtype                             */
   SIMSD_ERR_WORKSPACE = 5, /* workspace missing, misaligned or too small    */
   SIMSD_ERR_CUDA = 6,      /* a CUDA runtime call or launch failed          */
-  SIMSD_ERR_TIMEOUT = 7    /* a device-side bounded wait ran out            */
+  SIMSD_ERR_TIMEOUT = 7,   /* a device-side bounded wait ran out            */
+  SIMSD_ERR_ALIGN = 8      /* a device array is not 16-byte aligned         */
 } simsd_status;
 
 typedef enum { SIMSD_F32 = 0, SIMSD_BF16 = 1 } simsd_dtype;
@@ -195,7 +201,8 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * residual chunk of the rejected slot; the last CTA of a sequence draws).
  *   target_logits, draft_logits device [total_B][vocab] (dtype); row k of
  *                sequence b (at cu_B[b]+k) holds the logits read at D~_k
- *   draft_tokens device int32[total_B] in [0, vocab)
+ *   draft_tokens device int32[total_B] in [0, vocab); a token outside
+ *                sets the status word's bad-input bit and its step rejects
  *   tau, cu_B    device, as for simsd_verify_attn
  *   uniforms     device float32[batch][B_max+1], values in [0, 1)
  *   n_accept     device int32[batch] out: accepted prefix length (0..B_b)
@@ -204,6 +211,9 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  *                layout has no slot after D~_B)
  *   pos          device int32[batch] out: response position (0-based k) of
  *                the rejected slot, -1 when none
+ * Limits: 1 <= vocab <= 2^30; total_B <= 65535.
+ * Errors: SIMSD_ERR_NULL, SIMSD_ERR_SHAPE, SIMSD_ERR_DTYPE,
+ * SIMSD_ERR_WORKSPACE, SIMSD_ERR_CUDA.
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t batch;

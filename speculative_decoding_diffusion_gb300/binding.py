@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libsimsd.so")
 SIMSD_F32, SIMSD_BF16 = 0, 1
 STATUS = {0: "SIMSD_OK", 1: "SIMSD_ERR_NULL", 2: "SIMSD_ERR_SHAPE",
           3: "SIMSD_ERR_TAU", 4: "SIMSD_ERR_DTYPE", 5: "SIMSD_ERR_WORKSPACE",
-          6: "SIMSD_ERR_CUDA", 7: "SIMSD_ERR_TIMEOUT"}
+          6: "SIMSD_ERR_CUDA", 7: "SIMSD_ERR_TIMEOUT", 8: "SIMSD_ERR_ALIGN"}
 
 _i32, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
 

@@ -143,6 +143,8 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
   p->G = d->num_q_heads / d->num_kv_heads;
   p->M_max = 2 * d->B_max * p->G;
   p->esize = d->dtype == SIMSD_BF16 ? 2 : 4;
+  if ((size_t)(d->num_q_heads + 2 * d->num_kv_heads) * d->head_dim * p->esize > kMaxRowBytes)
+    return SIMSD_ERR_SHAPE;
   if (d->dtype == SIMSD_BF16) {
     p->rows_per_tile = 128;   // the tensor-core tile's M; smaller tiles are padded
     p->key_splits = 1;
@@ -206,6 +208,7 @@ const char *simsd_status_string(int status) {
     case SIMSD_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SIMSD_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case SIMSD_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+    case SIMSD_ERR_ALIGN: return "a device array is not 16-byte aligned";
     default: return "unknown status";
   }
 }
@@ -270,6 +273,9 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   if (!d->q || !d->k_cache || !d->v_cache || !d->block_table || !d->k_new ||
       !d->v_new || !d->tau || !d->lens || !d->cu_B || !d->out)
     return SIMSD_ERR_NULL;
+  if (!aligned16(d->q) || !aligned16(d->k_cache) || !aligned16(d->v_cache) ||
+      !aligned16(d->k_new) || !aligned16(d->v_new) || !aligned16(d->out))
+    return SIMSD_ERR_ALIGN;
   if (d->workspace == nullptr || ((uintptr_t)d->workspace % kAlign) != 0 ||
       d->workspace_bytes < p.total)
     return SIMSD_ERR_WORKSPACE;
@@ -325,6 +331,8 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream_ptr) {
   if (!d->k || !d->v || !d->start || !d->cu_n || !d->k_cache || !d->v_cache ||
       !d->block_table)
     return SIMSD_ERR_NULL;
+  if (!aligned16(d->k) || !aligned16(d->v) || !aligned16(d->k_cache) || !aligned16(d->v_cache))
+    return SIMSD_ERR_ALIGN;
   if (d->total_n == 0) return SIMSD_OK;
   return launch_rope_append(d, (cudaStream_t)stream_ptr) == cudaSuccess ? SIMSD_OK
                                                                         : SIMSD_ERR_CUDA;

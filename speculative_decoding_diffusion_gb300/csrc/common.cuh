@@ -131,6 +131,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap,
       : "memory");
 }
 
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a
+// multiple of 16), completion on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -15,6 +15,9 @@ namespace simsd {
 constexpr int kBlockKeys = 128;   // keys per pipeline stage of the attention
 constexpr int kPageTokens = 16;  // tokens per KV-cache page (ABI page_size)
 constexpr int kMaxB = 32;
+constexpr size_t kMaxRowBytes = 192 * 1024;   // raw q + k + v of one new token (staged in smem)
+
+inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 constexpr size_t kAlign = 256;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -96,8 +96,8 @@ __device__ __forceinline__ void rotate_rows(const T *__restrict__ src, T *__rest
       const int i = i0 + u * blockDim.x;
       if (i < items) {
         const T *x = src + (long)(i / per_head) * hd + (i % per_head) * N;
-        va[u] = __ldg(reinterpret_cast<const typename VT::V *>(x));
-        vb[u] = __ldg(reinterpret_cast<const typename VT::V *>(x + half));
+        va[u] = *reinterpret_cast<const typename VT::V *>(x);
+        vb[u] = *reinterpret_cast<const typename VT::V *>(x + half);
       }
     }
 #pragma unroll
@@ -134,8 +134,8 @@ __device__ __forceinline__ void copy_rows(const T *__restrict__ src, T *__restri
     for (int u = 0; u < BATCH; ++u) {
       const int i = i0 + u * blockDim.x;
       if (i < items)
-        v[u] = __ldg(reinterpret_cast<const typename VT::V *>(src + (long)(i / per_head) * hd +
-                                                               (i % per_head) * N));
+        v[u] = *reinterpret_cast<const typename VT::V *>(src + (long)(i / per_head) * hd +
+                                                         (i % per_head) * N);
     }
 #pragma unroll
     for (int u = 0; u < BATCH; ++u) {
@@ -168,21 +168,25 @@ constexpr int kStageSeqs = 2048;   // sequences whose cu_B / lens fit the smem s
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
+  extern __shared__ __align__(16) uint8_t rows_s[];   // raw q | k | v rows of the token
   __shared__ float2 cs[64];
   __shared__ int32_t cu_s[kStageSeqs + 1], lens_s[kStageSeqs];
+  __shared__ __align__(8) uint64_t bar_s;
   grid_dep_launch();                         // the attention kernel may start its prologue
   const int r = blockIdx.x;                  // new-token row
-  // this token's rows are needed whatever its sequence: start them towards L2
-  {
-    const char *qrow = (const char *)a.q + (long)r * a.Hq * a.hd * sizeof(T);
-    const char *krow = (const char *)a.k_new + (long)r * a.Hkv * a.hd * sizeof(T);
-    const char *vrow = (const char *)a.v_new + (long)r * a.Hkv * a.hd * sizeof(T);
-    const int qlines = a.Hq * a.hd * (int)sizeof(T) / 128, kvlines = a.Hkv * a.hd * (int)sizeof(T) / 128;
-    for (int i = threadIdx.x; i < qlines; i += blockDim.x) prefetch_l2(qrow + 128 * i);
-    for (int i = threadIdx.x; i < kvlines; i += blockDim.x) {
-      prefetch_l2(krow + 128 * i);
-      prefetch_l2(vrow + 128 * i);
-    }
+  const uint32_t qbytes = (uint32_t)(a.Hq * a.hd * sizeof(T));
+  const uint32_t kvbytes = (uint32_t)(a.Hkv * a.hd * sizeof(T));
+  const uint32_t bar = smem_u32(&bar_s), rows = smem_u32(rows_s);
+  // the token's raw rows are needed whatever its sequence: one thread starts
+  // three bulk copies into shared memory before anything else
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(bar, qbytes + 2 * kvbytes);
+    bulk_load(rows, (const char *)a.q + (long)r * qbytes, qbytes, bar);
+    bulk_load(rows + qbytes, (const char *)a.k_new + (long)r * kvbytes, kvbytes, bar);
+    bulk_load(rows + qbytes + kvbytes, (const char *)a.v_new + (long)r * kvbytes, kvbytes, bar);
   }
   // sequence of the token: cu_B (and lens) staged once, searched in smem
   int b, c0, B, P;
@@ -201,29 +205,31 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
     P = __ldg(a.lens + b);
   }
   if (threadIdx.x == 0) a.tok_seq[r] = b;    // the merge kernel reads it
-  if (B < 1 || B > kMaxSection || P < 0 || (long)P + 2 * B > (long)a.max_pages * kPage) {
-    if (threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
-    return;                                  // malformed sequence: write nothing
-  }
   const int j = r - 2 * c0;                  // 0..2B-1 within the sequence
   const int k = j < B ? j : j - B;           // response index (0-based)
   const int pos = P + k;                     // D~_k copies D_k's position
   const int slot = P + j;                    // layout index = cache slot
-  const int page = j < 2 * B ? __ldg(a.block_table + (long)b * a.max_pages + slot / kPage) : -1;
-  if (page < 0 || page >= a.num_pages) {     // cu_B or block table out of range
-    if (threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
+  bool ok = !(B < 1 || B > kMaxSection || P < 0 || (long)P + 2 * B > (long)a.max_pages * kPage);
+  const int page = ok ? __ldg(a.block_table + (long)b * a.max_pages + slot / kPage) : -1;
+  ok = ok && page >= 0 && page < a.num_pages;   // cu_B or block table out of range
+  if (!ok && threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
+  if (ok) angles(a.tab, a.hd, pos, cs);
+  __syncthreads();
+  // every exit waits for the copies into this CTA's shared memory
+  if (!mbar_wait(bar, 0)) {
+    if (threadIdx.x == 0) raise_status(a.status, kStatusTimeout);
+    (void)mbar_wait(bar, 0);
     return;
   }
-  angles(a.tab, a.hd, pos, cs);
-  __syncthreads();
-  const T *q = (const T *)a.q + (long)r * a.Hq * a.hd;
-  rotate_rows<T>(q, (T *)a.q_rot + (long)r * a.Hq * a.hd, a.Hq, a.hd, a.hd, cs);
+  if (!ok) return;                           // malformed sequence: write nothing
+  const T *qs = reinterpret_cast<const T *>(rows_s);
+  const T *ks = reinterpret_cast<const T *>(rows_s + qbytes);
+  const T *vs = reinterpret_cast<const T *>(rows_s + qbytes + kvbytes);
+  rotate_rows<T>(qs, (T *)a.q_rot + (long)r * a.Hq * a.hd, a.Hq, a.hd, a.hd, cs);
   const long base = ((long)page * a.Hkv * kPage + slot % kPage) * a.hd;
   const long stride = (long)kPage * a.hd;    // next KV head, same slot
-  rotate_rows<T>((const T *)a.k_new + (long)r * a.Hkv * a.hd,
-                 (T *)a.k_cache + base, a.Hkv, a.hd, stride, cs);
-  copy_rows<T>((const T *)a.v_new + (long)r * a.Hkv * a.hd,
-               (T *)a.v_cache + base, a.Hkv, a.hd, stride);
+  rotate_rows<T>(ks, (T *)a.k_cache + base, a.Hkv, a.hd, stride, cs);
+  copy_rows<T>(vs, (T *)a.v_cache + base, a.Hkv, a.hd, stride);
 }
 
 struct RopeAppendArgs {
@@ -282,10 +288,17 @@ cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
   a.Hkv = d->num_kv_heads;
   a.hd = d->head_dim;
   a.max_pages = d->max_pages_per_seq;
+  const size_t smem = (size_t)(a.Hq + 2 * a.Hkv) * a.hd * p.esize;   // <= kMaxRowBytes
+  const void *kern = d->dtype == SIMSD_BF16 ? (const void *)rope_verify_kernel<__nv_bfloat16>
+                                            : (const void *)rope_verify_kernel<float>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   if (d->dtype == SIMSD_BF16)
-    rope_verify_kernel<__nv_bfloat16><<<p.T, kThreads, 0, stream>>>(a);
+    rope_verify_kernel<__nv_bfloat16><<<p.T, kThreads, smem, stream>>>(a);
   else
-    rope_verify_kernel<float><<<p.T, kThreads, 0, stream>>>(a);
+    rope_verify_kernel<float><<<p.T, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -42,7 +42,7 @@ def test_exports_every_declared_function(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert lib.simsd_version() >= 100
-    for code in range(8):
+    for code in range(9):
         assert binding.status_string(code) != "unknown status"
 
 
@@ -119,6 +119,11 @@ def test_verify_workspace_errors(lib):
     d.workspace = fake
     d.workspace_bytes = lib.simsd_verify_workspace_size(ctypes.byref(d)) - 1
     assert lib.simsd_verify_attn(ctypes.byref(d), None) == 5
+    # value arrays off a 16-byte boundary are refused before the workspace
+    for f in ("q", "k_cache", "v_cache", "k_new", "v_new", "out"):
+        setattr(d, f, fake + 8)
+        assert lib.simsd_verify_attn(ctypes.byref(d), None) == 8, f
+        setattr(d, f, fake)
 
 
 def test_accept_errors(lib):
@@ -147,3 +152,18 @@ def test_append_errors(lib):
     d = binding.AppendDesc()
     assert lib.simsd_prompt_append(ctypes.byref(d), None) == 2
     assert lib.simsd_prompt_append(None, None) == 1
+    fake = 1 << 40
+    for k, v in dict(batch=1, num_kv_heads=2, head_dim=128, page_size=16, num_pages=4,
+                     max_pages_per_seq=4, total_n=3, dtype=1, rope_base=1e4).items():
+        setattr(d, k, v)
+    for f in ("k", "v", "start", "cu_n", "k_cache", "v_cache", "block_table"):
+        setattr(d, f, fake)
+    d.k = fake + 4
+    assert lib.simsd_prompt_append(ctypes.byref(d), None) == 8
+
+
+def test_verify_row_bytes_limit(lib):
+    # (Hq + 2 Hkv) * hd * 4 bytes above 192 KiB: one token's rows cannot be staged
+    assert lib.simsd_verify_workspace_size(ctypes.byref(_desc(num_q_heads=376, num_kv_heads=8,
+                                                              dtype=binding.SIMSD_F32))) == 0
+    assert lib.simsd_verify_workspace_size(ctypes.byref(_desc(num_q_heads=376, num_kv_heads=8))) > 0
