@@ -196,9 +196,10 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  *   accept iff u[t-1] * q(x) < p(x);
  *   at the first rejection draw a token from max(0, p - q) normalised (p
  *   itself if that is empty) by inverse CDF with u[B_b], and stop.
- * Kernels: K4a (per slot and vocabulary chunk: max and sum of exponentials
- * of both rows; the last CTA of a sequence walks its steps), K4b (per
- * residual chunk of the rejected slot; the last CTA of a sequence draws).
+ * Kernel: K4, one thread-block cluster of 8 CTAs per sequence, each CTA
+ * owning an eighth of the vocabulary: max and sum of exponentials of both
+ * rows of every slot, the walk of the steps, and at a rejection the
+ * residual masses and the inverse-CDF draw -- all on chip.
  *   target_logits, draft_logits device [total_B][vocab] (dtype); row k of
  *                sequence b (at cu_B[b]+k) holds the logits read at D~_k
  *   draft_tokens device int32[total_B] in [0, vocab); a token outside
@@ -211,7 +212,11 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  *                layout has no slot after D~_B)
  *   pos          device int32[batch] out: response position (0-based k) of
  *                the rejected slot, -1 when none
- * Limits: 1 <= vocab <= 2^30; total_B <= 65535.
+ * Limits: 1 <= vocab <= 2^21; batch <= 65535.  Rows whose byte length is
+ * a multiple of 16 (and 16-byte aligned logits) are streamed by bulk
+ * copies; other vocabularies take a slower element-wise copy.
+ * Workspace: the status word only (simsd_accept_workspace_size returns 256
+ * for every valid size).
  * Errors: SIMSD_ERR_NULL, SIMSD_ERR_SHAPE, SIMSD_ERR_DTYPE,
  * SIMSD_ERR_WORKSPACE, SIMSD_ERR_CUDA.
  * ---------------------------------------------------------------------- */
@@ -238,7 +243,7 @@ size_t simsd_accept_workspace_size(const simsd_accept_desc *d);
 simsd_status simsd_accept(const simsd_accept_desc *d, void *stream);
 
 /* Same as simsd_accept, recording events (cudaEvent_t or NULL) on `stream`:
- * events[0] before K4a, [1] after K4a, [2] after K4b. */
+ * events[0] before K4, [1] and [2] after it. */
 simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
                                 void *const events[3]);
 
@@ -255,7 +260,8 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
  * bytes that every GPU loading the library holds until the process exits.
  *   - It calls no cudaMalloc, cudaFree or allocating library routine.
  *   - Sizes whose scratch (what simsd_accept_workspace_size reports) exceeds
- *     the array are rejected with SIMSD_ERR_WORKSPACE before any launch.
+ *     the array are rejected with SIMSD_ERR_WORKSPACE before any launch
+ *     (none at present: the scratch is one status word for every size).
  *   - The first call on each device looks up the array's device address
  *     (once per device, with that device current); make that first call
  *     before any stream capture.
@@ -266,7 +272,7 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
  *   - The kernels' status word lives in that array, so simsd_read_status
  *     cannot read it; device-detected input errors are not reported here.
  * ---------------------------------------------------------------------- */
-#define SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+#define SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES ((size_t)4096)
 simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream);
 
 /* ------------------------------------------------------------------------

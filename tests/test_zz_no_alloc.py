@@ -6,7 +6,8 @@ cudaMalloc.  The no-allocation entry point keeps its scratch in a static
 device array instead.  Its decisions must equal those of simsd_accept (the
 same kernels on the same inputs, so integers compare exactly), on two calls
 in a row -- the second call sees the first call's leftovers in the shared
-array -- and sizes beyond the array are refused before anything runs.
+array -- and the static array covers the scratch of every valid size
+(one status word), while invalid sizes are refused before anything runs.
 
 This file is named to be collected last: it must pass both on its own in a
 fresh process and after every other test.
@@ -50,16 +51,21 @@ def test_noalloc_matches_workspace_entry_point_twice():
         assert (got[0] >= 0).all()
 
 
-def test_noalloc_rejects_sizes_beyond_its_array():
-    # 4096 slots x vocab 1e6 needs far more scratch than the static array
+def test_noalloc_scratch_covers_every_size_and_refuses_bad_ones():
+    lib = binding.lib()
     d = binding.AcceptDesc()
-    for k, v in dict(batch=4096, vocab=1_000_000, total_B=4096, B_max=1,
-                     dtype=binding.SIMSD_BF16).items():
+    for k, v in dict(batch=4096, vocab=1 << 21, total_B=4096 * 32, B_max=32,
+                     dtype=binding.SIMSD_F32).items():
         setattr(d, k, v)
-    fake = 1 << 40   # never dereferenced: the call returns before launching
+    # the largest valid sizes still need only the status word
+    assert 0 < lib.simsd_accept_workspace_size(d) <= 4096
+    fake = 1 << 40   # never dereferenced: every call below returns before launching
     for f in ("target_logits", "draft_logits", "draft_tokens", "tau", "cu_B",
               "uniforms", "n_accept", "token", "pos"):
         setattr(d, f, fake)
-    lib = binding.lib()
-    assert lib.simsd_accept_workspace_size(d) > 8 << 20
-    assert lib.simsd_accept_noalloc(d, None) == 5   # SIMSD_ERR_WORKSPACE
+    d.vocab = (1 << 21) + 1                          # beyond the vocabulary limit
+    assert lib.simsd_accept_workspace_size(d) == 0
+    assert lib.simsd_accept_noalloc(d, None) == 2    # SIMSD_ERR_SHAPE
+    d.vocab = 1000
+    d.target_logits = None
+    assert lib.simsd_accept_noalloc(d, None) == 1    # SIMSD_ERR_NULL
