@@ -8,9 +8,9 @@
 // first rejection a token is drawn from max(0, p - q) normalised (p itself
 // when that is empty) by inverse CDF with u[B].
 //
-// One launch; one thread-block cluster of C CTAs per sequence (C <= 8, the
-// largest size whose clusters for the whole batch are resident at once --
-// 7 or 8 on GB300 for small batches), CTA r owning the vocabulary slice
+// One launch; one thread-block cluster of C CTAs per sequence (C <= 8, from
+// a makespan estimate over the resident-cluster waves: 6-8 for small
+// batches, 1-2 for large ones), CTA r owning the vocabulary slice
 // [r * per, (r + 1) * per) of every row of the sequence.  Each CTA streams its slices of the 2B rows (target and draft of
 // every slot) through a 5-stage shared-memory ring of 32 KB pieces filled by
 // bulk copies (one producer warp; 16 consumer warps):
@@ -237,7 +237,7 @@ struct AcceptParams {
   int32_t *token;
   int32_t *pos;
   uint32_t *status;
-  int batch, vocab, B_max;
+  int batch, vocab, B_max, total_B;
   int csize;   // CTAs per cluster (one cluster per sequence)
   int per;     // entries per CTA slice (a multiple of 16 bytes' worth)
   int piece;   // entries per ring stage
@@ -774,18 +774,27 @@ cudaError_t max_active_clusters(int dev, int csize, int *out) {
 template <typename T>
 cudaError_t launch(AcceptParams a, cudaStream_t stream) {
   const int dev = current_device();
-  // the largest cluster whose clusters for the whole batch fit at once; 8
-  // when none does (several waves either way); never so small that a slice
-  // needs more pieces than the kernel tracks
+  // Cluster size by a makespan estimate: clusters run in waves of the
+  // resident count; a CTA's time is its share of the sequence's exponentials
+  // (16 per clock per SM: the MUFU rate) plus the fixed cost of the walk,
+  // residual and draw phases.  Small batches get large clusters (every SM
+  // busy), large batches small ones (fewer waves).  Never so small that a
+  // slice needs more pieces than the kernel tracks.
   const int piece = kStageBytes / (int)sizeof(T), vec = 16 / (int)sizeof(T);
   const int64_t max_slice = (int64_t)kMaxPieces * piece;
+  const double per_seq = (2.0 * a.total_B / a.batch + 2.0) * a.vocab;   // exponentials
+  constexpr double kPhaseCycles = 20000.0;
   int csize = kMaxCluster;
-  for (int c = kMaxCluster; c >= 4; --c) {
+  double best = 1e300;
+  for (int c = kMaxCluster; c >= 1; --c) {
     if (((int64_t)a.vocab + c - 1) / c > max_slice) break;
     int n = 0;
     cudaError_t e = max_active_clusters<T>(dev, c, &n);
     if (e != cudaSuccess) return e;
-    if (n >= a.batch) { csize = c; break; }
+    if (n <= 0) continue;
+    const double waves = (double)((a.batch + n - 1) / n);
+    const double cost = waves * (per_seq / c / 16.0 + kPhaseCycles);
+    if (cost < best * (1.0 - 1e-9)) { best = cost; csize = c; }
   }
   a.csize = csize;
   a.per = ((a.vocab + csize - 1) / csize + vec - 1) / vec * vec;
@@ -853,6 +862,7 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t strea
   a.batch = d->batch;
   a.vocab = d->vocab;
   a.B_max = d->B_max;
+  a.total_B = d->total_B;
   const int es = d->dtype == SIMSD_BF16 ? 2 : 4;
   // slices of whole 16-byte vectors (set with the cluster size at launch);
   // a piece is one ring stage

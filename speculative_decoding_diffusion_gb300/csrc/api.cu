@@ -178,7 +178,9 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
   // workspace
   size_t off = 0;
   p->off_status = off;  off = align_up(off + sizeof(uint32_t), kAlign);
-  p->off_qrot = off;    off = align_up(off + (size_t)p->T * d->num_q_heads * d->head_dim * p->esize, kAlign);
+  p->off_qrot = off;    // rotated queries: the fp32 path only (the bf16 kernel rotates its own)
+  if (d->dtype == SIMSD_F32)
+    off = align_up(off + (size_t)p->T * d->num_q_heads * d->head_dim * p->esize, kAlign);
   p->off_tokseq = off;  off = align_up(off + (size_t)p->T * sizeof(int32_t), kAlign);
   p->off_opart = off;
   if (p->n_splits > 1) {
@@ -292,7 +294,9 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
     return SIMSD_ERR_CUDA;
   AttnParams a;
   memset(&a, 0, sizeof(a));
+  a.q = d->q;
   a.q_rot = q_rot;
+  make_rope_table(d->rope_base, d->head_dim, &a.tab);
   a.out = d->out;
   a.o_part = (float *)(ws + p.off_opart);
   a.ml_part = (float2 *)(ws + p.off_ml);

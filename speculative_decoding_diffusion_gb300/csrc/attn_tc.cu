@@ -9,76 +9,76 @@
 // One CTA per (key split, KV head x 128-row tile, sequence).  The query tile
 // stacks the 2B tokens x G query heads of one KV head (row = token*G + head
 // in group; rows past 2B*G are zero padding), so each key/value byte read
-// from HBM serves every row.  The CTA's keys come in 64-key blocks dealt
-// alternately to two independent streams, each with its own score tile S,
-// two probability tiles P (so a stream's next softmax never waits for its
-// previous P.V) and output accumulator O (and running max / sum); the two
-// are merged in the epilogue.  Warp roles:
-//   warp 0     TMA producer: K and V of each block (4 pages, one 2 KB box
+// from HBM serves every row.  Keys come in 128-key blocks: an MMA
+// instruction costs nearly the same at N = 64 as at N = 128, so wide score
+// tiles halve the instructions per key.  Warp roles:
+//   warp 0     TMA producer: K and V of each block (8 pages, one 2 KB box
 //              per page and 64-column half, 128-byte swizzle) into a
-//              5-stage ring;
-//   warp 1     TMEM owner and MMA issuer (one thread): S = Q K^T into the
-//              stream's TMEM tile (128 x 64 fp32), O += P V into the stream's
-//              TMEM accumulator (128 x hd fp32); completion by commit;
-//   warps 2-5  softmax of stream 0, warps 6-9 of stream 1, one thread per
-//              query row: S from TMEM, scale, mask, running max with an 8
+//              3-stage ring;
+//   warp 1     TMEM owner and MMA issuer (one thread, never blocking on one
+//              barrier): S = Q K^T into one of two TMEM score tiles (128 x
+//              128 fp32), O += P V into the TMEM accumulator (128 x hd fp32)
+//              with P read from TMEM as the A operand; completion by commit;
+//   warps 2-5  softmax, one thread per query row: S from TMEM (a max pass,
+//              then an exponent pass), scale, mask, running max with an 8
 //              (log2) headroom -- O is rescaled in TMEM only when a row's
 //              maximum outgrows it, which keeps the result exact (O and l
-//              share the stale reference) -- and P as bf16 into a 128-byte
-//              swizzled shared tile.
-// Q lives in TMEM as the score MMA's A operand (loaded once by the stream-0
-// softmax warps, a row per thread), which leaves shared memory to the P
-// tiles and a 5-stage K/V ring.
-// Every mbarrier wait is bounded; a wait that runs out sets the status word
-// and the CTA drains and returns.
+//              share the stale reference) -- and P as bf16 written back
+//              over the score tile it came from.  Warps whose rows are all
+//              padding sit out the key loop.
+// Q lives in TMEM as the score MMA's A operand: the softmax warps rotate the
+// raw queries themselves (a cos/sin table for the section's B positions in
+// shared memory), so the kernel waits for the cache append only before the
+// block holding the new keys.  Every mbarrier wait is
+// bounded; a wait that runs out sets the status word and the CTA drains and
+// returns.
 #include <cuda.h>
 
 #include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
+#include "rope.cuh"
 #include "tc.cuh"
 
 namespace simsd {
 namespace {
 
 constexpr int kRows = 128;           // query rows per CTA: the MMA's M
-constexpr int kKeys = 64;            // keys per block: S width, P.V depth
-constexpr int kPagesPerBlock = kKeys / kPage;
-constexpr int kStages = 5;
-constexpr int kStreams = 2;
-constexpr int kWarps = 2 + 4 * kStreams;
+constexpr int kKeys = 128;           // keys per block: S width, P.V depth
+static_assert(kKeys == kBlockKeys, "split chunks are whole blocks");
+constexpr int kStages = 3;
+constexpr int kWarps = 6;
 constexpr int kThreads = kWarps * 32;
-constexpr uint32_t kColO = kStreams * kKeys;   // O accumulators after the S tiles
+constexpr int kSoftmax = 4 * 32;     // softmax threads (warps 2-5)
 constexpr int kBoxBytes = kPage * 128;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kHeadroom = 8.f;     // log2 units a row max may grow before O is rescaled
-
-constexpr int kPBufs = 2;            // P tiles per stream (double buffered)
+constexpr uint32_t kColS = 0;        // two score / probability tiles: columns 0 and kKeys
+constexpr uint32_t kColO = 2 * kKeys;
 
 enum { kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarSFull = kBarKvEmpty + kStages,
-       kBarSEmpty = kBarSFull + kStreams, kBarPFull = kBarSEmpty + kStreams,
-       kBarPvDone = kBarPFull + kStreams * kPBufs, kBarQReady = kBarPvDone + kStreams * kPBufs,
-       kNumBars = kBarQReady + 1 };
+       kBarPFull = kBarSFull + 2, kBarPvDone = kBarPFull + 2, kBarMx = kBarPvDone + 2,
+       kBarQReady = kBarMx + 2, kNumBars = kBarQReady + 1 };
 
 template <int HD>
 struct TcSmem {
   static constexpr int kHalves = HD / 64;
-  static constexpr int kHalfRows = kRows * 128;        // one 64-column half of a 128-row tile
-  static constexpr int kP = kHalfRows;                  // 64 keys: one half
-  static constexpr int kKvHalf = kKeys * 128;           // 64 keys x 64 columns
+  static constexpr int kKvHalf = kKeys * 128;           // 128 keys x 64 columns
   static constexpr int kKv = kHalves * kKvHalf;         // K or V tile of a block
   static constexpr int kStage = 2 * kKv;
-  static constexpr int kOffP = 0;                       // kStreams x kPBufs tiles
-  static constexpr int kOffKv = kOffP + kStreams * kPBufs * kP;
+  static constexpr int kOffKv = 0;
   static constexpr int kOffBar = kOffKv + kStages * kStage;
   static constexpr int kOffTau = kOffBar + kNumBars * 8;
-  static constexpr int kOffMl = kOffTau + 2 * kMaxB * 4;    // stream 1's (m, l) per row
-  static constexpr int kOffMisc = kOffMl + kRows * 8;       // tmem address, error flag
+  static constexpr int kOffMx = kOffTau + 2 * kMaxB * 4;     // [2][4][32] block maxima
+  static constexpr int kOffCs = kOffMx + 2 * 4 * 32 * 4;    // [kMaxB][HD/2] (cos, sin)
+  static constexpr int kOffMisc = kOffCs + kMaxB * (HD / 2) * 8;  // tmem address, error flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;              // 1024-byte alignment slack
-  static constexpr uint32_t kColQ = kColO + kStreams * HD;  // Q: hd bf16 = hd/2 columns
-  static constexpr uint32_t kTmemCols = (kColQ + HD / 2) <= 256 ? 256 : 512;
+  static constexpr uint32_t kColQ = kColO + HD;             // Q: hd bf16 = hd/2 columns
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kColQ + HD / 2 <= kTmemCols, "TMEM budget");
+  static_assert(4 * 32 * (HD + 4) * 4 <= kStages * kStage, "epilogue exchange fits the ring");
 };
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -94,16 +94,21 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+template <int V> struct IntC { static constexpr int value = V; };
+
+// Word i (a compile-time constant after unrolling) of a 16-byte vector.
+__device__ __forceinline__ uint32_t word4(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// Visibility of key `key` (0..Lk-1) for a new row (token index tok of the
-// 2B, slot row or data row, step label ti); tau of the new tokens in tau_s.
-__device__ __forceinline__ bool visible(int key, int P, int B, const int *tau_s, bool row_slot,
-                                        int ti) {
-  if (key < P) return true;
-  const int jj = key - P;
+// Visibility of new key jj (0..2B-1 past the prompt) for a new row (slot row
+// or data row, step label ti); tau of the new tokens in tau_s.
+__device__ __forceinline__ bool visible_new(int jj, int B, const int *tau_s, bool row_slot,
+                                            int ti) {
   const int tj = tau_s[jj];
   const bool key_slot = jj >= B;
   return row_slot ? (key_slot ? tj >= ti : tj < ti) : (!key_slot && tj <= ti);
@@ -118,10 +123,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t *sb = smem_raw + (base - raw);
-  const uint32_t sP = base + L::kOffP, sKv = base + L::kOffKv;
+  const uint32_t sKv = base + L::kOffKv;
   auto bar = [&](int i) { return base + L::kOffBar + 8u * i; };
   int *tau_s = reinterpret_cast<int *>(sb + L::kOffTau);
-  float2 *ml_s = reinterpret_cast<float2 *>(sb + L::kOffMl);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + L::kOffMisc);
   int *flag_s = reinterpret_cast<int *>(sb + L::kOffMisc + 4);
 
@@ -145,22 +149,41 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int n_blocks = (k_end - k_begin + kKeys - 1) / kKeys;
   const int n_splits_b = (Lk + a.chunk - 1) / a.chunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // copies of the tile's rows across the four TMEM lane quadrants (4 when
+  // one 32-row group holds every real row, 2 for two groups, else 1), and
+  // the softmax warps that own real rows (the others hold padding only)
+  const int n_groups = min(4, (M - row0 + 31) / 32);
+  const int R = n_groups == 1 ? 4 : n_groups == 2 ? 2 : 1;
+  const int n_valid = R > 1 ? 4 : n_groups;
   grid_dep_launch();                         // the split merge may be scheduled
+  // softmax threads request their raw query row first, ahead of the K/V
+  // stream the producer starts below (each thread one row of the tile)
+  uint4 qv[HD / 8];
+  if (warp >= 2) {
+    const int qg = (warp & 3) % (4 / R), qrow_i = row0 + 32 * qg + lane;
+    if (qrow_i < M) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          (const __nv_bfloat16 *)a.q + ((2L * c0 + qrow_i / a.G) * a.Hq + kvh * a.G + qrow_i % a.G) * HD);
+#pragma unroll
+      for (int e = 0; e < HD / 8; ++e) qv[e] = __ldg(src + e);
+    } else {
+#pragma unroll
+      for (int e = 0; e < HD / 8; ++e) qv[e] = make_uint4(0, 0, 0, 0);
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bar(kBarKvFull + i), 1);
       mbar_init(bar(kBarKvEmpty + i), 1);
     }
-    for (int i = 0; i < kStreams; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
-      mbar_init(bar(kBarSEmpty + i), 4);
-    }
-    for (int i = 0; i < kStreams * kPBufs; ++i) {
-      mbar_init(bar(kBarPFull + i), 4);
+      mbar_init(bar(kBarPFull + i), n_valid);
       mbar_init(bar(kBarPvDone + i), 1);
+      mbar_init(bar(kBarMx + i), 4);
     }
-    mbar_init(bar(kBarQReady), 4 * kStreams + 1);
+    mbar_init(bar(kBarQReady), 4);
     *flag_s = 0;
     fence_barrier_init();
   }
@@ -172,43 +195,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  if (warp != 0) {
-    // tau, the P tiles zeroed once (padding rows are never written again),
-    // and Q into TMEM -- one row per thread of the stream-0 softmax warps,
-    // two bf16 per column -- while the producer already streams K and V;
-    // then arrive on the Q barrier
-    const int t = threadIdx.x - 32, nt = kThreads - 32;
-    for (int j = t; j < 2 * B; j += nt) tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
-    for (int e = t; e < kStreams * kPBufs * L::kP / 16; e += nt)
-      reinterpret_cast<uint4 *>(sb + L::kOffP)[e] = make_uint4(0, 0, 0, 0);
-    fence_proxy_async_smem();
-    if (warp >= 2 && warp < 6) {
-      grid_dep_wait();                       // rotated q comes from the rotation kernel
-      const int q4 = warp & 3, r = 32 * q4 + lane, grow = row0 + r;
-      const uint4 *qrow = nullptr;
-      if (grow < M)
-        qrow = reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q_rot +
-                                               ((2L * c0 + grow / a.G) * a.Hq + kvh * a.G + grow % a.G) * HD);
-#pragma unroll
-      for (int c = 0; c < HD / 64; ++c) {     // 64 bf16 = 32 columns per store
-        uint32_t w[32];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint4 v = qrow ? __ldg(qrow + 8 * c + e) : make_uint4(0, 0, 0, 0);
-          w[4 * e] = v.x; w[4 * e + 1] = v.y; w[4 * e + 2] = v.z; w[4 * e + 3] = v.w;
-        }
-        tc::st32(tmem + ((uint32_t)(32 * q4) << 16) + L::kColQ + 32 * c, w);
-      }
-      tc::wait_st();
-      tc::fence_before_sync();
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(kBarQReady));
-    // every consumer needs the whole Q tile, tau and zeroed P tiles
-    if (!mbar_wait_warp(bar(kBarQReady), 0)) {
-      if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
-    }
-  }
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -249,61 +235,47 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    // One thread schedules both MMA kinds as their inputs become ready, so
-    // a P.V never waits behind a later block's K load: S of block ns needs
-    // its K/V stage and its stream's score tile free; P.V of block np needs
-    // its P tile.  P.V goes in block order.
+    // One thread issues both MMA kinds as their inputs become ready: S of
+    // block ns needs its K/V stage and its score tile free (the P.V that
+    // read the tile two blocks ago done); P.V of block np needs its P.
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0);
       constexpr uint32_t idO = tc::idesc_bf16(kRows, HD, 1);
+      bool ok = mbar_wait(bar(kBarQReady), 0);
       int ns = 0, np = 0;
       uint32_t idle = 0;
-      while (np < n_blocks) {
+      while (ok && np < n_blocks) {
         bool progressed = false;
         if (ns < n_blocks) {
-          const int s = ns % kStages, st = ns & 1;
+          const int s = ns % kStages, tb = ns & 1;
           if (mbar_test(bar(kBarKvFull + s), (ns / kStages) & 1) &&
-              (ns < kStreams || mbar_test(bar(kBarSEmpty + st), ((ns >> 1) - 1) & 1))) {
+              (ns < 2 || mbar_test(bar(kBarPvDone + tb), ((ns >> 1) - 1) & 1))) {
             tc::fence_after_sync();
             const uint32_t kt = sKv + s * L::kStage;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
               const uint32_t ka = kt + (kk >> 2) * L::kKvHalf + (kk & 3) * 32;
-              tc::mma_bf16_ts(tmem + st * kKeys, tmem + L::kColQ + kk * 8,
+              tc::mma_bf16_ts(tmem + kColS + tb * kKeys, tmem + L::kColQ + kk * 8,
                               tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
             }
-            tc::commit(bar(kBarSFull + st));
+            tc::commit(bar(kBarSFull + tb));
             ++ns;
             progressed = true;
           }
         }
         if (np < ns) {
-          const int st = np & 1, s = np % kStages;
-          const int ib = np >> 1;                 // block index within the stream
-          const int pb = st * kPBufs + (ib & 1);  // its P tile
-          if (mbar_test(bar(kBarPFull + pb), (ib >> 1) & 1)) {
+          const int tb = np & 1, s = np % kStages;
+          if (mbar_test(bar(kBarPFull + tb), (np >> 1) & 1)) {
             tc::fence_after_sync();
             const int kb = k_begin + np * kKeys;
             const int valid = min(kKeys, k_end - kb);
             const int loaded = (valid + kPage - 1) & ~(kPage - 1);
             const uint32_t vt = sKv + s * L::kStage + L::kKv;
-            if (kb + valid == Lk && loaded > valid) {
-              // slots past the sequence end in its last page hold arbitrary
-              // data; P is 0 there, but 0 * NaN would poison O: zero V rows
-              constexpr int CH = HD / 8;
-              for (int e = 0; e < (loaded - valid) * CH; ++e) {
-                const int r = valid + e / CH, c = e % CH;
-                *reinterpret_cast<uint4 *>(sb + (vt - base) + (c >> 3) * L::kKvHalf + swz(r, c & 7)) =
-                    make_uint4(0, 0, 0, 0);
-              }
-              fence_proxy_async_smem();
-            }
-            const uint32_t pt = sP + pb * L::kP;
             for (int kk = 0; kk < loaded / 16; ++kk)
-              tc::mma_bf16(tmem + kColO + st * HD, tc::smem_desc_sw128(pt + kk * 32, 16, 1024),
-                           tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
-                           (np >= kStreams || kk > 0));
-            tc::commit(bar(kBarPvDone + pb));
+              tc::mma_bf16_ts(tmem + kColO, tmem + kColS + tb * kKeys + kk * 8,
+                              tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
+                              (np > 0 || kk > 0));
+            tc::commit(bar(kBarPvDone + tb));
             tc::commit(bar(kBarKvEmpty + s));
             ++np;
             progressed = true;
@@ -312,76 +284,141 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         if (progressed) {
           idle = 0;
         } else if (++idle > (kWaitPolls << 4)) {  // bounded: give up, flag, drain
-          raise_status(a.status, kStatusTimeout);
-          atomicOr(flag_s, 1);
-          break;
+          ok = false;
         }
+      }
+      if (!ok) {
+        raise_status(a.status, kStatusTimeout);
+        atomicOr(flag_s, 1);
       }
     }
   } else {
     // ---------------------------------------------------------- softmax
-    const int st = (warp - 2) >> 2;          // stream of this warpgroup
+    // With at most 64 real rows the tile's rows are replicated across the
+    // four TMEM lane quadrants (R = 4 or 2 copies) and the copies split each
+    // block's keys: every quadrant's warp handles 128/R keys of the same
+    // rows, the warps agree on the block maximum through shared memory, and
+    // each writes P for its keys (zeros elsewhere), so the P.V MMA leaves R
+    // partial outputs per row that the epilogue adds up.
     const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
-    const int r = 32 * q4 + lane;            // query row within the tile
+    const int groups = 4 / R;                // 32-row groups held per copy
+    const int g = q4 % groups, kp = q4 / groups;
+    const int r = 32 * g + lane;             // query row within the tile
     const int grow = row0 + r;
     const bool row_valid = grow < M;
-    const bool warp_valid = row0 + 32 * q4 < M;
+    const bool warp_valid = row0 + 32 * g < M;
     const int tok = row_valid ? grow / a.G : 0;
     const bool row_slot = tok >= B;
-    const int row_tau = tau_s[tok];
     const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
-    const uint32_t tS = trow + st * kKeys, tO = trow + kColO + st * HD;
+    // tau of the section and the (cos, sin) table of its B positions, then
+    // Q rotated into TMEM (one row per thread, two bf16 per column, zeros
+    // for padding rows); then the issuer may start
+    const int t = threadIdx.x - 64;
+    float2 *cs_s = reinterpret_cast<float2 *>(sb + L::kOffCs);
+    for (int j = t; j < 2 * B; j += kSoftmax) tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
+    for (int e = t; e < B * (HD / 2); e += kSoftmax)
+      cs_s[e] = rope_cs(a.tab, e % (HD / 2), P + e / (HD / 2));   // D~_k copies D_k's position
+    named_sync(1, kSoftmax);
+    {
+      const int kq = row_valid ? (tok < B ? tok : tok - B) : 0;   // response index
+      const float2 *cs = cs_s + kq * (HD / 2);
+#pragma unroll
+      for (int d0 = 0; d0 < HD / 2; d0 += 32) {
+        // elements d0.. and d0 + hd/2.. of the row: y1 = x1 c - x2 s,
+        // y2 = x2 c + x1 s, rounded to bf16 (rotate-half pairing); padding
+        // rows are zero and stay zero
+        uint32_t w1[16], w2[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const uint32_t a1 = word4(qv[(d0 >> 3) + (e >> 2)], e & 3);
+          const uint32_t a2 = word4(qv[((HD / 2 + d0) >> 3) + (e >> 2)], e & 3);
+          const float x1l = __uint_as_float(a1 << 16), x1h = __uint_as_float(a1 & 0xffff0000u);
+          const float x2l = __uint_as_float(a2 << 16), x2h = __uint_as_float(a2 & 0xffff0000u);
+          const float2 cl = cs[d0 + 2 * e], ch = cs[d0 + 2 * e + 1];
+          w1[e] = pack_bf16x2(x1l * cl.x - x2l * cl.y, x1h * ch.x - x2h * ch.y);
+          w2[e] = pack_bf16x2(x2l * cl.x + x1l * cl.y, x2h * ch.x + x1h * ch.y);
+        }
+        tc::st16(trow + L::kColQ + d0 / 2, w1);
+        tc::st16(trow + L::kColQ + (HD / 2 + d0) / 2, w2);
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kBarQReady));
+    const int row_tau = tau_s[tok];
+    const uint32_t tO = trow + kColO;
     const float scale = a.sm_scale * kLog2e;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    int i = 0;                               // blocks of this stream so far
-    for (int j = st; j < n_blocks; j += kStreams, ++i) {
-      if (!mbar_wait_warp(bar(kBarSFull + st), i & 1)) { ok = false; break; }
-      tc::fence_after_sync();
-      uint32_t sr[kKeys];
-      if (warp_valid) {
-        tc::ld32(tS, sr);
-        tc::ld32(tS + 32, sr + 32);
-        tc::wait_ld();
-      }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarSEmpty + st));
-      const int kb = k_begin + j * kKeys;
-      float mx = -INFINITY;                  // block max of the raw scores
-      if (warp_valid) {
-        if (kb + kKeys > min(P, k_end)) {
-          // the block reaches past the prompt or the split's end: mask it
-          uint64_t vis = 0;
-          for (int c = 0; c < kKeys; ++c) {
-            const int key = kb + c;
-            if (key < k_end && visible(key, P, B, tau_s, row_slot, row_tau)) vis |= 1ull << c;
+    int j = 0;
+    // the key loop, compiled once per copy count (chunk loops unrolled)
+    auto key_loop = [&](auto rc) {
+      constexpr int RC = decltype(rc)::value;
+      constexpr int KW = kKeys / RC;         // this warp's keys per block
+      const int k_lo = kp * KW;
+      for (; warp_valid && j < n_blocks; ++j) {
+        const int tb = j & 1;
+        const uint32_t tS = trow + kColS + tb * kKeys;
+        if (!mbar_wait_warp(bar(kBarSFull + tb), (j >> 1) & 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        const int kb = k_begin + j * kKeys;
+        // visibility of this warp's keys: prompt keys below the split's end
+        // are visible; only blocks that reach the new keys or the end need
+        // the bitmask (bit c: key kb + k_lo + c)
+        uint64_t vis[(KW + 63) / 64];
+#pragma unroll
+        for (int h = 0; h < (KW + 63) / 64; ++h) vis[h] = ~0ull;
+        if (kb + k_lo + KW > min(P, k_end)) {
+          for (int c = max(0, min(P, k_end) - kb - k_lo); c < KW; ++c) {
+            const int key = kb + k_lo + c;
+            const bool v = key < k_end && (key < P || visible_new(key - P, B, tau_s, row_slot, row_tau));
+            if (!v) {
+#pragma unroll
+              for (int h = 0; h < (KW + 63) / 64; ++h)
+                if ((c >> 6) == h) vis[h] &= ~(1ull << (c & 63));
+            }
           }
-#pragma unroll
-          for (int c = 0; c < kKeys; ++c)
-            if (!((vis >> c) & 1ull)) sr[c] = __float_as_uint(-INFINITY);
         }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // pass 1: the maximum of the raw scores over this warp's keys, 64
+        // columns per TMEM round trip (the loop stays rolled: an unrolled
+        // 128-key body overflows the instruction cache)
+        constexpr int CB = KW < 64 ? KW : 64;
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int ck = 0; ck < KW; ck += CB) {
+          uint32_t sr[CB];
+          const uint64_t vh = KW > 64 && ck >= 64 ? vis[KW > 64 ? 1 : 0] : vis[0];
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(sr[c]));
-        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;   // scale > 0
-      }
-      // reference maximum: moves only when this block's max outgrows it
-      const bool move = row_valid && mx > m_ref + kHeadroom;
-      const float m_new = move ? mx : m_ref;
-      const float alpha = move ? ex2(m_ref - m_new) : 1.f;     // m_ref = -inf -> 0
-      const int pb = st * kPBufs + (i & 1);
-      if (i >= kPBufs) {
-        // the P.V that read this P tile two blocks ago must be done
-        if (!mbar_wait_warp(bar(kBarPvDone + pb), ((i >> 1) - 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-      }
-      if (i > 0 && __any_sync(0xffffffffu, move)) {
-        // rescaling O needs the stream's previous P.V (the latest) done
-        const int pp = st * kPBufs + ((i - 1) & 1);
-        if (!mbar_wait_warp(bar(kBarPvDone + pp), ((i - 1) >> 1) & 1)) { ok = false; break; }
-        tc::fence_after_sync();
-        {
+          for (int q = 0; q < CB; q += 32) tc::ld32(tS + k_lo + ck + q, sr + q);
+          tc::wait_ld();
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < CB; ++c) {
+            const float v = ((vh >> ((ck & 63) + c)) & 1ull) ? __uint_as_float(sr[c]) : -INFINITY;
+            m4[c & 3] = fmaxf(m4[c & 3], v);
+          }
+          mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+        }
+        if (RC > 1) {
+          // the block maximum over the copies of this row (bounded exchange)
+          float *mx_s = reinterpret_cast<float *>(sb + L::kOffMx) + (tb * 4) * 32;
+          mx_s[q4 * 32 + lane] = mx;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarMx + tb));
+          if (!mbar_wait_warp(bar(kBarMx + tb), (j >> 1) & 1)) { ok = false; break; }
+#pragma unroll
+          for (int c = 0; c < RC; ++c) mx = fmaxf(mx, mx_s[(c * (4 / RC) + g) * 32 + lane]);
+        }
+        mx *= scale;                         // scale > 0
+        // reference maximum: moves only when this block's max outgrows it
+        const bool move = row_valid && mx > m_ref + kHeadroom;
+        const float m_new = move ? mx : m_ref;
+        const float alpha = move ? ex2(m_ref - m_new) : 1.f;     // m_ref = -inf -> 0
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          // rescaling O needs the previous block's P.V done
+          if (!mbar_wait_warp(bar(kBarPvDone + (tb ^ 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
+          tc::fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {
             uint32_t o[32];
@@ -393,81 +430,142 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           }
           tc::wait_st();
         }
-      }
-      l *= alpha;
-      m_ref = m_new;
-      if (row_valid) {
-        // P row (bf16) into the swizzled tile: keys are the K dimension
-        // p = 2^(s * scale - m_ref): one fma and the MUFU per score
+        l *= alpha;
+        m_ref = m_new;
+        // pass 2: p = 2^(s * scale - m_ref) as bf16 pairs into P columns
+        // k_lo/2 .. (k_lo + KW)/2 of the score tile (the scores there are
+        // read already or belong to other copies' keys), zeros in the rest
         const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-        uint8_t *prow = sb + L::kOffP + pb * L::kP;
         float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int ck = 0; ck < KW; ck += CB) {
+          uint32_t sr[CB], pw[CB / 2];
+          const uint64_t vh = KW > 64 && ck >= 64 ? vis[KW > 64 ? 1 : 0] : vis[0];
 #pragma unroll
-        for (int c = 0; c < kKeys / 8; ++c) {
-          uint32_t w[4];
+          for (int q = 0; q < CB; q += 32) tc::ld32(tS + k_lo + ck + q, sr + q);
+          tc::wait_ld();
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[8 * c + 2 * e]), scale, -mu));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[8 * c + 2 * e + 1]), scale, -mu));
-            rs4[e] += p0 + p1;
-            w[e] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < CB / 2; ++e) {
+            const int c = (ck & 63) + 2 * e;
+            const float s0 = ((vh >> c) & 1ull) ? __uint_as_float(sr[2 * e]) : -INFINITY;
+            const float s1 = ((vh >> (c + 1)) & 1ull) ? __uint_as_float(sr[2 * e + 1]) : -INFINITY;
+            const float p0 = ex2(fmaf(s0, scale, -mu));
+            const float p1 = ex2(fmaf(s1, scale, -mu));
+            rs4[e & 3] += p0 + p1;
+            pw[e] = pack_bf16x2(p0, p1);
           }
-          *reinterpret_cast<uint4 *>(prow + swz(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int q = 0; q < CB / 2; q += 16) tc::st16(tS + (k_lo + ck) / 2 + q, pw + q);
         }
+        if (RC > 1) {
+          uint32_t z[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) z[e] = 0u;
+#pragma unroll
+          for (int c = 0; c < kKeys / 2; c += 16)
+            if (c < k_lo / 2 || c >= (k_lo + KW) / 2) tc::st16(tS + c, z);
+        }
+        tc::wait_st();
         l += (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+        {
+          // slots past the sequence end in its last page hold arbitrary
+          // data; P is 0 there, but 0 * NaN would poison O: zero those V
+          // rows (the stage landed before S was computed) before P.V reads
+          const int valid = min(kKeys, k_end - kb);
+          const int loaded = (valid + kPage - 1) & ~(kPage - 1);
+          if (q4 == 0 && kb + valid == Lk && loaded > valid) {
+            constexpr int CH = HD / 8;
+            uint8_t *vt = sb + L::kOffKv + (j % kStages) * L::kStage + L::kKv;
+            for (int e = lane; e < (loaded - valid) * CH; e += 32) {
+              const int rr = valid + e / CH, c = e % CH;
+              *reinterpret_cast<uint4 *>(vt + (c >> 3) * L::kKvHalf + swz(rr, c & 7)) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarPFull + tb));
       }
-      fence_proxy_async_smem();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarPFull + pb));
-    }
-    if (ok && i > 0 &&
-        !mbar_wait_warp(bar(kBarPvDone + st * kPBufs + ((i - 1) & 1)), ((i - 1) >> 1) & 1))
+    };
+    if (R == 4) key_loop(IntC<4>{});
+    else if (R == 2) key_loop(IntC<2>{});
+    else key_loop(IntC<1>{});
+    if (ok && j > 0 &&
+        !mbar_wait_warp(bar(kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1))
       ok = false;
     if (!ok && lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
     tc::fence_after_sync();
     // -------------------------------------------------------- epilogue
-    // stream 1 hands its (m, l) to stream 0, which merges the two O tiles
-    if (st == 1) ml_s[r] = make_float2(m_ref, l);
-    tc::fence_before_sync();                 // stream 1's O reads/waits before the sync
-    named_sync(1, 4 * kStreams * 32);
-    tc::fence_after_sync();
     const bool failed = *(volatile int *)flag_s != 0;
-    if (st == 0 && warp_valid) {
-      const bool has1 = n_blocks > 1;        // stream 1 saw at least one block
-      const float2 ml1 = has1 ? ml_s[r] : make_float2(-INFINITY, 0.f);
-      const float mm = fmaxf(m_ref, ml1.x);
-      const float mu = mm == -INFINITY ? 0.f : mm;
-      const float f0 = exp2f(m_ref - mu), f1 = has1 ? exp2f(ml1.x - mu) : 0.f;
-      const float lt = l * f0 + ml1.y * f1;
+    const long orow = (2L * c0 + tok) * a.Hq + kvh * a.G + (row_valid ? grow % a.G : 0);
+    // writes columns [c0c, c0c + n) of this thread's row from v (O sums,
+    // unnormalised) with sum lt
+    auto write_cols = [&](const float *v, int c0c, int n, float lt) {
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const long orow = (2L * c0 + tok) * a.Hq + kvh * a.G + (row_valid ? grow % a.G : 0);
+      if (n_splits_b == 1) {
+        uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)a.out + orow * HD + c0c);
+        for (int e = 0; e < n / 8; ++e)
+          dst[e] = make_uint4(pack_bf16x2(v[8 * e] * inv, v[8 * e + 1] * inv),
+                              pack_bf16x2(v[8 * e + 2] * inv, v[8 * e + 3] * inv),
+                              pack_bf16x2(v[8 * e + 4] * inv, v[8 * e + 5] * inv),
+                              pack_bf16x2(v[8 * e + 6] * inv, v[8 * e + 7] * inv));
+      } else {
+        const long prow = (long)split * a.T * a.Hq + orow;
+        float4 *dst = reinterpret_cast<float4 *>(a.o_part + prow * HD + c0c);
+        for (int e = 0; e < n / 4; ++e)
+          dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        if (c0c == 0) a.ml_part[prow] = make_float2(m_ref, lt);   // O, l relative to m_ref
+      }
+    };
+    if (R == 1) {
+      if (warp_valid) {
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t o[32];
+          tc::ld32(tO + 32 * c, o);
+          tc::wait_ld();
+          if (!row_valid || failed) continue;
+          write_cols(reinterpret_cast<const float *>(o), 32 * c, 32, l);
+        }
+      }
+    } else {
+      // every copy puts its partial output and sum in the (now idle) K/V
+      // ring; then copy kp adds the R partials of columns [kp * HD/R, ..)
+      float *part = reinterpret_cast<float *>(sb + L::kOffKv);   // [R][groups][32][HD + 4]
+      float *mine = part + ((kp * groups + g) * 32 + lane) * (HD + 4);
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
-        uint32_t o0[32], o1[32];
-        tc::ld32(trow + kColO + 32 * c, o0);
-        if (has1) tc::ld32(trow + kColO + HD + 32 * c, o1);
+        uint32_t o[32];
+        tc::ld32(tO + 32 * c, o);
         tc::wait_ld();
-        if (!row_valid || failed) continue;
-        float v[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          v[e] = __uint_as_float(o0[e]) * f0 + (has1 ? __uint_as_float(o1[e]) * f1 : 0.f);
-        if (n_splits_b == 1) {
-          uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)a.out + orow * HD + 32 * c);
+        for (int e = 0; e < 8; ++e)
+          *reinterpret_cast<float4 *>(mine + 32 * c + 4 * e) =
+              make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                          __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+      }
+      mine[HD] = l;
+      named_sync(1, kSoftmax);
+      if (row_valid && !failed) {
+        const int cw = HD / R, cb = kp * cw;    // 16, 32 or 64 columns
+        float lt = 0.f;
+        for (int c = 0; c < R; ++c) lt += part[((c * groups + g) * 32 + lane) * (HD + 4) + HD];
+        for (int q = 0; q < cw; q += 32) {
+          const int n = min(32, cw - q);        // a multiple of 16
+          float v[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pack_bf16x2(v[8 * e] * inv, v[8 * e + 1] * inv),
-                                pack_bf16x2(v[8 * e + 2] * inv, v[8 * e + 3] * inv),
-                                pack_bf16x2(v[8 * e + 4] * inv, v[8 * e + 5] * inv),
-                                pack_bf16x2(v[8 * e + 6] * inv, v[8 * e + 7] * inv));
-        } else {
-          const long prow = (long)split * a.T * a.Hq + orow;
-          float4 *dst = reinterpret_cast<float4 *>(a.o_part + prow * HD + 32 * c);
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          for (int c = 0; c < R; ++c) {
+            const float *src = part + ((c * groups + g) * 32 + lane) * (HD + 4) + cb + q;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-          if (c == 0) a.ml_part[prow] = make_float2(mm, lt);
+            for (int e = 0; e < 8; ++e) {
+              if (4 * e >= n) break;
+              const float4 p4 = *reinterpret_cast<const float4 *>(src + 4 * e);
+              v[4 * e] += p4.x; v[4 * e + 1] += p4.y; v[4 * e + 2] += p4.z; v[4 * e + 3] += p4.w;
+            }
+          }
+          write_cols(v, cb + q, n, lt);
         }
       }
     }

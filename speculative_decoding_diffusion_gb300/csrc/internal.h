@@ -40,9 +40,18 @@ struct VerifyPlan {
 // Fills *plan; returns SIMSD_OK or the first argument error.
 simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *plan);
 
+// RoPE inverse frequencies base^(-2d/hd), d < hd/2, computed in double on
+// the host and passed both as double and as a pair of floats hi + lo.
+struct RopeTable {
+  double inv_freq[64];
+  float hi[64], lo[64];
+};
+void make_rope_table(float base, int hd, RopeTable *t);   // cached per (base, hd)
+
 // Parameters every attention kernel reads.
 struct AttnParams {
-  const void *q_rot;          // [T][Hq][hd], rotated
+  const void *q;              // [T][Hq][hd], raw (the bf16 kernel rotates it)
+  const void *q_rot;          // [T][Hq][hd], rotated by K1 (fp32 path)
   void *out;                  // [T][Hq][hd]
   float *o_part;              // [n_splits][T][Hq][hd]
   float2 *ml_part;            // [n_splits][T][Hq]  (running max, sum)
@@ -58,6 +67,7 @@ struct AttnParams {
   int Hq, Hkv, G, T;
   int chunk, rows_per_tile;
   float sm_scale;
+  RopeTable tab;              // angles of the query rotation (bf16 kernel)
 };
 
 // K1: rotate q and k_new at the layout positions, append k/v to the cache.
@@ -114,12 +124,5 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// RoPE inverse frequencies base^(-2d/hd), d < hd/2, computed in double on
-// the host and passed both as double and as a pair of floats hi + lo.
-struct RopeTable {
-  double inv_freq[64];
-  float hi[64], lo[64];
-};
-void make_rope_table(float base, int hd, RopeTable *t);   // cached per (base, hd)
 
 }  // namespace simsd

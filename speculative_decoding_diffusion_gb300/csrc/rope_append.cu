@@ -6,46 +6,25 @@
 // Section 1 "Input Layout": the 2B new tokens occupy layout indices
 // P .. P+2B-1 (D_1..D_B then D~_1..D~_B); those are the cache slots written.
 //
-// One CTA per new token.  Positions reach ~3.3e4, where a plain fp32
-// product pos * base^(-2d/hd) is off by ~2e-3 rad, so the angle is formed
-// as an unevaluated sum: the frequency as two floats hi + lo (from fp64 on
-// the host), pos * hi with its exact rounding error recovered by an fma,
-// then reduced modulo 2*pi with Cody and Waite's split constant (2*pi =
-// C1 + C2, each product folded in by one fma) -- ~3e-7 rad, fp32 only (the
-// GB300's fp64 rate is a small fraction of fp32's).  Positions >= 2^24 use
-// fp64.  Sine and cosine of the reduced angle and the rotation are fp32.
+// One CTA per new token; angles from rope.cuh (float-pair product and
+// Cody-Waite reduction), the rotation in fp32.  The bf16 attention kernel
+// rotates its own query tile, so the queries are rotated here only for the
+// fp32 path.
 // Rotate-half pairing: element d pairs with d + hd/2.  16-byte vector I/O.
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
+#include "rope.cuh"
 
 namespace simsd {
 namespace {
 
 constexpr int kThreads = 128;
 
-// Angles for one position into smem: cs[2d] = cos, cs[2d+1] = sin.
-__device__ __forceinline__ void angles(const RopeTable &tab, int hd, int pos,
-                                       float2 *cs) {
-  // 2*pi = C1 + C2 (C1 the float nearest 2*pi, C2 the float nearest the rest)
-  const float C1 = 6.28318548202514648f, C2 = -1.7484555314695172e-07f;
-  const float inv_two_pi = 0.159154943091895336f;
-  for (int d = threadIdx.x; d < hd / 2; d += blockDim.x) {
-    float r;
-    if (pos < (1 << 24)) {
-      const float p = (float)pos;                       // exact
-      const float t = p * tab.hi[d];
-      const float t_lo = fmaf(p, tab.lo[d], fmaf(p, tab.hi[d], -t));  // rest of p*(hi+lo)
-      const float n = rintf(t * inv_two_pi);
-      r = fmaf(-n, C2, fmaf(-n, C1, t)) + t_lo;         // t + t_lo - 2*pi*n
-    } else {
-      const double two_pi = 6.283185307179586476925286766559;
-      const double th = (double)pos * tab.inv_freq[d];
-      r = (float)fma(-rint(th * (1.0 / two_pi)), two_pi, th);
-    }
-    float s, c;
-    sincosf(r, &s, &c);
-    cs[d] = make_float2(c, s);
-  }
+// Angles for one position into smem: cs[d] = (cos, sin) of frequency d.
+__device__ __forceinline__ void angles(const RopeTable &tab, int hd, int pos, float2 *cs) {
+  for (int d = threadIdx.x; d < hd / 2; d += blockDim.x) cs[d] = rope_cs(tab, d, pos);
 }
 
 template <typename T> struct Vec;
@@ -161,9 +140,13 @@ struct RopeVerifyArgs {
   int32_t *tok_seq;
   uint32_t *status;
   int batch, Hq, Hkv, hd, max_pages, num_pages;
+  int rotate_q;         // write rotated queries to q_rot (fp32 path)
 };
 
-constexpr int kStageSeqs = 2048;   // sequences whose cu_B / lens fit the smem stage
+// sequences whose cu_B / lens are staged in shared memory; kept small so
+// the attention kernel's CTAs (launched early, programmatic dependent
+// launch) fit on the same SMs as this kernel's
+constexpr int kStageSeqs = 512;
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
@@ -174,7 +157,7 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
   __shared__ __align__(8) uint64_t bar_s;
   grid_dep_launch();                         // the attention kernel may start its prologue
   const int r = blockIdx.x;                  // new-token row
-  const uint32_t qbytes = (uint32_t)(a.Hq * a.hd * sizeof(T));
+  const uint32_t qbytes = a.rotate_q ? (uint32_t)(a.Hq * a.hd * sizeof(T)) : 0u;
   const uint32_t kvbytes = (uint32_t)(a.Hkv * a.hd * sizeof(T));
   const uint32_t bar = smem_u32(&bar_s), rows = smem_u32(rows_s);
   // the token's raw rows are needed whatever its sequence: one thread starts
@@ -184,7 +167,7 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
     fence_barrier_init();
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(bar, qbytes + 2 * kvbytes);
-    bulk_load(rows, (const char *)a.q + (long)r * qbytes, qbytes, bar);
+    if (qbytes) bulk_load(rows, (const char *)a.q + (long)r * qbytes, qbytes, bar);
     bulk_load(rows + qbytes, (const char *)a.k_new + (long)r * kvbytes, kvbytes, bar);
     bulk_load(rows + qbytes + kvbytes, (const char *)a.v_new + (long)r * kvbytes, kvbytes, bar);
   }
@@ -225,7 +208,7 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
   const T *qs = reinterpret_cast<const T *>(rows_s);
   const T *ks = reinterpret_cast<const T *>(rows_s + qbytes);
   const T *vs = reinterpret_cast<const T *>(rows_s + qbytes + kvbytes);
-  rotate_rows<T>(qs, (T *)a.q_rot + (long)r * a.Hq * a.hd, a.Hq, a.hd, a.hd, cs);
+  if (a.rotate_q) rotate_rows<T>(qs, (T *)a.q_rot + (long)r * a.Hq * a.hd, a.Hq, a.hd, a.hd, cs);
   const long base = ((long)page * a.Hkv * kPage + slot % kPage) * a.hd;
   const long stride = (long)kPage * a.hd;    // next KV head, same slot
   rotate_rows<T>(ks, (T *)a.k_cache + base, a.Hkv, a.hd, stride, cs);
@@ -288,12 +271,29 @@ cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
   a.Hkv = d->num_kv_heads;
   a.hd = d->head_dim;
   a.max_pages = d->max_pages_per_seq;
-  const size_t smem = (size_t)(a.Hq + 2 * a.Hkv) * a.hd * p.esize;   // <= kMaxRowBytes
+  a.rotate_q = d->dtype == SIMSD_F32;
+  const size_t smem = (size_t)((a.rotate_q ? a.Hq : 0) + 2 * a.Hkv) * a.hd * p.esize;   // <= kMaxRowBytes
   const void *kern = d->dtype == SIMSD_BF16 ? (const void *)rope_verify_kernel<__nv_bfloat16>
                                             : (const void *)rope_verify_kernel<float>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+  }
+  {
+    // the SMs running this kernel keep the largest shared-memory split, so
+    // the attention kernel's CTAs (programmatic dependent launch) can start
+    // beside it instead of waiting for the SM to drain (set once per device
+    // and dtype)
+    static std::atomic<uint64_t> carved[2];
+    const int dev = current_device();
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+    std::atomic<uint64_t> &flag = carved[d->dtype == SIMSD_BF16 ? 1 : 0];
+    if (!bit || !(flag.load() & bit)) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+      flag.fetch_or(bit);
+    }
   }
   if (d->dtype == SIMSD_BF16)
     rope_verify_kernel<__nv_bfloat16><<<p.T, kThreads, smem, stream>>>(a);
