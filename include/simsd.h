@@ -22,8 +22,12 @@
  *     synchronise the host.
  *   - Argument errors are detected on the host and returned before anything
  *     is launched.  A launch failure returns SIMSD_ERR_CUDA.  Kernels never
- *     trap: a bounded wait that runs out sets a bit in the workspace status
- *     word, read with simsd_read_status() (which synchronises the stream).
+ *     trap: a bounded wait that runs out, or device arrays that disagree
+ *     with the limits, set a bit in the workspace's status word (its first
+ *     4 bytes).  The bits stay set across calls until simsd_read_status()
+ *     reads and clears them (no call clears it on the hot path), so a new
+ *     workspace must start zero-filled (or be passed to simsd_read_status
+ *     once).
  *   - Token order inside a sequence with section length B is
  *     D_1..D_B, D~_1..D~_B (2B tokens); sequences are back to back, so
  *     sequence b's tokens start at row 2*cu_B[b].
@@ -265,8 +269,8 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
  *   - The first call on each device looks up the array's device address
  *     (once per device, with that device current); make that first call
  *     before any stream capture.
- *   - Every call shares the one array per device and it keeps the previous
- *     call's contents (the call clears what must start at zero).  Calls that
+ *   - Every call shares the one array per device (zero at load time) and it
+ *     keeps the previous call's contents.  Calls that
  *     overlap on the GPU -- on different streams, or from several host
  *     threads -- race on it: serialise them.
  *   - The kernels' status word lives in that array, so simsd_read_status

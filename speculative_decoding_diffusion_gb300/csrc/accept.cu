@@ -844,10 +844,10 @@ cudaError_t static_scratch(char **out) {
   return cudaSuccess;
 }
 
-// Clears the status word and launches K4.
+// Launches K4 (the status word is not cleared here: its bits stay set until
+// simsd_read_status reads them).
 simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t stream,
                         void *const *events) {
-  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream) != cudaSuccess) return SIMSD_ERR_CUDA;
   AcceptParams a;
   a.target = d->target_logits;
   a.draft = d->draft_logits;

@@ -286,8 +286,6 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   uint32_t *status = (uint32_t *)(ws + p.off_status);
   void *q_rot = ws + p.off_qrot;
   int32_t *tok_seq = (int32_t *)(ws + p.off_tokseq);
-  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), stream) != cudaSuccess)
-    return SIMSD_ERR_CUDA;
   if (!mark(events, 0, stream) ||
       launch_rope_verify(d, p, q_rot, tok_seq, status, stream) != cudaSuccess ||
       !mark(events, 1, stream))

@@ -55,7 +55,7 @@ class DeviceWorkload:
             self._fill_prompt(w, spec)
             self.out = torch.empty_like(self.q)
             nbytes = binding.verify_workspace_size(*self._verify_args())
-            self.verify_ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.verify_ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
         if with_accept and w.target is not None:
             self.target = to_device(w.target, dev)
             self.draft = to_device(w.draft, dev)
@@ -66,7 +66,7 @@ class DeviceWorkload:
             self.token = torch.empty(batch, dtype=torch.int32, device=dev)
             self.pos = torch.empty(batch, dtype=torch.int32, device=dev)
             nbytes = binding.accept_workspace_size(*self._accept_args())
-            self.accept_ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            self.accept_ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     # ------------------------------------------------------------ prompt
     def _fill_prompt(self, w, spec):

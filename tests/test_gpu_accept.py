@@ -1,4 +1,4 @@
-"""GPU parity of simsd_accept (K4a, K4b) against the fp64 oracle.
+"""GPU parity of simsd_accept (K4) against the fp64 oracle.
 
 Decisions (accepted length, rejected position, drawn token) must match the
 oracle exactly on the same logits and uniforms, except for tie-zone
@@ -118,7 +118,7 @@ def test_walk_distribution_monte_carlo():
         c = cu[s:e + 1] - cu[s]
         args = (target[B * s:B * e], draft[B * s:B * e], toks[B * s:B * e], taus[B * s:B * e],
                 c, uni[s:e], n_acc[s:e], tok[s:e], pos[s:e], B * (e - s), B)
-        ws = torch.empty(binding.accept_workspace_size(*args), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(binding.accept_workspace_size(*args), dtype=torch.uint8, device=dev)
         binding.accept(*args[:9], ws, *args[9:])
     torch.cuda.synchronize()
     na, tk, ps = n_acc.cpu().numpy(), tok.cpu().numpy(), pos.cpu().numpy()
