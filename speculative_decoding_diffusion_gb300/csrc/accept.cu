@@ -11,15 +11,16 @@
 // One launch; one thread-block cluster of C CTAs per sequence (C <= 8, from
 // a makespan estimate over the resident-cluster waves: 6-8 for small
 // batches, 1-2 for large ones), CTA r owning the vocabulary slice
-// [r * per, (r + 1) * per) of every row of the sequence.  Each CTA streams its slices of the 2B rows (target and draft of
-// every slot) through a 5-stage shared-memory ring of 32 KB pieces filled by
+// [r * per, (r + 1) * per) of every row of the sequence.  Each CTA streams
+// its slices of the 2B rows (target and draft of every slot) through a 5-stage shared-memory ring of 32 KB pieces filled by
 // bulk copies (one producer warp; 16 consumer warps):
 //   1. per (slot, row): maximum and sum of exponentials of the slice;
-//   2. cluster barrier; CTA 0 merges the C slices' partials through
-//      distributed shared memory, evaluates p(x), q(x) and walks the steps;
-//   3. cluster barrier; on a rejection every CTA streams its slices of the
-//      rejected slot's two rows again (from L2) for the residual and target
-//      masses of each 32 KB piece;
+//   2. cluster barrier; every CTA merges the C slices' partials through
+//      distributed shared memory, evaluates p(x), q(x) and walks the steps
+//      (identically: same inputs, same order; CTA 0 writes the outputs);
+//   3. on a rejection every CTA streams its slices of the rejected slot's
+//      two rows again (from L2) for the residual and target masses of each
+//      32 KB piece;
 //   4. cluster barrier; every CTA reads the C slice totals, so all agree on
 //      the CTA whose slice holds u * S; that CTA finds the piece, then the
 //      entry, by a block scan of the piece in vocabulary order.
@@ -418,7 +419,10 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     cluster_sync();                          // B1: every slice's partials are in place
 
     // ---------------------------------------------------- 2. the walk
-    if (rank == 0 && !producer) {
+    // every CTA merges the slices' partials and walks the steps itself (the
+    // same inputs in the same order give the same decisions everywhere), so
+    // no barrier is needed before the residual pass; CTA 0 writes outputs
+    if (!producer) {
       if (t < 2 * B) {
         float2 v[kMaxCluster];
         float M = -INFINITY;
@@ -443,7 +447,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         if (x < 0 || x >= a.vocab) {         // no slice holds it: the step rejects
           S.px[t] = 0.f;
           S.qx[t] = 0.f;
-          raise_status(a.status, kStatusBadInput);
+          if (rank == 0) raise_status(a.status, kStatusBadInput);
         } else {
           S.px[t] = rel_exp(S.xg[t].x, S.norm[2 * t].x) / S.norm[2 * t].y;
           S.qx[t] = rel_exp(S.xg[t].y, S.norm[2 * t + 1].x) / S.norm[2 * t + 1].y;
@@ -461,12 +465,13 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const int k = S.slot_of_step[st - 1];
           if (!(S.u[st - 1] * S.qx[k] < S.px[k])) { n = st - 1; rej = k; break; }
         }
-        a.n_accept[b] = n;
-        a.pos[b] = rej;
+        if (rank == 0) {
+          a.n_accept[b] = n;
+          a.pos[b] = rej;
+          if (rej < 0) a.token[b] = -1;
+        }
         WalkInfo w{-1, 0.f, 0.f, 1.f, 1.f, 0.f, 0, 0};
-        if (rej < 0) {
-          a.token[b] = -1;
-        } else {
+        if (rej >= 0) {
           w.slot = rej;
           w.Mt = S.norm[2 * rej].x;
           w.Md = S.norm[2 * rej + 1].x;
@@ -477,14 +482,8 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         S.walk = w;
       }
     }
-    cluster_sync();                          // B2: the walk's result is in CTA 0
-    WalkInfo w;
-    {
-      const uint32_t wa = dsmem(&S.walk, 0);
-      const float4 w0 = ld_dsmem4(wa), w1 = ld_dsmem4(wa + 16);
-      w.slot = __float_as_int(w0.x); w.Mt = w0.y; w.Md = w0.z; w.inv_st = w0.w;
-      w.inv_sd = w1.x; w.u = w1.y;
-    }
+    __syncthreads();                         // the walk's result, for the producer too
+    const WalkInfo w = S.walk;
 
     if (w.slot >= 0) {
       // -------------------------------------------------- 3. residual masses
