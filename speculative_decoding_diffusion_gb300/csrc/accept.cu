@@ -20,10 +20,12 @@
 //      (identically: same inputs, same order; CTA 0 writes the outputs);
 //   3. on a rejection every CTA streams its slices of the rejected slot's
 //      two rows again (from L2) for the residual and target masses of each
-//      32 KB piece;
+//      warp's contiguous range of each 32 KB piece;
 //   4. cluster barrier; every CTA reads the C slice totals, so all agree on
-//      the CTA whose slice holds u * S; that CTA finds the piece, then the
-//      entry, by a block scan of the piece in vocabulary order.
+//      the CTA whose slice holds u * S; one warp of that CTA narrows down to
+//      the piece, then the warp range (by warp scans of the stored masses),
+//      then reloads that range (64 B of each row per lane) and finds the
+//      entry by a warp scan in vocabulary order.
 // No global atomics, no partial results in global memory, no second launch.
 // Numerics: a partial state is (R, s) with R a reference in log2 units (the
 // maximum of x log2 e seen so far, rounded once) and s = sum 2^(x log2 e - R),
@@ -49,7 +51,10 @@ constexpr int kThreads = kConsumers + 32;          // + the producer warp
 constexpr int kStages = 5;
 constexpr int kStageBytes = 32768;                 // one piece of one row slice
 constexpr int kVecs = kStageBytes / 16 / kConsumers;   // 16-byte vectors per thread per piece
+constexpr int kWarpVecs = 32 * kVecs;              // 16-byte vectors per warp per piece
 constexpr int kMaxPieces = 32;                     // pieces per row slice
+static_assert(kMaxPieces <= 32 && kConsumerWarps <= 32 && kMaxCluster <= 32,
+              "the draw picks pieces, warps and slices one per lane");
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
 constexpr int kMaxVocab = 1 << 21;                 // kMaxCluster * kMaxPieces * 8192 fp32 entries
 constexpr float kLog2e = 1.4426950408889634f;
@@ -215,16 +220,13 @@ struct __align__(16) AccShared {
   float2 cpart[kMaxPairs];                    // this CTA's slice: (R, s)
   float2 norm[kMaxPairs];                     // CTA 0: merged (M, S) of each row
   float2 xv[kMaxB];                           // logits at the draft token, if in this slice
-  float2 xg[kMaxB];                           // CTA 0: the same, gathered
   float px[kMaxB], qx[kMaxB], u[kMaxB + 1];
   int tau[kMaxB], x[kMaxB], slot_of_step[kMaxB];
   float4 piece_w[kMaxPieces][kConsumerWarps]; // residual pass: per warp (r pair, p pair)
   float4 piece_s[kMaxPieces];
   float4 tot;                                 // this slice's residual and target mass
   WalkInfo walk;                              // CTA 0's result, read by every CTA
-  Ff scan_tot[kConsumerWarps];
-  Ff base, U;
-  int flag, chosen, use_p, sel, best, lastpos;
+  int flag;
 };
 
 struct AcceptParams {
@@ -267,21 +269,24 @@ __device__ __forceinline__ void copy_piece(uint8_t *dst, uint32_t dst_s, const T
   }
 }
 
-// Exclusive scan of two-sum pairs over the consumer threads in thread
-// order: the sum of the values of the lower-numbered threads.
-__device__ __forceinline__ Ff consumer_excl_scan(Ff x, Ff *warp_tot) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Ff inc = x;
+// Warp-wide choice among up to 32 consecutive ranges: lane i holds the
+// mass m of range i (0 for lanes without one), the ranges start at `base`.
+// Returns the first range whose running total exceeds U (else the last one
+// with mass, else 0), and in *start the running total before it.
+__device__ __forceinline__ int warp_pick(Ff m, Ff base, Ff U, Ff *start) {
+  const int lane = threadIdx.x & 31;
+  Ff inc = m;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
     const Ff y = ff_shfl_up(inc, d);
     if (lane >= d) inc = ff_add(y, inc);
   }
-  if (lane == 31) warp_tot[warp] = inc;
-  consumers_sync();
-  Ff base = ff_of(0.f);
-  for (int w = 0; w < warp; ++w) base = ff_add(base, warp_tot[w]);
-  return ff_add(base, ff_add(inc, ff_neg(x)));
+  const Ff run = ff_add(base, inc);
+  const unsigned cross = __ballot_sync(0xffffffffu, m.hi > 0.f && ff_gt(run, U));
+  const unsigned nz = __ballot_sync(0xffffffffu, m.hi > 0.f);
+  const int ch = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : 0);
+  *start = ff_shfl(ff_add(base, ff_add(inc, ff_neg(m))), ch);
+  return ch;
 }
 
 template <typename T>
@@ -423,7 +428,10 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     // same inputs in the same order give the same decisions everywhere), so
     // no barrier is needed before the residual pass; CTA 0 writes outputs
     if (!producer) {
-      if (t < 2 * B) {
+      if (t < 2 * B) {                       // pair t: slot t / 2, row t % 2
+        const int k = t >> 1, row = t & 1, x = S.x[k];
+        const bool xin = x >= 0 && x < a.vocab;
+        const float2 xl = xin ? ld_dsmem2(dsmem(&S.xv[k], x / a.per)) : make_float2(0.f, 0.f);
         float2 v[kMaxCluster];
         float M = -INFINITY;
 #pragma unroll
@@ -437,21 +445,10 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           for (int r = 0; r < kMaxCluster; ++r)
             if (v[r].y > 0.f) sm = ff_add(sm, ff_of(v[r].y * ex2(v[r].x - M)));
         S.norm[t] = make_float2(M, sm.hi + sm.lo);
-      } else if (t >= 2 * kMaxB && t < 2 * kMaxB + B) {
-        const int k = t - 2 * kMaxB, x = S.x[k];
-        S.xg[k] = x >= 0 && x < a.vocab ? ld_dsmem2(dsmem(&S.xv[k], x / a.per)) : make_float2(0.f, 0.f);
-      }
-      consumers_sync();
-      if (t < B) {
-        const int x = S.x[t];
-        if (x < 0 || x >= a.vocab) {         // no slice holds it: the step rejects
-          S.px[t] = 0.f;
-          S.qx[t] = 0.f;
-          if (rank == 0) raise_status(a.status, kStatusBadInput);
-        } else {
-          S.px[t] = rel_exp(S.xg[t].x, S.norm[2 * t].x) / S.norm[2 * t].y;
-          S.qx[t] = rel_exp(S.xg[t].y, S.norm[2 * t + 1].x) / S.norm[2 * t + 1].y;
-        }
+        // p(x) (row 0) or q(x) (row 1); a token no slice holds rejects
+        const float pr = xin ? rel_exp(row ? xl.y : xl.x, M) / (sm.hi + sm.lo) : 0.f;
+        if (row) S.qx[k] = pr; else S.px[k] = pr;
+        if (!xin && row == 0 && rank == 0) raise_status(a.status, kStatusBadInput);
       }
       consumers_sync();
       if (t == 0) {
@@ -510,12 +507,15 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
             if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); }
             break;
           }
+          // warp w reads the contiguous vectors [w * kWarpVecs, (w + 1) * kWarpVecs)
+          // of the piece (lane-interleaved), so its sums are those of one
+          // vocabulary range, which the draw narrows down to
           const uint4 *tv = reinterpret_cast<const uint4 *>(smem + st * kStageBytes);
           const uint4 *dv = reinterpret_cast<const uint4 *>(smem + sd * kStageBytes);
           uint4 wt[kVecs], wd[kVecs];
 #pragma unroll
           for (int i = 0; i < kVecs; ++i) {
-            const int idx = i * kConsumers + t;
+            const int idx = warp * kWarpVecs + i * 32 + lane;
             const bool in = idx * N < n;
             wt[i] = in ? tv[idx] : Ld<T>::neg_inf();
             wd[i] = in ? dv[idx] : Ld<T>::neg_inf();
@@ -549,158 +549,131 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           if (lane == 0) S.piece_w[pc][warp] = make_float4(fr.hi, fr.lo, fp.hi, fp.lo);
         }
         consumers_sync();
-        const bool failed = *(volatile int *)&S.flag != 0;
-        if (t < npieces) {
+        if (warp == 0) {                     // lane i: piece i (npieces <= 32)
+          const bool failed = *(volatile int *)&S.flag != 0;
           Ff r = ff_of(0.f), p = ff_of(0.f);
-          if (!failed)
+          if (lane < npieces && !failed)
             for (int ww = 0; ww < kConsumerWarps; ++ww) {
-              const float4 v = S.piece_w[t][ww];
+              const float4 v = S.piece_w[lane][ww];
               r = ff_add(r, Ff{v.x, v.y});
               p = ff_add(p, Ff{v.z, v.w});
             }
-          S.piece_s[t] = make_float4(r.hi, r.lo, p.hi, p.lo);
-        }
-        consumers_sync();
-        if (t == 0) {
-          Ff r = ff_of(0.f), p = ff_of(0.f);
-          for (int i = 0; i < npieces; ++i) {
-            const float4 v = S.piece_s[i];
-            r = ff_add(r, Ff{v.x, v.y});
-            p = ff_add(p, Ff{v.z, v.w});
+          if (lane < npieces) S.piece_s[lane] = make_float4(r.hi, r.lo, p.hi, p.lo);
+#pragma unroll
+          for (int m = 16; m > 0; m >>= 1) {
+            r = ff_add(r, ff_shfl_xor(r, m));
+            p = ff_add(p, ff_shfl_xor(p, m));
           }
-          S.tot = make_float4(r.hi, r.lo, p.hi, p.lo);
+          if (lane == 0) S.tot = make_float4(r.hi, r.lo, p.hi, p.lo);
         }
       }
       cluster_sync();                        // B3: every slice's masses are in place
 
       // -------------------------------------------------- 4. the draw
-      // Every CTA computes the same choice from the same C totals (in rank
-      // order): U = u * S (u * Sp when the residual is empty) and the first
-      // slice whose running mass exceeds U (else the last with mass).
+      // U = u * S (u * Sp when the residual is empty).  Every CTA makes the
+      // same choice from the same C slice totals (in rank order): the first
+      // slice whose running mass exceeds U, else the last with mass.  Warp 0
+      // of that CTA narrows down the same way to a piece, then to one warp's
+      // vocabulary range of the piece, then to the entry.
       if (warp == 0) {
         const float4 v = lane < a.csize ? ld_dsmem4(dsmem(&S.tot, lane)) : make_float4(0.f, 0.f, 0.f, 0.f);
         Ff Sr{v.x, v.y}, Sp{v.z, v.w};
 #pragma unroll
-        for (int m = kMaxCluster / 2; m > 0; m >>= 1) {
+        for (int m = 16; m > 0; m >>= 1) {
           Sr = ff_add(Sr, ff_shfl_xor(Sr, m));
           Sp = ff_add(Sp, ff_shfl_xor(Sp, m));
         }
-        const int use_p = !(Sr.hi > 0.f);
+        cluster_arrive();                    // B4: this CTA's remote reads are done (used above)
+        const bool use_p = !(Sr.hi > 0.f);
         const Ff tot = use_p ? Sp : Sr;
         const float uh = w.u * tot.hi;
         const Ff U = ff_add(Ff{uh, fmaf(w.u, tot.hi, -uh)}, ff_of(w.u * tot.lo));
-        const Ff m = lane < a.csize ? (use_p ? Ff{v.z, v.w} : Ff{v.x, v.y}) : ff_of(0.f);
-        Ff inc = m;
+        auto mass_of = [&](float4 q) { return use_p ? Ff{q.z, q.w} : Ff{q.x, q.y}; };
+        Ff base;
+        const int ch = warp_pick(mass_of(v), ff_of(0.f), U, &base);
+        if (ch == rank && !*(volatile int *)&S.flag) {
+          const float4 vp = lane < npieces ? S.piece_s[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+          const int sel = warp_pick(mass_of(vp), base, U, &base);
+          const float4 vw = lane < kConsumerWarps ? S.piece_w[sel][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+          const int ws = warp_pick(mass_of(vw), base, U, &base);
+          // lane l: the E consecutive entries from e0 of the warp range's
+          // vectors (the same entries the residual pass summed for it)
+          constexpr int E = kVecs * N;
+          const int n = npieces > 0 ? piece_len(sel) : 0;
+          const int e0 = (ws * kWarpVecs + lane * kVecs) * N;
+          const T *tr = row_ptr(w.slot, 0) + sel * a.piece;
+          const T *dr = row_ptr(w.slot, 1) + sel * a.piece;
+          float mass[E];
+          if (a.bulk && e0 + E <= n) {
+            uint4 vt[kVecs], vd[kVecs];
 #pragma unroll
-        for (int d = 1; d < kMaxCluster; d <<= 1) {
-          const Ff y = ff_shfl_up(inc, d);
-          if (lane >= d) inc = ff_add(y, inc);
-        }
-        const Ff T0 = ff_add(inc, ff_neg(m));
-        const unsigned cross = __ballot_sync(0xffffffffu, m.hi > 0.f && ff_gt(inc, U));
-        const unsigned nz = __ballot_sync(0xffffffffu, m.hi > 0.f);
-        const int ch = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : 0);
-        const Ff base = ff_shfl(T0, ch);
-        if (lane == 0) {
-          S.chosen = ch;
-          S.base = base;
-          S.U = U;
-          S.use_p = use_p;
-          S.best = 0x7fffffff;
-          S.lastpos = -1;
-        }
-      }
-      cluster_arrive();                      // B4: this CTA's remote reads are done
-      __syncthreads();
-      if (S.chosen == rank && !producer && !*(volatile int *)&S.flag) {
-        if (t == 0) {                        // the piece, by a walk over piece masses
-          Ff run = S.base, last_base = S.base;
-          int sel = -1, last_nz = -1;
-          for (int i = 0; i < npieces; ++i) {
-            const float4 v = S.piece_s[i];
-            const Ff m = S.use_p ? Ff{v.z, v.w} : Ff{v.x, v.y};
-            const Ff nxt = ff_add(run, m);
-            if (m.hi > 0.f) {
-              last_nz = i;
-              last_base = run;
-              if (ff_gt(nxt, S.U)) { sel = i; break; }
+            for (int i = 0; i < kVecs; ++i) {
+              vt[i] = __ldg(reinterpret_cast<const uint4 *>(tr + e0) + i);
+              vd[i] = __ldg(reinterpret_cast<const uint4 *>(dr + e0) + i);
             }
-            run = nxt;
-          }
-          if (sel < 0) { sel = max(last_nz, 0); run = last_base; }
-          S.sel = sel;
-          S.base = run;
-        }
-        consumers_sync();
-        // the piece in vocabulary order: thread t holds E consecutive entries
-        constexpr int E = kStageBytes / (int)sizeof(T) / kConsumers;
-        const int sel = S.sel, n = npieces > 0 ? piece_len(sel) : 0;
-        const int e0 = t * E;
-        const T *tr = row_ptr(w.slot, 0) + sel * a.piece;
-        const T *dr = row_ptr(w.slot, 1) + sel * a.piece;
-        float mass[E];
-        if (a.bulk && e0 + E <= n) {
-          uint4 vt[E / N], vd[E / N];
 #pragma unroll
-          for (int i = 0; i < E / N; ++i) {
-            vt[i] = __ldg(reinterpret_cast<const uint4 *>(tr + e0) + i);
-            vd[i] = __ldg(reinterpret_cast<const uint4 *>(dr + e0) + i);
-          }
+            for (int i = 0; i < kVecs; ++i) {
+              float ft[N], fd[N];
+              Ld<T>::unpack(vt[i], ft);
+              Ld<T>::unpack(vd[i], fd);
 #pragma unroll
-          for (int i = 0; i < E / N; ++i) {
-            float ft[N], fd[N];
-            Ld<T>::unpack(vt[i], ft);
-            Ld<T>::unpack(vd[i], fd);
+              for (int e = 0; e < N; ++e) {
+                const float p = rel_exp(ft[e], w.Mt) * w.inv_st;
+                const float q = rel_exp(fd[e], w.Md) * w.inv_sd;
+                mass[i * N + e] = use_p ? p : fmaxf(p - q, 0.f);
+              }
+            }
+          } else {
 #pragma unroll
-            for (int e = 0; e < N; ++e) {
-              const float p = rel_exp(ft[e], w.Mt) * w.inv_st;
-              const float q = rel_exp(fd[e], w.Md) * w.inv_sd;
-              mass[i * N + e] = S.use_p ? p : fmaxf(p - q, 0.f);
+            for (int e = 0; e < E; ++e) {
+              mass[e] = 0.f;
+              if (e0 + e < n) {
+                const float p = rel_exp(Ld<T>::value(tr[e0 + e]), w.Mt) * w.inv_st;
+                const float q = rel_exp(Ld<T>::value(dr[e0 + e]), w.Md) * w.inv_sd;
+                mass[e] = use_p ? p : fmaxf(p - q, 0.f);
+              }
             }
           }
-        } else {
+          // this lane's mass (pairwise fp32) and the lanes' exclusive prefix
+          // as a pair.  Every lane whose range ends beyond U claims its first
+          // entry whose running mass (fp32, relative to the lane's start:
+          // small, so the rounding stays far below the residual tie zone)
+          // exceeds U; the earliest claim wins, else the last entry with mass.
+          float part[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            mass[e] = 0.f;
-            if (e0 + e < n) {
-              const float p = rel_exp(Ld<T>::value(tr[e0 + e]), w.Mt) * w.inv_st;
-              const float q = rel_exp(Ld<T>::value(dr[e0 + e]), w.Md) * w.inv_sd;
-              mass[e] = S.use_p ? p : fmaxf(p - q, 0.f);
+          for (int e = 0; e < E; ++e) part[e] = mass[e];
+#pragma unroll
+          for (int h = E / 2; h > 0; h >>= 1)
+#pragma unroll
+            for (int e = 0; e < h; ++e) part[e] += part[e + h];
+          Ff inc = ff_of(part[0]);
+#pragma unroll
+          for (int dd = 1; dd < 32; dd <<= 1) {
+            const Ff y = ff_shfl_up(inc, dd);
+            if (lane >= dd) inc = ff_add(y, inc);
+          }
+          const Ff start = ff_add(base, ff_add(inc, ff_of(-part[0])));
+          const Ff D = ff_add(U, ff_neg(start));
+          const float d = D.hi + D.lo;       // U - start
+          const int vbase = s0 + sel * a.piece + e0;
+          int first = 0x7fffffff, last_pos = -1;
+#pragma unroll
+          for (int e = 0; e < E; ++e)
+            if (mass[e] > 0.f) last_pos = vbase + e;
+          if (d < part[0]) {
+            float run = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              run += mass[e];
+              if (first == 0x7fffffff && mass[e] > 0.f && run > d) first = vbase + e;
             }
           }
+          first = __reduce_min_sync(0xffffffffu, first);
+          last_pos = __reduce_max_sync(0xffffffffu, last_pos);
+          if (lane == 0) a.token[b] = first != 0x7fffffff ? first : last_pos;
         }
-        // this thread's mass (pairwise fp32) and the consumers' exclusive
-        // prefix as a pair.  Every thread whose range ends beyond U claims
-        // its first entry whose running mass (fp32, relative to the thread's
-        // start: small, so the rounding stays far below the residual tie
-        // zone) exceeds U; the earliest claim wins.
-        float part[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) part[e] = mass[e];
-#pragma unroll
-        for (int h = E / 2; h > 0; h >>= 1)
-#pragma unroll
-          for (int e = 0; e < h; ++e) part[e] += part[e + h];
-        const Ff start = ff_add(S.base, consumer_excl_scan(ff_of(part[0]), S.scan_tot));
-        const Ff D = ff_add(S.U, ff_neg(start));
-        const float d = D.hi + D.lo;           // U - start
-        const int vbase = s0 + sel * a.piece + e0;
-        int first = 0x7fffffff, last_pos = -1;
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          if (mass[e] > 0.f) last_pos = vbase + e;
-        if (d < part[0]) {
-          float run = 0.f;
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            run += mass[e];
-            if (first == 0x7fffffff && mass[e] > 0.f && run > d) first = vbase + e;
-          }
-        }
-        if (first != 0x7fffffff) atomicMin(&S.best, first);
-        if (last_pos >= 0) atomicMax(&S.lastpos, last_pos);
-        consumers_sync();
-        if (t == 0) a.token[b] = S.best != 0x7fffffff ? S.best : S.lastpos;
+      } else {
+        cluster_arrive();                    // B4
       }
     } else {
       cluster_arrive();                      // B4
