@@ -12,20 +12,24 @@
 // a makespan estimate over the resident-cluster waves: 6-8 for small
 // batches, 1-2 for large ones), CTA r owning the vocabulary slice
 // [r * per, (r + 1) * per) of every row of the sequence.  Each CTA streams
-// its slices of the 2B rows (target and draft of every slot) through a 5-stage shared-memory ring of 32 KB pieces filled by
-// bulk copies (one producer warp; 16 consumer warps):
+// its slices of the 2B rows (target and draft of every slot) in pieces of
+// equal size (at most 32 KB) through a 6-stage shared-memory ring filled by
+// bulk copies (one producer warp); two groups of 8 consumer warps take
+// alternate pieces, so one group's waits and reductions overlap the other's
+// exponentials:
 //   1. per (slot, row): maximum and sum of exponentials of the slice;
 //   2. cluster barrier; every CTA merges the C slices' partials through
 //      distributed shared memory, evaluates p(x), q(x) and walks the steps
 //      (identically: same inputs, same order; CTA 0 writes the outputs);
 //   3. on a rejection every CTA streams its slices of the rejected slot's
-//      two rows again (from L2) for the residual and target masses of each
-//      warp's contiguous range of each 32 KB piece;
+//      two rows again (from L2) for the residual and target masses of 16
+//      contiguous vocabulary ranges of each piece;
 //   4. cluster barrier; every CTA reads the C slice totals, so all agree on
 //      the CTA whose slice holds u * S; one warp of that CTA narrows down to
-//      the piece, then the warp range (by warp scans of the stored masses),
-//      then reloads that range (64 B of each row per lane) and finds the
-//      entry by a warp scan in vocabulary order.
+//      the piece, then the range (warp scans of the stored masses), then
+//      rereads that range (64 B of each row per lane; from the ring when the
+//      piece is still there) and finds the entry by a warp scan in
+//      vocabulary order.
 // No global atomics, no partial results in global memory, no second launch.
 // Numerics: a partial state is (R, s) with R a reference in log2 units (the
 // maximum of x log2 e seen so far, rounded once) and s = sum 2^(x log2 e - R),
@@ -48,13 +52,19 @@ constexpr int kMaxCluster = 8;                     // CTAs per sequence, at most
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;          // + the producer warp
-constexpr int kStages = 5;
-constexpr int kStageBytes = 32768;                 // one piece of one row slice
-constexpr int kVecs = kStageBytes / 16 / kConsumers;   // 16-byte vectors per thread per piece
+constexpr int kGroupWarps = kConsumerWarps / 2;    // two groups take alternate pieces
+constexpr int kGroupThreads = kGroupWarps * 32;
+constexpr int kStages = 6;
+constexpr int kStageBytes = 32768;                 // at most one piece of one row slice
+constexpr int kVecs = kStageBytes / 16 / kGroupThreads;   // 16-byte vectors per thread per piece
 constexpr int kWarpVecs = 32 * kVecs;              // 16-byte vectors per warp per piece
+constexpr int kRanges = 2 * kGroupWarps;           // vocabulary ranges per piece (residual sums)
+constexpr int kRangeVecs = kWarpVecs / 2;
 constexpr int kMaxPieces = 32;                     // pieces per row slice
-static_assert(kMaxPieces <= 32 && kConsumerWarps <= 32 && kMaxCluster <= 32,
-              "the draw picks pieces, warps and slices one per lane");
+static_assert(kMaxPieces <= 32 && kRanges <= 32 && kMaxCluster <= 32,
+              "the draw picks pieces, ranges and slices one per lane");
+static_assert(kVecs % 2 == 0 && kRangeVecs % 32 == 0, "a range is whole vectors per lane");
+static_assert(kVecs * 8 % 8 == 0 && (kVecs / 2) * 4 % 8 == 0, "accumulator slots repeat every half");
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
 constexpr int kMaxVocab = 1 << 21;                 // kMaxCluster * kMaxPieces * 8192 fp32 entries
 constexpr float kLog2e = 1.4426950408889634f;
@@ -99,14 +109,6 @@ __device__ __forceinline__ float ex2(float x) {
 
 // 2^(x log2 e - R): the argument rounded once.
 __device__ __forceinline__ float rel_exp(float x, float R) { return ex2(fmaf(x, kLog2e, -R)); }
-
-// (R, s) with s = sum 2^(x log2 e - R): merge two partial states.
-__device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
-  const float mm = fmaxf(m, m2);
-  if (mm == -INFINITY) { m = mm; s = 0.f; return; }
-  s = s * ex2(m - mm) + s2 * ex2(m2 - mm);
-  m = mm;
-}
 
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -157,6 +159,15 @@ template <> struct Ld<float> {
     f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
     f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
   }
+  // the vector at p (16-byte aligned if `aligned`): entries past `valid`
+  // (which may be <= 0) read as -inf
+  static __device__ __forceinline__ uint4 load(const float *p, int valid, bool aligned) {
+    if (aligned && valid >= N) return *reinterpret_cast<const uint4 *>(p);
+    uint32_t r[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) r[e] = e < valid ? __float_as_uint(p[e]) : kNegInf;
+    return make_uint4(r[0], r[1], r[2], r[3]);
+  }
   static __device__ __forceinline__ float vmax(const uint4 *w, int n) {
     float m0 = -INFINITY, m1 = -INFINITY;
     for (int i = 0; i < n; ++i) {
@@ -179,6 +190,17 @@ template <> struct Ld<__nv_bfloat16> {
       f[2 * i] = __uint_as_float(w[i] << 16);
       f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
+  }
+  static __device__ __forceinline__ uint4 load(const __nv_bfloat16 *p, int valid, bool aligned) {
+    if (aligned && valid >= N) return *reinterpret_cast<const uint4 *>(p);
+    uint32_t r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = 2 * i < valid ? __bfloat16_as_ushort(p[2 * i]) : 0xff80u;
+      const uint32_t hi = 2 * i + 1 < valid ? __bfloat16_as_ushort(p[2 * i + 1]) : 0xff80u;
+      r[i] = lo | (hi << 16);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
   }
   static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
     uint32_t d;
@@ -222,7 +244,7 @@ struct __align__(16) AccShared {
   float2 xv[kMaxB];                           // logits at the draft token, if in this slice
   float px[kMaxB], qx[kMaxB], u[kMaxB + 1];
   int tau[kMaxB], x[kMaxB], slot_of_step[kMaxB];
-  float4 piece_w[kMaxPieces][kConsumerWarps]; // residual pass: per warp (r pair, p pair)
+  float4 piece_w[kMaxPieces][kRanges];        // residual pass: per range (r pair, p pair)
   float4 piece_s[kMaxPieces];
   float4 tot;                                 // this slice's residual and target mass
   WalkInfo walk;                              // CTA 0's result, read by every CTA
@@ -273,7 +295,7 @@ __device__ __forceinline__ void copy_piece(uint8_t *dst, uint32_t dst_s, const T
 // mass m of range i (0 for lanes without one), the ranges start at `base`.
 // Returns the first range whose running total exceeds U (else the last one
 // with mass, else 0), and in *start the running total before it.
-__device__ __forceinline__ int warp_pick(Ff m, Ff base, Ff U, Ff *start) {
+__device__ __noinline__ int warp_pick(Ff m, Ff base, Ff U, Ff *start) {
   const int lane = threadIdx.x & 31;
   Ff inc = m;
 #pragma unroll
@@ -347,11 +369,18 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         if (++pc == npieces) { pc = 0; ++pair; }
       }
     } else {
+      // The two consumer groups (warps 0-7, 8-15) take alternate pieces, so
+      // one group's barrier wait, loads and merges overlap the other's
+      // exponentials instead of all warps moving in step.
+      const int grp = warp / kGroupWarps, gtid = t % kGroupThreads;
+      if (lane == 0)                         // pairs this warp sees no piece of
+        for (int q = 0; q < 2 * B; ++q) S.part_w[q][warp] = make_float2(-INFINITY, 0.f);
       float R = -INFINITY, sum = 0.f;
-      for (int pair = 0, pc = 0; g < J; ++g) {
-        const int s = g % kStages;
+      for (int gg = grp; gg < J; gg += 2) {
+        const int pair = gg / npieces, pc = gg - pair * npieces;
+        const int s = gg % kStages;
         const int n = piece_len(pc);
-        if (!mbar_wait_warp(smem_u32(&S.full[s]), (g / kStages) & 1)) {
+        if (!mbar_wait_warp(smem_u32(&S.full[s]), (gg / kStages) & 1)) {
           if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); }
           break;
         }
@@ -359,33 +388,16 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         uint4 w[kVecs];
 #pragma unroll
         for (int i = 0; i < kVecs; ++i) {
-          const int idx = i * kConsumers + t;
+          const int idx = i * kGroupThreads + gtid;
           w[i] = idx * N < n ? sv[idx] : Ld<T>::neg_inf();
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
-        const float mx = Ld<T>::vmax(w, kVecs);
-        const float Rn = mx * kLog2e;
-        if (Rn > R) {
-          sum = R == -INFINITY ? 0.f : sum * ex2(R - Rn);
-          R = Rn;
-        }
-        if (R != -INFINITY) {
-          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < kVecs; ++i) {
-            float f[N];
-            Ld<T>::unpack(w[i], f);
-#pragma unroll
-            for (int e = 0; e < N; ++e) acc[(i * N + e) & 7] += rel_exp(f[e], R);
-          }
-          sum += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-        }
+        if (lane == 0) mbar_arrive_n(smem_u32(&S.empty[s]), 2);
         // the logit at the slot's draft token, if this piece holds it
         const int k = pair >> 1, row = pair & 1;
         const int off = S.x[k] - (s0 + pc * a.piece);
-        if (off >= 0 && off < n && t == (off / N) % kConsumers) {
-          const int i = off / N / kConsumers;
+        if (off >= 0 && off < n && gtid == (off / N) % kGroupThreads) {
+          const int i = off / N / kGroupThreads;
           uint4 wi = w[0];
 #pragma unroll
           for (int ii = 1; ii < kVecs; ++ii)
@@ -393,16 +405,47 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const float v = pick<T>(wi, off % N);
           if (row) S.xv[k].y = v; else S.xv[k].x = v;
         }
-        if (pc == npieces - 1) {             // the pair's slice is done: warp merge
+        const float mx = Ld<T>::vmax(w, kVecs);
+        const float Rn = mx * kLog2e;
+        if (Rn > R) {
+          sum = R == -INFINITY ? 0.f : sum * ex2(R - Rn);
+          R = Rn;
+        }
+        if (R != -INFINITY) {
+          // vectors past the piece's end hold -inf (adding their zeros
+          // changes nothing): a warp skips those of a short piece.  Two
+          // rolled halves of four vectors (the code stays small: it is
+          // often fetched cold, after other kernels ran).
+          const int nvec = (n + N - 1) / N;
+          const int v0 = (warp % kGroupWarps) * 32;
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
 #pragma unroll
-          for (int m = 16; m > 0; m >>= 1)
-            lse_merge(R, sum, __shfl_xor_sync(0xffffffffu, R, m),
-                      __shfl_xor_sync(0xffffffffu, sum, m));
-          if (lane == 0) S.part_w[pair][warp] = make_float2(R, sum);
+            for (int i = 0; i < kVecs / 2; ++i) {
+              if ((h * kVecs / 2 + i) * kGroupThreads + v0 >= nvec) break;
+              float f[N];
+              Ld<T>::unpack(w[i], f);
+#pragma unroll
+              for (int e = 0; e < N; ++e) acc[(i * N + e) & 7] += rel_exp(f[e], R);
+            }
+#pragma unroll
+            for (int i = 0; i < kVecs / 2; ++i) w[i] = w[i + kVecs / 2];
+          }
+          sum += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        }
+        if (gg + 2 >= (pair + 1) * npieces) {   // the group's last piece of the pair: warp merge
+          // to the warp's largest reference: one rescale per lane, one sum
+          float Rm = R;
+#pragma unroll
+          for (int m = 16; m > 0; m >>= 1) Rm = fmaxf(Rm, __shfl_xor_sync(0xffffffffu, Rm, m));
+          float sc = Rm == -INFINITY ? 0.f : sum * ex2(R - Rm);
+#pragma unroll
+          for (int m = 16; m > 0; m >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, m);
+          if (lane == 0) S.part_w[pair][warp] = make_float2(Rm, sc);
           R = -INFINITY;
           sum = 0.f;
         }
-        if (++pc == npieces) { pc = 0; ++pair; }
       }
       consumers_sync();
       if (t < 2 * B) {                       // this CTA's slice of pair t
@@ -498,7 +541,12 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           issued = g + 1;
         }
       } else {
-        for (int pc = 0; pc < npieces && !*(volatile int *)&S.flag; ++pc) {
+        // the groups take alternate pieces; warp w of a group reads the
+        // contiguous vectors [w * kWarpVecs, (w + 1) * kWarpVecs) of the
+        // piece (lane-interleaved) and sums its two halves apart: the masses
+        // of two vocabulary ranges, which the draw narrows down to
+        const int gwarp = warp % kGroupWarps;
+        for (int pc = warp / kGroupWarps; pc < npieces && !*(volatile int *)&S.flag; pc += 2) {
           const int gt = J + 2 * pc, gd = gt + 1;
           const int st = gt % kStages, sd = gd % kStages;
           const int n = piece_len(pc);
@@ -507,53 +555,50 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
             if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); }
             break;
           }
-          // warp w reads the contiguous vectors [w * kWarpVecs, (w + 1) * kWarpVecs)
-          // of the piece (lane-interleaved), so its sums are those of one
-          // vocabulary range, which the draw narrows down to
           const uint4 *tv = reinterpret_cast<const uint4 *>(smem + st * kStageBytes);
           const uint4 *dv = reinterpret_cast<const uint4 *>(smem + sd * kStageBytes);
-          uint4 wt[kVecs], wd[kVecs];
+          const int nvec = (n + N - 1) / N;
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {          // the two ranges
+            float rs[4] = {0.f, 0.f, 0.f, 0.f}, ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+            for (int i = 0; i < kVecs / 2; ++i) {   // rolled: this code runs cold
+              const int col = gwarp * kWarpVecs + (h * kVecs / 2 + i) * 32;
+              if (col >= nvec) break;               // only -inf beyond
+              const int idx = col + lane;
+              const bool in = idx * N < n;
+              float ft[N], fd[N];
+              Ld<T>::unpack(in ? tv[idx] : Ld<T>::neg_inf(), ft);
+              Ld<T>::unpack(in ? dv[idx] : Ld<T>::neg_inf(), fd);
 #pragma unroll
-          for (int i = 0; i < kVecs; ++i) {
-            const int idx = warp * kWarpVecs + i * 32 + lane;
-            const bool in = idx * N < n;
-            wt[i] = in ? tv[idx] : Ld<T>::neg_inf();
-            wd[i] = in ? dv[idx] : Ld<T>::neg_inf();
+              for (int e = 0; e < N; ++e) {
+                const float p = rel_exp(ft[e], w.Mt) * w.inv_st;
+                const float q = rel_exp(fd[e], w.Md) * w.inv_sd;
+                rs[e & 3] += fmaxf(p - q, 0.f);
+                ps[e & 3] += p;
+              }
+            }
+            Ff fr = ff_add(ff_of(rs[0] + rs[1]), ff_of(rs[2] + rs[3]));
+            Ff fp = ff_add(ff_of(ps[0] + ps[1]), ff_of(ps[2] + ps[3]));
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) {
+              fr = ff_add(fr, ff_shfl_xor(fr, m));
+              fp = ff_add(fp, ff_shfl_xor(fp, m));
+            }
+            if (lane == 0) S.piece_w[pc][2 * gwarp + h] = make_float4(fr.hi, fr.lo, fp.hi, fp.lo);
           }
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_u32(&S.empty[st]));
-            mbar_arrive(smem_u32(&S.empty[sd]));
+            mbar_arrive_n(smem_u32(&S.empty[st]), 2);
+            mbar_arrive_n(smem_u32(&S.empty[sd]), 2);
           }
-          float rs[4] = {0.f, 0.f, 0.f, 0.f}, ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < kVecs; ++i) {
-            float ft[N], fd[N];
-            Ld<T>::unpack(wt[i], ft);
-            Ld<T>::unpack(wd[i], fd);
-#pragma unroll
-            for (int e = 0; e < N; ++e) {
-              const float p = rel_exp(ft[e], w.Mt) * w.inv_st;
-              const float q = rel_exp(fd[e], w.Md) * w.inv_sd;
-              rs[e & 3] += fmaxf(p - q, 0.f);
-              ps[e & 3] += p;
-            }
-          }
-          Ff fr = ff_add(ff_of(rs[0] + rs[1]), ff_of(rs[2] + rs[3]));
-          Ff fp = ff_add(ff_of(ps[0] + ps[1]), ff_of(ps[2] + ps[3]));
-#pragma unroll
-          for (int m = 16; m > 0; m >>= 1) {
-            fr = ff_add(fr, ff_shfl_xor(fr, m));
-            fp = ff_add(fp, ff_shfl_xor(fp, m));
-          }
-          if (lane == 0) S.piece_w[pc][warp] = make_float4(fr.hi, fr.lo, fp.hi, fp.lo);
         }
         consumers_sync();
         if (warp == 0) {                     // lane i: piece i (npieces <= 32)
           const bool failed = *(volatile int *)&S.flag != 0;
           Ff r = ff_of(0.f), p = ff_of(0.f);
           if (lane < npieces && !failed)
-            for (int ww = 0; ww < kConsumerWarps; ++ww) {
+            for (int ww = 0; ww < kRanges; ++ww) {
               const float4 v = S.piece_w[lane][ww];
               r = ff_add(r, Ff{v.x, v.y});
               p = ff_add(p, Ff{v.z, v.w});
@@ -594,81 +639,74 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         if (ch == rank && !*(volatile int *)&S.flag) {
           const float4 vp = lane < npieces ? S.piece_s[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
           const int sel = warp_pick(mass_of(vp), base, U, &base);
-          const float4 vw = lane < kConsumerWarps ? S.piece_w[sel][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 vw = lane < kRanges ? S.piece_w[sel][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
           const int ws = warp_pick(mass_of(vw), base, U, &base);
-          // lane l: the E consecutive entries from e0 of the warp range's
-          // vectors (the same entries the residual pass summed for it)
-          constexpr int E = kVecs * N;
+          // The range's 128 vectors as 4 columns of 32 (lane l: vectors
+          // l, l + 32, l + 64, l + 96), read from the ring if the piece is
+          // among the residual pass's last kStages stages, else from L2.
+          // Column by column in vocabulary order: the lanes' masses, their
+          // inclusive scan (fp32, relative to the range start: small, so the
+          // rounding stays far below the residual tie zone); the lane whose
+          // span holds U claims its first entry with mass whose running
+          // total exceeds U; else the last entry with mass.
           const int n = npieces > 0 ? piece_len(sel) : 0;
-          const int e0 = (ws * kWarpVecs + lane * kVecs) * N;
-          const T *tr = row_ptr(w.slot, 0) + sel * a.piece;
-          const T *dr = row_ptr(w.slot, 1) + sel * a.piece;
-          float mass[E];
-          if (a.bulk && e0 + E <= n) {
-            uint4 vt[kVecs], vd[kVecs];
+          const int gsel = J + 2 * sel;
+          const bool in_ring = gsel >= J + 2 * npieces - kStages;
+          const T *tr = in_ring ? reinterpret_cast<const T *>(smem + (gsel % kStages) * kStageBytes)
+                                : row_ptr(w.slot, 0) + sel * a.piece;
+          const T *dr = in_ring ? reinterpret_cast<const T *>(smem + ((gsel + 1) % kStages) * kStageBytes)
+                                : row_ptr(w.slot, 1) + sel * a.piece;
+          constexpr int kCols = kRangeVecs / 32;
+          uint4 vt[kCols], vd[kCols];
 #pragma unroll
-            for (int i = 0; i < kVecs; ++i) {
-              vt[i] = __ldg(reinterpret_cast<const uint4 *>(tr + e0) + i);
-              vd[i] = __ldg(reinterpret_cast<const uint4 *>(dr + e0) + i);
+          for (int i = 0; i < kCols; ++i) {
+            const int e = (ws * kRangeVecs + i * 32 + lane) * N;   // first entry of the vector
+            vt[i] = Ld<T>::load(tr + e, n - e, a.bulk != 0);
+            vd[i] = Ld<T>::load(dr + e, n - e, a.bulk != 0);
+          }
+          const Ff D0 = ff_add(U, ff_neg(base));
+          const float d = D0.hi + D0.lo;     // U - the range's start
+          float col_base = 0.f;
+          int first = 0x7fffffff, last_pos = -1;
+#pragma unroll 1
+          for (int i = 0; i < kCols && first == 0x7fffffff; ++i) {
+            const int vbase = s0 + sel * a.piece + (ws * kRangeVecs + i * 32 + lane) * N;
+            float ft[N], fd[N], m[N];
+            Ld<T>::unpack(vt[0], ft);
+            Ld<T>::unpack(vd[0], fd);
+            float ls = 0.f;
+#pragma unroll
+            for (int e = 0; e < N; ++e) {
+              const float p = rel_exp(ft[e], w.Mt) * w.inv_st;
+              const float q = rel_exp(fd[e], w.Md) * w.inv_sd;
+              m[e] = use_p ? p : fmaxf(p - q, 0.f);
+              ls += m[e];
+              if (m[e] > 0.f) last_pos = vbase + e;
             }
+            float inc = ls;
 #pragma unroll
-            for (int i = 0; i < kVecs; ++i) {
-              float ft[N], fd[N];
-              Ld<T>::unpack(vt[i], ft);
-              Ld<T>::unpack(vd[i], fd);
+            for (int dd = 1; dd < 32; dd <<= 1) {
+              const float y = __shfl_up_sync(0xffffffffu, inc, dd);
+              if (lane >= dd) inc += y;
+            }
+            const float prev = __shfl_up_sync(0xffffffffu, inc, 1);
+            const float start = col_base + (lane ? prev : 0.f);
+            if (d < col_base + inc) {
+              float run = 0.f;
 #pragma unroll
               for (int e = 0; e < N; ++e) {
-                const float p = rel_exp(ft[e], w.Mt) * w.inv_st;
-                const float q = rel_exp(fd[e], w.Md) * w.inv_sd;
-                mass[i * N + e] = use_p ? p : fmaxf(p - q, 0.f);
+                run += m[e];
+                if (first == 0x7fffffff && m[e] > 0.f && start + run > d) first = vbase + e;
               }
             }
-          } else {
+            first = __reduce_min_sync(0xffffffffu, first);
+            col_base += __shfl_sync(0xffffffffu, inc, 31);
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-              mass[e] = 0.f;
-              if (e0 + e < n) {
-                const float p = rel_exp(Ld<T>::value(tr[e0 + e]), w.Mt) * w.inv_st;
-                const float q = rel_exp(Ld<T>::value(dr[e0 + e]), w.Md) * w.inv_sd;
-                mass[e] = use_p ? p : fmaxf(p - q, 0.f);
-              }
+            for (int c = 0; c + 1 < kCols; ++c) {
+              vt[c] = vt[c + 1];
+              vd[c] = vd[c + 1];
             }
           }
-          // this lane's mass (pairwise fp32) and the lanes' exclusive prefix
-          // as a pair.  Every lane whose range ends beyond U claims its first
-          // entry whose running mass (fp32, relative to the lane's start:
-          // small, so the rounding stays far below the residual tie zone)
-          // exceeds U; the earliest claim wins, else the last entry with mass.
-          float part[E];
-#pragma unroll
-          for (int e = 0; e < E; ++e) part[e] = mass[e];
-#pragma unroll
-          for (int h = E / 2; h > 0; h >>= 1)
-#pragma unroll
-            for (int e = 0; e < h; ++e) part[e] += part[e + h];
-          Ff inc = ff_of(part[0]);
-#pragma unroll
-          for (int dd = 1; dd < 32; dd <<= 1) {
-            const Ff y = ff_shfl_up(inc, dd);
-            if (lane >= dd) inc = ff_add(y, inc);
-          }
-          const Ff start = ff_add(base, ff_add(inc, ff_of(-part[0])));
-          const Ff D = ff_add(U, ff_neg(start));
-          const float d = D.hi + D.lo;       // U - start
-          const int vbase = s0 + sel * a.piece + e0;
-          int first = 0x7fffffff, last_pos = -1;
-#pragma unroll
-          for (int e = 0; e < E; ++e)
-            if (mass[e] > 0.f) last_pos = vbase + e;
-          if (d < part[0]) {
-            float run = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) {
-              run += mass[e];
-              if (first == 0x7fffffff && mass[e] > 0.f && run > d) first = vbase + e;
-            }
-          }
-          first = __reduce_min_sync(0xffffffffu, first);
           last_pos = __reduce_max_sync(0xffffffffu, last_pos);
           if (lane == 0) a.token[b] = first != 0x7fffffff ? first : last_pos;
         }
@@ -770,7 +808,9 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
   }
   a.csize = csize;
   a.per = ((a.vocab + csize - 1) / csize + vec - 1) / vec * vec;
-  a.piece = piece;
+  // pieces of equal size (whole vectors, at most one stage) per slice
+  const int np = (a.per + piece - 1) / piece;
+  a.piece = ((a.per + np - 1) / np + vec - 1) / vec * vec;
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg = launch_config(csize, a.batch, stream, attr);
   return cudaLaunchKernelEx(&cfg, accept_kernel<T>, a);
