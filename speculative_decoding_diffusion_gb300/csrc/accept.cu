@@ -64,6 +64,8 @@ constexpr int kMaxPieces = 32;                     // pieces per row slice
 static_assert(kMaxPieces <= 32 && kRanges <= 32 && kMaxCluster <= 32,
               "the draw picks pieces, ranges and slices one per lane");
 static_assert(kVecs % 2 == 0 && kRangeVecs % 32 == 0, "a range is whole vectors per lane");
+static_assert(2 * kMaxB * kMaxCluster <= kConsumers && 32 % kMaxCluster == 0,
+              "one consumer thread per (pair, slice)");
 static_assert(kVecs * 8 % 8 == 0 && (kVecs / 2) * 4 % 8 == 0, "accumulator slots repeat every half");
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
 constexpr int kMaxVocab = 1 << 21;                 // kMaxCluster * kMaxPieces * 8192 fp32 entries
@@ -274,7 +276,7 @@ struct AcceptParams {
 // and a plain arrival; those fill the rest of the last 16-byte vector with
 // -inf, since consumers read whole vectors).
 template <typename T>
-__device__ __forceinline__ void copy_piece(uint8_t *dst, uint32_t dst_s, const T *src, int n,
+__device__ __noinline__ void copy_piece(uint8_t *dst, uint32_t dst_s, const T *src, int n,
                                            uint32_t full, bool bulk, int lane) {
   if (bulk) {
     if (lane == 0) {
@@ -391,20 +393,17 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const int idx = i * kGroupThreads + gtid;
           w[i] = idx * N < n ? sv[idx] : Ld<T>::neg_inf();
         }
+        // the logit at the slot's draft token, if this piece holds it
+        if (gtid == 0) {
+          const int k = pair >> 1, row = pair & 1;
+          const int off = S.x[k] - (s0 + pc * a.piece);
+          if (off >= 0 && off < n) {
+            const float v = pick<T>(sv[off / N], off % N);
+            if (row) S.xv[k].y = v; else S.xv[k].x = v;
+          }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive_n(smem_u32(&S.empty[s]), 2);
-        // the logit at the slot's draft token, if this piece holds it
-        const int k = pair >> 1, row = pair & 1;
-        const int off = S.x[k] - (s0 + pc * a.piece);
-        if (off >= 0 && off < n && gtid == (off / N) % kGroupThreads) {
-          const int i = off / N / kGroupThreads;
-          uint4 wi = w[0];
-#pragma unroll
-          for (int ii = 1; ii < kVecs; ++ii)
-            if (i == ii) wi = w[ii];
-          const float v = pick<T>(wi, off % N);
-          if (row) S.xv[k].y = v; else S.xv[k].x = v;
-        }
         const float mx = Ld<T>::vmax(w, kVecs);
         const float Rn = mx * kLog2e;
         if (Rn > R) {
@@ -455,6 +454,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, S.part_w[t][w].x);
           Ff sm = ff_of(0.f);
           if (M != -INFINITY)
+#pragma unroll 1
             for (int w = 0; w < kConsumerWarps; ++w) {
               const float2 v = S.part_w[t][w];
               if (v.y > 0.f) sm = ff_add(sm, ff_of(v.y * ex2(v.x - M)));
@@ -471,27 +471,28 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     // same inputs in the same order give the same decisions everywhere), so
     // no barrier is needed before the residual pass; CTA 0 writes outputs
     if (!producer) {
-      if (t < 2 * B) {                       // pair t: slot t / 2, row t % 2
-        const int k = t >> 1, row = t & 1, x = S.x[k];
+      // thread (pair q, slice r) reads one slice's partial; 8-lane groups
+      // merge them (pair q: slot q / 2, row q % 2)
+      if (warp * 32 < 2 * B * kMaxCluster) {  // whole warps: the shuffles need every lane
+        const int q = t / kMaxCluster, r = t % kMaxCluster;
+        const bool mine = q < 2 * B;
+        const int k = q >> 1, row = q & 1, x = mine ? S.x[k] : -1;
         const bool xin = x >= 0 && x < a.vocab;
-        const float2 xl = xin ? ld_dsmem2(dsmem(&S.xv[k], x / a.per)) : make_float2(0.f, 0.f);
-        float2 v[kMaxCluster];
-        float M = -INFINITY;
+        const float2 xl = r == 0 && xin ? ld_dsmem2(dsmem(&S.xv[k], x / a.per)) : make_float2(0.f, 0.f);
+        const float2 v = mine && r < a.csize ? ld_dsmem2(dsmem(&S.cpart[q], r)) : make_float2(-INFINITY, 0.f);
+        float M = v.x;
 #pragma unroll
-        for (int r = 0; r < kMaxCluster; ++r) {
-          v[r] = r < a.csize ? ld_dsmem2(dsmem(&S.cpart[t], r)) : make_float2(-INFINITY, 0.f);
-          M = fmaxf(M, v[r].x);
+        for (int m = kMaxCluster / 2; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+        Ff sm = ff_of(M != -INFINITY && v.y > 0.f ? v.y * ex2(v.x - M) : 0.f);
+#pragma unroll 1
+        for (int m = kMaxCluster / 2; m > 0; m >>= 1) sm = ff_add(sm, ff_shfl_xor(sm, m));
+        if (mine && r == 0) {
+          S.norm[q] = make_float2(M, sm.hi + sm.lo);
+          // p(x) (row 0) or q(x) (row 1); a token no slice holds rejects
+          const float pr = xin ? rel_exp(row ? xl.y : xl.x, M) / (sm.hi + sm.lo) : 0.f;
+          if (row) S.qx[k] = pr; else S.px[k] = pr;
+          if (!xin && row == 0 && rank == 0) raise_status(a.status, kStatusBadInput);
         }
-        Ff sm = ff_of(0.f);
-        if (M != -INFINITY)
-#pragma unroll
-          for (int r = 0; r < kMaxCluster; ++r)
-            if (v[r].y > 0.f) sm = ff_add(sm, ff_of(v[r].y * ex2(v[r].x - M)));
-        S.norm[t] = make_float2(M, sm.hi + sm.lo);
-        // p(x) (row 0) or q(x) (row 1); a token no slice holds rejects
-        const float pr = xin ? rel_exp(row ? xl.y : xl.x, M) / (sm.hi + sm.lo) : 0.f;
-        if (row) S.qx[k] = pr; else S.px[k] = pr;
-        if (!xin && row == 0 && rank == 0) raise_status(a.status, kStatusBadInput);
       }
       consumers_sync();
       if (t == 0) {
@@ -580,7 +581,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
             }
             Ff fr = ff_add(ff_of(rs[0] + rs[1]), ff_of(rs[2] + rs[3]));
             Ff fp = ff_add(ff_of(ps[0] + ps[1]), ff_of(ps[2] + ps[3]));
-#pragma unroll
+#pragma unroll 1
             for (int m = 16; m > 0; m >>= 1) {
               fr = ff_add(fr, ff_shfl_xor(fr, m));
               fp = ff_add(fp, ff_shfl_xor(fp, m));
@@ -598,13 +599,14 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const bool failed = *(volatile int *)&S.flag != 0;
           Ff r = ff_of(0.f), p = ff_of(0.f);
           if (lane < npieces && !failed)
+#pragma unroll 1
             for (int ww = 0; ww < kRanges; ++ww) {
               const float4 v = S.piece_w[lane][ww];
               r = ff_add(r, Ff{v.x, v.y});
               p = ff_add(p, Ff{v.z, v.w});
             }
           if (lane < npieces) S.piece_s[lane] = make_float4(r.hi, r.lo, p.hi, p.lo);
-#pragma unroll
+#pragma unroll 1
           for (int m = 16; m > 0; m >>= 1) {
             r = ff_add(r, ff_shfl_xor(r, m));
             p = ff_add(p, ff_shfl_xor(p, m));
@@ -623,7 +625,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
       if (warp == 0) {
         const float4 v = lane < a.csize ? ld_dsmem4(dsmem(&S.tot, lane)) : make_float4(0.f, 0.f, 0.f, 0.f);
         Ff Sr{v.x, v.y}, Sp{v.z, v.w};
-#pragma unroll
+#pragma unroll 1
         for (int m = 16; m > 0; m >>= 1) {
           Sr = ff_add(Sr, ff_shfl_xor(Sr, m));
           Sp = ff_add(Sp, ff_shfl_xor(Sp, m));
@@ -657,23 +659,17 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const T *dr = in_ring ? reinterpret_cast<const T *>(smem + ((gsel + 1) % kStages) * kStageBytes)
                                 : row_ptr(w.slot, 1) + sel * a.piece;
           constexpr int kCols = kRangeVecs / 32;
-          uint4 vt[kCols], vd[kCols];
-#pragma unroll
-          for (int i = 0; i < kCols; ++i) {
-            const int e = (ws * kRangeVecs + i * 32 + lane) * N;   // first entry of the vector
-            vt[i] = Ld<T>::load(tr + e, n - e, a.bulk != 0);
-            vd[i] = Ld<T>::load(dr + e, n - e, a.bulk != 0);
-          }
           const Ff D0 = ff_add(U, ff_neg(base));
           const float d = D0.hi + D0.lo;     // U - the range's start
           float col_base = 0.f;
           int first = 0x7fffffff, last_pos = -1;
 #pragma unroll 1
           for (int i = 0; i < kCols && first == 0x7fffffff; ++i) {
-            const int vbase = s0 + sel * a.piece + (ws * kRangeVecs + i * 32 + lane) * N;
+            const int e = (ws * kRangeVecs + i * 32 + lane) * N;   // the vector's first entry
+            const int vbase = s0 + sel * a.piece + e;
             float ft[N], fd[N], m[N];
-            Ld<T>::unpack(vt[0], ft);
-            Ld<T>::unpack(vd[0], fd);
+            Ld<T>::unpack(Ld<T>::load(tr + e, n - e, a.bulk != 0), ft);
+            Ld<T>::unpack(Ld<T>::load(dr + e, n - e, a.bulk != 0), fd);
             float ls = 0.f;
 #pragma unroll
             for (int e = 0; e < N; ++e) {
@@ -701,11 +697,6 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
             }
             first = __reduce_min_sync(0xffffffffu, first);
             col_base += __shfl_sync(0xffffffffu, inc, 31);
-#pragma unroll
-            for (int c = 0; c + 1 < kCols; ++c) {
-              vt[c] = vt[c + 1];
-              vd[c] = vd[c + 1];
-            }
           }
           last_pos = __reduce_max_sync(0xffffffffu, last_pos);
           if (lane == 0) a.token[b] = first != 0x7fffffff ? first : last_pos;
