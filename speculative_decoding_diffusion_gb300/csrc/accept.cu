@@ -57,13 +57,13 @@ constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kStages = 6;
 constexpr int kStageBytes = 32768;                 // at most one piece of one row slice
 constexpr int kVecs = kStageBytes / 16 / kGroupThreads;   // 16-byte vectors per thread per piece
-constexpr int kWarpVecs = 32 * kVecs;              // 16-byte vectors per warp per piece
-constexpr int kRanges = 2 * kGroupWarps;           // vocabulary ranges per piece (residual sums)
-constexpr int kRangeVecs = kWarpVecs / 2;
+constexpr int kRanges = kConsumerWarps;           // vocabulary ranges per piece (residual sums)
+constexpr int kRangeVecs = kStageBytes / 16 / kRanges;
 constexpr int kMaxPieces = 32;                     // pieces per row slice
 static_assert(kMaxPieces <= 32 && kRanges <= 32 && kMaxCluster <= 32,
               "the draw picks pieces, ranges and slices one per lane");
 static_assert(kVecs % 2 == 0 && kRangeVecs % 32 == 0, "a range is whole vectors per lane");
+static_assert(kRanges * kRangeVecs * 16 == kStageBytes, "the ranges tile a stage");
 static_assert(2 * kMaxB * kMaxCluster <= kConsumers && 32 % kMaxCluster == 0,
               "one consumer thread per (pair, slice)");
 static_assert(kVecs * 8 % 8 == 0 && (kVecs / 2) * 4 % 8 == 0, "accumulator slots repeat every half");
@@ -371,15 +371,21 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         if (++pc == npieces) { pc = 0; ++pair; }
       }
     } else {
-      // The two consumer groups (warps 0-7, 8-15) take alternate pieces, so
-      // one group's barrier wait, loads and merges overlap the other's
+      // The two consumer groups (warps 0-7, 8-15) take alternate chunks of
+      // stages -- whole (slot, row) pairs when a slice is at most two
+      // pieces (one warp merge per pair), else single pieces -- so one
+      // group's barrier waits, loads and merges overlap the other's
       // exponentials instead of all warps moving in step.
       const int grp = warp / kGroupWarps, gtid = t % kGroupThreads;
-      if (lane == 0)                         // pairs this warp sees no piece of
+      const int v0 = (warp % kGroupWarps) * 32;
+      const int chunk = npieces == 2 ? 2 : 1;
+      if (lane == 0)                         // pairs this warp may see no piece of
         for (int q = 0; q < 2 * B; ++q) S.part_w[q][warp] = make_float2(-INFINITY, 0.f);
       float R = -INFINITY, sum = 0.f;
-      for (int gg = grp; gg < J; gg += 2) {
-        const int pair = gg / npieces, pc = gg - pair * npieces;
+      int gg = grp * chunk, pair = 0, pc = gg;
+      if (npieces > 0)
+        while (pc >= npieces) { pc -= npieces; ++pair; }
+      while (gg < J) {
         const int s = gg % kStages;
         const int n = piece_len(pc);
         if (!mbar_wait_warp(smem_u32(&S.full[s]), (gg / kStages) & 1)) {
@@ -395,11 +401,10 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         }
         // the logit at the slot's draft token, if this piece holds it
         if (gtid == 0) {
-          const int k = pair >> 1, row = pair & 1;
-          const int off = S.x[k] - (s0 + pc * a.piece);
+          const int off = S.x[pair >> 1] - (s0 + pc * a.piece);
           if (off >= 0 && off < n) {
             const float v = pick<T>(sv[off / N], off % N);
-            if (row) S.xv[k].y = v; else S.xv[k].x = v;
+            if (pair & 1) S.xv[pair >> 1].y = v; else S.xv[pair >> 1].x = v;
           }
         }
         __syncwarp();
@@ -416,7 +421,6 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           // rolled halves of four vectors (the code stays small: it is
           // often fetched cold, after other kernels ran).
           const int nvec = (n + N - 1) / N;
-          const int v0 = (warp % kGroupWarps) * 32;
           float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
           for (int h = 0; h < 2; ++h) {
@@ -433,15 +437,23 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           }
           sum += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         }
-        if (gg + 2 >= (pair + 1) * npieces) {   // the group's last piece of the pair: warp merge
-          // to the warp's largest reference: one rescale per lane, one sum
-          float Rm = R;
-#pragma unroll
-          for (int m = 16; m > 0; m >>= 1) Rm = fmaxf(Rm, __shfl_xor_sync(0xffffffffu, Rm, m));
+        // this group's next stage
+        const int gn = (gg + 1) % chunk != 0 ? gg + 1 : gg + chunk + 1;
+        const int pair_now = pair;
+        pc += gn - gg;
+        while (pc >= npieces) { pc -= npieces; ++pair; }
+        gg = gn;
+        if (pair != pair_now || gg >= J) {
+          // the group's part of the pair is done: warp merge to the warp's
+          // largest reference (an order-preserving integer maximum), one
+          // rescale per lane, one sum
+          const uint32_t ru = __float_as_uint(R);
+          const uint32_t km = __reduce_max_sync(0xffffffffu, (ru & 0x80000000u) ? ~ru : (ru | 0x80000000u));
+          const float Rm = __uint_as_float((km & 0x80000000u) ? (km & 0x7fffffffu) : ~km);
           float sc = Rm == -INFINITY ? 0.f : sum * ex2(R - Rm);
 #pragma unroll
           for (int m = 16; m > 0; m >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, m);
-          if (lane == 0) S.part_w[pair][warp] = make_float2(Rm, sc);
+          if (lane == 0) S.part_w[pair_now][warp] = make_float2(Rm, sc);
           R = -INFINITY;
           sum = 0.f;
         }
@@ -542,12 +554,10 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           issued = g + 1;
         }
       } else {
-        // the groups take alternate pieces; warp w of a group reads the
-        // contiguous vectors [w * kWarpVecs, (w + 1) * kWarpVecs) of the
-        // piece (lane-interleaved) and sums its two halves apart: the masses
-        // of two vocabulary ranges, which the draw narrows down to
-        const int gwarp = warp % kGroupWarps;
-        for (int pc = warp / kGroupWarps; pc < npieces && !*(volatile int *)&S.flag; pc += 2) {
+        // every warp takes part in every piece: warp w reads range w, the
+        // contiguous vectors [w * kRangeVecs, (w + 1) * kRangeVecs) of the
+        // piece (lane-interleaved), whose masses the draw narrows down to
+        for (int pc = 0; pc < npieces && !*(volatile int *)&S.flag; ++pc) {
           const int gt = J + 2 * pc, gd = gt + 1;
           const int st = gt % kStages, sd = gd % kStages;
           const int n = piece_len(pc);
@@ -559,15 +569,12 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const uint4 *tv = reinterpret_cast<const uint4 *>(smem + st * kStageBytes);
           const uint4 *dv = reinterpret_cast<const uint4 *>(smem + sd * kStageBytes);
           const int nvec = (n + N - 1) / N;
-#pragma unroll 1
-          for (int h = 0; h < 2; ++h) {          // the two ranges
-            float rs[4] = {0.f, 0.f, 0.f, 0.f}, ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-            for (int i = 0; i < kVecs / 2; ++i) {   // rolled: this code runs cold
-              const int col = gwarp * kWarpVecs + (h * kVecs / 2 + i) * 32;
-              if (col >= nvec) break;               // only -inf beyond
-              const int idx = col + lane;
-              const bool in = idx * N < n;
+          float rs[4] = {0.f, 0.f, 0.f, 0.f}, ps[4] = {0.f, 0.f, 0.f, 0.f};
+          if (warp * kRangeVecs < nvec) {
+#pragma unroll
+            for (int i = 0; i < kRangeVecs / 32; ++i) {
+              const int idx = warp * kRangeVecs + i * 32 + lane;
+              const bool in = idx < nvec;
               float ft[N], fd[N];
               Ld<T>::unpack(in ? tv[idx] : Ld<T>::neg_inf(), ft);
               Ld<T>::unpack(in ? dv[idx] : Ld<T>::neg_inf(), fd);
@@ -579,20 +586,20 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
                 ps[e & 3] += p;
               }
             }
-            Ff fr = ff_add(ff_of(rs[0] + rs[1]), ff_of(rs[2] + rs[3]));
-            Ff fp = ff_add(ff_of(ps[0] + ps[1]), ff_of(ps[2] + ps[3]));
-#pragma unroll 1
-            for (int m = 16; m > 0; m >>= 1) {
-              fr = ff_add(fr, ff_shfl_xor(fr, m));
-              fp = ff_add(fp, ff_shfl_xor(fp, m));
-            }
-            if (lane == 0) S.piece_w[pc][2 * gwarp + h] = make_float4(fr.hi, fr.lo, fp.hi, fp.lo);
           }
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive_n(smem_u32(&S.empty[st]), 2);
-            mbar_arrive_n(smem_u32(&S.empty[sd]), 2);
+            mbar_arrive(smem_u32(&S.empty[st]));
+            mbar_arrive(smem_u32(&S.empty[sd]));
           }
+          Ff fr = ff_add(ff_of(rs[0] + rs[1]), ff_of(rs[2] + rs[3]));
+          Ff fp = ff_add(ff_of(ps[0] + ps[1]), ff_of(ps[2] + ps[3]));
+#pragma unroll 1
+          for (int m = 16; m > 0; m >>= 1) {
+            fr = ff_add(fr, ff_shfl_xor(fr, m));
+            fp = ff_add(fp, ff_shfl_xor(fp, m));
+          }
+          if (lane == 0) S.piece_w[pc][warp] = make_float4(fr.hi, fr.lo, fp.hi, fp.lo);
         }
         consumers_sync();
         if (warp == 0) {                     // lane i: piece i (npieces <= 32)
