@@ -200,10 +200,11 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  *   accept iff u[t-1] * q(x) < p(x);
  *   at the first rejection draw a token from max(0, p - q) normalised (p
  *   itself if that is empty) by inverse CDF with u[B_b], and stop.
- * Kernel: K4, one thread-block cluster of 8 CTAs per sequence, each CTA
- * owning an eighth of the vocabulary: max and sum of exponentials of both
- * rows of every slot, the walk of the steps, and at a rejection the
- * residual masses and the inverse-CDF draw -- all on chip.
+ * Kernel: K4, one thread-block cluster of C CTAs per sequence (C <= 16,
+ * chosen at launch from the batch size and the clusters the device can
+ * hold at once), each CTA owning 1/C of the vocabulary: max and sum of
+ * exponentials of both rows of every slot, the walk of the steps, and at a
+ * rejection the residual masses and the inverse-CDF draw -- all on chip.
  *   target_logits, draft_logits device [total_B][vocab] (dtype); row k of
  *                sequence b (at cu_B[b]+k) holds the logits read at D~_k
  *   draft_tokens device int32[total_B] in [0, vocab); a token outside

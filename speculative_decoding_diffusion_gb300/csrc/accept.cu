@@ -8,8 +8,8 @@
 // first rejection a token is drawn from max(0, p - q) normalised (p itself
 // when that is empty) by inverse CDF with u[B].
 //
-// One launch; one thread-block cluster of C CTAs per sequence (C <= 8, from
-// a makespan estimate over the resident-cluster waves: 6-8 for small
+// One launch; one thread-block cluster of C CTAs per sequence (C <= 16, from
+// a makespan estimate over the resident-cluster waves: 8-16 for small
 // batches, 1-2 for large ones), CTA r owning the vocabulary slice
 // [r * per, (r + 1) * per) of every row of the sequence.  Each CTA streams
 // its slices of the 2B rows (target and draft of every slot) in pieces of
@@ -48,7 +48,7 @@
 namespace simsd {
 namespace {
 
-constexpr int kMaxCluster = 8;                     // CTAs per sequence, at most
+constexpr int kMaxCluster = 16;                    // CTAs per sequence, at most (over 8: non-portable)
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;          // + the producer warp
@@ -64,8 +64,8 @@ static_assert(kMaxPieces <= 32 && kRanges <= 32 && kMaxCluster <= 32,
               "the draw picks pieces, ranges and slices one per lane");
 static_assert(kVecs % 2 == 0 && kRangeVecs % 32 == 0, "a range is whole vectors per lane");
 static_assert(kRanges * kRangeVecs * 16 == kStageBytes, "the ranges tile a stage");
-static_assert(2 * kMaxB * kMaxCluster <= kConsumers && 32 % kMaxCluster == 0,
-              "one consumer thread per (pair, slice)");
+static_assert(kConsumers % kMaxCluster == 0 && 32 % kMaxCluster == 0,
+              "whole groups of consumer threads per pair");
 static_assert(kVecs * 8 % 8 == 0 && (kVecs / 2) * 4 % 8 == 0, "accumulator slots repeat every half");
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
 constexpr int kMaxVocab = 1 << 21;                 // kMaxCluster * kMaxPieces * 8192 fp32 entries
@@ -483,21 +483,24 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     // same inputs in the same order give the same decisions everywhere), so
     // no barrier is needed before the residual pass; CTA 0 writes outputs
     if (!producer) {
-      // thread (pair q, slice r) reads one slice's partial; 8-lane groups
-      // merge them (pair q: slot q / 2, row q % 2)
-      if (warp * 32 < 2 * B * kMaxCluster) {  // whole warps: the shuffles need every lane
-        const int q = t / kMaxCluster, r = t % kMaxCluster;
+      // thread (pair q, slice r) reads one slice's partial; groups of gs
+      // lanes (8, or 16 for clusters over 8) merge them (pair q: slot q / 2,
+      // row q % 2)
+      const int lg = a.csize > 8 ? 4 : 3, gs = 1 << lg;
+      for (int q0 = 0; q0 < 2 * B; q0 += kConsumers >> lg) {
+      if (warp * 32 < (2 * B - q0) << lg) {  // whole warps: the shuffles need every lane
+        const int q = q0 + (t >> lg), r = t & (gs - 1);
         const bool mine = q < 2 * B;
         const int k = q >> 1, row = q & 1, x = mine ? S.x[k] : -1;
         const bool xin = x >= 0 && x < a.vocab;
         const float2 xl = r == 0 && xin ? ld_dsmem2(dsmem(&S.xv[k], x / a.per)) : make_float2(0.f, 0.f);
         const float2 v = mine && r < a.csize ? ld_dsmem2(dsmem(&S.cpart[q], r)) : make_float2(-INFINITY, 0.f);
         float M = v.x;
-#pragma unroll
-        for (int m = kMaxCluster / 2; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+#pragma unroll 1
+        for (int m = gs / 2; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
         Ff sm = ff_of(M != -INFINITY && v.y > 0.f ? v.y * ex2(v.x - M) : 0.f);
 #pragma unroll 1
-        for (int m = kMaxCluster / 2; m > 0; m >>= 1) sm = ff_add(sm, ff_shfl_xor(sm, m));
+        for (int m = gs / 2; m > 0; m >>= 1) sm = ff_add(sm, ff_shfl_xor(sm, m));
         if (mine && r == 0) {
           S.norm[q] = make_float2(M, sm.hi + sm.lo);
           // p(x) (row 0) or q(x) (row 1); a token no slice holds rejects
@@ -505,6 +508,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           if (row) S.qx[k] = pr; else S.px[k] = pr;
           if (!xin && row == 0 && rank == 0) raise_status(a.status, kStatusBadInput);
         }
+      }
       }
       consumers_sync();
       if (t == 0) {
@@ -753,8 +757,9 @@ cudaLaunchConfig_t launch_config(int csize, int batch, cudaStream_t stream,
   return cfg;
 }
 
-// Per device and cluster size 1..8: clusters of this kernel resident at
-// once (queried once; the answer depends on the device only).
+// Per device and cluster size 1..kMaxCluster: clusters of this kernel
+// resident at once (queried once; the answer depends on the device only;
+// -1 for a size the device cannot place).
 template <typename T>
 cudaError_t max_active_clusters(int dev, int csize, int *out) {
   static std::mutex mu;
@@ -765,6 +770,10 @@ cudaError_t max_active_clusters(int dev, int csize, int *out) {
     cudaError_t e = cudaFuncSetAttribute(accept_kernel<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
+    // sizes over 8 are optional: without the attribute they are skipped
+    if (cudaFuncSetAttribute(accept_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
+      (void)cudaGetLastError();
     cache[dev][0] = 1;
   }
   if (cache[dev][csize] == 0) {
@@ -772,7 +781,11 @@ cudaError_t max_active_clusters(int dev, int csize, int *out) {
     const cudaLaunchConfig_t cfg = launch_config(csize, csize, nullptr, attr);
     int n = 0;
     cudaError_t e = cudaOccupancyMaxActiveClusters(&n, accept_kernel<T>, &cfg);
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess) {
+      if (csize <= 8) return e;
+      (void)cudaGetLastError();              // a non-portable size this device refuses
+      n = 0;
+    }
     cache[dev][csize] = n > 0 ? n : -1;
   }
   *out = cache[dev][csize];
