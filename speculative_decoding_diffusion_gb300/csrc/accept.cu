@@ -68,7 +68,7 @@ static_assert(kConsumers % kMaxCluster == 0 && 32 % kMaxCluster == 0,
               "whole groups of consumer threads per pair");
 static_assert(kVecs * 8 % 8 == 0 && (kVecs / 2) * 4 % 8 == 0, "accumulator slots repeat every half");
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
-constexpr int kMaxVocab = 1 << 21;                 // kMaxCluster * kMaxPieces * 8192 fp32 entries
+constexpr int kMaxVocab = 1 << 21;                 // 8 slices of kMaxPieces pieces of 8192 fp32 entries
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------ two-sum pairs
