@@ -54,6 +54,18 @@ def test_odd_vocab_and_mixed_B(dtype, vocab):
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
 
 
+@pytest.mark.parametrize("dtype,vocab,batch,B", [("bf16", 151936, 2, 32), ("bf16", 65539, 3, 32),
+                                                 ("f32", 100003, 4, 17), ("bf16", 151936, 5, 1)])
+def test_few_sequences_large_clusters(dtype, vocab, batch, B):
+    """Few sequences get the largest clusters (up to 16 CTAs each): slices
+    of 1/16 of the vocabulary, the slice merge in 16-lane groups and, at
+    B = 32, in two rounds of pairs; element copies where rows are not
+    16-byte multiples."""
+    w = synth.make(tiny_accept_spec(batch=batch, B=B, dtype=dtype, vocab=vocab), seed=vocab + B)
+    n, tok, pos = run_accept(w)
+    parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
+
+
 def test_p_equals_q_accepts_everything():
     w = synth.make(tiny_accept_spec(), seed=1)
     w.draft = w.target.copy()
