@@ -58,8 +58,8 @@ constexpr uint32_t kColS = 0;        // two score / probability tiles: columns 0
 constexpr uint32_t kColO = 2 * kKeys;
 
 enum { kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarSFull = kBarKvEmpty + kStages,
-       kBarPFull = kBarSFull + 2, kBarPvDone = kBarPFull + 2, kBarMx = kBarPvDone + 2,
-       kBarQReady = kBarMx + 2, kNumBars = kBarQReady + 1 };
+       kBarPFull = kBarSFull + 2, kBarPvDone = kBarPFull + 2,
+       kBarQReady = kBarPvDone + 2, kNumBars = kBarQReady + 1 };
 
 template <int HD>
 struct TcSmem {
@@ -70,8 +70,7 @@ struct TcSmem {
   static constexpr int kOffKv = 0;
   static constexpr int kOffBar = kOffKv + kStages * kStage;
   static constexpr int kOffTau = kOffBar + kNumBars * 8;
-  static constexpr int kOffMx = kOffTau + 2 * kMaxB * 4;     // [2][4][32] block maxima
-  static constexpr int kOffCs = kOffMx + 2 * 4 * 32 * 4;    // [kMaxB][HD/2] (cos, sin)
+  static constexpr int kOffCs = kOffTau + 2 * kMaxB * 4;     // [kMaxB][HD/2] (cos, sin)
   static constexpr int kOffMisc = kOffCs + kMaxB * (HD / 2) * 8;  // tmem address, error flag
   static constexpr int kBytes = kOffMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;              // 1024-byte alignment slack
@@ -181,7 +180,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       mbar_init(bar(kBarSFull + i), 1);
       mbar_init(bar(kBarPFull + i), n_valid);
       mbar_init(bar(kBarPvDone + i), 1);
-      mbar_init(bar(kBarMx + i), 4);
     }
     mbar_init(bar(kBarQReady), 4);
     *flag_s = 0;
@@ -400,16 +398,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           }
           mx = fmaxf(mx, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
         }
-        if (RC > 1) {
-          // the block maximum over the copies of this row (bounded exchange)
-          float *mx_s = reinterpret_cast<float *>(sb + L::kOffMx) + (tb * 4) * 32;
-          mx_s[q4 * 32 + lane] = mx;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kBarMx + tb));
-          if (!mbar_wait_warp(bar(kBarMx + tb), (j >> 1) & 1)) { ok = false; break; }
-#pragma unroll
-          for (int c = 0; c < RC; ++c) mx = fmaxf(mx, mx_s[(c * (4 / RC) + g) * 32 + lane]);
-        }
+        // (each copy of a replicated row keeps its own reference; the
+        // epilogue merges the copies' (O, l, m) like splits)
         mx *= scale;                         // scale > 0
         // reference maximum: moves only when this block's max outgrows it
         const bool move = row_valid && mx > m_ref + kHeadroom;
@@ -500,8 +490,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const bool failed = *(volatile int *)flag_s != 0;
     const long orow = (2L * c0 + tok) * a.Hq + kvh * a.G + (row_valid ? grow % a.G : 0);
     // writes columns [c0c, c0c + n) of this thread's row from v (O sums,
-    // unnormalised) with sum lt
-    auto write_cols = [&](const float *v, int c0c, int n, float lt) {
+    // unnormalised, relative to reference mr) with sum lt
+    auto write_cols = [&](const float *v, int c0c, int n, float lt, float mr) {
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       if (n_splits_b == 1) {
         uint4 *dst = reinterpret_cast<uint4 *>((__nv_bfloat16 *)a.out + orow * HD + c0c);
@@ -515,7 +505,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         float4 *dst = reinterpret_cast<float4 *>(a.o_part + prow * HD + c0c);
         for (int e = 0; e < n / 4; ++e)
           dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-        if (c0c == 0) a.ml_part[prow] = make_float2(m_ref, lt);   // O, l relative to m_ref
+        if (c0c == 0) a.ml_part[prow] = make_float2(mr, lt);   // O, l relative to mr
       }
     };
     if (R == 1) {
@@ -526,12 +516,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           tc::ld32(tO + 32 * c, o);
           tc::wait_ld();
           if (!row_valid || failed) continue;
-          write_cols(reinterpret_cast<const float *>(o), 32 * c, 32, l);
+          write_cols(reinterpret_cast<const float *>(o), 32 * c, 32, l, m_ref);
         }
       }
     } else {
-      // every copy puts its partial output and sum in the (now idle) K/V
-      // ring; then copy kp adds the R partials of columns [kp * HD/R, ..)
+      // every copy puts its partial output, sum and reference in the (now
+      // idle) K/V ring; then copy kp merges the R partials of columns
+      // [kp * HD/R, ..) to the largest reference
       float *part = reinterpret_cast<float *>(sb + L::kOffKv);   // [R][groups][32][HD + 4]
       float *mine = part + ((kp * groups + g) * 32 + lane) * (HD + 4);
 #pragma unroll 1
@@ -546,11 +537,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                           __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
       }
       mine[HD] = l;
+      mine[HD + 1] = m_ref;
       named_sync(1, kSoftmax);
       if (row_valid && !failed) {
         const int cw = HD / R, cb = kp * cw;    // 16, 32 or 64 columns
-        float lt = 0.f;
-        for (int c = 0; c < R; ++c) lt += part[((c * groups + g) * 32 + lane) * (HD + 4) + HD];
+        float mt = -INFINITY;
+        for (int c = 0; c < R; ++c) mt = fmaxf(mt, part[((c * groups + g) * 32 + lane) * (HD + 4) + HD + 1]);
+        float wc[4], lt = 0.f;
+        for (int c = 0; c < R; ++c) {
+          const float *pc = part + ((c * groups + g) * 32 + lane) * (HD + 4);
+          wc[c] = mt == -INFINITY ? 0.f : ex2(pc[HD + 1] - mt);   // -inf reference -> 0
+          lt += wc[c] * pc[HD];
+        }
         for (int q = 0; q < cw; q += 32) {
           const int n = min(32, cw - q);        // a multiple of 16
           float v[32];
@@ -562,10 +560,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             for (int e = 0; e < 8; ++e) {
               if (4 * e >= n) break;
               const float4 p4 = *reinterpret_cast<const float4 *>(src + 4 * e);
-              v[4 * e] += p4.x; v[4 * e + 1] += p4.y; v[4 * e + 2] += p4.z; v[4 * e + 3] += p4.w;
+              v[4 * e] += wc[c] * p4.x; v[4 * e + 1] += wc[c] * p4.y;
+              v[4 * e + 2] += wc[c] * p4.z; v[4 * e + 3] += wc[c] * p4.w;
             }
           }
-          write_cols(v, cb + q, n, lt);
+          write_cols(v, cb + q, n, lt, mt);
         }
       }
     }
