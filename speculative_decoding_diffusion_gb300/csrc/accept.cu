@@ -342,15 +342,16 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     S.flag = 0;
     fence_barrier_init();
   }
-  if (valid) {
+  __syncthreads();                           // the ring's barriers are ready
+  if (valid && !producer) {                  // (the producer starts streaming meanwhile)
     if (t < B) {
       S.tau[t] = __ldg(a.tau + c0 + t);
       S.x[t] = __ldg(a.draft_tokens + c0 + t);
       S.xv[t] = make_float2(0.f, 0.f);
     }
     if (t <= B) S.u[t] = __ldg(a.uniforms + (long)b * (a.B_max + 1) + t);
+    consumers_sync();                        // the sequence's labels, tokens, uniforms
   }
-  __syncthreads();
 
   int issued = 0;                            // producer: stages started so far
   int g = 0;                                 // stage counter (producer and consumers)
