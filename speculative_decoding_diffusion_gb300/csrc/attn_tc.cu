@@ -113,6 +113,15 @@ __device__ __forceinline__ bool visible_new(int jj, int B, const int *tau_s, boo
   return row_slot ? (key_slot ? tj >= ti : tj < ti) : (!key_slot && tj <= ti);
 }
 
+// bits [0, n) set (n clamped to 0..64)
+__device__ __forceinline__ uint64_t low_bits(int n) {
+  return n <= 0 ? 0ull : n >= 64 ? ~0ull : (1ull << n) - 1ull;
+}
+// x >> s for any s (negative: shift left); shifts of 64 or more give 0
+__device__ __forceinline__ uint64_t shift_bits(uint64_t x, int s) {
+  return s >= 64 || s <= -64 ? 0ull : s >= 0 ? x >> s : x << (-s);
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -345,6 +354,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(kBarQReady));
     const int row_tau = tau_s[tok];
+    // this row's visibility of the 2B new keys (bit jj: new key jj), built
+    // while the first K/V stage is still in flight
+    uint64_t newvis = 0;
+#pragma unroll 8
+    for (int jj = 0; jj < 2 * B; ++jj)
+      if (visible_new(jj, B, tau_s, row_slot, row_tau)) newvis |= 1ull << jj;
     const uint32_t tO = trow + kColO;
     const float scale = a.sm_scale * kLog2e;
     float m_ref = -INFINITY, l = 0.f;
@@ -368,15 +383,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 #pragma unroll
         for (int h = 0; h < (KW + 63) / 64; ++h) vis[h] = ~0ull;
         if (kb + k_lo + KW > min(P, k_end)) {
-          for (int c = max(0, min(P, k_end) - kb - k_lo); c < KW; ++c) {
-            const int key = kb + k_lo + c;
-            const bool v = key < k_end && (key < P || visible_new(key - P, B, tau_s, row_slot, row_tau));
-            if (!v) {
+          // prompt keys below the split's end, and new keys per newvis
+          const int first_new = P - kb - k_lo, kend = k_end - kb - k_lo;
 #pragma unroll
-              for (int h = 0; h < (KW + 63) / 64; ++h)
-                if ((c >> 6) == h) vis[h] &= ~(1ull << (c & 63));
-            }
-          }
+          for (int h = 0; h < (KW + 63) / 64; ++h)
+            vis[h] = (low_bits(first_new - 64 * h) | shift_bits(newvis, 64 * h - first_new)) &
+                     low_bits(kend - 64 * h);
         }
         // pass 1: the maximum of the raw scores over this warp's keys, 64
         // columns per TMEM round trip (the loop stays rolled: an unrolled
