@@ -160,9 +160,10 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- ncu traffic record
-def recorded_traffic():
+def recorded_traffic(workload):
     """DRAM bytes per K2 launch from the committed ncu summary, valid only
-    while the kernel source is unchanged (hash recorded with the counters)."""
+    for the workload it was captured on and while the kernel source is
+    unchanged (hash recorded with the counters)."""
     src = os.path.join(ROOT, "speculative_decoding_diffusion_gb300", "csrc", "attn_tc.cu")
     rec = os.path.join(ROOT, "profiles", "k2_traffic.json")
     if not os.path.exists(rec):
@@ -170,7 +171,7 @@ def recorded_traffic():
     try:
         d = json.load(open(rec))
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if d.get("source_sha256") == h and d.get("workload") == "sdar8b-verify":
+        if d.get("source_sha256") == h and d.get("workload") == workload:
             return float(d["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -413,7 +414,7 @@ def main():
     peak, peak_kind = hbm_peak()
     k2_mean = float(np.mean(k_ms["K2"]))
     achieved = k2_bytes(w) / (k2_mean / 1e3) / 1e9
-    traffic = recorded_traffic()
+    traffic = recorded_traffic(w.spec.name)
     n_launch = 4 if any(t > 0.0005 for t in k_ms["K3"]) else 3
     kernels = {n: {"ms": float(np.mean(t))} for n, t in k_ms.items()}
     attn_ms = sum(kernels[n]["ms"] for n in ("K1", "K2", "K3"))
