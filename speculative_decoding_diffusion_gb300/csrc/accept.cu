@@ -798,10 +798,11 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
   const int dev = current_device();
   // Cluster size by a makespan estimate: clusters run in waves of the
   // resident count; a CTA's time is its share of the sequence's exponentials
-  // (16 per clock per SM: the MUFU rate) plus the fixed cost of the walk,
-  // residual and draw phases.  Small batches get large clusters (every SM
-  // busy), large batches small ones (fewer waves).  Never so small that a
-  // slice needs more pieces than the kernel tracks.
+  // at 16 per clock per SM (a round figure: the MUFU alone sustains ~24, the
+  // whole streaming loop fewer) plus the fixed cost of the walk, residual
+  // and draw phases.  Small batches get large clusters (every SM busy),
+  // large batches small ones (fewer waves).  Never so small that a slice
+  // needs more pieces than the kernel tracks.
   const int piece = kStageBytes / (int)sizeof(T), vec = 16 / (int)sizeof(T);
   const int64_t max_slice = (int64_t)kMaxPieces * piece;
   const double per_seq = (2.0 * a.total_B / a.batch + 2.0) * a.vocab;   // exponentials
