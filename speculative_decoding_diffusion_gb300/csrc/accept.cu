@@ -112,6 +112,15 @@ __device__ __forceinline__ float ex2(float x) {
 // 2^(x log2 e - R): the argument rounded once.
 __device__ __forceinline__ float rel_exp(float x, float R) { return ex2(fmaf(x, kLog2e, -R)); }
 
+// p(v) = 2^(x log2 e - M) / S with the reciprocal normaliser, and the
+// residual max(0, p - q): separately rounded (no fused multiply-subtract),
+// so identical target and draft rows give p == q and an exactly empty
+// residual, and the residual pass and the draw compute the same values.
+__device__ __forceinline__ float prob(float x, float M, float inv_s) {
+  return __fmul_rn(rel_exp(x, M), inv_s);
+}
+__device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsub_rn(p, q), 0.f); }
+
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -585,9 +594,9 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
               Ld<T>::unpack(in ? dv[idx] : Ld<T>::neg_inf(), fd);
 #pragma unroll
               for (int e = 0; e < N; ++e) {
-                const float p = rel_exp(ft[e], w.Mt) * w.inv_st;
-                const float q = rel_exp(fd[e], w.Md) * w.inv_sd;
-                rs[e & 3] += fmaxf(p - q, 0.f);
+                const float p = prob(ft[e], w.Mt, w.inv_st);
+                const float q = prob(fd[e], w.Md, w.inv_sd);
+                rs[e & 3] += residual(p, q);
                 ps[e & 3] += p;
               }
             }
@@ -685,9 +694,9 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
             float ls = 0.f;
 #pragma unroll
             for (int e = 0; e < N; ++e) {
-              const float p = rel_exp(ft[e], w.Mt) * w.inv_st;
-              const float q = rel_exp(fd[e], w.Md) * w.inv_sd;
-              m[e] = use_p ? p : fmaxf(p - q, 0.f);
+              const float p = prob(ft[e], w.Mt, w.inv_st);
+              const float q = prob(fd[e], w.Md, w.inv_sd);
+              m[e] = use_p ? p : residual(p, q);
               ls += m[e];
               if (m[e] > 0.f) last_pos = vbase + e;
             }

@@ -13,6 +13,7 @@ import torch
 
 import parity
 import synth
+import oracle
 from oracle import exact
 from speculative_decoding_diffusion_gb300 import binding
 from speculative_decoding_diffusion_gb300.staging import DeviceWorkload
@@ -64,6 +65,42 @@ def test_few_sequences_large_clusters(dtype, vocab, batch, B):
     w = synth.make(tiny_accept_spec(batch=batch, B=B, dtype=dtype, vocab=vocab), seed=vocab + B)
     n, tok, pos = run_accept(w)
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
+
+
+def test_invalid_token_rejects_and_empty_residual_draws_from_p():
+    """A draft token outside the vocabulary rejects its step and sets the
+    status word's bad-input bit; with identical target and draft rows the
+    residual max(0, p - q) is empty, so the token is drawn from p itself
+    (the fallback the pages' rule needs when p <= q everywhere)."""
+    w = synth.make(tiny_accept_spec(batch=8, B=3, vocab=5000), seed=11)
+    w.draft = w.target.copy()
+    V, B = w.spec.vocab, 3
+    first = []
+    for b in range(len(w.lens)):
+        s0 = int(w.cu_B[b])
+        k = int(np.nonzero(w.tau[s0:s0 + B] == 1)[0][0])   # the slot tested first
+        w.draft_tokens[s0 + k] = -1 if b % 2 else V
+        first.append(k)
+    dw = DeviceWorkload(w, with_verify=False)
+    dw.accept()
+    torch.cuda.synchronize()
+    assert binding.read_status(dw.accept_ws) == 2             # the bad-input bit
+    n, tok, pos = dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy()
+    for b, k in enumerate(first):
+        assert n[b] == 0 and pos[b] == k
+        s0 = int(w.cu_B[b])
+        r, S = oracle.residual(synth.to_f64(w.target[s0 + k]), synth.to_f64(w.draft[s0 + k]))
+        C = np.cumsum(r)                  # r = p: the residual is empty
+        U = float(w.uniforms[b, B]) * S
+        v = int(np.searchsorted(C, U, side="right"))
+        lo = C[v - 1] if v > 0 else 0.0
+        if v < V and min(U - lo, C[v] - U) >= parity.TIE_RESIDUAL:
+            assert tok[b] == v, (b, tok[b], v)
+        else:
+            g = int(tok[b])
+            assert 0 <= g < V and r[g] > 0
+            glo = C[g - 1] if g > 0 else 0.0
+            assert glo - parity.TIE_RESIDUAL <= U < C[g] + parity.TIE_RESIDUAL
 
 
 def test_p_equals_q_accepts_everything():
