@@ -3,8 +3,9 @@
 // SimSD section 2 "Temporal Attention Mask" and section 4 (one verification
 // forward): every new row attends to the whole prompt; a slot row D~_i also
 // to D_j with tau(j) < tau(i) and to D~_j with tau(j) >= tau(i); a data row
-// D_i (convention) to D_j with tau(j) <= tau(i).  The mask is evaluated on
-// the fly, only on blocks that reach the 2B new keys.
+// D_i (convention) to D_j with tau(j) <= tau(i).  Each softmax thread
+// builds its row's visibility of the 2B new keys once, as a bitmask; only
+// blocks that reach the new keys (or the split's end) apply it.
 //
 // One CTA per (key split, KV head x 128-row tile, sequence).  The query tile
 // stacks the 2B tokens x G query heads of one KV head (row = token*G + head
@@ -304,9 +305,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // With at most 64 real rows the tile's rows are replicated across the
     // four TMEM lane quadrants (R = 4 or 2 copies) and the copies split each
     // block's keys: every quadrant's warp handles 128/R keys of the same
-    // rows, the warps agree on the block maximum through shared memory, and
-    // each writes P for its keys (zeros elsewhere), so the P.V MMA leaves R
-    // partial outputs per row that the epilogue adds up.
+    // rows with its own running reference, and writes P for its keys (zeros
+    // elsewhere), so the P.V MMA leaves R partial outputs per row that the
+    // epilogue merges to the largest reference.
     const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
     const int groups = 4 / R;                // 32-row groups held per copy
     const int g = q4 % groups, kp = q4 / groups;
