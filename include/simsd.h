@@ -196,10 +196,16 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * simsd_accept -- section 4, acceptance: standard rejection sampling along
  * the temporal order tau.  For sequence b and steps t = 1..B_b, slot
  * k = tau^-1(t) with draft token x = draft_tokens[k]:
- *   p = softmax(target row k), q = softmax(draft row k) (fp32 math);
+ *   p = softmax(target row k / T), q = softmax(draft row k / T) (fp32
+ *   math; T = temperature, 1 by default);
  *   accept iff u[t-1] * q(x) < p(x);
  *   at the first rejection draw a token from max(0, p - q) normalised (p
  *   itself if that is empty) by inverse CDF with u[B_b], and stop.
+ * Variant rule SIMSD_ACCEPT_GREEDY (the temperature -> 0 limit): step t
+ * accepts iff x is the target row's argmax (the smallest index among equal
+ * maxima); the first rejection emits that argmax.  It reads neither the
+ * draft logits nor the uniforms (they may be NULL), and runs a separate,
+ * lighter kernel (one pass over the target rows).
  * Kernel: K4, one thread-block cluster of C CTAs per sequence (C <= 16,
  * chosen at launch from the batch size and the clusters the device can
  * hold at once), each CTA owning 1/C of the vocabulary: max and sum of
@@ -222,9 +228,15 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * copies; other vocabularies take a slower element-wise copy.
  * Workspace: the status word only (simsd_accept_workspace_size returns 256
  * for every valid size).
- * Errors: SIMSD_ERR_NULL, SIMSD_ERR_SHAPE, SIMSD_ERR_DTYPE,
+ * Errors: SIMSD_ERR_NULL, SIMSD_ERR_SHAPE (also: an unknown rule, or a
+ * temperature that is negative or not finite), SIMSD_ERR_DTYPE,
  * SIMSD_ERR_WORKSPACE, SIMSD_ERR_CUDA.
  * ---------------------------------------------------------------------- */
+typedef enum {
+  SIMSD_ACCEPT_SAMPLE = 0,    /* rejection sampling at temperature T         */
+  SIMSD_ACCEPT_GREEDY = 1     /* accept iff x = argmax of the target row      */
+} simsd_accept_rule;
+
 typedef struct {
   int32_t batch;
   int32_t vocab;
@@ -242,6 +254,9 @@ typedef struct {
   int32_t *pos;
   void *workspace;            /* device, 256-byte aligned                   */
   size_t workspace_bytes;
+  simsd_accept_rule rule;     /* 0 (a zero-filled descriptor): sampling      */
+  float temperature;          /* > 0; 0 selects 1 (a zero-filled descriptor
+                                 keeps the standard rule)                    */
 } simsd_accept_desc;
 
 size_t simsd_accept_workspace_size(const simsd_accept_desc *d);

@@ -46,6 +46,7 @@ def _lib():
                                            P, P, P, I]
         lib.oracle_accept.argtypes = [I, I, P, P, P, P, P, P, I, P, P, P, P,
                                       P, I]
+        lib.oracle_accept_greedy.argtypes = [I, I, P, P, P, P, P, P, P]
         lib.oracle_residual.argtypes = [I, P, P, P]
         lib.oracle_residual.restype = D
         _LIB = lib
@@ -137,12 +138,16 @@ def verify_attn(lens, cu_B, q, k_prompt, v_prompt, k_new, v_new, tau,
     return out
 
 
-def accept(cu_B, target, draft, draft_tokens, tau, uniforms, n_threads=0):
+def accept(cu_B, target, draft, draft_tokens, tau, uniforms, n_threads=0, temperature=1.0):
     """Returns dict(n_accept, token, pos, accept_margin, resample_margin).
     target/draft [sum B, V] (any float dtype, taken exactly to fp64);
-    uniforms [batch, u_stride] float32."""
+    uniforms [batch, u_stride] float32.  temperature T: p = softmax(target / T),
+    q = softmax(draft / T) (the logits divided in fp64)."""
     cu_B = _c(cu_B, np.int32)
     target, draft = _c(target, np.float64), _c(draft, np.float64)
+    if temperature != 1.0:
+        target = np.ascontiguousarray(target / float(temperature))
+        draft = np.ascontiguousarray(draft / float(temperature))
     draft_tokens, tau = _c(draft_tokens, np.int32), _c(tau, np.int32)
     uniforms = _c(uniforms, np.float32)
     batch = len(cu_B) - 1
@@ -158,6 +163,21 @@ def accept(cu_B, target, draft, draft_tokens, tau, uniforms, n_threads=0):
         _p(am), _p(rm), int(n_threads)), "oracle_accept")
     return dict(n_accept=n_accept, token=token, pos=pos, accept_margin=am,
                 resample_margin=rm)
+
+
+def accept_greedy(cu_B, target, draft_tokens, tau):
+    """Greedy verification: dict(n_accept, token, pos); target [sum B, V]."""
+    cu_B = _c(cu_B, np.int32)
+    target = _c(target, np.float64)
+    draft_tokens, tau = _c(draft_tokens, np.int32), _c(tau, np.int32)
+    batch = len(cu_B) - 1
+    n_accept = np.zeros(batch, np.int32)
+    token = np.zeros(batch, np.int32)
+    pos = np.zeros(batch, np.int32)
+    _check(_lib().oracle_accept_greedy(
+        batch, target.shape[1], _p(cu_B), _p(target), _p(draft_tokens), _p(tau),
+        _p(n_accept), _p(token), _p(pos)), "oracle_accept_greedy")
+    return dict(n_accept=n_accept, token=token, pos=pos)
 
 
 def residual(target_row, draft_row):

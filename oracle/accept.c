@@ -141,3 +141,38 @@ int oracle_accept(int batch, int V, const int *cu_B, const double *target,
   }
   return rc;
 }
+
+/* Greedy verification (the acceptance variant with temperature -> 0): step t
+ * tests slot k = tau^-1(t) and accepts iff its draft token equals the
+ * target's most likely token a_k = argmax_v target_k(v) (the smallest index
+ * among equal maxima).  At the first rejection the token is a_k and the walk
+ * stops; no uniform is read and the draft logits play no part. */
+int oracle_accept_greedy(int batch, int V, const int *cu_B, const double *target,
+                         const int *draft_tokens, const int *tau,
+                         int *n_accept, int *token, int *pos) {
+  if (batch < 0 || V < 1 || !cu_B || !target || !draft_tokens || !tau || !n_accept ||
+      !token || !pos)
+    return ORACLE_ERR_ARG;
+  for (int b = 0; b < batch; ++b) {
+    const int s0 = cu_B[b], B = cu_B[b + 1] - s0;
+    if (B < 1) return ORACLE_ERR_ARG;
+    if (!oracle_tau_is_permutation(B, tau + s0)) return ORACLE_ERR_TAU;
+    n_accept[b] = B;
+    token[b] = -1;
+    pos[b] = -1;
+    for (int t = 1; t <= B; ++t) {
+      int k = 0;
+      while (tau[s0 + k] != t) ++k;
+      const double *row = target + (size_t)(s0 + k) * V;
+      int a = 0;
+      for (int v = 1; v < V; ++v)
+        if (row[v] > row[a]) a = v;
+      if (draft_tokens[s0 + k] == a) continue;
+      n_accept[b] = t - 1;
+      token[b] = a;
+      pos[b] = k;
+      break;
+    }
+  }
+  return ORACLE_OK;
+}

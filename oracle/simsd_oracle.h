@@ -118,6 +118,13 @@ int oracle_accept(int batch, int V, const int *cu_B, const double *target,
                   double *accept_margin, double *resample_margin,
                   int n_threads);
 
+/* Greedy verification: step t accepts iff its draft token is the target's
+ * argmax (smallest index among equal maxima); the first rejection emits that
+ * argmax.  Uniforms and draft logits are not used. */
+int oracle_accept_greedy(int batch, int V, const int *cu_B, const double *target,
+                         const int *draft_tokens, const int *tau,
+                         int *n_accept, int *token, int *pos);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,6 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsimsd.so")
 
 SIMSD_F32, SIMSD_BF16 = 0, 1
+SIMSD_ACCEPT_SAMPLE, SIMSD_ACCEPT_GREEDY = 0, 1
 STATUS = {0: "SIMSD_OK", 1: "SIMSD_ERR_NULL", 2: "SIMSD_ERR_SHAPE",
           3: "SIMSD_ERR_TAU", 4: "SIMSD_ERR_DTYPE", 5: "SIMSD_ERR_WORKSPACE",
           6: "SIMSD_ERR_CUDA", 7: "SIMSD_ERR_TIMEOUT", 8: "SIMSD_ERR_ALIGN"}
@@ -46,7 +47,7 @@ class AcceptDesc(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("target_logits", _vp), ("draft_logits", _vp),
                 ("draft_tokens", _vp), ("tau", _vp), ("cu_B", _vp), ("uniforms", _vp),
                 ("n_accept", _vp), ("token", _vp), ("pos", _vp), ("workspace", _vp),
-                ("workspace_bytes", _sz)]
+                ("workspace_bytes", _sz), ("rule", ctypes.c_int), ("temperature", ctypes.c_float)]
 
 
 class SimsdError(RuntimeError):
@@ -203,16 +204,19 @@ def prompt_append(k, v, start, cu_n, k_cache, v_cache, block_table, rope_base,
 
 
 def _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
-                 pos, total_B, B_max, workspace=None):
+                 pos, total_B, B_max, workspace=None, rule=SIMSD_ACCEPT_SAMPLE, temperature=1.0):
     d = AcceptDesc()
+    d.rule = int(rule)
+    d.temperature = float(temperature)
     d.batch = cu_B.shape[0] - 1
     d.vocab = target.shape[1]
     d.total_B = int(total_B)
     d.B_max = int(B_max)
     d.dtype = _dtype_code(target)
-    d.target_logits, d.draft_logits = _ptr(target), _ptr(draft)
+    d.target_logits = _ptr(target)
+    d.draft_logits = None if draft is None else _ptr(draft)
     d.draft_tokens, d.tau, d.cu_B = _ptr(draft_tokens), _ptr(tau), _ptr(cu_B)
-    d.uniforms = _ptr(uniforms)
+    d.uniforms = None if uniforms is None else _ptr(uniforms)
     d.n_accept, d.token, d.pos = _ptr(n_accept), _ptr(token), _ptr(pos)
     if workspace is not None:
         d.workspace = _ptr(workspace)
@@ -231,10 +235,12 @@ def accept_workspace_size(target, draft, draft_tokens, tau, cu_B, uniforms, n_ac
 
 
 def accept(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token, pos,
-           workspace, total_B, B_max, stream=None, events=None):
-    """simsd_accept; events: optional 3 recorded torch.cuda.Event objects."""
+           workspace, total_B, B_max, stream=None, events=None, rule=SIMSD_ACCEPT_SAMPLE,
+           temperature=1.0):
+    """simsd_accept; events: optional 3 recorded torch.cuda.Event objects;
+    rule SIMSD_ACCEPT_GREEDY takes draft = uniforms = None."""
     d = _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
-                     pos, total_B, B_max, workspace)
+                     pos, total_B, B_max, workspace, rule, temperature)
     if events is None:
         _check(lib().simsd_accept(ctypes.byref(d), _stream(stream)), "simsd_accept")
     else:
@@ -243,11 +249,11 @@ def accept(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token, po
 
 
 def accept_noalloc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
-                   pos, total_B, B_max, stream=None):
+                   pos, total_B, B_max, stream=None, rule=SIMSD_ACCEPT_SAMPLE, temperature=1.0):
     """simsd_accept_noalloc: acceptance with the library's static scratch, for
     callers that may not allocate device memory (no workspace argument)."""
     d = _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
-                     pos, total_B, B_max)
+                     pos, total_B, B_max, None, rule, temperature)
     _check(lib().simsd_accept_noalloc(ctypes.byref(d), _stream(stream)),
            "simsd_accept_noalloc")
 

@@ -110,14 +110,15 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // 2^(x log2 e - R): the argument rounded once.
-__device__ __forceinline__ float rel_exp(float x, float R) { return ex2(fmaf(x, kLog2e, -R)); }
+// (ls = log2(e) / temperature: the logits' scale into log2 units)
+__device__ __forceinline__ float rel_exp(float x, float R, float ls) { return ex2(fmaf(x, ls, -R)); }
 
 // p(v) = 2^(x log2 e - M) / S with the reciprocal normaliser, and the
 // residual max(0, p - q): separately rounded (no fused multiply-subtract),
 // so identical target and draft rows give p == q and an exactly empty
 // residual, and the residual pass and the draw compute the same values.
-__device__ __forceinline__ float prob(float x, float M, float inv_s) {
-  return __fmul_rn(rel_exp(x, M), inv_s);
+__device__ __forceinline__ float prob(float x, float M, float inv_s, float ls) {
+  return __fmul_rn(rel_exp(x, M, ls), inv_s);
 }
 __device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsub_rn(p, q), 0.f); }
 
@@ -278,6 +279,7 @@ struct AcceptParams {
   int per;     // entries per CTA slice (a multiple of 16 bytes' worth)
   int piece;   // entries per ring stage
   int bulk;    // rows 16-byte aligned: bulk copies; else element copies
+  float ls;    // log2(e) / temperature
 };
 
 // Producer warp: one piece of a row slice into a ring stage, completion on
@@ -333,6 +335,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
   const bool producer = warp == kConsumerWarps;
+  const float ls = a.ls;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
   const bool valid = B >= 1 && B <= kMaxB;  // the same in every CTA of the cluster
@@ -420,7 +423,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         __syncwarp();
         if (lane == 0) mbar_arrive_n(smem_u32(&S.empty[s]), 2);
         const float mx = Ld<T>::vmax(w, kVecs);
-        const float Rn = mx * kLog2e;
+        const float Rn = mx * ls;
         if (Rn > R) {
           sum = R == -INFINITY ? 0.f : sum * ex2(R - Rn);
           R = Rn;
@@ -440,7 +443,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
               float f[N];
               Ld<T>::unpack(w[i], f);
 #pragma unroll
-              for (int e = 0; e < N; ++e) acc[(i * N + e) & 7] += rel_exp(f[e], R);
+              for (int e = 0; e < N; ++e) acc[(i * N + e) & 7] += rel_exp(f[e], R, ls);
             }
 #pragma unroll
             for (int i = 0; i < kVecs / 2; ++i) w[i] = w[i + kVecs / 2];
@@ -514,7 +517,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         if (mine && r == 0) {
           S.norm[q] = make_float2(M, sm.hi + sm.lo);
           // p(x) (row 0) or q(x) (row 1); a token no slice holds rejects
-          const float pr = xin ? rel_exp(row ? xl.y : xl.x, M) / (sm.hi + sm.lo) : 0.f;
+          const float pr = xin ? rel_exp(row ? xl.y : xl.x, M, ls) / (sm.hi + sm.lo) : 0.f;
           if (row) S.qx[k] = pr; else S.px[k] = pr;
           if (!xin && row == 0 && rank == 0) raise_status(a.status, kStatusBadInput);
         }
@@ -594,8 +597,8 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
               Ld<T>::unpack(in ? dv[idx] : Ld<T>::neg_inf(), fd);
 #pragma unroll
               for (int e = 0; e < N; ++e) {
-                const float p = prob(ft[e], w.Mt, w.inv_st);
-                const float q = prob(fd[e], w.Md, w.inv_sd);
+                const float p = prob(ft[e], w.Mt, w.inv_st, ls);
+                const float q = prob(fd[e], w.Md, w.inv_sd, ls);
                 rs[e & 3] += residual(p, q);
                 ps[e & 3] += p;
               }
@@ -686,21 +689,21 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           int first = 0x7fffffff, last_pos = -1;
 #pragma unroll 1
           for (int i = 0; i < kCols && first == 0x7fffffff; ++i) {
-            const int e = (ws * kRangeVecs + i * 32 + lane) * N;   // the vector's first entry
-            const int vbase = s0 + sel * a.piece + e;
+            const int e0 = (ws * kRangeVecs + i * 32 + lane) * N;  // the vector's first entry
+            const int vbase = s0 + sel * a.piece + e0;
             float ft[N], fd[N], m[N];
-            Ld<T>::unpack(Ld<T>::load(tr + e, n - e, a.bulk != 0), ft);
-            Ld<T>::unpack(Ld<T>::load(dr + e, n - e, a.bulk != 0), fd);
-            float ls = 0.f;
+            Ld<T>::unpack(Ld<T>::load(tr + e0, n - e0, a.bulk != 0), ft);
+            Ld<T>::unpack(Ld<T>::load(dr + e0, n - e0, a.bulk != 0), fd);
+            float lane_mass = 0.f;
 #pragma unroll
             for (int e = 0; e < N; ++e) {
-              const float p = prob(ft[e], w.Mt, w.inv_st);
-              const float q = prob(fd[e], w.Md, w.inv_sd);
+              const float p = prob(ft[e], w.Mt, w.inv_st, ls);
+              const float q = prob(fd[e], w.Md, w.inv_sd, ls);
               m[e] = use_p ? p : residual(p, q);
-              ls += m[e];
+              lane_mass += m[e];
               if (m[e] > 0.f) last_pos = vbase + e;
             }
-            float inc = ls;
+            float inc = lane_mass;
 #pragma unroll
             for (int dd = 1; dd < 32; dd <<= 1) {
               const float y = __shfl_up_sync(0xffffffffu, inc, dd);
@@ -838,6 +841,143 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, accept_kernel<T>, a);
 }
 
+// ---------------------------------------------------------------- greedy
+// The greedy rule: per slot the target row's argmax (the largest value, the
+// smallest index among equal values), then the walk.  One cluster of C CTAs
+// per sequence, CTA r scanning vocabulary slice r of every target row with
+// 16-byte loads; CTA 0 merges the slices' candidates through distributed
+// shared memory and walks the steps.  Neither the draft logits nor the
+// uniforms are read.
+constexpr int kGreedyThreads = 256;
+constexpr int kGreedyCluster = 8;
+
+struct GreedyParams {
+  const void *target;
+  const int32_t *draft_tokens;
+  const int32_t *tau;
+  const int32_t *cu_B;
+  int32_t *n_accept;
+  int32_t *token;
+  int32_t *pos;
+  uint32_t *status;
+  int vocab, csize, per, bulk;
+};
+
+// candidate (v, i) beats (w, j): a larger value, or an equal one at a
+// smaller index (-inf entries still win over "none", index 2^31 - 1)
+__device__ __forceinline__ bool beats(float v, int i, float w, int j) {
+  return v > w || (v == w && i < j);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kGreedyThreads)
+accept_greedy_kernel(const __grid_constant__ GreedyParams a) {
+  constexpr int N = Ld<T>::N;
+  __shared__ float2 cand[kMaxB];                    // per slot: (value, index bits)
+  __shared__ float2 wbest[kGreedyThreads / 32];
+  const int rank = blockIdx.x, b = blockIdx.y;    // the cluster spans x
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int c0 = __ldg(a.cu_B + b);
+  const int B = __ldg(a.cu_B + b + 1) - c0;
+  const bool valid = B >= 1 && B <= kMaxB;
+  const int s0 = min(a.vocab, rank * a.per);
+  const int len = min(a.vocab, s0 + a.per) - s0;
+  if (valid) {
+    for (int k = 0; k < B; ++k) {
+      const T *row = (const T *)a.target + (long)(c0 + k) * a.vocab + s0;
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      if (a.bulk) {                                 // len is whole vectors here
+        const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+        for (int i = t; i < len / N; i += kGreedyThreads) {
+          float f[N];
+          Ld<T>::unpack(__ldg(rv + i), f);
+#pragma unroll
+          for (int e = 0; e < N; ++e)
+            if (beats(f[e], s0 + i * N + e, bv, bi)) { bv = f[e]; bi = s0 + i * N + e; }
+        }
+      } else {
+        for (int e = t; e < len; e += kGreedyThreads) {
+          const float v = Ld<T>::value(row[e]);
+          if (beats(v, s0 + e, bv, bi)) { bv = v; bi = s0 + e; }
+        }
+      }
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, m);
+        if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) wbest[warp] = make_float2(bv, __int_as_float(bi));
+      __syncthreads();
+      if (t == 0) {
+        float v = -INFINITY;
+        int i = 0x7fffffff;
+        for (int w = 0; w < kGreedyThreads / 32; ++w) {
+          const float2 c = wbest[w];
+          if (beats(c.x, __float_as_int(c.y), v, i)) { v = c.x; i = __float_as_int(c.y); }
+        }
+        cand[k] = make_float2(v, __int_as_float(i));
+      }
+      __syncthreads();
+    }
+  }
+  cluster_sync();                                   // every slice's candidates are in place
+  if (rank == 0 && t == 0) {
+    if (!valid) {                                   // malformed sequence: no walk
+      a.n_accept[b] = 0;
+      a.token[b] = -1;
+      a.pos[b] = -1;
+      raise_status(a.status, kStatusBadInput);
+    } else {
+      int slot_of_step[kMaxB];
+      for (int k = 0; k < B; ++k) slot_of_step[k] = 0;
+      for (int k = 0; k < B; ++k) {
+        const int tk = __ldg(a.tau + c0 + k);     // a label outside 1..B is ignored
+        if (tk >= 1 && tk <= B) slot_of_step[tk - 1] = k;
+      }
+      int n = B, tok = -1, ps = -1;
+      for (int st = 1; st <= B; ++st) {
+        const int k = slot_of_step[st - 1];
+        float v = -INFINITY;
+        int am = 0x7fffffff;
+        for (int r = 0; r < a.csize; ++r) {
+          const float2 c = ld_dsmem2(dsmem(&cand[k], r));
+          if (beats(c.x, __float_as_int(c.y), v, am)) { v = c.x; am = __float_as_int(c.y); }
+        }
+        const int x = __ldg(a.draft_tokens + c0 + k);
+        if (x < 0 || x >= a.vocab) raise_status(a.status, kStatusBadInput);
+        if (x != am) { n = st - 1; tok = am; ps = k; break; }
+      }
+      a.n_accept[b] = n;
+      a.token[b] = tok;
+      a.pos[b] = ps;
+    }
+  }
+  cluster_sync();                                   // no CTA leaves while CTA 0 reads it
+}
+
+template <typename T>
+cudaError_t launch_greedy(GreedyParams a, int batch, cudaStream_t stream) {
+  // about one CTA per SM across the batch, at most kGreedyCluster per sequence
+  const int vec = 16 / (int)sizeof(T);
+  a.csize = max(1, min(kGreedyCluster, device_sm_count() / max(1, batch)));
+  a.per = ((a.vocab + a.csize - 1) / a.csize + vec - 1) / vec * vec;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.csize, batch);
+  cfg.blockDim = dim3(kGreedyThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, accept_greedy_kernel<T>, a);
+}
+
 simsd_status accept_check(const simsd_accept_desc *d) {
   if (d == nullptr) return SIMSD_ERR_NULL;
   if (d->dtype != SIMSD_F32 && d->dtype != SIMSD_BF16) return SIMSD_ERR_DTYPE;
@@ -845,7 +985,17 @@ simsd_status accept_check(const simsd_accept_desc *d) {
       d->B_max < 1 || d->B_max > kMaxB || d->total_B < d->batch ||
       (int64_t)d->total_B > (int64_t)d->batch * d->B_max)
     return SIMSD_ERR_SHAPE;
+  if ((d->rule != SIMSD_ACCEPT_SAMPLE && d->rule != SIMSD_ACCEPT_GREEDY) ||
+      !(d->temperature >= 0.f && d->temperature <= 3.0e38f))   // negative, NaN or inf
+    return SIMSD_ERR_SHAPE;
   return SIMSD_OK;
+}
+
+// The pointers each rule reads (greedy reads no draft logits, no uniforms).
+bool accept_pointers_ok(const simsd_accept_desc *d) {
+  const bool greedy = d->rule == SIMSD_ACCEPT_GREEDY;
+  return d->target_logits && d->draft_tokens && d->tau && d->cu_B && d->n_accept &&
+         d->token && d->pos && (greedy || (d->draft_logits && d->uniforms));
 }
 
 // The workspace holds the status word only (everything else stays on chip).
@@ -882,6 +1032,28 @@ cudaError_t static_scratch(char **out) {
 // simsd_read_status reads them).
 simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t stream,
                         void *const *events) {
+  const int es = d->dtype == SIMSD_BF16 ? 2 : 4;
+  if (d->rule == SIMSD_ACCEPT_GREEDY) {
+    GreedyParams g;
+    g.target = d->target_logits;
+    g.draft_tokens = d->draft_tokens;
+    g.tau = d->tau;
+    g.cu_B = d->cu_B;
+    g.n_accept = d->n_accept;
+    g.token = d->token;
+    g.pos = d->pos;
+    g.status = (uint32_t *)ws;
+    g.vocab = d->vocab;
+    g.csize = 1;
+    g.per = 0;
+    g.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits);
+    mark(events, 0, stream);
+    const cudaError_t e = d->dtype == SIMSD_BF16 ? launch_greedy<__nv_bfloat16>(g, d->batch, stream)
+                                                 : launch_greedy<float>(g, d->batch, stream);
+    mark(events, 1, stream);
+    mark(events, 2, stream);
+    return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
+  }
   AcceptParams a;
   a.target = d->target_logits;
   a.draft = d->draft_logits;
@@ -897,7 +1069,7 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t strea
   a.vocab = d->vocab;
   a.B_max = d->B_max;
   a.total_B = d->total_B;
-  const int es = d->dtype == SIMSD_BF16 ? 2 : 4;
+  a.ls = kLog2e / (d->temperature > 0.f ? d->temperature : 1.f);
   // slices of whole 16-byte vectors (set with the cluster size at launch);
   // a piece is one ring stage
   a.csize = kMaxCluster;
@@ -933,9 +1105,7 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream_ptr,
                                 void *const events[3]) {
   simsd_status st = accept_check(d);
   if (st != SIMSD_OK) return st;
-  if (!d->target_logits || !d->draft_logits || !d->draft_tokens || !d->tau ||
-      !d->cu_B || !d->uniforms || !d->n_accept || !d->token || !d->pos)
-    return SIMSD_ERR_NULL;
+  if (!accept_pointers_ok(d)) return SIMSD_ERR_NULL;
   if (d->workspace == nullptr || ((uintptr_t)d->workspace % kAlign) != 0 ||
       d->workspace_bytes < kAcceptWorkspace)
     return SIMSD_ERR_WORKSPACE;
@@ -947,9 +1117,7 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream_ptr,
 simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream_ptr) {
   simsd_status st = accept_check(d);
   if (st != SIMSD_OK) return st;
-  if (!d->target_logits || !d->draft_logits || !d->draft_tokens || !d->tau ||
-      !d->cu_B || !d->uniforms || !d->n_accept || !d->token || !d->pos)
-    return SIMSD_ERR_NULL;
+  if (!accept_pointers_ok(d)) return SIMSD_ERR_NULL;
   if (kAcceptWorkspace > SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES) return SIMSD_ERR_WORKSPACE;
   char *ws = nullptr;
   if (static_scratch(&ws) != cudaSuccess) return SIMSD_ERR_CUDA;

@@ -75,12 +75,12 @@ def check_attention(got, ref, dtype):
     return err
 
 
-def oracle_accept(w):
+def oracle_accept(w, temperature=1.0):
     return oracle.accept(w.cu_B, synth.to_f64(w.target), synth.to_f64(w.draft),
-                         w.draft_tokens, w.tau, w.uniforms)
+                         w.draft_tokens, w.tau, w.uniforms, temperature=temperature)
 
 
-def check_accept(w, ref, n_accept, token, pos):
+def check_accept(w, ref, n_accept, token, pos, temperature=1.0):
     """Exact agreement outside the tie zone; validity inside it.
     Returns (accept-step ties, residual-draw ties, residual draws)."""
     am = ref["accept_margin"]
@@ -103,7 +103,8 @@ def check_accept(w, ref, n_accept, token, pos):
             continue
         draws += 1
         k = s0 + int(ref["pos"][b])
-        r, S = oracle.residual(synth.to_f64(w.target[k]), synth.to_f64(w.draft[k]))
+        r, S = oracle.residual(synth.to_f64(w.target[k]) / temperature,
+                               synth.to_f64(w.draft[k]) / temperature)
         C = np.cumsum(r)
         U = float(w.uniforms[b, B]) * S
         v = int(ref["token"][b])

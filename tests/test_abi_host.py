@@ -167,3 +167,32 @@ def test_verify_row_bytes_limit(lib):
     assert lib.simsd_verify_workspace_size(ctypes.byref(_desc(num_q_heads=376, num_kv_heads=8,
                                                               dtype=binding.SIMSD_F32))) == 0
     assert lib.simsd_verify_workspace_size(ctypes.byref(_desc(num_q_heads=376, num_kv_heads=8))) > 0
+
+
+def test_accept_rule_and_temperature_checks(lib):
+    """The rule and the temperature are checked before any launch; the greedy
+    rule needs neither draft logits nor uniforms (so with those NULL the call
+    gets as far as the workspace check)."""
+    d = binding.AcceptDesc()
+    for k, v in dict(batch=4, vocab=1000, total_B=16, B_max=4, dtype=1).items():
+        setattr(d, k, v)
+    fake = 1 << 40
+    for f in ("target_logits", "draft_logits", "draft_tokens", "tau", "cu_B",
+              "uniforms", "n_accept", "token", "pos"):
+        setattr(d, f, fake)
+    assert lib.simsd_accept_workspace_size(ctypes.byref(d)) > 0   # zero-filled: rule 0, T -> 1
+    for rule, temp in ((2, 1.0), (-1, 1.0), (0, -0.5), (0, float("nan")), (0, float("inf")),
+                       (1, -1.0)):
+        d.rule, d.temperature = rule, temp
+        assert lib.simsd_accept_workspace_size(ctypes.byref(d)) == 0, (rule, temp)
+        assert lib.simsd_accept(ctypes.byref(d), None) == 2, (rule, temp)
+        assert lib.simsd_accept_noalloc(ctypes.byref(d), None) == 2, (rule, temp)
+    d.rule, d.temperature = binding.SIMSD_ACCEPT_GREEDY, 0.0
+    d.draft_logits = None
+    d.uniforms = None
+    assert lib.simsd_accept(ctypes.byref(d), None) == 5          # reached the workspace check
+    d.target_logits = None
+    assert lib.simsd_accept(ctypes.byref(d), None) == 1
+    d.target_logits = fake
+    d.rule, d.temperature = binding.SIMSD_ACCEPT_SAMPLE, 0.7
+    assert lib.simsd_accept(ctypes.byref(d), None) == 1          # sampling needs both

@@ -189,3 +189,51 @@ def test_walk_distribution_monte_carlo():
     chi2 = (((obs - expc) ** 2 / expc)[keep]).sum()
     dof = keep.sum() - 1
     assert chi2 < dof + 4.0 * np.sqrt(2.0 * dof) + 10, (chi2, dof)
+
+
+# ------------------------------------------------------------------ variants
+def run_rule(w, rule, temperature=1.0):
+    dw = DeviceWorkload(w, with_verify=False)
+    greedy = rule == binding.SIMSD_ACCEPT_GREEDY
+    binding.accept(dw.target, None if greedy else dw.draft, dw.draft_tokens, dw.tau, dw.cu_B,
+                   None if greedy else dw.uniforms, dw.n_accept, dw.token, dw.pos,
+                   dw.accept_ws, dw.total_B, dw.B_max, rule=rule, temperature=temperature)
+    torch.cuda.synchronize()
+    assert binding.read_status(dw.accept_ws) == 0
+    return (dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy())
+
+
+def greedy_case(name):
+    if name == "sdar8b":
+        return synth.config(1)
+    dtype, vocab, batch = {"bf16-1003": ("bf16", 1003, 64), "f32-777": ("f32", 777, 64),
+                           "bf16-few": ("bf16", 151936, 3), "f32-odd": ("f32", 100003, 5)}[name]
+    return synth.make(tiny_accept_spec(batch=batch, dtype=dtype, vocab=vocab), seed=vocab + batch)
+
+
+@pytest.mark.parametrize("name", ["sdar8b", "bf16-1003", "f32-777", "bf16-few", "f32-odd"])
+def test_greedy_matches_oracle(name):
+    """The greedy rule: accepted lengths, positions and tokens bit-exact
+    against the oracle (argmax over the same bf16 / fp32 values, the
+    smallest index among equal maxima).  70% of the draft tokens are made the
+    target argmax so the walks get past their first step."""
+    w = greedy_case(name)
+    a = synth.to_f64(w.target).argmax(1).astype(np.int32)
+    rng = np.random.default_rng(7)
+    w.draft_tokens = np.where(rng.random(len(a)) < 0.7, a, w.draft_tokens).astype(np.int32)
+    n, tok, pos = run_rule(w, binding.SIMSD_ACCEPT_GREEDY)
+    ref = oracle.accept_greedy(w.cu_B, synth.to_f64(w.target), w.draft_tokens, w.tau)
+    np.testing.assert_array_equal(n, ref["n_accept"])
+    np.testing.assert_array_equal(pos, ref["pos"])
+    np.testing.assert_array_equal(tok, ref["token"])
+    assert (n > 0).any() and (n < w.Bs).any()
+
+
+@pytest.mark.parametrize("name,T", [("sdar8b", 0.5), ("sdar8b", 2.0), ("f32-777", 0.7),
+                                    ("bf16-1003", 1.5)])
+def test_temperature_matches_oracle(name, T):
+    """Sampling at temperature T: p = softmax(target / T), q = softmax(draft / T);
+    decisions exact outside the tie zone, valid inside."""
+    w = greedy_case(name)
+    n, tok, pos = run_rule(w, binding.SIMSD_ACCEPT_SAMPLE, T)
+    parity.check_accept(w, parity.oracle_accept(w, T), n, tok, pos, T)

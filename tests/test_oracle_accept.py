@@ -171,3 +171,82 @@ def test_margins_and_errors():
     with pytest.raises(oracle.OracleError):
         oracle.accept([0, 1], np.zeros((1, 4)), np.zeros((1, 4)), [4], [1],
                       np.zeros((1, 2), np.float32))
+
+
+# ------------------------------------------------------------------ variants
+def test_greedy_rule():
+    """Greedy verification: accept iff the draft token is the target's argmax
+    (first index among equal maxima); the first rejection emits the argmax.
+    Expected values from numpy's argmax and a hand walk over tau."""
+    rng = np.random.default_rng(21)
+    B, V = 5, 40
+    tau = np.array([3, 1, 5, 2, 4], np.int32)
+    target = np.round(rng.standard_normal((B, V)) * 4) / 4      # ties occur
+    target[1, 7] = target[1, 30] = target[1].max() + 1.0          # a tie at the top
+    a = target.argmax(1)
+    assert a[1] == 7
+    cu = np.array([0, B], np.int32)
+    # every draft token is the argmax: all accepted
+    r = oracle.accept_greedy(cu, target, a.astype(np.int32), tau)
+    assert r["n_accept"][0] == B and r["token"][0] == -1 and r["pos"][0] == -1
+    # the slot tested third (tau = 3 -> k = 0) proposes another token
+    x = a.astype(np.int32).copy()
+    x[0] = (a[0] + 1) % V
+    r = oracle.accept_greedy(cu, target, x, tau)
+    assert r["n_accept"][0] == 2 and r["token"][0] == a[0] and r["pos"][0] == 0
+    # the tied row: the later maximum is rejected in favour of the first
+    x = a.astype(np.int32).copy()
+    x[1] = 30
+    r = oracle.accept_greedy(cu, target, x, tau)
+    assert r["n_accept"][0] == 0 and r["token"][0] == 7 and r["pos"][0] == 1
+
+
+def test_greedy_is_the_zero_temperature_limit():
+    """Sampling at temperature -> 0 concentrates p and q on their argmax:
+    a step accepts iff x = argmax p, and the residual max(0, p - q) is the
+    point mass at argmax p.  The sampling oracle at T = 1e-6 must therefore
+    agree with the greedy oracle (tie-free logits, any uniforms)."""
+    rng = np.random.default_rng(22)
+    n, B, V = 200, 4, 64
+    target = rng.permutation(V * n * B).reshape(n * B, V) * 0.01       # distinct values
+    draft = target + rng.standard_normal((n * B, V))
+    cu = np.arange(0, n * B + 1, B, dtype=np.int32)
+    tau = np.concatenate([rng.permutation(B) + 1 for _ in range(n)]).astype(np.int32)
+    a = target.argmax(1)
+    # half of the draft tokens are the target argmax, the rest random
+    x = np.where(rng.random(n * B) < 0.7, a, rng.integers(0, V, n * B)).astype(np.int32)
+    uni = rng.random((n, B + 1), dtype=np.float32)
+    s = oracle.accept(cu, target, draft, x, tau, uni, temperature=1e-6)
+    g = oracle.accept_greedy(cu, target, x, tau)
+    np.testing.assert_array_equal(s["n_accept"], g["n_accept"])
+    np.testing.assert_array_equal(s["pos"], g["pos"])
+    np.testing.assert_array_equal(s["token"], g["token"])
+
+
+def test_temperature_scales_both_rows():
+    """Temperature T divides both rows' logits: at T = 2 the one-step outcome
+    distribution (exact enumeration over the uniforms' grid of the oracle's
+    own decisions) follows softmax(l / 2), not softmax(l)."""
+    rng = np.random.default_rng(23)
+    V, N = 6, 400
+    lt = rng.standard_normal(V) * 2
+    ld = lt + rng.standard_normal(V)
+    T = 2.0
+    grid = (np.arange(N) + 0.5) / N
+    u0, u1 = np.meshgrid(grid, grid, indexing="ij")
+    u0, u1 = u0.ravel(), u1.ravel()
+    p = softmax(lt / T)
+    q = softmax(ld / T)
+    expected = np.zeros(V)
+    for x in range(V):
+        n = len(u0)
+        cu = np.arange(n + 1, dtype=np.int32)
+        r = oracle.accept(cu, np.broadcast_to(lt, (n, V)), np.broadcast_to(ld, (n, V)),
+                          np.full(n, x, np.int32), np.ones(n, np.int32),
+                          np.stack([u0, u1], 1).astype(np.float32), n_threads=4,
+                          temperature=T)
+        emitted = np.where(r["n_accept"] == 1, x, r["token"])
+        expected += q[x] * np.bincount(emitted, minlength=V) / n
+    # losslessness at temperature T: the emitted token follows p = softmax(l / T)
+    np.testing.assert_allclose(expected, p, atol=3e-3)
+    assert np.abs(expected - softmax(lt)).max() > 2e-2
