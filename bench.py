@@ -60,7 +60,15 @@ def parse():
                     help="synthetic configuration index (1 = SDAR-8B verify step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--accept", default="sample", choices=["sample", "greedy"],
+                    help="acceptance rule: rejection sampling (default) or greedy")
+    ap.add_argument("--temperature", type=float, default=1.0,
+                    help="sampling temperature (rejection sampling only)")
     return ap.parse_args()
+
+
+def rule_code(args):
+    return 1 if args.accept == "greedy" else 0
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -86,9 +94,10 @@ def k2_bytes(w):
     return keys * 2 * s.Hkv * s.hd * es + T * s.Hq * s.hd * es * 2
 
 
-def accept_bytes(w):
+def accept_bytes(w, greedy=False):
+    """Logits read once per slot: both rows, or the target row alone (greedy)."""
     es = 2 if w.spec.dtype == "bf16" else 4
-    return int(w.cu_B[-1]) * 2 * w.spec.vocab * es
+    return int(w.cu_B[-1]) * (1 if greedy else 2) * w.spec.vocab * es
 
 
 # ---------------------------------------------------------------- peaks / clocks
@@ -179,7 +188,7 @@ def recorded_traffic(workload):
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_step_sample(w, seconds, threads):
+def oracle_step_sample(w, seconds, threads, greedy=False, temperature=1.0):
     """Time the oracle (attention + acceptance) over whole batches of the
     workload until `seconds` have passed; returns (tokens/s, sample text)."""
     import oracle
@@ -196,7 +205,11 @@ def oracle_step_sample(w, seconds, threads):
     while True:
         oracle.verify_attn(w.lens, w.cu_B, q, kp, vp, kn, vn, w.tau, w.spec.rope_base,
                            w.spec.sm_scale, n_threads=threads)
-        oracle.accept(w.cu_B, tl, dl, w.draft_tokens, w.tau, w.uniforms, n_threads=threads)
+        if greedy:
+            oracle.accept_greedy(w.cu_B, tl, w.draft_tokens, w.tau)
+        else:
+            oracle.accept(w.cu_B, tl, dl, w.draft_tokens, w.tau, w.uniforms, n_threads=threads,
+                          temperature=temperature)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -222,7 +235,8 @@ def run_reference(args):
     per_step = []
     per = max(1.0, min(8.0, 60.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup + args.steps):
-        v, el, reps = oracle_step_sample(w, per, threads)
+        v, el, reps = oracle_step_sample(w, per, threads, args.accept == "greedy",
+                                         args.temperature)
         if i >= args.warmup:
             per_step.append(el / reps)
     ms = float(np.mean(per_step)) * 1e3
@@ -246,7 +260,9 @@ def config_of(w, args):
             "seq_len": int(w.lens.max()), "B": int(w.Bs.max()), "q_heads": s.Hq,
             "kv_heads": s.Hkv, "head_dim": s.hd, "vocab": s.vocab,
             "parallelism": "replicas x%d" % max(1, args.gpus),
-            "l2": "flushed (512 MB write) before every timed step"}
+            "l2": "flushed (512 MB write) before every timed step",
+            "accept": args.accept + ("" if args.accept == "greedy" or args.temperature == 1.0
+                                     else " at temperature %g" % args.temperature)}
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -282,7 +298,8 @@ def main():
 
     def step(timed):
         dw.verify(events=vev if timed else None)
-        dw.accept(events=aev if timed else None)
+        dw.accept(events=aev if timed else None, rule=rule_code(args),
+                  temperature=args.temperature)
 
     # warm-up outside any graph (builds device-side caches and attributes)
     for _ in range(args.warmup):
@@ -342,6 +359,8 @@ def main():
         "draft_tokens": pin(w.draft_tokens.astype(np.int32)), "tau": pin(w.tau),
         "uniforms": pin(w.uniforms), "lens": pin(w.lens), "cu_B": pin(w.cu_B),
         "block_table": pin(w.block_table)}
+    if args.accept == "greedy":              # the greedy rule reads neither
+        del host_in["draft"], host_in["uniforms"]
     dev_of = {"q": dw.q, "k_new": dw.k_new, "v_new": dw.v_new, "target": dw.target,
               "draft": dw.draft, "draft_tokens": dw.draft_tokens, "tau": dw.tau,
               "uniforms": dw.uniforms, "lens": dw.lens, "cu_B": dw.cu_B,
@@ -357,7 +376,7 @@ def main():
         for k, h in host_in.items():
             dev_of[k].copy_(h, non_blocking=True)
         dw.verify()
-        dw.accept()
+        dw.accept(rule=rule_code(args), temperature=args.temperature)
         host_out["out"].copy_(dw.out, non_blocking=True)
         host_out["n_accept"].copy_(dw.n_accept, non_blocking=True)
         host_out["token"].copy_(dw.token, non_blocking=True)
@@ -380,7 +399,7 @@ def main():
         for k, h in host_in.items():
             dev_of[k].copy_(h, non_blocking=True)
         dw.verify()
-        dw.accept()
+        dw.accept(rule=rule_code(args), temperature=args.temperature)
         host_out["out"].copy_(dw.out, non_blocking=True)
         host_out["n_accept"].copy_(dw.n_accept, non_blocking=True)
         host_out["token"].copy_(dw.token, non_blocking=True)
@@ -435,14 +454,15 @@ def main():
                          "traffic": traffic,
                          "algorithmic_bytes_per_launch": k2_bytes(w)},
             "verify_attn_GBps": attn_bytes(w) / (attn_ms / 1e3) / 1e9,
-            "accept_GBps": accept_bytes(w) / (acc_ms / 1e3) / 1e9,
+            "accept_GBps": accept_bytes(w, args.accept == "greedy") / (acc_ms / 1e3) / 1e9,
             "kernels_ms": {n: round(k["ms"], 5) for n, k in kernels.items()},
             "clocks": clk, "status_word": status}
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import build as obuild
         obuild.build()
         threads = cpu_threads()
-        v, el, reps = oracle_step_sample(w, args.cpu_seconds, threads)
+        v, el, reps = oracle_step_sample(w, args.cpu_seconds, threads, args.accept == "greedy",
+                                         args.temperature)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": "%d whole batch(es) of %s (attention + acceptance), %.1f s"
                                           % (reps, w.spec.name, el)}

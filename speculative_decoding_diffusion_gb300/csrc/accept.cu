@@ -848,7 +848,8 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
 // 16-byte loads; CTA 0 merges the slices' candidates through distributed
 // shared memory and walks the steps.  Neither the draft logits nor the
 // uniforms are read.
-constexpr int kGreedyThreads = 256;
+constexpr int kGreedyThreads = 512;
+constexpr int kGreedyUnroll = 8;
 constexpr int kGreedyCluster = 8;
 
 struct GreedyParams {
@@ -888,13 +889,25 @@ accept_greedy_kernel(const __grid_constant__ GreedyParams a) {
       float bv = -INFINITY;
       int bi = 0x7fffffff;
       if (a.bulk) {                                 // len is whole vectors here
+        // kGreedyUnroll independent 16-byte loads in flight per thread
         const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-        for (int i = t; i < len / N; i += kGreedyThreads) {
-          float f[N];
-          Ld<T>::unpack(__ldg(rv + i), f);
+        const int nv = len / N;
+        for (int i0 = t; i0 < nv; i0 += kGreedyUnroll * kGreedyThreads) {
+          uint4 w[kGreedyUnroll];
 #pragma unroll
-          for (int e = 0; e < N; ++e)
-            if (beats(f[e], s0 + i * N + e, bv, bi)) { bv = f[e]; bi = s0 + i * N + e; }
+          for (int u = 0; u < kGreedyUnroll; ++u) {
+            const int i = i0 + u * kGreedyThreads;
+            w[u] = i < nv ? __ldg(rv + i) : Ld<T>::neg_inf();
+          }
+#pragma unroll
+          for (int u = 0; u < kGreedyUnroll; ++u) {
+            const int i = i0 + u * kGreedyThreads;
+            float f[N];
+            Ld<T>::unpack(w[u], f);
+#pragma unroll
+            for (int e = 0; e < N; ++e)
+              if (i < nv && beats(f[e], s0 + i * N + e, bv, bi)) { bv = f[e]; bi = s0 + i * N + e; }
+          }
         }
       } else {
         for (int e = t; e < len; e += kGreedyThreads) {

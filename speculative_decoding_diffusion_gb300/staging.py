@@ -106,7 +106,10 @@ class DeviceWorkload:
                 self.uniforms, self.n_accept, self.token, self.pos, self.total_B,
                 self.B_max)
 
-    def accept(self, stream=None, events=None):
+    def accept(self, stream=None, events=None, rule=binding.SIMSD_ACCEPT_SAMPLE,
+               temperature=1.0):
         (t, d, x, tau, cu, u, n, tok, pos, tb, bm) = self._accept_args()
+        if rule == binding.SIMSD_ACCEPT_GREEDY:      # reads neither draft logits nor uniforms
+            d = u = None
         binding.accept(t, d, x, tau, cu, u, n, tok, pos, self.accept_ws, tb, bm,
-                       stream=stream, events=events)
+                       stream=stream, events=events, rule=rule, temperature=temperature)
