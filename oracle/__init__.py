@@ -47,6 +47,7 @@ def _lib():
         lib.oracle_accept.argtypes = [I, I, P, P, P, P, P, P, I, P, P, P, P,
                                       P, I]
         lib.oracle_accept_greedy.argtypes = [I, I, P, P, P, P, P, P, P]
+        lib.oracle_accept_match.argtypes = [I, I, P, P, P, P, P, I, P, P, P]
         lib.oracle_residual.argtypes = [I, P, P, P]
         lib.oracle_residual.restype = D
         _LIB = lib
@@ -177,6 +178,23 @@ def accept_greedy(cu_B, target, draft_tokens, tau):
     _check(_lib().oracle_accept_greedy(
         batch, target.shape[1], _p(cu_B), _p(target), _p(draft_tokens), _p(tau),
         _p(n_accept), _p(token), _p(pos)), "oracle_accept_greedy")
+    return dict(n_accept=n_accept, token=token, pos=pos)
+
+
+def accept_match(cu_B, target, draft_tokens, tau, uniforms):
+    """Sample matching: dict(n_accept, token, pos); uniforms [batch, >= B]."""
+    cu_B = _c(cu_B, np.int32)
+    target = _c(target, np.float64)
+    draft_tokens, tau = _c(draft_tokens, np.int32), _c(tau, np.int32)
+    uniforms = _c(uniforms, np.float32)
+    batch = len(cu_B) - 1
+    n_accept = np.zeros(batch, np.int32)
+    token = np.zeros(batch, np.int32)
+    pos = np.zeros(batch, np.int32)
+    _check(_lib().oracle_accept_match(
+        batch, target.shape[1], _p(cu_B), _p(target), _p(draft_tokens), _p(tau),
+        _p(uniforms), uniforms.shape[1], _p(n_accept), _p(token), _p(pos)),
+        "oracle_accept_match")
     return dict(n_accept=n_accept, token=token, pos=pos)
 
 

@@ -176,3 +176,47 @@ int oracle_accept_greedy(int batch, int V, const int *cu_B, const double *target
   }
   return ORACLE_OK;
 }
+
+/* Sample matching (Spiffy's verification, read for one slot per step): step
+ * t draws the target's own token y_t from p_k by inverse CDF with u[t-1] (the
+ * smallest v whose running mass exceeds u[t-1]; the last v with p > 0 if
+ * rounding leaves none) and accepts iff y_t equals the draft token; the
+ * first rejection emits y_t and stops.  Every emitted token is a sample of
+ * p_k; a step accepts with probability p_k(x).  u[B] is not used. */
+int oracle_accept_match(int batch, int V, const int *cu_B, const double *target,
+                        const int *draft_tokens, const int *tau, const float *uniforms,
+                        int u_stride, int *n_accept, int *token, int *pos) {
+  if (batch < 0 || V < 1 || !cu_B || !target || !draft_tokens || !tau || !uniforms ||
+      !n_accept || !token || !pos)
+    return ORACLE_ERR_ARG;
+  for (int b = 0; b < batch; ++b) {
+    const int s0 = cu_B[b], B = cu_B[b + 1] - s0;
+    if (B < 1 || u_stride < B) return ORACLE_ERR_ARG;
+    if (!oracle_tau_is_permutation(B, tau + s0)) return ORACLE_ERR_TAU;
+    n_accept[b] = B;
+    token[b] = -1;
+    pos[b] = -1;
+    for (int t = 1; t <= B; ++t) {
+      int k = 0;
+      while (tau[s0 + k] != t) ++k;
+      const double *row = target + (size_t)(s0 + k) * V;
+      const double lse = log_sum_exp(row, V);
+      const double U = (double)uniforms[(size_t)b * u_stride + t - 1];
+      int y = -1, last = -1;
+      double c = 0.0;
+      for (int v = 0; v < V; ++v) {
+        const double pv = exp(row[v] - lse);
+        if (pv > 0.0) last = v;
+        c += pv;
+        if (y < 0 && c > U) y = v;
+      }
+      if (y < 0) y = last;
+      if (draft_tokens[s0 + k] == y) continue;
+      n_accept[b] = t - 1;
+      token[b] = y;
+      pos[b] = k;
+      break;
+    }
+  }
+  return ORACLE_OK;
+}

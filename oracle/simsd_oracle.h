@@ -125,6 +125,12 @@ int oracle_accept_greedy(int batch, int V, const int *cu_B, const double *target
                          const int *draft_tokens, const int *tau,
                          int *n_accept, int *token, int *pos);
 
+/* Sample matching: step t draws y_t from p by inverse CDF with u[t-1] and
+ * accepts iff y_t is the draft token; the first rejection emits y_t. */
+int oracle_accept_match(int batch, int V, const int *cu_B, const double *target,
+                        const int *draft_tokens, const int *tau, const float *uniforms,
+                        int u_stride, int *n_accept, int *token, int *pos);
+
 #ifdef __cplusplus
 }
 #endif

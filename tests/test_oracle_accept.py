@@ -250,3 +250,49 @@ def test_temperature_scales_both_rows():
     # losslessness at temperature T: the emitted token follows p = softmax(l / T)
     np.testing.assert_allclose(expected, p, atol=3e-3)
     assert np.abs(expected - softmax(lt)).max() > 2e-2
+
+
+def test_sample_matching_rule():
+    """Sample matching: over a midpoint grid of u, a single step accepts with
+    probability p(x) and the emitted token (x when accepted, the target's
+    sample otherwise) follows p; a point-mass target accepts its token always
+    and rejects every other one, emitting the point."""
+    rng = np.random.default_rng(24)
+    V, N = 7, 4000
+    lt = rng.standard_normal(V) * 1.5
+    p = softmax(lt)
+    u = ((np.arange(N) + 0.5) / N).astype(np.float32)[:, None]
+    cu = np.arange(N + 1, dtype=np.int32)
+    for x in range(V):
+        r = oracle.accept_match(cu, np.broadcast_to(lt, (N, V)), np.full(N, x, np.int32),
+                                np.ones(N, np.int32), u)
+        acc = r["n_accept"] == 1
+        np.testing.assert_allclose(acc.mean(), p[x], atol=2.0 / N)
+        emitted = np.where(acc, x, r["token"])
+        np.testing.assert_allclose(np.bincount(emitted, minlength=V) / N, p, atol=2.0 / N)
+        assert (r["pos"][~acc] == 0).all() and (r["token"][acc] == -1).all()
+    point = np.full(V, -np.inf)
+    point[3] = 0.0
+    for x, want in ((3, 1), (5, 0)):
+        r = oracle.accept_match(np.array([0, 1], np.int32), point[None], np.array([x], np.int32),
+                                np.ones(1, np.int32), np.array([[0.99]], np.float32))
+        assert r["n_accept"][0] == want and r["token"][0] == (-1 if want else 3)
+
+
+def test_sample_matching_walk_order():
+    """The walk follows tau: the steps use u[0], u[1], ... in temporal order
+    and stop at the first mismatch (hand-built three-slot case)."""
+    V = 4
+    target = np.log(np.array([[0.1, 0.2, 0.3, 0.4],      # slot 0: tested second
+                              [0.7, 0.1, 0.1, 0.1],      # slot 1: tested first
+                              [0.25, 0.25, 0.25, 0.25]]))  # slot 2: tested third
+    tau = np.array([2, 1, 3], np.int32)
+    cu = np.array([0, 3], np.int32)
+    # step 1 (slot 1): u = 0.5 -> token 0; step 2 (slot 0): u = 0.65 -> token 3
+    u = np.array([[0.5, 0.65, 0.1, 0.0]], np.float32)
+    r = oracle.accept_match(cu, target, np.array([3, 0, 0], np.int32), tau, u)
+    assert r["n_accept"][0] == 3 and r["token"][0] == -1
+    r = oracle.accept_match(cu, target, np.array([2, 0, 0], np.int32), tau, u)
+    assert r["n_accept"][0] == 1 and r["pos"][0] == 0 and r["token"][0] == 3
+    r = oracle.accept_match(cu, target, np.array([3, 1, 0], np.int32), tau, u)
+    assert r["n_accept"][0] == 0 and r["pos"][0] == 1 and r["token"][0] == 0
