@@ -206,6 +206,12 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * maxima); the first rejection emits that argmax.  It reads neither the
  * draft logits nor the uniforms (they may be NULL), and runs a separate,
  * lighter kernel (one pass over the target rows).
+ * Variant rule SIMSD_ACCEPT_MATCH (sample matching, Spiffy's verification):
+ * step t draws the target's own token y from p (at temperature T) by
+ * inverse CDF with u[t-1] and accepts iff y = x; the first rejection emits
+ * y (u[B_b] unused, draft logits not read and may be NULL).  A separate
+ * kernel: one pass over the target rows, then a scan of one vocabulary
+ * slice at a rejection.
  * Kernel: K4, one thread-block cluster of C CTAs per sequence (C <= 16,
  * chosen at launch from the batch size and the clusters the device can
  * hold at once), each CTA owning 1/C of the vocabulary: max and sum of
@@ -234,7 +240,8 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * ---------------------------------------------------------------------- */
 typedef enum {
   SIMSD_ACCEPT_SAMPLE = 0,    /* rejection sampling at temperature T         */
-  SIMSD_ACCEPT_GREEDY = 1     /* accept iff x = argmax of the target row      */
+  SIMSD_ACCEPT_GREEDY = 1,    /* accept iff x = argmax of the target row      */
+  SIMSD_ACCEPT_MATCH = 2      /* accept iff x = the target's own sample       */
 } simsd_accept_rule;
 
 typedef struct {

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libsimsd.so")
 
 SIMSD_F32, SIMSD_BF16 = 0, 1
-SIMSD_ACCEPT_SAMPLE, SIMSD_ACCEPT_GREEDY = 0, 1
+SIMSD_ACCEPT_SAMPLE, SIMSD_ACCEPT_GREEDY, SIMSD_ACCEPT_MATCH = 0, 1, 2
 STATUS = {0: "SIMSD_OK", 1: "SIMSD_ERR_NULL", 2: "SIMSD_ERR_SHAPE",
           3: "SIMSD_ERR_TAU", 4: "SIMSD_ERR_DTYPE", 5: "SIMSD_ERR_WORKSPACE",
           6: "SIMSD_ERR_CUDA", 7: "SIMSD_ERR_TIMEOUT", 8: "SIMSD_ERR_ALIGN"}

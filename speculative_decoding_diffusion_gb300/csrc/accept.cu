@@ -991,6 +991,285 @@ cudaError_t launch_greedy(GreedyParams a, int batch, cudaStream_t stream) {
   return cudaLaunchKernelEx(&cfg, accept_greedy_kernel<T>, a);
 }
 
+// ---------------------------------------------------------------- match
+// Sample matching: step t draws the target's own token y_t from p by inverse
+// CDF with u[t-1] and accepts iff y_t is the draft token; the first
+// rejection emits y_t.  In mass units of S = sum_v 2^(l_v ls - M): the step
+// accepts iff Pre(x) <= u S < Pre(x) + 2^(l_x ls - M), Pre(x) the mass of
+// the entries below x.  One cluster of C CTAs per sequence; CTA r streams
+// slice r of every target row once for (reference, mass, mass below x, l_x);
+// every CTA merges the C slices' partials through distributed shared memory
+// and walks the steps identically; at a rejection the CTA whose slice holds
+// u S finds y_t by a block scan of its slice in vocabulary order.
+constexpr int kMatchThreads = 512;
+constexpr int kMatchWarps = kMatchThreads / 32;
+constexpr int kMatchUnroll = 8;
+
+struct MatchParams {
+  const void *target;
+  const int32_t *draft_tokens;
+  const int32_t *tau;
+  const int32_t *cu_B;
+  const float *uniforms;
+  int32_t *n_accept;
+  int32_t *token;
+  int32_t *pos;
+  uint32_t *status;
+  int vocab, B_max, csize, per, bulk;
+  float ls;
+};
+
+struct __align__(16) MatchSlot {
+  float R, xl;       // the slice's reference (log2 units) and l_x if x lies in it
+  Ff s, pre;         // sum of 2^(l ls - R) over the slice, and over its entries below x
+};
+
+// (R, s, pre) += (R2, s2, pre2): both sums to the larger reference
+__device__ __forceinline__ void match_merge(float &R, Ff &s, Ff &pre, float R2, Ff s2, Ff pre2) {
+  const float M = fmaxf(R, R2);
+  if (M == -INFINITY) return;
+  const float a = ex2(R - M), b = ex2(R2 - M);
+  s = ff_add(Ff{s.hi * a, s.lo * a}, Ff{s2.hi * b, s2.lo * b});
+  pre = ff_add(Ff{pre.hi * a, pre.lo * a}, Ff{pre2.hi * b, pre2.lo * b});
+  R = M;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMatchThreads)
+accept_match_kernel(const __grid_constant__ MatchParams a) {
+  constexpr int N = Ld<T>::N;
+  __shared__ MatchSlot slot[kMaxB];
+  __shared__ MatchSlot wpart[kMatchWarps];
+  __shared__ Ff wsum[kMatchWarps];
+  __shared__ int s_ch, s_best, s_last, s_k;
+  __shared__ Ff s_U, s_base;
+  __shared__ float s_M;
+  const int rank = blockIdx.x, b = blockIdx.y;    // the cluster spans x
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const float ls = a.ls;
+  const int c0 = __ldg(a.cu_B + b);
+  const int B = __ldg(a.cu_B + b + 1) - c0;
+  const bool valid = B >= 1 && B <= kMaxB;
+  const int s0 = min(a.vocab, rank * a.per);
+  const int len = min(a.vocab, s0 + a.per) - s0;
+  auto value_at = [&](const T *row, int e) { return Ld<T>::value(row[e]); };
+  if (valid) {
+    for (int k = 0; k < B; ++k) {
+      const T *row = (const T *)a.target + (long)(c0 + k) * a.vocab + s0;
+      const int x = __ldg(a.draft_tokens + c0 + k);
+      const int xo = x - s0;                        // x's offset in this slice
+      float R = -INFINITY, sm = 0.f, pr = 0.f, xl = -INFINITY;
+      // one group of kMatchUnroll entries (vectors in the bulk case) per round
+      const int unit = a.bulk ? N : 1;
+      const int nu = a.bulk ? len / N : len;
+      for (int i0 = t; i0 < nu; i0 += kMatchUnroll * kMatchThreads) {
+        float f[kMatchUnroll][N];
+#pragma unroll
+        for (int u = 0; u < kMatchUnroll; ++u) {
+          const int i = i0 + u * kMatchThreads;
+          if (a.bulk) {
+            Ld<T>::unpack(i < nu ? __ldg(reinterpret_cast<const uint4 *>(row) + i) : Ld<T>::neg_inf(), f[u]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < N; ++e) f[u][e] = (e == 0 && i < nu) ? value_at(row, i) : -INFINITY;
+          }
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kMatchUnroll; ++u)
+#pragma unroll
+          for (int e = 0; e < N; ++e) mx = fmaxf(mx, f[u][e]);
+        const float Rn = mx * ls;
+        if (Rn > R) {
+          const float c = R == -INFINITY ? 0.f : ex2(R - Rn);
+          sm *= c;
+          pr *= c;
+          R = Rn;
+        }
+        if (R == -INFINITY) continue;
+#pragma unroll
+        for (int u = 0; u < kMatchUnroll; ++u) {
+          const int base_e = (i0 + u * kMatchThreads) * unit;
+#pragma unroll
+          for (int e = 0; e < N; ++e) {
+            const float m = rel_exp(f[u][e], R, ls);
+            sm += m;
+            if (base_e + e < xo) pr += m;
+            if (base_e + e == xo) xl = f[u][e];
+          }
+        }
+      }
+      // warp, then block: to the largest reference, sums as pairs
+      Ff s2 = ff_of(sm), p2 = ff_of(pr);
+      float Rw = R;
+#pragma unroll 1
+      for (int m = 16; m > 0; m >>= 1) {
+        const float R2 = __shfl_xor_sync(0xffffffffu, Rw, m);
+        const Ff so = ff_shfl_xor(s2, m), po = ff_shfl_xor(p2, m);
+        match_merge(Rw, s2, p2, R2, so, po);
+        xl = fmaxf(xl, __shfl_xor_sync(0xffffffffu, xl, m));
+      }
+      if (lane == 0) wpart[warp] = MatchSlot{Rw, xl, s2, p2};
+      __syncthreads();
+      if (t == 0) {
+        MatchSlot c = wpart[0];
+        for (int w = 1; w < kMatchWarps; ++w) {
+          const MatchSlot o = wpart[w];
+          match_merge(c.R, c.s, c.pre, o.R, o.s, o.pre);
+          c.xl = fmaxf(c.xl, o.xl);
+        }
+        slot[k] = c;
+      }
+      __syncthreads();
+    }
+  }
+  cluster_sync();                                   // B1: every slice's partials are in place
+  if (t == 0) {
+    s_ch = -1;
+    s_k = -1;
+    if (valid) {
+      int slot_of_step[kMaxB];
+      for (int k = 0; k < B; ++k) slot_of_step[k] = 0;
+      for (int k = 0; k < B; ++k) {
+        const int tk = __ldg(a.tau + c0 + k);     // a label outside 1..B is ignored
+        if (tk >= 1 && tk <= B) slot_of_step[tk - 1] = k;
+      }
+      int n = B, rej = -1;
+      for (int st = 1; st <= B; ++st) {
+        const int k = slot_of_step[st - 1];
+        // the slices' partials in rank order, merged to the largest reference
+        float M = -INFINITY, xl = -INFINITY;
+        for (int r = 0; r < a.csize; ++r) {
+          const float4 h = ld_dsmem4(dsmem(&slot[k], r));
+          M = fmaxf(M, h.x);
+          xl = fmaxf(xl, h.y);
+        }
+        Ff S = ff_of(0.f), Pre = ff_of(0.f);
+        if (M != -INFINITY)
+          for (int r = 0; r < a.csize; ++r) {
+            const float4 h = ld_dsmem4(dsmem(&slot[k], r));
+            const float4 q = ld_dsmem4(dsmem(reinterpret_cast<const float4 *>(&slot[k]) + 1, r));
+            if (h.x == -INFINITY) continue;
+            const float w = ex2(h.x - M);
+            S = ff_add(S, Ff{h.z * w, h.w * w});
+            Pre = ff_add(Pre, Ff{q.x * w, q.y * w});
+          }
+        const int x = __ldg(a.draft_tokens + c0 + k);
+        if (x < 0 || x >= a.vocab) raise_status(a.status, kStatusBadInput);
+        const float u = __ldg(a.uniforms + (long)b * (a.B_max + 1) + st - 1);
+        const float uh = u * S.hi;
+        const Ff U = ff_add(Ff{uh, fmaf(u, S.hi, -uh)}, ff_of(u * S.lo));
+        const float px = (x >= 0 && x < a.vocab) ? ex2(fmaf(xl, ls, -M)) : 0.f;   // mass of x
+        const bool acc = px > 0.f && !ff_gt(Pre, U) && ff_gt(ff_add(Pre, ff_of(px)), U);
+        if (acc) continue;
+        n = st - 1;
+        rej = k;
+        // the slice holding U: the first whose running total exceeds it,
+        // else the last with mass
+        Ff run = ff_of(0.f), base = ff_of(0.f);
+        int ch = -1, lastnz = 0;
+        Ff lastbase = ff_of(0.f);
+        for (int r = 0; r < a.csize; ++r) {
+          const float4 h = ld_dsmem4(dsmem(&slot[k], r));
+          const float w = h.x == -INFINITY ? 0.f : ex2(h.x - M);
+          const Ff m = Ff{h.z * w, h.w * w};
+          const Ff nx = ff_add(run, m);
+          if (m.hi > 0.f) {
+            lastnz = r;
+            lastbase = run;
+            if (ff_gt(nx, U)) { ch = r; base = run; break; }
+          }
+          run = nx;
+        }
+        if (ch < 0) { ch = lastnz; base = lastbase; }
+        s_ch = ch;
+        s_k = k;
+        s_U = U;
+        s_base = base;
+        s_best = 0x7fffffff;
+        s_last = -1;
+        s_M = M;
+        break;
+      }
+      if (rank == 0) {
+        a.n_accept[b] = n;
+        a.pos[b] = rej;
+        if (rej < 0) a.token[b] = -1;
+      }
+    } else if (rank == 0) {                         // malformed sequence: no walk
+      a.n_accept[b] = 0;
+      a.token[b] = -1;
+      a.pos[b] = -1;
+      raise_status(a.status, kStatusBadInput);
+    }
+  }
+  __syncthreads();
+  if (s_ch == rank && s_k >= 0) {
+    // block scan of this slice of row k in vocabulary order: thread t holds
+    // the contiguous chunk [t * chunk, (t + 1) * chunk)
+    const int k = s_k;
+    const float M = s_M;
+    const T *row = (const T *)a.target + (long)(c0 + k) * a.vocab + s0;
+    const int chunk = (len + kMatchThreads - 1) / kMatchThreads;
+    const int e0 = min(len, t * chunk), e1 = min(len, e0 + chunk);
+    float part = 0.f;
+    int last = -1;
+    for (int e = e0; e < e1; ++e) {
+      const float m = rel_exp(value_at(row, e), M, ls);
+      part += m;
+      if (m > 0.f) last = s0 + e;
+    }
+    // exclusive prefix of the chunk masses (pairs) over the block
+    Ff inc = ff_of(part);
+#pragma unroll 1
+    for (int d = 1; d < 32; d <<= 1) {
+      const Ff y = ff_shfl_up(inc, d);
+      if (lane >= d) inc = ff_add(y, inc);
+    }
+    if (lane == 31) wsum[warp] = inc;
+    __syncthreads();
+    Ff start = s_base;
+    for (int w = 0; w < warp; ++w) start = ff_add(start, wsum[w]);
+    start = ff_add(start, ff_add(inc, ff_of(-part)));
+    const Ff D = ff_add(s_U, ff_neg(start));
+    const float dd = D.hi + D.lo;                   // U - this chunk's start
+    int first = 0x7fffffff;
+    if (dd < part) {
+      float run = 0.f;
+      for (int e = e0; e < e1; ++e) {
+        const float m = rel_exp(value_at(row, e), M, ls);
+        run += m;
+        if (m > 0.f && run > dd) { first = s0 + e; break; }
+      }
+    }
+    if (first != 0x7fffffff) atomicMin(&s_best, first);
+    if (last >= 0) atomicMax(&s_last, last);
+    __syncthreads();
+    if (t == 0) a.token[b] = s_best != 0x7fffffff ? s_best : s_last;
+  }
+  cluster_sync();                                   // B2: no CTA leaves while others read it
+}
+
+template <typename T>
+cudaError_t launch_match(MatchParams a, int batch, cudaStream_t stream) {
+  const int vec = 16 / (int)sizeof(T);
+  a.csize = max(1, min(kGreedyCluster, device_sm_count() / max(1, batch)));
+  a.per = ((a.vocab + a.csize - 1) / a.csize + vec - 1) / vec * vec;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.csize, batch);
+  cfg.blockDim = dim3(kMatchThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, accept_match_kernel<T>, a);
+}
+
 simsd_status accept_check(const simsd_accept_desc *d) {
   if (d == nullptr) return SIMSD_ERR_NULL;
   if (d->dtype != SIMSD_F32 && d->dtype != SIMSD_BF16) return SIMSD_ERR_DTYPE;
@@ -998,17 +1277,20 @@ simsd_status accept_check(const simsd_accept_desc *d) {
       d->B_max < 1 || d->B_max > kMaxB || d->total_B < d->batch ||
       (int64_t)d->total_B > (int64_t)d->batch * d->B_max)
     return SIMSD_ERR_SHAPE;
-  if ((d->rule != SIMSD_ACCEPT_SAMPLE && d->rule != SIMSD_ACCEPT_GREEDY) ||
+  if ((d->rule != SIMSD_ACCEPT_SAMPLE && d->rule != SIMSD_ACCEPT_GREEDY &&
+       d->rule != SIMSD_ACCEPT_MATCH) ||
       !(d->temperature >= 0.f && d->temperature <= 3.0e38f))   // negative, NaN or inf
     return SIMSD_ERR_SHAPE;
   return SIMSD_OK;
 }
 
-// The pointers each rule reads (greedy reads no draft logits, no uniforms).
+// The pointers each rule reads (greedy: no draft logits, no uniforms;
+// sample matching: no draft logits).
 bool accept_pointers_ok(const simsd_accept_desc *d) {
-  const bool greedy = d->rule == SIMSD_ACCEPT_GREEDY;
+  const bool draft = d->rule == SIMSD_ACCEPT_SAMPLE;
+  const bool uni = d->rule != SIMSD_ACCEPT_GREEDY;
   return d->target_logits && d->draft_tokens && d->tau && d->cu_B && d->n_accept &&
-         d->token && d->pos && (greedy || (d->draft_logits && d->uniforms));
+         d->token && d->pos && (!draft || d->draft_logits) && (!uni || d->uniforms);
 }
 
 // The workspace holds the status word only (everything else stays on chip).
@@ -1063,6 +1345,30 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t strea
     mark(events, 0, stream);
     const cudaError_t e = d->dtype == SIMSD_BF16 ? launch_greedy<__nv_bfloat16>(g, d->batch, stream)
                                                  : launch_greedy<float>(g, d->batch, stream);
+    mark(events, 1, stream);
+    mark(events, 2, stream);
+    return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
+  }
+  if (d->rule == SIMSD_ACCEPT_MATCH) {
+    MatchParams m;
+    m.target = d->target_logits;
+    m.draft_tokens = d->draft_tokens;
+    m.tau = d->tau;
+    m.cu_B = d->cu_B;
+    m.uniforms = d->uniforms;
+    m.n_accept = d->n_accept;
+    m.token = d->token;
+    m.pos = d->pos;
+    m.status = (uint32_t *)ws;
+    m.vocab = d->vocab;
+    m.B_max = d->B_max;
+    m.csize = 1;
+    m.per = 0;
+    m.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits);
+    m.ls = kLog2e / (d->temperature > 0.f ? d->temperature : 1.f);
+    mark(events, 0, stream);
+    const cudaError_t e = d->dtype == SIMSD_BF16 ? launch_match<__nv_bfloat16>(m, d->batch, stream)
+                                                 : launch_match<float>(m, d->batch, stream);
     mark(events, 1, stream);
     mark(events, 2, stream);
     return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;

@@ -181,8 +181,8 @@ def test_accept_rule_and_temperature_checks(lib):
               "uniforms", "n_accept", "token", "pos"):
         setattr(d, f, fake)
     assert lib.simsd_accept_workspace_size(ctypes.byref(d)) > 0   # zero-filled: rule 0, T -> 1
-    for rule, temp in ((2, 1.0), (-1, 1.0), (0, -0.5), (0, float("nan")), (0, float("inf")),
-                       (1, -1.0)):
+    for rule, temp in ((3, 1.0), (-1, 1.0), (0, -0.5), (0, float("nan")), (0, float("inf")),
+                       (1, -1.0), (2, -2.0)):
         d.rule, d.temperature = rule, temp
         assert lib.simsd_accept_workspace_size(ctypes.byref(d)) == 0, (rule, temp)
         assert lib.simsd_accept(ctypes.byref(d), None) == 2, (rule, temp)
@@ -196,3 +196,7 @@ def test_accept_rule_and_temperature_checks(lib):
     d.target_logits = fake
     d.rule, d.temperature = binding.SIMSD_ACCEPT_SAMPLE, 0.7
     assert lib.simsd_accept(ctypes.byref(d), None) == 1          # sampling needs both
+    d.rule = binding.SIMSD_ACCEPT_MATCH                          # matching needs the uniforms
+    assert lib.simsd_accept(ctypes.byref(d), None) == 1
+    d.uniforms = fake
+    assert lib.simsd_accept(ctypes.byref(d), None) == 5          # but no draft logits

@@ -237,3 +237,67 @@ def test_temperature_matches_oracle(name, T):
     w = greedy_case(name)
     n, tok, pos = run_rule(w, binding.SIMSD_ACCEPT_SAMPLE, T)
     parity.check_accept(w, parity.oracle_accept(w, T), n, tok, pos, T)
+
+
+def check_match(w, n, tok, pos, temperature=1.0, tie=parity.TIE_RESIDUAL):
+    """Sample matching against the oracle, decision by decision: exact unless
+    u lies within `tie` of a bin edge the decision depends on (then validity)."""
+    ref = oracle.accept_match(w.cu_B, synth.to_f64(w.target) / temperature, w.draft_tokens,
+                              w.tau, w.uniforms)
+    V = w.spec.vocab
+    ties = 0
+    for b in range(len(w.lens)):
+        s0, s1 = int(w.cu_B[b]), int(w.cu_B[b + 1])
+        B = s1 - s0
+        order = [int(np.nonzero(w.tau[s0:s1] == t)[0][0]) for t in range(1, B + 1)]
+        near = False
+        for t, k in enumerate(order[:int(ref["n_accept"][b]) + 1]):
+            lt = synth.to_f64(w.target[s0 + k]) / temperature
+            p = np.exp(lt - lt.max()); p /= p.sum()
+            C = np.cumsum(p)
+            u = float(w.uniforms[b, t])
+            y = min(int(np.searchsorted(C, u, side="right")), V - 1)
+            edges = [C[y - 1] if y > 0 else 0.0, C[y]]
+            if min(abs(u - e) for e in edges) < tie:
+                near = True
+        if near:
+            ties += 1
+            assert 0 <= n[b] <= B
+            if pos[b] >= 0:
+                assert n[b] < B and 0 <= tok[b] < V
+            continue
+        assert n[b] == ref["n_accept"][b], (b, n[b], ref["n_accept"][b])
+        assert pos[b] == ref["pos"][b], (b, pos[b], ref["pos"][b])
+        assert tok[b] == ref["token"][b], (b, tok[b], ref["token"][b])
+    return ties
+
+
+@pytest.mark.parametrize("name,T", [("sdar8b", 1.0), ("bf16-1003", 1.0), ("f32-777", 0.8),
+                                    ("bf16-few", 1.0), ("f32-odd", 1.3)])
+def test_sample_matching_matches_oracle(name, T):
+    """Sample matching (accept iff the target's own inverse-CDF sample at
+    u[t-1] equals the draft token; the rejection emits that sample): exact
+    against the oracle outside the tie zone.  Half of the draft tokens are
+    the target's own samples so that walks get past their first step."""
+    w = greedy_case(name)
+    rng = np.random.default_rng(8)
+    tl = synth.to_f64(w.target) / T
+    for b in range(len(w.lens)):
+        s0, s1 = int(w.cu_B[b]), int(w.cu_B[b + 1])
+        for k in range(s1 - s0):
+            if rng.random() < 0.5:
+                t = int(w.tau[s0 + k]) - 1
+                p = np.exp(tl[s0 + k] - tl[s0 + k].max()); p /= p.sum()
+                y = int(np.searchsorted(np.cumsum(p), float(w.uniforms[b, t]), side="right"))
+                w.draft_tokens[s0 + k] = min(y, w.spec.vocab - 1)
+    dw = DeviceWorkload(w, with_verify=False)
+    binding.accept(dw.target, None, dw.draft_tokens, dw.tau, dw.cu_B, dw.uniforms, dw.n_accept,
+                   dw.token, dw.pos, dw.accept_ws, dw.total_B, dw.B_max,
+                   rule=binding.SIMSD_ACCEPT_MATCH, temperature=T)
+    torch.cuda.synchronize()
+    assert binding.read_status(dw.accept_ws) == 0
+    n, tok, pos = dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy()
+    ties = check_match(w, n, tok, pos, T)
+    if w.spec.vocab < 2000:          # large bins: nearly every decision is checked exactly
+        assert ties <= 4
+    assert (n > 0).any()
