@@ -60,15 +60,16 @@ def parse():
                     help="synthetic configuration index (1 = SDAR-8B verify step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--accept", default="sample", choices=["sample", "greedy"],
-                    help="acceptance rule: rejection sampling (default) or greedy")
+    ap.add_argument("--accept", default="sample", choices=["sample", "greedy", "match"],
+                    help="acceptance rule: rejection sampling (default), greedy, or "
+                         "sample matching")
     ap.add_argument("--temperature", type=float, default=1.0,
                     help="sampling temperature (rejection sampling only)")
     return ap.parse_args()
 
 
 def rule_code(args):
-    return 1 if args.accept == "greedy" else 0
+    return {"sample": 0, "greedy": 1, "match": 2}[args.accept]
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -94,10 +95,11 @@ def k2_bytes(w):
     return keys * 2 * s.Hkv * s.hd * es + T * s.Hq * s.hd * es * 2
 
 
-def accept_bytes(w, greedy=False):
-    """Logits read once per slot: both rows, or the target row alone (greedy)."""
+def accept_bytes(w, target_only=False):
+    """Logits read once per slot: both rows, or the target row alone (greedy,
+    sample matching)."""
     es = 2 if w.spec.dtype == "bf16" else 4
-    return int(w.cu_B[-1]) * (1 if greedy else 2) * w.spec.vocab * es
+    return int(w.cu_B[-1]) * (1 if target_only else 2) * w.spec.vocab * es
 
 
 # ---------------------------------------------------------------- peaks / clocks
@@ -188,7 +190,7 @@ def recorded_traffic(workload):
 
 
 # ---------------------------------------------------------------- CPU oracle
-def oracle_step_sample(w, seconds, threads, greedy=False, temperature=1.0):
+def oracle_step_sample(w, seconds, threads, rule="sample", temperature=1.0):
     """Time the oracle (attention + acceptance) over whole batches of the
     workload until `seconds` have passed; returns (tokens/s, sample text)."""
     import oracle
@@ -205,8 +207,10 @@ def oracle_step_sample(w, seconds, threads, greedy=False, temperature=1.0):
     while True:
         oracle.verify_attn(w.lens, w.cu_B, q, kp, vp, kn, vn, w.tau, w.spec.rope_base,
                            w.spec.sm_scale, n_threads=threads)
-        if greedy:
+        if rule == "greedy":
             oracle.accept_greedy(w.cu_B, tl, w.draft_tokens, w.tau)
+        elif rule == "match":
+            oracle.accept_match(w.cu_B, tl / temperature, w.draft_tokens, w.tau, w.uniforms)
         else:
             oracle.accept(w.cu_B, tl, dl, w.draft_tokens, w.tau, w.uniforms, n_threads=threads,
                           temperature=temperature)
@@ -235,8 +239,7 @@ def run_reference(args):
     per_step = []
     per = max(1.0, min(8.0, 60.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup + args.steps):
-        v, el, reps = oracle_step_sample(w, per, threads, args.accept == "greedy",
-                                         args.temperature)
+        v, el, reps = oracle_step_sample(w, per, threads, args.accept, args.temperature)
         if i >= args.warmup:
             per_step.append(el / reps)
     ms = float(np.mean(per_step)) * 1e3
@@ -359,8 +362,10 @@ def main():
         "draft_tokens": pin(w.draft_tokens.astype(np.int32)), "tau": pin(w.tau),
         "uniforms": pin(w.uniforms), "lens": pin(w.lens), "cu_B": pin(w.cu_B),
         "block_table": pin(w.block_table)}
-    if args.accept == "greedy":              # the greedy rule reads neither
-        del host_in["draft"], host_in["uniforms"]
+    if args.accept != "sample":              # greedy and matching read no draft logits,
+        del host_in["draft"]                 # greedy no uniforms either
+    if args.accept == "greedy":
+        del host_in["uniforms"]
     dev_of = {"q": dw.q, "k_new": dw.k_new, "v_new": dw.v_new, "target": dw.target,
               "draft": dw.draft, "draft_tokens": dw.draft_tokens, "tau": dw.tau,
               "uniforms": dw.uniforms, "lens": dw.lens, "cu_B": dw.cu_B,
@@ -454,14 +459,14 @@ def main():
                          "traffic": traffic,
                          "algorithmic_bytes_per_launch": k2_bytes(w)},
             "verify_attn_GBps": attn_bytes(w) / (attn_ms / 1e3) / 1e9,
-            "accept_GBps": accept_bytes(w, args.accept == "greedy") / (acc_ms / 1e3) / 1e9,
+            "accept_GBps": accept_bytes(w, args.accept != "sample") / (acc_ms / 1e3) / 1e9,
             "kernels_ms": {n: round(k["ms"], 5) for n, k in kernels.items()},
             "clocks": clk, "status_word": status}
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import build as obuild
         obuild.build()
         threads = cpu_threads()
-        v, el, reps = oracle_step_sample(w, args.cpu_seconds, threads, args.accept == "greedy",
+        v, el, reps = oracle_step_sample(w, args.cpu_seconds, threads, args.accept,
                                          args.temperature)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": "%d whole batch(es) of %s (attention + acceptance), %.1f s"

@@ -109,7 +109,9 @@ class DeviceWorkload:
     def accept(self, stream=None, events=None, rule=binding.SIMSD_ACCEPT_SAMPLE,
                temperature=1.0):
         (t, d, x, tau, cu, u, n, tok, pos, tb, bm) = self._accept_args()
-        if rule == binding.SIMSD_ACCEPT_GREEDY:      # reads neither draft logits nor uniforms
-            d = u = None
+        if rule != binding.SIMSD_ACCEPT_SAMPLE:      # greedy and matching read no draft logits
+            d = None
+        if rule == binding.SIMSD_ACCEPT_GREEDY:      # greedy reads no uniforms either
+            u = None
         binding.accept(t, d, x, tau, cu, u, n, tok, pos, self.accept_ws, tb, bm,
                        stream=stream, events=events, rule=rule, temperature=temperature)
