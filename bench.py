@@ -26,6 +26,10 @@ its mean event-timed duration.
 `cpu_baseline`: the fp64 oracle on a bounded sample of the same workload,
 timed on this host's cores.
 
+--accept greedy / match times the other acceptance rules (the greedy rule,
+sample matching), --temperature T sampling at temperature T; the default is
+rejection sampling at T = 1.
+
 --impl reference runs the oracle as the reference arm.  Multi-GPU (torchrun):
 each rank runs its own replica batch (sequences are independent; no
 collective on the data path), rank 0 prints the aggregate.
