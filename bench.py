@@ -272,6 +272,24 @@ def config_of(w, args):
                                      else " at temperature %g" % args.temperature)}
 
 
+# ---------------------------------------------------------------- multi-rank helpers
+def max_over_ranks(dist, x, device):
+    """The largest rank's value of x (x itself on a single rank): the job's
+    time is its slowest rank's."""
+    if not dist:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput(tokens_per_rank_step, world, total_ms, steps):
+    """Whole-job tokens/s: every rank's tokens of a step over the step time
+    (the slowest rank's total over the steps)."""
+    return tokens_per_rank_step * world / (total_ms / steps / 1e3)
+
+
 # ---------------------------------------------------------------- GPU arm
 def main():
     args = parse()
@@ -348,11 +366,7 @@ def main():
             k_ms[n].append(t)
         k_ms["K4"].append(aev[0].elapsed_time(aev[1]))
     torch.cuda.synchronize()
-    dev_total_ms = float(np.sum(step_ms))
-    if dist:
-        t = torch.tensor([dev_total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_total_ms = float(t.item())
+    dev_total_ms = max_over_ranks(dist, float(np.sum(step_ms)), "cuda")
 
     # ---- end to end through the C ABI with host buffers
     def pin(a):
@@ -426,19 +440,15 @@ def main():
         g2.replay()
         stream.synchronize()
         e2eg_ms.append((time.perf_counter() - t0) * 1e3)
-    e2eg_total = float(np.sum(e2eg_ms))
-    if dist:
-        t = torch.tensor([e2e_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
+    e2e_total = max_over_ranks(dist, e2e_total, "cuda")
+    e2eg_total = max_over_ranks(dist, float(np.sum(e2eg_ms)), "cuda")
     clk = clocks.stop()
     status = binding.read_status(dw.verify_ws) | binding.read_status(dw.accept_ws)
 
-    tokens_per_step = int(w.cu_B[-1]) * world
     ms_per_step = dev_total_ms / args.steps
-    value = tokens_per_step / (ms_per_step / 1e3)
-    e2e_value = tokens_per_step / (e2e_total / args.steps / 1e3)
-    e2eg_value = tokens_per_step / (e2eg_total / args.steps / 1e3)
+    value = throughput(int(w.cu_B[-1]), world, dev_total_ms, args.steps)
+    e2e_value = throughput(int(w.cu_B[-1]), world, e2e_total, args.steps)
+    e2eg_value = throughput(int(w.cu_B[-1]), world, e2eg_total, args.steps)
     peak, peak_kind = hbm_peak()
     k2_mean = float(np.mean(k_ms["K2"]))
     achieved = k2_bytes(w) / (k2_mean / 1e3) / 1e9
