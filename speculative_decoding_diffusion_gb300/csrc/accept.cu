@@ -3,10 +3,12 @@
 // SimSD section 4 "Speculative Decoding Pipeline", acceptance: standard
 // rejection sampling along the draft-induced temporal order; the longest
 // accepted prefix is committed.  For sequence b, step t = 1..B tests the
-// slot k = tau^-1(t) with draft token x: p = softmax(target row k),
-// q = softmax(draft row k); accept iff u[t-1] * q(x) < p(x) (fp32).  At the
-// first rejection a token is drawn from max(0, p - q) normalised (p itself
-// when that is empty) by inverse CDF with u[B].
+// slot k = tau^-1(t) with draft token x: p = softmax(target row k / T),
+// q = softmax(draft row k / T) at temperature T (1 by default); accept iff
+// u[t-1] * q(x) < p(x) (fp32).  At the first rejection a token is drawn
+// from max(0, p - q) normalised (p itself when that is empty) by inverse
+// CDF with u[B].  The greedy rule and sample matching have their own,
+// simpler kernels at the end of this file.
 //
 // One launch; one thread-block cluster of C CTAs per sequence (C <= 16, from
 // a makespan estimate over the resident-cluster waves: 8-16 for small
