@@ -48,6 +48,7 @@ def _lib():
                                       P, I]
         lib.oracle_accept_greedy.argtypes = [I, I, P, P, P, P, P, P, P]
         lib.oracle_accept_match.argtypes = [I, I, P, P, P, P, P, I, P, P, P]
+        lib.oracle_draft_step.argtypes = [I, I, P, P, P, I, P, P, P]
         lib.oracle_residual.argtypes = [I, P, P, P]
         lib.oracle_residual.restype = D
         _LIB = lib
@@ -196,6 +197,25 @@ def accept_match(cu_B, target, draft_tokens, tau, uniforms):
         _p(uniforms), uniforms.shape[1], _p(n_accept), _p(token), _p(pos)),
         "oracle_accept_match")
     return dict(n_accept=n_accept, token=token, pos=pos)
+
+
+def draft_step(cu_B, draft, uniforms, temperature=1.0):
+    """The draft-side step: dict(draft_tokens, tau, confidence) per slot;
+    draft [sum B, V] logits (divided by the temperature), uniforms
+    [batch, >= B] (u[k] samples slot k)."""
+    cu_B = _c(cu_B, np.int32)
+    draft = _c(draft, np.float64)
+    if temperature != 1.0:
+        draft = np.ascontiguousarray(draft / float(temperature))
+    uniforms = _c(uniforms, np.float32)
+    n = int(cu_B[-1])
+    toks = np.zeros(n, np.int32)
+    tau = np.zeros(n, np.int32)
+    conf = np.zeros(n, np.float64)
+    _check(_lib().oracle_draft_step(len(cu_B) - 1, draft.shape[1], _p(cu_B), _p(draft),
+                                    _p(uniforms), uniforms.shape[1], _p(toks), _p(tau),
+                                    _p(conf)), "oracle_draft_step")
+    return dict(draft_tokens=toks, tau=tau, confidence=conf)
 
 
 def residual(target_row, draft_row):

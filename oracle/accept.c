@@ -220,3 +220,48 @@ int oracle_accept_match(int batch, int V, const int *cu_B, const double *target,
   }
   return ORACLE_OK;
 }
+
+/* The draft-side step (the step before the layout): each slot k of a
+ * sequence samples its draft token x_k from q_k = softmax(draft row k) by
+ * inverse CDF with u[k] (the smallest v whose running mass exceeds u[k];
+ * the last v with q > 0 if rounding leaves none), and the step labels order
+ * the slots by the draft's confidence q_k(x_k), most confident first (tau = 1),
+ * equal confidences in position order.  The pages leave the ordering rule
+ * open; confidence order is the reading taken. */
+int oracle_draft_step(int batch, int V, const int *cu_B, const double *draft,
+                      const float *uniforms, int u_stride, int *draft_tokens, int *tau,
+                      double *confidence) {
+  if (batch < 0 || V < 1 || !cu_B || !draft || !uniforms || !draft_tokens || !tau ||
+      !confidence)
+    return ORACLE_ERR_ARG;
+  for (int b = 0; b < batch; ++b) {
+    const int s0 = cu_B[b], B = cu_B[b + 1] - s0;
+    if (B < 1 || u_stride < B) return ORACLE_ERR_ARG;
+    for (int k = 0; k < B; ++k) {
+      const double *row = draft + (size_t)(s0 + k) * V;
+      const double lse = log_sum_exp(row, V);
+      const double U = (double)uniforms[(size_t)b * u_stride + k];
+      int y = -1, last = -1;
+      double c = 0.0, py = 0.0, plast = 0.0;
+      for (int v = 0; v < V; ++v) {
+        const double qv = exp(row[v] - lse);
+        if (qv > 0.0) { last = v; plast = qv; }
+        c += qv;
+        if (y < 0 && c > U) { y = v; py = qv; }
+      }
+      if (y < 0) { y = last; py = plast; }
+      draft_tokens[s0 + k] = y;
+      confidence[s0 + k] = py;
+    }
+    /* tau(k) = 1 + the number of slots that come before k */
+    for (int k = 0; k < B; ++k) {
+      int before = 0;
+      for (int j = 0; j < B; ++j) {
+        const double cj = confidence[s0 + j], ck = confidence[s0 + k];
+        if (cj > ck || (cj == ck && j < k)) ++before;
+      }
+      tau[s0 + k] = before + 1;
+    }
+  }
+  return ORACLE_OK;
+}

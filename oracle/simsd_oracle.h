@@ -131,6 +131,13 @@ int oracle_accept_match(int batch, int V, const int *cu_B, const double *target,
                         const int *draft_tokens, const int *tau, const float *uniforms,
                         int u_stride, int *n_accept, int *token, int *pos);
 
+/* The draft-side step: each slot samples its token from the draft softmax by
+ * inverse CDF with u[k]; tau orders the slots by that token's draft
+ * probability (most confident first, ties in position order). */
+int oracle_draft_step(int batch, int V, const int *cu_B, const double *draft,
+                      const float *uniforms, int u_stride, int *draft_tokens, int *tau,
+                      double *confidence);
+
 #ifdef __cplusplus
 }
 #endif

@@ -296,3 +296,48 @@ def test_sample_matching_walk_order():
     assert r["n_accept"][0] == 1 and r["pos"][0] == 0 and r["token"][0] == 3
     r = oracle.accept_match(cu, target, np.array([3, 1, 0], np.int32), tau, u)
     assert r["n_accept"][0] == 0 and r["pos"][0] == 1 and r["token"][0] == 0
+
+
+# ------------------------------------------------------------------ draft side
+def test_draft_step_samples_the_draft_distribution():
+    """Over a midpoint grid of u, the draft-side step's token for a slot
+    follows q = softmax(draft row) (exact up to the grid), and its confidence
+    is q of that token."""
+    rng = np.random.default_rng(25)
+    V, N = 9, 3000
+    ld = rng.standard_normal(V) * 1.2
+    q = softmax(ld)
+    cu = np.arange(N + 1, dtype=np.int32)
+    u = ((np.arange(N) + 0.5) / N).astype(np.float32)[:, None]
+    r = oracle.draft_step(cu, np.broadcast_to(ld, (N, V)), u)
+    np.testing.assert_allclose(np.bincount(r["draft_tokens"], minlength=V) / N, q, atol=2.0 / N)
+    np.testing.assert_allclose(r["confidence"], q[r["draft_tokens"]], rtol=1e-12)
+    assert (r["tau"] == 1).all()
+
+
+def test_draft_step_orders_by_confidence():
+    """tau is a permutation ordering the slots by the draft probability of
+    their sampled tokens, most confident first, equal ones in position order
+    (hand-built: slot 2 certain, slots 0 and 3 tied, slot 1 least sure)."""
+    V = 4
+    rows = np.log(np.array([[0.5, 0.5, 1e-300, 1e-300],    # slot 0: either token, q = 0.5
+                            [0.3, 0.3, 0.2, 0.2],          # slot 1: q <= 0.3
+                            [1.0, 1e-300, 1e-300, 1e-300],  # slot 2: q = 1
+                            [1e-300, 0.5, 0.5, 1e-300]]))  # slot 3: q = 0.5
+    cu = np.array([0, 4], np.int32)
+    u = np.array([[0.2, 0.7, 0.9, 0.8]], np.float32)
+    r = oracle.draft_step(cu, rows, u)
+    np.testing.assert_array_equal(r["draft_tokens"], [0, 2, 0, 2])
+    np.testing.assert_allclose(r["confidence"], [0.5, 0.2, 1.0, 0.5], rtol=1e-9)
+    np.testing.assert_array_equal(r["tau"], [2, 4, 1, 3])
+    rng = np.random.default_rng(26)
+    B, n = 6, 50
+    cu = np.arange(0, B * n + 1, B, dtype=np.int32)
+    r = oracle.draft_step(cu, rng.standard_normal((B * n, 20)) * 2,
+                          rng.random((n, B), dtype=np.float32))
+    for b in range(n):
+        t = r["tau"][b * B:(b + 1) * B]
+        c = r["confidence"][b * B:(b + 1) * B]
+        assert sorted(t) == list(range(1, B + 1))
+        by_step = c[np.argsort(t)]
+        assert (np.diff(by_step) <= 0).all()
