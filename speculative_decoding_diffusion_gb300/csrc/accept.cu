@@ -68,7 +68,9 @@ static_assert(kVecs % 2 == 0 && kRangeVecs % 32 == 0, "a range is whole vectors 
 static_assert(kRanges * kRangeVecs * 16 == kStageBytes, "the ranges tile a stage");
 static_assert(kConsumers % kMaxCluster == 0 && 32 % kMaxCluster == 0,
               "whole groups of consumer threads per pair");
-static_assert(kVecs * 8 % 8 == 0 && (kVecs / 2) * 4 % 8 == 0, "accumulator slots repeat every half");
+// the main pass's 8 accumulators see the same slots in both rolled halves:
+// (kVecs / 2) vectors of N >= 4 entries are a multiple of 8 entries
+static_assert((kVecs / 2) * 4 % 8 == 0, "accumulator slots repeat every half");
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
 constexpr int kMaxVocab = 1 << 21;                 // 8 slices of kMaxPieces pieces of 8192 fp32 entries
 constexpr float kLog2e = 1.4426950408889634f;
