@@ -203,7 +203,7 @@ def run_rule(w, rule, temperature=1.0):
     return (dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy())
 
 
-def greedy_case(name):
+def variant_case(name):
     if name == "sdar8b":
         return synth.config(1)
     dtype, vocab, batch = {"bf16-1003": ("bf16", 1003, 64), "f32-777": ("f32", 777, 64),
@@ -217,7 +217,7 @@ def test_greedy_matches_oracle(name):
     against the oracle (argmax over the same bf16 / fp32 values, the
     smallest index among equal maxima).  70% of the draft tokens are made the
     target argmax so the walks get past their first step."""
-    w = greedy_case(name)
+    w = variant_case(name)
     a = synth.to_f64(w.target).argmax(1).astype(np.int32)
     rng = np.random.default_rng(7)
     w.draft_tokens = np.where(rng.random(len(a)) < 0.7, a, w.draft_tokens).astype(np.int32)
@@ -234,7 +234,7 @@ def test_greedy_matches_oracle(name):
 def test_temperature_matches_oracle(name, T):
     """Sampling at temperature T: p = softmax(target / T), q = softmax(draft / T);
     decisions exact outside the tie zone, valid inside."""
-    w = greedy_case(name)
+    w = variant_case(name)
     n, tok, pos = run_rule(w, binding.SIMSD_ACCEPT_SAMPLE, T)
     parity.check_accept(w, parity.oracle_accept(w, T), n, tok, pos, T)
 
@@ -279,7 +279,7 @@ def test_sample_matching_matches_oracle(name, T):
     u[t-1] equals the draft token; the rejection emits that sample): exact
     against the oracle outside the tie zone.  Half of the draft tokens are
     the target's own samples so that walks get past their first step."""
-    w = greedy_case(name)
+    w = variant_case(name)
     rng = np.random.default_rng(8)
     tl = synth.to_f64(w.target) / T
     for b in range(len(w.lens)):
