@@ -45,10 +45,11 @@ def _lib():
         lib.oracle_verify_attn.argtypes = [I, P, P, I, I, I, D, D, P, P, P, P,
                                            P, P, P, I]
         lib.oracle_accept.argtypes = [I, I, P, P, P, P, P, P, I, P, P, P, P,
-                                      P, I]
-        lib.oracle_accept_greedy.argtypes = [I, I, P, P, P, P, P, P, P]
-        lib.oracle_accept_match.argtypes = [I, I, P, P, P, P, P, I, P, P, P]
-        lib.oracle_draft_step.argtypes = [I, I, P, P, P, I, P, P, P]
+                                      P, P, I]
+        lib.oracle_accept_greedy.argtypes = [I, I, P, P, P, P, P, P, P, P]
+        lib.oracle_accept_match.argtypes = [I, I, P, P, P, P, P, I, P, P, P, P]
+        lib.oracle_draft_step.argtypes = [I, I, P, P, P, I, P, P, P, P, P]
+        lib.oracle_commit.argtypes = [I, P, P, P, P, P, P, P, P, P]
         lib.oracle_residual.argtypes = [I, P, P, P]
         lib.oracle_residual.restype = D
         _LIB = lib
@@ -140,11 +141,17 @@ def verify_attn(lens, cu_B, q, k_prompt, v_prompt, k_new, v_new, tau,
     return out
 
 
-def accept(cu_B, target, draft, draft_tokens, tau, uniforms, n_threads=0, temperature=1.0):
+def _first(first_step, batch):
+    return None if first_step is None else _c(first_step, np.int32).reshape(batch)
+
+
+def accept(cu_B, target, draft, draft_tokens, tau, uniforms, n_threads=0, temperature=1.0,
+           first_step=None):
     """Returns dict(n_accept, token, pos, accept_margin, resample_margin).
     target/draft [sum B, V] (any float dtype, taken exactly to fp64);
     uniforms [batch, u_stride] float32.  temperature T: p = softmax(target / T),
-    q = softmax(draft / T) (the logits divided in fp64)."""
+    q = softmax(draft / T) (the logits divided in fp64).  first_step [batch]
+    (optional): the walk's first step per sequence (earlier steps decided)."""
     cu_B = _c(cu_B, np.int32)
     target, draft = _c(target, np.float64), _c(draft, np.float64)
     if temperature != 1.0:
@@ -159,15 +166,16 @@ def accept(cu_B, target, draft, draft_tokens, tau, uniforms, n_threads=0, temper
     pos = np.zeros(batch, np.int32)
     am = np.zeros(int(cu_B[-1]), np.float64)
     rm = np.zeros(batch, np.float64)
+    fs = _first(first_step, batch)
     _check(_lib().oracle_accept(
         batch, V, _p(cu_B), _p(target), _p(draft), _p(draft_tokens), _p(tau),
-        _p(uniforms), uniforms.shape[1], _p(n_accept), _p(token), _p(pos),
+        _p(uniforms), uniforms.shape[1], _p(fs), _p(n_accept), _p(token), _p(pos),
         _p(am), _p(rm), int(n_threads)), "oracle_accept")
     return dict(n_accept=n_accept, token=token, pos=pos, accept_margin=am,
                 resample_margin=rm)
 
 
-def accept_greedy(cu_B, target, draft_tokens, tau):
+def accept_greedy(cu_B, target, draft_tokens, tau, first_step=None):
     """Greedy verification: dict(n_accept, token, pos); target [sum B, V]."""
     cu_B = _c(cu_B, np.int32)
     target = _c(target, np.float64)
@@ -176,13 +184,14 @@ def accept_greedy(cu_B, target, draft_tokens, tau):
     n_accept = np.zeros(batch, np.int32)
     token = np.zeros(batch, np.int32)
     pos = np.zeros(batch, np.int32)
+    fs = _first(first_step, batch)
     _check(_lib().oracle_accept_greedy(
-        batch, target.shape[1], _p(cu_B), _p(target), _p(draft_tokens), _p(tau),
+        batch, target.shape[1], _p(cu_B), _p(target), _p(draft_tokens), _p(tau), _p(fs),
         _p(n_accept), _p(token), _p(pos)), "oracle_accept_greedy")
     return dict(n_accept=n_accept, token=token, pos=pos)
 
 
-def accept_match(cu_B, target, draft_tokens, tau, uniforms):
+def accept_match(cu_B, target, draft_tokens, tau, uniforms, first_step=None):
     """Sample matching: dict(n_accept, token, pos); uniforms [batch, >= B]."""
     cu_B = _c(cu_B, np.int32)
     target = _c(target, np.float64)
@@ -192,30 +201,52 @@ def accept_match(cu_B, target, draft_tokens, tau, uniforms):
     n_accept = np.zeros(batch, np.int32)
     token = np.zeros(batch, np.int32)
     pos = np.zeros(batch, np.int32)
+    fs = _first(first_step, batch)
     _check(_lib().oracle_accept_match(
         batch, target.shape[1], _p(cu_B), _p(target), _p(draft_tokens), _p(tau),
-        _p(uniforms), uniforms.shape[1], _p(n_accept), _p(token), _p(pos)),
+        _p(uniforms), uniforms.shape[1], _p(fs), _p(n_accept), _p(token), _p(pos)),
         "oracle_accept_match")
     return dict(n_accept=n_accept, token=token, pos=pos)
 
 
-def draft_step(cu_B, draft, uniforms, temperature=1.0):
+def draft_step(cu_B, draft, uniforms, temperature=1.0, decided=None, tau_prev=None,
+               tokens_prev=None):
     """The draft-side step: dict(draft_tokens, tau, confidence) per slot;
     draft [sum B, V] logits (divided by the temperature), uniforms
-    [batch, >= B] (u[k] samples slot k)."""
+    [batch, >= B] (u[k] samples slot k).  Within a block: decided [batch]
+    steps already decided keep their labels (tau_prev) and tokens
+    (tokens_prev); confidence is -1 there."""
     cu_B = _c(cu_B, np.int32)
     draft = _c(draft, np.float64)
     if temperature != 1.0:
         draft = np.ascontiguousarray(draft / float(temperature))
     uniforms = _c(uniforms, np.float32)
     n = int(cu_B[-1])
-    toks = np.zeros(n, np.int32)
+    batch = len(cu_B) - 1
+    toks = np.zeros(n, np.int32) if tokens_prev is None else _c(tokens_prev, np.int32).copy()
     tau = np.zeros(n, np.int32)
     conf = np.zeros(n, np.float64)
-    _check(_lib().oracle_draft_step(len(cu_B) - 1, draft.shape[1], _p(cu_B), _p(draft),
-                                    _p(uniforms), uniforms.shape[1], _p(toks), _p(tau),
-                                    _p(conf)), "oracle_draft_step")
+    dec = None if decided is None else _c(decided, np.int32).reshape(batch)
+    tp = None if tau_prev is None else _c(tau_prev, np.int32)
+    _check(_lib().oracle_draft_step(batch, draft.shape[1], _p(cu_B), _p(draft),
+                                    _p(uniforms), uniforms.shape[1], _p(dec), _p(tp),
+                                    _p(toks), _p(tau), _p(conf)), "oracle_draft_step")
     return dict(draft_tokens=toks, tau=tau, confidence=conf)
+
+
+def commit(cu_B, tau, n_accept, token, pos, block_tokens, decided, lens):
+    """Commit after a pass of the blockwise loop; returns dict(block_tokens,
+    decided, lens, done) (new arrays; the inputs are not modified)."""
+    cu_B, tau = _c(cu_B, np.int32), _c(tau, np.int32)
+    batch = len(cu_B) - 1
+    bt = _c(block_tokens, np.int32).copy()
+    dec = _c(decided, np.int32).copy()
+    ln = _c(lens, np.int32).copy()
+    done = np.zeros(batch, np.int32)
+    _check(_lib().oracle_commit(batch, _p(cu_B), _p(tau), _p(_c(n_accept, np.int32)),
+                                _p(_c(token, np.int32)), _p(_c(pos, np.int32)), _p(bt),
+                                _p(dec), _p(ln), _p(done)), "oracle_commit")
+    return dict(block_tokens=bt, decided=dec, lens=ln, done=done)
 
 
 def residual(target_row, draft_row):

@@ -103,6 +103,9 @@ double oracle_residual(int V, const double *target, const double *draft, double 
  *   draft_tokens:  [sum B_b], tau: [sum B_b]
  *   uniforms:      [batch][u_stride] in [0,1): u[t-1] tests step t,
  *                  u[B_b] draws the residual token.
+ *   first_step:    [batch] or NULL (1): the walk starts at this step
+ *                  (1..B_b+1); earlier steps are positions decided in
+ *                  earlier passes of the block, counted as accepted.
  * Outputs per sequence: n_accept (accepted prefix length in temporal
  * order), token (resampled token at the first rejection, -1 if all were
  * accepted), pos (response position of that rejection, -1 if none).
@@ -114,29 +117,41 @@ double oracle_residual(int V, const double *target, const double *draft, double 
 int oracle_accept(int batch, int V, const int *cu_B, const double *target,
                   const double *draft, const int *draft_tokens,
                   const int *tau, const float *uniforms, int u_stride,
-                  int *n_accept, int *token, int *pos,
+                  const int *first_step, int *n_accept, int *token, int *pos,
                   double *accept_margin, double *resample_margin,
                   int n_threads);
 
 /* Greedy verification: step t accepts iff its draft token is the target's
  * argmax (smallest index among equal maxima); the first rejection emits that
- * argmax.  Uniforms and draft logits are not used. */
+ * argmax.  Uniforms and draft logits are not used.  first_step as above. */
 int oracle_accept_greedy(int batch, int V, const int *cu_B, const double *target,
-                         const int *draft_tokens, const int *tau,
+                         const int *draft_tokens, const int *tau, const int *first_step,
                          int *n_accept, int *token, int *pos);
 
 /* Sample matching: step t draws y_t from p by inverse CDF with u[t-1] and
- * accepts iff y_t is the draft token; the first rejection emits y_t. */
+ * accepts iff y_t is the draft token; the first rejection emits y_t.
+ * first_step as above. */
 int oracle_accept_match(int batch, int V, const int *cu_B, const double *target,
                         const int *draft_tokens, const int *tau, const float *uniforms,
-                        int u_stride, int *n_accept, int *token, int *pos);
+                        int u_stride, const int *first_step, int *n_accept, int *token,
+                        int *pos);
 
-/* The draft-side step: each slot samples its token from the draft softmax by
- * inverse CDF with u[k]; tau orders the slots by that token's draft
- * probability (most confident first, ties in position order). */
+/* The draft-side step: each open slot samples its token from the draft
+ * softmax by inverse CDF with u[k]; tau orders the open slots by the row's
+ * largest draft probability (most confident first, ties in position order)
+ * after the decided[b] steps decided in earlier passes of the block, which
+ * keep their tokens and labels (from tau_prev).  decided == NULL: all open. */
 int oracle_draft_step(int batch, int V, const int *cu_B, const double *draft,
-                      const float *uniforms, int u_stride, int *draft_tokens, int *tau,
-                      double *confidence);
+                      const float *uniforms, int u_stride, const int *decided,
+                      const int *tau_prev, int *draft_tokens, int *tau, double *confidence);
+
+/* Commit after a pass of the blockwise loop: the drawn token goes to
+ * block_tokens at pos, decided[b] becomes the count of decided positions,
+ * and a block whose positions are all decided by a pass that drew nothing
+ * closes (lens[b] += B_b, decided[b] = 0, done[b] = 1). */
+int oracle_commit(int batch, const int *cu_B, const int *tau, const int *n_accept,
+                  const int *token, const int *pos, int *block_tokens, int *decided,
+                  int *lens, int *done);
 
 #ifdef __cplusplus
 }
