@@ -50,6 +50,9 @@ def _lib():
         lib.oracle_accept_match.argtypes = [I, I, P, P, P, P, P, I, P, P, P, P]
         lib.oracle_draft_step.argtypes = [I, I, P, P, P, I, P, P, P, P, P]
         lib.oracle_commit.argtypes = [I, P, P, P, P, P, P, P, P, P]
+        lib.oracle_graph_mask_entry.argtypes = [I, I, I, I, I]
+        lib.oracle_verify_attn_graph_seq.argtypes = [I, I, I, I, I, I, D, D, P, P, P, P, P,
+                                                     P]
         lib.oracle_residual.argtypes = [I, P, P, P]
         lib.oracle_residual.restype = D
         _LIB = lib
@@ -247,6 +250,39 @@ def commit(cu_B, tau, n_accept, token, pos, block_tokens, decided, lens):
                                 _p(_c(token, np.int32)), _p(_c(pos, np.int32)), _p(bt),
                                 _p(dec), _p(ln), _p(done)), "oracle_commit")
     return dict(block_tokens=bt, decided=dec, lens=ln, done=done)
+
+
+def graph_mask(P, n_nodes, node_size):
+    """The draft-graph verification mask of the new rows, uint8
+    [n_nodes * node_size, P + n_nodes * node_size], entry by entry."""
+    T = n_nodes * node_size
+    m = np.zeros((T, P + T), np.uint8)
+    f = _lib().oracle_graph_mask_entry
+    for r in range(T):
+        for c in range(P + T):
+            m[r, c] = f(P, n_nodes, node_size, r, c)
+    return m
+
+
+def verify_attn_graph_seq(q, k_prompt, v_prompt, k_new, v_new, node_size, rope_base,
+                          sm_scale):
+    """Attention of one sequence's candidate nodes (see simsd_oracle.h):
+    q [T, Hq, hd], k_new / v_new [T, Hkv, hd] raw, node-major; prompt keys
+    rotated.  Returns [T, Hq, hd]."""
+    q = _c(q, np.float64)
+    k_new, v_new = _c(k_new, np.float64), _c(v_new, np.float64)
+    T, Hq, hd = q.shape
+    if T % node_size:
+        raise ValueError("the rows are not whole nodes")
+    P = 0 if k_prompt is None else k_prompt.shape[0]
+    kp = None if P == 0 else _c(k_prompt, np.float64)
+    vp = None if P == 0 else _c(v_prompt, np.float64)
+    out = np.empty_like(q)
+    _check(_lib().oracle_verify_attn_graph_seq(
+        P, T // node_size, node_size, Hq, k_new.shape[1], hd, float(rope_base),
+        float(sm_scale), _p(q), _p(kp), _p(vp), _p(k_new), _p(v_new), _p(out)),
+        "oracle_verify_attn_graph_seq")
+    return out
 
 
 def residual(target_row, draft_row):

@@ -139,3 +139,73 @@ int oracle_verify_attn(int batch, const int *lens, const int *cu_B, int Hq,
   free(prompt_off);
   return rc;
 }
+
+/* ------------------------------------------------------------------------
+ * Spiffy (gist.science, paper 2509.18085), "Metodologia: Spiffy": draft
+ * states form a directed graph (a block at timestep t_a is a parent of one
+ * at t_b = t_a - 1 whose unmasked tokens are a superset of its own), and
+ * verification evaluates several draft candidates in parallel under a
+ * custom blockwise attention mask.  Reading taken: each node of the graph
+ * is a complete candidate state of the block (node_size tokens, unmasked
+ * or [MASK]); the section holds n_nodes such copies after the prompt; a
+ * row of node n attends to the whole prompt and to every token of node n
+ * (a dLLM attends bidirectionally within its block), and to no token of
+ * another node -- a child already holds its parent's unmasked tokens, so
+ * the parent set orders the acceptance walk, not the mask.  Every node's
+ * token k sits at position P + k (each node is a copy of the block). */
+int oracle_graph_mask_entry(int P, int n_nodes, int node_size, int r, int c) {
+  if (r < 0 || r >= n_nodes * node_size || c < 0 || c >= P + n_nodes * node_size) return 0;
+  if (c < P) return 1;
+  return (c - P) / node_size == r / node_size;
+}
+
+int oracle_verify_attn_graph_seq(int P, int n_nodes, int node_size, int Hq, int Hkv, int hd,
+                                 double rope_base, double sm_scale, const double *q,
+                                 const double *k_prompt, const double *v_prompt,
+                                 const double *k_new, const double *v_new, double *out) {
+  if (P < 0 || n_nodes < 1 || node_size < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ||
+      hd < 2 || hd % 2 != 0 || !q || !k_new || !v_new || !out ||
+      (P > 0 && (!k_prompt || !v_prompt)))
+    return ORACLE_ERR_ARG;
+  const int T = n_nodes * node_size, L = P + T, G = Hq / Hkv;
+  int *pos = (int *)malloc(sizeof(int) * (size_t)T);
+  double *k_rot = (double *)malloc(sizeof(double) * (size_t)T * Hkv * hd);
+  double *qr = (double *)malloc(sizeof(double) * (size_t)hd);
+  double *score = (double *)malloc(sizeof(double) * (size_t)L);
+  if (!pos || !k_rot || !qr || !score) {
+    free(pos); free(k_rot); free(qr); free(score);
+    return ORACLE_ERR_ARG;
+  }
+  for (int j = 0; j < T; ++j) pos[j] = P + j % node_size;
+  oracle_rope(k_new, T, Hkv, hd, pos, rope_base, k_rot);
+  for (int r = 0; r < T; ++r) {
+    for (int h = 0; h < Hq; ++h) {
+      const int g = h / G;
+      oracle_rope(q + ((size_t)r * Hq + h) * hd, 1, 1, hd, &pos[r], rope_base, qr);
+      double m = -INFINITY;
+      for (int c = 0; c < L; ++c) {
+        if (!oracle_graph_mask_entry(P, n_nodes, node_size, r, c)) { score[c] = -INFINITY; continue; }
+        const double *kc = (c < P) ? k_prompt + ((size_t)c * Hkv + g) * hd
+                                   : k_rot + ((size_t)(c - P) * Hkv + g) * hd;
+        double sc = 0.0;
+        for (int d = 0; d < hd; ++d) sc += qr[d] * kc[d];
+        score[c] = sc * sm_scale;
+        if (score[c] > m) m = score[c];
+      }
+      double denom = 0.0;
+      for (int c = 0; c < L; ++c)
+        if (score[c] != -INFINITY) denom += exp(score[c] - m);
+      double *o = out + ((size_t)r * Hq + h) * hd;
+      for (int d = 0; d < hd; ++d) o[d] = 0.0;
+      for (int c = 0; c < L; ++c) {
+        if (score[c] == -INFINITY) continue;
+        const double w = exp(score[c] - m) / denom;
+        const double *vc = (c < P) ? v_prompt + ((size_t)c * Hkv + g) * hd
+                                   : v_new + ((size_t)(c - P) * Hkv + g) * hd;
+        for (int d = 0; d < hd; ++d) o[d] += w * vc[d];
+      }
+    }
+  }
+  free(pos); free(k_rot); free(qr); free(score);
+  return ORACLE_OK;
+}

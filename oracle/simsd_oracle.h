@@ -92,6 +92,22 @@ int oracle_verify_attn(int batch, const int *lens, const int *cu_B, int Hq,
                        const double *k_new, const double *v_new,
                        double *out, int n_threads);
 
+/* Spiffy's draft-graph verification (reading: each node a complete
+ * candidate state of the block).  Mask entry for new row r (node r /
+ * node_size) and column c: 1 for every prompt column and for the columns
+ * of the same node, else 0. */
+int oracle_graph_mask_entry(int P, int n_nodes, int node_size, int r, int c);
+
+/* Attention of one sequence's n_nodes x node_size new rows under that mask,
+ * fp64.  q [T][Hq][hd], k_new / v_new [T][Hkv][hd] raw (T = n_nodes *
+ * node_size, node-major); k_prompt / v_prompt [P][Hkv][hd] with the keys
+ * rotated; every node's token k is rotated at position P + k.
+ * out [T][Hq][hd]. */
+int oracle_verify_attn_graph_seq(int P, int n_nodes, int node_size, int Hq, int Hkv, int hd,
+                                 double rope_base, double sm_scale, const double *q,
+                                 const double *k_prompt, const double *v_prompt,
+                                 const double *k_new, const double *v_new, double *out);
+
 /* Residual of one slot: r[v] = max(0, p(v) - q(v)) with p, q the softmax of
  * the target and draft logit rows (p itself when that is empty); returns
  * S = sum r.  The acceptance walk draws its token from r / S. */
