@@ -117,8 +117,12 @@ simsd_status simsd_layout(int32_t prompt_len, int32_t B, const int32_t *tau,
  *   out          device [T][Hq][hd]    attention output of every new row
  * dtype applies to q, k/v (new and cache) and out.
  * Host-side fields (total_B, B_max, max_pages_per_seq) must agree with the
- * device arrays; the device trusts them and tau (a wrong tau gives a wrong
- * mask, never an out-of-bounds access; lens[b]+2B_b must fit the table).
+ * device arrays.  A sequence whose device arrays disagree with them (cu_B
+ * not within 0..total_B, B_b outside 1..B_max, lens[b]+2B_b beyond the
+ * table row, a page id outside the cache) sets the status word's bad-input
+ * bit (2) and is skipped: nothing is read or written out of range for it.
+ * tau is trusted: a wrong tau gives a wrong mask, never an out-of-bounds
+ * access.
  * ---------------------------------------------------------------------- */
 typedef struct {
   int32_t batch;
@@ -145,6 +149,24 @@ typedef struct {
   void *out;
   void *workspace;            /* device, 256-byte aligned                   */
   size_t workspace_bytes;
+  int32_t wait_polls;         /* polls a kernel's bounded wait makes before
+                                 it gives up: 0 (a zero-filled descriptor)
+                                 selects the default 2^24; a negative value
+                                 gives up at once, which runs the timeout
+                                 path (status bit 0, nothing written to the
+                                 cache; out undefined) -- for tests        */
+  int32_t node_size;          /* 0: SimSD's paired layout under the temporal
+                                 mask (above).  > 0: Spiffy's draft-graph
+                                 verification: a sequence's 2B_b new tokens
+                                 are 2B_b / node_size candidate states of the
+                                 block (nodes of node_size <= 32 tokens, node
+                                 after node); token k of every node sits at
+                                 position lens[b] + k; a row attends to the
+                                 whole prompt and to every token of its own
+                                 node, nothing of another node; tau is not
+                                 read (may be NULL).  A sequence whose 2B_b
+                                 is not a multiple of node_size sets the
+                                 bad-input bit and is skipped                */
 } simsd_verify_desc;
 
 /* Bytes of workspace simsd_verify_attn needs for these sizes (reads only
@@ -212,15 +234,26 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * y (u[B_b] unused, draft logits not read and may be NULL).  A separate
  * kernel: one pass over the target rows, then a scan of one vocabulary
  * slice at a rejection.
- * Kernel: K4, one thread-block cluster of C CTAs per sequence (C <= 16,
+ * Kernels (sampling rule): K4a, a pass over (row, 8192-entry chunk) items
+ * on every SM, writes each chunk's maximum and sum of exponentials of both
+ * rows of every slot, and the logits at the draft tokens, to the
+ * workspace; K4b, one thread-block cluster of C CTAs per sequence (C <= 16,
  * chosen at launch from the batch size and the clusters the device can
- * hold at once), each CTA owning 1/C of the vocabulary: max and sum of
- * exponentials of both rows of every slot, the walk of the steps, and at a
- * rejection the residual masses and the inverse-CDF draw -- all on chip.
+ * hold at once), each CTA owning 1/C of the vocabulary, merges them, walks
+ * the steps, and at a rejection streams the rejected slot's two rows for
+ * the residual masses and the inverse-CDF draw.  With a workspace of only
+ * the status word, or with `decided` (the blockwise loop: decided slots'
+ * rows are not read), the cluster kernel streams the rows itself in one
+ * launch instead.
  *   target_logits, draft_logits device [total_B][vocab] (dtype); row k of
  *                sequence b (at cu_B[b]+k) holds the logits read at D~_k
  *   draft_tokens device int32[total_B] in [0, vocab); a token outside
  *                sets the status word's bad-input bit and its step rejects
+ * A sequence whose cu_B entries fall outside 0..total_B, whose B_b is
+ * outside 1..B_max, or whose tau is not a permutation of 1..B_b sets the
+ * bad-input bit and gets n_accept = 0, token = -1, pos = -1 without reading
+ * its logits.  Logits must not be NaN (-inf is allowed; the greedy rule
+ * gives index 0 for a row with no larger entry).
  *   tau, cu_B    device, as for simsd_verify_attn
  *   uniforms     device float32[batch][B_max+1], values in [0, 1)
  *   n_accept     device int32[batch] out: accepted prefix length (0..B_b)
@@ -232,8 +265,11 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * Limits: 1 <= vocab <= 2^21; batch <= 65535.  Rows whose byte length is
  * a multiple of 16 (and 16-byte aligned logits) are streamed by bulk
  * copies; other vocabularies take a slower element-wise copy.
- * Workspace: the status word only (simsd_accept_workspace_size returns 256
- * for every valid size).
+ * Workspace: simsd_accept_workspace_size returns the size of the
+ * two-kernel path (sampling rule: 256 + 2 total_B ceil(vocab/8192) * 8 +
+ * 2 total_B * 4 bytes, rounded up to 256-byte multiples; 256 for the other
+ * rules); any workspace of at least 256 bytes is accepted, and one smaller
+ * than that size runs the single-launch path.
  * Errors: SIMSD_ERR_NULL, SIMSD_ERR_SHAPE (also: an unknown rule, or a
  * temperature that is negative or not finite), SIMSD_ERR_DTYPE,
  * SIMSD_ERR_WORKSPACE, SIMSD_ERR_CUDA.
@@ -263,16 +299,127 @@ typedef struct {
   size_t workspace_bytes;
   simsd_accept_rule rule;     /* 0 (a zero-filled descriptor): sampling      */
   float temperature;          /* > 0; 0 selects 1 (a zero-filled descriptor
-                                 keeps the standard rule)                    */
+                                 keeps the standard rule); the logits are
+                                 divided by this float's exact value         */
+  int32_t wait_polls;         /* as in simsd_verify_desc; a sequence whose
+                                 wait gave up gets n_accept = 0, token = -1,
+                                 pos = -1                                    */
+  const int32_t *decided;     /* device int32[batch] or NULL (all 0): steps
+                                 1..decided[b] belong to positions decided
+                                 in earlier passes of the block (the
+                                 blockwise loop, simsd_commit); the walk
+                                 starts at step decided[b]+1 and counts the
+                                 earlier ones as accepted (0..B_b; B_b: no
+                                 step is tested, n_accept = B_b)             */
 } simsd_accept_desc;
 
 size_t simsd_accept_workspace_size(const simsd_accept_desc *d);
 simsd_status simsd_accept(const simsd_accept_desc *d, void *stream);
 
 /* Same as simsd_accept, recording events (cudaEvent_t or NULL) on `stream`:
- * events[0] before K4, [1] and [2] after it. */
+ * events[0] before K4, [1] after K4a (the chunk pass; recorded right after
+ * [0] on the single-launch path), [2] after K4b. */
 simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
                                 void *const events[3]);
+
+/* ------------------------------------------------------------------------
+ * simsd_draft_step -- section 4, drafting: the draft proposes the section's
+ * tokens and their temporal order.  For each open slot k of sequence b
+ * (every slot when decided is NULL; else those with tau_prev[k] >
+ * decided[b]): q = softmax(draft row k / T); the token is the smallest v
+ * whose running mass exceeds u[k] (inverse CDF; the last v with q > 0 if
+ * rounding leaves none); the open slots take the step labels
+ * decided[b]+1 .. B_b in order of the row's largest probability, max_v q(v)
+ * (most confident first, equal ones in position order).  The order depends
+ * on the draft rows only, not on the drawn tokens, which keeps the walk's
+ * rejection sampling exact.  Decided slots keep their token and label.
+ *   draft_logits device [total_B][vocab] (dtype)
+ *   uniforms     device float32[batch][B_max], values in [0, 1): u[k]
+ *                draws slot k
+ *   decided      device int32[batch] or NULL
+ *   tau_prev     device int32[total_B], read when decided is not NULL: the
+ *                block's labels so far (decided slots: 1..decided[b])
+ *   tokens       device int32[total_B] in/out: decided slots are kept,
+ *                open slots get their drawn token
+ *   tau          device int32[total_B] out (may be tau_prev itself)
+ *   confidence   device float32[total_B] out or NULL: max_v q(v) of open
+ *                slots, -1 at decided ones
+ * Kernel: one thread-block cluster per sequence (as simsd_accept's rules):
+ * one pass over every open row for its normaliser, then each slot's
+ * inverse-CDF scan in the vocabulary slice holding its u*S.
+ * Errors: as simsd_accept (SIMSD_ERR_SHAPE also for a negative or
+ * non-finite temperature).  Bad device arrays (cu_B, decided outside
+ * 0..B_b, tau_prev not a permutation) set the bad-input bit and leave the
+ * sequence's tokens and tau unwritten.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t batch;
+  int32_t vocab;
+  int32_t total_B;            /* host copy                                  */
+  int32_t B_max;              /* host copy, 1..32                           */
+  simsd_dtype dtype;          /* of the logits                              */
+  float temperature;          /* > 0; 0 selects 1                           */
+  const void *draft_logits;
+  const int32_t *cu_B;
+  const float *uniforms;
+  const int32_t *decided;
+  const int32_t *tau_prev;
+  int32_t *tokens;
+  int32_t *tau;
+  float *confidence;
+  void *workspace;            /* device, 256-byte aligned (status word)     */
+  size_t workspace_bytes;
+} simsd_draft_desc;
+
+size_t simsd_draft_workspace_size(const simsd_draft_desc *d);
+simsd_status simsd_draft_step(const simsd_draft_desc *d, void *stream);
+
+/* ------------------------------------------------------------------------
+ * simsd_commit -- section 4: "the longest accepted prefix is committed, and
+ * the process is repeated", with the KV cache and blockwise decoding
+ * (section "Contributions").  One pass of the blockwise loop is
+ * simsd_draft_step -> simsd_verify_attn -> simsd_accept (decided) ->
+ * simsd_commit.  For sequence b, with the walk's n_accept, token, pos:
+ *   - positions with tau <= n_accept stay decided with their tokens;
+ *   - a rejection (pos >= 0) decides position pos with the drawn token
+ *     (written to tokens[pos]); it holds label n_accept + 1, so
+ *     decided[b] = n_accept + 1;
+ *   - every position decided by a pass that drew nothing (n_accept = B_b,
+ *     pos = -1): the cache slots [lens, lens+B_b) written by that pass's
+ *     verification hold the final tokens' keys and values, so the block
+ *     closes: lens[b] += B_b, decided[b] = 0, done[b] = 1 (the mask-slot
+ *     slots past them are free again).  A block whose last position was
+ *     decided by a draw stays open with decided[b] = B_b: its next pass
+ *     tests nothing, rewrites the section's keys and values from the final
+ *     tokens, and closes it.
+ *   tau, cu_B, n_accept, token, pos  device, as written by simsd_accept
+ *   tokens   device int32[total_B] in/out (the pass's data-section tokens)
+ *   decided  device int32[batch] in/out
+ *   lens     device int32[batch] in/out
+ *   done     device int32[batch] out
+ * A sequence whose arrays are inconsistent (cu_B outside 0..total_B, B_b
+ * outside 1..B_max, a walk that does not fit its tau) sets the bad-input
+ * bit and is left unchanged (done = 0).  One thread per sequence.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  int32_t batch;
+  int32_t total_B;            /* host copy                                  */
+  int32_t B_max;              /* host copy, 1..32                           */
+  const int32_t *cu_B;
+  const int32_t *tau;
+  const int32_t *n_accept;
+  const int32_t *token;
+  const int32_t *pos;
+  int32_t *tokens;
+  int32_t *decided;
+  int32_t *lens;
+  int32_t *done;
+  void *workspace;            /* device, 256-byte aligned (status word)     */
+  size_t workspace_bytes;
+} simsd_commit_desc;
+
+size_t simsd_commit_workspace_size(const simsd_commit_desc *d);
+simsd_status simsd_commit(const simsd_commit_desc *d, void *stream);
 
 /* ------------------------------------------------------------------------
  * simsd_accept_noalloc -- simsd_accept for callers that cannot allocate
@@ -286,9 +433,11 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
  * its scratch in a static device array of SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES
  * bytes that every GPU loading the library holds until the process exits.
  *   - It calls no cudaMalloc, cudaFree or allocating library routine.
- *   - Sizes whose scratch (what simsd_accept_workspace_size reports) exceeds
- *     the array are rejected with SIMSD_ERR_WORKSPACE before any launch
- *     (none at present: the scratch is one status word for every size).
+ *   - It runs the single-launch path, whose scratch is one status word
+ *     for every size (the two-kernel path's chunk partials grow with the
+ *     batch and take that path only where they fit the array); a scratch
+ *     need beyond the array would be rejected with SIMSD_ERR_WORKSPACE
+ *     before any launch.
  *   - The first call on each device looks up the array's device address
  *     (once per device, with that device current); make that first call
  *     before any stream capture.
@@ -298,6 +447,9 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
  *     threads -- race on it: serialise them.
  *   - The kernels' status word lives in that array, so simsd_read_status
  *     cannot read it; device-detected input errors are not reported here.
+ *   - The address is cached per device ordinal for the life of the process:
+ *     it assumes the device's primary context (the one the CUDA runtime
+ *     uses) and no cudaDeviceReset in between.
  * ---------------------------------------------------------------------- */
 #define SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES ((size_t)4096)
 simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream);

@@ -31,7 +31,7 @@ class VerifyDesc(ctypes.Structure):
                 ("q", _vp), ("k_cache", _vp), ("v_cache", _vp), ("block_table", _vp),
                 ("k_new", _vp), ("v_new", _vp), ("tau", _vp), ("lens", _vp),
                 ("cu_B", _vp), ("out", _vp), ("workspace", _vp),
-                ("workspace_bytes", _sz)]
+                ("workspace_bytes", _sz), ("wait_polls", _i32), ("node_size", _i32)]
 
 
 class AppendDesc(ctypes.Structure):
@@ -47,7 +47,23 @@ class AcceptDesc(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("target_logits", _vp), ("draft_logits", _vp),
                 ("draft_tokens", _vp), ("tau", _vp), ("cu_B", _vp), ("uniforms", _vp),
                 ("n_accept", _vp), ("token", _vp), ("pos", _vp), ("workspace", _vp),
-                ("workspace_bytes", _sz), ("rule", ctypes.c_int), ("temperature", ctypes.c_float)]
+                ("workspace_bytes", _sz), ("rule", ctypes.c_int), ("temperature", ctypes.c_float),
+                ("wait_polls", _i32), ("decided", _vp)]
+
+
+class DraftDesc(ctypes.Structure):
+    _fields_ = [("batch", _i32), ("vocab", _i32), ("total_B", _i32), ("B_max", _i32),
+                ("dtype", ctypes.c_int), ("temperature", _f32), ("draft_logits", _vp),
+                ("cu_B", _vp), ("uniforms", _vp), ("decided", _vp), ("tau_prev", _vp),
+                ("tokens", _vp), ("tau", _vp), ("confidence", _vp), ("workspace", _vp),
+                ("workspace_bytes", _sz)]
+
+
+class CommitDesc(ctypes.Structure):
+    _fields_ = [("batch", _i32), ("total_B", _i32), ("B_max", _i32), ("cu_B", _vp),
+                ("tau", _vp), ("n_accept", _vp), ("token", _vp), ("pos", _vp),
+                ("tokens", _vp), ("decided", _vp), ("lens", _vp), ("done", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz)]
 
 
 class SimsdError(RuntimeError):
@@ -87,6 +103,14 @@ def lib():
         L.simsd_accept_timed.argtypes = [ctypes.POINTER(AcceptDesc), _vp, ctypes.POINTER(_vp)]
         L.simsd_accept_noalloc.restype = ctypes.c_int
         L.simsd_accept_noalloc.argtypes = [ctypes.POINTER(AcceptDesc), _vp]
+        L.simsd_draft_workspace_size.restype = _sz
+        L.simsd_draft_workspace_size.argtypes = [ctypes.POINTER(DraftDesc)]
+        L.simsd_draft_step.restype = ctypes.c_int
+        L.simsd_draft_step.argtypes = [ctypes.POINTER(DraftDesc), _vp]
+        L.simsd_commit_workspace_size.restype = _sz
+        L.simsd_commit_workspace_size.argtypes = [ctypes.POINTER(CommitDesc)]
+        L.simsd_commit.restype = ctypes.c_int
+        L.simsd_commit.argtypes = [ctypes.POINTER(CommitDesc), _vp]
         L.simsd_read_status.restype = ctypes.c_int
         L.simsd_read_status.argtypes = [_vp, _vp, ctypes.POINTER(ctypes.c_uint32)]
         _LIB = L
@@ -132,8 +156,11 @@ def layout(prompt_len, tau, with_mask=True):
 
 
 def _verify_desc(q, k_cache, v_cache, block_table, k_new, v_new, tau, lens, cu_B,
-                 out, total_B, B_max, rope_base, sm_scale, workspace=None):
+                 out, total_B, B_max, rope_base, sm_scale, workspace=None, wait_polls=0,
+                 node_size=0):
     d = VerifyDesc()
+    d.wait_polls = int(wait_polls)
+    d.node_size = int(node_size)
     d.batch = lens.shape[0]
     d.num_q_heads = q.shape[1]
     d.num_kv_heads = k_new.shape[1]
@@ -156,9 +183,9 @@ def _verify_desc(q, k_cache, v_cache, block_table, k_new, v_new, tau, lens, cu_B
 
 
 def verify_workspace_size(q, k_cache, v_cache, block_table, k_new, v_new, tau,
-                          lens, cu_B, out, total_B, B_max, rope_base, sm_scale):
+                          lens, cu_B, out, total_B, B_max, rope_base, sm_scale, node_size=0):
     d = _verify_desc(q, k_cache, v_cache, block_table, k_new, v_new, tau, lens,
-                     cu_B, out, total_B, B_max, rope_base, sm_scale)
+                     cu_B, out, total_B, B_max, rope_base, sm_scale, node_size=node_size)
     n = lib().simsd_verify_workspace_size(ctypes.byref(d))
     if n == 0:
         raise SimsdError(2, "simsd_verify_workspace_size")
@@ -174,11 +201,14 @@ def _events(evs, n):
 
 def verify_attn(q, k_cache, v_cache, block_table, k_new, v_new, tau, lens, cu_B,
                 out, workspace, total_B, B_max, rope_base, sm_scale, stream=None,
-                events=None):
+                events=None, wait_polls=0, node_size=0):
     """simsd_verify_attn on the current (or given) torch stream.  events:
-    optional 4 recorded torch.cuda.Event objects (see simsd_verify_attn_timed)."""
+    optional 4 recorded torch.cuda.Event objects (see simsd_verify_attn_timed).
+    wait_polls: the descriptor field (0: default limit; < 0: give up at once).
+    node_size > 0: the draft-graph layout (tau may be None)."""
     d = _verify_desc(q, k_cache, v_cache, block_table, k_new, v_new, tau, lens,
-                     cu_B, out, total_B, B_max, rope_base, sm_scale, workspace)
+                     cu_B, out, total_B, B_max, rope_base, sm_scale, workspace, wait_polls,
+                     node_size)
     if events is None:
         _check(lib().simsd_verify_attn(ctypes.byref(d), _stream(stream)), "simsd_verify_attn")
     else:
@@ -204,8 +234,11 @@ def prompt_append(k, v, start, cu_n, k_cache, v_cache, block_table, rope_base,
 
 
 def _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
-                 pos, total_B, B_max, workspace=None, rule=SIMSD_ACCEPT_SAMPLE, temperature=1.0):
+                 pos, total_B, B_max, workspace=None, rule=SIMSD_ACCEPT_SAMPLE, temperature=1.0,
+                 wait_polls=0, decided=None):
     d = AcceptDesc()
+    d.wait_polls = int(wait_polls)
+    d.decided = _ptr(decided)
     d.rule = int(rule)
     d.temperature = float(temperature)
     d.batch = cu_B.shape[0] - 1
@@ -236,11 +269,12 @@ def accept_workspace_size(target, draft, draft_tokens, tau, cu_B, uniforms, n_ac
 
 def accept(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token, pos,
            workspace, total_B, B_max, stream=None, events=None, rule=SIMSD_ACCEPT_SAMPLE,
-           temperature=1.0):
+           temperature=1.0, wait_polls=0, decided=None):
     """simsd_accept; events: optional 3 recorded torch.cuda.Event objects;
-    rule SIMSD_ACCEPT_GREEDY takes draft = uniforms = None."""
+    rule SIMSD_ACCEPT_GREEDY takes draft = uniforms = None; wait_polls as for
+    verify_attn; decided: int32 [batch] steps decided in earlier passes."""
     d = _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
-                     pos, total_B, B_max, workspace, rule, temperature)
+                     pos, total_B, B_max, workspace, rule, temperature, wait_polls, decided)
     if events is None:
         _check(lib().simsd_accept(ctypes.byref(d), _stream(stream)), "simsd_accept")
     else:
@@ -256,6 +290,41 @@ def accept_noalloc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, t
                      pos, total_B, B_max, None, rule, temperature)
     _check(lib().simsd_accept_noalloc(ctypes.byref(d), _stream(stream)),
            "simsd_accept_noalloc")
+
+
+def _status_ws(workspace):
+    return _ptr(workspace), (0 if workspace is None else workspace.numel() * workspace.element_size())
+
+
+def draft_step(draft, cu_B, uniforms, tokens, tau, workspace, total_B, B_max, decided=None,
+               tau_prev=None, confidence=None, temperature=1.0, stream=None):
+    """simsd_draft_step: tokens (in/out) and tau (out) of every sequence's
+    open slots; uniforms float32 [batch, B_max]."""
+    d = DraftDesc()
+    d.batch = cu_B.shape[0] - 1
+    d.vocab = draft.shape[1]
+    d.total_B, d.B_max = int(total_B), int(B_max)
+    d.dtype = _dtype_code(draft)
+    d.temperature = float(temperature)
+    d.draft_logits, d.cu_B, d.uniforms = _ptr(draft), _ptr(cu_B), _ptr(uniforms)
+    d.decided, d.tau_prev = _ptr(decided), _ptr(tau_prev)
+    d.tokens, d.tau, d.confidence = _ptr(tokens), _ptr(tau), _ptr(confidence)
+    d.workspace, d.workspace_bytes = _status_ws(workspace)
+    _check(lib().simsd_draft_step(ctypes.byref(d), _stream(stream)), "simsd_draft_step")
+
+
+def commit(cu_B, tau, n_accept, token, pos, tokens, decided, lens, done, workspace,
+           total_B, B_max, stream=None):
+    """simsd_commit: applies a pass's walk to the block state (tokens,
+    decided, lens in/out; done out)."""
+    d = CommitDesc()
+    d.batch = cu_B.shape[0] - 1
+    d.total_B, d.B_max = int(total_B), int(B_max)
+    d.cu_B, d.tau, d.n_accept, d.token, d.pos = (_ptr(cu_B), _ptr(tau), _ptr(n_accept),
+                                                  _ptr(token), _ptr(pos))
+    d.tokens, d.decided, d.lens, d.done = _ptr(tokens), _ptr(decided), _ptr(lens), _ptr(done)
+    d.workspace, d.workspace_bytes = _status_ws(workspace)
+    _check(lib().simsd_commit(ctypes.byref(d), _stream(stream)), "simsd_commit")
 
 
 def read_status(workspace, stream=None):

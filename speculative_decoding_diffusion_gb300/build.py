@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libsimsd.so")
-SOURCES = ["api.cu", "rope_append.cu", "attn_tc.cu", "attn_f32.cu", "accept.cu"]
+SOURCES = ["api.cu", "rope_append.cu", "attn_tc.cu", "attn_f32.cu", "accept.cu", "loop.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-Wall", "-I", INCLUDE, "-I", CSRC]

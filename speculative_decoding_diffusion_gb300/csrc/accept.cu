@@ -41,14 +41,18 @@
 // compensated fp32 pairs (two-sum), never fp64 (GB300's fp64 rate is a
 // small fraction of its fp32 rate).  The residual CDF is then within ~1e-6
 // (absolute probability mass) of the exact one.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "vocab.cuh"
 
 namespace simsd {
 namespace {
+
+using namespace vocab;
 
 constexpr int kMaxCluster = 16;                    // CTAs per sequence, at most (over 8: non-portable)
 constexpr int kConsumerWarps = 16;
@@ -71,183 +75,35 @@ static_assert(kConsumers % kMaxCluster == 0 && 32 % kMaxCluster == 0,
 // the main pass's 8 accumulators see the same slots in both rolled halves:
 // (kVecs / 2) vectors of N >= 4 entries are a multiple of 8 entries
 static_assert((kVecs / 2) * 4 % 8 == 0, "accumulator slots repeat every half");
+// the chunk pass (K4a) of the two-kernel path
+// a chunk is one ring stage: kStageBytes / sizeof(T) entries (and a K4b piece)
+constexpr int kAStages = 3;
+constexpr int kAConsumerWarps = 8;
+constexpr int kAConsumers = kAConsumerWarps * 32;
+constexpr int kAThreads = kAConsumers + 32;
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
 constexpr int kMaxVocab = 1 << 21;                 // 8 slices of kMaxPieces pieces of 8192 fp32 entries
-constexpr float kLog2e = 1.4426950408889634f;
+// The residual in target-mass units: with e_t = 2^(x ls - Mt) (so p =
+// e_t / St) and e_d = 2^(y ls - Md) (q = e_d / Sd), S_t max(0, p - q) =
+// max(0, e_t - rho e_d), rho = St / Sd (a pair).  The draw is the same in
+// any common unit, so no normaliser is rounded into the entries.  rho e_d
+// takes a product and one fused multiply-add, the difference its own
+// rounding (no contraction), so identical target and draft rows (rho
+// exactly 1) give an exactly empty residual, and the residual pass and the
+// draw compute the same values.
+__device__ __forceinline__ float draft_mass(float y, float Md, Ff rho, Scale ls) {
+  const float e = rel_exp(y, Md, ls);
+  return __fmaf_rn(e, rho.lo, __fmul_rn(e, rho.hi));
+}
+__device__ __forceinline__ float residual(float et, float ed) { return fmaxf(__fsub_rn(et, ed), 0.f); }
 
-// ------------------------------------------------------------ two-sum pairs
-// value = hi + lo with |lo| <= ulp(hi)/2 (Knuth's two-sum; Dekker's
-// fast-two-sum for the renormalisation).
-struct Ff {
-  float hi, lo;
-};
-__device__ __forceinline__ Ff ff_add(Ff a, Ff b) {
-  const float s = a.hi + b.hi;
-  const float bb = s - a.hi;
-  const float err = (a.hi - (s - bb)) + (b.hi - bb);
-  const float lo = err + a.lo + b.lo;
-  const float hi = s + lo;
-  return Ff{hi, lo - (hi - s)};
-}
-__device__ __forceinline__ Ff ff_of(float x) { return Ff{x, 0.f}; }
-__device__ __forceinline__ Ff ff_neg(Ff a) { return Ff{-a.hi, -a.lo}; }
-__device__ __forceinline__ Ff ff_shfl_xor(Ff a, int m) {
-  return Ff{__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
-}
-__device__ __forceinline__ Ff ff_shfl_up(Ff a, int d) {
-  return Ff{__shfl_up_sync(0xffffffffu, a.hi, d), __shfl_up_sync(0xffffffffu, a.lo, d)};
-}
-__device__ __forceinline__ Ff ff_shfl(Ff a, int l) {
-  return Ff{__shfl_sync(0xffffffffu, a.hi, l), __shfl_sync(0xffffffffu, a.lo, l)};
-}
-// a > u where u is a pair: compare the exact sums' signs
-__device__ __forceinline__ bool ff_gt(Ff a, Ff u) {
-  const Ff d = ff_add(a, ff_neg(u));
-  return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
-}
-
-// 2^x on the MUFU (approximate, ~2 ulp; subnormal results flush to zero).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// 2^(x log2 e - R): the argument rounded once.
-// (ls = log2(e) / temperature: the logits' scale into log2 units)
-__device__ __forceinline__ float rel_exp(float x, float R, float ls) { return ex2(fmaf(x, ls, -R)); }
-
-// p(v) = 2^(x log2 e - M) / S with the reciprocal normaliser, and the
-// residual max(0, p - q): separately rounded (no fused multiply-subtract),
-// so identical target and draft rows give p == q and an exactly empty
-// residual, and the residual pass and the draw compute the same values.
-__device__ __forceinline__ float prob(float x, float M, float inv_s, float ls) {
-  return __fmul_rn(rel_exp(x, M, ls), inv_s);
-}
-__device__ __forceinline__ float residual(float p, float q) { return fmaxf(__fsub_rn(p, q), 0.f); }
-
-__device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 __device__ __forceinline__ void consumers_sync() { named_sync(1, kConsumers); }
-
-// ---------------------------------------------------------------- cluster
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-  cluster_arrive();
-  cluster_wait();
-}
-// Address of the same shared-memory variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t dsmem(const void *p, int rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float2 ld_dsmem2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
-// ---------------------------------------------------------------- logits
-// Raw 16-byte vectors of logits: unpacking, lane-wise maximum, the -inf fill.
-template <typename T> struct Ld;
-template <> struct Ld<float> {
-  static constexpr int N = 4;
-  static constexpr uint32_t kNegInf = 0xff800000u;
-  static __device__ __forceinline__ uint4 neg_inf() { return make_uint4(kNegInf, kNegInf, kNegInf, kNegInf); }
-  static __device__ __forceinline__ float value(float v) { return v; }
-  static __device__ __forceinline__ float neg_inf_elem() { return -INFINITY; }
-  static __device__ __forceinline__ void unpack(uint4 v, float *f) {
-    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
-    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
-  }
-  // the vector at p (16-byte aligned if `aligned`): entries past `valid`
-  // (which may be <= 0) read as -inf
-  static __device__ __forceinline__ uint4 load(const float *p, int valid, bool aligned) {
-    if (aligned && valid >= N) return *reinterpret_cast<const uint4 *>(p);
-    uint32_t r[N];
-#pragma unroll
-    for (int e = 0; e < N; ++e) r[e] = e < valid ? __float_as_uint(p[e]) : kNegInf;
-    return make_uint4(r[0], r[1], r[2], r[3]);
-  }
-  static __device__ __forceinline__ float vmax(const uint4 *w, int n) {
-    float m0 = -INFINITY, m1 = -INFINITY;
-    for (int i = 0; i < n; ++i) {
-      m0 = fmaxf(m0, fmaxf(__uint_as_float(w[i].x), __uint_as_float(w[i].y)));
-      m1 = fmaxf(m1, fmaxf(__uint_as_float(w[i].z), __uint_as_float(w[i].w)));
-    }
-    return fmaxf(m0, m1);
-  }
-};
-template <> struct Ld<__nv_bfloat16> {
-  static constexpr int N = 8;
-  static constexpr uint32_t kNegInf2 = 0xff80ff80u;
-  static __device__ __forceinline__ uint4 neg_inf() { return make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2); }
-  static __device__ __forceinline__ float value(__nv_bfloat16 v) { return __bfloat162float(v); }
-  static __device__ __forceinline__ __nv_bfloat16 neg_inf_elem() { return __ushort_as_bfloat16(0xff80); }
-  static __device__ __forceinline__ void unpack(uint4 v, float *f) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(w[i] << 16);
-      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-  }
-  static __device__ __forceinline__ uint4 load(const __nv_bfloat16 *p, int valid, bool aligned) {
-    if (aligned && valid >= N) return *reinterpret_cast<const uint4 *>(p);
-    uint32_t r[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = 2 * i < valid ? __bfloat16_as_ushort(p[2 * i]) : 0xff80u;
-      const uint32_t hi = 2 * i + 1 < valid ? __bfloat16_as_ushort(p[2 * i + 1]) : 0xff80u;
-      r[i] = lo | (hi << 16);
-    }
-    return make_uint4(r[0], r[1], r[2], r[3]);
-  }
-  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-  }
-  // packed maximum of the bf16 pairs (exact), then of the two halves
-  static __device__ __forceinline__ float vmax(const uint4 *w, int n) {
-    uint32_t m = kNegInf2;
-    for (int i = 0; i < n; ++i) m = max2(m, max2(max2(w[i].x, w[i].y), max2(w[i].z, w[i].w)));
-    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
-  }
-};
-
-// Element e (dynamic) of the N entries held in vector w.
-template <typename T>
-__device__ __forceinline__ float pick(uint4 w, int e) {
-  float f[Ld<T>::N];
-  Ld<T>::unpack(w, f);
-  float v = f[0];
-#pragma unroll
-  for (int i = 1; i < Ld<T>::N; ++i)
-    if (e == i) v = f[i];
-  return v;
-}
 
 // ---------------------------------------------------------------- state
 struct __align__(16) WalkInfo {
   int slot;              // rejected slot (0-based within the sequence), -1: none
   float Mt, Md;          // its references (log2 units)
-  float inv_st, inv_sd;  // reciprocal normalisers
+  Ff rho;                // St / Sd
   float u;               // the residual draw's uniform
   int pad0, pad1;
 };
@@ -256,7 +112,7 @@ struct __align__(16) AccShared {
   uint64_t full[kStages], empty[kStages];
   float2 part_w[kMaxPairs][kConsumerWarps];   // per warp: (R, s) of each (slot, row)
   float2 cpart[kMaxPairs];                    // this CTA's slice: (R, s)
-  float2 norm[kMaxPairs];                     // CTA 0: merged (M, S) of each row
+  float4 norm[kMaxPairs];                     // merged (M, S.hi, S.lo) of each (slot, row)
   float2 xv[kMaxB];                           // logits at the draft token, if in this slice
   float px[kMaxB], qx[kMaxB], u[kMaxB + 1];
   int tau[kMaxB], x[kMaxB], slot_of_step[kMaxB];
@@ -264,7 +120,9 @@ struct __align__(16) AccShared {
   float4 piece_s[kMaxPieces];
   float4 tot;                                 // this slice's residual and target mass
   WalkInfo walk;                              // CTA 0's result, read by every CTA
-  int flag;
+  int flag;                                   // any wait of this CTA gave up
+  int fail1, fail3;                           // ... in phase 1 / phase 3 (read remotely
+                                              // after the barrier closing that phase)
 };
 
 struct AcceptParams {
@@ -274,16 +132,25 @@ struct AcceptParams {
   const int32_t *tau;
   const int32_t *cu_B;
   const float *uniforms;
+  const int32_t *decided;   // steps decided in earlier passes (NULL: none)
   int32_t *n_accept;
   int32_t *token;
   int32_t *pos;
   uint32_t *status;
   int batch, vocab, B_max, total_B;
+  uint32_t polls;  // bounded-wait polls
   int csize;   // CTAs per cluster (one cluster per sequence)
   int per;     // entries per CTA slice (a multiple of 16 bytes' worth)
   int piece;   // entries per ring stage
   int bulk;    // rows 16-byte aligned: bulk copies; else element copies
-  float ls;    // log2(e) / temperature
+  Scale ls;    // log2(e) / temperature
+  // partials mode (the two-kernel path): the per-chunk (reference, sum) of
+  // every row, [2 total_B][nchunks], and each row's logit at its slot's
+  // draft token, [2 total_B] (both written by the chunk pass); NULL: this
+  // kernel streams the rows itself.  Slices are then cpc whole chunks.
+  const float2 *part;
+  const float *xlogit;
+  int nchunks, cpc;
 };
 
 // Producer warp: one piece of a row slice into a ring stage, completion on
@@ -339,10 +206,13 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
   const bool producer = warp == kConsumerWarps;
-  const float ls = a.ls;
+  const Scale ls = a.ls;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
-  const bool valid = B >= 1 && B <= kMaxB;  // the same in every CTA of the cluster
+  const int dcd = a.decided ? __ldg(a.decided + b) : 0;   // the walk starts at step dcd + 1
+  // the same in every CTA of the cluster; rows c0 .. c0+B-1 exist
+  const bool valid = B >= 1 && B <= a.B_max && c0 >= 0 && c0 + B <= a.total_B && dcd >= 0 &&
+                     dcd <= B;
   const int s0 = min(a.vocab, rank * a.per);
   const int len = min(a.vocab, s0 + a.per) - s0;
   const int npieces = (len + a.piece - 1) / a.piece;
@@ -356,6 +226,8 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
       mbar_init(smem_u32(&S.empty[i]), kConsumerWarps);
     }
     S.flag = 0;
+    S.fail1 = 0;
+    S.fail3 = 0;
     fence_barrier_init();
   }
   __syncthreads();                           // the ring's barriers are ready
@@ -363,26 +235,47 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     if (t < B) {
       S.tau[t] = __ldg(a.tau + c0 + t);
       S.x[t] = __ldg(a.draft_tokens + c0 + t);
-      S.xv[t] = make_float2(0.f, 0.f);
     }
+    // partials mode: launched while the chunk pass finishes (programmatic
+    // dependent launch); its results are read only after this wait
+    if (a.part) grid_dep_wait();
+    if (t < B)
+      S.xv[t] = a.part ? make_float2(a.xlogit[2 * (c0 + t)], a.xlogit[2 * (c0 + t) + 1])
+                       : make_float2(0.f, 0.f);
     if (t <= B) S.u[t] = __ldg(a.uniforms + (long)b * (a.B_max + 1) + t);
     consumers_sync();                        // the sequence's labels, tokens, uniforms
   }
+  // the open slots (labels above dcd): only their rows are streamed; open
+  // pair q is (open slot number q / 2, row q % 2)
+  uint32_t open = 0;
+  if (valid) {
+    if (a.decided == nullptr) {
+      open = B == 32 ? 0xffffffffu : (1u << B) - 1u;
+    } else if (producer) {
+      open = __ballot_sync(0xffffffffu, lane < B && __ldg(a.tau + c0 + lane) > dcd);
+    } else {
+      for (int k = 0; k < B; ++k)
+        if (S.tau[k] > dcd) open |= 1u << k;
+    }
+  }
+  const int n_open = __popc(open);
+  auto slot_of = [&](int i) { return (int)__fns(open, 0, i + 1); };   // open slot number i
 
   int issued = 0;                            // producer: stages started so far
   int g = 0;                                 // stage counter (producer and consumers)
   if (valid) {
     // ---------------------------------------------------- 1. row slices
-    const int J = 2 * B * npieces;
+    // (in partials mode the chunk pass did this: nothing is streamed)
+    const int J = a.part ? 0 : 2 * n_open * npieces;
     if (producer) {
       for (int pair = 0, pc = 0; g < J; ++g) {
         const int s = g % kStages;
-        if (g >= kStages && !mbar_wait_warp(smem_u32(&S.empty[s]), ((g / kStages) - 1) & 1)) {
-          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); }
+        if (g >= kStages && !mbar_wait_warp(smem_u32(&S.empty[s]), ((g / kStages) - 1) & 1, a.polls)) {
+          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); atomicOr(&S.fail1, 1); }
           break;
         }
         copy_piece<T>(smem + s * kStageBytes, ring + s * kStageBytes,
-                      row_ptr(pair >> 1, pair & 1) + pc * a.piece, piece_len(pc),
+                      row_ptr(slot_of(pair >> 1), pair & 1) + pc * a.piece, piece_len(pc),
                       smem_u32(&S.full[s]), a.bulk, lane);
         issued = g + 1;
         if (++pc == npieces) { pc = 0; ++pair; }
@@ -397,7 +290,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
       const int v0 = (warp % kGroupWarps) * 32;
       const int chunk = npieces == 2 ? 2 : 1;
       if (lane == 0)                         // pairs this warp may see no piece of
-        for (int q = 0; q < 2 * B; ++q) S.part_w[q][warp] = make_float2(-INFINITY, 0.f);
+        for (int q = 0; q < 2 * n_open; ++q) S.part_w[q][warp] = make_float2(-INFINITY, 0.f);
       float R = -INFINITY, sum = 0.f;
       int gg = grp * chunk, pair = 0, pc = gg;
       if (npieces > 0)
@@ -405,8 +298,8 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
       while (gg < J) {
         const int s = gg % kStages;
         const int n = piece_len(pc);
-        if (!mbar_wait_warp(smem_u32(&S.full[s]), (gg / kStages) & 1)) {
-          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); }
+        if (!mbar_wait_warp(smem_u32(&S.full[s]), (gg / kStages) & 1, a.polls)) {
+          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); atomicOr(&S.fail1, 1); }
           break;
         }
         const uint4 *sv = reinterpret_cast<const uint4 *>(smem + s * kStageBytes);
@@ -418,18 +311,19 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         }
         // the logit at the slot's draft token, if this piece holds it
         if (gtid == 0) {
-          const int off = S.x[pair >> 1] - (s0 + pc * a.piece);
+          const int ks = slot_of(pair >> 1);
+          const int off = S.x[ks] - (s0 + pc * a.piece);
           if (off >= 0 && off < n) {
             const float v = pick<T>(sv[off / N], off % N);
-            if (pair & 1) S.xv[pair >> 1].y = v; else S.xv[pair >> 1].x = v;
+            if (pair & 1) S.xv[ks].y = v; else S.xv[ks].x = v;
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive_n(smem_u32(&S.empty[s]), 2);
         const float mx = Ld<T>::vmax(w, kVecs);
-        const float Rn = mx * ls;
+        const float Rn = ref_of(mx, ls);
         if (Rn > R) {
-          sum = R == -INFINITY ? 0.f : sum * ex2(R - Rn);
+          sum = R == -INFINITY ? 0.f : sum * exp2_int(R - Rn);
           R = Rn;
         }
         if (R != -INFINITY) {
@@ -467,7 +361,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const uint32_t ru = __float_as_uint(R);
           const uint32_t km = __reduce_max_sync(0xffffffffu, (ru & 0x80000000u) ? ~ru : (ru | 0x80000000u));
           const float Rm = __uint_as_float((km & 0x80000000u) ? (km & 0x7fffffffu) : ~km);
-          float sc = Rm == -INFINITY ? 0.f : sum * ex2(R - Rm);
+          float sc = Rm == -INFINITY ? 0.f : sum * exp2_int(R - Rm);
 #pragma unroll
           for (int m = 16; m > 0; m >>= 1) sc += __shfl_xor_sync(0xffffffffu, sc, m);
           if (lane == 0) S.part_w[pair_now][warp] = make_float2(Rm, sc);
@@ -476,7 +370,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         }
       }
       consumers_sync();
-      if (t < 2 * B) {                       // this CTA's slice of pair t
+      if (t < 2 * n_open && !a.part) {       // this CTA's slice of open pair t
         float2 c = make_float2(-INFINITY, 0.f);
         if (npieces > 0 && !*(volatile int *)&S.flag) {
           float M = -INFINITY;
@@ -486,40 +380,72 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
 #pragma unroll 1
             for (int w = 0; w < kConsumerWarps; ++w) {
               const float2 v = S.part_w[t][w];
-              if (v.y > 0.f) sm = ff_add(sm, ff_of(v.y * ex2(v.x - M)));
+              if (v.y > 0.f) sm = ff_add(sm, ff_of(v.y * exp2_int(v.x - M)));
             }
           c = make_float2(M, sm.hi + sm.lo);
         }
         S.cpart[t] = c;
       }
     }
-    cluster_sync();                          // B1: every slice's partials are in place
+    if (!a.part) cluster_sync();             // B1: every slice's partials are in place
 
     // ---------------------------------------------------- 2. the walk
     // every CTA merges the slices' partials and walks the steps itself (the
     // same inputs in the same order give the same decisions everywhere), so
     // no barrier is needed before the residual pass; CTA 0 writes outputs
-    if (!producer) {
+    if (!producer && a.part) {
+      // partials mode: every CTA merges all of every open row's chunk
+      // partials itself (warp w: open pairs w, w + 16, ...; lanes stride
+      // over the row's chunks x the chunk pass's warps), so no cluster
+      // barrier and no exchange come before the walk
+      const int per_row = a.nchunks * kAConsumerWarps;
+      for (int q = warp; q < 2 * n_open; q += kConsumerWarps) {
+        const int k = slot_of(q >> 1), row = q & 1, x = S.x[k];
+        const float2 *pr_ = a.part + (long)(2 * (c0 + k) + row) * per_row;
+        float M = -INFINITY;
+        for (int i = lane; i < per_row; i += 32) M = fmaxf(M, __ldg(&pr_[i].x));
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+        Ff sm = ff_of(0.f);
+        if (M != -INFINITY)
+          for (int i = lane; i < per_row; i += 32) {
+            const float2 v = __ldg(pr_ + i);
+            if (v.y > 0.f) sm = ff_add(sm, ff_of(v.y * exp2_int(v.x - M)));
+          }
+#pragma unroll
+        for (int m = 16; m > 0; m >>= 1) sm = ff_add(sm, ff_shfl_xor(sm, m));
+        if (lane == 0) {
+          S.norm[2 * k + row] = make_float4(M, sm.hi, sm.lo, 0.f);
+          // p(x) (row 0) or q(x) (row 1); a token outside the vocabulary rejects
+          const bool xin = x >= 0 && x < a.vocab;
+          const float pr = xin ? rel_exp(row ? S.xv[k].y : S.xv[k].x, M, ls) / (sm.hi + sm.lo) : 0.f;
+          if (row) S.qx[k] = pr; else S.px[k] = pr;
+          if (!xin && row == 0 && rank == 0) raise_status(a.status, kStatusBadInput);
+        }
+      }
+    } else if (!producer) {
       // thread (pair q, slice r) reads one slice's partial; groups of gs
       // lanes (8, or 16 for clusters over 8) merge them (pair q: slot q / 2,
       // row q % 2)
       const int lg = a.csize > 8 ? 4 : 3, gs = 1 << lg;
-      for (int q0 = 0; q0 < 2 * B; q0 += kConsumers >> lg) {
-      if (warp * 32 < (2 * B - q0) << lg) {  // whole warps: the shuffles need every lane
+      for (int q0 = 0; q0 < 2 * n_open; q0 += kConsumers >> lg) {
+      if (warp * 32 < (2 * n_open - q0) << lg) {  // whole warps: the shuffles need every lane
         const int q = q0 + (t >> lg), r = t & (gs - 1);
-        const bool mine = q < 2 * B;
-        const int k = q >> 1, row = q & 1, x = mine ? S.x[k] : -1;
+        const bool mine = q < 2 * n_open;
+        const int k = mine ? slot_of(q >> 1) : 0, row = q & 1, x = mine ? S.x[k] : -1;
         const bool xin = x >= 0 && x < a.vocab;
+        // the logits at x: from the slice that holds x (every CTA has them
+        // in partials mode)
         const float2 xl = r == 0 && xin ? ld_dsmem2(dsmem(&S.xv[k], x / a.per)) : make_float2(0.f, 0.f);
         const float2 v = mine && r < a.csize ? ld_dsmem2(dsmem(&S.cpart[q], r)) : make_float2(-INFINITY, 0.f);
         float M = v.x;
 #pragma unroll 1
         for (int m = gs / 2; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-        Ff sm = ff_of(M != -INFINITY && v.y > 0.f ? v.y * ex2(v.x - M) : 0.f);
+        Ff sm = ff_of(M != -INFINITY && v.y > 0.f ? v.y * exp2_int(v.x - M) : 0.f);
 #pragma unroll 1
         for (int m = gs / 2; m > 0; m >>= 1) sm = ff_add(sm, ff_shfl_xor(sm, m));
         if (mine && r == 0) {
-          S.norm[q] = make_float2(M, sm.hi + sm.lo);
+          S.norm[2 * k + row] = make_float4(M, sm.hi, sm.lo, 0.f);
           // p(x) (row 0) or q(x) (row 1); a token no slice holds rejects
           const float pr = xin ? rel_exp(row ? xl.y : xl.x, M, ls) / (sm.hi + sm.lo) : 0.f;
           if (row) S.qx[k] = pr; else S.px[k] = pr;
@@ -527,30 +453,48 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         }
       }
       }
+    }
+    if (!producer) {
       consumers_sync();
       if (t == 0) {
         for (int k = 0; k < kMaxB; ++k) S.slot_of_step[k] = 0;
+        uint32_t seen = 0;
         for (int k = 0; k < B; ++k) {
-          const int tk = S.tau[k];           // a label outside 1..B is ignored
-          if (tk >= 1 && tk <= B) S.slot_of_step[tk - 1] = k;
+          const int tk = S.tau[k];
+          if (tk >= 1 && tk <= B) {
+            seen |= 1u << (tk - 1);
+            S.slot_of_step[tk - 1] = k;
+          }
         }
+        // a tau that is not a permutation of 1..B, or a wait in any CTA of
+        // the cluster that gave up in phase 1 (the snapshots are final
+        // after B1, so every CTA decides alike): no walk
+        bool any_fail = false;                 // (partials mode: phase 1 has no waits)
+        if (!a.part)
+          for (int r = 0; r < a.csize; ++r) any_fail |= ld_dsmem_i32(dsmem(&S.fail1, r)) != 0;
+        const bool perm = seen == (B == 32 ? 0xffffffffu : (1u << B) - 1u);
         int n = B, rej = -1;
-        for (int st = 1; st <= B; ++st) {
-          const int k = S.slot_of_step[st - 1];
-          if (!(S.u[st - 1] * S.qx[k] < S.px[k])) { n = st - 1; rej = k; break; }
+        if (!perm || any_fail) {
+          n = 0;
+          if (!perm && rank == 0) raise_status(a.status, kStatusBadInput);
+        } else {
+          for (int st = dcd + 1; st <= B; ++st) {
+            const int k = S.slot_of_step[st - 1];
+            if (!(S.u[st - 1] * S.qx[k] < S.px[k])) { n = st - 1; rej = k; break; }
+          }
         }
         if (rank == 0) {
           a.n_accept[b] = n;
           a.pos[b] = rej;
           if (rej < 0) a.token[b] = -1;
         }
-        WalkInfo w{-1, 0.f, 0.f, 1.f, 1.f, 0.f, 0, 0};
+        WalkInfo w{-1, 0.f, 0.f, Ff{1.f, 0.f}, 0.f, 0, 0};
         if (rej >= 0) {
+          const float4 nt = S.norm[2 * rej], nd = S.norm[2 * rej + 1];
           w.slot = rej;
-          w.Mt = S.norm[2 * rej].x;
-          w.Md = S.norm[2 * rej + 1].x;
-          w.inv_st = 1.f / S.norm[2 * rej].y;
-          w.inv_sd = 1.f / S.norm[2 * rej + 1].y;
+          w.Mt = nt.x;
+          w.Md = nd.x;
+          w.rho = ff_div(Ff{nt.y, nt.z}, Ff{nd.y, nd.z});
           w.u = S.u[B];
         }
         S.walk = w;
@@ -565,8 +509,8 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
       if (producer) {
         for (; g < J2 && !*(volatile int *)&S.flag; ++g) {
           const int s = g % kStages, pc = (g - J) >> 1, row = (g - J) & 1;
-          if (g >= kStages && !mbar_wait_warp(smem_u32(&S.empty[s]), ((g / kStages) - 1) & 1)) {
-            if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); }
+          if (g >= kStages && !mbar_wait_warp(smem_u32(&S.empty[s]), ((g / kStages) - 1) & 1, a.polls)) {
+            if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); atomicOr(&S.fail3, 1); }
             break;
           }
           copy_piece<T>(smem + s * kStageBytes, ring + s * kStageBytes,
@@ -582,9 +526,9 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const int gt = J + 2 * pc, gd = gt + 1;
           const int st = gt % kStages, sd = gd % kStages;
           const int n = piece_len(pc);
-          if (!mbar_wait_warp(smem_u32(&S.full[st]), (gt / kStages) & 1) ||
-              !mbar_wait_warp(smem_u32(&S.full[sd]), (gd / kStages) & 1)) {
-            if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); }
+          if (!mbar_wait_warp(smem_u32(&S.full[st]), (gt / kStages) & 1, a.polls) ||
+              !mbar_wait_warp(smem_u32(&S.full[sd]), (gd / kStages) & 1, a.polls)) {
+            if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(&S.flag, 1); atomicOr(&S.fail3, 1); }
             break;
           }
           const uint4 *tv = reinterpret_cast<const uint4 *>(smem + st * kStageBytes);
@@ -601,10 +545,9 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
               Ld<T>::unpack(in ? dv[idx] : Ld<T>::neg_inf(), fd);
 #pragma unroll
               for (int e = 0; e < N; ++e) {
-                const float p = prob(ft[e], w.Mt, w.inv_st, ls);
-                const float q = prob(fd[e], w.Md, w.inv_sd, ls);
-                rs[e & 3] += residual(p, q);
-                ps[e & 3] += p;
+                const float et = rel_exp(ft[e], w.Mt, ls);
+                rs[e & 3] += residual(et, draft_mass(fd[e], w.Md, w.rho, ls));
+                ps[e & 3] += et;
               }
             }
           }
@@ -652,6 +595,10 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
       // vocabulary range of the piece, then to the entry.
       if (warp == 0) {
         const float4 v = lane < a.csize ? ld_dsmem4(dsmem(&S.tot, lane)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        // a wait that gave up in any CTA's residual pass (snapshots final
+        // after B3): every CTA skips the draw, CTA 0 reports no walk
+        const bool any_fail =
+            __any_sync(0xffffffffu, lane < a.csize && ld_dsmem_i32(dsmem(&S.fail3, lane)) != 0);
         Ff Sr{v.x, v.y}, Sp{v.z, v.w};
 #pragma unroll 1
         for (int m = 16; m > 0; m >>= 1) {
@@ -666,7 +613,12 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         auto mass_of = [&](float4 q) { return use_p ? Ff{q.z, q.w} : Ff{q.x, q.y}; };
         Ff base;
         const int ch = warp_pick(mass_of(v), ff_of(0.f), U, &base);
-        if (ch == rank && !*(volatile int *)&S.flag) {
+        if (any_fail && rank == 0 && lane == 0) {
+          a.n_accept[b] = 0;
+          a.token[b] = -1;
+          a.pos[b] = -1;
+        }
+        if (!any_fail && ch == rank && !*(volatile int *)&S.flag) {
           const float4 vp = lane < npieces ? S.piece_s[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
           const int sel = warp_pick(mass_of(vp), base, U, &base);
           const float4 vw = lane < kRanges ? S.piece_w[sel][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -701,9 +653,8 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
             float lane_mass = 0.f;
 #pragma unroll
             for (int e = 0; e < N; ++e) {
-              const float p = prob(ft[e], w.Mt, w.inv_st, ls);
-              const float q = prob(fd[e], w.Md, w.inv_sd, ls);
-              m[e] = use_p ? p : residual(p, q);
+              const float et = rel_exp(ft[e], w.Mt, ls);
+              m[e] = use_p ? et : residual(et, draft_mass(fd[e], w.Md, w.rho, ls));
               lane_mass += m[e];
               if (m[e] > 0.f) last_pos = vbase + e;
             }
@@ -751,6 +702,152 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
   cluster_wait();                            // B4: no CTA leaves while others read it
 }
 
+// ---------------------------------------------------------------- chunk pass
+// K4a of the two-kernel path: every SM streams (row, chunk) items -- rows
+// are the target and draft rows of every slot, chunks kChunk entries --
+// through a bulk-copy ring.  Each consumer warp takes its own 1/8 of every
+// item (kV 16-byte vectors per lane), reduces it against its own
+// whole-number reference and writes (reference, sum) for (row, chunk,
+// warp); the warp whose part holds the slot's draft token also writes that
+// logit.  Warps never wait for one another -- only for the ring -- so a
+// warp can be on the next item while another finishes this one.  No item
+// depends on another, so the grid is as many CTAs as the SMs hold (two per
+// SM for bf16) and every SM streams until the items run out; the
+// per-sequence walk and residual draw (K4b, the cluster kernel in partials
+// mode) then read only these partials and the rejected slots' rows.
+
+struct ChunkParams {
+  const void *target;
+  const void *draft;
+  const int32_t *draft_tokens;
+  float2 *part;       // [2 total_B][nchunks][kAConsumerWarps]: (reference, sum of 2^(l ls - ref))
+  float *xlogit;      // [2 total_B]
+  uint32_t *status;
+  int vocab, total_B, nchunks, bulk;
+  uint32_t polls;
+  Scale ls;
+};
+
+template <typename T>
+__host__ __device__ constexpr int chunk_stage_bytes() { return kStageBytes; }
+template <typename T>
+__host__ __device__ constexpr int chunk_entries() { return kStageBytes / (int)sizeof(T); }
+template <typename T>
+constexpr size_t chunk_smem_bytes() { return (size_t)kAStages * chunk_stage_bytes<T>() + 256; }
+
+template <typename T>
+__global__ void __launch_bounds__(kAThreads)
+vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
+  constexpr int N = Ld<T>::N;
+  constexpr int kStage = chunk_stage_bytes<T>();
+  constexpr int kChunk = chunk_entries<T>();
+  constexpr int kWarpVecs = kStage / 16 / kAConsumerWarps;   // a warp's part of an item
+  constexpr int kV = kWarpVecs / 32;                         // 16-byte vectors per lane
+  static_assert(kV * 32 * kAConsumerWarps * 16 == kStage, "the warps' parts tile an item");
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kAStages * kStage);
+  uint64_t *empty = full + kAStages;
+  int *stage_x = reinterpret_cast<int *>(empty + kAStages);   // [kAStages]: the item's draft token
+  int *flag = stage_x + kAStages;                             // a wait gave up (the drain)
+  const uint32_t ring = smem_u32(smem);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const bool producer = warp == kAConsumerWarps;
+  grid_dep_launch();                           // the cluster kernel may be scheduled
+  const long items = 2L * a.total_B * a.nchunks;
+  const long mine = blockIdx.x < items ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  auto item_of = [&](long j) { return blockIdx.x + j * (long)gridDim.x; };
+  if (t == 0) {
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), kAConsumerWarps);
+    }
+    *flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  long issued = 0;
+  if (producer) {
+    for (long j = 0; j < mine; ++j) {
+      const int s = (int)(j % kAStages);
+      if (j >= kAStages && !mbar_wait_warp(smem_u32(&empty[s]), ((j / kAStages) - 1) & 1, a.polls)) {
+        if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); }
+        break;
+      }
+      const long i = item_of(j);
+      const long p = i / a.nchunks;                 // row pair index: slot p/2, target or draft
+      const int c = (int)(i % a.nchunks);
+      const int n = min(kChunk, a.vocab - c * kChunk);
+      // the draft token goes beside the stage before the copy's arrival
+      // (release) makes the stage visible to the consumers
+      if (lane == 0) stage_x[s] = __ldg(a.draft_tokens + (p >> 1));
+      __syncwarp();
+      const T *src = (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab + (long)c * kChunk;
+      copy_piece<T>(smem + s * kStage, ring + s * kStage, src, n, smem_u32(&full[s]), a.bulk, lane);
+      issued = j + 1;
+    }
+  } else {
+    for (long j = 0; j < mine; ++j) {
+      const int s = (int)(j % kAStages);
+      // a warp whose wait gave up neither reads nor releases the stage (its
+      // copy may still land) and stops; the others are not held up by it
+      if (!mbar_wait_warp(smem_u32(&full[s]), (j / kAStages) & 1, a.polls)) {
+        if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); }
+        break;
+      }
+      const long i = item_of(j);
+      const long p = i / a.nchunks;
+      const int c = (int)(i % a.nchunks);
+      const int n = min(kChunk, a.vocab - c * kChunk);
+      const uint4 *sv = reinterpret_cast<const uint4 *>(smem + s * kStage);
+      const int v0 = warp * kWarpVecs;              // this warp's vectors: v0 + v * 32 + lane
+      uint4 w[kV];
+#pragma unroll
+      for (int v = 0; v < kV; ++v) {
+        const int idx = v0 + v * 32 + lane;
+        w[v] = idx * N < n ? sv[idx] : Ld<T>::neg_inf();
+      }
+      // the logit at the slot's draft token, if this warp's part holds it
+      const int off = stage_x[s] - c * kChunk;
+      if (off >= 0 && off < n && off / N >= v0 && off / N < v0 + kWarpVecs && (off / N - v0) % 32 == lane) {
+        const int vx = (off / N - v0) / 32;
+        uint4 wx = w[0];
+#pragma unroll
+        for (int v = 1; v < kV; ++v)
+          if (v == vx) wx = w[v];
+        a.xlogit[p] = pick<T>(wx, off % N);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      // this warp's part: its maximum, then its sum against a whole-number
+      // reference (combined with the others' by exact powers of two)
+      const float mx = Ld<T>::vmax(w, kV);
+      const uint32_t mu = __float_as_uint(mx);
+      const uint32_t km = __reduce_max_sync(0xffffffffu, (mu & 0x80000000u) ? ~mu : (mu | 0x80000000u));
+      const float R = ref_of(__uint_as_float((km & 0x80000000u) ? (km & 0x7fffffffu) : ~km), a.ls);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (R != -INFINITY) {
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+          float f[N];
+          Ld<T>::unpack(w[v], f);
+#pragma unroll
+          for (int e = 0; e < N; ++e) acc[(v * N + e) & 3] += rel_exp(f[e], R, a.ls);
+        }
+      }
+      float sm = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      if (lane == 0) a.part[(p * a.nchunks + c) * kAConsumerWarps + warp] = make_float2(R, sm);
+    }
+  }
+  // after a wait that gave up the copies in flight land before the CTA
+  // can exit (the flag is final after the barrier)
+  __syncthreads();
+  if (producer && *(volatile int *)flag)
+    for (long j = max(0L, issued - kAStages); j < issued; ++j)
+      (void)mbar_wait_warp(smem_u32(&full[j % kAStages]), (j / kAStages) & 1);
+}
+
 constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(AccShared);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
@@ -759,7 +856,7 @@ void mark(void *const *events, int i, cudaStream_t stream) {
 }
 
 cudaLaunchConfig_t launch_config(int csize, int batch, cudaStream_t stream,
-                                 cudaLaunchAttribute *attr) {
+                                 cudaLaunchAttribute *attr, bool after_chunks = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize, batch);
   cfg.blockDim = dim3(kThreads);
@@ -769,8 +866,12 @@ cudaLaunchConfig_t launch_config(int csize, int batch, cudaStream_t stream,
   attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // after the chunk pass: programmatic dependent launch (the kernel waits
+  // for the chunk pass's results on the device)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = after_chunks ? 2 : 1;
   return cfg;
 }
 
@@ -794,7 +895,7 @@ cudaError_t max_active_clusters(int dev, int csize, int *out) {
     cache[dev][0] = 1;
   }
   if (cache[dev][csize] == 0) {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     const cudaLaunchConfig_t cfg = launch_config(csize, csize, nullptr, attr);
     int n = 0;
     cudaError_t e = cudaOccupancyMaxActiveClusters(&n, accept_kernel<T>, &cfg);
@@ -818,10 +919,12 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
   // whole streaming loop fewer) plus the fixed cost of the walk, residual
   // and draw phases.  Small batches get large clusters (every SM busy),
   // large batches small ones (fewer waves).  Never so small that a slice
-  // needs more pieces than the kernel tracks.
-  const int piece = kStageBytes / (int)sizeof(T), vec = 16 / (int)sizeof(T);
+  // needs more pieces than the kernel tracks.  In partials mode only the
+  // residual pass of the rejected slot's two rows streams.
+  const int vec = 16 / (int)sizeof(T);
+  const int piece = kStageBytes / (int)sizeof(T);
   const int64_t max_slice = (int64_t)kMaxPieces * piece;
-  const double per_seq = (2.0 * a.total_B / a.batch + 2.0) * a.vocab;   // exponentials
+  const double per_seq = (a.part ? 2.0 : 2.0 * a.total_B / a.batch + 2.0) * a.vocab;   // exponentials
   constexpr double kPhaseCycles = 20000.0;
   int csize = kMaxCluster;
   double best = 1e300;
@@ -836,13 +939,50 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
     if (cost < best * (1.0 - 1e-9)) { best = cost; csize = c; }
   }
   a.csize = csize;
-  a.per = ((a.vocab + csize - 1) / csize + vec - 1) / vec * vec;
-  // pieces of equal size (whole vectors, at most one stage) per slice
-  const int np = (a.per + piece - 1) / piece;
-  a.piece = ((a.per + np - 1) / np + vec - 1) / vec * vec;
-  cudaLaunchAttribute attr[1];
-  const cudaLaunchConfig_t cfg = launch_config(csize, a.batch, stream, attr);
+  if (a.part) {
+    // slices of whole chunks: the chunk pass's items are the pieces
+    a.cpc = (a.nchunks + csize - 1) / csize;
+    a.per = a.cpc * piece;
+    a.piece = piece;
+  } else {
+    a.per = ((a.vocab + csize - 1) / csize + vec - 1) / vec * vec;
+    // pieces of equal size (whole vectors, at most one stage) per slice
+    const int np = (a.per + piece - 1) / piece;
+    a.piece = ((a.per + np - 1) / np + vec - 1) / vec * vec;
+  }
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = launch_config(csize, a.batch, stream, attr, a.part != nullptr);
   return cudaLaunchKernelEx(&cfg, accept_kernel<T>, a);
+}
+
+// The chunk pass: as many CTAs as the device holds at once (queried once
+// per device and dtype), never more than the items.
+template <typename T>
+cudaError_t launch_chunks(const ChunkParams &c, cudaStream_t stream) {
+  static std::mutex mu;
+  static int resident[64] = {0};
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (resident[dev] == 0) {
+      cudaError_t e = cudaFuncSetAttribute(vocab_chunk_kernel<T>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)chunk_smem_bytes<T>());
+      if (e != cudaSuccess) return e;
+      int n = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, vocab_chunk_kernel<T>, kAThreads,
+                                                        chunk_smem_bytes<T>());
+      if (e != cudaSuccess) return e;
+      resident[dev] = n > 0 ? n : 1;
+    }
+    per_sm = resident[dev];
+  }
+  const long items = 2L * c.total_B * c.nchunks;
+  const long grid = std::min<long>(items, (long)per_sm * device_sm_count());
+  vocab_chunk_kernel<T><<<(unsigned)grid, kAThreads, chunk_smem_bytes<T>(), stream>>>(c);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- greedy
@@ -865,7 +1005,8 @@ struct GreedyParams {
   int32_t *token;
   int32_t *pos;
   uint32_t *status;
-  int vocab, csize, per, bulk;
+  const int32_t *decided;
+  int vocab, total_B, B_max, csize, per, bulk;
 };
 
 // candidate (v, i) beats (w, j): a larger value, or an equal one at a
@@ -884,11 +1025,14 @@ accept_greedy_kernel(const __grid_constant__ GreedyParams a) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
-  const bool valid = B >= 1 && B <= kMaxB;
+  const int dcd = a.decided ? __ldg(a.decided + b) : 0;
+  const bool valid = B >= 1 && B <= a.B_max && c0 >= 0 && c0 + B <= a.total_B && dcd >= 0 &&
+                     dcd <= B;
   const int s0 = min(a.vocab, rank * a.per);
   const int len = min(a.vocab, s0 + a.per) - s0;
   if (valid) {
     for (int k = 0; k < B; ++k) {
+      if (dcd > 0 && __ldg(a.tau + c0 + k) <= dcd) continue;   // decided: never tested
       const T *row = (const T *)a.target + (long)(c0 + k) * a.vocab + s0;
       float bv = -INFINITY;
       int bi = 0x7fffffff;
@@ -949,12 +1093,15 @@ accept_greedy_kernel(const __grid_constant__ GreedyParams a) {
     } else {
       int slot_of_step[kMaxB];
       for (int k = 0; k < B; ++k) slot_of_step[k] = 0;
+      uint32_t seen = 0;
       for (int k = 0; k < B; ++k) {
-        const int tk = __ldg(a.tau + c0 + k);     // a label outside 1..B is ignored
-        if (tk >= 1 && tk <= B) slot_of_step[tk - 1] = k;
+        const int tk = __ldg(a.tau + c0 + k);
+        if (tk >= 1 && tk <= B) { seen |= 1u << (tk - 1); slot_of_step[tk - 1] = k; }
       }
-      int n = B, tok = -1, ps = -1;
-      for (int st = 1; st <= B; ++st) {
+      const bool perm = seen == (B == 32 ? 0xffffffffu : (1u << B) - 1u);
+      if (!perm) raise_status(a.status, kStatusBadInput);
+      int n = perm ? B : 0, tok = -1, ps = -1;
+      for (int st = dcd + 1; perm && st <= B; ++st) {
         const int k = slot_of_step[st - 1];
         float v = -INFINITY;
         int am = 0x7fffffff;
@@ -962,6 +1109,7 @@ accept_greedy_kernel(const __grid_constant__ GreedyParams a) {
           const float2 c = ld_dsmem2(dsmem(&cand[k], r));
           if (beats(c.x, __float_as_int(c.y), v, am)) { v = c.x; am = __float_as_int(c.y); }
         }
+        if (am == 0x7fffffff) am = 0;               // no entry beat "none" (NaN row)
         const int x = __ldg(a.draft_tokens + c0 + k);
         if (x < 0 || x >= a.vocab) raise_status(a.status, kStatusBadInput);
         if (x != am) { n = st - 1; tok = am; ps = k; break; }
@@ -1019,8 +1167,9 @@ struct MatchParams {
   int32_t *token;
   int32_t *pos;
   uint32_t *status;
-  int vocab, B_max, csize, per, bulk;
-  float ls;
+  const int32_t *decided;
+  int vocab, total_B, B_max, csize, per, bulk;
+  Scale ls;
 };
 
 struct __align__(16) MatchSlot {
@@ -1032,7 +1181,7 @@ struct __align__(16) MatchSlot {
 __device__ __forceinline__ void match_merge(float &R, Ff &s, Ff &pre, float R2, Ff s2, Ff pre2) {
   const float M = fmaxf(R, R2);
   if (M == -INFINITY) return;
-  const float a = ex2(R - M), b = ex2(R2 - M);
+  const float a = exp2_int(R - M), b = exp2_int(R2 - M);
   s = ff_add(Ff{s.hi * a, s.lo * a}, Ff{s2.hi * b, s2.lo * b});
   pre = ff_add(Ff{pre.hi * a, pre.lo * a}, Ff{pre2.hi * b, pre2.lo * b});
   R = M;
@@ -1050,15 +1199,18 @@ accept_match_kernel(const __grid_constant__ MatchParams a) {
   __shared__ float s_M;
   const int rank = blockIdx.x, b = blockIdx.y;    // the cluster spans x
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const float ls = a.ls;
+  const Scale ls = a.ls;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
-  const bool valid = B >= 1 && B <= kMaxB;
+  const int dcd = a.decided ? __ldg(a.decided + b) : 0;
+  const bool valid = B >= 1 && B <= a.B_max && c0 >= 0 && c0 + B <= a.total_B && dcd >= 0 &&
+                     dcd <= B;
   const int s0 = min(a.vocab, rank * a.per);
   const int len = min(a.vocab, s0 + a.per) - s0;
   auto value_at = [&](const T *row, int e) { return Ld<T>::value(row[e]); };
   if (valid) {
     for (int k = 0; k < B; ++k) {
+      if (dcd > 0 && __ldg(a.tau + c0 + k) <= dcd) continue;   // decided: never tested
       const T *row = (const T *)a.target + (long)(c0 + k) * a.vocab + s0;
       const int x = __ldg(a.draft_tokens + c0 + k);
       const int xo = x - s0;                        // x's offset in this slice
@@ -1083,9 +1235,9 @@ accept_match_kernel(const __grid_constant__ MatchParams a) {
         for (int u = 0; u < kMatchUnroll; ++u)
 #pragma unroll
           for (int e = 0; e < N; ++e) mx = fmaxf(mx, f[u][e]);
-        const float Rn = mx * ls;
+        const float Rn = ref_of(mx, ls);
         if (Rn > R) {
-          const float c = R == -INFINITY ? 0.f : ex2(R - Rn);
+          const float c = R == -INFINITY ? 0.f : exp2_int(R - Rn);
           sm *= c;
           pr *= c;
           R = Rn;
@@ -1134,12 +1286,15 @@ accept_match_kernel(const __grid_constant__ MatchParams a) {
     if (valid) {
       int slot_of_step[kMaxB];
       for (int k = 0; k < B; ++k) slot_of_step[k] = 0;
+      uint32_t seen = 0;
       for (int k = 0; k < B; ++k) {
-        const int tk = __ldg(a.tau + c0 + k);     // a label outside 1..B is ignored
-        if (tk >= 1 && tk <= B) slot_of_step[tk - 1] = k;
+        const int tk = __ldg(a.tau + c0 + k);
+        if (tk >= 1 && tk <= B) { seen |= 1u << (tk - 1); slot_of_step[tk - 1] = k; }
       }
-      int n = B, rej = -1;
-      for (int st = 1; st <= B; ++st) {
+      const bool perm = seen == (B == 32 ? 0xffffffffu : (1u << B) - 1u);
+      if (!perm && rank == 0) raise_status(a.status, kStatusBadInput);
+      int n = perm ? B : 0, rej = -1;
+      for (int st = dcd + 1; perm && st <= B; ++st) {
         const int k = slot_of_step[st - 1];
         // the slices' partials in rank order, merged to the largest reference
         float M = -INFINITY, xl = -INFINITY;
@@ -1154,7 +1309,7 @@ accept_match_kernel(const __grid_constant__ MatchParams a) {
             const float4 h = ld_dsmem4(dsmem(&slot[k], r));
             const float4 q = ld_dsmem4(dsmem(reinterpret_cast<const float4 *>(&slot[k]) + 1, r));
             if (h.x == -INFINITY) continue;
-            const float w = ex2(h.x - M);
+            const float w = exp2_int(h.x - M);
             S = ff_add(S, Ff{h.z * w, h.w * w});
             Pre = ff_add(Pre, Ff{q.x * w, q.y * w});
           }
@@ -1163,7 +1318,7 @@ accept_match_kernel(const __grid_constant__ MatchParams a) {
         const float u = __ldg(a.uniforms + (long)b * (a.B_max + 1) + st - 1);
         const float uh = u * S.hi;
         const Ff U = ff_add(Ff{uh, fmaf(u, S.hi, -uh)}, ff_of(u * S.lo));
-        const float px = (x >= 0 && x < a.vocab) ? ex2(fmaf(xl, ls, -M)) : 0.f;   // mass of x
+        const float px = (x >= 0 && x < a.vocab) ? rel_exp(xl, M, ls) : 0.f;   // mass of x
         const bool acc = px > 0.f && !ff_gt(Pre, U) && ff_gt(ff_add(Pre, ff_of(px)), U);
         if (acc) continue;
         n = st - 1;
@@ -1175,7 +1330,7 @@ accept_match_kernel(const __grid_constant__ MatchParams a) {
         Ff lastbase = ff_of(0.f);
         for (int r = 0; r < a.csize; ++r) {
           const float4 h = ld_dsmem4(dsmem(&slot[k], r));
-          const float w = h.x == -INFINITY ? 0.f : ex2(h.x - M);
+          const float w = h.x == -INFINITY ? 0.f : exp2_int(h.x - M);
           const Ff m = Ff{h.z * w, h.w * w};
           const Ff nx = ff_add(run, m);
           if (m.hi > 0.f) {
@@ -1297,8 +1452,29 @@ bool accept_pointers_ok(const simsd_accept_desc *d) {
          d->token && d->pos && (!draft || d->draft_logits) && (!uni || d->uniforms);
 }
 
-// The workspace holds the status word only (everything else stays on chip).
+// Workspace: the status word; for the sampling rule's two-kernel path also
+// the chunk partials [2 total_B][nchunks] (float2) and the draft-token logits
+// [2 total_B] (float).  A workspace of just the status word runs the single
+// cluster kernel (the rows streamed per sequence), as do walks from decided
+// steps (that kernel skips the decided slots' rows).
 constexpr size_t kAcceptWorkspace = kAlign;
+struct AcceptLayout {
+  int nchunks;
+  size_t off_part, off_xlogit, total;
+};
+AcceptLayout accept_layout(const simsd_accept_desc *d) {
+  AcceptLayout L;
+  const int chunk = kStageBytes / (d->dtype == SIMSD_BF16 ? 2 : 4);
+  L.nchunks = (d->vocab + chunk - 1) / chunk;
+  L.off_part = kAcceptWorkspace;
+  L.off_xlogit = align_up(L.off_part + (size_t)2 * d->total_B * L.nchunks * kAConsumerWarps *
+                                           sizeof(float2), kAlign);
+  L.total = align_up(L.off_xlogit + (size_t)2 * d->total_B * sizeof(float), kAlign);
+  return L;
+}
+size_t accept_workspace(const simsd_accept_desc *d) {
+  return d->rule == SIMSD_ACCEPT_SAMPLE ? accept_layout(d).total : kAcceptWorkspace;
+}
 
 // Scratch of simsd_accept_noalloc: one static array per device, alive until
 // the process exits.  Host code may not take its address directly (the
@@ -1328,9 +1504,9 @@ cudaError_t static_scratch(char **out) {
 }
 
 // Launches K4 (the status word is not cleared here: its bits stay set until
-// simsd_read_status reads them).
-simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t stream,
-                        void *const *events) {
+// simsd_read_status reads them).  ws_bytes: the workspace's size.
+simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
+                        cudaStream_t stream, void *const *events) {
   const int es = d->dtype == SIMSD_BF16 ? 2 : 4;
   if (d->rule == SIMSD_ACCEPT_GREEDY) {
     GreedyParams g;
@@ -1342,7 +1518,10 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t strea
     g.token = d->token;
     g.pos = d->pos;
     g.status = (uint32_t *)ws;
+    g.decided = d->decided;
     g.vocab = d->vocab;
+    g.total_B = d->total_B;
+    g.B_max = d->B_max;
     g.csize = 1;
     g.per = 0;
     g.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits);
@@ -1364,12 +1543,14 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t strea
     m.token = d->token;
     m.pos = d->pos;
     m.status = (uint32_t *)ws;
+    m.decided = d->decided;
     m.vocab = d->vocab;
+    m.total_B = d->total_B;
     m.B_max = d->B_max;
     m.csize = 1;
     m.per = 0;
     m.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits);
-    m.ls = kLog2e / (d->temperature > 0.f ? d->temperature : 1.f);
+    m.ls = scale_of(d->temperature > 0.f ? (double)d->temperature : 1.0);
     mark(events, 0, stream);
     const cudaError_t e = d->dtype == SIMSD_BF16 ? launch_match<__nv_bfloat16>(m, d->batch, stream)
                                                  : launch_match<float>(m, d->batch, stream);
@@ -1384,6 +1565,7 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t strea
   a.tau = d->tau;
   a.cu_B = d->cu_B;
   a.uniforms = d->uniforms;
+  a.decided = d->decided;
   a.n_accept = d->n_accept;
   a.token = d->token;
   a.pos = d->pos;
@@ -1392,7 +1574,8 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t strea
   a.vocab = d->vocab;
   a.B_max = d->B_max;
   a.total_B = d->total_B;
-  a.ls = kLog2e / (d->temperature > 0.f ? d->temperature : 1.f);
+  a.polls = wait_polls_of(d->wait_polls);
+  a.ls = scale_of(d->temperature > 0.f ? (double)d->temperature : 1.0);
   // slices of whole 16-byte vectors (set with the cluster size at launch);
   // a piece is one ring stage
   a.csize = kMaxCluster;
@@ -1400,10 +1583,36 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, cudaStream_t strea
   a.piece = 0;
   a.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits) &&
            aligned16(d->draft_logits);
+  a.part = nullptr;
+  a.xlogit = nullptr;
+  a.nchunks = 0;
+  a.cpc = 0;
+  const AcceptLayout L = accept_layout(d);
+  const bool two_pass = d->decided == nullptr && ws_bytes >= L.total;
   mark(events, 0, stream);
-  const cudaError_t e = d->dtype == SIMSD_BF16 ? launch<__nv_bfloat16>(a, stream)
-                                               : launch<float>(a, stream);
+  cudaError_t e = cudaSuccess;
+  if (two_pass) {
+    ChunkParams c;
+    c.target = d->target_logits;
+    c.draft = d->draft_logits;
+    c.draft_tokens = d->draft_tokens;
+    c.part = (float2 *)(ws + L.off_part);
+    c.xlogit = (float *)(ws + L.off_xlogit);
+    c.status = a.status;
+    c.vocab = d->vocab;
+    c.total_B = d->total_B;
+    c.nchunks = L.nchunks;
+    c.bulk = a.bulk;
+    c.polls = a.polls;
+    c.ls = a.ls;
+    e = d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16>(c, stream) : launch_chunks<float>(c, stream);
+    a.part = c.part;
+    a.xlogit = c.xlogit;
+    a.nchunks = L.nchunks;
+  }
   mark(events, 1, stream);
+  if (e == cudaSuccess)
+    e = d->dtype == SIMSD_BF16 ? launch<__nv_bfloat16>(a, stream) : launch<float>(a, stream);
   mark(events, 2, stream);
   return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
 }
@@ -1417,7 +1626,7 @@ extern "C" {
 
 size_t simsd_accept_workspace_size(const simsd_accept_desc *d) {
   if (accept_check(d) != SIMSD_OK) return 0;
-  return kAcceptWorkspace;
+  return accept_workspace(d);
 }
 
 simsd_status simsd_accept(const simsd_accept_desc *d, void *stream_ptr) {
@@ -1432,7 +1641,7 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream_ptr,
   if (d->workspace == nullptr || ((uintptr_t)d->workspace % kAlign) != 0 ||
       d->workspace_bytes < kAcceptWorkspace)
     return SIMSD_ERR_WORKSPACE;
-  return run_accept(d, (char *)d->workspace, (cudaStream_t)stream_ptr, events);
+  return run_accept(d, (char *)d->workspace, d->workspace_bytes, (cudaStream_t)stream_ptr, events);
 }
 
 // Same kernel and arguments as simsd_accept; scratch from the static array
@@ -1444,7 +1653,7 @@ simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream_ptr) 
   if (kAcceptWorkspace > SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES) return SIMSD_ERR_WORKSPACE;
   char *ws = nullptr;
   if (static_scratch(&ws) != cudaSuccess) return SIMSD_ERR_CUDA;
-  return run_accept(d, ws, (cudaStream_t)stream_ptr, nullptr);
+  return run_accept(d, ws, SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES, (cudaStream_t)stream_ptr, nullptr);
 }
 
 }  // extern "C"

@@ -8,6 +8,7 @@
 
 #include <mutex>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace simsd {
@@ -136,7 +137,8 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
       d->B_max > kMaxB || d->total_B < d->batch ||
       (int64_t)d->total_B > (int64_t)d->batch * d->B_max)
     return SIMSD_ERR_SHAPE;
-  if (!(d->sm_scale > 0.0f) || !(d->sm_scale < INFINITY) || !(d->rope_base > 1.0f))
+  if (!(d->sm_scale > 0.0f) || !(d->sm_scale < INFINITY) || !(d->rope_base > 1.0f) ||
+      d->node_size < 0 || d->node_size > kMaxB)
     return SIMSD_ERR_SHAPE;
   memset(p, 0, sizeof(*p));
   p->T = 2 * d->total_B;
@@ -273,7 +275,7 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   simsd_status st = verify_plan(d, &p);
   if (st != SIMSD_OK) return st;
   if (!d->q || !d->k_cache || !d->v_cache || !d->block_table || !d->k_new ||
-      !d->v_new || !d->tau || !d->lens || !d->cu_B || !d->out)
+      !d->v_new || (d->node_size == 0 && !d->tau) || !d->lens || !d->cu_B || !d->out)
     return SIMSD_ERR_NULL;
   if (!aligned16(d->q) || !aligned16(d->k_cache) || !aligned16(d->v_cache) ||
       !aligned16(d->k_new) || !aligned16(d->v_new) || !aligned16(d->out))
@@ -307,10 +309,15 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   a.status = status;
   a.max_pages_per_seq = d->max_pages_per_seq;
   a.num_pages = d->num_pages;
+  a.batch = d->batch;
   a.Hq = d->num_q_heads;
   a.Hkv = d->num_kv_heads;
   a.G = p.G;
   a.T = p.T;
+  a.total_B = d->total_B;
+  a.B_max = d->B_max;
+  a.polls = wait_polls_of(d->wait_polls);
+  a.node_size = d->node_size;
   a.chunk = p.chunk;
   a.rows_per_tile = p.rows_per_tile;
   a.sm_scale = d->sm_scale;

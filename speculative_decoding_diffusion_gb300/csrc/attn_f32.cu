@@ -21,10 +21,13 @@ constexpr int kWarps = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Visibility of key index `key` (0..P+2B-1) for a new row with token index
-// `tok` (0..2B-1), tau of the new tokens in tau_s[0..2B).
-__device__ __forceinline__ bool visible(int P, int B, const int *tau_s, int tok, int key) {
+// `tok` (0..2B-1), tau of the new tokens in tau_s[0..2B); node_size > 0:
+// the draft-graph layout (the row's own node).
+__device__ __forceinline__ bool visible(int P, int B, const int *tau_s, int tok, int key,
+                                        int node_size) {
   if (key < P) return true;
   const int j = key - P;
+  if (node_size > 0) return j / node_size == tok / node_size;
   const int ti = tau_s[tok], tj = tau_s[j];
   const bool row_slot = tok >= B, key_slot = j >= B;
   if (row_slot) return key_slot ? tj >= ti : tj < ti;
@@ -46,15 +49,18 @@ attn_f32_kernel(const __grid_constant__ AttnParams a) {
   const int Lk = P + 2 * B;
   const int M = 2 * B * a.G;
   const int k_begin = split * a.chunk;
-  if (B < 1 || B > kMaxSection || P < 0 || (long)Lk > (long)a.max_pages_per_seq * kPage) {
+  if (B < 1 || B > kMaxSection || B > a.B_max || c0 < 0 || c0 + B > a.total_B || P < 0 ||
+      (long)Lk > (long)a.max_pages_per_seq * kPage ||
+      (a.node_size > 0 && (2 * B) % a.node_size != 0)) {
     if (threadIdx.x == 0 && split == 0 && kvh == 0) raise_status(a.status, kStatusBadInput);
     return;
   }
   if (k_begin >= Lk) return;
   const int k_end = min(Lk, k_begin + a.chunk);
   const int n_splits_b = (Lk + a.chunk - 1) / a.chunk;
-  for (int j = threadIdx.x; j < 2 * B; j += blockDim.x)
-    tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
+  if (a.node_size == 0)
+    for (int j = threadIdx.x; j < 2 * B; j += blockDim.x)
+      tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float *qr = (const float *)a.q_rot;
@@ -75,7 +81,7 @@ attn_f32_kernel(const __grid_constant__ AttnParams a) {
       const int key = base + lane;
       float s = -INFINITY;
       const int kpage = key < k_end ? __ldg(bt + key / kPage) : -1;
-      if (kpage >= 0 && kpage < a.num_pages && visible(P, B, tau_s, tok, key)) {
+      if (kpage >= 0 && kpage < a.num_pages && visible(P, B, tau_s, tok, key, a.node_size)) {
         const int page = kpage;
         const float *kr = kc + (((long)page * a.Hkv + kvh) * kPage + key % kPage) * HD;
         float acc = 0.f;
@@ -134,9 +140,15 @@ combine_kernel(const __grid_constant__ AttnParams a, const int32_t *tok_seq) {
   const int tok = (int)(row / a.Hq);
   const int b = __ldg(tok_seq + tok);
   const int c0 = __ldg(a.cu_B + b);
-  const int Lk = __ldg(a.lens + b) + 2 * (__ldg(a.cu_B + b + 1) - c0);
+  const int B = __ldg(a.cu_B + b + 1) - c0;
+  const int P = __ldg(a.lens + b);
+  const int Lk = P + 2 * B;
   const int ns = (Lk + a.chunk - 1) / a.chunk;
-  if (ns <= 1 || (long)Lk > (long)a.max_pages_per_seq * kPage) return;
+  // malformed sequences (the attention kernel flagged and skipped them)
+  if (B < 1 || B > kMaxSection || B > a.B_max || c0 < 0 || c0 + B > a.total_B || P < 0 ||
+      (long)Lk > (long)a.max_pages_per_seq * kPage)
+    return;
+  if (ns <= 1) return;
   const long stride = (long)a.T * a.Hq;
   float mstar = -INFINITY;
   for (int s = 0; s < ns; ++s) mstar = fmaxf(mstar, a.ml_part[s * stride + row].x);

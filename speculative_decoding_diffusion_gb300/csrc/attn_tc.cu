@@ -146,7 +146,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int B = __ldg(a.cu_B + b + 1) - c0;
   const int P = __ldg(a.lens + b);
   const int Lk = P + 2 * B;
-  if (B < 1 || B > kMaxSection || P < 0 || (long)Lk > (long)a.max_pages_per_seq * kPage) {
+  if (B < 1 || B > kMaxSection || B > a.B_max || c0 < 0 || c0 + B > a.total_B || P < 0 ||
+      (long)Lk > (long)a.max_pages_per_seq * kPage ||
+      (a.node_size > 0 && (2 * B) % a.node_size != 0)) {
     if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) raise_status(a.status, kStatusBadInput);
     return;
   }
@@ -203,12 +205,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  int issued = 0;                            // producer: blocks whose loads were started
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
     if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
     const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
-    int issued = 0;
     bool dep_done = false;
     for (int j = 0; j < n_blocks; ++j) {
       const int s = j % kStages;
@@ -219,7 +221,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       }
       const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
       const int page = lane < n_pages ? __ldg(bt + kb / kPage + lane) : 0;   // before the wait
-      if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1)) {
+      if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1, a.polls)) {
         if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
         break;
       }
@@ -236,11 +238,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       }
       issued = j + 1;
     }
-    if (*(volatile int *)flag_s) {
-      // let copies already in flight land before the CTA can exit
-      for (int j = max(0, issued - kStages); j < issued; ++j)
-        (void)mbar_wait_warp(bar(kBarKvFull + j % kStages), (j / kStages) & 1);
-    }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     // One thread issues both MMA kinds as their inputs become ready: S of
@@ -249,9 +246,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(kRows, kKeys, 0);
       constexpr uint32_t idO = tc::idesc_bf16(kRows, HD, 1);
-      bool ok = mbar_wait(bar(kBarQReady), 0);
+      bool ok = mbar_wait(bar(kBarQReady), 0, a.polls);
       int ns = 0, np = 0;
-      uint32_t idle = 0;
+      uint64_t idle = 0;
       while (ok && np < n_blocks) {
         bool progressed = false;
         if (ns < n_blocks) {
@@ -291,7 +288,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
         if (progressed) {
           idle = 0;
-        } else if (++idle > (kWaitPolls << 4)) {  // bounded: give up, flag, drain
+        } else if (++idle > ((uint64_t)a.polls << 4)) {  // bounded: give up, flag, drain
           ok = false;
         }
       }
@@ -322,13 +319,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // Q rotated into TMEM (one row per thread, two bf16 per column, zeros
     // for padding rows); then the issuer may start
     const int t = threadIdx.x - 64;
+    const bool graph = a.node_size > 0;        // draft-graph nodes instead of D | D~
+    const int npos = graph ? a.node_size : B;  // distinct positions of the new tokens
     float2 *cs_s = reinterpret_cast<float2 *>(sb + L::kOffCs);
-    for (int j = t; j < 2 * B; j += kSoftmax) tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
-    for (int e = t; e < B * (HD / 2); e += kSoftmax)
+    if (!graph)
+      for (int j = t; j < 2 * B; j += kSoftmax) tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
+    for (int e = t; e < npos * (HD / 2); e += kSoftmax)
       cs_s[e] = rope_cs(a.tab, e % (HD / 2), P + e / (HD / 2));   // D~_k copies D_k's position
     named_sync(1, kSoftmax);
     {
-      const int kq = row_valid ? (tok < B ? tok : tok - B) : 0;   // response index
+      const int kq = !row_valid ? 0 : graph ? tok % a.node_size : (tok < B ? tok : tok - B);
       const float2 *cs = cs_s + kq * (HD / 2);
 #pragma unroll
       for (int d0 = 0; d0 < HD / 2; d0 += 32) {
@@ -354,13 +354,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(kBarQReady));
-    const int row_tau = tau_s[tok];
     // this row's visibility of the 2B new keys (bit jj: new key jj), built
-    // while the first K/V stage is still in flight
+    // while the first K/V stage is still in flight: the temporal mask, or
+    // (draft-graph layout) the tokens of the row's own node
     uint64_t newvis = 0;
+    if (graph) {
+      newvis = low_bits(a.node_size) << ((tok / a.node_size) * a.node_size);
+    } else {
+      const int row_tau = tau_s[tok];
 #pragma unroll 8
-    for (int jj = 0; jj < 2 * B; ++jj)
-      if (visible_new(jj, B, tau_s, row_slot, row_tau)) newvis |= 1ull << jj;
+      for (int jj = 0; jj < 2 * B; ++jj)
+        if (visible_new(jj, B, tau_s, row_slot, row_tau)) newvis |= 1ull << jj;
+    }
     const uint32_t tO = trow + kColO;
     const float scale = a.sm_scale * kLog2e;
     float m_ref = -INFINITY, l = 0.f;
@@ -374,7 +379,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       for (; warp_valid && j < n_blocks; ++j) {
         const int tb = j & 1;
         const uint32_t tS = trow + kColS + tb * kKeys;
-        if (!mbar_wait_warp(bar(kBarSFull + tb), (j >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait_warp(bar(kBarSFull + tb), (j >> 1) & 1, a.polls)) { ok = false; break; }
         tc::fence_after_sync();
         const int kb = k_begin + j * kKeys;
         // visibility of this warp's keys: prompt keys below the split's end
@@ -420,7 +425,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         const float alpha = move ? ex2(m_ref - m_new) : 1.f;     // m_ref = -inf -> 0
         if (j > 0 && __any_sync(0xffffffffu, move)) {
           // rescaling O needs the previous block's P.V done
-          if (!mbar_wait_warp(bar(kBarPvDone + (tb ^ 1)), ((j - 1) >> 1) & 1)) { ok = false; break; }
+          if (!mbar_wait_warp(bar(kBarPvDone + (tb ^ 1)), ((j - 1) >> 1) & 1, a.polls)) { ok = false; break; }
           tc::fence_after_sync();
 #pragma unroll 1
           for (int c = 0; c < HD / 32; ++c) {
@@ -495,7 +500,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     else if (R == 2) key_loop(IntC<2>{});
     else key_loop(IntC<1>{});
     if (ok && j > 0 &&
-        !mbar_wait_warp(bar(kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1))
+        !mbar_wait_warp(bar(kBarPvDone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, a.polls))
       ok = false;
     if (!ok && lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
     tc::fence_after_sync();
@@ -585,6 +590,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   // -------------------------------------------------------------- teardown
   tc::fence_before_sync();
   __syncthreads();
+  // after a wait that gave up (any warp's: the flag is final here), the
+  // copies still in flight land before the CTA can exit (default limit)
+  if (warp == 0 && *(volatile int *)flag_s)
+    for (int j = max(0, issued - kStages); j < issued; ++j)
+      (void)mbar_wait_warp(bar(kBarKvFull + j % kStages), (j / kStages) & 1);
   if (warp == 1) {
     tc::fence_after_sync();
     tc::dealloc(tmem, L::kTmemCols);

@@ -107,19 +107,30 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of the barrier to complete; false after kWaitPolls
-// unsuccessful polls (each try_wait itself blocks for a bounded time).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
+// Wait for phase `parity` of the barrier to complete; false after `polls`
+// unsuccessful polls (each try_wait itself blocks for a bounded time; 0
+// polls gives up at once).  The kernels' own waits take the caller's limit
+// (wait_polls of the descriptors); the waits that drain copies still in
+// flight before a CTA exits always take the default kWaitPolls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint32_t polls = kWaitPolls) {
+  for (uint32_t i = 0; i < polls; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
 
 // Whole-warp wait: every lane polls (each needs the acquire), and the
 // outcome is made warp-uniform so the caller can branch on it safely.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               uint32_t polls = kWaitPolls) {
+  const bool ok = mbar_wait(bar, parity, polls);
   return __all_sync(0xffffffffu, ok);
+}
+
+// Polls of the kernels' bounded waits from a descriptor's wait_polls field:
+// 0 selects the default, a negative value gives up at once.
+__host__ __device__ __forceinline__ uint32_t wait_polls_of(int32_t field) {
+  return field == 0 ? kWaitPolls : field < 0 ? 0u : (uint32_t)field;
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later

@@ -64,8 +64,12 @@ struct AttnParams {
   uint32_t *status;
   int max_pages_per_seq;
   int num_pages;
+  int batch;
   int Hq, Hkv, G, T;
+  int total_B, B_max;         // host copies: a sequence's cu_B and B must fit them
+  int node_size;              // 0: SimSD's temporal layout; > 0: draft-graph nodes
   int chunk, rows_per_tile;
+  uint32_t polls;             // bounded-wait polls (wait_polls_of the descriptor)
   float sm_scale;
   RopeTable tab;              // angles of the query rotation (bf16 kernel)
 };

@@ -140,6 +140,9 @@ struct RopeVerifyArgs {
   int32_t *tok_seq;
   uint32_t *status;
   int batch, Hq, Hkv, hd, max_pages, num_pages;
+  int total_B, B_max;   // host copies: a sequence's cu_B and B must fit them
+  uint32_t polls;       // bounded-wait polls
+  int node_size;        // 0: SimSD's paired layout; > 0: draft-graph nodes
   int rotate_q;         // write rotated queries to q_rot (fp32 path)
 };
 
@@ -189,17 +192,22 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
   }
   if (threadIdx.x == 0) a.tok_seq[r] = b;    // the merge kernel reads it
   const int j = r - 2 * c0;                  // 0..2B-1 within the sequence
-  const int k = j < B ? j : j - B;           // response index (0-based)
-  const int pos = P + k;                     // D~_k copies D_k's position
+  // response index (0-based): D~_k copies D_k's position; in the
+  // draft-graph layout every node's token k sits at the same position
+  const int k = a.node_size > 0 ? j % a.node_size : (j < B ? j : j - B);
+  const int pos = P + k;
   const int slot = P + j;                    // layout index = cache slot
-  bool ok = !(B < 1 || B > kMaxSection || P < 0 || (long)P + 2 * B > (long)a.max_pages * kPage);
+  bool ok = !(B < 1 || B > kMaxSection || B > a.B_max || c0 < 0 || c0 + B > a.total_B ||
+              j < 0 || j >= 2 * B || P < 0 || (long)P + 2 * B > (long)a.max_pages * kPage ||
+              (a.node_size > 0 && (2 * B) % a.node_size != 0));
   const int page = ok ? __ldg(a.block_table + (long)b * a.max_pages + slot / kPage) : -1;
   ok = ok && page >= 0 && page < a.num_pages;   // cu_B or block table out of range
   if (!ok && threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
   if (ok) angles(a.tab, a.hd, pos, cs);
   __syncthreads();
-  // every exit waits for the copies into this CTA's shared memory
-  if (!mbar_wait(bar, 0)) {
+  // every exit waits for the copies into this CTA's shared memory (the
+  // drain after a wait that gave up takes the default limit)
+  if (!mbar_wait(bar, 0, a.polls)) {
     if (threadIdx.x == 0) raise_status(a.status, kStatusTimeout);
     (void)mbar_wait(bar, 0);
     return;
@@ -271,6 +279,10 @@ cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
   a.Hkv = d->num_kv_heads;
   a.hd = d->head_dim;
   a.max_pages = d->max_pages_per_seq;
+  a.total_B = d->total_B;
+  a.B_max = d->B_max;
+  a.polls = wait_polls_of(d->wait_polls);
+  a.node_size = d->node_size;
   a.rotate_q = d->dtype == SIMSD_F32;
   const size_t smem = (size_t)((a.rotate_q ? a.Hq : 0) + 2 * a.Hkv) * a.hd * p.esize;   // <= kMaxRowBytes
   const void *kern = d->dtype == SIMSD_BF16 ? (const void *)rope_verify_kernel<__nv_bfloat16>

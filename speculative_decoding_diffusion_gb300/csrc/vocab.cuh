@@ -1,0 +1,224 @@
+// vocab.cuh -- device helpers of the kernels that sweep vocabulary rows
+// (the acceptance rules and the draft-side step): compensated fp32 pairs,
+// 2^x on the MUFU, thread-block-cluster barriers and distributed shared
+// memory, and 16-byte vectors of bf16 or fp32 logits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace simsd {
+namespace vocab {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------ two-sum pairs
+// value = hi + lo with |lo| <= ulp(hi)/2 (Knuth's two-sum; Dekker's
+// fast-two-sum for the renormalisation).
+struct Ff {
+  float hi, lo;
+};
+__device__ __forceinline__ Ff ff_add(Ff a, Ff b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float err = (a.hi - (s - bb)) + (b.hi - bb);
+  const float lo = err + a.lo + b.lo;
+  const float hi = s + lo;
+  return Ff{hi, lo - (hi - s)};
+}
+__device__ __forceinline__ Ff ff_of(float x) { return Ff{x, 0.f}; }
+__device__ __forceinline__ Ff ff_neg(Ff a) { return Ff{-a.hi, -a.lo}; }
+__device__ __forceinline__ Ff ff_shfl_xor(Ff a, int m) {
+  return Ff{__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
+}
+__device__ __forceinline__ Ff ff_shfl_up(Ff a, int d) {
+  return Ff{__shfl_up_sync(0xffffffffu, a.hi, d), __shfl_up_sync(0xffffffffu, a.lo, d)};
+}
+__device__ __forceinline__ Ff ff_shfl(Ff a, int l) {
+  return Ff{__shfl_sync(0xffffffffu, a.hi, l), __shfl_sync(0xffffffffu, a.lo, l)};
+}
+// a > u where u is a pair: compare the exact sums' signs
+__device__ __forceinline__ bool ff_gt(Ff a, Ff u) {
+  const Ff d = ff_add(a, ff_neg(u));
+  return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
+}
+
+// 2^x on the MUFU (approximate, ~2 ulp; subnormal results flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// The logits' scale into log2 units, log2(e) / temperature, as an
+// unevaluated float pair hi + lo (from double on the host): a single float
+// would act like a temperature off by up to 2^-24 relative, which shifts
+// the whole distribution's shape consistently (an error that does not
+// average out over the vocabulary, unlike per-entry rounding).
+// hi is the float just below the exact scale, so lo > 0: a -inf logit then
+// gives -inf + (-inf) in the argument (mass 0), never -inf + inf (NaN).
+struct Scale {
+  float hi, lo;
+};
+inline Scale scale_of(double temperature) {
+  const double l = 1.4426950408889634074 / temperature;
+  float hi = (float)l;
+  if ((double)hi >= l) hi = nextafterf(hi, 0.f);
+  return Scale{hi, (float)(l - (double)hi)};
+}
+
+// 2^(x (hi + lo) - R): x hi - R exact before one rounding, then x lo added
+// with one more (the rounding is at the scale of the result's argument).
+__device__ __forceinline__ float rel_exp(float x, float R, Scale ls) {
+  return ex2(fmaf(x, ls.lo, fmaf(x, ls.hi, -R)));
+}
+
+// References (the R above) are whole numbers: ceil(max * hi) for a set of
+// logits whose largest is max, so every entry's argument is at most ~0.
+// Partial sums taken against different references then combine through
+// exact powers of two (exp2_int), and a hierarchy of partial masses
+// (slices, pieces, ranges) adds up to exactly what a scan of the entries
+// against the final reference sees, up to the sums' own rounding.
+__device__ __forceinline__ float ref_of(float mx, Scale ls) { return ceilf(mx * ls.hi); }
+
+// 2^d for a whole number d (0 below the normal range, -inf included).
+__device__ __forceinline__ float exp2_int(float d) {
+  return d < -126.f ? 0.f : d > 127.f ? INFINITY : __int_as_float(((int)d + 127) << 23);
+}
+
+// a / b for pairs (Dekker's division: quotient, remainder by fma, one
+// correction term); a / a is exactly (1, 0).
+__device__ __forceinline__ Ff ff_div(Ff a, Ff b) {
+  const float q1 = a.hi / b.hi;
+  const float r = fmaf(-q1, b.hi, a.hi) + a.lo - q1 * b.lo;
+  const float q2 = r / b.hi;
+  const float hi = q1 + q2;
+  return Ff{hi, q2 - (hi - q1)};
+}
+
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// ---------------------------------------------------------------- cluster
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+// Address of the same shared-memory variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem(const void *p, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_dsmem2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_dsmem_i32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_dsmem4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- logits
+// Raw 16-byte vectors of logits: unpacking, lane-wise maximum, the -inf fill.
+template <typename T> struct Ld;
+template <> struct Ld<float> {
+  static constexpr int N = 4;
+  static constexpr uint32_t kNegInf = 0xff800000u;
+  static __device__ __forceinline__ uint4 neg_inf() { return make_uint4(kNegInf, kNegInf, kNegInf, kNegInf); }
+  static __device__ __forceinline__ float value(float v) { return v; }
+  static __device__ __forceinline__ float neg_inf_elem() { return -INFINITY; }
+  static __device__ __forceinline__ void unpack(uint4 v, float *f) {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+  // the vector at p (16-byte aligned if `aligned`): entries past `valid`
+  // (which may be <= 0) read as -inf
+  static __device__ __forceinline__ uint4 load(const float *p, int valid, bool aligned) {
+    if (aligned && valid >= N) return *reinterpret_cast<const uint4 *>(p);
+    uint32_t r[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) r[e] = e < valid ? __float_as_uint(p[e]) : kNegInf;
+    return make_uint4(r[0], r[1], r[2], r[3]);
+  }
+  static __device__ __forceinline__ float vmax(const uint4 *w, int n) {
+    float m0 = -INFINITY, m1 = -INFINITY;
+    for (int i = 0; i < n; ++i) {
+      m0 = fmaxf(m0, fmaxf(__uint_as_float(w[i].x), __uint_as_float(w[i].y)));
+      m1 = fmaxf(m1, fmaxf(__uint_as_float(w[i].z), __uint_as_float(w[i].w)));
+    }
+    return fmaxf(m0, m1);
+  }
+};
+template <> struct Ld<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static constexpr uint32_t kNegInf2 = 0xff80ff80u;
+  static __device__ __forceinline__ uint4 neg_inf() { return make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2); }
+  static __device__ __forceinline__ float value(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 neg_inf_elem() { return __ushort_as_bfloat16(0xff80); }
+  static __device__ __forceinline__ void unpack(uint4 v, float *f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+  static __device__ __forceinline__ uint4 load(const __nv_bfloat16 *p, int valid, bool aligned) {
+    if (aligned && valid >= N) return *reinterpret_cast<const uint4 *>(p);
+    uint32_t r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = 2 * i < valid ? __bfloat16_as_ushort(p[2 * i]) : 0xff80u;
+      const uint32_t hi = 2 * i + 1 < valid ? __bfloat16_as_ushort(p[2 * i + 1]) : 0xff80u;
+      r[i] = lo | (hi << 16);
+    }
+    return make_uint4(r[0], r[1], r[2], r[3]);
+  }
+  static __device__ __forceinline__ uint32_t max2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  // packed maximum of the bf16 pairs (exact), then of the two halves
+  static __device__ __forceinline__ float vmax(const uint4 *w, int n) {
+    uint32_t m = kNegInf2;
+    for (int i = 0; i < n; ++i) m = max2(m, max2(max2(w[i].x, w[i].y), max2(w[i].z, w[i].w)));
+    return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+  }
+};
+
+// Element e (dynamic) of the N entries held in vector w.
+template <typename T>
+__device__ __forceinline__ float pick(uint4 w, int e) {
+  float f[Ld<T>::N];
+  Ld<T>::unpack(w, f);
+  float v = f[0];
+#pragma unroll
+  for (int i = 1; i < Ld<T>::N; ++i)
+    if (e == i) v = f[i];
+  return v;
+}
+
+}  // namespace vocab
+}  // namespace simsd

@@ -48,20 +48,23 @@ class Spec:
     shuffled_pages: bool = False
     raw_prompt_keys: bool = False
     sm_scale: float = 1.0
+    slug: str = ""            # short file-name form of the name
 
 
 CONFIGS = {
     0: Spec("tiny: 1 seq, P=64, B=4, Hq4/Hkv2/hd64, fp32, V=512", batch=1,
             prompt=64, B=4, Hq=4, Hkv=2, hd=64, dtype="f32", rope_base=1.0e4,
             vocab=512, qkv_sd=1.0 / 8.0, q_scale=1.0, logit_sd=2.0,
-            noise_sd=0.5, raw_prompt_keys=True),
-    1: Spec("sdar8b-verify: 16 seq, P=1024, B=4", batch=16, prompt=1024, B=4),
-    2: Spec("sdar8b-verify: 64 seq, P=4096, B=8", batch=64, prompt=4096, B=8),
+            noise_sd=0.5, raw_prompt_keys=True, slug="tiny_1x64_B4"),
+    1: Spec("sdar8b-verify: 16 seq, P=1024, B=4", batch=16, prompt=1024, B=4,
+            slug="sdar8b_16x1024_B4"),
+    2: Spec("sdar8b-verify: 64 seq, P=4096, B=8", batch=64, prompt=4096, B=8,
+            slug="sdar8b_64x4096_B8"),
     3: Spec("long-prefix: 8 seq, P=32768, B=16, shuffled pages", batch=8,
-            prompt=32768, B=16, shuffled_pages=True),
+            prompt=32768, B=16, shuffled_pages=True, slug="longprefix_8x32768_B16"),
     4: Spec("ragged-mix: 256 seq, P~U[256,8192], B in {4,8}", batch=256,
             prompt=(256, 8192), B=(4, 8), noise_sd=(0.25, 2.0),
-            shuffled_pages=True),
+            shuffled_pages=True, slug="ragged_256xU256-8192_B4-8"),
 }
 
 
@@ -210,6 +213,23 @@ def make(spec: Spec, seed: int, with_logits: bool = True,
     return Workload(spec, seed, lens_a, Bs_a, cu_B, tau, num_pages, max_pages,
                     block_table, q, k_prompt, v_prompt, k_new, v_new, target,
                     draft, draft_tokens, uniforms)
+
+
+def head(w: Workload, n: int) -> Workload:
+    """The first n sequences of w as a workload of their own (array slices
+    and the matching prefix of the block table; pages keep their ids)."""
+    n = min(n, len(w.lens))
+    off = w.prompt_offsets
+    nB, T, nP = int(w.cu_B[n]), 2 * int(w.cu_B[n]), int(off[n])
+    spec = dataclasses.replace(w.spec, batch=n)
+    return Workload(spec, w.seed, w.lens[:n], w.Bs[:n], w.cu_B[:n + 1], w.tau[:nB],
+                    w.num_pages, w.max_pages,
+                    w.block_table[:n], w.q[:T], w.k_prompt[:nP], w.v_prompt[:nP],
+                    w.k_new[:T], w.v_new[:T],
+                    None if w.target is None else w.target[:nB],
+                    None if w.draft is None else w.draft[:nB],
+                    None if w.draft_tokens is None else w.draft_tokens[:nB],
+                    None if w.uniforms is None else w.uniforms[:n])
 
 
 def config(i: int, **kw) -> Workload:

@@ -200,3 +200,36 @@ def test_accept_rule_and_temperature_checks(lib):
     assert lib.simsd_accept(ctypes.byref(d), None) == 1
     d.uniforms = fake
     assert lib.simsd_accept(ctypes.byref(d), None) == 5          # but no draft logits
+
+
+def test_descriptor_layouts_match_the_header(tmp_path):
+    """The binding's ctypes descriptors have the header's field offsets and
+    sizes (a C program compiled against include/simsd.h prints them)."""
+    import shutil
+    import subprocess
+    from speculative_decoding_diffusion_gb300 import binding
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"simsd_verify_desc": binding.VerifyDesc, "simsd_accept_desc": binding.AcceptDesc,
+               "simsd_append_desc": binding.AppendDesc}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "simsd.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append('  printf("%s sizeof %%zu\\n", sizeof(%s));' % (cname, cname))
+        for f, _ in py._fields_:
+            lines.append('  printf("%s %s %%zu\\n", offsetof(%s, %s));' % (cname, f, cname, f))
+    lines.append("  return 0;\n}")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    inc = os.path.join(ROOT, "include")
+    subprocess.run([cc, "-I", inc, str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    got = {}
+    for line in out.splitlines():
+        a, b, c = line.split()
+        got[(a, b)] = int(c)
+    for cname, py in structs.items():
+        assert got[(cname, "sizeof")] == ctypes.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)

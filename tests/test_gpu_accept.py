@@ -21,23 +21,37 @@ from speculative_decoding_diffusion_gb300.staging import DeviceWorkload
 pytestmark = pytest.mark.gpu
 
 
-def run_accept(w):
+def run_accept(w, status_only=False):
+    """simsd_accept with the workspace size the library asks for (the
+    two-kernel path: chunk pass, then the per-sequence cluster kernel) or,
+    with status_only, a workspace of just the status word (the single
+    cluster kernel streaming the rows itself)."""
     dw = DeviceWorkload(w, with_verify=False)
-    dw.accept()
+    if status_only:
+        ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+        binding.accept(dw.target, dw.draft, dw.draft_tokens, dw.tau, dw.cu_B, dw.uniforms,
+                       dw.n_accept, dw.token, dw.pos, ws, dw.total_B, dw.B_max)
+    else:
+        ws = dw.accept_ws
+        dw.accept()
     torch.cuda.synchronize()
-    assert binding.read_status(dw.accept_ws) == 0
+    assert binding.read_status(ws) == 0
     return (dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy())
 
 
+@pytest.mark.parametrize("path", ["two-kernel", "single-launch"])
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
-def test_configs_match_oracle(cfg):
+def test_configs_match_oracle(cfg, path):
     w = synth.config(cfg)
-    n, tok, pos = run_accept(w)
+    n, tok, pos = run_accept(w, status_only=path == "single-launch")
     ref = parity.oracle_accept(w)
-    step_ties, draw_ties, draws = parity.check_accept(w, ref, n, tok, pos)
-    print("cfg%d: %d sequences, %d residual draws, %d draw ties, %d step ties"
-          % (cfg, len(w.lens), draws, draw_ties, step_ties))
+    stats = []
+    step_ties, draw_ties, draws = parity.check_accept(w, ref, n, tok, pos, stats=stats)
+    rep = parity.tie_report(stats)
+    print("cfg%d %s: %d sequences, %d residual draws, %d draw ties, %d step ties; %s"
+          % (cfg, path, len(w.lens), draws, draw_ties, step_ties, rep))
     assert step_ties == 0
+    assert draw_ties <= 0.02 * draws, (draw_ties, draws)
 
 
 def tiny_accept_spec(**kw):
@@ -49,21 +63,23 @@ def tiny_accept_spec(**kw):
 
 @pytest.mark.parametrize("dtype,vocab", [("bf16", 1003), ("bf16", 4096 + 8), ("f32", 777),
                                          ("f32", 2048), ("bf16", 9)])
-def test_odd_vocab_and_mixed_B(dtype, vocab):
+@pytest.mark.parametrize("status_only", [False, True])
+def test_odd_vocab_and_mixed_B(dtype, vocab, status_only):
     w = synth.make(tiny_accept_spec(dtype=dtype, vocab=vocab), seed=vocab)
-    n, tok, pos = run_accept(w)
+    n, tok, pos = run_accept(w, status_only)
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
 
 
 @pytest.mark.parametrize("dtype,vocab,batch,B", [("bf16", 151936, 2, 32), ("bf16", 65539, 3, 32),
                                                  ("f32", 100003, 4, 17), ("bf16", 151936, 5, 1)])
-def test_few_sequences_large_clusters(dtype, vocab, batch, B):
+@pytest.mark.parametrize("status_only", [False, True])
+def test_few_sequences_large_clusters(dtype, vocab, batch, B, status_only):
     """Few sequences get the largest clusters (up to 16 CTAs each): slices
     of 1/16 of the vocabulary, the slice merge in 16-lane groups and, at
     B = 32, in two rounds of pairs; element copies where rows are not
     16-byte multiples."""
     w = synth.make(tiny_accept_spec(batch=batch, B=B, dtype=dtype, vocab=vocab), seed=vocab + B)
-    n, tok, pos = run_accept(w)
+    n, tok, pos = run_accept(w, status_only)
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
 
 
@@ -229,14 +245,19 @@ def test_greedy_matches_oracle(name):
     assert (n > 0).any() and (n < w.Bs).any()
 
 
-@pytest.mark.parametrize("name,T", [("sdar8b", 0.5), ("sdar8b", 2.0), ("f32-777", 0.7),
+# temperatures are floats in the ABI: values a float holds exactly, so that
+# the oracle divides by the same number
+@pytest.mark.parametrize("name,T", [("sdar8b", 0.5), ("sdar8b", 2.0), ("f32-777", 0.75),
                                     ("bf16-1003", 1.5)])
 def test_temperature_matches_oracle(name, T):
     """Sampling at temperature T: p = softmax(target / T), q = softmax(draft / T);
     decisions exact outside the tie zone, valid inside."""
     w = variant_case(name)
     n, tok, pos = run_rule(w, binding.SIMSD_ACCEPT_SAMPLE, T)
-    parity.check_accept(w, parity.oracle_accept(w, T), n, tok, pos, T)
+    step_ties, draw_ties, draws = parity.check_accept(w, parity.oracle_accept(w, T), n, tok,
+                                                      pos, T)
+    print("%s T=%g: %d draws, %d draw ties, %d step ties" % (name, T, draws, draw_ties, step_ties))
+    assert step_ties == 0 and draw_ties <= parity.max_ties(draws)
 
 
 def check_match(w, n, tok, pos, temperature=1.0, tie=parity.TIE_RESIDUAL):
@@ -272,8 +293,8 @@ def check_match(w, n, tok, pos, temperature=1.0, tie=parity.TIE_RESIDUAL):
     return ties
 
 
-@pytest.mark.parametrize("name,T", [("sdar8b", 1.0), ("bf16-1003", 1.0), ("f32-777", 0.8),
-                                    ("bf16-few", 1.0), ("f32-odd", 1.3)])
+@pytest.mark.parametrize("name,T", [("sdar8b", 1.0), ("bf16-1003", 1.0), ("f32-777", 0.875),
+                                    ("bf16-few", 1.0), ("f32-odd", 1.25)])
 def test_sample_matching_matches_oracle(name, T):
     """Sample matching (accept iff the target's own inverse-CDF sample at
     u[t-1] equals the draft token; the rejection emits that sample): exact
@@ -298,6 +319,6 @@ def test_sample_matching_matches_oracle(name, T):
     assert binding.read_status(dw.accept_ws) == 0
     n, tok, pos = dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy()
     ties = check_match(w, n, tok, pos, T)
-    if w.spec.vocab < 2000:          # large bins: nearly every decision is checked exactly
-        assert ties <= 4
+    print("%s T=%g: %d sequences, %d with a tie-zone draw" % (name, T, len(w.lens), ties))
+    assert ties <= parity.max_ties(len(w.lens))
     assert (n > 0).any()

@@ -1,8 +1,7 @@
 """GPU parity of simsd_verify_attn (K1 + K2 + K3) against the fp64 oracle.
 
-Every case calls the library through the C ABI on seeded synthetic inputs.
-Small cases are compared on every output row; the full-size workloads on
-sampled rows (the oracle computes one row at a time).  Also checked: the
+Every case calls the library through the C ABI on seeded synthetic inputs
+and is compared on every output row, the full-size workloads included.  Also checked: the
 cache slots K1 writes (placement bit-exact, values within bf16 rounding of
 the oracle's rotation), that nothing else in the cache changes, the RoPE
 copy (equal raw inputs at D_k and D~_k give bit-identical cached keys),
@@ -175,28 +174,16 @@ def test_deterministic():
     assert all(np.array_equal(outs[0], o) for o in outs[1:])
 
 
-def sampled_rows(w, per_seq, seed):
-    rng = np.random.default_rng(seed)
-    picks = []
-    for b in range(len(w.lens)):
-        twoB = 2 * int(w.Bs[b])
-        toks = rng.integers(0, twoB, per_seq)
-        heads = rng.integers(0, w.spec.Hq, per_seq)
-        picks.append(list(zip(toks.tolist(), heads.tolist())))
-    return picks
-
-
-@pytest.mark.parametrize("cfg,seqs,per_seq", [(2, 8, 6), (3, 8, 8), (4, 12, 4)])
-def test_full_size_sampled(cfg, seqs, per_seq):
+@pytest.mark.slow
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_full_size_all_rows(cfg):
+    """Every output row of the 64 x 4096, 8 x 32768 (shuffled pages) and
+    256-sequence ragged workloads, in the bench's launch configuration,
+    against the fp64 oracle."""
     w = synth.config(cfg, with_logits=False)
     _, got = run(w)
     assert np.isfinite(got).all()
-    picks = sampled_rows(w, per_seq, seed=cfg)
-    rng = np.random.default_rng(cfg + 50)
-    chosen = rng.choice(len(w.lens), size=min(seqs, len(w.lens)), replace=False)
-    for b in chosen:
-        rows = picks[b]
-        ref = parity.oracle_seq(w, b, rows=rows)
-        t0 = 2 * int(w.cu_B[b])
-        g = np.stack([got[t0 + t, h] for t, h in rows])
-        parity.check_attention(g, ref, "bf16")
+    ref = parity.oracle_full_size(w)
+    err = parity.check_attention(got, ref, "bf16")
+    print("cfg%d: %d rows, max row rel err %.3g, mean %.3g"
+          % (cfg, err.size, err.max(), err.mean()))

@@ -3,11 +3,13 @@
 Serving loops with a fixed device-memory budget, or plugins whose host
 framework owns all device memory, cannot hand the library a workspace from
 cudaMalloc.  The no-allocation entry point keeps its scratch in a static
-device array instead.  Its decisions must equal those of simsd_accept (the
-same kernels on the same inputs, so integers compare exactly), on two calls
-in a row -- the second call sees the first call's leftovers in the shared
-array -- and the static array covers the scratch of every valid size
-(one status word), while invalid sizes are refused before anything runs.
+device array instead.  Its decisions must equal those of simsd_accept on a
+workspace of the same size (the same kernel on the same inputs, so integers
+compare exactly), and agree with simsd_accept's default path within the
+tie zone of the other acceptance tests, on two calls in a row -- the second
+call sees the first call's leftovers in the shared array -- and the static
+array covers the single-launch scratch of every valid size (one status
+word), while invalid sizes are refused before anything runs.
 
 This file is named to be collected last: it must pass both on its own in a
 fresh process and after every other test.
@@ -16,6 +18,7 @@ import numpy as np
 import pytest
 import torch
 
+import parity
 import synth
 from speculative_decoding_diffusion_gb300 import binding
 from speculative_decoding_diffusion_gb300.staging import DeviceWorkload
@@ -29,26 +32,38 @@ def _outputs(dw):
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
+    """Two calls in a row.  The static scratch holds the status word, so the
+    no-allocation call runs the single-launch kernel: its decisions equal
+    simsd_accept's on a workspace of the same size (the same kernel), and
+    agree with the oracle -- and so with simsd_accept's default two-kernel
+    path -- exactly outside the tie zone the other acceptance tests use."""
     w = synth.config(1)                       # 16 x vocab 151936, bf16
     dw = DeviceWorkload(w, with_verify=False)
     args = (dw.target, dw.draft, dw.draft_tokens, dw.tau, dw.cu_B, dw.uniforms,
             dw.n_accept, dw.token, dw.pos, dw.total_B, dw.B_max)
+    status_ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     rng = np.random.default_rng(77)
     for call in range(2):
         if call == 1:   # second call: other uniforms, same shared scratch
-            dw.uniforms.copy_(torch.from_numpy(
-                rng.random(tuple(dw.uniforms.shape), dtype=np.float32)))
+            w.uniforms = rng.random(tuple(dw.uniforms.shape), dtype=np.float32)
+            dw.uniforms.copy_(torch.from_numpy(w.uniforms))
+        binding.accept(*args[:9], status_ws, *args[9:])
+        torch.cuda.synchronize()
+        same_kernel = _outputs(dw)
         dw.accept()
         torch.cuda.synchronize()
-        ref = _outputs(dw)
+        default = _outputs(dw)
         for t in (dw.n_accept, dw.token, dw.pos):
             t.fill_(-7)
         binding.accept_noalloc(*args)
         torch.cuda.synchronize()
         got = _outputs(dw)
-        for g, r in zip(got, ref):
+        for g, r in zip(got, same_kernel):
             np.testing.assert_array_equal(g, r)
         assert (got[0] >= 0).all()
+        ref = parity.oracle_accept(w)
+        parity.check_accept(w, ref, *got)
+        parity.check_accept(w, ref, *default)
 
 
 def test_noalloc_scratch_covers_every_size_and_refuses_bad_ones():
@@ -57,8 +72,15 @@ def test_noalloc_scratch_covers_every_size_and_refuses_bad_ones():
     for k, v in dict(batch=4096, vocab=1 << 21, total_B=4096 * 32, B_max=32,
                      dtype=binding.SIMSD_F32).items():
         setattr(d, k, v)
-    # the largest valid sizes still need only the status word
-    assert 0 < lib.simsd_accept_workspace_size(d) <= 4096
+    # the largest valid sizes: the single-launch path (the no-allocation
+    # entry point's) needs only the status word for every rule -- what the
+    # greedy and matching rules ask for -- while the sampling rule's
+    # two-kernel path asks for more, which this entry point does not use
+    for rule in (binding.SIMSD_ACCEPT_GREEDY, binding.SIMSD_ACCEPT_MATCH):
+        d.rule = rule
+        assert 0 < lib.simsd_accept_workspace_size(d) <= 4096
+    d.rule = binding.SIMSD_ACCEPT_SAMPLE
+    assert lib.simsd_accept_workspace_size(d) > 4096
     fake = 1 << 40   # never dereferenced: every call below returns before launching
     for f in ("target_logits", "draft_logits", "draft_tokens", "tau", "cu_B",
               "uniforms", "n_accept", "token", "pos"):
