@@ -4,9 +4,11 @@ One step = the whole hot path over one batch: simsd_verify_attn (K1 RoPE-copy
 + paged append, K2 split-KV masked attention, K3 split merge) and
 simsd_accept (K4: one thread-block cluster per sequence computes the
 vocabulary normalisers, walks the steps along tau and draws the residual
-token at a rejection).  Default workload: the
-SDAR-8B-shaped verify step (16 sequences, prompt KV 1024, B = 4, 32/8 heads,
-head dim 128, vocabulary 151,936, bf16), seeded synthetic data.
+token at a rejection).  Default workload: the ragged serving mix (256
+sequences, prompt KV lengths uniform in [256, 8192], B in {4, 8}, 32/8
+heads, head dim 128, vocabulary 151,936, bf16, shuffled 16-token pages),
+the largest of the SDAR-8B-shaped workloads; --workload 1 is the
+16 x 1024, B = 4 step.  Seeded synthetic data.
 
 Prints ONE JSON line.  `value`: verified candidate tokens/s (sum of B over
 the batch / step time) with inputs resident in HBM: the step's library calls
@@ -23,8 +25,9 @@ results inside the timed region; host launch cost included); `e2e_graph`
 captures those copies and calls in a graph as well.  `roofline`: the
 attention kernel K2 (the dominant one), algorithmic bytes per launch over
 its mean event-timed duration.
-`cpu_baseline`: the fp64 oracle on a bounded sample of the same workload,
-timed on this host's cores.
+`cpu_baseline`: the fp64 oracle on a bounded sample of the same workload
+(its first sequences, as many as take about a second per pass), timed on
+this host's cores.
 
 --accept greedy / match times the other acceptance rules (the greedy rule,
 sample matching), --temperature T sampling at temperature T; the default is
@@ -60,8 +63,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", type=int, default=1,
-                    help="synthetic configuration index (1 = SDAR-8B verify step)")
+    ap.add_argument("--workload", type=int, default=4,
+                    help="synthetic configuration index (4 = 256-sequence ragged mix, "
+                         "1 = 16 x 1024 SDAR-8B verify step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--accept", default="sample", choices=["sample", "greedy", "match"],
@@ -69,6 +73,9 @@ def parse():
                          "sample matching")
     ap.add_argument("--temperature", type=float, default=1.0,
                     help="sampling temperature (rejection sampling only)")
+    ap.add_argument("--accept-path", default="auto", choices=["auto", "single"],
+                    help="acceptance: the library's choice for a full workspace (auto), or a "
+                         "workspace of only the status word (the single-launch cluster kernel)")
     return ap.parse_args()
 
 
@@ -175,18 +182,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- ncu traffic record
-def recorded_traffic(workload):
-    """DRAM bytes per K2 launch from the committed ncu summary, valid only
-    for the workload it was captured on and while the kernel source is
-    unchanged (hash recorded with the counters)."""
+def traffic_record_path(spec):
+    return os.path.join(ROOT, "profiles", "k2_traffic_%s.json" % spec.slug)
+
+
+def recorded_traffic(spec):
+    """DRAM bytes per K2 launch from the committed ncu summary of this
+    workload, valid only while the kernel source is unchanged (hash recorded
+    with the counters)."""
     src = os.path.join(ROOT, "speculative_decoding_diffusion_gb300", "csrc", "attn_tc.cu")
-    rec = os.path.join(ROOT, "profiles", "k2_traffic.json")
+    rec = traffic_record_path(spec)
     if not os.path.exists(rec):
         return None
     try:
         d = json.load(open(rec))
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if d.get("source_sha256") == h and d.get("workload") == workload:
+        if d.get("source_sha256") == h and d.get("workload") == spec.name:
             return float(d["dram_bytes_per_launch"])
     except Exception:
         pass
@@ -194,9 +205,26 @@ def recorded_traffic(workload):
 
 
 # ---------------------------------------------------------------- CPU oracle
+# sequences of the bounded CPU sample: about a second of oracle work per pass
+CPU_SAMPLE_SEQS = {0: 1, 1: 16, 2: 16, 3: 2, 4: 32}
+
+
+def cpu_sample(w, index):
+    """The first sequences of the workload (all of the small ones)."""
+    import synth
+    n = CPU_SAMPLE_SEQS.get(index, 16)
+    return synth.head(w, n) if n < len(w.lens) else w
+
+
+def sample_text(sub, w, reps, el):
+    return ("the first %d of %d sequences of %s (%d candidate tokens, prompt KV %d), "
+            "%d pass(es) in %.1f s" % (len(sub.lens), len(w.lens), w.spec.name,
+                                       int(sub.cu_B[-1]), int(sub.lens.sum()), reps, el))
+
+
 def oracle_step_sample(w, seconds, threads, rule="sample", temperature=1.0):
     """Time the oracle (attention + acceptance) over whole batches of the
-    workload until `seconds` have passed; returns (tokens/s, sample text)."""
+    workload w until `seconds` have passed; returns (tokens/s, seconds, passes)."""
     import oracle
     import synth
     q = synth.to_f64(w.q)
@@ -239,16 +267,18 @@ def run_reference(args):
     from oracle import build as obuild
     obuild.build()
     w = synth.config(args.workload)
+    sub = cpu_sample(w, args.workload)
     threads = cpu_threads()
     per_step = []
     per = max(1.0, min(8.0, 60.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup + args.steps):
-        v, el, reps = oracle_step_sample(w, per, threads, args.accept, args.temperature)
+        v, el, reps = oracle_step_sample(sub, per, threads, args.accept, args.temperature)
         if i >= args.warmup:
             per_step.append(el / reps)
     ms = float(np.mean(per_step)) * 1e3
-    value = int(w.cu_B[-1]) / (ms / 1e3)
-    sample = ("whole batches of %s, repeated for >= %.1f s per step" % (w.spec.name, per))
+    value = int(sub.cu_B[-1]) / (ms / 1e3)
+    sample = ("the first %d of %d sequences of %s per pass, passes repeated for >= %.1f s "
+              "per step" % (len(sub.lens), len(w.lens), w.spec.name, per))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -269,7 +299,8 @@ def config_of(w, args):
             "parallelism": "replicas x%d" % max(1, args.gpus),
             "l2": "flushed (512 MB write) before every timed step",
             "accept": args.accept + ("" if args.accept == "greedy" or args.temperature == 1.0
-                                     else " at temperature %g" % args.temperature)}
+                                     else " at temperature %g" % args.temperature)
+                      + ("" if args.accept_path == "auto" else " (single-launch path)")}
 
 
 # ---------------------------------------------------------------- multi-rank helpers
@@ -312,6 +343,8 @@ def main():
     libbuild.build()
     w = synth.config(args.workload)
     dw = DeviceWorkload(w, device="cuda:%d" % local)
+    if args.accept_path == "single":
+        dw.accept_ws = torch.zeros(256, dtype=torch.uint8, device="cuda:%d" % local)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -349,7 +382,7 @@ def main():
     clocks.start()
     torch.cuda.synchronize()
     t_start, t_end = ev(), ev()
-    step_ms, k_ms = [], {n: [] for n in ("K1", "K2", "K3", "K4")}
+    step_ms, k_ms = [], {n: [] for n in ("K1", "K2", "K3", "K4", "K4a", "K4b")}
     for _ in range(args.steps):
         flush.zero_()
         t_start.record()
@@ -364,7 +397,9 @@ def main():
         v = [vev[i].elapsed_time(vev[i + 1]) for i in range(3)]
         for n, t in zip(("K1", "K2", "K3"), v):
             k_ms[n].append(t)
-        k_ms["K4"].append(aev[0].elapsed_time(aev[1]))
+        k_ms["K4"].append(aev[0].elapsed_time(aev[2]))
+        k_ms["K4a"].append(aev[0].elapsed_time(aev[1]))
+        k_ms["K4b"].append(aev[1].elapsed_time(aev[2]))
     torch.cuda.synchronize()
     dev_total_ms = max_over_ranks(dist, float(np.sum(step_ms)), "cuda")
 
@@ -452,8 +487,11 @@ def main():
     peak, peak_kind = hbm_peak()
     k2_mean = float(np.mean(k_ms["K2"]))
     achieved = k2_bytes(w) / (k2_mean / 1e3) / 1e9
-    traffic = recorded_traffic(w.spec.name)
-    n_launch = 4 if any(t > 0.0005 for t in k_ms["K3"]) else 3
+    traffic = recorded_traffic(w.spec)
+    # K1, K2, K3 (only where a sequence's keys are split), and K4a (the chunk
+    # pass, sampling rule) + K4b or the single acceptance kernel
+    n_launch = (3 if any(t > 0.0005 for t in k_ms["K3"]) else 2) + \
+        (2 if any(t > 0.0005 for t in k_ms["K4a"]) else 1)
     kernels = {n: {"ms": float(np.mean(t))} for n, t in k_ms.items()}
     attn_ms = sum(kernels[n]["ms"] for n in ("K1", "K2", "K3"))
     acc_ms = kernels["K4"]["ms"]
@@ -474,17 +512,19 @@ def main():
                          "algorithmic_bytes_per_launch": k2_bytes(w)},
             "verify_attn_GBps": attn_bytes(w) / (attn_ms / 1e3) / 1e9,
             "accept_GBps": accept_bytes(w, args.accept != "sample") / (acc_ms / 1e3) / 1e9,
+            "accept_frac": accept_bytes(w, args.accept != "sample") / (acc_ms / 1e3) / 1e9 / peak,
             "kernels_ms": {n: round(k["ms"], 5) for n, k in kernels.items()},
             "clocks": clk, "status_word": status}
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import build as obuild
         obuild.build()
         threads = cpu_threads()
-        v, el, reps = oracle_step_sample(w, args.cpu_seconds, threads, args.accept,
+        sub = cpu_sample(w, args.workload)
+        v, el, reps = oracle_step_sample(sub, args.cpu_seconds, threads, args.accept,
                                          args.temperature)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                "sample": "%d whole batch(es) of %s (attention + acceptance), %.1f s"
-                                          % (reps, w.spec.name, el)}
+                                "sample": sample_text(sub, w, reps, el)
+                                          + " (attention + acceptance)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
