@@ -83,20 +83,6 @@ constexpr int kAConsumers = kAConsumerWarps * 32;
 constexpr int kAThreads = kAConsumers + 32;
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
 constexpr int kMaxVocab = 1 << 21;                 // 8 slices of kMaxPieces pieces of 8192 fp32 entries
-// The residual in target-mass units: with e_t = 2^(x ls - Mt) (so p =
-// e_t / St) and e_d = 2^(y ls - Md) (q = e_d / Sd), S_t max(0, p - q) =
-// max(0, e_t - rho e_d), rho = St / Sd (a pair).  The draw is the same in
-// any common unit, so no normaliser is rounded into the entries.  rho e_d
-// takes a product and one fused multiply-add, the difference its own
-// rounding (no contraction), so identical target and draft rows (rho
-// exactly 1) give an exactly empty residual, and the residual pass and the
-// draw compute the same values.
-__device__ __forceinline__ float draft_mass(float y, float Md, Ff rho, Scale ls) {
-  const float e = rel_exp(y, Md, ls);
-  return __fmaf_rn(e, rho.lo, __fmul_rn(e, rho.hi));
-}
-__device__ __forceinline__ float residual(float et, float ed) { return fmaxf(__fsub_rn(et, ed), 0.f); }
-
 __device__ __forceinline__ void consumers_sync() { named_sync(1, kConsumers); }
 
 // ---------------------------------------------------------------- state
@@ -152,48 +138,6 @@ struct AcceptParams {
   const float *xlogit;
   int nchunks, cpc;
 };
-
-// Producer warp: one piece of a row slice into a ring stage, completion on
-// `full` (bulk copy with a byte count, or element copies by the whole warp
-// and a plain arrival; those fill the rest of the last 16-byte vector with
-// -inf, since consumers read whole vectors).
-template <typename T>
-__device__ __noinline__ void copy_piece(uint8_t *dst, uint32_t dst_s, const T *src, int n,
-                                           uint32_t full, bool bulk, int lane) {
-  if (bulk) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(full, (uint32_t)(n * sizeof(T)));
-      bulk_load(dst_s, src, (uint32_t)(n * sizeof(T)), full);
-    }
-  } else {
-    constexpr int N = 16 / (int)sizeof(T);
-    T *d = reinterpret_cast<T *>(dst);
-    for (int e = lane; e < n; e += 32) d[e] = src[e];
-    for (int e = n + lane; e < (n + N - 1) / N * N; e += 32) d[e] = Ld<T>::neg_inf_elem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(full);
-  }
-}
-
-// Warp-wide choice among up to 32 consecutive ranges: lane i holds the
-// mass m of range i (0 for lanes without one), the ranges start at `base`.
-// Returns the first range whose running total exceeds U (else the last one
-// with mass, else 0), and in *start the running total before it.
-__device__ __noinline__ int warp_pick(Ff m, Ff base, Ff U, Ff *start) {
-  const int lane = threadIdx.x & 31;
-  Ff inc = m;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const Ff y = ff_shfl_up(inc, d);
-    if (lane >= d) inc = ff_add(y, inc);
-  }
-  const Ff run = ff_add(base, inc);
-  const unsigned cross = __ballot_sync(0xffffffffu, m.hi > 0.f && ff_gt(run, U));
-  const unsigned nz = __ballot_sync(0xffffffffu, m.hi > 0.f);
-  const int ch = cross ? __ffs(cross) - 1 : (nz ? 31 - __clz(nz) : 0);
-  *start = ff_shfl(ff_add(base, ff_add(inc, ff_neg(m))), ch);
-  return ch;
-}
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -183,7 +183,7 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
   p->off_qrot = off;    // rotated queries: the fp32 path only (the bf16 kernel rotates its own)
   if (d->dtype == SIMSD_F32)
     off = align_up(off + (size_t)p->T * d->num_q_heads * d->head_dim * p->esize, kAlign);
-  p->off_tokseq = off;  off = align_up(off + (size_t)p->T * sizeof(int32_t), kAlign);
+  p->off_tokns = off;  off = align_up(off + (size_t)p->T * sizeof(int32_t), kAlign);
   p->off_opart = off;
   if (p->n_splits > 1) {
     off = align_up(off + (size_t)p->n_splits * p->T * d->num_q_heads * d->head_dim * sizeof(float), kAlign);
@@ -287,9 +287,9 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   char *ws = (char *)d->workspace;
   uint32_t *status = (uint32_t *)(ws + p.off_status);
   void *q_rot = ws + p.off_qrot;
-  int32_t *tok_seq = (int32_t *)(ws + p.off_tokseq);
+  int32_t *tok_ns = (int32_t *)(ws + p.off_tokns);
   if (!mark(events, 0, stream) ||
-      launch_rope_verify(d, p, q_rot, tok_seq, status, stream) != cudaSuccess ||
+      launch_rope_verify(d, p, q_rot, tok_ns, status, stream) != cudaSuccess ||
       !mark(events, 1, stream))
     return SIMSD_ERR_CUDA;
   AttnParams a;
@@ -324,7 +324,7 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   cudaError_t e = d->dtype == SIMSD_BF16 ? launch_attn_tc(d, p, a, stream)
                                          : launch_attn_f32(d, p, a, stream);
   if (e != cudaSuccess || !mark(events, 2, stream)) return SIMSD_ERR_CUDA;
-  if (p.n_splits > 1 && launch_combine(d, p, a, tok_seq, stream) != cudaSuccess)
+  if (p.n_splits > 1 && launch_combine(d, p, a, tok_ns, stream) != cudaSuccess)
     return SIMSD_ERR_CUDA;
   return mark(events, 3, stream) ? SIMSD_OK : SIMSD_ERR_CUDA;
 }

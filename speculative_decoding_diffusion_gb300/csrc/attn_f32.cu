@@ -128,41 +128,59 @@ attn_f32_kernel(const __grid_constant__ AttnParams a) {
 }
 
 // K3: O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s, one warp per
-// (token, query head) row; rows of single-split sequences were finished by K2.
+// (token, query head) row; rows of single-split sequences were finished by
+// the attention kernel.  The split count comes from the append kernel (one
+// load), and up to kMergeBatch splits' partials are requested at once.
+constexpr int kMergeBatch = 8;
+
 template <typename T, int HD>
 __global__ void __launch_bounds__(256)
-combine_kernel(const __grid_constant__ AttnParams a, const int32_t *tok_seq) {
+combine_kernel(const __grid_constant__ AttnParams a, const int32_t *tok_ns) {
   constexpr int PER = HD / 32;
   grid_dep_wait();                           // partials come from the attention kernel
   const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= (long)a.T * a.Hq) return;
-  const int tok = (int)(row / a.Hq);
-  const int b = __ldg(tok_seq + tok);
-  const int c0 = __ldg(a.cu_B + b);
-  const int B = __ldg(a.cu_B + b + 1) - c0;
-  const int P = __ldg(a.lens + b);
-  const int Lk = P + 2 * B;
-  const int ns = (Lk + a.chunk - 1) / a.chunk;
-  // malformed sequences (the attention kernel flagged and skipped them)
-  if (B < 1 || B > kMaxSection || B > a.B_max || c0 < 0 || c0 + B > a.total_B || P < 0 ||
-      (long)Lk > (long)a.max_pages_per_seq * kPage)
-    return;
+  const int ns = __ldg(tok_ns + row / a.Hq);   // 0 for a malformed sequence (skipped)
   if (ns <= 1) return;
   const long stride = (long)a.T * a.Hq;
-  float mstar = -INFINITY;
-  for (int s = 0; s < ns; ++s) mstar = fmaxf(mstar, a.ml_part[s * stride + row].x);
-  const float mu = mstar == -INFINITY ? 0.f : mstar;
-  float den = 0.f, o[PER];
+  float mstar = -INFINITY, den = 0.f, o[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) o[i] = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float2 ml = a.ml_part[s * stride + row];
-    const float w = exp2f(ml.x - mu);
-    den += w * ml.y;
-    const float *op = a.o_part + (s * stride + row) * HD;
+  for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
+    const int n = min(kMergeBatch, ns - s0);
+    float2 ml[kMergeBatch];
+    float v[kMergeBatch][PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) o[i] = fmaf(w, op[lane + 32 * i], o[i]);
+    for (int s = 0; s < kMergeBatch; ++s) {
+      if (s < n) {
+        const long pr = (s0 + s) * stride + row;
+        ml[s] = __ldcg(a.ml_part + pr);
+#pragma unroll
+        for (int i = 0; i < PER; ++i) v[s][i] = __ldcg(a.o_part + pr * HD + lane + 32 * i);
+      }
+    }
+    float mb = mstar;
+#pragma unroll
+    for (int s = 0; s < kMergeBatch; ++s)
+      if (s < n) mb = fmaxf(mb, ml[s].x);
+    if (mb > mstar && mstar != -INFINITY) {  // a later batch raised the reference
+      const float r = exp2f(mstar - mb);
+      den *= r;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) o[i] *= r;
+    }
+    mstar = mb;
+    const float mu = mstar == -INFINITY ? 0.f : mstar;
+#pragma unroll
+    for (int s = 0; s < kMergeBatch; ++s) {
+      if (s < n) {
+        const float w = exp2f(ml[s].x - mu);
+        den += w * ml[s].y;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) o[i] = fmaf(w, v[s][i], o[i]);
+      }
+    }
   }
   const float inv = 1.f / den;
   T *out = (T *)a.out + row * HD;
@@ -183,11 +201,11 @@ cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
 }
 
 cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
-                           const AttnParams &a, const int32_t *tok_seq,
+                           const AttnParams &a, const int32_t *tok_ns,
                            cudaStream_t stream) {
   const long rows = (long)p.T * d->num_q_heads;
   const unsigned blocks = (unsigned)((rows + 7) / 8);
-  const int32_t *ts = tok_seq;
+  const int32_t *ts = tok_ns;
   if (d->dtype == SIMSD_BF16)
     return d->head_dim == 128
                ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(256), 0, stream, a, ts)

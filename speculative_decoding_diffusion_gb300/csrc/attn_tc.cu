@@ -211,6 +211,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     // ---------------------------------------------------------- producer
     if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
     const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
+    // lane i: page i of a block; the pages of the next kStages blocks are
+    // requested ahead (the first kStages at once), so no block's copies
+    // wait for a block-table round trip
+    auto block_page = [&](int jj) {
+      if (jj >= n_blocks) return 0;
+      const int kb = k_begin + jj * kKeys;
+      return lane < (min(kKeys, k_end - kb) + kPage - 1) / kPage ? __ldg(bt + kb / kPage + lane) : 0;
+    };
+    int pages[kStages];
+#pragma unroll
+    for (int d = 0; d < kStages; ++d) pages[d] = block_page(d);
     bool dep_done = false;
     for (int j = 0; j < n_blocks; ++j) {
       const int s = j % kStages;
@@ -220,7 +231,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         dep_done = true;
       }
       const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
-      const int page = lane < n_pages ? __ldg(bt + kb / kPage + lane) : 0;   // before the wait
+      const int page = pages[0];
+#pragma unroll
+      for (int d = 0; d + 1 < kStages; ++d) pages[d] = pages[d + 1];
+      pages[kStages - 1] = block_page(j + kStages);
       if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1, a.polls)) {
         if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
         break;
@@ -290,6 +304,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           idle = 0;
         } else if (++idle > ((uint64_t)a.polls << 4)) {  // bounded: give up, flag, drain
           ok = false;
+        } else if (idle > 8) {
+          // nothing ready for a while (usually: the softmax is on a block):
+          // leave the issue slots to the softmax warp sharing this scheduler
+          __nanosleep(32);
         }
       }
       if (!ok) {

@@ -34,7 +34,7 @@ struct VerifyPlan {
   int n_splits;      // splits of the longest possible sequence
   size_t esize;      // bytes per q/k/v/out element
   // workspace carve-up (byte offsets)
-  size_t off_status, off_qrot, off_tokseq, off_opart, off_ml, total;
+  size_t off_status, off_qrot, off_tokns, off_opart, off_ml, total;
 };
 
 // Fills *plan; returns SIMSD_OK or the first argument error.
@@ -76,7 +76,7 @@ struct AttnParams {
 
 // K1: rotate q and k_new at the layout positions, append k/v to the cache.
 cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
-                               void *q_rot, int32_t *tok_seq, uint32_t *status,
+                               void *q_rot, int32_t *tok_ns, uint32_t *status,
                                cudaStream_t stream);
 cudaError_t launch_rope_append(const simsd_append_desc *d, cudaStream_t stream);
 
@@ -88,7 +88,7 @@ cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
 
 // K3: merge split partials.
 cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
-                           const AttnParams &a, const int32_t *tok_seq,
+                           const AttnParams &a, const int32_t *tok_ns,
                            cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).

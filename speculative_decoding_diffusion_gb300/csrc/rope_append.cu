@@ -137,9 +137,10 @@ struct RopeVerifyArgs {
   const int32_t *block_table;
   const int32_t *lens;
   const int32_t *cu_B;
-  int32_t *tok_seq;
+  int32_t *tok_ns;      // [T]: key splits of the token's sequence (0: malformed)
   uint32_t *status;
   int batch, Hq, Hkv, hd, max_pages, num_pages;
+  int chunk;            // keys per split of the attention kernels
   int total_B, B_max;   // host copies: a sequence's cu_B and B must fit them
   uint32_t polls;       // bounded-wait polls
   int node_size;        // 0: SimSD's paired layout; > 0: draft-graph nodes
@@ -190,7 +191,6 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
     B = __ldg(a.cu_B + b + 1) - c0;
     P = __ldg(a.lens + b);
   }
-  if (threadIdx.x == 0) a.tok_seq[r] = b;    // the merge kernel reads it
   const int j = r - 2 * c0;                  // 0..2B-1 within the sequence
   // response index (0-based): D~_k copies D_k's position; in the
   // draft-graph layout every node's token k sits at the same position
@@ -202,6 +202,8 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
               (a.node_size > 0 && (2 * B) % a.node_size != 0));
   const int page = ok ? __ldg(a.block_table + (long)b * a.max_pages + slot / kPage) : -1;
   ok = ok && page >= 0 && page < a.num_pages;   // cu_B or block table out of range
+  // the split merge reads it: the rows it merges, without a search
+  if (threadIdx.x == 0) a.tok_ns[r] = ok ? (P + 2 * B + a.chunk - 1) / a.chunk : 0;
   if (!ok && threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
   if (ok) angles(a.tab, a.hd, pos, cs);
   __syncthreads();
@@ -258,7 +260,7 @@ rope_append_kernel(const __grid_constant__ RopeAppendArgs a) {
 }  // namespace
 
 cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
-                               void *q_rot, int32_t *tok_seq, uint32_t *status,
+                               void *q_rot, int32_t *tok_ns, uint32_t *status,
                                cudaStream_t stream) {
   RopeVerifyArgs a;
   make_rope_table(d->rope_base, d->head_dim, &a.tab);
@@ -271,7 +273,8 @@ cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
   a.block_table = d->block_table;
   a.lens = d->lens;
   a.cu_B = d->cu_B;
-  a.tok_seq = tok_seq;
+  a.tok_ns = tok_ns;
+  a.chunk = p.chunk;
   a.status = status;
   a.num_pages = d->num_pages;
   a.batch = d->batch;

@@ -21,13 +21,16 @@ from speculative_decoding_diffusion_gb300.staging import DeviceWorkload
 pytestmark = pytest.mark.gpu
 
 
-def run_accept(w, status_only=False):
+PATHS = ["two-kernel", "single-launch"]
+
+
+def run_accept(w, path="two-kernel"):
     """simsd_accept with the workspace size the library asks for (the
-    two-kernel path: chunk pass, then the per-sequence cluster kernel) or,
-    with status_only, a workspace of just the status word (the single
-    cluster kernel streaming the rows itself)."""
+    two-kernel path: chunk pass, then the per-sequence cluster kernel) or
+    one of just the status word (the single cluster kernel streaming the
+    rows itself)."""
     dw = DeviceWorkload(w, with_verify=False)
-    if status_only:
+    if path == "single-launch":
         ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
         binding.accept(dw.target, dw.draft, dw.draft_tokens, dw.tau, dw.cu_B, dw.uniforms,
                        dw.n_accept, dw.token, dw.pos, ws, dw.total_B, dw.B_max)
@@ -39,11 +42,11 @@ def run_accept(w, status_only=False):
     return (dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy())
 
 
-@pytest.mark.parametrize("path", ["two-kernel", "single-launch"])
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
 def test_configs_match_oracle(cfg, path):
     w = synth.config(cfg)
-    n, tok, pos = run_accept(w, status_only=path == "single-launch")
+    n, tok, pos = run_accept(w, path)
     ref = parity.oracle_accept(w)
     stats = []
     step_ties, draw_ties, draws = parity.check_accept(w, ref, n, tok, pos, stats=stats)
@@ -63,23 +66,23 @@ def tiny_accept_spec(**kw):
 
 @pytest.mark.parametrize("dtype,vocab", [("bf16", 1003), ("bf16", 4096 + 8), ("f32", 777),
                                          ("f32", 2048), ("bf16", 9)])
-@pytest.mark.parametrize("status_only", [False, True])
-def test_odd_vocab_and_mixed_B(dtype, vocab, status_only):
+@pytest.mark.parametrize("path", PATHS)
+def test_odd_vocab_and_mixed_B(dtype, vocab, path):
     w = synth.make(tiny_accept_spec(dtype=dtype, vocab=vocab), seed=vocab)
-    n, tok, pos = run_accept(w, status_only)
+    n, tok, pos = run_accept(w, path)
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
 
 
 @pytest.mark.parametrize("dtype,vocab,batch,B", [("bf16", 151936, 2, 32), ("bf16", 65539, 3, 32),
                                                  ("f32", 100003, 4, 17), ("bf16", 151936, 5, 1)])
-@pytest.mark.parametrize("status_only", [False, True])
-def test_few_sequences_large_clusters(dtype, vocab, batch, B, status_only):
+@pytest.mark.parametrize("path", PATHS)
+def test_few_sequences_large_clusters(dtype, vocab, batch, B, path):
     """Few sequences get the largest clusters (up to 16 CTAs each): slices
     of 1/16 of the vocabulary, the slice merge in 16-lane groups and, at
     B = 32, in two rounds of pairs; element copies where rows are not
     16-byte multiples."""
     w = synth.make(tiny_accept_spec(batch=batch, B=B, dtype=dtype, vocab=vocab), seed=vocab + B)
-    n, tok, pos = run_accept(w, status_only)
+    n, tok, pos = run_accept(w, path)
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
 
 
