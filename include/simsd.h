@@ -97,9 +97,14 @@ simsd_status simsd_layout(int32_t prompt_len, int32_t B, const int32_t *tau,
  *   K1  rotate q (all query heads) and k_new at the layout positions (D~_k
  *       uses D_k's), write rotated k and raw v of the 2B new tokens into
  *       cache slots [lens[b], lens[b]+2B_b) of sequence b;
- *   K2  split-KV attention of all 2B_b x Hq query rows of a sequence and KV
- *       head against the cache, the temporal mask evaluated on the fly;
- *   K3  merge of the per-split partial softmax states.
+ *   K2  attention of all 2B_b x Hq query rows of a sequence and KV head
+ *       against the cache, the temporal mask evaluated on the fly; a
+ *       (sequence, KV head) unit runs whole or in key splits (every unit
+ *       when the block-table width makes one unit long, or only the units
+ *       of the last partial wave of CTAs, so that wave takes a split's
+ *       time instead of a unit's);
+ *   K3  merge of the split units' partial softmax states (launched only
+ *       when some unit is split).
  * lens[] is NOT advanced: rolling back a rejected draft costs nothing, and
  * committing accepted tokens is the caller's business.
  *

@@ -346,16 +346,30 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
       for (int q = warp; q < 2 * n_open; q += kConsumerWarps) {
         const int k = slot_of(q >> 1), row = q & 1, x = S.x[k];
         const float2 *pr_ = a.part + (long)(2 * (c0 + k) + row) * per_row;
+        // the first 4 partials of each lane stay in registers: one round
+        // trip for both the maximum and the sum (vocabularies up to 16
+        // chunks); the rest are read twice
+        constexpr int kHeld = 4;
+        float2 held[kHeld];
+#pragma unroll
+        for (int i = 0; i < kHeld; ++i)
+          held[i] = lane + 32 * i < per_row ? __ldg(pr_ + lane + 32 * i) : make_float2(-INFINITY, 0.f);
         float M = -INFINITY;
-        for (int i = lane; i < per_row; i += 32) M = fmaxf(M, __ldg(&pr_[i].x));
+#pragma unroll
+        for (int i = 0; i < kHeld; ++i) M = fmaxf(M, held[i].x);
+        for (int i = lane + 32 * kHeld; i < per_row; i += 32) M = fmaxf(M, __ldg(&pr_[i].x));
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
         Ff sm = ff_of(0.f);
-        if (M != -INFINITY)
-          for (int i = lane; i < per_row; i += 32) {
+        if (M != -INFINITY) {
+#pragma unroll
+          for (int i = 0; i < kHeld; ++i)
+            if (held[i].y > 0.f) sm = ff_add(sm, ff_of(held[i].y * exp2_int(held[i].x - M)));
+          for (int i = lane + 32 * kHeld; i < per_row; i += 32) {
             const float2 v = __ldg(pr_ + i);
             if (v.y > 0.f) sm = ff_add(sm, ff_of(v.y * exp2_int(v.x - M)));
           }
+        }
 #pragma unroll
         for (int m = 16; m > 0; m >>= 1) sm = ff_add(sm, ff_shfl_xor(sm, m));
         if (lane == 0) {
@@ -711,23 +725,40 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   __syncthreads();
   long issued = 0;
   if (producer) {
-    for (long j = 0; j < mine; ++j) {
-      const int s = (int)(j % kAStages);
-      if (j >= kAStages && !mbar_wait_warp(smem_u32(&empty[s]), ((j / kAStages) - 1) & 1, a.polls)) {
-        if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); }
-        break;
+    // the items' draft tokens are requested kAStages items ahead into the
+    // same register slot (the loop is unrolled by kAStages, so no register
+    // moves while its load is in flight): no copy waits for that load
+    auto token_of = [&](long j) {
+      return j < mine ? __ldg(a.draft_tokens + (item_of(j) / a.nchunks >> 1)) : 0;
+    };
+    int xs[kAStages];
+#pragma unroll
+    for (int u = 0; u < kAStages; ++u) xs[u] = token_of(u);
+    bool ok = true;
+    for (long j0 = 0; ok && j0 < mine; j0 += kAStages) {
+#pragma unroll
+      for (int u = 0; u < kAStages; ++u) {
+        const long j = j0 + u;
+        if (j >= mine) break;
+        const int s = u;                            // j % kAStages (j0 is a multiple)
+        if (j >= kAStages && !mbar_wait_warp(smem_u32(&empty[s]), ((j / kAStages) - 1) & 1, a.polls)) {
+          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); }
+          ok = false;
+          break;
+        }
+        const long i = item_of(j);
+        const long p = i / a.nchunks;               // row pair index: slot p/2, target or draft
+        const int c = (int)(i % a.nchunks);
+        const int n = min(kChunk, a.vocab - c * kChunk);
+        // the draft token goes beside the stage before the copy's arrival
+        // (release) makes the stage visible to the consumers
+        if (lane == 0) stage_x[s] = xs[u];
+        __syncwarp();
+        const T *src = (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab + (long)c * kChunk;
+        copy_piece<T>(smem + s * kStage, ring + s * kStage, src, n, smem_u32(&full[s]), a.bulk, lane);
+        issued = j + 1;
+        xs[u] = token_of(j + kAStages);
       }
-      const long i = item_of(j);
-      const long p = i / a.nchunks;                 // row pair index: slot p/2, target or draft
-      const int c = (int)(i % a.nchunks);
-      const int n = min(kChunk, a.vocab - c * kChunk);
-      // the draft token goes beside the stage before the copy's arrival
-      // (release) makes the stage visible to the consumers
-      if (lane == 0) stage_x[s] = __ldg(a.draft_tokens + (p >> 1));
-      __syncwarp();
-      const T *src = (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab + (long)c * kChunk;
-      copy_piece<T>(smem + s * kStage, ring + s * kStage, src, n, smem_u32(&full[s]), a.bulk, lane);
-      issued = j + 1;
     }
   } else {
     for (long j = 0; j < mine; ++j) {

@@ -6,6 +6,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -177,13 +178,45 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
   int64_t blocks_per_split = (max_blocks + splits - 1) / splits;
   p->chunk = (int)(blocks_per_split * kBlockKeys);
   p->n_splits = (int)((max_keys + p->chunk - 1) / p->chunk);
+  // every unit split alike, or none
+  p->tail_from = p->n_splits > 1 ? 0 : (int)pairs;
+  p->s_tail = p->n_splits;
+  p->chunk_tail = p->chunk;
+  p->grid = (int)(pairs * p->n_splits);
+  p->merge_rows = (int64_t)p->T * d->num_q_heads;
+  if (d->dtype == SIMSD_BF16 && p->n_splits == 1 && pairs > sms && pairs % sms != 0) {
+    // Whole units in full waves, then the last partial wave's r units in
+    // s = sms / r splits each: that wave takes a split's time instead of a
+    // unit's (same block-time model, plus the split merge's read).
+    const int64_t W = pairs / sms, r = pairs - W * sms;
+    const int64_t s = std::min<int64_t>(sms / r, max_blocks);
+    if (s >= 2) {
+      const int64_t per = (max_blocks + s - 1) / s;
+      const double whole = (double)(W + 1) * ((double)max_blocks + 1.5);
+      const double tail = (double)W * ((double)max_blocks + 1.5) + ((double)per + 2.5) +
+                          (double)(r * s) / (double)sms;
+      if (tail < whole - 1e-9) {
+        p->tail_from = (int)(W * sms);
+        p->s_tail = (int)s;
+        p->chunk_tail = (int)(per * kBlockKeys);
+        p->n_splits = (int)((max_keys + p->chunk_tail - 1) / p->chunk_tail);
+        p->grid = (int)(W * sms + r * s);
+        // the split units belong to the last ceil(r / units per sequence)
+        // (+1 for a sequence cut by the boundary) sequences, whose tokens
+        // are the last ones
+        const int64_t per_seq = (int64_t)d->num_kv_heads * p->row_tiles;
+        const int64_t seqs = std::min<int64_t>(d->batch, (r + per_seq - 1) / per_seq + 1);
+        p->merge_rows = std::min<int64_t>(p->merge_rows, seqs * 2 * d->B_max * d->num_q_heads);
+      }
+    }
+  }
   // workspace
   size_t off = 0;
   p->off_status = off;  off = align_up(off + sizeof(uint32_t), kAlign);
   p->off_qrot = off;    // rotated queries: the fp32 path only (the bf16 kernel rotates its own)
   if (d->dtype == SIMSD_F32)
     off = align_up(off + (size_t)p->T * d->num_q_heads * d->head_dim * p->esize, kAlign);
-  p->off_tokns = off;  off = align_up(off + (size_t)p->T * sizeof(int32_t), kAlign);
+  p->off_tokinfo = off;  off = align_up(off + (size_t)p->T * sizeof(int4), kAlign);
   p->off_opart = off;
   if (p->n_splits > 1) {
     off = align_up(off + (size_t)p->n_splits * p->T * d->num_q_heads * d->head_dim * sizeof(float), kAlign);
@@ -287,9 +320,9 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   char *ws = (char *)d->workspace;
   uint32_t *status = (uint32_t *)(ws + p.off_status);
   void *q_rot = ws + p.off_qrot;
-  int32_t *tok_ns = (int32_t *)(ws + p.off_tokns);
+  int4 *tok_info = (int4 *)(ws + p.off_tokinfo);
   if (!mark(events, 0, stream) ||
-      launch_rope_verify(d, p, q_rot, tok_ns, status, stream) != cudaSuccess ||
+      launch_rope_verify(d, p, q_rot, tok_info, status, stream) != cudaSuccess ||
       !mark(events, 1, stream))
     return SIMSD_ERR_CUDA;
   AttnParams a;
@@ -319,12 +352,16 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   a.polls = wait_polls_of(d->wait_polls);
   a.node_size = d->node_size;
   a.chunk = p.chunk;
+  a.tail_from = p.tail_from;
+  a.s_tail = p.s_tail;
+  a.chunk_tail = p.chunk_tail;
+  a.row_tiles = p.row_tiles;
   a.rows_per_tile = p.rows_per_tile;
   a.sm_scale = d->sm_scale;
   cudaError_t e = d->dtype == SIMSD_BF16 ? launch_attn_tc(d, p, a, stream)
                                          : launch_attn_f32(d, p, a, stream);
   if (e != cudaSuccess || !mark(events, 2, stream)) return SIMSD_ERR_CUDA;
-  if (p.n_splits > 1 && launch_combine(d, p, a, tok_ns, stream) != cudaSuccess)
+  if (p.n_splits > 1 && launch_combine(d, p, a, tok_info, stream) != cudaSuccess)
     return SIMSD_ERR_CUDA;
   return mark(events, 3, stream) ? SIMSD_OK : SIMSD_ERR_CUDA;
 }

@@ -130,18 +130,24 @@ attn_f32_kernel(const __grid_constant__ AttnParams a) {
 // K3: O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s, one warp per
 // (token, query head) row; rows of single-split sequences were finished by
 // the attention kernel.  The split count comes from the append kernel (one
-// load), and up to kMergeBatch splits' partials are requested at once.
-constexpr int kMergeBatch = 8;
+// load), and kMergeBatch splits' partials are requested at a time.
+constexpr int kMergeBatch = 4;
 
+// four CTAs (32 warps) per SM without spills: enough loads in flight
 template <typename T, int HD>
-__global__ void __launch_bounds__(256)
-combine_kernel(const __grid_constant__ AttnParams a, const int32_t *tok_ns) {
+__global__ void __launch_bounds__(256, 4)
+combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long row0) {
   constexpr int PER = HD / 32;
   grid_dep_wait();                           // partials come from the attention kernel
-  const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const long row = row0 + (long)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= (long)a.T * a.Hq) return;
-  const int ns = __ldg(tok_ns + row / a.Hq);   // 0 for a malformed sequence (skipped)
+  // the row's unit (sequence, KV head, row tile) and whether it was split
+  const int4 ti = __ldg(tok_info + row / a.Hq);   // keys 0: a malformed sequence (skipped)
+  const int hq = (int)(row % a.Hq);
+  const int rtile = (ti.z * a.G + hq % a.G) / a.rows_per_tile;
+  const int unit = ti.y + rtile * a.Hkv + hq / a.G;
+  const int ns = unit >= a.tail_from ? (ti.x + a.chunk_tail - 1) / a.chunk_tail : 1;
   if (ns <= 1) return;
   const long stride = (long)a.T * a.Hq;
   float mstar = -INFINITY, den = 0.f, o[PER];
@@ -201,18 +207,19 @@ cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
 }
 
 cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
-                           const AttnParams &a, const int32_t *tok_ns,
+                           const AttnParams &a, const int4 *tok_info,
                            cudaStream_t stream) {
-  const long rows = (long)p.T * d->num_q_heads;
+  const long rows = (long)p.merge_rows;
+  const long row0 = (long)p.T * d->num_q_heads - rows;
   const unsigned blocks = (unsigned)((rows + 7) / 8);
-  const int32_t *ts = tok_ns;
+  const int4 *ts = tok_info;
   if (d->dtype == SIMSD_BF16)
     return d->head_dim == 128
-               ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(256), 0, stream, a, ts)
-               : launch_pdl(combine_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(256), 0, stream, a, ts);
+               ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(256), 0, stream, a, ts, row0)
+               : launch_pdl(combine_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(256), 0, stream, a, ts, row0);
   return d->head_dim == 128
-             ? launch_pdl(combine_kernel<float, 128>, dim3(blocks), dim3(256), 0, stream, a, ts)
-             : launch_pdl(combine_kernel<float, 64>, dim3(blocks), dim3(256), 0, stream, a, ts);
+             ? launch_pdl(combine_kernel<float, 128>, dim3(blocks), dim3(256), 0, stream, a, ts, row0)
+             : launch_pdl(combine_kernel<float, 64>, dim3(blocks), dim3(256), 0, stream, a, ts, row0);
 }
 
 }  // namespace simsd

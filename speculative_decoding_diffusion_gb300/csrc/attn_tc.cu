@@ -138,10 +138,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + L::kOffMisc);
   int *flag_s = reinterpret_cast<int *>(sb + L::kOffMisc + 4);
 
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y % a.Hkv;
-  const int rtile = blockIdx.y / a.Hkv;
-  const int b = blockIdx.z;
+  // unit (sequence, KV head, row tile) in launch order, and its split: the
+  // first tail_from units whole, later ones in s_tail splits of chunk_tail
+  // keys
+  const int ci = blockIdx.x;
+  const bool tail = ci >= a.tail_from;
+  const int unit = tail ? a.tail_from + (ci - a.tail_from) / a.s_tail : ci;
+  const int split = tail ? (ci - a.tail_from) % a.s_tail : 0;
+  const int chunk = tail ? a.chunk_tail : a.max_pages_per_seq * kPage;
+  const int per_seq = a.Hkv * a.row_tiles;
+  const int b = unit / per_seq;
+  const int kvh = unit % per_seq % a.Hkv;
+  const int rtile = unit % per_seq / a.Hkv;
   const int c0 = __ldg(a.cu_B + b);
   const int B = __ldg(a.cu_B + b + 1) - c0;
   const int P = __ldg(a.lens + b);
@@ -149,16 +157,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   if (B < 1 || B > kMaxSection || B > a.B_max || c0 < 0 || c0 + B > a.total_B || P < 0 ||
       (long)Lk > (long)a.max_pages_per_seq * kPage ||
       (a.node_size > 0 && (2 * B) % a.node_size != 0)) {
-    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) raise_status(a.status, kStatusBadInput);
+    if (threadIdx.x == 0 && split == 0 && unit % per_seq == 0) raise_status(a.status, kStatusBadInput);
     return;
   }
   const int M = 2 * B * a.G;
   const int row0 = rtile * kRows;
-  const int k_begin = split * a.chunk;
+  const int k_begin = split * chunk;
   if (row0 >= M || k_begin >= Lk) return;   // uniform: nothing to do here
-  const int k_end = min(Lk, k_begin + a.chunk);
+  const int k_end = min(Lk, k_begin + chunk);
   const int n_blocks = (k_end - k_begin + kKeys - 1) / kKeys;
-  const int n_splits_b = (Lk + a.chunk - 1) / a.chunk;
+  const int n_splits_b = (Lk + chunk - 1) / chunk;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // copies of the tile's rows across the four TMEM lane quadrants (4 when
   // one 32-row group holds every real row, 2 for two groups, else 1), and
@@ -167,6 +175,23 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   const int R = n_groups == 1 ? 4 : n_groups == 2 ? 2 : 1;
   const int n_valid = R > 1 ? 4 : n_groups;
   grid_dep_launch();                         // the split merge may be scheduled
+  // Producer lane i copies page i of a block (both halves of K and V).  The
+  // page ids of the first kStages blocks are requested before the setup
+  // below, later ones kStages blocks ahead into the same register slot
+  // (the loop is unrolled by kStages: no register is moved while its load
+  // is in flight), so no copy waits for a block-table round trip.
+  const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
+  auto block_page = [&](int jj) {
+    if (jj >= n_blocks) return 0;
+    const int kb = k_begin + jj * kKeys;
+    return lane < (min(kKeys, k_end - kb) + kPage - 1) / kPage ? __ldg(bt + kb / kPage + lane) : 0;
+  };
+  int pages[kStages];
+  if (warp == 0) {
+    if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
+#pragma unroll
+    for (int d = 0; d < kStages; ++d) pages[d] = block_page(d);
+  }
   // softmax threads request their raw query row first, ahead of the K/V
   // stream the producer starts below (each thread one row of the tile)
   uint4 qv[HD / 8];
@@ -182,6 +207,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
       for (int e = 0; e < HD / 8; ++e) qv[e] = make_uint4(0, 0, 0, 0);
     }
   }
+  // the section's step labels (softmax thread j < 2B: tau of new token j),
+  // requested with the query rows, before the producer's copies fill the
+  // memory system
+  const int tsm = threadIdx.x - 64;
+  const int tau_j = warp >= 2 && a.node_size == 0 && tsm < 2 * B
+                        ? __ldg(a.tau + c0 + (tsm < B ? tsm : tsm - B)) : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -209,48 +240,39 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
-    const int32_t *bt = a.block_table + (long)b * a.max_pages_per_seq;
-    // lane i: page i of a block; the pages of the next kStages blocks are
-    // requested ahead (the first kStages at once), so no block's copies
-    // wait for a block-table round trip
-    auto block_page = [&](int jj) {
-      if (jj >= n_blocks) return 0;
-      const int kb = k_begin + jj * kKeys;
-      return lane < (min(kKeys, k_end - kb) + kPage - 1) / kPage ? __ldg(bt + kb / kPage + lane) : 0;
-    };
-    int pages[kStages];
+    bool dep_done = false, ok = true;
+    for (int j0 = 0; ok && j0 < n_blocks; j0 += kStages) {
 #pragma unroll
-    for (int d = 0; d < kStages; ++d) pages[d] = block_page(d);
-    bool dep_done = false;
-    for (int j = 0; j < n_blocks; ++j) {
-      const int s = j % kStages;
-      const int kb = k_begin + j * kKeys;
-      if (!dep_done && kb + kKeys > P) {     // the block holds new keys K1 writes
-        grid_dep_wait();
-        dep_done = true;
-      }
-      const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
-      const int page = pages[0];
-#pragma unroll
-      for (int d = 0; d + 1 < kStages; ++d) pages[d] = pages[d + 1];
-      pages[kStages - 1] = block_page(j + kStages);
-      if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1, a.polls)) {
-        if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + s), n_pages * L::kHalves * 2 * kBoxBytes);
-      __syncwarp();
-      if (lane < n_pages) {
-        const uint32_t kt = sKv + s * L::kStage, vt = kt + L::kKv;
-#pragma unroll
-        for (int hh = 0; hh < L::kHalves; ++hh) {
-          const uint32_t off = hh * L::kKvHalf + lane * kBoxBytes;
-          tma_load_4d(kt + off, &tmK, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
-          tma_load_4d(vt + off, &tmV, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
+      for (int u = 0; u < kStages; ++u) {
+        const int j = j0 + u;
+        if (j >= n_blocks) break;
+        const int s = u;                       // j % kStages (j0 is a multiple)
+        const int kb = k_begin + j * kKeys;
+        if (!dep_done && kb + kKeys > P) {   // the block holds new keys K1 writes
+          grid_dep_wait();
+          dep_done = true;
         }
+        const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
+        const int page = pages[u];
+        if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1, a.polls)) {
+          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + s), n_pages * L::kHalves * 2 * kBoxBytes);
+        __syncwarp();
+        if (lane < n_pages) {
+          const uint32_t kt = sKv + s * L::kStage, vt = kt + L::kKv;
+#pragma unroll
+          for (int hh = 0; hh < L::kHalves; ++hh) {
+            const uint32_t off = hh * L::kKvHalf + lane * kBoxBytes;
+            tma_load_4d(kt + off, &tmK, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
+            tma_load_4d(vt + off, &tmV, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
+          }
+        }
+        issued = j + 1;
+        pages[u] = block_page(j + kStages);
       }
-      issued = j + 1;
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -341,7 +363,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const int npos = graph ? a.node_size : B;  // distinct positions of the new tokens
     float2 *cs_s = reinterpret_cast<float2 *>(sb + L::kOffCs);
     if (!graph)
-      for (int j = t; j < 2 * B; j += kSoftmax) tau_s[j] = __ldg(a.tau + c0 + (j < B ? j : j - B));
+      if (t < 2 * B) tau_s[t] = tau_j;      // 2B <= 64 <= kSoftmax
     for (int e = t; e < npos * (HD / 2); e += kSoftmax)
       cs_s[e] = rope_cs(a.tab, e % (HD / 2), P + e / (HD / 2));   // D~_k copies D_k's position
     named_sync(1, kSoftmax);
@@ -645,7 +667,7 @@ cudaError_t launch_attn_tc(const simsd_verify_desc *d, const VerifyPlan &p,
   if (!make_cache_map(&mk, d->k_cache, d->num_pages, d->num_kv_heads, d->head_dim) ||
       !make_cache_map(&mv, d->v_cache, d->num_pages, d->num_kv_heads, d->head_dim))
     return cudaErrorInvalidValue;
-  dim3 grid(p.n_splits, d->num_kv_heads * p.row_tiles, d->batch);
+  dim3 grid(p.grid);
   if (d->head_dim == 128) return launch_hd<128>(mk, mv, a, grid, stream);
   return launch_hd<64>(mk, mv, a, grid, stream);
 }

@@ -31,10 +31,18 @@ struct VerifyPlan {
   int row_tiles;     // CTAs per (sequence, KV head, split) along the rows
   int key_splits;    // warps sharing one stage's keys (mma path)
   int chunk;         // keys per split (multiple of kBlockKeys)
-  int n_splits;      // splits of the longest possible sequence
+  int n_splits;      // most splits of any unit (partials buffers)
+  // Units (sequence, KV head, row tile) in launch order: the first
+  // tail_from run whole, each later one in s_tail splits of chunk_tail
+  // keys (tail_from = 0: every unit split; tail_from = units: none)
+  int tail_from, s_tail, chunk_tail, grid;
+  // the split merge's rows: the last merge_rows of the T * Hq rows (the
+  // split units' sequences are the last ones; all rows when every unit is
+  // split)
+  int64_t merge_rows;
   size_t esize;      // bytes per q/k/v/out element
   // workspace carve-up (byte offsets)
-  size_t off_status, off_qrot, off_tokns, off_opart, off_ml, total;
+  size_t off_status, off_qrot, off_tokinfo, off_opart, off_ml, total;
 };
 
 // Fills *plan; returns SIMSD_OK or the first argument error.
@@ -69,6 +77,8 @@ struct AttnParams {
   int total_B, B_max;         // host copies: a sequence's cu_B and B must fit them
   int node_size;              // 0: SimSD's temporal layout; > 0: draft-graph nodes
   int chunk, rows_per_tile;
+  int tail_from, s_tail, chunk_tail;   // as in VerifyPlan
+  int row_tiles;
   uint32_t polls;             // bounded-wait polls (wait_polls_of the descriptor)
   float sm_scale;
   RopeTable tab;              // angles of the query rotation (bf16 kernel)
@@ -76,7 +86,7 @@ struct AttnParams {
 
 // K1: rotate q and k_new at the layout positions, append k/v to the cache.
 cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
-                               void *q_rot, int32_t *tok_ns, uint32_t *status,
+                               void *q_rot, int4 *tok_info, uint32_t *status,
                                cudaStream_t stream);
 cudaError_t launch_rope_append(const simsd_append_desc *d, cudaStream_t stream);
 
@@ -88,7 +98,7 @@ cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
 
 // K3: merge split partials.
 cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
-                           const AttnParams &a, const int32_t *tok_ns,
+                           const AttnParams &a, const int4 *tok_info,
                            cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).

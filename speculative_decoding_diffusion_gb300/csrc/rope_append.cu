@@ -137,10 +137,11 @@ struct RopeVerifyArgs {
   const int32_t *block_table;
   const int32_t *lens;
   const int32_t *cu_B;
-  int32_t *tok_ns;      // [T]: key splits of the token's sequence (0: malformed)
+  int4 *tok_info;       // [T]: (keys of the sequence or 0 if malformed, its first
+                        // unit, the token's index in the section, -)
   uint32_t *status;
   int batch, Hq, Hkv, hd, max_pages, num_pages;
-  int chunk;            // keys per split of the attention kernels
+  int row_tiles;        // row tiles per (sequence, KV head) of the attention kernel
   int total_B, B_max;   // host copies: a sequence's cu_B and B must fit them
   uint32_t polls;       // bounded-wait polls
   int node_size;        // 0: SimSD's paired layout; > 0: draft-graph nodes
@@ -202,8 +203,8 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
               (a.node_size > 0 && (2 * B) % a.node_size != 0));
   const int page = ok ? __ldg(a.block_table + (long)b * a.max_pages + slot / kPage) : -1;
   ok = ok && page >= 0 && page < a.num_pages;   // cu_B or block table out of range
-  // the split merge reads it: the rows it merges, without a search
-  if (threadIdx.x == 0) a.tok_ns[r] = ok ? (P + 2 * B + a.chunk - 1) / a.chunk : 0;
+  // the split merge reads it: which of its rows were split, without a search
+  if (threadIdx.x == 0) a.tok_info[r] = make_int4(ok ? P + 2 * B : 0, b * a.Hkv * a.row_tiles, j, 0);
   if (!ok && threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
   if (ok) angles(a.tab, a.hd, pos, cs);
   __syncthreads();
@@ -260,7 +261,7 @@ rope_append_kernel(const __grid_constant__ RopeAppendArgs a) {
 }  // namespace
 
 cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
-                               void *q_rot, int32_t *tok_ns, uint32_t *status,
+                               void *q_rot, int4 *tok_info, uint32_t *status,
                                cudaStream_t stream) {
   RopeVerifyArgs a;
   make_rope_table(d->rope_base, d->head_dim, &a.tab);
@@ -273,8 +274,8 @@ cudaError_t launch_rope_verify(const simsd_verify_desc *d, const VerifyPlan &p,
   a.block_table = d->block_table;
   a.lens = d->lens;
   a.cu_B = d->cu_B;
-  a.tok_ns = tok_ns;
-  a.chunk = p.chunk;
+  a.tok_info = tok_info;
+  a.row_tiles = p.row_tiles;
   a.status = status;
   a.num_pages = d->num_pages;
   a.batch = d->batch;
