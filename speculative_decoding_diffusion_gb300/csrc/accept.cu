@@ -136,6 +136,7 @@ struct AcceptParams {
   // kernel streams the rows itself.  Slices are then cpc whole chunks.
   const float2 *part;
   const float *xlogit;
+  int *claim;      // the chunk pass's item counter, zeroed here for the next call
   int nchunks, cpc;
 };
 
@@ -175,6 +176,10 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     fence_barrier_init();
   }
   __syncthreads();                           // the ring's barriers are ready
+  if (a.claim != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    grid_dep_wait();                         // the chunk pass has finished with it
+    *a.claim = 0;
+  }
   if (valid && !producer) {                  // (the producer starts streaming meanwhile)
     if (t < B) {
       S.tau[t] = __ldg(a.tau + c0 + t);
@@ -680,6 +685,7 @@ struct ChunkParams {
   const int32_t *draft_tokens;
   float2 *part;       // [2 total_B][nchunks][kAConsumerWarps]: (reference, sum of 2^(l ls - ref))
   float *xlogit;      // [2 total_B]
+  int *claim;         // item counter (zero at launch; the cluster kernel zeroes it again)
   uint32_t *status;
   int vocab, total_B, nchunks, bulk;
   uint32_t polls;
@@ -706,14 +712,13 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kAStages * kStage);
   uint64_t *empty = full + kAStages;
   int *stage_x = reinterpret_cast<int *>(empty + kAStages);   // [kAStages]: the item's draft token
-  int *flag = stage_x + kAStages;                             // a wait gave up (the drain)
+  int *stage_i = stage_x + kAStages;                          // [kAStages]: the item, -1: the end
+  int *flag = stage_i + kAStages;                             // a wait gave up (the drain)
   const uint32_t ring = smem_u32(smem);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool producer = warp == kAConsumerWarps;
   grid_dep_launch();                           // the cluster kernel may be scheduled
   const long items = 2L * a.total_B * a.nchunks;
-  const long mine = blockIdx.x < items ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  auto item_of = [&](long j) { return blockIdx.x + j * (long)gridDim.x; };
   if (t == 0) {
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
@@ -724,44 +729,74 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   }
   __syncthreads();
   long issued = 0;
+  bool ended = false;
   if (producer) {
-    // the items' draft tokens are requested kAStages items ahead into the
-    // same register slot (the loop is unrolled by kAStages, so no register
-    // moves while its load is in flight): no copy waits for that load
-    auto token_of = [&](long j) {
-      return j < mine ? __ldg(a.draft_tokens + (item_of(j) / a.nchunks >> 1)) : 0;
-    };
+    // Items: a CTA's first 2 kAStages items are static (blockIdx.x + k
+    // grid), the rest come from the workspace counter (first_dyn + c), so
+    // CTAs that stream faster take more.  Lane 0 keeps, per ring slot u,
+    // the slot's next item and its draft token (requested a ring ahead)
+    // and a claim one more ring ahead (its latency overlaps a ring of
+    // copies); the loop is unrolled by kAStages, so these stay in
+    // registers and none is moved while its load is in flight.
+    const long grid = gridDim.x, first_dyn = 2L * kAStages * grid;
+    auto token_of = [&](long i) { return i >= 0 ? __ldg(a.draft_tokens + (i / a.nchunks >> 1)) : 0; };
+    long it[kAStages], ahead[kAStages];
     int xs[kAStages];
+    if (lane == 0) {
 #pragma unroll
-    for (int u = 0; u < kAStages; ++u) xs[u] = token_of(u);
+      for (int u = 0; u < kAStages; ++u) {
+        const long i0 = blockIdx.x + u * grid, i1 = blockIdx.x + (kAStages + u) * grid;
+        it[u] = i0 < items ? i0 : -1;
+        ahead[u] = i1 < items ? i1 : -1;
+        xs[u] = token_of(it[u]);
+      }
+    }
     bool ok = true;
-    for (long j0 = 0; ok && j0 < mine; j0 += kAStages) {
+    for (long j0 = 0; ok && !ended; j0 += kAStages) {
 #pragma unroll
       for (int u = 0; u < kAStages; ++u) {
         const long j = j0 + u;
-        if (j >= mine) break;
         const int s = u;                            // j % kAStages (j0 is a multiple)
         if (j >= kAStages && !mbar_wait_warp(smem_u32(&empty[s]), ((j / kAStages) - 1) & 1, a.polls)) {
           if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); }
           ok = false;
           break;
         }
-        const long i = item_of(j);
+        const long i = __shfl_sync(0xffffffffu, lane == 0 ? it[u] : 0L, 0);
+        if (i < 0) {                                // the end: a stage without data
+          if (lane == 0) {
+            stage_i[s] = -1;
+            mbar_arrive(smem_u32(&full[s]));
+          }
+          ended = true;
+          break;
+        }
         const long p = i / a.nchunks;               // row pair index: slot p/2, target or draft
         const int c = (int)(i % a.nchunks);
         const int n = min(kChunk, a.vocab - c * kChunk);
-        // the draft token goes beside the stage before the copy's arrival
-        // (release) makes the stage visible to the consumers
-        if (lane == 0) stage_x[s] = xs[u];
+        // the item and its draft token go beside the stage before the
+        // copy's arrival (release) makes the stage visible to the consumers
+        if (lane == 0) {
+          stage_x[s] = xs[u];
+          stage_i[s] = (int)i;
+        }
         __syncwarp();
         const T *src = (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab + (long)c * kChunk;
         copy_piece<T>(smem + s * kStage, ring + s * kStage, src, n, smem_u32(&full[s]), a.bulk, lane);
         issued = j + 1;
-        xs[u] = token_of(j + kAStages);
+        if (lane == 0) {
+          it[u] = ahead[u];
+          xs[u] = token_of(it[u]);
+          ahead[u] = -1;
+          if (it[u] >= 0) {
+            const long i2 = first_dyn + atomicAdd(a.claim, 1);
+            ahead[u] = i2 < items ? i2 : -1;
+          }
+        }
       }
     }
   } else {
-    for (long j = 0; j < mine; ++j) {
+    for (long j = 0;; ++j) {
       const int s = (int)(j % kAStages);
       // a warp whose wait gave up neither reads nor releases the stage (its
       // copy may still land) and stops; the others are not held up by it
@@ -769,9 +804,10 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
         if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); }
         break;
       }
-      const long i = item_of(j);
+      const int i = stage_i[s];
+      if (i < 0) break;                             // the end
       const long p = i / a.nchunks;
-      const int c = (int)(i % a.nchunks);
+      const int c = i % a.nchunks;
       const int n = min(kChunk, a.vocab - c * kChunk);
       const uint4 *sv = reinterpret_cast<const uint4 *>(smem + s * kStage);
       const int v0 = warp * kWarpVecs;              // this warp's vectors: v0 + v * 32 + lane
@@ -816,11 +852,14 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
     }
   }
   // after a wait that gave up the copies in flight land before the CTA
-  // can exit (the flag is final after the barrier)
+  // can exit (the flag is final after the barrier; the end took the stage
+  // of item issued - kAStages, whose copy was consumed before)
   __syncthreads();
-  if (producer && *(volatile int *)flag)
-    for (long j = max(0L, issued - kAStages); j < issued; ++j)
+  if (producer && *(volatile int *)flag) {
+    const long from = issued - (ended ? kAStages - 1 : kAStages);
+    for (long j = from > 0 ? from : 0; j < issued; ++j)
       (void)mbar_wait_warp(smem_u32(&full[j % kAStages]), (j / kAStages) & 1);
+  }
 }
 
 constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(AccShared);
@@ -1435,7 +1474,7 @@ bool accept_pointers_ok(const simsd_accept_desc *d) {
 constexpr size_t kAcceptWorkspace = kAlign;
 struct AcceptLayout {
   int nchunks;
-  size_t off_part, off_xlogit, total;
+  size_t off_part, off_xlogit, off_claim, total;
 };
 AcceptLayout accept_layout(const simsd_accept_desc *d) {
   AcceptLayout L;
@@ -1444,7 +1483,8 @@ AcceptLayout accept_layout(const simsd_accept_desc *d) {
   L.off_part = kAcceptWorkspace;
   L.off_xlogit = align_up(L.off_part + (size_t)2 * d->total_B * L.nchunks * kAConsumerWarps *
                                            sizeof(float2), kAlign);
-  L.total = align_up(L.off_xlogit + (size_t)2 * d->total_B * sizeof(float), kAlign);
+  L.off_claim = align_up(L.off_xlogit + (size_t)2 * d->total_B * sizeof(float), kAlign);
+  L.total = L.off_claim + kAlign;
   return L;
 }
 size_t accept_workspace(const simsd_accept_desc *d) {
@@ -1560,6 +1600,7 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
            aligned16(d->draft_logits);
   a.part = nullptr;
   a.xlogit = nullptr;
+  a.claim = nullptr;
   a.nchunks = 0;
   a.cpc = 0;
   const AcceptLayout L = accept_layout(d);
@@ -1573,6 +1614,7 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     c.draft_tokens = d->draft_tokens;
     c.part = (float2 *)(ws + L.off_part);
     c.xlogit = (float *)(ws + L.off_xlogit);
+    c.claim = (int *)(ws + L.off_claim);
     c.status = a.status;
     c.vocab = d->vocab;
     c.total_B = d->total_B;
@@ -1583,6 +1625,7 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     e = d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16>(c, stream) : launch_chunks<float>(c, stream);
     a.part = c.part;
     a.xlogit = c.xlogit;
+    a.claim = c.claim;
     a.nchunks = L.nchunks;
   }
   mark(events, 1, stream);

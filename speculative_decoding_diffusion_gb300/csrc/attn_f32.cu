@@ -127,20 +127,26 @@ attn_f32_kernel(const __grid_constant__ AttnParams a) {
   }
 }
 
-// K3: O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s, one warp per
-// (token, query head) row; rows of single-split sequences were finished by
-// the attention kernel.  The split count comes from the append kernel (one
-// load), and kMergeBatch splits' partials are requested at a time.
-constexpr int kMergeBatch = 4;
+// K3: O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s, 16 threads per
+// (token, query head) row, each a contiguous hd/16 columns (16- or 32-byte
+// loads); rows of units that ran whole were finished by the attention
+// kernel.  Whether a row's unit was split comes from the append kernel (one
+// load); kMergeBatch splits' partials are requested at a time (3 at hd
+// 128, 4 at hd 64: what 64 registers hold without spilling).
+constexpr int kRowThreads = 16;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeRowsPerCta = kMergeThreads / kRowThreads;
 
-// four CTAs (32 warps) per SM without spills: enough loads in flight
+// four CTAs (64 rows) per SM without spills: every row of a large merge in
+// one wave, 128 KB of partials in flight per SM
 template <typename T, int HD>
-__global__ void __launch_bounds__(256, 4)
+__global__ void __launch_bounds__(kMergeThreads, 4)
 combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long row0) {
-  constexpr int PER = HD / 32;
+  constexpr int PER = HD / kRowThreads;      // 8 or 4 columns per thread
+  constexpr int kMergeBatch = HD == 128 ? 3 : 4;
   grid_dep_wait();                           // partials come from the attention kernel
-  const long row = row0 + (long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+  const long row = row0 + (long)blockIdx.x * kMergeRowsPerCta + threadIdx.x / kRowThreads;
+  const int col = (threadIdx.x % kRowThreads) * PER;
   if (row >= (long)a.T * a.Hq) return;
   // the row's unit (sequence, KV head, row tile) and whether it was split
   const int4 ti = __ldg(tok_info + row / a.Hq);   // keys 0: a malformed sequence (skipped)
@@ -156,14 +162,15 @@ combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long 
   for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
     const int n = min(kMergeBatch, ns - s0);
     float2 ml[kMergeBatch];
-    float v[kMergeBatch][PER];
+    float4 v[kMergeBatch][PER / 4];
 #pragma unroll
     for (int s = 0; s < kMergeBatch; ++s) {
       if (s < n) {
         const long pr = (s0 + s) * stride + row;
         ml[s] = __ldcg(a.ml_part + pr);
+        const float4 *src = reinterpret_cast<const float4 *>(a.o_part + pr * HD + col);
 #pragma unroll
-        for (int i = 0; i < PER; ++i) v[s][i] = __ldcg(a.o_part + pr * HD + lane + 32 * i);
+        for (int i = 0; i < PER / 4; ++i) v[s][i] = __ldcg(src + i);
       }
     }
     float mb = mstar;
@@ -184,14 +191,19 @@ combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long 
         const float w = exp2f(ml[s].x - mu);
         den += w * ml[s].y;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) o[i] = fmaf(w, v[s][i], o[i]);
+        for (int i = 0; i < PER / 4; ++i) {
+          o[4 * i] = fmaf(w, v[s][i].x, o[4 * i]);
+          o[4 * i + 1] = fmaf(w, v[s][i].y, o[4 * i + 1]);
+          o[4 * i + 2] = fmaf(w, v[s][i].z, o[4 * i + 2]);
+          o[4 * i + 3] = fmaf(w, v[s][i].w, o[4 * i + 3]);
+        }
       }
     }
   }
   const float inv = 1.f / den;
-  T *out = (T *)a.out + row * HD;
+  T *out = (T *)a.out + row * HD + col;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) Elem<T>::store(out + lane + 32 * i, o[i] * inv);
+  for (int i = 0; i < PER; ++i) Elem<T>::store(out + i, o[i] * inv);
 }
 
 }  // namespace
@@ -211,15 +223,15 @@ cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
                            cudaStream_t stream) {
   const long rows = (long)p.merge_rows;
   const long row0 = (long)p.T * d->num_q_heads - rows;
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  const unsigned blocks = (unsigned)((rows + kMergeRowsPerCta - 1) / kMergeRowsPerCta);
   const int4 *ts = tok_info;
   if (d->dtype == SIMSD_BF16)
     return d->head_dim == 128
-               ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(256), 0, stream, a, ts, row0)
-               : launch_pdl(combine_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(256), 0, stream, a, ts, row0);
+               ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0)
+               : launch_pdl(combine_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0);
   return d->head_dim == 128
-             ? launch_pdl(combine_kernel<float, 128>, dim3(blocks), dim3(256), 0, stream, a, ts, row0)
-             : launch_pdl(combine_kernel<float, 64>, dim3(blocks), dim3(256), 0, stream, a, ts, row0);
+             ? launch_pdl(combine_kernel<float, 128>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0)
+             : launch_pdl(combine_kernel<float, 64>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0);
 }
 
 }  // namespace simsd
