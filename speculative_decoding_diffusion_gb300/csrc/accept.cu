@@ -83,7 +83,6 @@ constexpr int kAConsumers = kAConsumerWarps * 32;
 constexpr int kAThreads = kAConsumers + 32;
 constexpr int kMaxPairs = 2 * kMaxB;               // (slot, row) pairs per sequence
 constexpr int kMaxVocab = 1 << 21;                 // 8 slices of kMaxPieces pieces of 8192 fp32 entries
-__device__ __forceinline__ void consumers_sync() { named_sync(1, kConsumers); }
 
 // ---------------------------------------------------------------- state
 struct __align__(16) WalkInfo {
@@ -94,9 +93,10 @@ struct __align__(16) WalkInfo {
   int pad0, pad1;
 };
 
-struct __align__(16) AccShared {
+template <int NW>                             // consumer warps
+struct __align__(16) AccSharedT {
   uint64_t full[kStages], empty[kStages];
-  float2 part_w[kMaxPairs][kConsumerWarps];   // per warp: (R, s) of each (slot, row)
+  float2 part_w[kMaxPairs][NW];               // per warp: (R, s) of each (slot, row)
   float2 cpart[kMaxPairs];                    // this CTA's slice: (R, s)
   float4 norm[kMaxPairs];                     // merged (M, S.hi, S.lo) of each (slot, row)
   float2 xv[kMaxB];                           // logits at the draft token, if in this slice
@@ -140,10 +140,23 @@ struct AcceptParams {
   int nchunks, cpc;
 };
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+// Two instances: NW = 16 consumer warps with a 6-stage ring (one CTA per
+// SM: the single-launch path, which streams every row itself), and NW = 8
+// with 3 stages (two CTAs per SM: partials mode, where only the rejected
+// slots' rows stream, so twice the sequences are resident at once).
+template <typename T, int NW, int NS>
+__global__ void __launch_bounds__((NW + 1) * 32, NW == 8 ? 2 : 1)
 accept_kernel(const __grid_constant__ AcceptParams a) {
   constexpr int N = Ld<T>::N;
+  constexpr int kConsumerWarps = NW, kConsumers = NW * 32, kStages = NS;
+  constexpr int kGroupWarps = NW / 2, kGroupThreads = kGroupWarps * 32;
+  constexpr int kVecs = kStageBytes / 16 / kGroupThreads;   // phase 1 (NW = 16 only)
+  constexpr bool kPartialsOnly = NW != 16;
+  constexpr int kRangesPerWarp = kRanges / NW;
+  static_assert(kRangesPerWarp * NW == kRanges, "whole ranges per warp");
+  using AccShared = AccSharedT<NW>;
+  auto consumers_sync = [] { named_sync(1, kConsumers); };
+  const bool part = kPartialsOnly || a.part != nullptr;   // partials mode
   extern __shared__ __align__(128) uint8_t smem[];
   AccShared &S = *reinterpret_cast<AccShared *>(smem + kStages * kStageBytes);
   const uint32_t ring = smem_u32(smem);
@@ -187,9 +200,9 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     }
     // partials mode: launched while the chunk pass finishes (programmatic
     // dependent launch); its results are read only after this wait
-    if (a.part) grid_dep_wait();
+    if (part) grid_dep_wait();
     if (t < B)
-      S.xv[t] = a.part ? make_float2(a.xlogit[2 * (c0 + t)], a.xlogit[2 * (c0 + t) + 1])
+      S.xv[t] = part ? make_float2(a.xlogit[2 * (c0 + t)], a.xlogit[2 * (c0 + t) + 1])
                        : make_float2(0.f, 0.f);
     if (t <= B) S.u[t] = __ldg(a.uniforms + (long)b * (a.B_max + 1) + t);
     consumers_sync();                        // the sequence's labels, tokens, uniforms
@@ -215,7 +228,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
   if (valid) {
     // ---------------------------------------------------- 1. row slices
     // (in partials mode the chunk pass did this: nothing is streamed)
-    const int J = a.part ? 0 : 2 * n_open * npieces;
+    const int J = part ? 0 : 2 * n_open * npieces;
     if (producer) {
       for (int pair = 0, pc = 0; g < J; ++g) {
         const int s = g % kStages;
@@ -319,7 +332,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         }
       }
       consumers_sync();
-      if (t < 2 * n_open && !a.part) {       // this CTA's slice of open pair t
+      if (t < 2 * n_open && !part) {       // this CTA's slice of open pair t
         float2 c = make_float2(-INFINITY, 0.f);
         if (npieces > 0 && !*(volatile int *)&S.flag) {
           float M = -INFINITY;
@@ -336,13 +349,13 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         S.cpart[t] = c;
       }
     }
-    if (!a.part) cluster_sync();             // B1: every slice's partials are in place
+    if (!part) cluster_sync();             // B1: every slice's partials are in place
 
     // ---------------------------------------------------- 2. the walk
     // every CTA merges the slices' partials and walks the steps itself (the
     // same inputs in the same order give the same decisions everywhere), so
     // no barrier is needed before the residual pass; CTA 0 writes outputs
-    if (!producer && a.part) {
+    if (!producer && part) {
       // partials mode: every CTA merges all of every open row's chunk
       // partials itself (warp w: open pairs w, w + 16, ...; lanes stride
       // over the row's chunks x the chunk pass's warps), so no cluster
@@ -433,7 +446,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         // the cluster that gave up in phase 1 (the snapshots are final
         // after B1, so every CTA decides alike): no walk
         bool any_fail = false;                 // (partials mode: phase 1 has no waits)
-        if (!a.part)
+        if (!part)
           for (int r = 0; r < a.csize; ++r) any_fail |= ld_dsmem_i32(dsmem(&S.fail1, r)) != 0;
         const bool perm = seen == (B == 32 ? 0xffffffffu : (1u << B) - 1u);
         int n = B, rej = -1;
@@ -482,9 +495,10 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           issued = g + 1;
         }
       } else {
-        // every warp takes part in every piece: warp w reads range w, the
-        // contiguous vectors [w * kRangeVecs, (w + 1) * kRangeVecs) of the
-        // piece (lane-interleaved), whose masses the draw narrows down to
+        // every warp takes part in every piece: warp w reads ranges w,
+        // w + NW, ..., each the contiguous vectors [r * kRangeVecs,
+        // (r + 1) * kRangeVecs) of the piece (lane-interleaved), whose
+        // masses the draw narrows down to
         for (int pc = 0; pc < npieces && !*(volatile int *)&S.flag; ++pc) {
           const int gt = J + 2 * pc, gd = gt + 1;
           const int st = gt % kStages, sd = gd % kStages;
@@ -497,20 +511,26 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
           const uint4 *tv = reinterpret_cast<const uint4 *>(smem + st * kStageBytes);
           const uint4 *dv = reinterpret_cast<const uint4 *>(smem + sd * kStageBytes);
           const int nvec = (n + N - 1) / N;
-          float rs[4] = {0.f, 0.f, 0.f, 0.f}, ps[4] = {0.f, 0.f, 0.f, 0.f};
-          if (warp * kRangeVecs < nvec) {
+          float rs[kRangesPerWarp][4], ps[kRangesPerWarp][4];
 #pragma unroll
-            for (int i = 0; i < kRangeVecs / 32; ++i) {
-              const int idx = warp * kRangeVecs + i * 32 + lane;
-              const bool in = idx < nvec;
-              float ft[N], fd[N];
-              Ld<T>::unpack(in ? tv[idx] : Ld<T>::neg_inf(), ft);
-              Ld<T>::unpack(in ? dv[idx] : Ld<T>::neg_inf(), fd);
+          for (int k = 0; k < kRangesPerWarp; ++k) {
+            const int r = warp + k * NW;
 #pragma unroll
-              for (int e = 0; e < N; ++e) {
-                const float et = rel_exp(ft[e], w.Mt, ls);
-                rs[e & 3] += residual(et, draft_mass(fd[e], w.Md, w.rho, ls));
-                ps[e & 3] += et;
+            for (int e = 0; e < 4; ++e) rs[k][e] = ps[k][e] = 0.f;
+            if (r * kRangeVecs < nvec) {
+#pragma unroll
+              for (int i = 0; i < kRangeVecs / 32; ++i) {
+                const int idx = r * kRangeVecs + i * 32 + lane;
+                const bool in = idx < nvec;
+                float ft[N], fd[N];
+                Ld<T>::unpack(in ? tv[idx] : Ld<T>::neg_inf(), ft);
+                Ld<T>::unpack(in ? dv[idx] : Ld<T>::neg_inf(), fd);
+#pragma unroll
+                for (int e = 0; e < N; ++e) {
+                  const float et = rel_exp(ft[e], w.Mt, ls);
+                  rs[k][e & 3] += residual(et, draft_mass(fd[e], w.Md, w.rho, ls));
+                  ps[k][e & 3] += et;
+                }
               }
             }
           }
@@ -519,14 +539,17 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
             mbar_arrive(smem_u32(&S.empty[st]));
             mbar_arrive(smem_u32(&S.empty[sd]));
           }
-          Ff fr = ff_add(ff_of(rs[0] + rs[1]), ff_of(rs[2] + rs[3]));
-          Ff fp = ff_add(ff_of(ps[0] + ps[1]), ff_of(ps[2] + ps[3]));
+#pragma unroll
+          for (int k = 0; k < kRangesPerWarp; ++k) {
+            Ff fr = ff_add(ff_of(rs[k][0] + rs[k][1]), ff_of(rs[k][2] + rs[k][3]));
+            Ff fp = ff_add(ff_of(ps[k][0] + ps[k][1]), ff_of(ps[k][2] + ps[k][3]));
 #pragma unroll 1
-          for (int m = 16; m > 0; m >>= 1) {
-            fr = ff_add(fr, ff_shfl_xor(fr, m));
-            fp = ff_add(fp, ff_shfl_xor(fp, m));
+            for (int m = 16; m > 0; m >>= 1) {
+              fr = ff_add(fr, ff_shfl_xor(fr, m));
+              fp = ff_add(fp, ff_shfl_xor(fp, m));
+            }
+            if (lane == 0) S.piece_w[pc][warp + k * NW] = make_float4(fr.hi, fr.lo, fp.hi, fp.lo);
           }
-          if (lane == 0) S.piece_w[pc][warp] = make_float4(fr.hi, fr.lo, fp.hi, fp.lo);
         }
         consumers_sync();
         if (warp == 0) {                     // lane i: piece i (npieces <= 32)
@@ -862,19 +885,29 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   }
 }
 
-constexpr size_t kSmemBytes = kStages * kStageBytes + sizeof(AccShared);
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// The two instances of the cluster kernel: consumer warps, ring stages,
+// threads and shared memory.
+template <int NW, int NS>
+struct AccCfg {
+  static constexpr int kNW = NW, kNS = NS, kThreadsPerCta = (NW + 1) * 32;
+  static constexpr size_t kSmem = (size_t)NS * kStageBytes + sizeof(AccSharedT<NW>);
+};
+using CfgSingle = AccCfg<kConsumerWarps, kStages>;   // streams every row itself
+using CfgPartials = AccCfg<8, 3>;                    // partials mode, two CTAs per SM
+static_assert(CfgSingle::kSmem <= 227 * 1024, "shared memory budget");
+static_assert(2 * (CfgPartials::kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
 void mark(void *const *events, int i, cudaStream_t stream) {
   if (events != nullptr) record_event(events[i], stream);
 }
 
+template <typename C>
 cudaLaunchConfig_t launch_config(int csize, int batch, cudaStream_t stream,
                                  cudaLaunchAttribute *attr, bool after_chunks = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize, batch);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(C::kThreadsPerCta);
+  cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = csize;
@@ -889,30 +922,29 @@ cudaLaunchConfig_t launch_config(int csize, int batch, cudaStream_t stream,
   return cfg;
 }
 
-// Per device and cluster size 1..kMaxCluster: clusters of this kernel
-// resident at once (queried once; the answer depends on the device only;
-// -1 for a size the device cannot place).
-template <typename T>
+// Per device, instance and cluster size 1..kMaxCluster: clusters resident
+// at once (queried once; the answer depends on the device only; -1 for a
+// size the device cannot place).
+template <typename T, typename C>
 cudaError_t max_active_clusters(int dev, int csize, int *out) {
   static std::mutex mu;
   static int cache[64][kMaxCluster + 1] = {};
+  auto kern = accept_kernel<T, C::kNW, C::kNS>;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev][0] == 0) {
-    cudaError_t e = cudaFuncSetAttribute(accept_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     // sizes over 8 are optional: without the attribute they are skipped
-    if (cudaFuncSetAttribute(accept_kernel<T>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
       (void)cudaGetLastError();
     cache[dev][0] = 1;
   }
   if (cache[dev][csize] == 0) {
     cudaLaunchAttribute attr[2];
-    const cudaLaunchConfig_t cfg = launch_config(csize, csize, nullptr, attr);
+    const cudaLaunchConfig_t cfg = launch_config<C>(csize, csize, nullptr, attr);
     int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, accept_kernel<T>, &cfg);
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) {
       if (csize <= 8) return e;
       (void)cudaGetLastError();              // a non-portable size this device refuses
@@ -924,8 +956,8 @@ cudaError_t max_active_clusters(int dev, int csize, int *out) {
   return cudaSuccess;
 }
 
-template <typename T>
-cudaError_t launch(AcceptParams a, cudaStream_t stream) {
+template <typename T, typename C>
+cudaError_t launch_cfg(AcceptParams a, cudaStream_t stream) {
   const int dev = current_device();
   // Cluster size by a makespan estimate: clusters run in waves of the
   // resident count; a CTA's time is its share of the sequence's exponentials
@@ -944,8 +976,9 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
   double best = 1e300;
   for (int c = kMaxCluster; c >= 1; --c) {
     if (((int64_t)a.vocab + c - 1) / c > max_slice) break;
+    if (a.part && c > a.nchunks) continue;   // every CTA's slice holds a chunk
     int n = 0;
-    cudaError_t e = max_active_clusters<T>(dev, c, &n);
+    cudaError_t e = max_active_clusters<T, C>(dev, c, &n);
     if (e != cudaSuccess) return e;
     if (n <= 0) continue;
     const double waves = (double)((a.batch + n - 1) / n);
@@ -965,8 +998,13 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
     a.piece = ((a.per + np - 1) / np + vec - 1) / vec * vec;
   }
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = launch_config(csize, a.batch, stream, attr, a.part != nullptr);
-  return cudaLaunchKernelEx(&cfg, accept_kernel<T>, a);
+  const cudaLaunchConfig_t cfg = launch_config<C>(csize, a.batch, stream, attr, a.part != nullptr);
+  return cudaLaunchKernelEx(&cfg, accept_kernel<T, C::kNW, C::kNS>, a);
+}
+
+template <typename T>
+cudaError_t launch(AcceptParams a, cudaStream_t stream) {
+  return a.part ? launch_cfg<T, CfgPartials>(a, stream) : launch_cfg<T, CfgSingle>(a, stream);
 }
 
 // The chunk pass: as many CTAs as the device holds at once (queried once
