@@ -11,6 +11,8 @@
 // stride over keys for the scores and over head dimensions for P.V.  The
 // softmax runs online in the log2 domain, like the bf16 kernel, so both
 // produce partials K3 can merge.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -127,27 +129,41 @@ attn_f32_kernel(const __grid_constant__ AttnParams a) {
   }
 }
 
-// K3: O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s, 16 threads per
-// (token, query head) row, each a contiguous hd/16 columns (16- or 32-byte
-// loads); rows of units that ran whole were finished by the attention
-// kernel.  Whether a row's unit was split comes from the append kernel (one
-// load); kMergeBatch splits' partials are requested at a time (3 at hd
-// 128, 4 at hd 64: what 64 registers hold without spilling).
-constexpr int kRowThreads = 16;
+// K3: O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s, one warp per
+// (token, query head) row, each lane a contiguous hd/32 columns (8- or
+// 16-byte loads); rows of units that ran whole were finished by the
+// attention kernel.  The partials of the first kMergeBatch splits are
+// requested before the row's split count is known (the buffer holds every
+// split of every row, so the reads stay in it; the extra ones are
+// dropped), so a merge of up to kMergeBatch splits costs one round trip.
+// Whether a row's unit was split comes from the append kernel's per-token
+// record.
+constexpr int kMergeBatch = 8;
 constexpr int kMergeThreads = 256;
-constexpr int kMergeRowsPerCta = kMergeThreads / kRowThreads;
+constexpr int kMergeRowsPerCta = kMergeThreads / 32;
 
-// four CTAs (64 rows) per SM without spills: every row of a large merge in
-// one wave, 128 KB of partials in flight per SM
+// four CTAs (32 rows) per SM without spills: lane s keeps split s's
+// (max, sum) and its weight is broadcast when the partials are summed
 template <typename T, int HD>
 __global__ void __launch_bounds__(kMergeThreads, 4)
-combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long row0) {
-  constexpr int PER = HD / kRowThreads;      // 8 or 4 columns per thread
-  constexpr int kMergeBatch = HD == 128 ? 3 : 4;
+combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long row0, int max_splits) {
+  constexpr int PER = HD / 32;               // 4 or 2 columns per lane
+  using V = typename std::conditional<PER == 4, float4, float2>::type;
   grid_dep_wait();                           // partials come from the attention kernel
-  const long row = row0 + (long)blockIdx.x * kMergeRowsPerCta + threadIdx.x / kRowThreads;
-  const int col = (threadIdx.x % kRowThreads) * PER;
+  const long row = row0 + (long)blockIdx.x * kMergeRowsPerCta + threadIdx.x / 32;
+  const int lane = threadIdx.x % 32, col = lane * PER;
   if (row >= (long)a.T * a.Hq) return;
+  const long stride = (long)a.T * a.Hq;
+  auto load_batch = [&](int s0, int n, V *v, float2 &ml) {
+#pragma unroll
+    for (int s = 0; s < kMergeBatch; ++s)
+      if (s < n) v[s] = __ldcg(reinterpret_cast<const V *>(a.o_part + ((s0 + s) * stride + row) * HD + col));
+    ml = lane < n ? __ldcg(a.ml_part + (s0 + lane) * stride + row) : make_float2(-INFINITY, 0.f);
+  };
+  // the first batch, requested with the row's record
+  V v[kMergeBatch];
+  float2 ml;
+  load_batch(0, min(kMergeBatch, max_splits), v, ml);
   // the row's unit (sequence, KV head, row tile) and whether it was split
   const int4 ti = __ldg(tok_info + row / a.Hq);   // keys 0: a malformed sequence (skipped)
   const int hq = (int)(row % a.Hq);
@@ -155,28 +171,17 @@ combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long 
   const int unit = ti.y + rtile * a.Hkv + hq / a.G;
   const int ns = unit >= a.tail_from ? (ti.x + a.chunk_tail - 1) / a.chunk_tail : 1;
   if (ns <= 1) return;
-  const long stride = (long)a.T * a.Hq;
   float mstar = -INFINITY, den = 0.f, o[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) o[i] = 0.f;
   for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
     const int n = min(kMergeBatch, ns - s0);
-    float2 ml[kMergeBatch];
-    float4 v[kMergeBatch][PER / 4];
+    if (s0 > 0) load_batch(s0, n, v, ml);
+    if (lane >= n) ml = make_float2(-INFINITY, 0.f);   // splits past the row's own
+    float mb = ml.x;
 #pragma unroll
-    for (int s = 0; s < kMergeBatch; ++s) {
-      if (s < n) {
-        const long pr = (s0 + s) * stride + row;
-        ml[s] = __ldcg(a.ml_part + pr);
-        const float4 *src = reinterpret_cast<const float4 *>(a.o_part + pr * HD + col);
-#pragma unroll
-        for (int i = 0; i < PER / 4; ++i) v[s][i] = __ldcg(src + i);
-      }
-    }
-    float mb = mstar;
-#pragma unroll
-    for (int s = 0; s < kMergeBatch; ++s)
-      if (s < n) mb = fmaxf(mb, ml[s].x);
+    for (int m = 16; m > 0; m >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, m));
+    mb = fmaxf(mb, mstar);
     if (mb > mstar && mstar != -INFINITY) {  // a later batch raised the reference
       const float r = exp2f(mstar - mb);
       den *= r;
@@ -185,18 +190,18 @@ combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long 
     }
     mstar = mb;
     const float mu = mstar == -INFINITY ? 0.f : mstar;
+    const float wl = lane < n ? exp2f(ml.x - mu) : 0.f;   // lane s: split s's weight
+    float dl = wl * ml.y;
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, m);
+    den += dl;
 #pragma unroll
     for (int s = 0; s < kMergeBatch; ++s) {
+      const float w = __shfl_sync(0xffffffffu, wl, s);
       if (s < n) {
-        const float w = exp2f(ml[s].x - mu);
-        den += w * ml[s].y;
+        const float *vf = reinterpret_cast<const float *>(&v[s]);
 #pragma unroll
-        for (int i = 0; i < PER / 4; ++i) {
-          o[4 * i] = fmaf(w, v[s][i].x, o[4 * i]);
-          o[4 * i + 1] = fmaf(w, v[s][i].y, o[4 * i + 1]);
-          o[4 * i + 2] = fmaf(w, v[s][i].z, o[4 * i + 2]);
-          o[4 * i + 3] = fmaf(w, v[s][i].w, o[4 * i + 3]);
-        }
+        for (int i = 0; i < PER; ++i) o[i] = fmaf(w, vf[i], o[i]);
       }
     }
   }
@@ -227,11 +232,11 @@ cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
   const int4 *ts = tok_info;
   if (d->dtype == SIMSD_BF16)
     return d->head_dim == 128
-               ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0)
-               : launch_pdl(combine_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0);
+               ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0, p.n_splits)
+               : launch_pdl(combine_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0, p.n_splits);
   return d->head_dim == 128
-             ? launch_pdl(combine_kernel<float, 128>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0)
-             : launch_pdl(combine_kernel<float, 64>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0);
+             ? launch_pdl(combine_kernel<float, 128>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0, p.n_splits)
+             : launch_pdl(combine_kernel<float, 64>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0, p.n_splits);
 }
 
 }  // namespace simsd
