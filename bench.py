@@ -26,6 +26,9 @@ results inside the timed region; host launch cost included); `e2e_graph`
 captures those copies and calls in a graph as well.  `roofline`: the
 attention kernel K2 (the dominant one), algorithmic bytes per launch over
 its mean event-timed duration.
+`next_rows`: the blockwise loop's draft-side step and commit and the
+greedy and sample-matching acceptance rules on the same workload, each
+replayed alone (event-timed, L2 flushed), outside the step's timed region.
 `cpu_baseline`: the fp64 oracle on a bounded sample of the same workload
 (its first sequences, as many as take about a second per pass), timed on
 this host's cores.
@@ -83,6 +86,68 @@ def parse():
 
 def rule_code(args):
     return {"sample": 0, "greedy": 1, "match": 2}[args.accept]
+
+
+# ---------------------------------------------------------------- the next rows
+def time_next_rows(w, dw, flush, reps, peak):
+    """The loop's other steps and the acceptance variants on the same
+    workload, each captured alone in a CUDA graph and replayed with L2
+    flushed before each replay (event-timed): the draft-side step over every
+    slot's draft row, the commit, the greedy rule and sample matching.
+    Algorithmic bytes: the draft rows once (draft step), the target rows
+    once (greedy, matching)."""
+    import torch
+    from speculative_decoding_diffusion_gb300 import binding
+    dev = dw.target.device
+    batch, B_max, total_B = len(w.lens), int(w.Bs.max()), int(w.cu_B[-1])
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    u_draft = torch.rand(batch, B_max, generator=g, device=dev, dtype=torch.float32)
+    tokens = torch.zeros(total_B, dtype=torch.int32, device=dev)
+    tau_out = torch.zeros(total_B, dtype=torch.int32, device=dev)
+    ws = torch.zeros(binding.draft_workspace_size(dw.draft, dw.cu_B, total_B, B_max),
+                     dtype=torch.uint8, device=dev)
+    dw.accept()                               # the walk the commit applies
+    c_tokens = dw.draft_tokens.clone()
+    c_decided = torch.zeros(batch, dtype=torch.int32, device=dev)
+    c_lens = dw.lens.clone()
+    c_done = torch.zeros(batch, dtype=torch.int32, device=dev)
+    cws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+    calls = {
+        "draft_step": lambda: binding.draft_step(dw.draft, dw.cu_B, u_draft, tokens, tau_out, ws,
+                                                 total_B, B_max),
+        "commit": lambda: binding.commit(dw.cu_B, dw.tau, dw.n_accept, dw.token, dw.pos, c_tokens,
+                                         c_decided, c_lens, c_done, cws, total_B, B_max),
+        "greedy": lambda: dw.accept(rule=binding.SIMSD_ACCEPT_GREEDY),
+        "match": lambda: dw.accept(rule=binding.SIMSD_ACCEPT_MATCH),
+    }
+    es = 2 if w.spec.dtype == "bf16" else 4
+    row_bytes = total_B * w.spec.vocab * es
+    out = {}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for name, call in calls.items():
+        call()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            call()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            t0.record()
+            gr.replay()
+            t1.record()
+            torch.cuda.synchronize()
+            ms.append(t0.elapsed_time(t1))
+        us = float(np.mean(ms)) * 1e3
+        rec = {"us": round(us, 2)}
+        if name != "commit":
+            gbs = row_bytes / (us / 1e6) / 1e9
+            rec.update({"GBps": round(gbs, 1), "frac": round(gbs / peak, 3)})
+        out[name] = rec
+    st = binding.read_status(ws) | binding.read_status(cws)
+    out["status_word"] = st
+    return out
 
 
 # ---------------------------------------------------------------- algorithmic bytes
@@ -482,6 +547,8 @@ def main():
         e2eg_ms.append((time.perf_counter() - t0) * 1e3)
     e2e_total = max_over_ranks(dist, e2e_total, "cuda")
     e2eg_total = max_over_ranks(dist, float(np.sum(e2eg_ms)), "cuda")
+    peak, peak_kind = hbm_peak()
+    next_rows = time_next_rows(w, dw, flush, max(10, args.steps // 4), peak)
     clk = clocks.stop()
     status = binding.read_status(dw.verify_ws) | binding.read_status(dw.accept_ws)
 
@@ -489,7 +556,6 @@ def main():
     value = throughput(int(w.cu_B[-1]), world, dev_total_ms, args.steps)
     e2e_value = throughput(int(w.cu_B[-1]), world, e2e_total, args.steps)
     e2eg_value = throughput(int(w.cu_B[-1]), world, e2eg_total, args.steps)
-    peak, peak_kind = hbm_peak()
     k2_mean = float(np.mean(k_ms["K2"]))
     achieved = k2_bytes(w) / (k2_mean / 1e3) / 1e9
     traffic = recorded_traffic(w.spec)
@@ -523,6 +589,7 @@ def main():
             "accept_GBps": accept_bytes(w, args.accept != "sample") / (acc_ms / 1e3) / 1e9,
             "accept_frac": accept_bytes(w, args.accept != "sample") / (acc_ms / 1e3) / 1e9 / peak,
             "kernels_ms": {n: round(k["ms"], 5) for n, k in kernels.items()},
+            "next_rows": next_rows,
             "clocks": clk, "status_word": status}
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import build as obuild

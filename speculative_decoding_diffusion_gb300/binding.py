@@ -296,6 +296,21 @@ def _status_ws(workspace):
     return _ptr(workspace), (0 if workspace is None else workspace.numel() * workspace.element_size())
 
 
+def draft_workspace_size(draft, cu_B, total_B, B_max, temperature=1.0):
+    """simsd_draft_workspace_size: the chunked path's workspace (a workspace
+    of only the status word runs the single cluster kernel)."""
+    d = DraftDesc()
+    d.batch = cu_B.shape[0] - 1
+    d.vocab = draft.shape[1]
+    d.total_B, d.B_max = int(total_B), int(B_max)
+    d.dtype = _dtype_code(draft)
+    d.temperature = float(temperature)
+    n = lib().simsd_draft_workspace_size(ctypes.byref(d))
+    if n == 0:
+        raise SimsdError(2, "simsd_draft_workspace_size")
+    return int(n)
+
+
 def draft_step(draft, cu_B, uniforms, tokens, tau, workspace, total_B, B_max, decided=None,
                tau_prev=None, confidence=None, temperature=1.0, stream=None):
     """simsd_draft_step: tokens (in/out) and tau (out) of every sequence's

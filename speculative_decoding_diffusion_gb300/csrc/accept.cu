@@ -708,6 +708,8 @@ struct ChunkParams {
   const int32_t *draft_tokens;
   float2 *part;       // [2 total_B][nchunks][kAConsumerWarps]: (reference, sum of 2^(l ls - ref))
   float *xlogit;      // [2 total_B]
+  float4 *part4;      // draft rows only: [total_B][nchunks][kAConsumerWarps]: (reference,
+                      // sum, the part's largest logit, -)
   int *claim;         // item counter (zero at launch; the cluster kernel zeroes it again)
   uint32_t *status;
   int vocab, total_B, nchunks, bulk;
@@ -722,7 +724,9 @@ __host__ __device__ constexpr int chunk_entries() { return kStageBytes / (int)si
 template <typename T>
 constexpr size_t chunk_smem_bytes() { return (size_t)kAStages * chunk_stage_bytes<T>() + 256; }
 
-template <typename T>
+// DRAFT: the draft-side step's pass over the draft rows alone (items
+// (row, chunk), no logit at a token, the part's largest logit kept).
+template <typename T, bool DRAFT>
 __global__ void __launch_bounds__(kAThreads)
 vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   constexpr int N = Ld<T>::N;
@@ -741,7 +745,7 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool producer = warp == kAConsumerWarps;
   grid_dep_launch();                           // the cluster kernel may be scheduled
-  const long items = 2L * a.total_B * a.nchunks;
+  const long items = (DRAFT ? 1L : 2L) * a.total_B * a.nchunks;
   if (t == 0) {
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
@@ -762,7 +766,9 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
     // copies); the loop is unrolled by kAStages, so these stay in
     // registers and none is moved while its load is in flight.
     const long grid = gridDim.x, first_dyn = 2L * kAStages * grid;
-    auto token_of = [&](long i) { return i >= 0 ? __ldg(a.draft_tokens + (i / a.nchunks >> 1)) : 0; };
+    auto token_of = [&](long i) {
+      return DRAFT || i < 0 ? 0 : __ldg(a.draft_tokens + (i / a.nchunks >> 1));
+    };
     long it[kAStages], ahead[kAStages];
     int xs[kAStages];
     if (lane == 0) {
@@ -804,7 +810,9 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
           stage_i[s] = (int)i;
         }
         __syncwarp();
-        const T *src = (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab + (long)c * kChunk;
+        const T *src = DRAFT ? (const T *)a.draft + p * a.vocab + (long)c * kChunk
+                             : (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab +
+                                   (long)c * kChunk;
         copy_piece<T>(smem + s * kStage, ring + s * kStage, src, n, smem_u32(&full[s]), a.bulk, lane);
         issued = j + 1;
         if (lane == 0) {
@@ -841,7 +849,7 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
         w[v] = idx * N < n ? sv[idx] : Ld<T>::neg_inf();
       }
       // the logit at the slot's draft token, if this warp's part holds it
-      const int off = stage_x[s] - c * kChunk;
+      const int off = DRAFT ? -1 : stage_x[s] - c * kChunk;
       if (off >= 0 && off < n && off / N >= v0 && off / N < v0 + kWarpVecs && (off / N - v0) % 32 == lane) {
         const int vx = (off / N - v0) / 32;
         uint4 wx = w[0];
@@ -857,7 +865,8 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
       const float mx = Ld<T>::vmax(w, kV);
       const uint32_t mu = __float_as_uint(mx);
       const uint32_t km = __reduce_max_sync(0xffffffffu, (mu & 0x80000000u) ? ~mu : (mu | 0x80000000u));
-      const float R = ref_of(__uint_as_float((km & 0x80000000u) ? (km & 0x7fffffffu) : ~km), a.ls);
+      const float wmax = __uint_as_float((km & 0x80000000u) ? (km & 0x7fffffffu) : ~km);
+      const float R = ref_of(wmax, a.ls);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       if (R != -INFINITY) {
 #pragma unroll
@@ -871,7 +880,12 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
       float sm = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
-      if (lane == 0) a.part[(p * a.nchunks + c) * kAConsumerWarps + warp] = make_float2(R, sm);
+      if (lane == 0) {
+        if (DRAFT)
+          a.part4[(p * a.nchunks + c) * kAConsumerWarps + warp] = make_float4(R, sm, wmax, 0.f);
+        else
+          a.part[(p * a.nchunks + c) * kAConsumerWarps + warp] = make_float2(R, sm);
+      }
     }
   }
   // after a wait that gave up the copies in flight land before the CTA
@@ -1009,7 +1023,7 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
 
 // The chunk pass: as many CTAs as the device holds at once (queried once
 // per device and dtype), never more than the items.
-template <typename T>
+template <typename T, bool DRAFT>
 cudaError_t launch_chunks(const ChunkParams &c, cudaStream_t stream) {
   static std::mutex mu;
   static int resident[64] = {0};
@@ -1019,21 +1033,21 @@ cudaError_t launch_chunks(const ChunkParams &c, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (resident[dev] == 0) {
-      cudaError_t e = cudaFuncSetAttribute(vocab_chunk_kernel<T>,
+      cudaError_t e = cudaFuncSetAttribute(vocab_chunk_kernel<T, DRAFT>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)chunk_smem_bytes<T>());
       if (e != cudaSuccess) return e;
       int n = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, vocab_chunk_kernel<T>, kAThreads,
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, vocab_chunk_kernel<T, DRAFT>, kAThreads,
                                                         chunk_smem_bytes<T>());
       if (e != cudaSuccess) return e;
       resident[dev] = n > 0 ? n : 1;
     }
     per_sm = resident[dev];
   }
-  const long items = 2L * c.total_B * c.nchunks;
+  const long items = (DRAFT ? 1L : 2L) * c.total_B * c.nchunks;
   const long grid = std::min<long>(items, (long)per_sm * device_sm_count());
-  vocab_chunk_kernel<T><<<(unsigned)grid, kAThreads, chunk_smem_bytes<T>(), stream>>>(c);
+  vocab_chunk_kernel<T, DRAFT><<<(unsigned)grid, kAThreads, chunk_smem_bytes<T>(), stream>>>(c);
   return cudaGetLastError();
 }
 
@@ -1653,6 +1667,7 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     c.part = (float2 *)(ws + L.off_part);
     c.xlogit = (float *)(ws + L.off_xlogit);
     c.claim = (int *)(ws + L.off_claim);
+    c.part4 = nullptr;
     c.status = a.status;
     c.vocab = d->vocab;
     c.total_B = d->total_B;
@@ -1660,7 +1675,8 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     c.bulk = a.bulk;
     c.polls = a.polls;
     c.ls = a.ls;
-    e = d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16>(c, stream) : launch_chunks<float>(c, stream);
+    e = d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16, false>(c, stream)
+                                 : launch_chunks<float, false>(c, stream);
     a.part = c.part;
     a.xlogit = c.xlogit;
     a.claim = c.claim;
@@ -1674,6 +1690,31 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
 }
 
 }  // namespace
+
+int draft_chunk_entries(int esize) { return kStageBytes / esize; }
+
+cudaError_t launch_draft_chunks(const simsd_draft_desc *d, float4 *part4, int *claim,
+                                uint32_t *status, int nchunks, cudaStream_t stream) {
+  ChunkParams c;
+  c.target = nullptr;
+  c.draft = d->draft_logits;
+  c.draft_tokens = nullptr;
+  c.part = nullptr;
+  c.xlogit = nullptr;
+  c.part4 = part4;
+  c.claim = claim;
+  c.status = status;
+  c.vocab = d->vocab;
+  c.total_B = d->total_B;
+  c.nchunks = nchunks;
+  const int es = d->dtype == SIMSD_BF16 ? 2 : 4;
+  c.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->draft_logits);
+  c.polls = kWaitPolls;
+  c.ls = scale_of(d->temperature > 0.f ? (double)d->temperature : 1.0);
+  return d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16, true>(c, stream)
+                                : launch_chunks<float, true>(c, stream);
+}
+
 }  // namespace simsd
 
 using namespace simsd;

@@ -139,4 +139,12 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 
+// The draft-side step's chunk pass over the draft rows (accept.cu): per
+// (row, 32 KB chunk, consumer warp) the reference, the sum of 2^(l ls -
+// reference) and the part's largest logit, into part4 [total_B][nchunks][8].
+// *claim must be zero; the finishing kernel zeroes it again.
+int draft_chunk_entries(int esize);
+cudaError_t launch_draft_chunks(const simsd_draft_desc *d, float4 *part4, int *claim,
+                                uint32_t *status, int nchunks, cudaStream_t stream);
+
 }  // namespace simsd

@@ -282,6 +282,187 @@ draft_kernel(const __grid_constant__ DraftParams a) {
   cluster_sync();                                   // B2: no CTA leaves while others read it
 }
 
+// The draft step over a chunk pass (no decided slots; a full workspace).
+// The chunk pass (accept.cu) left, per (row, 32 KB chunk, part of 1/8
+// chunk), the part's reference, sum of 2^(l ls - reference) and largest
+// logit; parts in (chunk, part) order are contiguous vocabulary ranges in
+// vocabulary order.  One CTA per sequence, a warp per slot: the row's
+// normaliser S and largest logit (exact merge by powers of two), U = u S,
+// the first part whose running mass exceeds U (else the last with mass),
+// then that part read again column by column in vocabulary order (an fp32
+// scan relative to the part's start) for the first entry whose running
+// mass exceeds U; then the slots ordered by their largest probability.
+constexpr int kFinishThreads = 512;
+constexpr int kFinishWarps = kFinishThreads / 32;
+constexpr int kParts = 8;                         // parts per chunk (the chunk pass's warps)
+
+struct FinishParams {
+  const void *draft;
+  const int32_t *cu_B;
+  const float *uniforms;
+  const float4 *part4;      // [total_B][nchunks][kParts]
+  int *claim;               // the chunk pass's item counter, zeroed here
+  int32_t *tokens;
+  int32_t *tau;
+  float *confidence;
+  uint32_t *status;
+  int vocab, total_B, B_max, nchunks, chunk, bulk;
+  Scale ls;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kFinishThreads)
+draft_finish_kernel(const __grid_constant__ FinishParams a) {
+  constexpr int N = Ld<T>::N;
+  __shared__ float conf_s[kMaxB];
+  const int b = blockIdx.x, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  grid_dep_wait();                                  // the chunk pass's partials
+  if (b == 0 && t == 0) *a.claim = 0;               // ready for the next call
+  const int c0 = __ldg(a.cu_B + b), B = __ldg(a.cu_B + b + 1) - c0;
+  const bool valid = B >= 1 && B <= a.B_max && c0 >= 0 && c0 + B <= a.total_B;
+  if (!valid) {
+    if (t == 0) raise_status(a.status, kStatusBadInput);
+    return;
+  }
+  const Scale ls = a.ls;
+  const int n_ent = a.nchunks * kParts;             // parts of a row
+  const int part_len = a.chunk / kParts;            // entries of a part
+  const int part_vecs = part_len / N;
+  for (int k = warp; k < B; k += kFinishWarps) {
+    const float4 *pr = a.part4 + (long)(c0 + k) * n_ent;
+    // the row: M, S, largest logit (the first 4 x 32 parts held)
+    constexpr int kHeld = 4;
+    float4 h[kHeld];
+#pragma unroll
+    for (int i = 0; i < kHeld; ++i)
+      h[i] = lane + 32 * i < n_ent ? __ldcg(pr + lane + 32 * i) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+    float M = -INFINITY, xm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kHeld; ++i) { M = fmaxf(M, h[i].x); xm = fmaxf(xm, h[i].z); }
+    for (int i = lane + 32 * kHeld; i < n_ent; i += 32) {
+      const float4 v = __ldcg(pr + i);
+      M = fmaxf(M, v.x);
+      xm = fmaxf(xm, v.z);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      xm = fmaxf(xm, __shfl_xor_sync(0xffffffffu, xm, o));
+    }
+    auto mass_of = [&](float4 v) {
+      const float w = (M != -INFINITY && v.x != -INFINITY) ? exp2_int(v.x - M) : 0.f;
+      return v.y > 0.f ? v.y * w : 0.f;
+    };
+    Ff S = ff_of(0.f);
+#pragma unroll
+    for (int i = 0; i < kHeld; ++i) S = ff_add(S, ff_of(mass_of(h[i])));
+    for (int i = lane + 32 * kHeld; i < n_ent; i += 32) S = ff_add(S, ff_of(mass_of(__ldcg(pr + i))));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) S = ff_add(S, ff_shfl_xor(S, o));
+    const float u = __ldg(a.uniforms + (long)b * a.B_max + k);
+    const float uh = u * S.hi;
+    const Ff U = ff_add(Ff{uh, fmaf(u, S.hi, -uh)}, ff_of(u * S.lo));
+    // the part holding U: groups of 32 parts in vocabulary order
+    Ff base = ff_of(0.f), last_start = ff_of(0.f);
+    int sel = -1, last_nz = 0;
+    auto group = [&](int g0, float4 v) {              // parts g0 .. g0 + 31
+      const Ff m = ff_of(g0 + lane < n_ent ? mass_of(v) : 0.f);
+      Ff inc = m;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const Ff y = ff_shfl_up(inc, d);
+        if (lane >= d) inc = ff_add(y, inc);
+      }
+      const Ff run = ff_add(base, inc);
+      const Ff start = ff_add(base, ff_add(inc, ff_neg(m)));
+      const unsigned cross = __ballot_sync(0xffffffffu, m.hi > 0.f && ff_gt(run, U));
+      const unsigned nz = __ballot_sync(0xffffffffu, m.hi > 0.f);
+      if (cross) {
+        const int l = __ffs(cross) - 1;
+        sel = g0 + l;
+        base = ff_shfl(start, l);
+      } else {
+        if (nz) {
+          const int l = 31 - __clz(nz);
+          last_nz = g0 + l;
+          last_start = ff_shfl(start, l);
+        }
+        base = ff_shfl(run, 31);
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kHeld; ++i)
+      if (sel < 0 && 32 * i < n_ent) group(32 * i, h[i]);
+    for (int g0 = 32 * kHeld; g0 < n_ent && sel < 0; g0 += 32)
+      group(g0, g0 + lane < n_ent ? __ldcg(pr + g0 + lane) : make_float4(-INFINITY, 0.f, 0.f, 0.f));
+    if (sel < 0) {
+      sel = last_nz;
+      base = last_start;
+    }
+    // the entry: the part's vectors, 32 per column, in vocabulary order
+    const int p0 = (sel / kParts) * a.chunk + (sel % kParts) * part_len;
+    const int n = min(part_len, a.vocab - p0);
+    const T *row = (const T *)a.draft + (long)(c0 + k) * a.vocab + p0;
+    const Ff D0 = ff_add(U, ff_neg(base));
+    const float dd = D0.hi + D0.lo;
+    float col_base = 0.f;
+    int first = 0x7fffffff, last_pos = -1;
+#pragma unroll 1
+    for (int c = 0; c * 32 < part_vecs && first == 0x7fffffff; ++c) {
+      const int e0 = (c * 32 + lane) * N;
+      float f[N], m[N];
+      Ld<T>::unpack(Ld<T>::load(row + e0, n - e0, a.bulk != 0), f);
+      float lane_mass = 0.f;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        m[e] = rel_exp(f[e], M, ls);
+        lane_mass += m[e];
+        if (m[e] > 0.f) last_pos = p0 + e0 + e;
+      }
+      float inc = lane_mass;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += y;
+      }
+      const float prev = __shfl_up_sync(0xffffffffu, inc, 1);
+      const float start = col_base + (lane ? prev : 0.f);
+      if (dd < col_base + inc) {
+        float run = 0.f;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          run += m[e];
+          if (first == 0x7fffffff && m[e] > 0.f && start + run > dd) first = p0 + e0 + e;
+        }
+      }
+      first = __reduce_min_sync(0xffffffffu, first);
+      col_base += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    last_pos = __reduce_max_sync(0xffffffffu, last_pos);
+    if (lane == 0) {
+      a.tokens[c0 + k] = first != 0x7fffffff ? first : last_pos;
+      // the row's largest probability, in the kernel's own arithmetic
+      conf_s[k] = rel_exp(xm, M, ls) / (S.hi + S.lo);
+    }
+  }
+  __syncthreads();
+  if (t < B) {                                      // largest first, equal ones in position order
+    const float ck = conf_s[t];
+    int before = 0;
+    for (int j = 0; j < B; ++j) {
+      const float cj = conf_s[j];
+      if (cj > ck || (cj == ck && j < t)) ++before;
+    }
+    a.tau[c0 + t] = 1 + before;
+    if (a.confidence) a.confidence[c0 + t] = ck;
+  }
+}
+
+template <typename T>
+cudaError_t launch_finish(const FinishParams &f, int batch, cudaStream_t stream) {
+  return launch_pdl(draft_finish_kernel<T>, dim3(batch), dim3(kFinishThreads), 0, stream, f);
+}
+
 // The commit: one thread per sequence.
 struct CommitParams {
   const int32_t *cu_B, *tau, *n_accept, *token, *pos;
@@ -360,8 +541,23 @@ using namespace simsd;
 
 extern "C" {
 
+// The chunked path's workspace: status | chunk partials | item counter.
+struct DraftLayout {
+  int nchunks, chunk;
+  size_t off_part, off_claim, total;
+};
+DraftLayout draft_layout(const simsd_draft_desc *d) {
+  DraftLayout L;
+  L.chunk = draft_chunk_entries(d->dtype == SIMSD_BF16 ? 2 : 4);
+  L.nchunks = (d->vocab + L.chunk - 1) / L.chunk;
+  L.off_part = kStatusWorkspace;
+  L.off_claim = align_up(L.off_part + (size_t)d->total_B * L.nchunks * kParts * sizeof(float4), kAlign);
+  L.total = L.off_claim + kAlign;
+  return L;
+}
+
 size_t simsd_draft_workspace_size(const simsd_draft_desc *d) {
-  return draft_check(d) == SIMSD_OK ? kStatusWorkspace : 0;
+  return draft_check(d) == SIMSD_OK ? draft_layout(d).total : 0;
 }
 
 simsd_status simsd_draft_step(const simsd_draft_desc *d, void *stream_ptr) {
@@ -389,9 +585,39 @@ simsd_status simsd_draft_step(const simsd_draft_desc *d, void *stream_ptr) {
   a.per = 0;
   a.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->draft_logits);
   a.ls = scale_of(d->temperature > 0.f ? (double)d->temperature : 1.0);
+  const cudaStream_t stream = (cudaStream_t)stream_ptr;
+  const DraftLayout L = draft_layout(d);
+  if (d->decided == nullptr && d->workspace_bytes >= L.total) {
+    // the chunk pass over every SM, then one CTA per sequence
+    char *ws = (char *)d->workspace;
+    FinishParams f;
+    f.draft = d->draft_logits;
+    f.cu_B = d->cu_B;
+    f.uniforms = d->uniforms;
+    f.part4 = (const float4 *)(ws + L.off_part);
+    f.claim = (int *)(ws + L.off_claim);
+    f.tokens = d->tokens;
+    f.tau = d->tau;
+    f.confidence = d->confidence;
+    f.status = a.status;
+    f.vocab = d->vocab;
+    f.total_B = d->total_B;
+    f.B_max = d->B_max;
+    f.nchunks = L.nchunks;
+    f.chunk = L.chunk;
+    f.bulk = a.bulk;
+    f.ls = a.ls;
+    cudaError_t e = launch_draft_chunks(d, (float4 *)(ws + L.off_part), f.claim, a.status, L.nchunks, stream);
+    if (e == cudaSuccess)
+      e = d->dtype == SIMSD_BF16 ? launch_finish<__nv_bfloat16>(f, d->batch, stream)
+                                 : launch_finish<float>(f, d->batch, stream);
+    return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
+  }
+  // the single cluster kernel (a workspace of only the status word, or
+  // decided slots)
   const cudaError_t e = d->dtype == SIMSD_BF16
-                            ? launch_draft<__nv_bfloat16>(a, d->batch, (cudaStream_t)stream_ptr)
-                            : launch_draft<float>(a, d->batch, (cudaStream_t)stream_ptr);
+                            ? launch_draft<__nv_bfloat16>(a, d->batch, stream)
+                            : launch_draft<float>(a, d->batch, stream);
   return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
 }
 

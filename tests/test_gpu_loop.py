@@ -41,12 +41,17 @@ def softmax64(row):
     return p / p.sum()
 
 
-def draft_on_gpu(w, draft_dev, u, decided=None, tau_prev=None, tokens_prev=None, T=1.0):
+def draft_on_gpu(w, draft_dev, u, decided=None, tau_prev=None, tokens_prev=None, T=1.0,
+                 chunked=False):
+    """chunked: the workspace the library asks for (the chunk pass and one
+    CTA per sequence); else only the status word (the cluster kernel)."""
     n = w.total_B
     tokens = dev_i32(np.zeros(n) if tokens_prev is None else tokens_prev)
     tau = torch.zeros(n, dtype=torch.int32, device="cuda")
     conf = torch.zeros(n, dtype=torch.float32, device="cuda")
-    wsp = ws()
+    wsp = ws() if not chunked else torch.zeros(
+        binding.draft_workspace_size(draft_dev, dev_i32(w.cu_B), w.total_B, w.B_max, T),
+        dtype=torch.uint8, device="cuda")
     binding.draft_step(draft_dev, dev_i32(w.cu_B), torch.from_numpy(u).to("cuda"), tokens, tau,
                        wsp, w.total_B, w.B_max,
                        decided=None if decided is None else dev_i32(decided),
@@ -98,16 +103,17 @@ def check_draft(w, draft_rows64, u, got_tok, got_tau, got_conf, ref, decided=Non
     return tok_ties, ord_ties
 
 
+@pytest.mark.parametrize("path", ["cluster", "chunked"])
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
-def test_draft_step_matches_oracle(cfg):
+def test_draft_step_matches_oracle(cfg, path):
     w = synth.config(cfg)
     u = np.random.default_rng(600 + cfg).random((len(w.lens), w.B_max), dtype=np.float32)
-    st, tok, tau, conf = draft_on_gpu(w, to_device(w.draft, "cuda"), u)
+    st, tok, tau, conf = draft_on_gpu(w, to_device(w.draft, "cuda"), u, chunked=path == "chunked")
     assert st == 0
     d64 = synth.to_f64(w.draft)
     ref = oracle.draft_step(w.cu_B, d64, u)
     ties = check_draft(w, d64, u, tok, tau, conf, ref)
-    print("cfg%d: %d slots, token ties %d, order ties %d" % (cfg, w.total_B, *ties))
+    print("cfg%d %s: %d slots, token ties %d, order ties %d" % (cfg, path, w.total_B, *ties))
     assert ties[0] <= parity.max_ties(w.total_B) and ties[1] <= parity.max_ties(len(w.lens))
 
 
@@ -117,6 +123,23 @@ def loop_spec(**kw):
                 shuffled_pages=True)
     base.update(kw)
     return synth.Spec(**base)
+
+
+@pytest.mark.parametrize("dtype,vocab,T", [("bf16", 1000, 1.0), ("f32", 777, 0.75),
+                                           ("bf16", 151936, 1.0), ("bf16", 4096 + 8, 1.25),
+                                           ("f32", 40000, 1.0), ("bf16", 9, 1.0)])
+def test_draft_step_chunked_mixed_B_and_vocab(dtype, vocab, T):
+    """The chunked path on sections of 1 to 32 slots, vocabularies that end
+    inside a chunk or a part, rows that are not 16-byte multiples (element
+    copies), and temperatures other than 1."""
+    w = synth.make(loop_spec(dtype=dtype, vocab=vocab, batch=12), seed=vocab + 5)
+    u = np.random.default_rng(vocab + 6).random((len(w.lens), w.B_max), dtype=np.float32)
+    st, tok, tau, conf = draft_on_gpu(w, to_device(w.draft, "cuda"), u, T=T, chunked=True)
+    assert st == 0
+    d64 = synth.to_f64(w.draft)
+    ref = oracle.draft_step(w.cu_B, d64, u, temperature=T)
+    ties = check_draft(w, d64, u, tok, tau, conf, ref, T=T)
+    assert ties[0] <= parity.max_ties(w.total_B) and ties[1] <= parity.max_ties(len(w.lens))
 
 
 @pytest.mark.parametrize("dtype,vocab,T", [("bf16", 1000, 1.0), ("f32", 777, 0.75),
