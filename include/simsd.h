@@ -231,25 +231,27 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * Variant rule SIMSD_ACCEPT_GREEDY (the temperature -> 0 limit): step t
  * accepts iff x is the target row's argmax (the smallest index among equal
  * maxima); the first rejection emits that argmax.  It reads neither the
- * draft logits nor the uniforms (they may be NULL), and runs a separate,
- * lighter kernel (one pass over the target rows).
+ * draft logits nor the uniforms (they may be NULL).
  * Variant rule SIMSD_ACCEPT_MATCH (sample matching, Spiffy's verification):
  * step t draws the target's own token y from p (at temperature T) by
  * inverse CDF with u[t-1] and accepts iff y = x; the first rejection emits
- * y (u[B_b] unused, draft logits not read and may be NULL).  A separate
- * kernel: one pass over the target rows, then a scan of one vocabulary
- * slice at a rejection.
- * Kernels (sampling rule): K4a, a pass over (row, 8192-entry chunk) items
- * on every SM, writes each chunk's maximum and sum of exponentials of both
- * rows of every slot, and the logits at the draft tokens, to the
- * workspace; K4b, one thread-block cluster of C CTAs per sequence (C <= 16,
- * chosen at launch from the batch size and the clusters the device can
- * hold at once), each CTA owning 1/C of the vocabulary, merges them, walks
- * the steps, and at a rejection streams the rejected slot's two rows for
- * the residual masses and the inverse-CDF draw.  With a workspace of only
- * the status word, or with `decided` (the blockwise loop: decided slots'
- * rows are not read), the cluster kernel streams the rows itself in one
- * launch instead.
+ * y (u[B_b] unused, draft logits not read and may be NULL).
+ * Kernels: K4a, a chunk pass over (row, 32 KB chunk) items on every SM,
+ * writes per eighth of a chunk (a "part") its maximum and sum of
+ * exponentials -- of both rows of every slot for the sampling rule; of the
+ * target rows and the mass below the draft token for sample matching; the
+ * largest value and its index for the greedy rule -- and the logits at the
+ * draft tokens, to the workspace.  K4b: sampling, one thread-block cluster
+ * of C CTAs per sequence (C <= 16, chosen at launch from the batch size and
+ * the clusters the device can hold at once), each CTA owning 1/C of the
+ * vocabulary, merges the parts, walks the steps, and at a rejection
+ * streams the rejected slot's two rows for the residual masses and the
+ * inverse-CDF draw; greedy and matching, one CTA per sequence merging each
+ * slot's parts (matching: a slot that rejects draws its token from the
+ * part holding u S) and walking the steps.  With a workspace smaller than
+ * simsd_accept_workspace_size, or with `decided` (the blockwise loop:
+ * decided slots' rows are not read), each rule's cluster kernel streams
+ * the rows itself in one launch instead.
  *   target_logits, draft_logits device [total_B][vocab] (dtype); row k of
  *                sequence b (at cu_B[b]+k) holds the logits read at D~_k
  *   draft_tokens device int32[total_B] in [0, vocab); a token outside
@@ -271,10 +273,13 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * a multiple of 16 (and 16-byte aligned logits) are streamed by bulk
  * copies; other vocabularies take a slower element-wise copy.
  * Workspace: simsd_accept_workspace_size returns the size of the
- * two-kernel path (sampling rule: 256 + 2 total_B ceil(vocab/8192) * 8 +
- * 2 total_B * 4 bytes, rounded up to 256-byte multiples; 256 for the other
- * rules); any workspace of at least 256 bytes is accepted, and one smaller
- * than that size runs the single-launch path.
+ * two-kernel path: 256 + R ceil(vocab / E) * 128 + R * 4 bytes, rounded up
+ * to a multiple of 256, with R = 2 total_B rows for the sampling rule and
+ * total_B for the others, and E = 16384 entries (bf16) or 8192 (fp32) per
+ * chunk.  Any workspace of at least 256 bytes is accepted; one smaller
+ * than that size runs the single-launch path.  A wait of the chunk pass
+ * that gives up leaves every sequence of the call with n_accept = 0,
+ * token = -1, pos = -1 (and the timeout bit set).
  * Errors: SIMSD_ERR_NULL, SIMSD_ERR_SHAPE (also: an unknown rule, or a
  * temperature that is negative or not finite), SIMSD_ERR_DTYPE,
  * SIMSD_ERR_WORKSPACE, SIMSD_ERR_CUDA.
@@ -349,9 +354,15 @@ simsd_status simsd_accept_timed(const simsd_accept_desc *d, void *stream,
  *   tau          device int32[total_B] out (may be tau_prev itself)
  *   confidence   device float32[total_B] out or NULL: max_v q(v) of open
  *                slots, -1 at decided ones
- * Kernel: one thread-block cluster per sequence (as simsd_accept's rules):
- * one pass over every open row for its normaliser, then each slot's
- * inverse-CDF scan in the vocabulary slice holding its u*S.
+ * Kernels: with a workspace of simsd_draft_workspace_size bytes and no
+ * decided slots, a chunk pass over (row, 32 KB chunk) items on every SM
+ * (per eighth of a chunk: maximum, sum of exponentials, largest logit),
+ * then one CTA per sequence: a warp per slot merges its row's parts, finds
+ * the part holding u*S and scans it; a wait of the chunk pass that gives
+ * up sets the timeout bit and leaves every tokens and tau entry of the
+ * call unwritten.  Otherwise one thread-block cluster per sequence (as
+ * simsd_accept's rules): one pass over every open row for its normaliser,
+ * then each slot's inverse-CDF scan in the vocabulary slice holding u*S.
  * Errors: as simsd_accept (SIMSD_ERR_SHAPE also for a negative or
  * non-finite temperature).  Bad device arrays (cu_B, decided outside
  * 0..B_b, tau_prev not a permutation) set the bad-input bit and leave the
@@ -372,7 +383,10 @@ typedef struct {
   int32_t *tokens;
   int32_t *tau;
   float *confidence;
-  void *workspace;            /* device, 256-byte aligned (status word)     */
+  void *workspace;            /* device, 256-byte aligned: the status word,
+                                 or simsd_draft_workspace_size bytes (256 +
+                                 total_B ceil(vocab / E) * 128, E as in
+                                 simsd_accept) for the chunked path       */
   size_t workspace_bytes;
 } simsd_draft_desc;
 
@@ -438,11 +452,11 @@ simsd_status simsd_commit(const simsd_commit_desc *d, void *stream);
  * its scratch in a static device array of SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES
  * bytes that every GPU loading the library holds until the process exits.
  *   - It calls no cudaMalloc, cudaFree or allocating library routine.
- *   - It runs the single-launch path, whose scratch is one status word
- *     for every size (the two-kernel path's chunk partials grow with the
- *     batch and take that path only where they fit the array); a scratch
- *     need beyond the array would be rejected with SIMSD_ERR_WORKSPACE
- *     before any launch.
+ *   - It runs the two-kernel path where its chunk partials (which grow
+ *     with total_B and vocab) fit the array, and the single-launch path,
+ *     whose scratch is one status word for every size, otherwise; a
+ *     scratch need beyond the array would be rejected with
+ *     SIMSD_ERR_WORKSPACE before any launch.
  *   - The first call on each device looks up the array's device address
  *     (once per device, with that device current); make that first call
  *     before any stream capture.
@@ -462,7 +476,8 @@ simsd_status simsd_accept_noalloc(const simsd_accept_desc *d, void *stream);
 /* ------------------------------------------------------------------------
  * simsd_read_status -- synchronise `stream`, copy the device status word of
  * a workspace used by simsd_verify_attn / simsd_accept to *word_out (bit 0:
- * a bounded wait ran out) and clear it.  Returns SIMSD_ERR_TIMEOUT when a
+ * a bounded wait ran out) and clear it, together with the chunk pass's
+ * control words (bytes 128..139 of a workspace, zero between calls).  Returns SIMSD_ERR_TIMEOUT when a
  * bit was set, SIMSD_OK otherwise, SIMSD_ERR_CUDA on a CUDA error.
  * ---------------------------------------------------------------------- */
 simsd_status simsd_read_status(void *workspace, void *stream,

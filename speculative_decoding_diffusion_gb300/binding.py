@@ -258,9 +258,11 @@ def _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, tok
 
 
 def accept_workspace_size(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept,
-                          token, pos, total_B, B_max):
+                          token, pos, total_B, B_max, rule=SIMSD_ACCEPT_SAMPLE):
+    """simsd_accept_workspace_size: the two-kernel path's workspace for `rule`
+    (the sampling rule's is the largest of the three)."""
     d = _accept_desc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,
-                     pos, total_B, B_max)
+                     pos, total_B, B_max, rule=rule)
     n = lib().simsd_accept_workspace_size(ctypes.byref(d))
     if n == 0:
         raise SimsdError(2, "simsd_accept_workspace_size")
@@ -280,6 +282,10 @@ def accept(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token, po
     else:
         _check(lib().simsd_accept_timed(ctypes.byref(d), _stream(stream), _events(events, 3)),
                "simsd_accept_timed")
+
+
+# the static scratch of simsd_accept_noalloc (include/simsd.h)
+SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES = 4096
 
 
 def accept_noalloc(target, draft, draft_tokens, tau, cu_B, uniforms, n_accept, token,

@@ -57,7 +57,6 @@ using namespace vocab;
 constexpr int kMaxCluster = 16;                    // CTAs per sequence, at most (over 8: non-portable)
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;          // + the producer warp
 constexpr int kGroupWarps = kConsumerWarps / 2;    // two groups take alternate pieces
 constexpr int kGroupThreads = kGroupWarps * 32;
 constexpr int kStages = 6;
@@ -109,6 +108,7 @@ struct __align__(16) AccSharedT {
   int flag;                                   // any wait of this CTA gave up
   int fail1, fail3;                           // ... in phase 1 / phase 3 (read remotely
                                               // after the barrier closing that phase)
+  int cfail;                                  // partials mode: a chunk-pass wait gave up
 };
 
 struct AcceptParams {
@@ -136,7 +136,7 @@ struct AcceptParams {
   // kernel streams the rows itself.  Slices are then cpc whole chunks.
   const float2 *part;
   const float *xlogit;
-  int *claim;      // the chunk pass's item counter, zeroed here for the next call
+  int *claim;      // the chunk pass's control words (item counter, give-up flag, count)
   int nchunks, cpc;
 };
 
@@ -186,12 +186,18 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     S.flag = 0;
     S.fail1 = 0;
     S.fail3 = 0;
+    S.cfail = 0;
     fence_barrier_init();
   }
   __syncthreads();                           // the ring's barriers are ready
-  if (a.claim != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-    grid_dep_wait();                         // the chunk pass has finished with it
-    *a.claim = 0;
+  // partials mode: the chunk pass's give-up flag, read by a thread with no
+  // loads of its own here (the consumers' barrier below waits for it); the
+  // CTA whose ticket is the last zeroes the chunk pass's words at exit
+  const int flag_t = kConsumers - 1;
+  int ticket = -1;
+  if (a.claim != nullptr && t == flag_t) {
+    grid_dep_wait();                         // the chunk pass has finished
+    S.cfail = chunk_flag_read(a.claim, &ticket);
   }
   if (valid && !producer) {                  // (the producer starts streaming meanwhile)
     if (t < B) {
@@ -445,7 +451,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         // a tau that is not a permutation of 1..B, or a wait in any CTA of
         // the cluster that gave up in phase 1 (the snapshots are final
         // after B1, so every CTA decides alike): no walk
-        bool any_fail = false;                 // (partials mode: phase 1 has no waits)
+        bool any_fail = S.cfail != 0;          // (partials mode: the chunk pass's waits)
         if (!part)
           for (int r = 0; r < a.csize; ++r) any_fail |= ld_dsmem_i32(dsmem(&S.fail1, r)) != 0;
         const bool perm = seen == (B == 32 ? 0xffffffffu : (1u << B) - 1u);
@@ -685,6 +691,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
   if (producer && *(volatile int *)&S.flag)
     for (int j = max(0, issued - kStages); j < issued; ++j)
       (void)mbar_wait_warp(smem_u32(&S.full[j % kStages]), (j / kStages) & 1);
+  if (ticket >= 0) chunk_flag_reset(a.claim, ticket, gridDim.x * gridDim.y);
   cluster_wait();                            // B4: no CTA leaves while others read it
 }
 
@@ -702,6 +709,12 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
 // per-sequence walk and residual draw (K4b, the cluster kernel in partials
 // mode) then read only these partials and the rejected slots' rows.
 
+// candidate (v, i) beats (w, j): a larger value, or an equal one at a
+// smaller index (-inf entries still win over "none", index 2^31 - 1)
+__device__ __forceinline__ bool beats(float v, int i, float w, int j) {
+  return v > w || (v == w && i < j);
+}
+
 struct ChunkParams {
   const void *target;
   const void *draft;
@@ -710,7 +723,8 @@ struct ChunkParams {
   float *xlogit;      // [2 total_B]
   float4 *part4;      // draft rows only: [total_B][nchunks][kAConsumerWarps]: (reference,
                       // sum, the part's largest logit, -)
-  int *claim;         // item counter (zero at launch; the cluster kernel zeroes it again)
+  int *claim;         // [0] item counter, [1] give-up flag, [2] readers' count (zero at
+                      // launch; the kernel reading the partials zeroes them again)
   uint32_t *status;
   int vocab, total_B, nchunks, bulk;
   uint32_t polls;
@@ -724,11 +738,20 @@ __host__ __device__ constexpr int chunk_entries() { return kStageBytes / (int)si
 template <typename T>
 constexpr size_t chunk_smem_bytes() { return (size_t)kAStages * chunk_stage_bytes<T>() + 256; }
 
-// DRAFT: the draft-side step's pass over the draft rows alone (items
-// (row, chunk), no logit at a token, the part's largest logit kept).
-template <typename T, bool DRAFT>
+// Modes: the sampling rule (target and draft rows in pairs; per part
+// (reference, sum); the logit at the slot's draft token); the draft-side
+// step (draft rows; per part (reference, sum, largest logit)); sample
+// matching (target rows; per part (reference, sum, the sum over the
+// entries below the draft token x when x is in the part); the logit at x);
+// the greedy rule (target rows; per part the largest value and its
+// smallest index).
+enum : int { kModeSample = 0, kModeDraft = 1, kModeMatch = 2, kModeGreedy = 3 };
+
+template <typename T, int MODE>
 __global__ void __launch_bounds__(kAThreads)
 vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
+  constexpr bool kPairs = MODE == kModeSample;
+  constexpr bool kToken = MODE == kModeSample || MODE == kModeMatch;
   constexpr int N = Ld<T>::N;
   constexpr int kStage = chunk_stage_bytes<T>();
   constexpr int kChunk = chunk_entries<T>();
@@ -745,7 +768,7 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool producer = warp == kAConsumerWarps;
   grid_dep_launch();                           // the cluster kernel may be scheduled
-  const long items = (DRAFT ? 1L : 2L) * a.total_B * a.nchunks;
+  const long items = (kPairs ? 2L : 1L) * a.total_B * a.nchunks;
   if (t == 0) {
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
@@ -767,7 +790,7 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
     // registers and none is moved while its load is in flight.
     const long grid = gridDim.x, first_dyn = 2L * kAStages * grid;
     auto token_of = [&](long i) {
-      return DRAFT || i < 0 ? 0 : __ldg(a.draft_tokens + (i / a.nchunks >> 1));
+      return !kToken || i < 0 ? 0 : __ldg(a.draft_tokens + (kPairs ? i / a.nchunks >> 1 : i / a.nchunks));
     };
     long it[kAStages], ahead[kAStages];
     int xs[kAStages];
@@ -787,7 +810,7 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
         const long j = j0 + u;
         const int s = u;                            // j % kAStages (j0 is a multiple)
         if (j >= kAStages && !mbar_wait_warp(smem_u32(&empty[s]), ((j / kAStages) - 1) & 1, a.polls)) {
-          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); }
+          if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); atomicOr(a.claim + 1, 1); }
           ok = false;
           break;
         }
@@ -810,9 +833,10 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
           stage_i[s] = (int)i;
         }
         __syncwarp();
-        const T *src = DRAFT ? (const T *)a.draft + p * a.vocab + (long)c * kChunk
-                             : (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab +
-                                   (long)c * kChunk;
+        const T *src = MODE == kModeDraft   ? (const T *)a.draft + p * a.vocab + (long)c * kChunk
+                       : MODE != kModeSample ? (const T *)a.target + p * a.vocab + (long)c * kChunk
+                                             : (const T *)((p & 1) ? a.draft : a.target) +
+                                                   (p >> 1) * a.vocab + (long)c * kChunk;
         copy_piece<T>(smem + s * kStage, ring + s * kStage, src, n, smem_u32(&full[s]), a.bulk, lane);
         issued = j + 1;
         if (lane == 0) {
@@ -832,7 +856,7 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
       // a warp whose wait gave up neither reads nor releases the stage (its
       // copy may still land) and stops; the others are not held up by it
       if (!mbar_wait_warp(smem_u32(&full[s]), (j / kAStages) & 1, a.polls)) {
-        if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); }
+        if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag, 1); atomicOr(a.claim + 1, 1); }
         break;
       }
       const int i = stage_i[s];
@@ -849,7 +873,7 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
         w[v] = idx * N < n ? sv[idx] : Ld<T>::neg_inf();
       }
       // the logit at the slot's draft token, if this warp's part holds it
-      const int off = DRAFT ? -1 : stage_x[s] - c * kChunk;
+      const int off = kToken ? stage_x[s] - c * kChunk : -1;
       if (off >= 0 && off < n && off / N >= v0 && off / N < v0 + kWarpVecs && (off / N - v0) % 32 == lane) {
         const int vx = (off / N - v0) / 32;
         uint4 wx = w[0];
@@ -860,6 +884,34 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      if (MODE == kModeGreedy) {
+        // this warp's part: its largest value (NaN entries never count: the
+        // maxima skip them, and a lane of NaN alone counts as -inf), then
+        // the smallest index holding it -- searched only by the lanes whose
+        // own maximum it is (usually one), vectors in order, entries past
+        // the row excluded
+        float lm = Ld<T>::vmax(w, kV);
+        if (lm != lm) lm = -INFINITY;
+        const uint32_t lu = __float_as_uint(lm);
+        const uint32_t kl = __reduce_max_sync(0xffffffffu, (lu & 0x80000000u) ? ~lu : (lu | 0x80000000u));
+        const float bv = __uint_as_float((kl & 0x80000000u) ? (kl & 0x7fffffffu) : ~kl);
+        uint32_t cand = 0x7fffffffu;
+        if (lm == bv) {
+#pragma unroll
+          for (int v = 0; v < kV; ++v) {
+            float f[N];
+            Ld<T>::unpack(w[v], f);
+            const int base = (v0 + v * 32 + lane) * N;
+#pragma unroll
+            for (int e = 0; e < N; ++e)
+              if (cand == 0x7fffffffu && f[e] == bv && base + e < n) cand = (uint32_t)(c * kChunk + base + e);
+          }
+        }
+        const int bi = (int)__reduce_min_sync(0xffffffffu, cand);
+        if (lane == 0)
+          a.part4[(p * a.nchunks + c) * kAConsumerWarps + warp] = make_float4(bv, __int_as_float(bi), 0.f, 0.f);
+        continue;
+      }
       // this warp's part: its maximum, then its sum against a whole-number
       // reference (combined with the others' by exact powers of two)
       const float mx = Ld<T>::vmax(w, kV);
@@ -867,22 +919,34 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
       const uint32_t km = __reduce_max_sync(0xffffffffu, (mu & 0x80000000u) ? ~mu : (mu | 0x80000000u));
       const float wmax = __uint_as_float((km & 0x80000000u) ? (km & 0x7fffffffu) : ~km);
       const float R = ref_of(wmax, a.ls);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[4] = {0.f, 0.f, 0.f, 0.f}, below = 0.f;
+      // sample matching: the entries below x, where x is in this part
+      const int xo = MODE == kModeMatch ? stage_x[s] - c * kChunk : -1;
+      const bool x_here = MODE == kModeMatch && xo > v0 * N && xo <= (v0 + kWarpVecs) * N;
       if (R != -INFINITY) {
 #pragma unroll
         for (int v = 0; v < kV; ++v) {
           float f[N];
           Ld<T>::unpack(w[v], f);
 #pragma unroll
-          for (int e = 0; e < N; ++e) acc[(v * N + e) & 3] += rel_exp(f[e], R, a.ls);
+          for (int e = 0; e < N; ++e) {
+            const float m = rel_exp(f[e], R, a.ls);
+            acc[(v * N + e) & 3] += m;
+            if (x_here && (v0 + v * 32 + lane) * N + e < xo) below += m;
+          }
         }
       }
       float sm = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      if (x_here)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) below += __shfl_xor_sync(0xffffffffu, below, o);
       if (lane == 0) {
-        if (DRAFT)
+        if (MODE == kModeDraft)
           a.part4[(p * a.nchunks + c) * kAConsumerWarps + warp] = make_float4(R, sm, wmax, 0.f);
+        else if (MODE == kModeMatch)
+          a.part4[(p * a.nchunks + c) * kAConsumerWarps + warp] = make_float4(R, sm, below, 0.f);
         else
           a.part[(p * a.nchunks + c) * kAConsumerWarps + warp] = make_float2(R, sm);
       }
@@ -1023,7 +1087,7 @@ cudaError_t launch(AcceptParams a, cudaStream_t stream) {
 
 // The chunk pass: as many CTAs as the device holds at once (queried once
 // per device and dtype), never more than the items.
-template <typename T, bool DRAFT>
+template <typename T, int MODE>
 cudaError_t launch_chunks(const ChunkParams &c, cudaStream_t stream) {
   static std::mutex mu;
   static int resident[64] = {0};
@@ -1033,22 +1097,194 @@ cudaError_t launch_chunks(const ChunkParams &c, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (resident[dev] == 0) {
-      cudaError_t e = cudaFuncSetAttribute(vocab_chunk_kernel<T, DRAFT>,
+      cudaError_t e = cudaFuncSetAttribute(vocab_chunk_kernel<T, MODE>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)chunk_smem_bytes<T>());
       if (e != cudaSuccess) return e;
       int n = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, vocab_chunk_kernel<T, DRAFT>, kAThreads,
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, vocab_chunk_kernel<T, MODE>, kAThreads,
                                                         chunk_smem_bytes<T>());
       if (e != cudaSuccess) return e;
       resident[dev] = n > 0 ? n : 1;
     }
     per_sm = resident[dev];
   }
-  const long items = (DRAFT ? 1L : 2L) * c.total_B * c.nchunks;
+  const long items = (MODE == kModeSample ? 2L : 1L) * c.total_B * c.nchunks;
   const long grid = std::min<long>(items, (long)per_sm * device_sm_count());
-  vocab_chunk_kernel<T, DRAFT><<<(unsigned)grid, kAThreads, chunk_smem_bytes<T>(), stream>>>(c);
+  vocab_chunk_kernel<T, MODE><<<(unsigned)grid, kAThreads, chunk_smem_bytes<T>(), stream>>>(c);
   return cudaGetLastError();
+}
+
+// ------------------------------------------------ greedy and matching finish
+// After a greedy or matching chunk pass over the target rows: one CTA per
+// sequence, a warp per slot.  Greedy: the row's argmax from the parts'
+// candidates (largest value, smallest index); the step accepts iff the
+// draft token is it, and a rejection emits it.  Matching: the row's
+// reference M and normaliser S, the mass below the draft token x, Pre(x) =
+// the parts before x's part plus the part's own mass below x, and x's mass
+// m(x); with U = u S the step accepts iff Pre(x) <= U < Pre(x) + m(x).  A
+// slot that rejects draws the target's own token at U at once (part_draw:
+// the part holding U, then a column scan), so the walk -- warp 0, over
+// every slot's verdict -- only picks the first rejected step's result.
+constexpr int kRuleThreads = 512;
+constexpr int kRuleWarps = kRuleThreads / 32;
+
+struct RuleFinishParams {
+  const void *target;
+  const int32_t *draft_tokens;
+  const int32_t *tau;
+  const int32_t *cu_B;
+  const float *uniforms;
+  const float4 *part4;      // [total_B][nchunks][kAConsumerWarps]
+  const float *xlogit;      // [total_B] (matching)
+  int *claim;               // the chunk pass's control words
+  int32_t *n_accept;
+  int32_t *token;
+  int32_t *pos;
+  uint32_t *status;
+  int vocab, total_B, B_max, nchunks, bulk;
+  Scale ls;
+};
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kRuleThreads)
+rule_finish_kernel(const __grid_constant__ RuleFinishParams a) {
+  static_assert(MODE == kModeGreedy || MODE == kModeMatch, "the greedy and matching rules");
+  constexpr int kChunk = chunk_entries<T>();
+  constexpr int kPartLen = kChunk / kAConsumerWarps;   // entries of a part
+  constexpr int kHeld = 4;                             // parts held per lane: 4 x 32
+  __shared__ int acc_s[kMaxB], tok_s[kMaxB];
+  __shared__ int fail_s;
+  const int b = blockIdx.x, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  grid_dep_wait();                                     // the chunk pass's partials
+  // the chunk pass's give-up flag, read by the last thread (checked at the
+  // walk); the CTA whose ticket is the last zeroes the chunk pass's words
+  const int flag_t = kRuleThreads - 1;
+  int ticket = -1;
+  if (t == flag_t) fail_s = chunk_flag_read(a.claim, &ticket);
+  const int c0 = __ldg(a.cu_B + b), B = __ldg(a.cu_B + b + 1) - c0;
+  const bool valid = B >= 1 && B <= a.B_max && c0 >= 0 && c0 + B <= a.total_B;
+  if (!valid) {                                        // malformed sequence: no walk
+    if (t == 0) {
+      a.n_accept[b] = 0;
+      a.token[b] = -1;
+      a.pos[b] = -1;
+      raise_status(a.status, kStatusBadInput);
+    }
+    if (t == flag_t) chunk_flag_reset(a.claim, ticket, gridDim.x);
+    return;
+  }
+  const Scale ls = a.ls;
+  const int n_ent = a.nchunks * kAConsumerWarps;       // parts of a row
+  for (int k = warp; k < B; k += kRuleWarps) {
+    const float4 *pr = a.part4 + (long)(c0 + k) * n_ent;
+    const int x = __ldg(a.draft_tokens + c0 + k);
+    const bool xin = x >= 0 && x < a.vocab;
+    float4 h[kHeld];
+#pragma unroll
+    for (int i = 0; i < kHeld; ++i)
+      h[i] = lane + 32 * i < n_ent ? __ldcg(pr + lane + 32 * i)
+                                   : make_float4(-INFINITY, MODE == kModeGreedy ? __int_as_float(0x7fffffff) : 0.f, 0.f, 0.f);
+    if (MODE == kModeGreedy) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      auto take = [&](float4 v) {
+        if (beats(v.x, __float_as_int(v.y), bv, bi)) { bv = v.x; bi = __float_as_int(v.y); }
+      };
+#pragma unroll
+      for (int i = 0; i < kHeld; ++i) take(h[i]);
+      for (int i = lane + 32 * kHeld; i < n_ent; i += 32) take(__ldcg(pr + i));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (lane == 0) {
+        const int am = bi == 0x7fffffff ? 0 : bi;   // no entry beat "none": a NaN row
+        acc_s[k] = xin && x == am;
+        tok_s[k] = am;
+      }
+    } else {
+      float M = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kHeld; ++i) M = fmaxf(M, h[i].x);
+      for (int i = lane + 32 * kHeld; i < n_ent; i += 32) M = fmaxf(M, __ldcg(pr + i).x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      // S and Pre(x), in units of 2^M, as compensated pairs
+      const int px = xin ? x / kPartLen : -1;        // x's part (parts are in vocabulary order)
+      Ff S = ff_of(0.f), Pre = ff_of(0.f);
+      auto add = [&](int i, float4 v) {
+        const float w = (M != -INFINITY && v.x != -INFINITY) ? exp2_int(v.x - M) : 0.f;
+        const float m = v.y > 0.f ? v.y * w : 0.f;
+        S = ff_add(S, ff_of(m));
+        if (i < px) Pre = ff_add(Pre, ff_of(m));
+        else if (i == px && v.z > 0.f) Pre = ff_add(Pre, ff_of(v.z * w));
+      };
+#pragma unroll
+      for (int i = 0; i < kHeld; ++i) add(lane + 32 * i, h[i]);
+      for (int i = lane + 32 * kHeld; i < n_ent; i += 32) add(i, __ldcg(pr + i));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        S = ff_add(S, ff_shfl_xor(S, o));
+        Pre = ff_add(Pre, ff_shfl_xor(Pre, o));
+      }
+      const int st = __ldg(a.tau + c0 + k);
+      const float u = st >= 1 && st <= B ? __ldg(a.uniforms + (long)b * (a.B_max + 1) + st - 1) : 0.f;
+      const float uh = u * S.hi;
+      const Ff U = ff_add(Ff{uh, fmaf(u, S.hi, -uh)}, ff_of(u * S.lo));
+      const float mx = xin ? rel_exp(__ldcg(a.xlogit + c0 + k), M, ls) : 0.f;   // m(x)
+      const bool acc = mx > 0.f && !ff_gt(Pre, U) && ff_gt(ff_add(Pre, ff_of(mx)), U);
+      int y = -1;
+      if (!acc)                                      // warp-uniform: the target's own token at U
+        y = part_draw<T, kHeld>(pr, h, n_ent, M, U, (const T *)a.target + (long)(c0 + k) * a.vocab,
+                                a.vocab, kChunk, a.bulk != 0, ls, lane);
+      if (lane == 0) {
+        acc_s[k] = acc;
+        tok_s[k] = y;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // the walk: the first rejected step over a permutation of 1..B
+    const int tk = lane < B ? __ldg(a.tau + c0 + lane) : 0;
+    const int x = lane < B ? __ldg(a.draft_tokens + c0 + lane) : 0;
+    const uint32_t seen = __reduce_or_sync(0xffffffffu, lane < B && tk >= 1 && tk <= B ? 1u << (tk - 1) : 0u);
+    const bool perm = seen == (B == 32 ? 0xffffffffu : (1u << B) - 1u);
+    const bool rejects = lane < B && !acc_s[lane];
+    const uint32_t rstep = __reduce_min_sync(0xffffffffu, rejects ? (uint32_t)tk : 0xffffffffu);
+    const int last = rstep == 0xffffffffu ? B : (int)rstep;   // the walk's last step
+    const bool badx = lane < B && tk <= last && (x < 0 || x >= a.vocab);
+    const bool fail = fail_s != 0;
+    const bool any_bad = __any_sync(0xffffffffu, badx);
+    const unsigned rl = __ballot_sync(0xffffffffu, rejects && (uint32_t)tk == rstep);
+    if (lane == 0) {
+      if (!perm) raise_status(a.status, kStatusBadInput);
+      else if (!fail && any_bad) raise_status(a.status, kStatusBadInput);
+      if (!perm || fail) {                            // no walk
+        a.n_accept[b] = 0;
+        a.token[b] = -1;
+        a.pos[b] = -1;
+      } else if (rstep == 0xffffffffu) {              // every step accepted
+        a.n_accept[b] = B;
+        a.token[b] = -1;
+        a.pos[b] = -1;
+      } else {
+        const int k = __ffs(rl) - 1;
+        a.n_accept[b] = (int)rstep - 1;
+        a.token[b] = tok_s[k];
+        a.pos[b] = k;
+      }
+    }
+  }
+  if (t == flag_t) chunk_flag_reset(a.claim, ticket, gridDim.x);
+}
+
+template <typename T, int MODE>
+cudaError_t launch_rule_finish(const RuleFinishParams &f, int batch, cudaStream_t stream) {
+  return launch_pdl(rule_finish_kernel<T, MODE>, dim3(batch), dim3(kRuleThreads), 0, stream, f);
 }
 
 // ---------------------------------------------------------------- greedy
@@ -1075,11 +1311,6 @@ struct GreedyParams {
   int vocab, total_B, B_max, csize, per, bulk;
 };
 
-// candidate (v, i) beats (w, j): a larger value, or an equal one at a
-// smaller index (-inf entries still win over "none", index 2^31 - 1)
-__device__ __forceinline__ bool beats(float v, int i, float w, int j) {
-  return v > w || (v == w && i < j);
-}
 
 template <typename T>
 __global__ void __launch_bounds__(kGreedyThreads)
@@ -1518,11 +1749,14 @@ bool accept_pointers_ok(const simsd_accept_desc *d) {
          d->token && d->pos && (!draft || d->draft_logits) && (!uni || d->uniforms);
 }
 
-// Workspace: the status word; for the sampling rule's two-kernel path also
-// the chunk partials [2 total_B][nchunks] (float2) and the draft-token logits
-// [2 total_B] (float).  A workspace of just the status word runs the single
-// cluster kernel (the rows streamed per sequence), as do walks from decided
-// steps (that kernel skips the decided slots' rows).
+// Workspace: the status word; for the chunked paths also the chunk pass's
+// control words (beside the status word), the chunk partials and the
+// draft-token logits.
+// Sampling: partials [2 total_B][nchunks][8] (float2), logits [2 total_B];
+// greedy and matching: partials [total_B][nchunks][8] (float4), logits
+// [total_B].  A workspace of just the status word runs the single cluster
+// kernel of the rule (the rows streamed per sequence), as do walks from
+// decided steps (those kernels skip the decided slots' rows).
 constexpr size_t kAcceptWorkspace = kAlign;
 struct AcceptLayout {
   int nchunks;
@@ -1531,17 +1765,17 @@ struct AcceptLayout {
 AcceptLayout accept_layout(const simsd_accept_desc *d) {
   AcceptLayout L;
   const int chunk = kStageBytes / (d->dtype == SIMSD_BF16 ? 2 : 4);
+  const bool pairs = d->rule == SIMSD_ACCEPT_SAMPLE;
+  const size_t rows = (size_t)(pairs ? 2 : 1) * d->total_B;
   L.nchunks = (d->vocab + chunk - 1) / chunk;
+  L.off_claim = kClaimOffset;                 // beside the status word
   L.off_part = kAcceptWorkspace;
-  L.off_xlogit = align_up(L.off_part + (size_t)2 * d->total_B * L.nchunks * kAConsumerWarps *
-                                           sizeof(float2), kAlign);
-  L.off_claim = align_up(L.off_xlogit + (size_t)2 * d->total_B * sizeof(float), kAlign);
-  L.total = L.off_claim + kAlign;
+  L.off_xlogit = align_up(L.off_part + rows * L.nchunks * kAConsumerWarps *
+                                           (pairs ? sizeof(float2) : sizeof(float4)), kAlign);
+  L.total = align_up(L.off_xlogit + rows * sizeof(float), kAlign);
   return L;
 }
-size_t accept_workspace(const simsd_accept_desc *d) {
-  return d->rule == SIMSD_ACCEPT_SAMPLE ? accept_layout(d).total : kAcceptWorkspace;
-}
+size_t accept_workspace(const simsd_accept_desc *d) { return accept_layout(d).total; }
 
 // Scratch of simsd_accept_noalloc: one static array per device, alive until
 // the process exits.  Host code may not take its address directly (the
@@ -1550,6 +1784,8 @@ size_t accept_workspace(const simsd_accept_desc *d) {
 constexpr int kMaxDevices = 64;
 static_assert(SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES % kAlign == 0, "scratch size");
 static_assert(SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES >= kAcceptWorkspace, "scratch size");
+static_assert(kClaimOffset >= sizeof(uint32_t) && kClaimOffset + kClaimBytes <= kAcceptWorkspace,
+              "the control words sit beside the status word");
 static __device__ __align__(256) unsigned char g_accept_scratch[SIMSD_ACCEPT_NOALLOC_SCRATCH_BYTES];
 
 cudaError_t static_scratch(char **out) {
@@ -1575,6 +1811,60 @@ cudaError_t static_scratch(char **out) {
 simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
                         cudaStream_t stream, void *const *events) {
   const int es = d->dtype == SIMSD_BF16 ? 2 : 4;
+  const AcceptLayout L = accept_layout(d);
+  const bool chunked = d->decided == nullptr && ws_bytes >= L.total;
+  const bool bf16 = d->dtype == SIMSD_BF16;
+  if (d->rule != SIMSD_ACCEPT_SAMPLE && chunked) {
+    // the chunk pass over the target rows on every SM, then one CTA per sequence
+    const bool greedy = d->rule == SIMSD_ACCEPT_GREEDY;
+    ChunkParams c;
+    c.target = d->target_logits;
+    c.draft = nullptr;
+    c.draft_tokens = d->draft_tokens;
+    c.part = nullptr;
+    c.xlogit = (float *)(ws + L.off_xlogit);
+    c.part4 = (float4 *)(ws + L.off_part);
+    c.claim = (int *)(ws + L.off_claim);
+    c.status = (uint32_t *)ws;
+    c.vocab = d->vocab;
+    c.total_B = d->total_B;
+    c.nchunks = L.nchunks;
+    c.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits);
+    c.polls = wait_polls_of(d->wait_polls);
+    c.ls = scale_of(d->temperature > 0.f ? (double)d->temperature : 1.0);
+    RuleFinishParams f;
+    f.target = d->target_logits;
+    f.draft_tokens = d->draft_tokens;
+    f.tau = d->tau;
+    f.cu_B = d->cu_B;
+    f.uniforms = d->uniforms;
+    f.part4 = c.part4;
+    f.xlogit = c.xlogit;
+    f.claim = c.claim;
+    f.n_accept = d->n_accept;
+    f.token = d->token;
+    f.pos = d->pos;
+    f.status = c.status;
+    f.vocab = d->vocab;
+    f.total_B = d->total_B;
+    f.B_max = d->B_max;
+    f.nchunks = L.nchunks;
+    f.bulk = c.bulk;
+    f.ls = c.ls;
+    mark(events, 0, stream);
+    cudaError_t e = greedy ? (bf16 ? launch_chunks<__nv_bfloat16, kModeGreedy>(c, stream)
+                                   : launch_chunks<float, kModeGreedy>(c, stream))
+                           : (bf16 ? launch_chunks<__nv_bfloat16, kModeMatch>(c, stream)
+                                   : launch_chunks<float, kModeMatch>(c, stream));
+    mark(events, 1, stream);
+    if (e == cudaSuccess)
+      e = greedy ? (bf16 ? launch_rule_finish<__nv_bfloat16, kModeGreedy>(f, d->batch, stream)
+                         : launch_rule_finish<float, kModeGreedy>(f, d->batch, stream))
+                 : (bf16 ? launch_rule_finish<__nv_bfloat16, kModeMatch>(f, d->batch, stream)
+                         : launch_rule_finish<float, kModeMatch>(f, d->batch, stream));
+    mark(events, 2, stream);
+    return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
+  }
   if (d->rule == SIMSD_ACCEPT_GREEDY) {
     GreedyParams g;
     g.target = d->target_logits;
@@ -1593,8 +1883,8 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     g.per = 0;
     g.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits);
     mark(events, 0, stream);
-    const cudaError_t e = d->dtype == SIMSD_BF16 ? launch_greedy<__nv_bfloat16>(g, d->batch, stream)
-                                                 : launch_greedy<float>(g, d->batch, stream);
+    const cudaError_t e = bf16 ? launch_greedy<__nv_bfloat16>(g, d->batch, stream)
+                               : launch_greedy<float>(g, d->batch, stream);
     mark(events, 1, stream);
     mark(events, 2, stream);
     return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
@@ -1619,8 +1909,8 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     m.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits);
     m.ls = scale_of(d->temperature > 0.f ? (double)d->temperature : 1.0);
     mark(events, 0, stream);
-    const cudaError_t e = d->dtype == SIMSD_BF16 ? launch_match<__nv_bfloat16>(m, d->batch, stream)
-                                                 : launch_match<float>(m, d->batch, stream);
+    const cudaError_t e = bf16 ? launch_match<__nv_bfloat16>(m, d->batch, stream)
+                               : launch_match<float>(m, d->batch, stream);
     mark(events, 1, stream);
     mark(events, 2, stream);
     return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
@@ -1655,11 +1945,9 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
   a.claim = nullptr;
   a.nchunks = 0;
   a.cpc = 0;
-  const AcceptLayout L = accept_layout(d);
-  const bool two_pass = d->decided == nullptr && ws_bytes >= L.total;
   mark(events, 0, stream);
   cudaError_t e = cudaSuccess;
-  if (two_pass) {
+  if (chunked) {
     ChunkParams c;
     c.target = d->target_logits;
     c.draft = d->draft_logits;
@@ -1675,8 +1963,8 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     c.bulk = a.bulk;
     c.polls = a.polls;
     c.ls = a.ls;
-    e = d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16, false>(c, stream)
-                                 : launch_chunks<float, false>(c, stream);
+    e = d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16, kModeSample>(c, stream)
+                                 : launch_chunks<float, kModeSample>(c, stream);
     a.part = c.part;
     a.xlogit = c.xlogit;
     a.claim = c.claim;
@@ -1711,8 +1999,8 @@ cudaError_t launch_draft_chunks(const simsd_draft_desc *d, float4 *part4, int *c
   c.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->draft_logits);
   c.polls = kWaitPolls;
   c.ls = scale_of(d->temperature > 0.f ? (double)d->temperature : 1.0);
-  return d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16, true>(c, stream)
-                                : launch_chunks<float, true>(c, stream);
+  return d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16, kModeDraft>(c, stream)
+                                : launch_chunks<float, kModeDraft>(c, stream);
 }
 
 }  // namespace simsd

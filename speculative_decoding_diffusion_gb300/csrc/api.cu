@@ -391,7 +391,9 @@ simsd_status simsd_read_status(void *workspace, void *stream_ptr, uint32_t *word
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SIMSD_ERR_CUDA;
   if (cudaMemcpy(&w, workspace, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess)
     return SIMSD_ERR_CUDA;
-  if (cudaMemset(workspace, 0, sizeof(w)) != cudaSuccess) return SIMSD_ERR_CUDA;
+  if (cudaMemset(workspace, 0, sizeof(w)) != cudaSuccess ||
+      cudaMemset((char *)workspace + kClaimOffset, 0, kClaimBytes) != cudaSuccess)
+    return SIMSD_ERR_CUDA;
   if (word_out) *word_out = w;
   return w ? SIMSD_ERR_TIMEOUT : SIMSD_OK;
 }

@@ -19,6 +19,13 @@ constexpr size_t kMaxRowBytes = 192 * 1024;   // raw q + k + v of one new token 
 
 inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 constexpr size_t kAlign = 256;
+// The first kAlign bytes of every workspace: the status word at offset 0
+// and, for the chunked acceptance and draft paths, the chunk pass's three
+// control words at this fixed offset (the same place for every size, so a
+// workspace reused at another size never finds partials there);
+// simsd_read_status clears both.
+constexpr size_t kClaimOffset = 128;
+constexpr size_t kClaimBytes = 3 * sizeof(int);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -142,7 +149,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // The draft-side step's chunk pass over the draft rows (accept.cu): per
 // (row, 32 KB chunk, consumer warp) the reference, the sum of 2^(l ls -
 // reference) and the part's largest logit, into part4 [total_B][nchunks][8].
-// *claim must be zero; the finishing kernel zeroes it again.
+// claim[0..2] must be zero; the finishing kernel zeroes them again.
 int draft_chunk_entries(int esize);
 cudaError_t launch_draft_chunks(const simsd_draft_desc *d, float4 *part4, int *claim,
                                 uint32_t *status, int nchunks, cudaStream_t stream);

@@ -301,7 +301,7 @@ struct FinishParams {
   const int32_t *cu_B;
   const float *uniforms;
   const float4 *part4;      // [total_B][nchunks][kParts]
-  int *claim;               // the chunk pass's item counter, zeroed here
+  int *claim;               // the chunk pass's control words, zeroed here
   int32_t *tokens;
   int32_t *tau;
   float *confidence;
@@ -313,21 +313,26 @@ struct FinishParams {
 template <typename T>
 __global__ void __launch_bounds__(kFinishThreads)
 draft_finish_kernel(const __grid_constant__ FinishParams a) {
-  constexpr int N = Ld<T>::N;
   __shared__ float conf_s[kMaxB];
   const int b = blockIdx.x, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  __shared__ int tok_s[kMaxB];
+  __shared__ int fail_s;
   grid_dep_wait();                                  // the chunk pass's partials
-  if (b == 0 && t == 0) *a.claim = 0;               // ready for the next call
+  // the chunk pass's give-up flag, read by the last thread (checked before
+  // any output is written); the CTA whose ticket is the last zeroes the
+  // chunk pass's words
+  const int flag_t = kFinishThreads - 1;
+  int ticket = -1;
+  if (t == flag_t) fail_s = chunk_flag_read(a.claim, &ticket);
   const int c0 = __ldg(a.cu_B + b), B = __ldg(a.cu_B + b + 1) - c0;
   const bool valid = B >= 1 && B <= a.B_max && c0 >= 0 && c0 + B <= a.total_B;
-  if (!valid) {
+  if (!valid) {                                     // tokens and tau are left unwritten
     if (t == 0) raise_status(a.status, kStatusBadInput);
+    if (t == flag_t) chunk_flag_reset(a.claim, ticket, gridDim.x);
     return;
   }
   const Scale ls = a.ls;
   const int n_ent = a.nchunks * kParts;             // parts of a row
-  const int part_len = a.chunk / kParts;            // entries of a part
-  const int part_vecs = part_len / N;
   for (int k = warp; k < B; k += kFinishWarps) {
     const float4 *pr = a.part4 + (long)(c0 + k) * n_ent;
     // the row: M, S, largest logit (the first 4 x 32 parts held)
@@ -362,100 +367,29 @@ draft_finish_kernel(const __grid_constant__ FinishParams a) {
     const float u = __ldg(a.uniforms + (long)b * a.B_max + k);
     const float uh = u * S.hi;
     const Ff U = ff_add(Ff{uh, fmaf(u, S.hi, -uh)}, ff_of(u * S.lo));
-    // the part holding U: groups of 32 parts in vocabulary order
-    Ff base = ff_of(0.f), last_start = ff_of(0.f);
-    int sel = -1, last_nz = 0;
-    auto group = [&](int g0, float4 v) {              // parts g0 .. g0 + 31
-      const Ff m = ff_of(g0 + lane < n_ent ? mass_of(v) : 0.f);
-      Ff inc = m;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const Ff y = ff_shfl_up(inc, d);
-        if (lane >= d) inc = ff_add(y, inc);
-      }
-      const Ff run = ff_add(base, inc);
-      const Ff start = ff_add(base, ff_add(inc, ff_neg(m)));
-      const unsigned cross = __ballot_sync(0xffffffffu, m.hi > 0.f && ff_gt(run, U));
-      const unsigned nz = __ballot_sync(0xffffffffu, m.hi > 0.f);
-      if (cross) {
-        const int l = __ffs(cross) - 1;
-        sel = g0 + l;
-        base = ff_shfl(start, l);
-      } else {
-        if (nz) {
-          const int l = 31 - __clz(nz);
-          last_nz = g0 + l;
-          last_start = ff_shfl(start, l);
-        }
-        base = ff_shfl(run, 31);
-      }
-    };
-#pragma unroll
-    for (int i = 0; i < kHeld; ++i)
-      if (sel < 0 && 32 * i < n_ent) group(32 * i, h[i]);
-    for (int g0 = 32 * kHeld; g0 < n_ent && sel < 0; g0 += 32)
-      group(g0, g0 + lane < n_ent ? __ldcg(pr + g0 + lane) : make_float4(-INFINITY, 0.f, 0.f, 0.f));
-    if (sel < 0) {
-      sel = last_nz;
-      base = last_start;
-    }
-    // the entry: the part's vectors, 32 per column, in vocabulary order
-    const int p0 = (sel / kParts) * a.chunk + (sel % kParts) * part_len;
-    const int n = min(part_len, a.vocab - p0);
-    const T *row = (const T *)a.draft + (long)(c0 + k) * a.vocab + p0;
-    const Ff D0 = ff_add(U, ff_neg(base));
-    const float dd = D0.hi + D0.lo;
-    float col_base = 0.f;
-    int first = 0x7fffffff, last_pos = -1;
-#pragma unroll 1
-    for (int c = 0; c * 32 < part_vecs && first == 0x7fffffff; ++c) {
-      const int e0 = (c * 32 + lane) * N;
-      float f[N], m[N];
-      Ld<T>::unpack(Ld<T>::load(row + e0, n - e0, a.bulk != 0), f);
-      float lane_mass = 0.f;
-#pragma unroll
-      for (int e = 0; e < N; ++e) {
-        m[e] = rel_exp(f[e], M, ls);
-        lane_mass += m[e];
-        if (m[e] > 0.f) last_pos = p0 + e0 + e;
-      }
-      float inc = lane_mass;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc += y;
-      }
-      const float prev = __shfl_up_sync(0xffffffffu, inc, 1);
-      const float start = col_base + (lane ? prev : 0.f);
-      if (dd < col_base + inc) {
-        float run = 0.f;
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-          run += m[e];
-          if (first == 0x7fffffff && m[e] > 0.f && start + run > dd) first = p0 + e0 + e;
-        }
-      }
-      first = __reduce_min_sync(0xffffffffu, first);
-      col_base += __shfl_sync(0xffffffffu, inc, 31);
-    }
-    last_pos = __reduce_max_sync(0xffffffffu, last_pos);
+    const int tok = part_draw<T, kHeld>(pr, h, n_ent, M, U, (const T *)a.draft + (long)(c0 + k) * a.vocab,
+                                        a.vocab, a.chunk, a.bulk != 0, ls, lane);
     if (lane == 0) {
-      a.tokens[c0 + k] = first != 0x7fffffff ? first : last_pos;
+      tok_s[k] = tok;
       // the row's largest probability, in the kernel's own arithmetic
       conf_s[k] = rel_exp(xm, M, ls) / (S.hi + S.lo);
     }
   }
   __syncthreads();
-  if (t < B) {                                      // largest first, equal ones in position order
+  // a chunk pass whose wait gave up (its status bit is set): tokens and
+  // tau are left unwritten
+  if (t < B && !fail_s) {                           // largest first, equal ones in position order
     const float ck = conf_s[t];
     int before = 0;
     for (int j = 0; j < B; ++j) {
       const float cj = conf_s[j];
       if (cj > ck || (cj == ck && j < t)) ++before;
     }
+    a.tokens[c0 + t] = tok_s[t];
     a.tau[c0 + t] = 1 + before;
     if (a.confidence) a.confidence[c0 + t] = ck;
   }
+  if (t == flag_t) chunk_flag_reset(a.claim, ticket, gridDim.x);
 }
 
 template <typename T>
@@ -541,7 +475,8 @@ using namespace simsd;
 
 extern "C" {
 
-// The chunked path's workspace: status | chunk partials | item counter.
+// The chunked path's workspace: status word and the chunk pass's control
+// words | chunk partials.
 struct DraftLayout {
   int nchunks, chunk;
   size_t off_part, off_claim, total;
@@ -550,9 +485,9 @@ DraftLayout draft_layout(const simsd_draft_desc *d) {
   DraftLayout L;
   L.chunk = draft_chunk_entries(d->dtype == SIMSD_BF16 ? 2 : 4);
   L.nchunks = (d->vocab + L.chunk - 1) / L.chunk;
+  L.off_claim = kClaimOffset;                 // beside the status word
   L.off_part = kStatusWorkspace;
-  L.off_claim = align_up(L.off_part + (size_t)d->total_B * L.nchunks * kParts * sizeof(float4), kAlign);
-  L.total = L.off_claim + kAlign;
+  L.total = align_up(L.off_part + (size_t)d->total_B * L.nchunks * kParts * sizeof(float4), kAlign);
   return L;
 }
 

@@ -278,5 +278,141 @@ static __device__ __noinline__ int warp_pick(Ff m, Ff base, Ff U, Ff *start) {
   return ch;
 }
 
+// ------------------------------------------------------------ part draws
+// Inverse-CDF draw from one row after a chunk pass: the pass left, per part
+// (1/8 of a 32 KB chunk, contiguous in the vocabulary; parts in (chunk,
+// part) order are in vocabulary order), the part's reference (.x) and sum
+// of 2^(l ls - reference) (.y).  M is the row's reference and U the draw
+// point, both in units of 2^M.  Lane l holds parts l + 32 i (i < HELD) in
+// h; the rest are read from pr.  The part whose running mass first exceeds
+// U (else the last with mass), then that part column by column in
+// vocabulary order (an fp32 scan relative to its start): the first entry
+// whose running mass exceeds U, else the last entry with mass.  All 32
+// lanes call it; every lane gets the token.
+template <typename T, int HELD>
+__device__ int part_draw(const float4 *pr, const float4 (&h)[HELD], int n_ent, float M, Ff U,
+                         const T *row, int vocab, int chunk, bool bulk, Scale ls, int lane) {
+  constexpr int N = Ld<T>::N;
+  constexpr int kParts = 8;
+  const int part_len = chunk / kParts, part_vecs = part_len / N;
+  auto mass_of = [&](float4 v) {
+    const float w = (M != -INFINITY && v.x != -INFINITY) ? exp2_int(v.x - M) : 0.f;
+    return v.y > 0.f ? v.y * w : 0.f;
+  };
+  Ff base = ff_of(0.f), last_start = ff_of(0.f);
+  int sel = -1, last_nz = 0;
+  auto group = [&](int g0, float4 v) {              // parts g0 .. g0 + 31
+    const Ff m = ff_of(g0 + lane < n_ent ? mass_of(v) : 0.f);
+    Ff inc = m;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const Ff y = ff_shfl_up(inc, d);
+      if (lane >= d) inc = ff_add(y, inc);
+    }
+    const Ff run = ff_add(base, inc);
+    const Ff start = ff_add(base, ff_add(inc, ff_neg(m)));
+    const unsigned cross = __ballot_sync(0xffffffffu, m.hi > 0.f && ff_gt(run, U));
+    const unsigned nz = __ballot_sync(0xffffffffu, m.hi > 0.f);
+    if (cross) {
+      const int l = __ffs(cross) - 1;
+      sel = g0 + l;
+      base = ff_shfl(start, l);
+    } else {
+      if (nz) {
+        const int l = 31 - __clz(nz);
+        last_nz = g0 + l;
+        last_start = ff_shfl(start, l);
+      }
+      base = ff_shfl(run, 31);
+    }
+  };
+#pragma unroll
+  for (int i = 0; i < HELD; ++i)
+    if (sel < 0 && 32 * i < n_ent) group(32 * i, h[i]);
+  for (int g0 = 32 * HELD; g0 < n_ent && sel < 0; g0 += 32)
+    group(g0, g0 + lane < n_ent ? __ldcg(pr + g0 + lane) : make_float4(-INFINITY, 0.f, 0.f, 0.f));
+  if (sel < 0) {
+    sel = last_nz;
+    base = last_start;
+  }
+  const int p0 = (sel / kParts) * chunk + (sel % kParts) * part_len;
+  const int n = min(part_len, vocab - p0);
+  const T *src = row + p0;
+  const Ff D0 = ff_add(U, ff_neg(base));
+  const float dd = D0.hi + D0.lo;
+  float col_base = 0.f;
+  int first = 0x7fffffff, last_pos = -1;
+  // kBatch columns of 32 vectors per round, their loads issued together
+  // (a part of a 32 KB chunk is 8 columns: one round)
+  constexpr int kBatch = 8;
+#pragma unroll 1
+  for (int c0 = 0; c0 * 32 < part_vecs && first == 0x7fffffff; c0 += kBatch) {
+    uint4 w[kBatch];
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c) {
+      const int e0 = ((c0 + c) * 32 + lane) * N;
+      w[c] = (c0 + c) * 32 < part_vecs ? Ld<T>::load(src + e0, n - e0, bulk) : Ld<T>::neg_inf();
+    }
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c) {
+      if (first != 0x7fffffff || (c0 + c) * 32 >= part_vecs) break;   // warp-uniform
+      const int e0 = ((c0 + c) * 32 + lane) * N;
+      float f[N], m[N];
+      Ld<T>::unpack(w[c], f);
+      float lane_mass = 0.f;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        m[e] = rel_exp(f[e], M, ls);
+        lane_mass += m[e];
+        if (m[e] > 0.f) last_pos = p0 + e0 + e;
+      }
+      float inc = lane_mass;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += y;
+      }
+      const float prev = __shfl_up_sync(0xffffffffu, inc, 1);
+      const float start = col_base + (lane ? prev : 0.f);
+      if (dd < col_base + inc) {
+        float run = 0.f;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          run += m[e];
+          if (first == 0x7fffffff && m[e] > 0.f && start + run > dd) first = p0 + e0 + e;
+        }
+      }
+      first = __reduce_min_sync(0xffffffffu, first);
+      col_base += __shfl_sync(0xffffffffu, inc, 31);
+    }
+  }
+  last_pos = __reduce_max_sync(0xffffffffu, last_pos);
+  return first != 0x7fffffff ? first : last_pos;
+}
+
+// ------------------------------------------------- chunk pass control words
+// claim[0]: the chunk pass's item counter; claim[1]: set when one of its
+// waits gave up (its partials are then incomplete); claim[2]: how many CTAs
+// of the kernel reading the partials have read claim[1].  One thread per
+// CTA calls chunk_flag_read after grid_dep_wait (the chunk pass has
+// finished, its writes visible): it returns claim[1] and the CTA's ticket
+// (its place in the count).  The CTA whose ticket is the last calls
+// chunk_flag_reset before it exits -- every CTA has read the flag by then
+// -- so the next call starts from zeros.  The ticket is compared only at
+// the end, so the atomic's round trip overlaps the CTA's work.
+__device__ __forceinline__ int chunk_flag_read(int *claim, int *ticket) {
+  const int fail = *(volatile int *)(claim + 1);
+  __threadfence();                               // the read precedes the count
+  *ticket = atomicAdd(claim + 2, 1);
+  return fail;
+}
+__device__ __forceinline__ void chunk_flag_reset(int *claim, int ticket, int ctas) {
+  if (ticket != ctas - 1) return;
+  __threadfence();
+  claim[0] = 0;
+  claim[1] = 0;
+  claim[2] = 0;
+}
+
 }  // namespace vocab
 }  // namespace simsd

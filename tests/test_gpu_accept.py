@@ -211,14 +211,25 @@ def test_walk_distribution_monte_carlo():
 
 
 # ------------------------------------------------------------------ variants
-def run_rule(w, rule, temperature=1.0):
+# The greedy and matching rules have two paths too: a chunk pass over the
+# target rows then one CTA per sequence (the full workspace), or one cluster
+# per sequence streaming its rows (a workspace of just the status word).
+RULE_PATHS = ["chunked", "cluster"]
+
+
+def rule_workspace(dw, path):
+    return dw.accept_ws if path == "chunked" else torch.zeros(256, dtype=torch.uint8, device="cuda")
+
+
+def run_rule(w, rule, temperature=1.0, path="chunked"):
     dw = DeviceWorkload(w, with_verify=False)
+    ws = rule_workspace(dw, path)
     greedy = rule == binding.SIMSD_ACCEPT_GREEDY
     binding.accept(dw.target, None if greedy else dw.draft, dw.draft_tokens, dw.tau, dw.cu_B,
                    None if greedy else dw.uniforms, dw.n_accept, dw.token, dw.pos,
-                   dw.accept_ws, dw.total_B, dw.B_max, rule=rule, temperature=temperature)
+                   ws, dw.total_B, dw.B_max, rule=rule, temperature=temperature)
     torch.cuda.synchronize()
-    assert binding.read_status(dw.accept_ws) == 0
+    assert binding.read_status(ws) == 0
     return (dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy())
 
 
@@ -230,8 +241,9 @@ def variant_case(name):
     return synth.make(tiny_accept_spec(batch=batch, dtype=dtype, vocab=vocab), seed=vocab + batch)
 
 
+@pytest.mark.parametrize("path", RULE_PATHS)
 @pytest.mark.parametrize("name", ["sdar8b", "bf16-1003", "f32-777", "bf16-few", "f32-odd"])
-def test_greedy_matches_oracle(name):
+def test_greedy_matches_oracle(name, path):
     """The greedy rule: accepted lengths, positions and tokens bit-exact
     against the oracle (argmax over the same bf16 / fp32 values, the
     smallest index among equal maxima).  70% of the draft tokens are made the
@@ -240,7 +252,7 @@ def test_greedy_matches_oracle(name):
     a = synth.to_f64(w.target).argmax(1).astype(np.int32)
     rng = np.random.default_rng(7)
     w.draft_tokens = np.where(rng.random(len(a)) < 0.7, a, w.draft_tokens).astype(np.int32)
-    n, tok, pos = run_rule(w, binding.SIMSD_ACCEPT_GREEDY)
+    n, tok, pos = run_rule(w, binding.SIMSD_ACCEPT_GREEDY, path=path)
     ref = oracle.accept_greedy(w.cu_B, synth.to_f64(w.target), w.draft_tokens, w.tau)
     np.testing.assert_array_equal(n, ref["n_accept"])
     np.testing.assert_array_equal(pos, ref["pos"])
@@ -296,9 +308,10 @@ def check_match(w, n, tok, pos, temperature=1.0, tie=parity.TIE_RESIDUAL):
     return ties
 
 
+@pytest.mark.parametrize("path", RULE_PATHS)
 @pytest.mark.parametrize("name,T", [("sdar8b", 1.0), ("bf16-1003", 1.0), ("f32-777", 0.875),
                                     ("bf16-few", 1.0), ("f32-odd", 1.25)])
-def test_sample_matching_matches_oracle(name, T):
+def test_sample_matching_matches_oracle(name, T, path):
     """Sample matching (accept iff the target's own inverse-CDF sample at
     u[t-1] equals the draft token; the rejection emits that sample): exact
     against the oracle outside the tie zone.  Half of the draft tokens are
@@ -314,14 +327,8 @@ def test_sample_matching_matches_oracle(name, T):
                 p = np.exp(tl[s0 + k] - tl[s0 + k].max()); p /= p.sum()
                 y = int(np.searchsorted(np.cumsum(p), float(w.uniforms[b, t]), side="right"))
                 w.draft_tokens[s0 + k] = min(y, w.spec.vocab - 1)
-    dw = DeviceWorkload(w, with_verify=False)
-    binding.accept(dw.target, None, dw.draft_tokens, dw.tau, dw.cu_B, dw.uniforms, dw.n_accept,
-                   dw.token, dw.pos, dw.accept_ws, dw.total_B, dw.B_max,
-                   rule=binding.SIMSD_ACCEPT_MATCH, temperature=T)
-    torch.cuda.synchronize()
-    assert binding.read_status(dw.accept_ws) == 0
-    n, tok, pos = dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy()
+    n, tok, pos = run_rule(w, binding.SIMSD_ACCEPT_MATCH, T, path)
     ties = check_match(w, n, tok, pos, T)
-    print("%s T=%g: %d sequences, %d with a tie-zone draw" % (name, T, len(w.lens), ties))
+    print("%s T=%g %s: %d sequences, %d with a tie-zone draw" % (name, T, path, len(w.lens), ties))
     assert ties <= parity.max_ties(len(w.lens))
     assert (n > 0).any()

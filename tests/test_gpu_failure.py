@@ -33,15 +33,22 @@ def accept_spec(**kw):
     return synth.Spec(**base)
 
 
-def run_rule(dw, rule, cu_B_dev, tau_dev, total_B, B_max):
+# every rule has a chunked path (the full workspace) and a single-launch
+# cluster path (a workspace of the status word alone)
+PATHS = ["chunked", "cluster"]
+
+
+def run_rule(dw, rule, cu_B_dev, tau_dev, total_B, B_max, path="chunked", wait_polls=0):
     for t in (dw.n_accept, dw.token, dw.pos):
         t.fill_(-7)
+    ws = dw.accept_ws if path == "chunked" else torch.zeros(256, dtype=torch.uint8, device="cuda")
     greedy = rule == binding.SIMSD_ACCEPT_GREEDY
     binding.accept(dw.target, None if rule != binding.SIMSD_ACCEPT_SAMPLE else dw.draft,
                    dw.draft_tokens, tau_dev, cu_B_dev, None if greedy else dw.uniforms,
-                   dw.n_accept, dw.token, dw.pos, dw.accept_ws, total_B, B_max, rule=rule)
+                   dw.n_accept, dw.token, dw.pos, ws, total_B, B_max, rule=rule,
+                   wait_polls=wait_polls)
     torch.cuda.synchronize()
-    st = binding.read_status(dw.accept_ws)
+    st = binding.read_status(ws)
     return st, dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy()
 
 
@@ -52,15 +59,16 @@ def big_accept_workload():
     return w, dw
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("rule", [binding.SIMSD_ACCEPT_SAMPLE, binding.SIMSD_ACCEPT_GREEDY,
                                   binding.SIMSD_ACCEPT_MATCH])
-def test_accept_cu_B_beyond_descriptor(rule):
+def test_accept_cu_B_beyond_descriptor(rule, path):
     w, dw = big_accept_workload()
     # the descriptor says 3 sequences, total_B 12, B_max 4; the device cu_B
     # gives sequence 1 a section of 6 (> B_max) and sequence 2 rows 10..13
     # (past total_B); only sequence 0 is well formed
     cu = torch.tensor([0, 4, 10, 14], dtype=torch.int32, device="cuda")
-    st, n, tok, pos = run_rule(dw, rule, cu, dw.tau, 12, 4)
+    st, n, tok, pos = run_rule(dw, rule, cu, dw.tau, 12, 4, path)
     assert st & BAD_INPUT
     for b in (1, 2):
         assert (n[b], tok[b], pos[b]) == (0, -1, -1), (b, n[b], tok[b], pos[b])
@@ -73,15 +81,16 @@ def test_accept_cu_B_beyond_descriptor(rule):
         assert 0 <= n[0] <= 4
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("rule", [binding.SIMSD_ACCEPT_SAMPLE, binding.SIMSD_ACCEPT_GREEDY,
                                   binding.SIMSD_ACCEPT_MATCH])
-def test_accept_tau_not_a_permutation(rule):
+def test_accept_tau_not_a_permutation(rule, path):
     w, dw = big_accept_workload()
     tau = w.tau.copy()
     tau[4:8] = [1, 1, 2, 3]                  # sequence 1: label 4 missing, 1 twice
     tau[8:12] = [1, 2, 3, 5]                 # sequence 2: a label outside 1..4
     tau_dev = torch.from_numpy(tau).to("cuda")
-    st, n, tok, pos = run_rule(dw, rule, dw.cu_B, tau_dev, w.total_B, w.B_max)
+    st, n, tok, pos = run_rule(dw, rule, dw.cu_B, tau_dev, w.total_B, w.B_max, path)
     assert st & BAD_INPUT
     for b in (1, 2):
         assert (n[b], tok[b], pos[b]) == (0, -1, -1), (b, n[b], tok[b], pos[b])
@@ -89,7 +98,8 @@ def test_accept_tau_not_a_permutation(rule):
         assert 0 <= n[b] <= 4 and (pos[b] == -1) == (n[b] == 4)
 
 
-def test_greedy_rows_without_a_larger_entry_give_index_zero():
+@pytest.mark.parametrize("path", PATHS)
+def test_greedy_rows_without_a_larger_entry_give_index_zero(path):
     """A target row of -inf everywhere (or NaN everywhere) has no entry
     larger than another: the argmax is index 0, as in the oracle."""
     w = synth.make(accept_spec(batch=2, dtype="f32", vocab=1000), seed=5)
@@ -99,7 +109,7 @@ def test_greedy_rows_without_a_larger_entry_give_index_zero():
     w.target[int(w.cu_B[0]) + int(np.argsort(w.tau[:4])[0])] = np.nan
     w.draft_tokens[:] = 5                    # not index 0: both first steps reject
     dw = DeviceWorkload(w, with_verify=False)
-    st, n, tok, pos = run_rule(dw, binding.SIMSD_ACCEPT_GREEDY, dw.cu_B, dw.tau, w.total_B, 4)
+    st, n, tok, pos = run_rule(dw, binding.SIMSD_ACCEPT_GREEDY, dw.cu_B, dw.tau, w.total_B, 4, path)
     assert st == 0
     ref = oracle.accept_greedy(w.cu_B, synth.to_f64(w.target), w.draft_tokens, w.tau)
     np.testing.assert_array_equal(n, ref["n_accept"])
@@ -174,3 +184,27 @@ def test_accept_wait_that_gives_up_returns_a_status():
     assert binding.read_status(dw.accept_ws) == 0
     n, tok, pos = dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy()
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
+
+
+@pytest.mark.parametrize("rule", [binding.SIMSD_ACCEPT_GREEDY, binding.SIMSD_ACCEPT_MATCH,
+                                  binding.SIMSD_ACCEPT_SAMPLE])
+def test_chunk_pass_that_gives_up_means_no_walk(rule):
+    """The chunked path with every wait giving up at once: the chunk pass
+    raises its give-up flag, so the kernel after it reports "no walk" for
+    every sequence (whatever stale partials the workspace holds) and sets
+    the timeout bit; it puts the chunk pass's control words back to zero, so
+    the next call on the same workspace is correct."""
+    w = synth.make(accept_spec(batch=6, B=(1, 3, 4), vocab=40000), seed=17)
+    dw = DeviceWorkload(w, with_verify=False)
+    # a correct call first leaves real partials in the workspace
+    st, n0, tok0, pos0 = run_rule(dw, rule, dw.cu_B, dw.tau, w.total_B, w.B_max)
+    assert st == 0
+    st, n, tok, pos = run_rule(dw, rule, dw.cu_B, dw.tau, w.total_B, w.B_max, wait_polls=-1)
+    assert st & TIMEOUT, st
+    assert (n == 0).all() and (tok == -1).all() and (pos == -1).all(), (n, tok, pos)
+    for _ in range(2):
+        st, n, tok, pos = run_rule(dw, rule, dw.cu_B, dw.tau, w.total_B, w.B_max)
+        assert st == 0
+        np.testing.assert_array_equal(n, n0)
+        np.testing.assert_array_equal(tok, tok0)
+        np.testing.assert_array_equal(pos, pos0)
