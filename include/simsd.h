@@ -241,17 +241,17 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * exponentials -- of both rows of every slot for the sampling rule; of the
  * target rows and the mass below the draft token for sample matching; the
  * largest value and its index for the greedy rule -- and the logits at the
- * draft tokens, to the workspace.  K4b: sampling, one thread-block cluster
- * of C CTAs per sequence (C <= 16, chosen at launch from the batch size and
- * the clusters the device can hold at once), each CTA owning 1/C of the
- * vocabulary, merges the parts, walks the steps, and at a rejection
- * streams the rejected slot's two rows for the residual masses and the
- * inverse-CDF draw; greedy and matching, one CTA per sequence merging each
- * slot's parts (matching: a slot that rejects draws its token from the
- * part holding u S) and walking the steps.  With a workspace smaller than
- * simsd_accept_workspace_size, or with `decided` (the blockwise loop:
- * decided slots' rows are not read), each rule's cluster kernel streams
- * the rows itself in one launch instead.
+ * draft tokens, to the workspace.  K4b: sampling, up to two CTAs per SM
+ * over the batch, each owning a range of a sequence's chunks: every CTA of
+ * a sequence merges its slots' parts and walks the steps alike, computes
+ * the residual masses of its chunks of the rejected slot's two rows, and
+ * the last CTA of the sequence draws from them; greedy and matching, one
+ * CTA per sequence merging each slot's parts (matching: a slot that
+ * rejects draws its token from the part holding u S) and walking the
+ * steps.  With a workspace smaller than simsd_accept_workspace_size, or
+ * with `decided` (the blockwise loop: decided slots' rows are not read),
+ * each rule's thread-block cluster kernel (C <= 16 CTAs per sequence, each
+ * owning 1/C of the vocabulary) streams the rows itself in one launch.
  *   target_logits, draft_logits device [total_B][vocab] (dtype); row k of
  *                sequence b (at cu_B[b]+k) holds the logits read at D~_k
  *   draft_tokens device int32[total_B] in [0, vocab); a token outside
@@ -273,10 +273,11 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * a multiple of 16 (and 16-byte aligned logits) are streamed by bulk
  * copies; other vocabularies take a slower element-wise copy.
  * Workspace: simsd_accept_workspace_size returns the size of the
- * two-kernel path: 256 + R ceil(vocab / E) * 128 + R * 4 bytes, rounded up
- * to a multiple of 256, with R = 2 total_B rows for the sampling rule and
- * total_B for the others, and E = 16384 entries (bf16) or 8192 (fp32) per
- * chunk.  Any workspace of at least 256 bytes is accepted; one smaller
+ * two-kernel path, with C = ceil(vocab / E) chunks of E = 16384 entries
+ * (bf16) or 8192 (fp32) and each term rounded up to a multiple of 256:
+ * sampling, 256 + 2 total_B C * 64 + 2 total_B * 4 + batch * 4 +
+ * batch C * 256 bytes; greedy and matching, 256 + total_B C * 128 +
+ * total_B * 4.  Any workspace of at least 256 bytes is accepted; one smaller
  * than that size runs the single-launch path.  A wait of the chunk pass
  * that gives up leaves every sequence of the call with n_accept = 0,
  * token = -1, pos = -1 (and the timeout bit set).

@@ -7,18 +7,25 @@
 // q = softmax(draft row k / T) at temperature T (1 by default); accept iff
 // u[t-1] * q(x) < p(x) (fp32).  At the first rejection a token is drawn
 // from max(0, p - q) normalised (p itself when that is empty) by inverse
-// CDF with u[B].  The greedy rule and sample matching have their own,
-// simpler kernels at the end of this file.
+// CDF with u[B].  The greedy rule and sample matching (Spiffy's
+// verification) share the machinery below.
 //
-// One launch; one thread-block cluster of C CTAs per sequence (C <= 16, from
-// a makespan estimate over the resident-cluster waves: 8-16 for small
-// batches, 1-2 for large ones), CTA r owning the vocabulary slice
-// [r * per, (r + 1) * per) of every row of the sequence.  Each CTA streams
-// its slices of the 2B rows (target and draft of every slot) in pieces of
-// equal size (at most 32 KB) through a 6-stage shared-memory ring filled by
-// bulk copies (one producer warp); two groups of 8 consumer warps take
-// alternate pieces, so one group's waits and reductions overlap the other's
-// exponentials:
+// Two paths.  The chunked path (a workspace of simsd_accept_workspace_size
+// bytes, no decided steps) runs K4a, the chunk pass: every SM streams
+// (row, 32 KB chunk) items through a bulk-copy ring and writes, per eighth
+// of a chunk (a "part"), what the rule needs (reference and sum of
+// exponentials; the largest value and its index; the mass below the draft
+// token), plus the logits at the draft tokens.  K4b then finishes from
+// those partials -- for sampling, CTAs per (sequence, chunk range) that
+// each repeat the sequence's walk, compute their chunks' residual masses and
+// let the last of them draw; for greedy and matching, a CTA per sequence.
+// The single-launch path (a workspace of just the status word, or decided
+// steps) is one thread-block cluster of C CTAs per sequence (C <= 16, from
+// a makespan estimate over the resident-cluster waves), CTA r owning the
+// vocabulary slice [r * per, (r + 1) * per) of every row of the sequence;
+// it streams its slices of the 2B rows in pieces of at most 32 KB through a
+// 6-stage shared-memory ring (one producer warp, two groups of 8 consumer
+// warps taking alternate pieces):
 //   1. per (slot, row): maximum and sum of exponentials of the slice;
 //   2. cluster barrier; every CTA merges the C slices' partials through
 //      distributed shared memory, evaluates p(x), q(x) and walks the steps
@@ -28,19 +35,16 @@
 //      contiguous vocabulary ranges of each piece;
 //   4. cluster barrier; every CTA reads the C slice totals, so all agree on
 //      the CTA whose slice holds u * S; one warp of that CTA narrows down to
-//      the piece, then the range (warp scans of the stored masses), then
-//      rereads that range (64 B of each row per lane; from the ring when the
-//      piece is still there) and finds the entry by a warp scan in
-//      vocabulary order.
-// No global atomics, no partial results in global memory, no second launch.
+//      the piece, then the range, then rereads that range and finds the
+//      entry by a warp scan in vocabulary order.
 // Numerics: a partial state is (R, s) with R a reference in log2 units (the
 // maximum of x log2 e seen so far, rounded once) and s = sum 2^(x log2 e - R),
 // each exponent argument formed by one fma (a single rounding, small for
 // the entries near the maximum that carry the mass) and exponentiated by
-// the MUFU ex2 instruction.  Normalisers, masses and running CDFs are
-// compensated fp32 pairs (two-sum), never fp64 (GB300's fp64 rate is a
-// small fraction of its fp32 rate).  The residual CDF is then within ~1e-6
-// (absolute probability mass) of the exact one.
+// the MUFU ex2 instruction.  Normalisers, masses and running CDFs across
+// parts are compensated fp32 pairs (two-sum), never fp64 (GB300's fp64
+// rate is a small fraction of its fp32 rate); within a part or range the
+// running mass is fp32 relative to its start.
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -108,7 +112,6 @@ struct __align__(16) AccSharedT {
   int flag;                                   // any wait of this CTA gave up
   int fail1, fail3;                           // ... in phase 1 / phase 3 (read remotely
                                               // after the barrier closing that phase)
-  int cfail;                                  // partials mode: a chunk-pass wait gave up
 };
 
 struct AcceptParams {
@@ -130,33 +133,20 @@ struct AcceptParams {
   int piece;   // entries per ring stage
   int bulk;    // rows 16-byte aligned: bulk copies; else element copies
   Scale ls;    // log2(e) / temperature
-  // partials mode (the two-kernel path): the per-chunk (reference, sum) of
-  // every row, [2 total_B][nchunks], and each row's logit at its slot's
-  // draft token, [2 total_B] (both written by the chunk pass); NULL: this
-  // kernel streams the rows itself.  Slices are then cpc whole chunks.
-  const float2 *part;
-  const float *xlogit;
-  int *claim;      // the chunk pass's control words (item counter, give-up flag, count)
-  int nchunks, cpc;
 };
 
-// Two instances: NW = 16 consumer warps with a 6-stage ring (one CTA per
-// SM: the single-launch path, which streams every row itself), and NW = 8
-// with 3 stages (two CTAs per SM: partials mode, where only the rejected
-// slots' rows stream, so twice the sequences are resident at once).
+// NW consumer warps (two groups) and an NS-stage ring: one CTA per SM.
 template <typename T, int NW, int NS>
-__global__ void __launch_bounds__((NW + 1) * 32, NW == 8 ? 2 : 1)
+__global__ void __launch_bounds__((NW + 1) * 32, 1)
 accept_kernel(const __grid_constant__ AcceptParams a) {
   constexpr int N = Ld<T>::N;
   constexpr int kConsumerWarps = NW, kConsumers = NW * 32, kStages = NS;
   constexpr int kGroupWarps = NW / 2, kGroupThreads = kGroupWarps * 32;
-  constexpr int kVecs = kStageBytes / 16 / kGroupThreads;   // phase 1 (NW = 16 only)
-  constexpr bool kPartialsOnly = NW != 16;
+  constexpr int kVecs = kStageBytes / 16 / kGroupThreads;   // phase 1
   constexpr int kRangesPerWarp = kRanges / NW;
   static_assert(kRangesPerWarp * NW == kRanges, "whole ranges per warp");
   using AccShared = AccSharedT<NW>;
   auto consumers_sync = [] { named_sync(1, kConsumers); };
-  const bool part = kPartialsOnly || a.part != nullptr;   // partials mode
   extern __shared__ __align__(128) uint8_t smem[];
   AccShared &S = *reinterpret_cast<AccShared *>(smem + kStages * kStageBytes);
   const uint32_t ring = smem_u32(smem);
@@ -186,30 +176,15 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
     S.flag = 0;
     S.fail1 = 0;
     S.fail3 = 0;
-    S.cfail = 0;
     fence_barrier_init();
   }
   __syncthreads();                           // the ring's barriers are ready
-  // partials mode: the chunk pass's give-up flag, read by a thread with no
-  // loads of its own here (the consumers' barrier below waits for it); the
-  // CTA whose ticket is the last zeroes the chunk pass's words at exit
-  const int flag_t = kConsumers - 1;
-  int ticket = -1;
-  if (a.claim != nullptr && t == flag_t) {
-    grid_dep_wait();                         // the chunk pass has finished
-    S.cfail = chunk_flag_read(a.claim, &ticket);
-  }
   if (valid && !producer) {                  // (the producer starts streaming meanwhile)
     if (t < B) {
       S.tau[t] = __ldg(a.tau + c0 + t);
       S.x[t] = __ldg(a.draft_tokens + c0 + t);
     }
-    // partials mode: launched while the chunk pass finishes (programmatic
-    // dependent launch); its results are read only after this wait
-    if (part) grid_dep_wait();
-    if (t < B)
-      S.xv[t] = part ? make_float2(a.xlogit[2 * (c0 + t)], a.xlogit[2 * (c0 + t) + 1])
-                       : make_float2(0.f, 0.f);
+    if (t < B) S.xv[t] = make_float2(0.f, 0.f);
     if (t <= B) S.u[t] = __ldg(a.uniforms + (long)b * (a.B_max + 1) + t);
     consumers_sync();                        // the sequence's labels, tokens, uniforms
   }
@@ -233,8 +208,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
   int g = 0;                                 // stage counter (producer and consumers)
   if (valid) {
     // ---------------------------------------------------- 1. row slices
-    // (in partials mode the chunk pass did this: nothing is streamed)
-    const int J = part ? 0 : 2 * n_open * npieces;
+    const int J = 2 * n_open * npieces;
     if (producer) {
       for (int pair = 0, pc = 0; g < J; ++g) {
         const int s = g % kStages;
@@ -338,7 +312,7 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         }
       }
       consumers_sync();
-      if (t < 2 * n_open && !part) {       // this CTA's slice of open pair t
+      if (t < 2 * n_open) {                // this CTA's slice of open pair t
         float2 c = make_float2(-INFINITY, 0.f);
         if (npieces > 0 && !*(volatile int *)&S.flag) {
           float M = -INFINITY;
@@ -355,57 +329,13 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         S.cpart[t] = c;
       }
     }
-    if (!part) cluster_sync();             // B1: every slice's partials are in place
+    cluster_sync();                        // B1: every slice's partials are in place
 
     // ---------------------------------------------------- 2. the walk
     // every CTA merges the slices' partials and walks the steps itself (the
     // same inputs in the same order give the same decisions everywhere), so
     // no barrier is needed before the residual pass; CTA 0 writes outputs
-    if (!producer && part) {
-      // partials mode: every CTA merges all of every open row's chunk
-      // partials itself (warp w: open pairs w, w + 16, ...; lanes stride
-      // over the row's chunks x the chunk pass's warps), so no cluster
-      // barrier and no exchange come before the walk
-      const int per_row = a.nchunks * kAConsumerWarps;
-      for (int q = warp; q < 2 * n_open; q += kConsumerWarps) {
-        const int k = slot_of(q >> 1), row = q & 1, x = S.x[k];
-        const float2 *pr_ = a.part + (long)(2 * (c0 + k) + row) * per_row;
-        // the first 4 partials of each lane stay in registers: one round
-        // trip for both the maximum and the sum (vocabularies up to 16
-        // chunks); the rest are read twice
-        constexpr int kHeld = 4;
-        float2 held[kHeld];
-#pragma unroll
-        for (int i = 0; i < kHeld; ++i)
-          held[i] = lane + 32 * i < per_row ? __ldg(pr_ + lane + 32 * i) : make_float2(-INFINITY, 0.f);
-        float M = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kHeld; ++i) M = fmaxf(M, held[i].x);
-        for (int i = lane + 32 * kHeld; i < per_row; i += 32) M = fmaxf(M, __ldg(&pr_[i].x));
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-        Ff sm = ff_of(0.f);
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int i = 0; i < kHeld; ++i)
-            if (held[i].y > 0.f) sm = ff_add(sm, ff_of(held[i].y * exp2_int(held[i].x - M)));
-          for (int i = lane + 32 * kHeld; i < per_row; i += 32) {
-            const float2 v = __ldg(pr_ + i);
-            if (v.y > 0.f) sm = ff_add(sm, ff_of(v.y * exp2_int(v.x - M)));
-          }
-        }
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) sm = ff_add(sm, ff_shfl_xor(sm, m));
-        if (lane == 0) {
-          S.norm[2 * k + row] = make_float4(M, sm.hi, sm.lo, 0.f);
-          // p(x) (row 0) or q(x) (row 1); a token outside the vocabulary rejects
-          const bool xin = x >= 0 && x < a.vocab;
-          const float pr = xin ? rel_exp(row ? S.xv[k].y : S.xv[k].x, M, ls) / (sm.hi + sm.lo) : 0.f;
-          if (row) S.qx[k] = pr; else S.px[k] = pr;
-          if (!xin && row == 0 && rank == 0) raise_status(a.status, kStatusBadInput);
-        }
-      }
-    } else if (!producer) {
+    if (!producer) {
       // thread (pair q, slice r) reads one slice's partial; groups of gs
       // lanes (8, or 16 for clusters over 8) merge them (pair q: slot q / 2,
       // row q % 2)
@@ -451,9 +381,8 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
         // a tau that is not a permutation of 1..B, or a wait in any CTA of
         // the cluster that gave up in phase 1 (the snapshots are final
         // after B1, so every CTA decides alike): no walk
-        bool any_fail = S.cfail != 0;          // (partials mode: the chunk pass's waits)
-        if (!part)
-          for (int r = 0; r < a.csize; ++r) any_fail |= ld_dsmem_i32(dsmem(&S.fail1, r)) != 0;
+        bool any_fail = false;
+        for (int r = 0; r < a.csize; ++r) any_fail |= ld_dsmem_i32(dsmem(&S.fail1, r)) != 0;
         const bool perm = seen == (B == 32 ? 0xffffffffu : (1u << B) - 1u);
         int n = B, rej = -1;
         if (!perm || any_fail) {
@@ -691,7 +620,6 @@ accept_kernel(const __grid_constant__ AcceptParams a) {
   if (producer && *(volatile int *)&S.flag)
     for (int j = max(0, issued - kStages); j < issued; ++j)
       (void)mbar_wait_warp(smem_u32(&S.full[j % kStages]), (j / kStages) & 1);
-  if (ticket >= 0) chunk_flag_reset(a.claim, ticket, gridDim.x * gridDim.y);
   cluster_wait();                            // B4: no CTA leaves while others read it
 }
 
@@ -725,6 +653,8 @@ struct ChunkParams {
                       // sum, the part's largest logit, -)
   int *claim;         // [0] item counter, [1] give-up flag, [2] readers' count (zero at
                       // launch; the kernel reading the partials zeroes them again)
+  int *zero;          // n_zero ints the pass zeroes for the kernel after it (or NULL)
+  int n_zero;
   uint32_t *status;
   int vocab, total_B, nchunks, bulk;
   uint32_t polls;
@@ -767,8 +697,11 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   const uint32_t ring = smem_u32(smem);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool producer = warp == kAConsumerWarps;
-  grid_dep_launch();                           // the cluster kernel may be scheduled
+  grid_dep_launch();                           // the kernel after it may be scheduled
   const long items = (kPairs ? 2L : 1L) * a.total_B * a.nchunks;
+  if (a.zero != nullptr)                       // counters the kernel after it starts from
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero; i += gridDim.x * blockDim.x)
+      a.zero[i] = 0;
   if (t == 0) {
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
@@ -963,25 +896,22 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   }
 }
 
-// The two instances of the cluster kernel: consumer warps, ring stages,
-// threads and shared memory.
+// The cluster kernel's instance: consumer warps, ring stages, threads and
+// shared memory.
 template <int NW, int NS>
 struct AccCfg {
   static constexpr int kNW = NW, kNS = NS, kThreadsPerCta = (NW + 1) * 32;
   static constexpr size_t kSmem = (size_t)NS * kStageBytes + sizeof(AccSharedT<NW>);
 };
-using CfgSingle = AccCfg<kConsumerWarps, kStages>;   // streams every row itself
-using CfgPartials = AccCfg<8, 3>;                    // partials mode, two CTAs per SM
+using CfgSingle = AccCfg<kConsumerWarps, kStages>;
 static_assert(CfgSingle::kSmem <= 227 * 1024, "shared memory budget");
-static_assert(2 * (CfgPartials::kSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
 void mark(void *const *events, int i, cudaStream_t stream) {
   if (events != nullptr) record_event(events[i], stream);
 }
 
 template <typename C>
-cudaLaunchConfig_t launch_config(int csize, int batch, cudaStream_t stream,
-                                 cudaLaunchAttribute *attr, bool after_chunks = false) {
+cudaLaunchConfig_t launch_config(int csize, int batch, cudaStream_t stream, cudaLaunchAttribute *attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(csize, batch);
   cfg.blockDim = dim3(C::kThreadsPerCta);
@@ -991,12 +921,8 @@ cudaLaunchConfig_t launch_config(int csize, int batch, cudaStream_t stream,
   attr[0].val.clusterDim.x = csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  // after the chunk pass: programmatic dependent launch (the kernel waits
-  // for the chunk pass's results on the device)
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = after_chunks ? 2 : 1;
+  cfg.numAttrs = 1;
   return cfg;
 }
 
@@ -1019,7 +945,7 @@ cudaError_t max_active_clusters(int dev, int csize, int *out) {
     cache[dev][0] = 1;
   }
   if (cache[dev][csize] == 0) {
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     const cudaLaunchConfig_t cfg = launch_config<C>(csize, csize, nullptr, attr);
     int n = 0;
     cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
@@ -1043,18 +969,16 @@ cudaError_t launch_cfg(AcceptParams a, cudaStream_t stream) {
   // whole streaming loop fewer) plus the fixed cost of the walk, residual
   // and draw phases.  Small batches get large clusters (every SM busy),
   // large batches small ones (fewer waves).  Never so small that a slice
-  // needs more pieces than the kernel tracks.  In partials mode only the
-  // residual pass of the rejected slot's two rows streams.
+  // needs more pieces than the kernel tracks.
   const int vec = 16 / (int)sizeof(T);
   const int piece = kStageBytes / (int)sizeof(T);
   const int64_t max_slice = (int64_t)kMaxPieces * piece;
-  const double per_seq = (a.part ? 2.0 : 2.0 * a.total_B / a.batch + 2.0) * a.vocab;   // exponentials
+  const double per_seq = (2.0 * a.total_B / a.batch + 2.0) * a.vocab;   // exponentials
   constexpr double kPhaseCycles = 20000.0;
   int csize = kMaxCluster;
   double best = 1e300;
   for (int c = kMaxCluster; c >= 1; --c) {
     if (((int64_t)a.vocab + c - 1) / c > max_slice) break;
-    if (a.part && c > a.nchunks) continue;   // every CTA's slice holds a chunk
     int n = 0;
     cudaError_t e = max_active_clusters<T, C>(dev, c, &n);
     if (e != cudaSuccess) return e;
@@ -1064,25 +988,18 @@ cudaError_t launch_cfg(AcceptParams a, cudaStream_t stream) {
     if (cost < best * (1.0 - 1e-9)) { best = cost; csize = c; }
   }
   a.csize = csize;
-  if (a.part) {
-    // slices of whole chunks: the chunk pass's items are the pieces
-    a.cpc = (a.nchunks + csize - 1) / csize;
-    a.per = a.cpc * piece;
-    a.piece = piece;
-  } else {
-    a.per = ((a.vocab + csize - 1) / csize + vec - 1) / vec * vec;
-    // pieces of equal size (whole vectors, at most one stage) per slice
-    const int np = (a.per + piece - 1) / piece;
-    a.piece = ((a.per + np - 1) / np + vec - 1) / vec * vec;
-  }
-  cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg = launch_config<C>(csize, a.batch, stream, attr, a.part != nullptr);
+  a.per = ((a.vocab + csize - 1) / csize + vec - 1) / vec * vec;
+  // pieces of equal size (whole vectors, at most one stage) per slice
+  const int np = (a.per + piece - 1) / piece;
+  a.piece = ((a.per + np - 1) / np + vec - 1) / vec * vec;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = launch_config<C>(csize, a.batch, stream, attr);
   return cudaLaunchKernelEx(&cfg, accept_kernel<T, C::kNW, C::kNS>, a);
 }
 
 template <typename T>
 cudaError_t launch(AcceptParams a, cudaStream_t stream) {
-  return a.part ? launch_cfg<T, CfgPartials>(a, stream) : launch_cfg<T, CfgSingle>(a, stream);
+  return launch_cfg<T, CfgSingle>(a, stream);
 }
 
 // The chunk pass: as many CTAs as the device holds at once (queried once
@@ -1285,6 +1202,289 @@ rule_finish_kernel(const __grid_constant__ RuleFinishParams a) {
 template <typename T, int MODE>
 cudaError_t launch_rule_finish(const RuleFinishParams &f, int batch, cudaStream_t stream) {
   return launch_pdl(rule_finish_kernel<T, MODE>, dim3(batch), dim3(kRuleThreads), 0, stream, f);
+}
+
+// ------------------------------------------------------------ sampling finish
+// After the sampling rule's chunk pass, one launch (started early by
+// programmatic dependent launch) of nsplit CTAs per sequence, CTA j owning
+// the 32 KB chunks [j cpc, (j + 1) cpc) of the rows (nsplit from the batch:
+// about two CTAs per SM in all):
+//   1. the walk, in every CTA of the sequence alike (same inputs, same
+//      order, so all agree): a warp per row merges the row's parts into its
+//      reference and normaliser and p(x) or q(x); warp 0 walks the steps
+//      (accept iff u[t-1] q(x) < p(x)); the first CTA writes n_accept and
+//      pos (and token -1 when nothing is drawn);
+//   2. on a rejection, a warp per sixteenth of each of its chunks (a "sub-
+//      part": 2 KB of each of the rejected slot's two rows, one round of
+//      loads): the residual mass, sum max(0, e_t - rho e_d), and the target
+//      mass, sum e_t, as pairs in units of 2^Mt (rho = St / Sd);
+//   3. the CTA that counts last for its sequence (a per-sequence counter in
+//      the workspace, zeroed by the chunk pass) draws: the residual total
+//      (the target total when the residual is empty), U = u[B] times it,
+//      the sub-part holding U, then its entries in vocabulary order.
+// So the whole GPU takes part in the residual pass (its rows come from L2
+// when the chunk pass left them there), and the walk, the residual and the
+// draw cost one launch after the chunk pass.
+constexpr int kFinThreads = 512;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kSubParts = kFinWarps;                 // sub-parts per chunk: a warp each
+
+struct SampleFinishParams {
+  const void *target;
+  const void *draft;
+  const int32_t *draft_tokens;
+  const int32_t *tau;
+  const int32_t *cu_B;
+  const float *uniforms;
+  const float2 *part;      // [2 total_B][nchunks][kAConsumerWarps]: the chunk pass's (R, s)
+  const float *xlogit;     // [2 total_B]: the logits at the draft tokens
+  float4 *res4;            // [batch][nchunks][kSubParts]: (residual pair, target pair)
+  int *count;              // [batch]: CTAs whose residual sub-parts are written (the
+                           // chunk pass zeroes them)
+  int *claim;              // the chunk pass's control words
+  int32_t *n_accept;
+  int32_t *token;
+  int32_t *pos;
+  uint32_t *status;
+  int batch, vocab, total_B, B_max, nchunks, bulk;
+  int nsplit, cpc;         // CTAs per sequence, chunks per CTA
+  Scale ls;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kFinThreads, 2)
+sample_finish_kernel(const __grid_constant__ SampleFinishParams a) {
+  constexpr int N = Ld<T>::N;
+  constexpr int kChunk = chunk_entries<T>();
+  constexpr int kSubLen = kChunk / kSubParts;          // entries of a sub-part
+  constexpr int kSubVecs = kSubLen / N;                // 16-byte vectors of a sub-part
+  constexpr int kV = kSubVecs / 32;                    // per lane and row
+  constexpr int kHeld = 4;                             // chunk-pass parts held per lane: 4 x 32
+  static_assert(kV * 32 * N * kSubParts == kChunk, "sub-parts tile a chunk");
+  __shared__ float4 nrm_s[2 * kMaxB];                  // per row (2k: target, 2k+1: draft): (M, S.hi, S.lo, p(x) or q(x))
+  __shared__ float4 wsum_s[kFinWarps];                // the draw: per warp (residual pair, target pair)
+  __shared__ int fail_s, rej_s, last_s;
+  const int j = blockIdx.x, b = blockIdx.y, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  // the inputs written before the chunk pass (the sections, labels and
+  // uniforms; warp 0 holds lane l: tau, u[l], and u[B]) are read while it
+  // finishes
+  const int c0 = __ldg(a.cu_B + b), B = __ldg(a.cu_B + b + 1) - c0;
+  const bool valid = B >= 1 && B <= a.B_max && c0 >= 0 && c0 + B <= a.total_B;
+  const int tk = valid && warp == 0 && lane < B ? __ldg(a.tau + c0 + lane) : 0;
+  const float ul = valid && warp == 0 && lane <= B ? __ldg(a.uniforms + (long)b * (a.B_max + 1) + lane) : 0.f;
+  const float uB = valid ? __ldg(a.uniforms + (long)b * (a.B_max + 1) + B) : 0.f;
+  grid_dep_wait();                                     // the chunk pass's partials
+  // the chunk pass's give-up flag (every CTA reads it; the last to count
+  // zeroes the chunk pass's words at exit)
+  const int flag_t = kFinThreads - 1;
+  int ticket = -1;
+  if (t == flag_t) fail_s = chunk_flag_read(a.claim, &ticket);
+  const int ctas = gridDim.x * gridDim.y;
+  if (!valid) {                                        // malformed sequence: no walk
+    if (j == 0 && t == 0) {
+      a.n_accept[b] = 0;
+      a.token[b] = -1;
+      a.pos[b] = -1;
+      raise_status(a.status, kStatusBadInput);
+    }
+    if (t == flag_t) chunk_flag_reset(a.claim, ticket, ctas);
+    return;
+  }
+  const Scale ls = a.ls;
+  // -------------------------------------------------------- 1. the walk
+  const int n_ent = a.nchunks * kAConsumerWarps;       // chunk-pass parts of a row
+  // rows warp and warp + kFinWarps together (their loads in one round)
+  for (int r0 = warp; r0 < 2 * B; r0 += 2 * kFinWarps) {
+    float2 h[2][kHeld];
+    float xl[2];
+    bool xin[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int r = r0 + q * kFinWarps;
+      const bool has = r < 2 * B;
+      const float2 *pr = a.part + (long)(2 * c0 + r) * n_ent;
+      const int x = has ? __ldg(a.draft_tokens + c0 + (r >> 1)) : 0;
+      xin[q] = x >= 0 && x < a.vocab;
+      xl[q] = has ? __ldcg(a.xlogit + 2 * c0 + r) : 0.f;
+#pragma unroll
+      for (int i = 0; i < kHeld; ++i)
+        h[q][i] = has && lane + 32 * i < n_ent ? __ldcg(pr + lane + 32 * i) : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int r = r0 + q * kFinWarps;
+      if (r >= 2 * B) break;                           // warp-uniform
+      const float2 *pr = a.part + (long)(2 * c0 + r) * n_ent;
+      float M = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kHeld; ++i) M = fmaxf(M, h[q][i].x);
+      for (int i = lane + 32 * kHeld; i < n_ent; i += 32) M = fmaxf(M, __ldcg(pr + i).x);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      auto mass_of = [&](float2 v) {
+        const float w = (M != -INFINITY && v.x != -INFINITY) ? exp2_int(v.x - M) : 0.f;
+        return ff_of(v.y > 0.f ? v.y * w : 0.f);
+      };
+      Ff S = ff_of(0.f);
+#pragma unroll
+      for (int i = 0; i < kHeld; ++i) S = ff_add(S, mass_of(h[q][i]));
+      for (int i = lane + 32 * kHeld; i < n_ent; i += 32) S = ff_add(S, mass_of(__ldcg(pr + i)));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) S = ff_add(S, ff_shfl_xor(S, o));
+      if (lane == 0) {
+        // p(x) or q(x); a token outside the vocabulary rejects
+        nrm_s[r] = make_float4(M, S.hi, S.lo, xin[q] ? rel_exp(xl[q], M, ls) / (S.hi + S.lo) : 0.f);
+        if (!xin[q] && (r & 1) == 0 && j == 0) raise_status(a.status, kStatusBadInput);
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // the first rejected step over a permutation of 1..B
+    const bool tin = lane < B && tk >= 1 && tk <= B;
+    const uint32_t seen = __reduce_or_sync(0xffffffffu, tin ? 1u << (tk - 1) : 0u);
+    const bool perm = seen == (B == 32 ? 0xffffffffu : (1u << B) - 1u);
+    const float ut = __shfl_sync(0xffffffffu, ul, tin ? tk - 1 : 0);
+    const bool rejects = tin && !(ut * nrm_s[2 * lane + 1].w < nrm_s[2 * lane].w);
+    const uint32_t rstep = __reduce_min_sync(0xffffffffu, rejects ? (uint32_t)tk : 0xffffffffu);
+    const unsigned rl = __ballot_sync(0xffffffffu, rejects && (uint32_t)tk == rstep);
+    const bool walk = perm && !fail_s;
+    if (lane == 0) {
+      rej_s = walk && rstep != 0xffffffffu ? __ffs(rl) - 1 : -1;
+      if (j == 0) {
+        if (!perm) raise_status(a.status, kStatusBadInput);
+        a.n_accept[b] = !walk ? 0 : rstep == 0xffffffffu ? B : (int)rstep - 1;
+        a.pos[b] = walk && rstep != 0xffffffffu ? __ffs(rl) - 1 : -1;
+        if (!walk || rstep == 0xffffffffu) a.token[b] = -1;   // else the draw writes it
+      }
+    }
+  }
+  __syncthreads();
+  const int k = rej_s;
+  if (k < 0) {
+    if (t == flag_t) chunk_flag_reset(a.claim, ticket, ctas);
+    return;
+  }
+  // ------------------------------------------------ 2. the residual sub-parts
+  const float4 nt = nrm_s[2 * k], nd = nrm_s[2 * k + 1];
+  const float Mt = nt.x, Md = nd.x;
+  const Ff rho = ff_div(Ff{nt.y, nt.z}, Ff{nd.y, nd.z});
+  const long row = c0 + k;
+  const T *trow = (const T *)a.target + row * a.vocab;
+  const T *drow = (const T *)a.draft + row * a.vocab;
+  const int cend = min(a.nchunks, (j + 1) * a.cpc);
+#pragma unroll 1
+  for (int c = j * a.cpc; c < cend; ++c) {
+    const int n = min(kChunk, a.vocab - c * kChunk);
+    uint4 wt[kV], wd[kV];
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+      const int e0 = (warp * kSubVecs + i * 32 + lane) * N;
+      wt[i] = Ld<T>::load(trow + (long)c * kChunk + e0, n - e0, a.bulk != 0);
+      wd[i] = Ld<T>::load(drow + (long)c * kChunk + e0, n - e0, a.bulk != 0);
+    }
+    float rs[4] = {0.f, 0.f, 0.f, 0.f}, ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kV; ++i) {
+      float ft[N], fd[N];
+      Ld<T>::unpack(wt[i], ft);
+      Ld<T>::unpack(wd[i], fd);
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        const float et = rel_exp(ft[e], Mt, ls);
+        rs[e & 3] += residual(et, draft_mass(fd[e], Md, rho, ls));
+        ps[e & 3] += et;
+      }
+    }
+    Ff fr = ff_add(ff_of(rs[0] + rs[1]), ff_of(rs[2] + rs[3]));
+    Ff fp = ff_add(ff_of(ps[0] + ps[1]), ff_of(ps[2] + ps[3]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      fr = ff_add(fr, ff_shfl_xor(fr, o));
+      fp = ff_add(fp, ff_shfl_xor(fp, o));
+    }
+    if (lane == 0)
+      a.res4[((long)b * a.nchunks + c) * kSubParts + warp] = make_float4(fr.hi, fr.lo, fp.hi, fp.lo);
+  }
+  __syncthreads();                                     // every sub-part of this CTA written
+  if (a.nsplit == 1) {
+    if (t == 0) last_s = 1;                            // (written by this CTA alone)
+  } else if (t == 0) {
+    __threadfence();                                   // the sub-parts precede the count
+    last_s = atomicAdd(a.count + b, 1) == a.nsplit - 1;
+    if (last_s) __threadfence();                       // the others' sub-parts are visible
+  }
+  __syncthreads();
+  if (last_s) {
+    // ------------------------------------------------------- 3. the draw
+    // warp w sums the sub-parts [w per, (w + 1) per); every warp finds, from
+    // the same 16 warp totals in the same order, the warp whose range holds
+    // U (the first whose running mass exceeds it, else the last with mass);
+    // that warp finds the sub-part in its range and scans its entries
+    const int n_sub = a.nchunks * kSubParts;
+    const int per = (n_sub + kFinWarps - 1) / kFinWarps;
+    const int s0 = min(n_sub, warp * per), s1 = min(n_sub, s0 + per);
+    const float4 *pr = a.res4 + (long)b * n_sub;
+    float4 h1[1];
+    h1[0] = s0 + lane < s1 ? __ldcg(pr + s0 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    Ff Sr{h1[0].x, h1[0].y}, Sp{h1[0].z, h1[0].w};
+    for (int i = s0 + 32 + lane; i < s1; i += 32) {
+      const float4 v = __ldcg(pr + i);
+      Sr = ff_add(Sr, Ff{v.x, v.y});
+      Sp = ff_add(Sp, Ff{v.z, v.w});
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Sr = ff_add(Sr, ff_shfl_xor(Sr, o));
+      Sp = ff_add(Sp, ff_shfl_xor(Sp, o));
+    }
+    if (lane == 0) wsum_s[warp] = make_float4(Sr.hi, Sr.lo, Sp.hi, Sp.lo);
+    __syncthreads();
+    float4 hw[1];
+    hw[0] = lane < kFinWarps ? wsum_s[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+    Ff Tr{hw[0].x, hw[0].y}, Tp{hw[0].z, hw[0].w};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Tr = ff_add(Tr, ff_shfl_xor(Tr, o));
+      Tp = ff_add(Tp, ff_shfl_xor(Tp, o));
+    }
+    // U = u[B] S (the target's own mass when the residual is empty)
+    const bool use_p = !(Tr.hi > 0.f);
+    const Ff tot = use_p ? Tp : Tr;
+    const float uh = uB * tot.hi;
+    const Ff U = ff_add(Ff{uh, fmaf(uB, tot.hi, -uh)}, ff_of(uB * tot.lo));
+    auto mass_of = [&](const float4 &v) { return use_p ? Ff{v.z, v.w} : Ff{v.x, v.y}; };
+    Ff wstart;                                         // (16 totals, all held: wsum_s is not re-read)
+    const int owner = locate_part<1>(wsum_s, hw, kFinWarps, U, mass_of, lane, &wstart);
+    if (warp == owner) {
+      const Ff U2 = ff_add(U, ff_neg(wstart));
+      Ff base;
+      const int sel = s0 + locate_part<1>(pr + s0, h1, s1 - s0, U2, mass_of, lane, &base);
+      const int p0 = (sel / kSubParts) * kChunk + (sel % kSubParts) * kSubLen;
+      const Ff D0 = ff_add(U2, ff_neg(base));
+      const T *const rows[2] = {trow, drow};
+      const int tok = scan_part<T, 2>(rows, p0, min(kSubLen, a.vocab - p0), kSubVecs, D0.hi + D0.lo,
+                                      a.bulk != 0, lane, [&](const float (&f)[2][N], float (&m)[N]) {
+#pragma unroll
+                                        for (int e = 0; e < N; ++e) {
+                                          const float et = rel_exp(f[0][e], Mt, ls);
+                                          m[e] = use_p ? et : residual(et, draft_mass(f[1][e], Md, rho, ls));
+                                        }
+                                      });
+      if (lane == 0) a.token[b] = tok;
+    }
+  }
+  if (t == flag_t) chunk_flag_reset(a.claim, ticket, ctas);
+}
+
+// At most two CTAs per SM over the batch (one wave), each CTA whole chunks.
+template <typename T>
+cudaError_t launch_sample_finish(SampleFinishParams f, cudaStream_t stream) {
+  const int want = 2 * device_sm_count() / f.batch;
+  const int ns = std::max(1, std::min(want, f.nchunks));
+  f.cpc = (f.nchunks + ns - 1) / ns;
+  f.nsplit = (f.nchunks + f.cpc - 1) / f.cpc;
+  return launch_pdl(sample_finish_kernel<T>, dim3(f.nsplit, f.batch), dim3(kFinThreads), 0, stream, f);
 }
 
 // ---------------------------------------------------------------- greedy
@@ -1752,7 +1952,9 @@ bool accept_pointers_ok(const simsd_accept_desc *d) {
 // Workspace: the status word; for the chunked paths also the chunk pass's
 // control words (beside the status word), the chunk partials and the
 // draft-token logits.
-// Sampling: partials [2 total_B][nchunks][8] (float2), logits [2 total_B];
+// Sampling: partials [2 total_B][nchunks][8] (float2), logits [2 total_B],
+// per-sequence counters [batch] (zeroed by the chunk pass) and the residual
+// sub-parts [batch][nchunks][16] (float4);
 // greedy and matching: partials [total_B][nchunks][8] (float4), logits
 // [total_B].  A workspace of just the status word runs the single cluster
 // kernel of the rule (the rows streamed per sequence), as do walks from
@@ -1760,7 +1962,7 @@ bool accept_pointers_ok(const simsd_accept_desc *d) {
 constexpr size_t kAcceptWorkspace = kAlign;
 struct AcceptLayout {
   int nchunks;
-  size_t off_part, off_xlogit, off_claim, total;
+  size_t off_part, off_xlogit, off_claim, off_count, off_res4, total;
 };
 AcceptLayout accept_layout(const simsd_accept_desc *d) {
   AcceptLayout L;
@@ -1772,7 +1974,10 @@ AcceptLayout accept_layout(const simsd_accept_desc *d) {
   L.off_part = kAcceptWorkspace;
   L.off_xlogit = align_up(L.off_part + rows * L.nchunks * kAConsumerWarps *
                                            (pairs ? sizeof(float2) : sizeof(float4)), kAlign);
-  L.total = align_up(L.off_xlogit + rows * sizeof(float), kAlign);
+  L.off_count = align_up(L.off_xlogit + rows * sizeof(float), kAlign);
+  L.off_res4 = align_up(L.off_count + (pairs ? (size_t)d->batch * sizeof(int) : 0), kAlign);
+  L.total = align_up(L.off_res4 + (pairs ? (size_t)d->batch * L.nchunks * kSubParts * sizeof(float4) : 0),
+                     kAlign);
   return L;
 }
 size_t accept_workspace(const simsd_accept_desc *d) { return accept_layout(d).total; }
@@ -1825,6 +2030,8 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     c.xlogit = (float *)(ws + L.off_xlogit);
     c.part4 = (float4 *)(ws + L.off_part);
     c.claim = (int *)(ws + L.off_claim);
+    c.zero = nullptr;
+    c.n_zero = 0;
     c.status = (uint32_t *)ws;
     c.vocab = d->vocab;
     c.total_B = d->total_B;
@@ -1940,14 +2147,11 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
   a.piece = 0;
   a.bulk = ((size_t)d->vocab * es) % 16 == 0 && aligned16(d->target_logits) &&
            aligned16(d->draft_logits);
-  a.part = nullptr;
-  a.xlogit = nullptr;
-  a.claim = nullptr;
-  a.nchunks = 0;
-  a.cpc = 0;
   mark(events, 0, stream);
   cudaError_t e = cudaSuccess;
   if (chunked) {
+    // the chunk pass over both rows of every slot on every SM, then the
+    // walk, the residual parts and the draw
     ChunkParams c;
     c.target = d->target_logits;
     c.draft = d->draft_logits;
@@ -1956,6 +2160,8 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     c.xlogit = (float *)(ws + L.off_xlogit);
     c.claim = (int *)(ws + L.off_claim);
     c.part4 = nullptr;
+    c.zero = (int *)(ws + L.off_count);
+    c.n_zero = d->batch;
     c.status = a.status;
     c.vocab = d->vocab;
     c.total_B = d->total_B;
@@ -1963,16 +2169,38 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     c.bulk = a.bulk;
     c.polls = a.polls;
     c.ls = a.ls;
-    e = d->dtype == SIMSD_BF16 ? launch_chunks<__nv_bfloat16, kModeSample>(c, stream)
-                                 : launch_chunks<float, kModeSample>(c, stream);
-    a.part = c.part;
-    a.xlogit = c.xlogit;
-    a.claim = c.claim;
-    a.nchunks = L.nchunks;
+    SampleFinishParams f;
+    f.target = d->target_logits;
+    f.draft = d->draft_logits;
+    f.draft_tokens = d->draft_tokens;
+    f.tau = d->tau;
+    f.cu_B = d->cu_B;
+    f.uniforms = d->uniforms;
+    f.part = c.part;
+    f.xlogit = c.xlogit;
+    f.count = (int *)(ws + L.off_count);
+    f.res4 = (float4 *)(ws + L.off_res4);
+    f.claim = c.claim;
+    f.n_accept = d->n_accept;
+    f.token = d->token;
+    f.pos = d->pos;
+    f.status = a.status;
+    f.batch = d->batch;
+    f.vocab = d->vocab;
+    f.total_B = d->total_B;
+    f.B_max = d->B_max;
+    f.nchunks = L.nchunks;
+    f.bulk = a.bulk;
+    f.ls = a.ls;
+    e = bf16 ? launch_chunks<__nv_bfloat16, kModeSample>(c, stream) : launch_chunks<float, kModeSample>(c, stream);
+    mark(events, 1, stream);
+    if (e == cudaSuccess)
+      e = bf16 ? launch_sample_finish<__nv_bfloat16>(f, stream) : launch_sample_finish<float>(f, stream);
+    mark(events, 2, stream);
+    return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
   }
   mark(events, 1, stream);
-  if (e == cudaSuccess)
-    e = d->dtype == SIMSD_BF16 ? launch<__nv_bfloat16>(a, stream) : launch<float>(a, stream);
+  e = bf16 ? launch<__nv_bfloat16>(a, stream) : launch<float>(a, stream);
   mark(events, 2, stream);
   return e == cudaSuccess ? SIMSD_OK : SIMSD_ERR_CUDA;
 }
@@ -1991,6 +2219,8 @@ cudaError_t launch_draft_chunks(const simsd_draft_desc *d, float4 *part4, int *c
   c.xlogit = nullptr;
   c.part4 = part4;
   c.claim = claim;
+  c.zero = nullptr;
+  c.n_zero = 0;
   c.status = status;
   c.vocab = d->vocab;
   c.total_B = d->total_B;

@@ -279,30 +279,22 @@ static __device__ __noinline__ int warp_pick(Ff m, Ff base, Ff U, Ff *start) {
 }
 
 // ------------------------------------------------------------ part draws
-// Inverse-CDF draw from one row after a chunk pass: the pass left, per part
+// Inverse-CDF draws from one row after a chunk pass, which left per part
 // (1/8 of a 32 KB chunk, contiguous in the vocabulary; parts in (chunk,
-// part) order are in vocabulary order), the part's reference (.x) and sum
-// of 2^(l ls - reference) (.y).  M is the row's reference and U the draw
-// point, both in units of 2^M.  Lane l holds parts l + 32 i (i < HELD) in
-// h; the rest are read from pr.  The part whose running mass first exceeds
-// U (else the last with mass), then that part column by column in
-// vocabulary order (an fp32 scan relative to its start): the first entry
-// whose running mass exceeds U, else the last entry with mass.  All 32
-// lanes call it; every lane gets the token.
-template <typename T, int HELD>
-__device__ int part_draw(const float4 *pr, const float4 (&h)[HELD], int n_ent, float M, Ff U,
-                         const T *row, int vocab, int chunk, bool bulk, Scale ls, int lane) {
-  constexpr int N = Ld<T>::N;
-  constexpr int kParts = 8;
-  const int part_len = chunk / kParts, part_vecs = part_len / N;
-  auto mass_of = [&](float4 v) {
-    const float w = (M != -INFINITY && v.x != -INFINITY) ? exp2_int(v.x - M) : 0.f;
-    return v.y > 0.f ? v.y * w : 0.f;
-  };
+// part) order are in vocabulary order) what the part's mass is made of.
+// All 32 lanes call these; every lane gets the result.
+//
+// locate_part: lane l holds parts l + 32 i (i < HELD) in h, the rest are
+// read from pr; mass_of(part) gives a part's mass (pairs, in the units of
+// U).  Returns the part whose running mass first exceeds U, else the last
+// part with mass (0 if none), and in *start the mass before it.
+template <int HELD, typename P, typename MassOf>
+__device__ int locate_part(const P *pr, const P (&h)[HELD], int n_ent, Ff U, MassOf mass_of, int lane,
+                           Ff *start_out) {
   Ff base = ff_of(0.f), last_start = ff_of(0.f);
   int sel = -1, last_nz = 0;
-  auto group = [&](int g0, float4 v) {              // parts g0 .. g0 + 31
-    const Ff m = ff_of(g0 + lane < n_ent ? mass_of(v) : 0.f);
+  auto group = [&](int g0, const P &v) {            // parts g0 .. g0 + 31
+    const Ff m = g0 + lane < n_ent ? mass_of(v) : ff_of(0.f);
     Ff inc = m;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -329,40 +321,54 @@ __device__ int part_draw(const float4 *pr, const float4 (&h)[HELD], int n_ent, f
 #pragma unroll
   for (int i = 0; i < HELD; ++i)
     if (sel < 0 && 32 * i < n_ent) group(32 * i, h[i]);
-  for (int g0 = 32 * HELD; g0 < n_ent && sel < 0; g0 += 32)
-    group(g0, g0 + lane < n_ent ? __ldcg(pr + g0 + lane) : make_float4(-INFINITY, 0.f, 0.f, 0.f));
+  for (int g0 = 32 * HELD; g0 < n_ent && sel < 0; g0 += 32) {
+    const P v = g0 + lane < n_ent ? __ldcg(pr + g0 + lane) : P{};
+    group(g0, v);
+  }
   if (sel < 0) {
     sel = last_nz;
     base = last_start;
   }
-  const int p0 = (sel / kParts) * chunk + (sel % kParts) * part_len;
-  const int n = min(part_len, vocab - p0);
-  const T *src = row + p0;
-  const Ff D0 = ff_add(U, ff_neg(base));
-  const float dd = D0.hi + D0.lo;
+  *start_out = base;
+  return sel;
+}
+
+// scan_part: the entries [p0, p0 + n) of ROWS rows (rows[r] + p0 is the
+// part's first entry in row r), column by column in vocabulary order
+// (lane l: vector l of each column of 32 vectors), with entry_mass(f, m)
+// turning the ROWS rows' values of a vector into its N masses.  The loads
+// of kBatch columns are issued together (a part of a 32 KB chunk is 8
+// columns: one round for one row, two for two).  Running masses are fp32 relative to the part's
+// start; dd is U minus the mass before the part.  Returns the first entry
+// whose running mass exceeds dd, else the last entry with mass (-1: none).
+template <typename T, int ROWS, typename EntryMass>
+__device__ int scan_part(const T *const (&rows)[ROWS], int p0, int n, int part_vecs, float dd, bool bulk,
+                         int lane, EntryMass entry_mass) {
+  constexpr int N = Ld<T>::N;
+  constexpr int kBatch = 8 / ROWS;
   float col_base = 0.f;
   int first = 0x7fffffff, last_pos = -1;
-  // kBatch columns of 32 vectors per round, their loads issued together
-  // (a part of a 32 KB chunk is 8 columns: one round)
-  constexpr int kBatch = 8;
 #pragma unroll 1
   for (int c0 = 0; c0 * 32 < part_vecs && first == 0x7fffffff; c0 += kBatch) {
-    uint4 w[kBatch];
+    uint4 w[kBatch][ROWS];
 #pragma unroll
     for (int c = 0; c < kBatch; ++c) {
       const int e0 = ((c0 + c) * 32 + lane) * N;
-      w[c] = (c0 + c) * 32 < part_vecs ? Ld<T>::load(src + e0, n - e0, bulk) : Ld<T>::neg_inf();
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r)
+        w[c][r] = (c0 + c) * 32 < part_vecs ? Ld<T>::load(rows[r] + p0 + e0, n - e0, bulk) : Ld<T>::neg_inf();
     }
 #pragma unroll
     for (int c = 0; c < kBatch; ++c) {
       if (first != 0x7fffffff || (c0 + c) * 32 >= part_vecs) break;   // warp-uniform
       const int e0 = ((c0 + c) * 32 + lane) * N;
-      float f[N], m[N];
-      Ld<T>::unpack(w[c], f);
+      float f[ROWS][N], m[N];
+#pragma unroll
+      for (int r = 0; r < ROWS; ++r) Ld<T>::unpack(w[c][r], f[r]);
+      entry_mass(f, m);
       float lane_mass = 0.f;
 #pragma unroll
       for (int e = 0; e < N; ++e) {
-        m[e] = rel_exp(f[e], M, ls);
         lane_mass += m[e];
         if (m[e] > 0.f) last_pos = p0 + e0 + e;
       }
@@ -388,6 +394,31 @@ __device__ int part_draw(const float4 *pr, const float4 (&h)[HELD], int n_ent, f
   }
   last_pos = __reduce_max_sync(0xffffffffu, last_pos);
   return first != 0x7fffffff ? first : last_pos;
+}
+
+// part_draw: a draw from one row's softmax after a chunk pass that left
+// per part its reference (.x) and sum of 2^(l ls - reference) (.y); M is the
+// row's reference and U the draw point, both in units of 2^M.
+template <typename T, int HELD>
+__device__ int part_draw(const float4 *pr, const float4 (&h)[HELD], int n_ent, float M, Ff U,
+                         const T *row, int vocab, int chunk, bool bulk, Scale ls, int lane) {
+  constexpr int N = Ld<T>::N;
+  constexpr int kParts = 8;
+  const int part_len = chunk / kParts;
+  auto mass_of = [&](const float4 &v) {
+    const float w = (M != -INFINITY && v.x != -INFINITY) ? exp2_int(v.x - M) : 0.f;
+    return ff_of(v.y > 0.f ? v.y * w : 0.f);
+  };
+  Ff base;
+  const int sel = locate_part<HELD>(pr, h, n_ent, U, mass_of, lane, &base);
+  const int p0 = (sel / kParts) * chunk + (sel % kParts) * part_len;
+  const Ff D0 = ff_add(U, ff_neg(base));
+  const T *const rows[1] = {row};
+  return scan_part<T, 1>(rows, p0, min(part_len, vocab - p0), part_len / N, D0.hi + D0.lo, bulk, lane,
+                         [&](const float (&f)[1][N], float (&m)[N]) {
+#pragma unroll
+                           for (int e = 0; e < N; ++e) m[e] = rel_exp(f[0][e], M, ls);
+                         });
 }
 
 // ------------------------------------------------- chunk pass control words

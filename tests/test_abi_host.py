@@ -233,3 +233,31 @@ def test_descriptor_layouts_match_the_header(tmp_path):
         assert got[(cname, "sizeof")] == ctypes.sizeof(py), cname
         for f, _ in py._fields_:
             assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
+
+
+@pytest.mark.parametrize("dtype,vocab,batch,total_B", [(binding.SIMSD_BF16, 151936, 16, 64),
+                                                       (binding.SIMSD_F32, 777, 3, 7),
+                                                       (binding.SIMSD_BF16, 1 << 21, 5, 160),
+                                                       (binding.SIMSD_F32, 100003, 256, 1536)])
+def test_accept_workspace_size_is_the_header_formula(lib, dtype, vocab, batch, total_B):
+    """simsd_accept_workspace_size equals the sum the header states, term by
+    term rounded up to 256 bytes, for every rule; and simsd_draft_workspace_size
+    equals its own."""
+    def r(x):
+        return -(-x // 256) * 256
+    E = 16384 if dtype == binding.SIMSD_BF16 else 8192
+    C = -(-vocab // E)
+    d = binding.AcceptDesc()
+    for k, v in dict(batch=batch, vocab=vocab, total_B=total_B, B_max=32, dtype=dtype).items():
+        setattr(d, k, v)
+    want = {binding.SIMSD_ACCEPT_SAMPLE: 256 + r(2 * total_B * C * 64) + r(2 * total_B * 4) +
+            r(batch * 4) + r(batch * C * 256),
+            binding.SIMSD_ACCEPT_GREEDY: 256 + r(total_B * C * 128) + r(total_B * 4),
+            binding.SIMSD_ACCEPT_MATCH: 256 + r(total_B * C * 128) + r(total_B * 4)}
+    for rule, n in want.items():
+        d.rule = rule
+        assert lib.simsd_accept_workspace_size(ctypes.byref(d)) == n, rule
+    dd = binding.DraftDesc()
+    for k, v in dict(batch=batch, vocab=vocab, total_B=total_B, B_max=32, dtype=dtype).items():
+        setattr(dd, k, v)
+    assert lib.simsd_draft_workspace_size(ctypes.byref(dd)) == 256 + r(total_B * C * 128)
