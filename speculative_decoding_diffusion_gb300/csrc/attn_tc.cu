@@ -13,9 +13,12 @@
 // from HBM serves every row.  Keys come in 128-key blocks: an MMA
 // instruction costs nearly the same at N = 64 as at N = 128, so wide score
 // tiles halve the instructions per key.  Warp roles:
-//   warp 0     TMA producer: K and V of each block (8 pages, one 2 KB box
-//              per page and 64-column half, 128-byte swizzle) into a
-//              3-stage ring;
+//   warps 0, 6 TMA producers: K (warp 0) and V (warp 6) of each block (8
+//              pages, one 2 KB box per page and 64-column half, 128-byte
+//              swizzle) into a 3-stage ring whose K and V halves are freed
+//              separately -- a K half once the block's S = Q K^T is done,
+//              so the next K copies start while the block's softmax and
+//              P.V still run;
 //   warp 1     TMEM owner and MMA issuer (one thread, never blocking on one
 //              barrier): S = Q K^T into one of two TMEM score tiles (128 x
 //              128 fp32), O += P V into the TMEM accumulator (128 x hd fp32)
@@ -49,7 +52,8 @@ constexpr int kRows = 128;           // query rows per CTA: the MMA's M
 constexpr int kKeys = 128;           // keys per block: S width, P.V depth
 static_assert(kKeys == kBlockKeys, "split chunks are whole blocks");
 constexpr int kStages = 3;
-constexpr int kWarps = 6;
+constexpr int kWarps = 7;                // producer K, MMA, 4 softmax, producer V
+constexpr int kVWarp = 6;
 constexpr int kThreads = kWarps * 32;
 constexpr int kSoftmax = 4 * 32;     // softmax threads (warps 2-5)
 constexpr int kBoxBytes = kPage * 128;
@@ -58,7 +62,8 @@ constexpr float kHeadroom = 8.f;     // log2 units a row max may grow before O i
 constexpr uint32_t kColS = 0;        // two score / probability tiles: columns 0 and kKeys
 constexpr uint32_t kColO = 2 * kKeys;
 
-enum { kBarKvFull = 0, kBarKvEmpty = kBarKvFull + kStages, kBarSFull = kBarKvEmpty + kStages,
+enum { kBarKFull = 0, kBarVFull = kBarKFull + kStages, kBarKEmpty = kBarVFull + kStages,
+       kBarVEmpty = kBarKEmpty + kStages, kBarSFull = kBarVEmpty + kStages,
        kBarPFull = kBarSFull + 2, kBarPvDone = kBarPFull + 2,
        kBarQReady = kBarPvDone + 2, kNumBars = kBarQReady + 1 };
 
@@ -187,15 +192,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     return lane < (min(kKeys, k_end - kb) + kPage - 1) / kPage ? __ldg(bt + kb / kPage + lane) : 0;
   };
   int pages[kStages];
-  if (warp == 0) {
-    if (lane == 0) { prefetch_tmap(&tmK); prefetch_tmap(&tmV); }
+  if (warp == 0 || warp == kVWarp) {
+    if (lane == 0) prefetch_tmap(warp == 0 ? &tmK : &tmV);
 #pragma unroll
     for (int d = 0; d < kStages; ++d) pages[d] = block_page(d);
   }
   // softmax threads request their raw query row first, ahead of the K/V
   // stream the producer starts below (each thread one row of the tile)
   uint4 qv[HD / 8];
-  if (warp >= 2) {
+  const bool softmax_warp = warp >= 2 && warp < 6;
+  if (softmax_warp) {
     const int qg = (warp & 3) % (4 / R), qrow_i = row0 + 32 * qg + lane;
     if (qrow_i < M) {
       const uint4 *src = reinterpret_cast<const uint4 *>(
@@ -211,13 +217,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   // requested with the query rows, before the producer's copies fill the
   // memory system
   const int tsm = threadIdx.x - 64;
-  const int tau_j = warp >= 2 && a.node_size == 0 && tsm < 2 * B
+  const int tau_j = softmax_warp && a.node_size == 0 && tsm < 2 * B
                         ? __ldg(a.tau + c0 + (tsm < B ? tsm : tsm - B)) : 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bar(kBarKvFull + i), 1);
-      mbar_init(bar(kBarKvEmpty + i), 1);
+      mbar_init(bar(kBarKFull + i), 1);
+      mbar_init(bar(kBarVFull + i), 1);
+      mbar_init(bar(kBarKEmpty + i), 1);
+      mbar_init(bar(kBarVEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarSFull + i), 1);
@@ -236,10 +244,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  int issued = 0;                            // producer: blocks whose loads were started
+  int issued = 0;                            // producers: blocks whose loads were started
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
+  if (warp == 0 || warp == kVWarp) {
+    // --------------------------------------------------------- producers
+    // warp 0 copies K, warp kVWarp copies V, each into its half of the
+    // stage once the MMA issuer has released that half
+    const bool kside = warp == 0;
+    const CUtensorMap *tm = kside ? &tmK : &tmV;
+    const int full0 = kside ? kBarKFull : kBarVFull, empty0 = kside ? kBarKEmpty : kBarVEmpty;
     bool dep_done = false, ok = true;
     for (int j0 = 0; ok && j0 < n_blocks; j0 += kStages) {
 #pragma unroll
@@ -254,21 +267,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
         const int n_pages = (min(kKeys, k_end - kb) + kPage - 1) / kPage;
         const int page = pages[u];
-        if (j >= kStages && !mbar_wait_warp(bar(kBarKvEmpty + s), ((j / kStages) - 1) & 1, a.polls)) {
+        if (j >= kStages && !mbar_wait_warp(bar(empty0 + s), ((j / kStages) - 1) & 1, a.polls)) {
           if (lane == 0) { raise_status(a.status, kStatusTimeout); atomicOr(flag_s, 1); }
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar(kBarKvFull + s), n_pages * L::kHalves * 2 * kBoxBytes);
+        if (lane == 0) mbar_arrive_expect_tx(bar(full0 + s), n_pages * L::kHalves * kBoxBytes);
         __syncwarp();
         if (lane < n_pages) {
-          const uint32_t kt = sKv + s * L::kStage, vt = kt + L::kKv;
+          const uint32_t t0 = sKv + s * L::kStage + (kside ? 0 : L::kKv);
 #pragma unroll
-          for (int hh = 0; hh < L::kHalves; ++hh) {
-            const uint32_t off = hh * L::kKvHalf + lane * kBoxBytes;
-            tma_load_4d(kt + off, &tmK, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
-            tma_load_4d(vt + off, &tmV, bar(kBarKvFull + s), hh * 64, 0, kvh, page);
-          }
+          for (int hh = 0; hh < L::kHalves; ++hh)
+            tma_load_4d(t0 + hh * L::kKvHalf + lane * kBoxBytes, tm, bar(full0 + s), hh * 64, 0, kvh, page);
         }
         issued = j + 1;
         pages[u] = block_page(j + kStages);
@@ -289,7 +299,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         bool progressed = false;
         if (ns < n_blocks) {
           const int s = ns % kStages, tb = ns & 1;
-          if (mbar_test(bar(kBarKvFull + s), (ns / kStages) & 1) &&
+          if (mbar_test(bar(kBarKFull + s), (ns / kStages) & 1) &&
               (ns < 2 || mbar_test(bar(kBarPvDone + tb), ((ns >> 1) - 1) & 1))) {
             tc::fence_after_sync();
             const uint32_t kt = sKv + s * L::kStage;
@@ -300,13 +310,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                               tc::smem_desc_sw128(ka, 16, 1024), idS, kk > 0);
             }
             tc::commit(bar(kBarSFull + tb));
+            tc::commit(bar(kBarKEmpty + s));   // the K half is free once S is done
             ++ns;
             progressed = true;
           }
         }
         if (np < ns) {
           const int tb = np & 1, s = np % kStages;
-          if (mbar_test(bar(kBarPFull + tb), (np >> 1) & 1)) {
+          if (mbar_test(bar(kBarPFull + tb), (np >> 1) & 1) &&
+              mbar_test(bar(kBarVFull + s), (np / kStages) & 1)) {
             tc::fence_after_sync();
             const int kb = k_begin + np * kKeys;
             const int valid = min(kKeys, k_end - kb);
@@ -317,7 +329,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                               tc::smem_desc_sw128(vt + kk * 2048, L::kKvHalf, 1024), idO,
                               (np > 0 || kk > 0));
             tc::commit(bar(kBarPvDone + tb));
-            tc::commit(bar(kBarKvEmpty + s));
+            tc::commit(bar(kBarVEmpty + s));
             ++np;
             progressed = true;
           }
@@ -522,6 +534,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
           const int valid = min(kKeys, k_end - kb);
           const int loaded = (valid + kPage - 1) & ~(kPage - 1);
           if (q4 == 0 && kb + valid == Lk && loaded > valid) {
+            // the block's V half may still be landing: wait for it first
+            if (!mbar_wait_warp(bar(kBarVFull + j % kStages), (j / kStages) & 1, a.polls)) { ok = false; break; }
             constexpr int CH = HD / 8;
             uint8_t *vt = sb + L::kOffKv + (j % kStages) * L::kStage + L::kKv;
             for (int e = lane; e < (loaded - valid) * CH; e += 32) {
@@ -632,9 +646,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   __syncthreads();
   // after a wait that gave up (any warp's: the flag is final here), the
   // copies still in flight land before the CTA can exit (default limit)
-  if (warp == 0 && *(volatile int *)flag_s)
+  if ((warp == 0 || warp == kVWarp) && *(volatile int *)flag_s)
     for (int j = max(0, issued - kStages); j < issued; ++j)
-      (void)mbar_wait_warp(bar(kBarKvFull + j % kStages), (j / kStages) & 1);
+      (void)mbar_wait_warp(bar((warp == 0 ? kBarKFull : kBarVFull) + j % kStages), (j / kStages) & 1);
   if (warp == 1) {
     tc::fence_after_sync();
     tc::dealloc(tmem, L::kTmemCols);
