@@ -86,6 +86,20 @@ def test_few_sequences_large_clusters(dtype, vocab, batch, B, path):
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
 
 
+@pytest.mark.parametrize("dtype,vocab", [("bf16", 40000), ("f32", 777), ("bf16", 1003)])
+def test_batches_over_twice_the_sm_count(dtype, vocab):
+    """More sequences than two per SM: the finishing kernel runs one CTA per
+    sequence (all chunks each) in more than one wave.  Against the oracle,
+    on 16-byte-aligned rows and on element-copied ones."""
+    w = synth.make(tiny_accept_spec(batch=400, dtype=dtype, vocab=vocab), seed=vocab + 400)
+    n, tok, pos = run_accept(w, "two-kernel")
+    step_ties, draw_ties, draws = parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
+    print("%s V=%d: %d sequences, %d draws, %d draw ties, %d step ties"
+          % (dtype, vocab, len(w.lens), draws, draw_ties, step_ties))
+    assert draw_ties <= parity.max_ties(draws)
+    assert draws > 100
+
+
 def test_invalid_token_rejects_and_empty_residual_draws_from_p():
     """A draft token outside the vocabulary rejects its step and sets the
     status word's bad-input bit; with identical target and draft rows the

@@ -186,15 +186,16 @@ def test_accept_wait_that_gives_up_returns_a_status():
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
 
 
-@pytest.mark.parametrize("rule", [binding.SIMSD_ACCEPT_GREEDY, binding.SIMSD_ACCEPT_MATCH,
-                                  binding.SIMSD_ACCEPT_SAMPLE])
-def test_chunk_pass_that_gives_up_means_no_walk(rule):
+@pytest.mark.parametrize("rule,batch", [(binding.SIMSD_ACCEPT_GREEDY, 6), (binding.SIMSD_ACCEPT_MATCH, 6),
+                                        (binding.SIMSD_ACCEPT_SAMPLE, 6), (binding.SIMSD_ACCEPT_SAMPLE, 200)])
+def test_chunk_pass_that_gives_up_means_no_walk(rule, batch):
     """The chunked path with every wait giving up at once: the chunk pass
     raises its give-up flag, so the kernel after it reports "no walk" for
     every sequence (whatever stale partials the workspace holds) and sets
     the timeout bit; it puts the chunk pass's control words back to zero, so
-    the next call on the same workspace is correct."""
-    w = synth.make(accept_spec(batch=6, B=(1, 3, 4), vocab=40000), seed=17)
+    the next call on the same workspace is correct (also with more
+    sequences than SMs: one finishing CTA per sequence)."""
+    w = synth.make(accept_spec(batch=batch, B=(1, 3, 4), vocab=40000), seed=17)
     dw = DeviceWorkload(w, with_verify=False)
     # a correct call first leaves real partials in the workspace
     st, n0, tok0, pos0 = run_rule(dw, rule, dw.cu_B, dw.tau, w.total_B, w.B_max)
