@@ -180,6 +180,7 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
   p->n_splits = (int)((max_keys + p->chunk - 1) / p->chunk);
   // every unit split alike, or none
   p->tail_from = p->n_splits > 1 ? 0 : (int)pairs;
+  p->tail_first = 0;
   p->s_tail = p->n_splits;
   p->chunk_tail = p->chunk;
   p->grid = (int)(pairs * p->n_splits);
@@ -197,6 +198,12 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
                           (double)(r * s) / (double)sms;
       if (tail < whole - 1e-9) {
         p->tail_from = (int)(W * sms);
+        // With few full waves the split units go first: the SMs that ran
+        // them then run whole units offset by a split, so the wave
+        // boundaries' ramps no longer coincide (64 x 4096: K2 208 -> 201
+        // us).  With many waves they go last, where they even out the end
+        // of a ragged batch (ragged 256: first, 716 -> 730 us).
+        p->tail_first = W <= 4;
         p->s_tail = (int)s;
         p->chunk_tail = (int)(per * kBlockKeys);
         p->n_splits = (int)((max_keys + p->chunk_tail - 1) / p->chunk_tail);
@@ -355,6 +362,7 @@ simsd_status simsd_verify_attn_timed(const simsd_verify_desc *d, void *stream_pt
   a.tail_from = p.tail_from;
   a.s_tail = p.s_tail;
   a.chunk_tail = p.chunk_tail;
+  a.tail_first = p.tail_first;
   a.row_tiles = p.row_tiles;
   a.rows_per_tile = p.rows_per_tile;
   a.sm_scale = d->sm_scale;

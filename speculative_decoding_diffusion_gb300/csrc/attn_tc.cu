@@ -143,13 +143,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sb + L::kOffMisc);
   int *flag_s = reinterpret_cast<int *>(sb + L::kOffMisc + 4);
 
-  // unit (sequence, KV head, row tile) in launch order, and its split: the
-  // first tail_from units whole, later ones in s_tail splits of chunk_tail
-  // keys
+  // unit (sequence, KV head, row tile) and split of this CTA: units from
+  // tail_from on run in s_tail splits of chunk_tail keys, the ones before
+  // whole.  The split units' CTAs come last in the grid (they even out the
+  // last wave), or first when the plan says so (tail_first: few full
+  // waves, where their SMs then run the whole units offset by a split, so
+  // the SMs' ramps at unit boundaries -- query rows, first copies -- no
+  // longer fall at the same time and DRAM stays busy through them).
   const int ci = blockIdx.x;
-  const bool tail = ci >= a.tail_from;
-  const int unit = tail ? a.tail_from + (ci - a.tail_from) / a.s_tail : ci;
-  const int split = tail ? (ci - a.tail_from) % a.s_tail : 0;
+  const int n_tail = (int)gridDim.x - a.tail_from;   // CTAs of split units
+  const bool tail = a.tail_first ? ci < n_tail : ci >= a.tail_from;
+  const int ti = a.tail_first ? ci : ci - a.tail_from;   // index among the split CTAs
+  const int unit = tail ? a.tail_from + ti / a.s_tail : (a.tail_first ? ci - n_tail : ci);
+  const int split = tail ? ti % a.s_tail : 0;
   const int chunk = tail ? a.chunk_tail : a.max_pages_per_seq * kPage;
   const int per_seq = a.Hkv * a.row_tiles;
   const int b = unit / per_seq;

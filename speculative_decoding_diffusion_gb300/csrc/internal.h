@@ -39,10 +39,12 @@ struct VerifyPlan {
   int key_splits;    // warps sharing one stage's keys (mma path)
   int chunk;         // keys per split (multiple of kBlockKeys)
   int n_splits;      // most splits of any unit (partials buffers)
-  // Units (sequence, KV head, row tile) in launch order: the first
-  // tail_from run whole, each later one in s_tail splits of chunk_tail
-  // keys (tail_from = 0: every unit split; tail_from = units: none)
+  // Units (sequence, KV head, row tile): the first tail_from run whole,
+  // each later one in s_tail splits of chunk_tail keys (tail_from = 0:
+  // every unit split; tail_from = units: none).  The split units' CTAs are
+  // launched after the whole ones, or before them when tail_first.
   int tail_from, s_tail, chunk_tail, grid;
+  int tail_first;
   // the split merge's rows: the last merge_rows of the T * Hq rows (the
   // split units' sequences are the last ones; all rows when every unit is
   // split)
@@ -85,6 +87,7 @@ struct AttnParams {
   int node_size;              // 0: SimSD's temporal layout; > 0: draft-graph nodes
   int chunk, rows_per_tile;
   int tail_from, s_tail, chunk_tail;   // as in VerifyPlan
+  int tail_first;             // as in VerifyPlan
   int row_tiles;
   uint32_t polls;             // bounded-wait polls (wait_polls_of the descriptor)
   float sm_scale;
