@@ -157,22 +157,30 @@ simsd_status verify_plan(const simsd_verify_desc *d, VerifyPlan *p) {
   }
   p->row_tiles = (p->M_max + p->rows_per_tile - 1) / p->rows_per_tile;
   // Split each sequence's keys into `splits` ranges of whole 128-key blocks.
-  // Cost model in block-times for one CTA per SM: waves x (blocks per CTA +
-  // fixed per-CTA cost ~1.5 blocks + 1 block of partial-output traffic when
-  // split) + the merge's read of the partials.  The longest possible
-  // sequence (the block-table width) stands for every sequence.
+  // Cost model in block-times (one 128-key block per SM with every SM
+  // streaming at the DRAM-bound rate; one CTA per SM): a wave of n CTAs of
+  // `per` blocks takes per * max(n / sms, kRho) -- DRAM-bound while at
+  // least kRho of the SMs stream, each SM at its own rate below that (kRho
+  // = K2's best GPU-wide rate, ~6.5 TB/s, over 152 SMs' own ~50 GB/s) --
+  // plus kRamp per wave (a CTA's setup and first copies, ~4.5 us) and, when
+  // split, the merge's read of the partials.  The longest possible sequence
+  // (the block-table width) stands for every sequence.  (On the 8 x 32768
+  // workload this picks 2 splits, one wave of 128 CTAs: K2 204 -> 188 us
+  // against the 7 splits in 3 waves an earlier model chose.)
   const int64_t max_keys = (int64_t)d->max_pages_per_seq * kPageTokens;
   const int64_t max_blocks = (max_keys + kBlockKeys - 1) / kBlockKeys;
   const int64_t pairs = (int64_t)d->batch * d->num_kv_heads * p->row_tiles;
   const int64_t sms = device_sm_count();
+  constexpr double kRho = 0.85, kRamp = 3.0;
   int64_t splits = 1;
   double best = 1e300;
   for (int64_t s = 1; s <= max_blocks && s <= 64; ++s) {
     const int64_t per = (max_blocks + s - 1) / s;
     if (s > 1 && (max_blocks + per - 1) / per < s) continue;   // same split as a smaller s
-    const double waves = (double)((pairs * s + sms - 1) / sms);
-    const double cost = waves * ((double)per + 1.5 + (s > 1 ? 1.0 : 0.0)) +
-                        (s > 1 ? (double)(pairs * s) / (double)sms : 0.0);
+    const int64_t ctas = pairs * s, full = ctas / sms, rest = ctas % sms;
+    double cost = (double)(full * per) + kRamp * (double)full;
+    if (rest > 0) cost += (double)per * std::max((double)rest / (double)sms, kRho) + kRamp;
+    if (s > 1) cost += (double)ctas / (double)sms;
     if (cost < best - 1e-9) { best = cost; splits = s; }
   }
   int64_t blocks_per_split = (max_blocks + splits - 1) / splits;
