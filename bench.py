@@ -569,14 +569,12 @@ def main():
     achieved = k2_bytes(w) / (k2_mean / 1e3) / 1e9
     traffic = recorded_traffic(w.spec)
     # K1, K2, K3 (only where a sequence's keys are split), and the
-    # acceptance: on the chunked path the chunk pass (K4a) and what follows
-    # it (K4b: the walk, the residual parts and the draw for the sampling
-    # rule; one finishing kernel for greedy and matching), else one cluster
-    # launch (K4a and K4b are reported only on the chunked path)
+    # acceptance: on the chunked path the chunk pass (K4a) and the one
+    # finishing kernel of the rule (K4b), else one cluster launch (K4a and
+    # K4b are reported only on the chunked path)
     chunked = args.accept_path == "auto"
     # (an event pair around no launch reads ~2 us; a K3 launch reads 6 us or more)
-    n_launch = (3 if float(np.median(k_ms["K3"])) > 0.004 else 2) + \
-        ((4 if args.accept == "sample" else 2) if chunked else 1)
+    n_launch = (3 if float(np.median(k_ms["K3"])) > 0.004 else 2) + (2 if chunked else 1)
     if not chunked:
         del k_ms["K4a"], k_ms["K4b"]
     kernels = {n: {"ms": float(np.mean(t))} for n, t in k_ms.items()}

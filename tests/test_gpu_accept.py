@@ -346,3 +346,34 @@ def test_sample_matching_matches_oracle(name, T, path):
     print("%s T=%g %s: %d sequences, %d with a tie-zone draw" % (name, T, path, len(w.lens), ties))
     assert ties <= parity.max_ties(len(w.lens))
     assert (n > 0).any()
+
+
+def test_rules_alternate_on_one_workspace():
+    """Sampling, greedy, matching and sampling again on one workspace (the
+    chunk pass's control words and counters shared between the calls):
+    every call equals the same call on a fresh zeroed workspace."""
+    w = variant_case("bf16-1003")
+    dw = DeviceWorkload(w, with_verify=False)
+    shared = torch.zeros_like(dw.accept_ws)
+
+    def call(rule, ws):
+        greedy = rule == binding.SIMSD_ACCEPT_GREEDY
+        for t in (dw.n_accept, dw.token, dw.pos):
+            t.fill_(-7)
+        binding.accept(dw.target, dw.draft if rule == binding.SIMSD_ACCEPT_SAMPLE else None,
+                       dw.draft_tokens, dw.tau, dw.cu_B, None if greedy else dw.uniforms,
+                       dw.n_accept, dw.token, dw.pos, ws, dw.total_B, dw.B_max, rule=rule)
+        torch.cuda.synchronize()
+        return [t.cpu().numpy().copy() for t in (dw.n_accept, dw.token, dw.pos)]
+
+    # (the shared workspace's status is read only at the end: reading it
+    # would also clear the control words the calls must reset themselves)
+    for rule in (binding.SIMSD_ACCEPT_SAMPLE, binding.SIMSD_ACCEPT_GREEDY, binding.SIMSD_ACCEPT_MATCH,
+                 binding.SIMSD_ACCEPT_SAMPLE):
+        got = call(rule, shared)
+        fresh = torch.zeros_like(dw.accept_ws)
+        ref = call(rule, fresh)
+        assert binding.read_status(fresh) == 0
+        for g, r in zip(got, ref):
+            np.testing.assert_array_equal(g, r)
+    assert binding.read_status(shared) == 0
