@@ -74,13 +74,15 @@ def test_odd_vocab_and_mixed_B(dtype, vocab, path):
 
 
 @pytest.mark.parametrize("dtype,vocab,batch,B", [("bf16", 151936, 2, 32), ("bf16", 65539, 3, 32),
-                                                 ("f32", 100003, 4, 17), ("bf16", 151936, 5, 1)])
+                                                 ("f32", 100003, 4, 17), ("bf16", 151936, 5, 1),
+                                                 ("f32", 1 << 21, 2, 2), ("bf16", 1 << 21, 2, 3)])
 @pytest.mark.parametrize("path", PATHS)
 def test_few_sequences_large_clusters(dtype, vocab, batch, B, path):
     """Few sequences get the largest clusters (up to 16 CTAs each): slices
     of 1/16 of the vocabulary, the slice merge in 16-lane groups and, at
     B = 32, in two rounds of pairs; element copies where rows are not
-    16-byte multiples."""
+    16-byte multiples.  The largest vocabulary (2^21) gives the chunked
+    path's merges and part searches more parts than a warp holds."""
     w = synth.make(tiny_accept_spec(batch=batch, B=B, dtype=dtype, vocab=vocab), seed=vocab + B)
     n, tok, pos = run_accept(w, path)
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
