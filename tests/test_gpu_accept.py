@@ -253,12 +253,13 @@ def variant_case(name):
     if name == "sdar8b":
         return synth.config(1)
     dtype, vocab, batch = {"bf16-1003": ("bf16", 1003, 64), "f32-777": ("f32", 777, 64),
-                           "bf16-few": ("bf16", 151936, 3), "f32-odd": ("f32", 100003, 5)}[name]
+                           "bf16-few": ("bf16", 151936, 3), "f32-odd": ("f32", 100003, 5),
+                           "f32-max": ("f32", 1 << 21, 2)}[name]
     return synth.make(tiny_accept_spec(batch=batch, dtype=dtype, vocab=vocab), seed=vocab + batch)
 
 
 @pytest.mark.parametrize("path", RULE_PATHS)
-@pytest.mark.parametrize("name", ["sdar8b", "bf16-1003", "f32-777", "bf16-few", "f32-odd"])
+@pytest.mark.parametrize("name", ["sdar8b", "bf16-1003", "f32-777", "bf16-few", "f32-odd", "f32-max"])
 def test_greedy_matches_oracle(name, path):
     """The greedy rule: accepted lengths, positions and tokens bit-exact
     against the oracle (argmax over the same bf16 / fp32 values, the
@@ -326,7 +327,7 @@ def check_match(w, n, tok, pos, temperature=1.0, tie=parity.TIE_RESIDUAL):
 
 @pytest.mark.parametrize("path", RULE_PATHS)
 @pytest.mark.parametrize("name,T", [("sdar8b", 1.0), ("bf16-1003", 1.0), ("f32-777", 0.875),
-                                    ("bf16-few", 1.0), ("f32-odd", 1.25)])
+                                    ("bf16-few", 1.0), ("f32-odd", 1.25), ("f32-max", 1.0)])
 def test_sample_matching_matches_oracle(name, T, path):
     """Sample matching (accept iff the target's own inverse-CDF sample at
     u[t-1] equals the draft token; the rejection emits that sample): exact

@@ -142,6 +142,21 @@ def test_draft_step_chunked_mixed_B_and_vocab(dtype, vocab, T):
     assert ties[0] <= parity.max_ties(w.total_B) and ties[1] <= parity.max_ties(len(w.lens))
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_draft_step_chunked_largest_vocabulary(dtype):
+    """The largest vocabulary (2^21): more parts per row than a warp holds
+    in the merge and in the part search."""
+    vocab = 1 << 21
+    w = synth.make(loop_spec(dtype=dtype, vocab=vocab, batch=2, B=(2, 5)), seed=33)
+    u = np.random.default_rng(34).random((len(w.lens), w.B_max), dtype=np.float32)
+    st, tok, tau, conf = draft_on_gpu(w, to_device(w.draft, "cuda"), u, chunked=True)
+    assert st == 0
+    d64 = synth.to_f64(w.draft)
+    ref = oracle.draft_step(w.cu_B, d64, u)
+    ties = check_draft(w, d64, u, tok, tau, conf, ref)
+    assert ties[0] <= parity.max_ties(w.total_B) and ties[1] <= parity.max_ties(len(w.lens))
+
+
 @pytest.mark.parametrize("dtype,vocab,T", [("bf16", 1000, 1.0), ("f32", 777, 0.75),
                                            ("bf16", 151936, 1.0), ("bf16", 4096 + 8, 1.25)])
 def test_draft_step_with_decided_slots(dtype, vocab, T):
