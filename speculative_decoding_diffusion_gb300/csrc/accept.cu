@@ -800,10 +800,15 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
       const uint4 *sv = reinterpret_cast<const uint4 *>(smem + s * kStage);
       const int v0 = warp * kWarpVecs;              // this warp's vectors: v0 + v * 32 + lane
       uint4 w[kV];
+      if (n == kChunk) {                            // a whole chunk: no bound checks
 #pragma unroll
-      for (int v = 0; v < kV; ++v) {
-        const int idx = v0 + v * 32 + lane;
-        w[v] = idx * N < n ? sv[idx] : Ld<T>::neg_inf();
+        for (int v = 0; v < kV; ++v) w[v] = sv[v0 + v * 32 + lane];
+      } else {
+#pragma unroll
+        for (int v = 0; v < kV; ++v) {
+          const int idx = v0 + v * 32 + lane;
+          w[v] = idx * N < n ? sv[idx] : Ld<T>::neg_inf();
+        }
       }
       // the logit at the slot's draft token, if this warp's part holds it
       const int off = kToken ? stage_x[s] - c * kChunk : -1;
