@@ -1047,7 +1047,7 @@ cudaError_t launch_chunks(const ChunkParams &c, cudaStream_t stream) {
 // m(x); with U = u S the step accepts iff Pre(x) <= U < Pre(x) + m(x).  A
 // slot that rejects draws the target's own token at U at once (part_draw:
 // the part holding U, then a column scan), so the walk -- warp 0, over
-// every slot's verdict -- only picks the first rejected step's result.
+// every slot's outcome -- only picks the first rejected step's result.
 constexpr int kRuleThreads = 512;
 constexpr int kRuleWarps = kRuleThreads / 32;
 
