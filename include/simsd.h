@@ -236,8 +236,10 @@ simsd_status simsd_prompt_append(const simsd_append_desc *d, void *stream);
  * step t draws the target's own token y from p (at temperature T) by
  * inverse CDF with u[t-1] and accepts iff y = x; the first rejection emits
  * y (u[B_b] unused, draft logits not read and may be NULL).
- * Kernels: K4a, a chunk pass over (row, 32 KB chunk) items on every SM,
- * writes per eighth of a chunk (a "part") its maximum and sum of
+ * Kernels: K4a, a chunk pass over (row, 32 KB chunk) items on every SM
+ * (for the sampling rule's small batches a pass that loads each part
+ * directly, a warp per part), writes per eighth of a chunk (a "part") its
+ * maximum and sum of
  * exponentials -- of both rows of every slot for the sampling rule; of the
  * target rows and the mass below the draft token for sample matching; the
  * largest value and its index for the greedy rule -- and the logits at the
@@ -314,7 +316,9 @@ typedef struct {
                                  divided by this float's exact value         */
   int32_t wait_polls;         /* as in simsd_verify_desc; a sequence whose
                                  wait gave up gets n_accept = 0, token = -1,
-                                 pos = -1                                    */
+                                 pos = -1 (the sampling rule's chunk pass for
+                                 small batches and the finishing kernels have
+                                 no waits)                                   */
   const int32_t *decided;     /* device int32[batch] or NULL (all 0): steps
                                  1..decided[b] belong to positions decided
                                  in earlier passes of the block (the

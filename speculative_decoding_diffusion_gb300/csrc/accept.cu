@@ -901,6 +901,109 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
   }
 }
 
+// The sampling rule's chunk pass for small batches: no ring, a warp per
+// part (1/8 of a 32 KB chunk of one row) with its 16-byte loads issued at
+// once, as many warps as the device holds looping over the parts -- so a
+// batch of a few thousand parts is requested from memory in one go instead
+// of three ring stages at a time per CTA.  Each warp reduces its part
+// exactly as a consumer warp of the ring kernel does (the same loads, the
+// same order of operations), so the partials are the same bits.
+constexpr int kPartThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kPartThreads)
+vocab_part_kernel(const __grid_constant__ ChunkParams a) {
+  constexpr int N = Ld<T>::N;
+  constexpr int kChunk = chunk_entries<T>();
+  constexpr int kWarpVecs = kStageBytes / 16 / kAConsumerWarps;   // a part's vectors
+  constexpr int kV = kWarpVecs / 32;
+  grid_dep_launch();                           // the kernel after it may be scheduled
+  if (a.zero != nullptr)                       // counters the kernel after it starts from
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero; i += gridDim.x * blockDim.x)
+      a.zero[i] = 0;
+  const int lane = threadIdx.x & 31;
+  const long parts = 2L * a.total_B * a.nchunks * kAConsumerWarps;
+  const long nwarps = (long)gridDim.x * (kPartThreads / 32);
+#pragma unroll 1
+  for (long pi = (long)blockIdx.x * (kPartThreads / 32) + (threadIdx.x >> 5); pi < parts; pi += nwarps) {
+    const int pw = (int)(pi % kAConsumerWarps);                // the part within its chunk
+    const long i = pi / kAConsumerWarps;                       // the (row pair, chunk) item
+    const long p = i / a.nchunks;                              // row pair: slot p/2, target or draft
+    const int c = (int)(i % a.nchunks);
+    const int n = min(kChunk, a.vocab - c * kChunk);
+    const T *src = (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab + (long)c * kChunk;
+    const int v0 = pw * kWarpVecs;
+    uint4 w[kV];
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+      const int idx = v0 + v * 32 + lane;
+      w[v] = idx * N < n ? Ld<T>::load(src + idx * N, n - idx * N, a.bulk != 0) : Ld<T>::neg_inf();
+    }
+    // the logit at the slot's draft token, if this part holds it
+    const int off = __ldg(a.draft_tokens + (p >> 1)) - c * kChunk;
+    if (off >= 0 && off < n && off / N >= v0 && off / N < v0 + kWarpVecs && (off / N - v0) % 32 == lane) {
+      const int vx = (off / N - v0) / 32;
+      uint4 wx = w[0];
+#pragma unroll
+      for (int v = 1; v < kV; ++v)
+        if (v == vx) wx = w[v];
+      a.xlogit[p] = pick<T>(wx, off % N);
+    }
+    const float mx = Ld<T>::vmax(w, kV);
+    const uint32_t mu = __float_as_uint(mx);
+    const uint32_t km = __reduce_max_sync(0xffffffffu, (mu & 0x80000000u) ? ~mu : (mu | 0x80000000u));
+    const float wmax = __uint_as_float((km & 0x80000000u) ? (km & 0x7fffffffu) : ~km);
+    const float R = ref_of(wmax, a.ls);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (R != -INFINITY) {
+#pragma unroll
+      for (int v = 0; v < kV; ++v) {
+        float f[N];
+        Ld<T>::unpack(w[v], f);
+#pragma unroll
+        for (int e = 0; e < N; ++e) acc[(v * N + e) & 3] += rel_exp(f[e], R, a.ls);
+      }
+    }
+    float sm = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    if (lane == 0) a.part[(p * a.nchunks + c) * kAConsumerWarps + pw] = make_float2(R, sm);
+  }
+}
+
+// Parts per resident warp up to which the sampling rule's chunk pass takes
+// the ring-free kernel above (an A/B on one GPU: 16 x 1024, 2.1 parts per
+// warp, step 59.4 -> 55.9 us; 8 x 32768, 4.2, 230.3 -> 226.6 us; 64 x 4096,
+// 16.8, 288.3 -> 290.7 us, so the ring keeps that one).  The ring-free
+// kernel has no bounded waits.
+constexpr double kDirectPartsPerWarp = 6.0;
+
+template <typename T>
+cudaError_t launch_parts(const ChunkParams &c, cudaStream_t stream, bool *taken) {
+  static std::mutex mu;
+  static int resident[64] = {0};
+  const int dev = current_device();
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (resident[dev] == 0) {
+      int n = 0;
+      cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, vocab_part_kernel<T>, kPartThreads, 0);
+      if (e != cudaSuccess) return e;
+      resident[dev] = n > 0 ? n : 1;
+    }
+    per_sm = resident[dev];
+  }
+  const long parts = 2L * c.total_B * c.nchunks * kAConsumerWarps;
+  const long ctas = (long)per_sm * device_sm_count();
+  *taken = (double)parts <= kDirectPartsPerWarp * (double)(ctas * (kPartThreads / 32));
+  if (!*taken) return cudaSuccess;
+  const long grid = std::min<long>(ctas, (parts + kPartThreads / 32 - 1) / (kPartThreads / 32));
+  vocab_part_kernel<T><<<(unsigned)grid, kPartThreads, 0, stream>>>(c);
+  return cudaGetLastError();
+}
+
 // The cluster kernel's instance: consumer warps, ring stages, threads and
 // shared memory.
 template <int NW, int NS>
@@ -2197,7 +2300,10 @@ simsd_status run_accept(const simsd_accept_desc *d, char *ws, size_t ws_bytes,
     f.nchunks = L.nchunks;
     f.bulk = a.bulk;
     f.ls = a.ls;
-    e = bf16 ? launch_chunks<__nv_bfloat16, kModeSample>(c, stream) : launch_chunks<float, kModeSample>(c, stream);
+    bool direct = false;
+    e = bf16 ? launch_parts<__nv_bfloat16>(c, stream, &direct) : launch_parts<float>(c, stream, &direct);
+    if (e == cudaSuccess && !direct)
+      e = bf16 ? launch_chunks<__nv_bfloat16, kModeSample>(c, stream) : launch_chunks<float, kModeSample>(c, stream);
     mark(events, 1, stream);
     if (e == cudaSuccess)
       e = bf16 ? launch_sample_finish<__nv_bfloat16>(f, stream) : launch_sample_finish<float>(f, stream);

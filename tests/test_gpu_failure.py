@@ -168,7 +168,9 @@ def test_verify_wait_that_gives_up_returns_a_status():
 
 
 def test_accept_wait_that_gives_up_returns_a_status():
-    w = synth.config(1)
+    # a batch whose sampling chunk pass runs the ring (the ring-free pass
+    # for small batches has no bounded waits)
+    w = synth.make(accept_spec(batch=64, B=8, vocab=151936), seed=2)
     dw = DeviceWorkload(w, with_verify=False)
     args = (dw.target, dw.draft, dw.draft_tokens, dw.tau, dw.cu_B, dw.uniforms,
             dw.n_accept, dw.token, dw.pos, dw.accept_ws, dw.total_B, dw.B_max)
@@ -186,16 +188,33 @@ def test_accept_wait_that_gives_up_returns_a_status():
     parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
 
 
-@pytest.mark.parametrize("rule,batch", [(binding.SIMSD_ACCEPT_GREEDY, 6), (binding.SIMSD_ACCEPT_MATCH, 6),
-                                        (binding.SIMSD_ACCEPT_SAMPLE, 6), (binding.SIMSD_ACCEPT_SAMPLE, 200)])
-def test_chunk_pass_that_gives_up_means_no_walk(rule, batch):
+def test_small_sampling_batches_have_no_bounded_waits():
+    """The sampling rule's chunk pass for small batches loads each part
+    directly (no ring, no waits) and the finishing kernel waits on nothing
+    either: with every wait set to give up at once, the call still returns
+    the oracle's decisions and no timeout bit."""
+    w = synth.config(1)
+    dw = DeviceWorkload(w, with_verify=False)
+    binding.accept(dw.target, dw.draft, dw.draft_tokens, dw.tau, dw.cu_B, dw.uniforms,
+                   dw.n_accept, dw.token, dw.pos, dw.accept_ws, dw.total_B, dw.B_max, wait_polls=-1)
+    torch.cuda.synchronize()
+    assert binding.read_status(dw.accept_ws) == 0
+    n, tok, pos = dw.n_accept.cpu().numpy(), dw.token.cpu().numpy(), dw.pos.cpu().numpy()
+    parity.check_accept(w, parity.oracle_accept(w), n, tok, pos)
+
+
+@pytest.mark.parametrize("rule,batch,vocab", [(binding.SIMSD_ACCEPT_GREEDY, 6, 40000),
+                                              (binding.SIMSD_ACCEPT_MATCH, 6, 40000),
+                                              (binding.SIMSD_ACCEPT_SAMPLE, 200, 151936)])
+def test_chunk_pass_that_gives_up_means_no_walk(rule, batch, vocab):
     """The chunked path with every wait giving up at once: the chunk pass
     raises its give-up flag, so the kernel after it reports "no walk" for
     every sequence (whatever stale partials the workspace holds) and sets
     the timeout bit; it puts the chunk pass's control words back to zero, so
     the next call on the same workspace is correct (also with more
-    sequences than SMs: one finishing CTA per sequence)."""
-    w = synth.make(accept_spec(batch=batch, B=(1, 3, 4), vocab=40000), seed=17)
+    sequences than SMs: one finishing CTA per sequence).  The sampling case
+    is a batch large enough for the ring."""
+    w = synth.make(accept_spec(batch=batch, B=(1, 3, 4), vocab=vocab), seed=17)
     dw = DeviceWorkload(w, with_verify=False)
     # a correct call first leaves real partials in the workspace
     st, n0, tok0, pos0 = run_rule(dw, rule, dw.cu_B, dw.tau, w.total_B, w.B_max)
