@@ -922,22 +922,30 @@ vocab_part_kernel(const __grid_constant__ ChunkParams a) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < a.n_zero; i += gridDim.x * blockDim.x)
       a.zero[i] = 0;
   const int lane = threadIdx.x & 31;
-  const long parts = 2L * a.total_B * a.nchunks * kAConsumerWarps;
-  const long nwarps = (long)gridDim.x * (kPartThreads / 32);
+  // fewer than 2^31 parts (the launch checks): 32-bit index arithmetic
+  const unsigned parts = 2u * (unsigned)a.total_B * (unsigned)a.nchunks * kAConsumerWarps;
+  const unsigned nwarps = gridDim.x * (kPartThreads / 32);
+  const unsigned nch = (unsigned)a.nchunks;
 #pragma unroll 1
-  for (long pi = (long)blockIdx.x * (kPartThreads / 32) + (threadIdx.x >> 5); pi < parts; pi += nwarps) {
+  for (unsigned pi = blockIdx.x * (kPartThreads / 32) + (threadIdx.x >> 5); pi < parts; pi += nwarps) {
     const int pw = (int)(pi % kAConsumerWarps);                // the part within its chunk
-    const long i = pi / kAConsumerWarps;                       // the (row pair, chunk) item
-    const long p = i / a.nchunks;                              // row pair: slot p/2, target or draft
-    const int c = (int)(i % a.nchunks);
+    const unsigned i = pi / kAConsumerWarps;                   // the (row pair, chunk) item
+    const unsigned p = i / nch;                                // row pair: slot p/2, target or draft
+    const int c = (int)(i - p * nch);
     const int n = min(kChunk, a.vocab - c * kChunk);
-    const T *src = (const T *)((p & 1) ? a.draft : a.target) + (p >> 1) * a.vocab + (long)c * kChunk;
+    const T *src = (const T *)((p & 1) ? a.draft : a.target) + (size_t)(p >> 1) * a.vocab + (size_t)c * kChunk;
     const int v0 = pw * kWarpVecs;
     uint4 w[kV];
+    if (n == kChunk && a.bulk != 0) {          // a whole chunk of 16-byte rows: no bound checks
 #pragma unroll
-    for (int v = 0; v < kV; ++v) {
-      const int idx = v0 + v * 32 + lane;
-      w[v] = idx * N < n ? Ld<T>::load(src + idx * N, n - idx * N, a.bulk != 0) : Ld<T>::neg_inf();
+      for (int v = 0; v < kV; ++v)
+        w[v] = *reinterpret_cast<const uint4 *>(src + (v0 + v * 32 + lane) * N);
+    } else {
+#pragma unroll
+      for (int v = 0; v < kV; ++v) {
+        const int idx = v0 + v * 32 + lane;
+        w[v] = idx * N < n ? Ld<T>::load(src + idx * N, n - idx * N, a.bulk != 0) : Ld<T>::neg_inf();
+      }
     }
     // the logit at the slot's draft token, if this part holds it
     const int off = __ldg(a.draft_tokens + (p >> 1)) - c * kChunk;
@@ -997,7 +1005,8 @@ cudaError_t launch_parts(const ChunkParams &c, cudaStream_t stream, bool *taken)
   }
   const long parts = 2L * c.total_B * c.nchunks * kAConsumerWarps;
   const long ctas = (long)per_sm * device_sm_count();
-  *taken = (double)parts <= kDirectPartsPerWarp * (double)(ctas * (kPartThreads / 32));
+  *taken = (double)parts <= kDirectPartsPerWarp * (double)(ctas * (kPartThreads / 32)) &&
+           parts < (1L << 31);
   if (!*taken) return cudaSuccess;
   const long grid = std::min<long>(ctas, (parts + kPartThreads / 32 - 1) / (kPartThreads / 32));
   vocab_part_kernel<T><<<(unsigned)grid, kPartThreads, 0, stream>>>(c);

@@ -132,56 +132,85 @@ attn_f32_kernel(const __grid_constant__ AttnParams a) {
 // K3: O = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s, one warp per
 // (token, query head) row, each lane a contiguous hd/32 columns (8- or
 // 16-byte loads); rows of units that ran whole were finished by the
-// attention kernel.  The partials of the first kMergeBatch splits are
-// requested before the row's split count is known (the buffer holds every
-// split of every row, so the reads stay in it; the extra ones are
-// dropped), so a merge of up to kMergeBatch splits costs one round trip.
-// Whether a row's unit was split comes from the append kernel's per-token
-// record.
-constexpr int kMergeBatch = 8;
+// attention kernel.  The grid is (token, group of kMergeRowsPerCta heads),
+// so a row needs no division to find its token.  The partials of the first
+// MB splits (MB = 2, 4 or 8: the plan's split count rounded up, at most 8)
+// are requested before the row's split count is known (the buffer holds
+// every split of every row, so the reads stay in it; the extra ones are
+// dropped), so a merge of up to MB splits costs one round trip, and the
+// max and sum reductions run over MB lanes only.  Whether a row's unit was
+// split comes from the append kernel's per-token record.
 constexpr int kMergeThreads = 256;
 constexpr int kMergeRowsPerCta = kMergeThreads / 32;
 
+template <typename T, int PER> struct MergeOut;
+template <> struct MergeOut<float, 4> {
+  static __device__ __forceinline__ void store(float *p, const float *o) {
+    *reinterpret_cast<float4 *>(p) = make_float4(o[0], o[1], o[2], o[3]);
+  }
+};
+template <> struct MergeOut<float, 2> {
+  static __device__ __forceinline__ void store(float *p, const float *o) {
+    *reinterpret_cast<float2 *>(p) = make_float2(o[0], o[1]);
+  }
+};
+template <> struct MergeOut<__nv_bfloat16, 4> {
+  static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float *o) {
+    *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]));
+  }
+};
+template <> struct MergeOut<__nv_bfloat16, 2> {
+  static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float *o) {
+    *reinterpret_cast<uint32_t *>(p) = pack_bf16x2(o[0], o[1]);
+  }
+};
+
 // four CTAs (32 rows) per SM without spills: lane s keeps split s's
 // (max, sum) and its weight is broadcast when the partials are summed
-template <typename T, int HD>
+template <typename T, int HD, int MB>
 __global__ void __launch_bounds__(kMergeThreads, 4)
-combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long row0, int max_splits) {
+combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, int tok0, int max_splits) {
   constexpr int PER = HD / 32;               // 4 or 2 columns per lane
   using V = typename std::conditional<PER == 4, float4, float2>::type;
   grid_dep_wait();                           // partials come from the attention kernel
-  const long row = row0 + (long)blockIdx.x * kMergeRowsPerCta + threadIdx.x / 32;
-  const int lane = threadIdx.x % 32, col = lane * PER;
-  if (row >= (long)a.T * a.Hq) return;
-  const long stride = (long)a.T * a.Hq;
+  const int hq = blockIdx.y * kMergeRowsPerCta + threadIdx.x / 32;
+  if (hq >= a.Hq) return;
+  const int tok = tok0 + (int)blockIdx.x, lane = threadIdx.x % 32;
+  const size_t stride = (size_t)a.T * a.Hq;  // rows per split
+  const size_t row = (size_t)tok * a.Hq + hq;
+  const V *src = reinterpret_cast<const V *>(a.o_part + row * HD) + lane;
+  const float2 *ml_src = a.ml_part + row;
+  const size_t vstep = stride * (HD / PER);  // one split, in V units
   auto load_batch = [&](int s0, int n, V *v, float2 &ml) {
 #pragma unroll
-    for (int s = 0; s < kMergeBatch; ++s)
-      if (s < n) v[s] = __ldcg(reinterpret_cast<const V *>(a.o_part + ((s0 + s) * stride + row) * HD + col));
-    ml = lane < n ? __ldcg(a.ml_part + (s0 + lane) * stride + row) : make_float2(-INFINITY, 0.f);
+    for (int s = 0; s < MB; ++s)
+      if (s < n) v[s] = __ldcg(src + (size_t)(s0 + s) * vstep);
+    ml = lane < n ? __ldcg(ml_src + (size_t)(s0 + lane) * stride) : make_float2(-INFINITY, 0.f);
   };
   // the first batch, requested with the row's record
-  V v[kMergeBatch];
+  V v[MB];
   float2 ml;
-  load_batch(0, min(kMergeBatch, max_splits), v, ml);
+  load_batch(0, min(MB, max_splits), v, ml);
   // the row's unit (sequence, KV head, row tile) and whether it was split
-  const int4 ti = __ldg(tok_info + row / a.Hq);   // keys 0: a malformed sequence (skipped)
-  const int hq = (int)(row % a.Hq);
-  const int rtile = (ti.z * a.G + hq % a.G) / a.rows_per_tile;
-  const int unit = ti.y + rtile * a.Hkv + hq / a.G;
+  const int4 ti = __ldg(tok_info + tok);     // keys 0: a malformed sequence (skipped)
+  const int g = hq / a.G;
+  const int rtile = (ti.z * a.G + (hq - g * a.G)) / a.rows_per_tile;
+  const int unit = ti.y + rtile * a.Hkv + g;
   const int ns = unit >= a.tail_from ? (ti.x + a.chunk_tail - 1) / a.chunk_tail : 1;
   if (ns <= 1) return;
   float mstar = -INFINITY, den = 0.f, o[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) o[i] = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += kMergeBatch) {
-    const int n = min(kMergeBatch, ns - s0);
+  for (int s0 = 0; s0 < ns; s0 += MB) {
+    const int n = min(MB, ns - s0);
     if (s0 > 0) load_batch(s0, n, v, ml);
     if (lane >= n) ml = make_float2(-INFINITY, 0.f);   // splits past the row's own
+    // lanes [0, MB) hold the batch: reduce within groups of MB lanes and
+    // take lane 0's
     float mb = ml.x;
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, m));
-    mb = fmaxf(mb, mstar);
+    for (int m = MB / 2; m > 0; m >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, m));
+    mb = fmaxf(__shfl_sync(0xffffffffu, mb, 0), mstar);
     if (mb > mstar && mstar != -INFINITY) {  // a later batch raised the reference
       const float r = exp2f(mstar - mb);
       den *= r;
@@ -193,10 +222,10 @@ combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long 
     const float wl = lane < n ? exp2f(ml.x - mu) : 0.f;   // lane s: split s's weight
     float dl = wl * ml.y;
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, m);
-    den += dl;
+    for (int m = MB / 2; m > 0; m >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, m);
+    den += __shfl_sync(0xffffffffu, dl, 0);
 #pragma unroll
-    for (int s = 0; s < kMergeBatch; ++s) {
+    for (int s = 0; s < MB; ++s) {
       const float w = __shfl_sync(0xffffffffu, wl, s);
       if (s < n) {
         const float *vf = reinterpret_cast<const float *>(&v[s]);
@@ -206,9 +235,19 @@ combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, long 
     }
   }
   const float inv = 1.f / den;
-  T *out = (T *)a.out + row * HD + col;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) Elem<T>::store(out + i, o[i] * inv);
+  for (int i = 0; i < PER; ++i) o[i] *= inv;
+  MergeOut<T, PER>::store((T *)a.out + row * HD + lane * PER, o);
+}
+
+template <typename T, int HD>
+cudaError_t launch_combine_t(dim3 grid, cudaStream_t stream, const AttnParams &a,
+                             const int4 *ts, int tok0, int n_splits) {
+  if (n_splits <= 2)
+    return launch_pdl(combine_kernel<T, HD, 2>, grid, dim3(kMergeThreads), 0, stream, a, ts, tok0, n_splits);
+  if (n_splits <= 4)
+    return launch_pdl(combine_kernel<T, HD, 4>, grid, dim3(kMergeThreads), 0, stream, a, ts, tok0, n_splits);
+  return launch_pdl(combine_kernel<T, HD, 8>, grid, dim3(kMergeThreads), 0, stream, a, ts, tok0, n_splits);
 }
 
 }  // namespace
@@ -226,17 +265,18 @@ cudaError_t launch_attn_f32(const simsd_verify_desc *d, const VerifyPlan &p,
 cudaError_t launch_combine(const simsd_verify_desc *d, const VerifyPlan &p,
                            const AttnParams &a, const int4 *tok_info,
                            cudaStream_t stream) {
-  const long rows = (long)p.merge_rows;
-  const long row0 = (long)p.T * d->num_q_heads - rows;
-  const unsigned blocks = (unsigned)((rows + kMergeRowsPerCta - 1) / kMergeRowsPerCta);
-  const int4 *ts = tok_info;
+  // merge_rows is a whole number of tokens (the last ones)
+  const int tokens = (int)(p.merge_rows / d->num_q_heads);
+  const int tok0 = p.T - tokens;
+  const dim3 grid((unsigned)tokens, (unsigned)((d->num_q_heads + kMergeRowsPerCta - 1) / kMergeRowsPerCta));
+  if (tokens == 0) return cudaSuccess;
   if (d->dtype == SIMSD_BF16)
     return d->head_dim == 128
-               ? launch_pdl(combine_kernel<__nv_bfloat16, 128>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0, p.n_splits)
-               : launch_pdl(combine_kernel<__nv_bfloat16, 64>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0, p.n_splits);
+               ? launch_combine_t<__nv_bfloat16, 128>(grid, stream, a, tok_info, tok0, p.n_splits)
+               : launch_combine_t<__nv_bfloat16, 64>(grid, stream, a, tok_info, tok0, p.n_splits);
   return d->head_dim == 128
-             ? launch_pdl(combine_kernel<float, 128>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0, p.n_splits)
-             : launch_pdl(combine_kernel<float, 64>, dim3(blocks), dim3(kMergeThreads), 0, stream, a, ts, row0, p.n_splits);
+             ? launch_combine_t<float, 128>(grid, stream, a, tok_info, tok0, p.n_splits)
+             : launch_combine_t<float, 64>(grid, stream, a, tok_info, tok0, p.n_splits);
 }
 
 }  // namespace simsd
