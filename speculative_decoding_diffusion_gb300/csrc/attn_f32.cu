@@ -165,10 +165,11 @@ template <> struct MergeOut<__nv_bfloat16, 2> {
   }
 };
 
-// four CTAs (32 rows) per SM without spills: lane s keeps split s's
-// (max, sum) and its weight is broadcast when the partials are summed
+// four CTAs (32 rows) per SM without spills, eight (64 rows: 9728 rows in
+// one wave) for batches of two splits: lane s keeps split s's (max, sum)
+// and its weight is broadcast when the partials are summed
 template <typename T, int HD, int MB>
-__global__ void __launch_bounds__(kMergeThreads, 4)
+__global__ void __launch_bounds__(kMergeThreads, MB <= 2 ? 8 : 4)
 combine_kernel(const __grid_constant__ AttnParams a, const int4 *tok_info, int tok0, int max_splits) {
   constexpr int PER = HD / 32;               // 4 or 2 columns per lane
   using V = typename std::conditional<PER == 4, float4, float2>::type;

@@ -57,14 +57,15 @@ template <> struct Vec<__nv_bfloat16> {
 
 // Rotate `heads` rows of hd elements from src into dst (row h at h*hd; dst
 // rows at dst_stride apart) with the angles in cs.  Each thread loads a
-// batch of its vectors before storing any, so the loads are in flight
-// together rather than serialised behind possibly aliasing stores.
-template <typename T>
+// batch of its vectors before storing any, so global loads are in flight
+// together rather than serialised behind possibly aliasing stores (a
+// source in shared memory takes BATCH 1: fewer registers, more CTAs).
+template <typename T, int BATCH>
 __device__ __forceinline__ void rotate_rows(const T *__restrict__ src, T *__restrict__ dst,
                                             int heads, int hd, long dst_stride,
                                             const float2 *cs) {
   using VT = Vec<T>;
-  constexpr int N = VT::N, BATCH = 4;
+  constexpr int N = VT::N;
   const int half = hd / 2;
   const int per_head = half / N;  // vector pairs per head
   const int items = heads * per_head;
@@ -100,11 +101,11 @@ __device__ __forceinline__ void rotate_rows(const T *__restrict__ src, T *__rest
   }
 }
 
-template <typename T>
+template <typename T, int BATCH>
 __device__ __forceinline__ void copy_rows(const T *__restrict__ src, T *__restrict__ dst,
                                           int heads, int hd, long dst_stride) {
   using VT = Vec<T>;
-  constexpr int N = VT::N, BATCH = 4;
+  constexpr int N = VT::N;
   const int per_head = hd / N;
   const int items = heads * per_head;
   for (int i0 = threadIdx.x; i0 < items; i0 += BATCH * blockDim.x) {
@@ -153,8 +154,10 @@ struct RopeVerifyArgs {
 // launch) fit on the same SMs as this kernel's
 constexpr int kStageSeqs = 512;
 
+// 16 CTAs (2048 threads) per SM at bf16 (32 registers, no spills): a batch
+// of a few thousand new tokens runs in about one wave of CTAs
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 16 : 12)
 rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
   extern __shared__ __align__(16) uint8_t rows_s[];   // raw q | k | v rows of the token
   __shared__ float2 cs[64];
@@ -179,8 +182,30 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
   // sequence of the token: cu_B (and lens) staged once, searched in smem
   int b, c0, B, P;
   if (a.batch <= kStageSeqs) {
-    for (int i = threadIdx.x; i <= a.batch; i += blockDim.x) cu_s[i] = __ldg(a.cu_B + i);
-    for (int i = threadIdx.x; i < a.batch; i += blockDim.x) lens_s[i] = __ldg(a.lens + i);
+    // every load is issued before the first store to shared memory, so the
+    // staging costs one round trip, not one per loop step
+    constexpr int kCu = (kStageSeqs + 1 + kThreads - 1) / kThreads, kLen = kStageSeqs / kThreads;
+    int cu_v[kCu], len_v[kLen];
+#pragma unroll
+    for (int u = 0; u < kCu; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      cu_v[u] = i <= a.batch ? __ldg(a.cu_B + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kLen; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      len_v[u] = i < a.batch ? __ldg(a.lens + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kCu; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      if (i <= a.batch) cu_s[i] = cu_v[u];
+    }
+#pragma unroll
+    for (int u = 0; u < kLen; ++u) {
+      const int i = threadIdx.x + u * kThreads;
+      if (i < a.batch) lens_s[i] = len_v[u];
+    }
     __syncthreads();
     b = find_seq_smem(cu_s, a.batch, r >> 1);
     c0 = cu_s[b];
@@ -219,11 +244,11 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
   const T *qs = reinterpret_cast<const T *>(rows_s);
   const T *ks = reinterpret_cast<const T *>(rows_s + qbytes);
   const T *vs = reinterpret_cast<const T *>(rows_s + qbytes + kvbytes);
-  if (a.rotate_q) rotate_rows<T>(qs, (T *)a.q_rot + (long)r * a.Hq * a.hd, a.Hq, a.hd, a.hd, cs);
+  if (a.rotate_q) rotate_rows<T, 1>(qs, (T *)a.q_rot + (long)r * a.Hq * a.hd, a.Hq, a.hd, a.hd, cs);
   const long base = ((long)page * a.Hkv * kPage + slot % kPage) * a.hd;
   const long stride = (long)kPage * a.hd;    // next KV head, same slot
-  rotate_rows<T>(ks, (T *)a.k_cache + base, a.Hkv, a.hd, stride, cs);
-  copy_rows<T>(vs, (T *)a.v_cache + base, a.Hkv, a.hd, stride);
+  rotate_rows<T, 1>(ks, (T *)a.k_cache + base, a.Hkv, a.hd, stride, cs);
+  copy_rows<T, 1>(vs, (T *)a.v_cache + base, a.Hkv, a.hd, stride);
 }
 
 struct RopeAppendArgs {
@@ -252,10 +277,10 @@ rope_append_kernel(const __grid_constant__ RopeAppendArgs a) {
   __syncthreads();
   const long base = ((long)page * a.Hkv * kPage + pos % kPage) * a.hd;
   const long stride = (long)kPage * a.hd;
-  rotate_rows<T>((const T *)a.k + (long)r * a.Hkv * a.hd, (T *)a.k_cache + base,
-                 a.Hkv, a.hd, stride, cs);
-  copy_rows<T>((const T *)a.v + (long)r * a.Hkv * a.hd, (T *)a.v_cache + base,
-               a.Hkv, a.hd, stride);
+  rotate_rows<T, 4>((const T *)a.k + (long)r * a.Hkv * a.hd, (T *)a.k_cache + base,
+                    a.Hkv, a.hd, stride, cs);
+  copy_rows<T, 4>((const T *)a.v + (long)r * a.Hkv * a.hd, (T *)a.v_cache + base,
+                  a.Hkv, a.hd, stride);
 }
 
 }  // namespace
