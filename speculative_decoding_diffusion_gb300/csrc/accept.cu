@@ -910,8 +910,10 @@ vocab_chunk_kernel(const __grid_constant__ ChunkParams a) {
 // same order of operations), so the partials are the same bits.
 constexpr int kPartThreads = 256;
 
+// five CTAs (40 warps, 40 parts in flight) per SM at 48 registers, no
+// spills: the pass is bound by the bytes it has in flight
 template <typename T>
-__global__ void __launch_bounds__(kPartThreads)
+__global__ void __launch_bounds__(kPartThreads, 5)
 vocab_part_kernel(const __grid_constant__ ChunkParams a) {
   constexpr int N = Ld<T>::N;
   constexpr int kChunk = chunk_entries<T>();
