@@ -227,11 +227,12 @@ rope_verify_kernel(const __grid_constant__ RopeVerifyArgs a) {
               j < 0 || j >= 2 * B || P < 0 || (long)P + 2 * B > (long)a.max_pages * kPage ||
               (a.node_size > 0 && (2 * B) % a.node_size != 0));
   const int page = ok ? __ldg(a.block_table + (long)b * a.max_pages + slot / kPage) : -1;
+  // the angles need only the position: computed while the page is loaded
+  if (ok) angles(a.tab, a.hd, pos, cs);
   ok = ok && page >= 0 && page < a.num_pages;   // cu_B or block table out of range
   // the split merge reads it: which of its rows were split, without a search
   if (threadIdx.x == 0) a.tok_info[r] = make_int4(ok ? P + 2 * B : 0, b * a.Hkv * a.row_tiles, j, 0);
   if (!ok && threadIdx.x == 0) raise_status(a.status, kStatusBadInput);
-  if (ok) angles(a.tab, a.hd, pos, cs);
   __syncthreads();
   // every exit waits for the copies into this CTA's shared memory (the
   // drain after a wait that gave up takes the default limit)
