@@ -982,10 +982,11 @@ vocab_part_kernel(const __grid_constant__ ChunkParams a) {
 }
 
 // Parts per resident warp up to which the sampling rule's chunk pass takes
-// the ring-free kernel above (an A/B on one GPU: 16 x 1024, 2.1 parts per
-// warp, step 59.4 -> 55.9 us; 8 x 32768, 4.2, 230.3 -> 226.6 us; 64 x 4096,
-// 16.8, 288.3 -> 290.7 us, so the ring keeps that one).  The ring-free
-// kernel has no bounded waits.
+// the ring-free kernel above.  At five CTAs per SM, 16 x 1024 has 1.7 parts
+// per warp, 8 x 32768 3.4 and 64 x 4096 13.5; an A/B on one GPU (ring-free
+// against ring, step time): 59.4 -> 55.9 us, 230.3 -> 226.6 us and
+// 288.3 -> 290.7 us, so the ring keeps the third.  The ring-free kernel has
+// no bounded waits.
 constexpr double kDirectPartsPerWarp = 6.0;
 
 template <typename T>
