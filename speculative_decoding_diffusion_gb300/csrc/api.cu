@@ -14,16 +14,20 @@
 
 namespace simsd {
 
+// SMs of the current device (a GB300's 152 when no device is visible, so
+// that workspace sizes queried on a host without a GPU match the plan one
+// would make on it)
 int device_sm_count() {
+  constexpr int kDefaultSms = 152;
   static std::mutex mu;
   static int cached[64] = {0};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return kDefaultSms;
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 64 && cached[dev] > 0) return cached[dev];
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-    n = 148;
+    n = kDefaultSms;
   if (dev < 64) cached[dev] = n;
   return n;
 }

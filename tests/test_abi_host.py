@@ -261,3 +261,35 @@ def test_accept_workspace_size_is_the_header_formula(lib, dtype, vocab, batch, t
     for k, v in dict(batch=batch, vocab=vocab, total_B=total_B, B_max=32, dtype=dtype).items():
         setattr(dd, k, v)
     assert lib.simsd_draft_workspace_size(ctypes.byref(dd)) == 256 + r(total_B * C * 128)
+
+
+def _verify_ws_bytes(T, Hq, hd, n_splits):
+    # the workspace carve-up of simsd_verify_attn (bf16): status word, one
+    # int4 per new token, then, when the plan splits, the fp32 partial
+    # outputs and the (max, sum) pairs of every split; each region 256-byte
+    # aligned
+    up = lambda n: (n + 255) // 256 * 256
+    total = up(4) + up(T * 16)
+    if n_splits > 1:
+        total += up(n_splits * T * Hq * hd * 4) + up(n_splits * T * Hq * 8)
+    return total
+
+
+@pytest.mark.parametrize("batch,P,B,splits", [
+    (16, 1024, 4, 1),      # 128 units of 9 blocks: one wave, no split
+    (64, 4096, 8, 2),      # 512 units: three full waves, the last 56 units in 2 splits
+    (8, 32768, 16, 2),     # 64 units of 257 blocks: every unit in 2 (one wave of 128 CTAs)
+    (1, 32768, 4, 19),     # 8 units: 19 splits of 14 blocks fill one wave of 152 CTAs
+])
+def test_verify_split_plan(lib, batch, P, B, splits):
+    """The key-split plan the host makes for a 152-SM device (the library's
+    count when no device is visible), read back from the workspace size."""
+    if torch.cuda.is_available():
+        pytest.skip("the plan follows the visible device's SM count")
+    max_pages = (P + 2 * B + 15) // 16
+    d = _desc(batch=batch, num_pages=batch * max_pages, max_pages_per_seq=max_pages,
+              total_B=batch * B, B_max=B)
+    got = lib.simsd_verify_workspace_size(ctypes.byref(d))
+    T = 2 * batch * B
+    assert got == _verify_ws_bytes(T, 32, 128, splits), \
+        [(s, _verify_ws_bytes(T, 32, 128, s)) for s in (1, 2, 3, splits)] + [got]
