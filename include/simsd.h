@@ -175,7 +175,10 @@ typedef struct {
 } simsd_verify_desc;
 
 /* Bytes of workspace simsd_verify_attn needs for these sizes (reads only
- * the host-side fields).  Returns 0 if the sizes are invalid. */
+ * the host-side fields).  Returns 0 if the sizes are invalid.  The size
+ * follows the key-split plan, which depends on the current device's SM
+ * count (152 when no device is visible): query it with the device that
+ * will run the call current. */
 size_t simsd_verify_workspace_size(const simsd_verify_desc *d);
 simsd_status simsd_verify_attn(const simsd_verify_desc *d, void *stream);
 
@@ -390,8 +393,9 @@ typedef struct {
   float *confidence;
   void *workspace;            /* device, 256-byte aligned: the status word,
                                  or simsd_draft_workspace_size bytes (256 +
-                                 total_B ceil(vocab / E) * 128, E as in
-                                 simsd_accept) for the chunked path       */
+                                 total_B ceil(vocab / E) * 128 rounded up to
+                                 a multiple of 256, E as in simsd_accept)
+                                 for the chunked path                      */
   size_t workspace_bytes;
 } simsd_draft_desc;
 
