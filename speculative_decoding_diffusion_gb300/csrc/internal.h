@@ -116,9 +116,9 @@ int device_sm_count();
 
 // TMA descriptor of a paged bf16 cache [num_pages][Hkv][16][hd] as the 4-D
 // tensor (hd, slot, head, page); one box = one page of one head, 64 columns
-// (128 bytes) wide, 128-byte swizzle.  False if the driver call fails.
-// Descriptors are cached per (device, pointer, sizes): repeated calls on the
-// same cache cost no driver call.
+// (128 bytes) wide, 128-byte swizzle.  False if the CUDA driver's tensor-map
+// encoding fails.  Descriptors are cached per (device, pointer, sizes):
+// repeated calls on the same cache encode nothing.
 bool make_cache_map(CUtensorMap *m, void *ptr, int num_pages, int Hkv, int hd);
 
 // Records `event` (a cudaEvent_t, may be NULL) on `stream`; under stream
