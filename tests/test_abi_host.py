@@ -293,3 +293,14 @@ def test_verify_split_plan(lib, batch, P, B, splits):
     T = 2 * batch * B
     assert got == _verify_ws_bytes(T, 32, 128, splits), \
         [(s, _verify_ws_bytes(T, 32, 128, s)) for s in (1, 2, 3, splits)] + [got]
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """With no built library the binding raises on the first call: there is
+    no other path to the results."""
+    monkeypatch.setattr(binding, "_LIB", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "libsimsd.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        binding.layout(4, [2, 1, 3])
