@@ -322,6 +322,18 @@ def oracle_step_sample(w, seconds, threads, rule="sample", temperature=1.0):
     return toks / el, el, reps
 
 
+def merge_launches(w, ws_bytes):
+    """1 when the verify plan splits some unit's keys (K3 runs), else 0: the
+    workspace then holds split partials beyond the status word, the rotated
+    queries (fp32 path) and one int4 per new token, each 256-byte aligned."""
+    up = lambda n: (n + 255) // 256 * 256
+    T = 2 * int(w.cu_B[-1])
+    base = up(4) + up(T * 16)
+    if w.spec.dtype != "bf16":
+        base += up(T * w.spec.Hq * w.spec.hd * 4)
+    return 1 if ws_bytes > base else 0
+
+
 def cpu_threads():
     return len(os.sched_getaffinity(0))
 
@@ -573,8 +585,7 @@ def main():
     # finishing kernel of the rule (K4b), else one cluster launch (K4a and
     # K4b are reported only on the chunked path)
     chunked = args.accept_path == "auto"
-    # (an event pair around no launch reads ~2 us; a K3 launch reads 6 us or more)
-    n_launch = (3 if float(np.median(k_ms["K3"])) > 0.004 else 2) + (2 if chunked else 1)
+    n_launch = 2 + merge_launches(w, dw.verify_ws.numel()) + (2 if chunked else 1)
     if not chunked:
         del k_ms["K4a"], k_ms["K4b"]
     kernels = {n: {"ms": float(np.mean(t))} for n, t in k_ms.items()}

@@ -304,3 +304,22 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
         binding.lib()
     with pytest.raises(RuntimeError, match="not built"):
         binding.layout(4, [2, 1, 3])
+
+
+@pytest.mark.parametrize("dtype,batch,P,B,merges", [
+    (binding.SIMSD_BF16, 16, 1024, 4, 0), (binding.SIMSD_BF16, 64, 4096, 8, 1),
+    (binding.SIMSD_BF16, 8, 32768, 16, 1), (binding.SIMSD_BF16, 1, 32768, 4, 1),
+    (binding.SIMSD_F32, 1, 64, 4, 0), (binding.SIMSD_F32, 2, 4096, 4, 1)])
+def test_bench_counts_the_merge_from_the_plan(lib, dtype, batch, P, B, merges):
+    """bench.py counts the split merge's launch from the workspace size the
+    library plans (the merge runs iff some unit's keys are split)."""
+    import types
+    import bench
+    max_pages = (P + 2 * B + 15) // 16
+    d = _desc(batch=batch, num_pages=batch * max_pages, max_pages_per_seq=max_pages,
+              total_B=batch * B, B_max=B, dtype=dtype)
+    ws = lib.simsd_verify_workspace_size(ctypes.byref(d))
+    w = types.SimpleNamespace(cu_B=np.arange(batch + 1) * B,
+                              spec=types.SimpleNamespace(dtype="bf16" if dtype == binding.SIMSD_BF16
+                                                         else "f32", Hq=32, hd=128))
+    assert bench.merge_launches(w, ws) == merges
